@@ -1,0 +1,38 @@
+"""Pure-Python brute force for tiny inputs (test infrastructure only).
+
+These loops restate the definitions a second, independent way (Python floats,
+with exact rational arithmetic where asked) so the C oracle can be checked
+against something that is not itself.  Use only for tiny shapes.
+"""
+from fractions import Fraction
+
+
+def sum_exact(values):
+    """Exact rational sum of float values (each float is an exact rational)."""
+    total = Fraction(0)
+    for v in values:
+        total += Fraction(float(v))
+    return total
+
+
+def axis_sum_exact(flat, outer, reduce, inner):
+    """Exact out[o][i] = sum_r x[o, r, i], index arithmetic written out."""
+    out = []
+    for o in range(outer):
+        row = []
+        for i in range(inner):
+            terms = [flat[(o * reduce + r) * inner + i] for r in range(reduce)]
+            row.append(sum_exact(terms))
+        out.append(row)
+    return out
+
+
+def reverse_cumsum_exact(flat, rows, n):
+    """Exact y[i][j] = sum over k from j to n-1 of x[i, k] (O(n^2) per row)."""
+    out = []
+    for i in range(rows):
+        row = []
+        for j in range(n):
+            row.append(sum_exact(flat[i * n + k] for k in range(j, n)))
+        out.append(row)
+    return out

@@ -1,0 +1,97 @@
+"""Seeded synthetic inputs for the three primitives.
+
+This module draws input values only; it holds none of the arithmetic of the
+reductions or the scan, so the oracle and the CUDA path can both be fed from
+it.  Every draw is a pure function of (shape, distribution, seed, device type):
+
+* ``uniform01``   torch.rand on a generator seeded with ``seed``.
+* ``uniform_pm1`` 2 * torch.rand - 1 (exact in fp32: a power-of-two scale and
+  a subtraction of 1 from a value in [0, 2)).
+* ``normal``      torch.randn.
+* ``harmonic``    x[i] = 1/(i+1), the fp64 reciprocal rounded to fp32 (the
+  synthetic fallback input of the "High-Performance Reduction Kernels" README,
+  "Layout" section).
+* ``const:c``     every element equal to c.
+* ``int:lo:hi``   integers drawn uniformly from [lo, hi], stored as fp32.
+
+The generator never reads files and never reaches the network.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+DISTRIBUTIONS = ("uniform01", "uniform_pm1", "normal", "harmonic", "const", "int")
+
+
+def _generator(seed: int, device) -> torch.Generator:
+    dev = torch.device(device)
+    g = torch.Generator(device=dev.type if dev.type == "cpu" else dev)
+    g.manual_seed(int(seed))
+    return g
+
+
+def make(shape, dist: str, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Return a contiguous float32 tensor of ``shape`` drawn from ``dist``."""
+    shape = tuple(int(s) for s in (shape if isinstance(shape, (tuple, list)) else (shape,)))
+    n = math.prod(shape)
+    dev = torch.device(device)
+    if dist == "uniform01":
+        return torch.rand(shape, generator=_generator(seed, dev), dtype=torch.float32, device=dev)
+    if dist == "uniform_pm1":
+        t = torch.rand(shape, generator=_generator(seed, dev), dtype=torch.float32, device=dev)
+        return t.mul_(2.0).sub_(1.0)
+    if dist == "normal":
+        return torch.randn(shape, generator=_generator(seed, dev), dtype=torch.float32, device=dev)
+    if dist == "harmonic":
+        i = torch.arange(1, n + 1, dtype=torch.float64, device=dev)
+        return torch.reciprocal(i).to(torch.float32).reshape(shape)
+    if dist.startswith("const:"):
+        c = float(dist.split(":", 1)[1])
+        return torch.full(shape, c, dtype=torch.float32, device=dev)
+    if dist.startswith("int:"):
+        _, lo, hi = dist.split(":")
+        t = torch.randint(int(lo), int(hi) + 1, shape, generator=_generator(seed, dev),
+                          dtype=torch.int32, device=dev)
+        return t.to(torch.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+# The five workloads, by what they are.  ``op`` names the primitive; ``view``
+# gives its arguments; ``bytes`` is the algorithmic traffic (every input read
+# once, every output written once).
+WORKLOADS = {
+    "sum_1e6_harmonic": dict(op="sum", shape=(1_000_000,), dist="harmonic", seed=0),
+    "sum_1e6_pm1": dict(op="sum", shape=(1_000_000,), dist="uniform_pm1", seed=42),
+    "sum_1e9": dict(op="sum", shape=(1_000_000_000,), dist="uniform01", seed=42),
+    "axis_128x4096x4095_d1": dict(op="axis", shape=(128, 4096, 4095), dim=1, dist="normal", seed=7),
+    "axis_4096x65536_d1": dict(op="axis", shape=(4096, 65536), dim=1, dist="uniform_pm1", seed=11),
+    "axis_65536x4096_d0": dict(op="axis", shape=(65536, 4096), dim=0, dist="uniform_pm1", seed=11),
+    "rcumsum_32768x32768": dict(op="rcumsum", shape=(32768, 32768), dist="uniform01", seed=3),
+}
+
+# The 1D sweep sizes of the sum benchmark (uniform[0,1), seed 42).
+SUM_SWEEP = (10_000, 100_000, 1_000_000, 10_000_000, 100_000_000, 500_000_000, 1_000_000_000)
+
+
+def canonical_axis(shape, dim):
+    """(outer, reduce, inner) of a contiguous tensor reduced along ``dim``."""
+    shape = tuple(int(s) for s in shape)
+    dim = dim % len(shape)
+    outer = math.prod(shape[:dim])
+    inner = math.prod(shape[dim + 1:])
+    return outer, shape[dim], inner
+
+
+def algorithmic_bytes(w: dict) -> int:
+    """Bytes the primitive must move: read each input once, write each output once."""
+    n = math.prod(w["shape"])
+    if w["op"] == "sum":
+        return 4 * n + 4
+    if w["op"] == "axis":
+        outer, _, inner = canonical_axis(w["shape"], w["dim"])
+        return 4 * n + 4 * outer * inner
+    if w["op"] == "rcumsum":
+        return 8 * n
+    raise ValueError(w["op"])

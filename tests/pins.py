@@ -1,0 +1,202 @@
+"""Pins of the CPU oracle: checks against facts fixed by the pages and by
+arithmetic, not by the oracle itself.
+
+Each ``pin_*`` function takes an :class:`oracle.Oracle` and raises
+AssertionError when the oracle disagrees with a closed form, an exact integer
+sum, a brute-force rational evaluation, an invariant, or a worked example
+printed on the pages.  tests/test_oracle_pins.py runs them on the real oracle;
+tests/test_oracle_mutants.py runs them on deliberately broken builds of the
+oracle to show that a plausible mistake (a dropped term, a wrong sign, a
+transposed index, a wrong scan direction) fails at least one pin.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+from oracle import brute
+from reduction_scan_primitives_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+EULER_GAMMA = 0.57721566490153286060651209008240243104215933593992
+U64 = 2.0 ** -53
+
+
+def _np(t):
+    return t.numpy() if hasattr(t, "numpy") else np.asarray(t)
+
+
+def harmonic_closed_form(n: int) -> float:
+    """H_n from the Euler-Maclaurin expansion (truncation error < 1/(240 n^8))."""
+    return (math.log(n) + EULER_GAMMA + 1.0 / (2 * n) - 1.0 / (12 * n ** 2)
+            + 1.0 / (120 * n ** 4) - 1.0 / (252 * n ** 6))
+
+
+def pin_sum_harmonic(orc):
+    """x[i] = fp32(1/(i+1)) sums to H_n (High-Performance Reduction Kernels
+    README, 'Layout' section).  Each input carries a rounding error of at most
+    half an fp32 ulp, so the fp64 sum of the rounded inputs must lie within
+    2^-24 * H_n of the exact harmonic number, and within fp64 rounding of the
+    correctly rounded sum (math.fsum) of the same fp32 values."""
+    for n in (1, 2, 3, 4, 7, 10):
+        x = _np(inputs.make((n,), "harmonic"))
+        s, a = orc.sum1d(x)
+        exact = sum((Fraction(1, i + 1) for i in range(n)), Fraction(0))
+        assert abs(s - float(exact)) <= 2.0 ** -24 * float(exact) + 1e-15, (n, s, exact)
+        assert a == s
+    n = 1_000_000
+    x = _np(inputs.make((n,), "harmonic"))
+    s, a = orc.sum1d(x)
+    h = harmonic_closed_form(n)
+    assert abs(s - h) <= 2.0 ** -24 * h, (s, h)
+    fs = math.fsum(x.astype(np.float64).tolist())
+    assert abs(s - fs) <= 1e-12 * fs, (s, fs)
+    assert a == s
+
+
+def pin_sum_constant(orc):
+    """A constant c summed n times is n*c.  fp32 c has 24 significant bits, so
+    every partial k*c (k < 2^29) is exact in fp64 and the result is exact."""
+    for c in (1.0, 0.5, -3.0, float(np.float32(0.1))):
+        for n in (0, 1, 17, 1000, 100_003):
+            x = np.full(n, c, dtype=np.float32)
+            s, a = orc.sum1d(x)
+            assert s == n * float(np.float32(c)), (c, n, s)
+            assert a == n * abs(float(np.float32(c))), (c, n, a)
+
+
+def pin_sum_integers(orc):
+    """Small-integer inputs sum exactly: compare with an int64 sum."""
+    for dist, n, seed in (("int:-8:8", 100_003, 5), ("int:-1:1", 1_000_000, 42), ("int:0:3", 777, 9)):
+        x = _np(inputs.make((n,), dist, seed))
+        s, a = orc.sum1d(x)
+        xi = x.astype(np.int64)
+        assert s == float(xi.sum()), (dist, s, xi.sum())
+        assert a == float(np.abs(xi).sum())
+
+
+def _mixed_values(rng, n):
+    """Random fp32 values with mixed signs and exponents."""
+    v = rng.standard_normal(n) * np.exp2(rng.integers(-6, 7, n))
+    return v.astype(np.float32)
+
+
+def pin_sum_bruteforce(orc):
+    """Against an exact rational sum on tiny arrays.  A sequential fp64 sum of
+    n terms is within (n-1) * 2^-53 * sum|x| of the exact value."""
+    rng = np.random.default_rng(1234)
+    for n in list(range(0, 13)) + [31, 64]:
+        x = _mixed_values(rng, n)
+        s, a = orc.sum1d(x)
+        exact = brute.sum_exact(x.tolist())
+        exact_abs = brute.sum_exact(abs(v) for v in x.tolist())
+        assert abs(s - float(exact)) <= max(n - 1, 0) * U64 * float(exact_abs) + 1e-300, (n, s, exact)
+        assert abs(a - float(exact_abs)) <= max(n - 1, 0) * U64 * float(exact_abs) + 1e-300
+
+
+AXIS_SHAPES = [(1, 1, 1), (2, 3, 4), (3, 1, 5), (4, 5, 1), (1, 6, 3), (2, 0, 3), (0, 3, 2),
+               (3, 7, 2), (2, 5, 3), (5, 2, 6)]
+
+
+def pin_axis_bruteforce(orc):
+    """out[o, i] = sum_r x[o, r, i] against exact rational sums written with
+    their own index arithmetic (POPCORNBENCH trace l1_p47, problem statement:
+    [batch, dim1, dim2] summed over dim 1)."""
+    rng = np.random.default_rng(99)
+    for (o, r, i) in AXIS_SHAPES:
+        x = _mixed_values(rng, o * r * i)
+        out, aout = orc.axis_sum(x, o, r, i)
+        assert out.shape == (o, i)
+        ex = brute.axis_sum_exact(x.tolist(), o, r, i)
+        exa = brute.axis_sum_exact([abs(v) for v in x.tolist()], o, r, i)
+        for a in range(o):
+            for b in range(i):
+                bound = max(r - 1, 0) * U64 * float(exa[a][b]) + 1e-300
+                assert abs(out[a, b] - float(ex[a][b])) <= bound, ((o, r, i), a, b)
+                assert abs(aout[a, b] - float(exa[a][b])) <= bound
+        if r == 0:
+            assert np.all(out == 0.0)
+
+
+def pin_axis_integers_and_invariants(orc):
+    """Exact on small integers (int64 reference over the same axis); inner == 1
+    reduces each row like the 1D sum; outer == inner == 1 is the 1D sum; the
+    positional variant agrees with the full one."""
+    x = _np(inputs.make((3, 100, 7), "int:-8:8", 5))
+    out, aout = orc.axis_sum(x, 3, 100, 7)
+    xi = x.astype(np.int64)
+    assert np.array_equal(out, xi.sum(axis=1).astype(np.float64))
+    assert np.array_equal(aout, np.abs(xi).sum(axis=1).astype(np.float64))
+    rng = np.random.default_rng(7)
+    rows = _mixed_values(rng, 5 * 33).reshape(5, 33)
+    out, _ = orc.axis_sum(rows, 5, 33, 1)
+    for k in range(5):
+        assert out[k, 0] == orc.sum1d(rows[k])[0]
+    flat = _mixed_values(rng, 50)
+    assert orc.axis_sum(flat, 1, 50, 1)[0][0, 0] == orc.sum1d(flat)[0]
+    x = _mixed_values(rng, 4 * 9 * 6)
+    full, fabs_ = orc.axis_sum(x, 4, 9, 6)
+    pos = np.array([0, 5, 6, 13, 23, 17], dtype=np.int64)
+    at, at_abs = orc.axis_sum_at(x, 4, 9, 6, pos)
+    assert np.array_equal(at, full.reshape(-1)[pos])
+    assert np.array_equal(at_abs, fabs_.reshape(-1)[pos])
+
+
+def pin_scan_worked_examples(orc):
+    """The worked examples of the POPCORNBENCH trace l1_p91 (reverse cumsum):
+    [1..8] -> [36, 35, 33, 30, 26, 21, 15, 8]; [a, b, c, d] -> [a+b+c+d,
+    b+c+d, c+d, d]."""
+    with open(os.path.join(GOLDEN, "rcumsum_worked_examples.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        x = np.asarray(c["x"], dtype=np.float32)
+        y, ay = orc.reverse_cumsum(x, 1, x.size)
+        assert y.reshape(-1).tolist() == [float(v) for v in c["y"]], (c, y)
+        assert ay.reshape(-1).tolist() == [float(v) for v in c["y"]]
+
+
+def pin_scan_bruteforce(orc):
+    """Against the O(N^2) definition (exact rationals) on tiny shapes, plus:
+    the last column equals x exactly (a suffix of one term), the first column
+    is the row sum."""
+    rng = np.random.default_rng(5)
+    for rows, n in ((1, 1), (1, 2), (2, 3), (3, 5), (2, 8), (4, 1), (1, 13), (3, 4)):
+        x = _mixed_values(rng, rows * n)
+        y, ay = orc.reverse_cumsum(x, rows, n)
+        ex = brute.reverse_cumsum_exact(x.tolist(), rows, n)
+        exa = brute.reverse_cumsum_exact([abs(v) for v in x.tolist()], rows, n)
+        for a in range(rows):
+            for j in range(n):
+                bound = (n - j) * U64 * float(exa[a][j]) + 1e-300
+                assert abs(y[a, j] - float(ex[a][j])) <= bound, (rows, n, a, j)
+                assert abs(ay[a, j] - float(exa[a][j])) <= bound
+        xr = x.reshape(rows, n).astype(np.float64)
+        assert np.array_equal(y[:, -1], xr[:, -1])
+        for a in range(rows):
+            s, sa = orc.sum1d(x.reshape(rows, n)[a])
+            assert abs(y[a, 0] - s) <= n * U64 * sa + 1e-300
+
+
+def pin_scan_integers(orc):
+    """Exact on small integers: the result equals flip-cumsum-flip in int64
+    (the reference expression of the POPCORNBENCH trace l1_p91), and
+    consecutive differences give back x."""
+    x = _np(inputs.make((6, 301), "int:0:3", 3))
+    y, ay = orc.reverse_cumsum(x, 6, 301)
+    xi = x.astype(np.int64)
+    ref = np.flip(np.cumsum(np.flip(xi, axis=1), axis=1), axis=1)
+    assert np.array_equal(y, ref.astype(np.float64))
+    assert np.array_equal(ay, ref.astype(np.float64))
+    assert np.array_equal(y[:, :-1] - y[:, 1:], xi[:, :-1].astype(np.float64))
+    x = _np(inputs.make((2, 257), "int:-8:8", 4))
+    y, ay = orc.reverse_cumsum(x, 2, 257)
+    xi = x.astype(np.int64)
+    assert np.array_equal(y, np.flip(np.cumsum(np.flip(xi, 1), 1), 1).astype(np.float64))
+    assert np.array_equal(ay, np.flip(np.cumsum(np.flip(np.abs(xi), 1), 1), 1).astype(np.float64))
+
+
+ALL_PINS = [pin_sum_harmonic, pin_sum_constant, pin_sum_integers, pin_sum_bruteforce,
+            pin_axis_bruteforce, pin_axis_integers_and_invariants, pin_scan_worked_examples,
+            pin_scan_bruteforce, pin_scan_integers]
