@@ -1,0 +1,495 @@
+"""Benchmark of the libreduce hot path on GB300.
+
+One step runs every primitive once over its full-size synthetic workload:
+
+  sum_1e9                 reduce_sum_f32   x[1e9]                uniform[0,1)  seed 42
+  axis_128x4096x4095_d1   reduce_axis_f32  [128, 4096, 4095] d1  N(0,1)        seed 7
+  axis_4096x65536_d1      reduce_axis_f32  [4096, 65536] d1      uniform[-1,1) seed 11
+  axis_65536x4096_d0      reduce_axis_f32  [65536, 4096] d0      uniform[-1,1) seed 11
+  rcumsum_32768x32768     reverse_cumsum   [32768, 32768]        uniform[0,1)  seed 3
+
+The metric is effective HBM bandwidth: algorithmic bytes (every input read
+once, every output written once) divided by device time, in GB/s, and as a
+fraction of the measured HBM copy bandwidth.  Inputs are resident in HBM and
+each is larger than L2 (>= 1 GiB), so no flush is needed between launches;
+the small-n sweep of the 1D sum flushes L2 before every timed launch.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) each rank runs the same step on its own GPU (replicas,
+weak scaling); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from reduction_scan_primitives_gb300 import inputs  # noqa: E402
+
+METRIC = "effective HBM GB/s and % of GB300 peak per reduce/scan config (1 GPU)"
+STEP_WORKLOADS = ["sum_1e9", "axis_128x4096x4095_d1", "axis_4096x65536_d1", "axis_65536x4096_d0",
+                  "rcumsum_32768x32768"]
+FALLBACK_HBM_GBS = 6800.0
+# Context only (another machine): the page's T4 figures for the 1D sum.
+PAGES_T4 = {"sum_1e8_ms": 1.4716, "sum_1e9_ms": 14.4983}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (timing only; no data-path collective).
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (the job time is the slowest rank's)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# Peaks, clocks, profiles.
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "reduction_scan_primitives_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, keyed by workload,
+    valid only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    digest = source_digest()
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            if len(parts) >= 3 and parts[2] == digest:
+                out[parts[0]] = float(parts[1])
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Workloads.
+# ---------------------------------------------------------------------------
+def make_call(name, x, out):
+    from reduction_scan_primitives_gb300 import libreduce as L
+    w = inputs.WORKLOADS[name]
+    if w["op"] == "sum":
+        return lambda: L.reduce_sum_f32(x, out=out)
+    if w["op"] == "axis":
+        return lambda: L.reduce_axis_f32(x, w["dim"], out=out)
+    return lambda: L.reverse_cumsum_f32(x, out=out)
+
+
+def alloc_workload(name, device):
+    w = inputs.WORKLOADS[name]
+    x = inputs.make(w["shape"], w["dist"], w["seed"], device=device)
+    if w["op"] == "sum":
+        out = torch.empty((), dtype=torch.float32, device=device)
+    elif w["op"] == "axis":
+        shp = list(w["shape"])
+        del shp[w["dim"]]
+        out = torch.empty(shp, dtype=torch.float32, device=device)
+    else:
+        out = torch.empty_like(x)
+    return x, out
+
+
+def time_sweep(device, reps=10):
+    """1D sum sweep n = 1e4 .. 1e9, L2 flushed before every timed launch."""
+    from reduction_scan_primitives_gb300 import libreduce as L
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    res = {}
+    peak, _ = hbm_peak()
+    for n in inputs.SUM_SWEEP:
+        x = inputs.make((n,), "uniform01", 42, device=device)
+        out = torch.empty((), dtype=torch.float32, device=device)
+        for _ in range(3):
+            L.reduce_sum_f32(x, out=out)
+        times = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            L.reduce_sum_f32(x, out=out)
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        gbs = (4 * n + 4) / (ms * 1e-3) / 1e9
+        res[str(n)] = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        del x
+    del flush
+    return res
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of each workload.
+# ---------------------------------------------------------------------------
+def oracle_sample(name, x_dev):
+    """(callable running the oracle on a sample, sample's algorithmic bytes, description)."""
+    import numpy as np
+
+    import oracle
+    w = inputs.WORKLOADS[name]
+    if w["op"] == "sum":
+        m = 25_000_000
+        xs = x_dev.reshape(-1)[:m].cpu().numpy()
+        return (lambda: oracle.sum1d(xs)), 4 * m + 4, f"first {m} elements"
+    if w["op"] == "axis":
+        o, r, i = inputs.canonical_axis(w["shape"], w["dim"])
+        x3 = x_dev.reshape(o, r, i)
+        if o > 1:
+            k = max(1, o // 128) if i > 1 else max(1, o // 64)
+            xs = np.ascontiguousarray(x3[:k].cpu().numpy())
+            return ((lambda: oracle.axis_sum(xs, k, r, i)), 4 * k * r * i + 4 * k * i,
+                    f"first {k} of {o} outer slices")
+        rr = max(1, r // 64)
+        xs = np.ascontiguousarray(x3[:, :rr].cpu().numpy())
+        return ((lambda: oracle.axis_sum(xs, 1, rr, i)), 4 * rr * i + 4 * i,
+                f"first {rr} of {r} reduce rows")
+    rows, n = w["shape"]
+    k = max(1, rows // 128)
+    xs = np.ascontiguousarray(x_dev[:k].cpu().numpy())
+    return (lambda: oracle.reverse_cumsum(xs, k, n)), 8 * k * n, f"first {k} of {rows} rows"
+
+
+def cpu_baseline(data, device):
+    total_bytes, total_s, desc = 0, 0.0, []
+    for name in STEP_WORKLOADS:
+        fn, nbytes, what = oracle_sample(name, data[name][0])
+        fn()  # first touch
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        total_bytes += nbytes
+        total_s += dt
+        desc.append(f"{name}: {what}")
+    return {"value": round(total_bytes / total_s / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "sample": "; ".join(desc), "seconds": round(total_s, 2)}
+
+
+# ---------------------------------------------------------------------------
+# Arms.
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    world, rank, local = dist_env()
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from reduction_scan_primitives_gb300 import build as lib_build
+    from reduction_scan_primitives_gb300 import libreduce as L
+    if rank == 0 or not os.path.exists(lib_build.LIB):
+        lib_build.build()
+    barrier(world)
+    L.load()
+
+    data = {name: alloc_workload(name, device) for name in STEP_WORKLOADS}
+    calls = {name: make_call(name, *data[name]) for name in STEP_WORKLOADS}
+    nbytes = {name: inputs.algorithmic_bytes(inputs.WORKLOADS[name]) for name in STEP_WORKLOADS}
+    step_bytes = sum(nbytes.values())
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        for name in STEP_WORKLOADS:
+            calls[name]()
+    torch.cuda.synchronize()
+    L.check(device)
+
+    stream = torch.cuda.current_stream(device)
+    ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)] for name in STEP_WORKLOADS}
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = L.launch_count()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(args.steps):
+            for name in STEP_WORKLOADS:
+                a, b = ev[name][k]
+                a.record(stream)
+                calls[name]()
+                b.record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    launches = L.launch_count() - launches0
+    L.check(device)
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), world, device)
+
+    peak, peak_kind = hbm_peak()
+    per = {}
+    for name in STEP_WORKLOADS:
+        t = [a.elapsed_time(b) for a, b in ev[name]]
+        mean = sum(t) / len(t)
+        gbs = nbytes[name] / (mean * 1e-3) / 1e9
+        per[name] = {"ms_mean": round(mean, 5), "ms_median": round(statistics.median(t), 5),
+                     "ms_min": round(min(t), 5), "GB/s": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "bytes": nbytes[name]}
+    total_kernel_ms = sum(per[n]["ms_mean"] for n in STEP_WORKLOADS)
+    for name in STEP_WORKLOADS:
+        per[name]["share"] = round(per[name]["ms_mean"] / total_kernel_ms, 4)
+    dom = max(STEP_WORKLOADS, key=lambda n: per[n]["ms_mean"])
+    traffic = recorded_traffic()
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": per[dom]["GB/s"], "peak": peak,
+                "unit": "GB/s", "frac": per[dom]["frac"], "peak_kind": f"of {peak_kind}",
+                "traffic": traffic.get(dom)}
+
+    ms_per_step = elapsed_ms / args.steps
+    value = step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+
+    e2e = run_e2e(args, data, nbytes, device, world) if not args.no_e2e else None
+    sweep = time_sweep(device) if (rank == 0 and not args.no_sweep) else None
+    cpu = cpu_baseline(data, device) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded torch generators on the device)",
+            "config": {"workload": "one pass of: " + ", ".join(STEP_WORKLOADS),
+                       "step_bytes": step_bytes, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (each >= 1 GiB); sweep flushes L2"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks.summary(), "per_config": per, "sum_sweep": sweep,
+            "pages_context_t4": PAGES_T4,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, data, nbytes, device, world):
+    """Same metric through the public API with host buffers: every step copies
+    each input from pinned host memory, runs the call, copies the result back."""
+    from reduction_scan_primitives_gb300 import libreduce as L
+    host_in, host_out = {}, {}
+    h2d = d2h = 0
+    for name in STEP_WORKLOADS:
+        x, out = data[name]
+        host_in[name] = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        host_in[name].copy_(x)
+        host_out[name] = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d += x.numel() * 4
+        d2h += out.numel() * 4
+    stream = torch.cuda.current_stream(device)
+    steps = max(1, min(args.steps, 5))
+
+    def step():
+        for name in STEP_WORKLOADS:
+            x, out = data[name]
+            x.copy_(host_in[name], non_blocking=True)
+            make_call(name, x, out)()
+            host_out[name].copy_(out, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world, device)
+    L.check(device)
+    value = sum(nbytes.values()) * steps * world / (ms * 1e-3) / 1e9
+    return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 3)}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on bounded samples."""
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    samples = {}
+    for name in STEP_WORKLOADS:
+        w = inputs.WORKLOADS[name]
+        # The same recipe on the CPU generator; the sample is a slice of the
+        # workload's leading rows / elements.
+        shape = list(w["shape"])
+        lead = {"sum": 25_000_000}.get(w["op"])
+        if w["op"] == "sum":
+            shape = [lead]
+        elif w["op"] == "axis":
+            o, r, i = inputs.canonical_axis(w["shape"], w["dim"])
+            shape = [max(1, o // 128), r, i] if o > 1 and i > 1 else (
+                [max(1, o // 64), r, i] if o > 1 else [1, max(1, r // 64), i])
+        else:
+            shape = [max(1, shape[0] // 128), shape[1]]
+        samples[name] = inputs.make(tuple(shape), w["dist"], w["seed"]).numpy()
+    import oracle
+
+    def one(name):
+        w = inputs.WORKLOADS[name]
+        x = samples[name]
+        if w["op"] == "sum":
+            oracle.sum1d(x)
+            return 4 * x.size + 4
+        if w["op"] == "axis":
+            o, r, i = x.shape
+            oracle.axis_sum(x, o, r, i)
+            return 4 * x.size + 4 * o * i
+        rows, n = x.shape
+        oracle.reverse_cumsum(x, rows, n)
+        return 8 * x.size
+
+    for _ in range(args.warmup):
+        for name in STEP_WORKLOADS:
+            one(name)
+    t0 = time.perf_counter()
+    total = 0
+    for _ in range(args.steps):
+        for name in STEP_WORKLOADS:
+            total += one(name)
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    sample = "; ".join(f"{n}: {list(samples[n].shape)}" for n in STEP_WORKLOADS)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": "one pass of: " + ", ".join(STEP_WORKLOADS) + " (bounded samples)"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("bench: --warmup raised to 3 (minimum)", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/*
+ * libreduce.h -- C ABI of libreduce, fp32 sum reductions and the reverse
+ * cumulative sum on NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensor pointers (x, out, y) are DEVICE pointers to memory of the device
+ *    that is current on the calling thread (cudaMalloc, the PyTorch caching
+ *    allocator, or managed memory).  The caller owns them.  Host pointers are
+ *    rejected with LIBREDUCE_ERR_INVALID_ARG before any work is queued.
+ *  - Every float* must be 4-byte aligned.  Any 4-byte alignment is accepted;
+ *    16-byte aligned buffers take the vectorised (128-bit) paths.
+ *  - Arrays are contiguous and row-major.  Sizes are element counts (int64).
+ *  - `stream` is a cudaStream_t (NULL means the legacy default stream).  A
+ *    call only enqueues work on `stream`: it never synchronises the host and
+ *    never copies results back.  The caller keeps the inputs alive and
+ *    unmodified until that work completes.
+ *  - Results are deterministic: the same input on the same device gives
+ *    bit-identical output on every call.  No floating-point atomics are used;
+ *    partial sums are combined in a fixed order.
+ *  - Accuracy: each output is within 1e-5 * (sum of |x| over its terms) +
+ *    1e-6 of the exact sum, and exact when every partial sum is an integer of
+ *    magnitude below 2^24.  NaN and Inf propagate as IEEE addition does.
+ *  - Scratch: the library keeps one workspace per device for partial sums,
+ *    tickets and look-back flags.  It is allocated (cudaMalloc) by the first
+ *    call on that device that needs it, so that first call must not be made
+ *    inside a stream capture.  Because the workspace is shared, calls on one
+ *    device must not run concurrently on different streams; calls queued on
+ *    one stream are always safe.
+ *  - Errors: validation happens before any work is queued, and a failed call
+ *    queues nothing.  LIBREDUCE_ERR_CUDA means a CUDA runtime call failed; its
+ *    code is available from libreduce_last_cuda_error().  Device-side errors
+ *    (a bounded wait that ran out) are reported by libreduce_check().
+ *
+ * Sources (by page):
+ *  - "High-Performance Reduction Kernels" (README of a 1D fp32 sum benchmark):
+ *    the 1D sum, 'Key design decisions' and 'Optimization: ILP4 accumulator'.
+ *  - "Seven-step reduction: 30x from one kernel": warp-shuffle trees, V7.
+ *  - POPCORNBENCH trace l1_p47: sum over dim=1 of a contiguous
+ *    [128, 4096, 4095] tensor, the [outer, reduce, inner] view.
+ *  - POPCORNBENCH trace l1_p91: reverse cumulative sum,
+ *    y = cumsum(x.flip(1), 1).flip(1).
+ */
+#ifndef LIBREDUCE_H_
+#define LIBREDUCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so callers need no CUDA header. */
+typedef struct CUstream_st* libreduce_stream_t;
+
+/* Status codes returned by every entry point. */
+#define LIBREDUCE_OK 0
+#define LIBREDUCE_ERR_INVALID_ARG 1 /* null pointer with a nonzero extent, negative extent,
+                                       misaligned or non-device pointer, bad option */
+#define LIBREDUCE_ERR_OVERFLOW 2    /* extent product overflows int64, or exceeds what the
+                                       chosen strategy's workspace can hold */
+#define LIBREDUCE_ERR_ALIAS 3       /* output overlaps input (the scan is out-of-place only) */
+#define LIBREDUCE_ERR_CUDA 4        /* a CUDA runtime call failed (see libreduce_last_cuda_error) */
+#define LIBREDUCE_ERR_TIMEOUT 5     /* a bounded device-side wait ran out (from libreduce_check) */
+
+/*
+ * reduce_sum_f32 -- out[0] = sum_{i<n} x[i].
+ *
+ * The 1D fp32 sum of the "High-Performance Reduction Kernels" README (its
+ * benchmark sums n = 1e4 .. 1e9 elements).
+ *   x    device, n floats (may be NULL when n == 0)
+ *   n    element count, n >= 0; n == 0 writes +0.0f
+ *   out  device, 1 float, written once
+ * Errors: INVALID_ARG (n < 0, x NULL with n > 0, out NULL, bad pointer),
+ *         OVERFLOW (4*n overflows int64), ALIAS (out inside x), CUDA.
+ */
+int reduce_sum_f32(const float* x, int64_t n, float* out, libreduce_stream_t stream);
+
+/*
+ * reduce_axis_f32 -- out[o*inner + i] = sum_{r<reduce} x[(o*reduce + r)*inner + i].
+ *
+ * The sum over one axis of a contiguous tensor, viewed as [outer, reduce,
+ * inner] (outer = product of the dims before the reduced one, inner = product
+ * of the dims after it), as set up in the POPCORNBENCH trace l1_p47 problem
+ * statement.  The output is the flat [outer, inner] array; keeping the reduced
+ * dim as size 1 is a view for the caller.
+ *   x      device, outer*reduce*inner floats
+ *   out    device, outer*inner floats, each written once
+ *   reduce == 0 writes +0.0f everywhere; outer == 0 or inner == 0 is a no-op.
+ * Errors: INVALID_ARG (negative extent, NULL pointer with nonzero size, bad
+ *         pointer), OVERFLOW (outer*reduce*inner overflows int64), ALIAS (out
+ *         overlaps x), CUDA.
+ */
+int reduce_axis_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
+                    libreduce_stream_t stream);
+
+/*
+ * reverse_cumsum_f32 -- y[i*N + j] = sum_{k=j}^{N-1} x[i*N + k] for every row i.
+ *
+ * The reverse inclusive cumulative sum along the last dim of a contiguous
+ * [rows, N] array, cumsum(x.flip(1), 1).flip(1) in the POPCORNBENCH trace
+ * l1_p91 problem statement.  Every output is formed by additions over its own
+ * suffix only (no subtraction of prefix sums).
+ *   x     device, rows*N floats
+ *   y     device, rows*N floats; must not overlap x (out-of-place only)
+ *   rows == 0 or N == 0 is a no-op.
+ * Rows with few tiles run one block per row; few long rows run a single-pass
+ * decoupled look-back scan whose waits are bounded (see libreduce_check).
+ * Errors: INVALID_ARG, OVERFLOW (rows*N overflows int64, or a few-row scan
+ *         larger than the look-back workspace holds), ALIAS, CUDA.
+ */
+int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, float* y,
+                       libreduce_stream_t stream);
+
+/*
+ * libreduce_check -- synchronise `stream`, then return and clear the current
+ * device's error word: LIBREDUCE_OK, or LIBREDUCE_ERR_TIMEOUT if a bounded
+ * device-side wait ran out since the last check (the affected outputs are then
+ * undefined), or LIBREDUCE_ERR_CUDA if the synchronisation itself failed.
+ */
+int libreduce_check(libreduce_stream_t stream);
+
+/* Text for a status code (static storage, never NULL). */
+const char* libreduce_strerror(int status);
+
+/* The cudaError_t of the last CUDA failure seen on this thread (0 if none). */
+int libreduce_last_cuda_error(void);
+
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t libreduce_launch_count(void);
+
+/*
+ * Process-wide dispatch options, for tests and benchmarks.  Not thread-safe
+ * against concurrent calls; set them before queuing work.
+ *   LIBREDUCE_OPT_SCAN_STRATEGY  0 auto, 1 one block per row, 2 look-back
+ *   LIBREDUCE_OPT_AXIS_SPLIT     0 auto, k > 0 forces k slices of the reduce axis
+ *                                (inner > 1), or k chunks per row (inner == 1)
+ *   LIBREDUCE_OPT_SPIN_LIMIT     0 default, else the look-back wait limit in polls
+ *   LIBREDUCE_OPT_STALL_TILE     -1 off, else the look-back tile (in scan order) that
+ *                                never publishes its aggregate: a host-chosen fault
+ *                                that makes the waits behind it run out, for tests
+ * Returns INVALID_ARG for an unknown option or value.
+ */
+#define LIBREDUCE_OPT_SCAN_STRATEGY 1
+#define LIBREDUCE_OPT_AXIS_SPLIT 2
+#define LIBREDUCE_OPT_SPIN_LIMIT 3
+#define LIBREDUCE_OPT_STALL_TILE 4
+/* Launch-shape overrides for tuning sweeps (-1 = automatic):
+ *   LIBREDUCE_OPT_CONTIG_VARIANT  loads in flight per thread of the 1D / long-row
+ *                                 kernel: 0 -> 4, 1 -> 8, 2 -> 16 (x 16 bytes)
+ *   LIBREDUCE_OPT_COLS_VARIANT    inner > 1 kernel: 0..2 scalar columns with 1, 4 or
+ *                                 8 warps along the reduce dim; 3..5 the same with
+ *                                 float4 columns (needs inner % 4 == 0, aligned x)
+ *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
+ *                                 2 float4 x 4 (float4 needs N % 4 == 0, aligned x, y)
+ *   LIBREDUCE_OPT_WAVES           1D sum: blocks = waves x resident blocks (0 = 1) */
+#define LIBREDUCE_OPT_CONTIG_VARIANT 5
+#define LIBREDUCE_OPT_COLS_VARIANT 6
+#define LIBREDUCE_OPT_RSCAN_VARIANT 7
+#define LIBREDUCE_OPT_WAVES 8
+int libreduce_set_option(int option, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBREDUCE_H_ */

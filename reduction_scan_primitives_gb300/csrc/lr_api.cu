@@ -1,0 +1,436 @@
+// lr_api.cu -- the C ABI of libreduce: argument validation, strategy choice,
+// workspace management and kernel launches.  See include/libreduce.h for the
+// contract of each entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "libreduce.h"
+#include "lr_internal.h"
+
+namespace lr {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Process state.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxTickets = 1 << 16;       // integer tickets (per row / column tile)
+constexpr int64_t kMaxPartials = 1 << 22;      // fp32 partial sums (16 MiB)
+constexpr size_t kHeaderBytes = 256;           // device error word and spare
+constexpr size_t kWorkspaceBytes =
+    kHeaderBytes + sizeof(unsigned) * kMaxTickets + sizeof(float) * kMaxPartials;
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  int occ_contig[kNumContigVariants] = {};
+  int occ_rows_warp = 0;
+  int occ_cols[kNumColsVariants] = {};
+  int occ_rscan[kNumRScanVariants] = {};
+  // Workspace (allocated by the first call that needs it).
+  char* ws = nullptr;
+  unsigned* err_word = nullptr;
+  unsigned* tickets = nullptr;
+  float* partials = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<int64_t> g_launches{0};
+std::atomic<int64_t> g_opt_scan_strategy{0};
+std::atomic<int64_t> g_opt_axis_split{0};
+std::atomic<int64_t> g_opt_spin_limit{0};
+std::atomic<int64_t> g_opt_stall_tile{-1};
+std::atomic<int64_t> g_opt_contig_variant{-1};
+std::atomic<int64_t> g_opt_cols_variant{-1};
+std::atomic<int64_t> g_opt_rscan_variant{-1};
+std::atomic<int64_t> g_opt_waves{0};
+thread_local int t_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return LIBREDUCE_ERR_CUDA;
+}
+
+// Query the current device and fill its cached properties.
+int device_state(DeviceState** out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return LIBREDUCE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    for (int v = 0; v < kNumContigVariants; ++v) st.occ_contig[v] = std::max(1, occupancy_reduce_contig(v));
+    st.occ_rows_warp = std::max(1, occupancy_reduce_rows_warp());
+    for (int v = 0; v < kNumColsVariants; ++v) st.occ_cols[v] = std::max(1, occupancy_reduce_cols(v));
+    for (int v = 0; v < kNumRScanVariants; ++v) st.occ_rscan[v] = std::max(1, occupancy_rscan_rows(v));
+    cudaGetLastError();  // occupancy queries leave no error behind
+    st.ready = true;
+  }
+  *out = &st;
+  if (dev_out) *dev_out = dev;
+  return LIBREDUCE_OK;
+}
+
+// Allocate and zero the device workspace once per device.
+int ensure_workspace(DeviceState* st) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (st->ws) return LIBREDUCE_OK;
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, kWorkspaceBytes);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = cudaMemset(p, 0, kWorkspaceBytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(p);
+    return fail_cuda(e);
+  }
+  char* base = static_cast<char*>(p);
+  st->ws = base;
+  st->err_word = reinterpret_cast<unsigned*>(base);
+  st->tickets = reinterpret_cast<unsigned*>(base + kHeaderBytes);
+  st->partials = reinterpret_cast<float*>(base + kHeaderBytes + sizeof(unsigned) * kMaxTickets);
+  return LIBREDUCE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Validation.
+// ---------------------------------------------------------------------------
+using GetAddressRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+GetAddressRangeFn address_range_fn() {
+  static GetAddressRangeFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      f = nullptr;
+    }
+    return reinterpret_cast<GetAddressRangeFn>(f);
+  }();
+  return fn;
+}
+
+// `p` must be device (or managed) memory of device `dev`, 4-byte aligned, and
+// [p, p + bytes) must lie inside one allocation.  This keeps a wrong size or a
+// host pointer from ever reaching a kernel.
+int check_buffer(const void* p, size_t bytes, int dev) {
+  if (p == nullptr) return LIBREDUCE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(p) & 3u) return LIBREDUCE_ERR_INVALID_ARG;
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return LIBREDUCE_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeDevice) {
+    if (a.device != dev) return LIBREDUCE_ERR_INVALID_ARG;
+  } else if (a.type != cudaMemoryTypeManaged) {
+    return LIBREDUCE_ERR_INVALID_ARG;
+  }
+  GetAddressRangeFn fn = address_range_fn();
+  if (fn) {
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (fn(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return LIBREDUCE_ERR_INVALID_ARG;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    if (lo < base || bytes > size || lo - base > size - bytes) return LIBREDUCE_ERR_INVALID_ARG;
+  }
+  return LIBREDUCE_OK;
+}
+
+bool mul_overflows(int64_t a, int64_t b, int64_t* r) {
+  return __builtin_mul_overflow(a, b, r);
+}
+
+bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+  if (abytes == 0 || bbytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t m) { return ceil_div(a, m) * m; }
+
+int launched(cudaError_t e) {
+  if (e != cudaSuccess) return fail_cuda(e);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return LIBREDUCE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Strategies.
+// ---------------------------------------------------------------------------
+constexpr int64_t kMinChunk = 8192;         // floats per block, lower bound
+constexpr int64_t kRowsWarpMaxLen = 2048;   // rows up to this length: one warp per row
+
+int contig_variant() {
+  const int64_t v = g_opt_contig_variant.load();
+  return (v >= 0 && v < kNumContigVariants) ? (int)v : kContigU8;
+}
+
+// Sum of `segments` contiguous segments of seg_len floats each.
+int run_contig(DeviceState* st, const float* x, int64_t segments, int64_t seg_len, float* out,
+               cudaStream_t s) {
+  const int variant = contig_variant();
+  const int64_t slots = (int64_t)st->sm_count * st->occ_contig[variant];
+  const int64_t waves = std::max<int64_t>(1, g_opt_waves.load());
+  int64_t chunks = 1;
+  const int64_t forced = g_opt_axis_split.load();
+  if (forced > 0) {
+    chunks = std::min<int64_t>(forced, ceil_div(seg_len, 4));
+  } else if (segments < 4 * slots) {
+    // Too few segments to fill the GPU: cut each into chunks.
+    const int64_t target = (segments == 1 ? waves * slots : 4 * slots);
+    chunks = ceil_div(target, segments);
+    chunks = std::min(chunks, std::max<int64_t>(1, seg_len / kMinChunk));
+  }
+  int64_t chunk_len = round_up(ceil_div(seg_len, chunks), 4);
+  chunks = ceil_div(seg_len, chunk_len);
+  if (chunks > 1 && (segments > kMaxTickets || segments * chunks > kMaxPartials)) {
+    chunks = 1;
+    chunk_len = round_up(seg_len, 4);
+  }
+  const int64_t grid = segments * chunks;
+  if (grid > INT32_MAX) return LIBREDUCE_ERR_OVERFLOW;
+  ContigParams p{x, seg_len, chunk_len, (int32_t)chunks, out, nullptr, nullptr};
+  if (chunks > 1) {
+    int rc = ensure_workspace(st);
+    if (rc) return rc;
+    p.partials = st->partials;
+    p.tickets = st->tickets;
+  }
+  return launched(launch_reduce_contig(variant, p, grid, s));
+}
+
+int run_rows_warp(DeviceState* st, const float* x, int64_t rows, int64_t len, float* out,
+                  cudaStream_t s) {
+  const int64_t slots = (int64_t)st->sm_count * st->occ_rows_warp;
+  const int64_t grid = std::max<int64_t>(1, std::min(ceil_div(rows, kThreads / 32), 8 * slots));
+  RowsWarpParams p{x, rows, len, out};
+  return launched(launch_reduce_rows_warp(p, grid, s));
+}
+
+int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int64_t inner,
+             float* out, cudaStream_t s) {
+  const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
+  int variant = vec4 ? kColsV4W8 : kColsV1W4;
+  const int64_t forced_v = g_opt_cols_variant.load();
+  if (forced_v >= 0 && forced_v < kNumColsVariants) {
+    const bool fv4 = forced_v >= kColsV4W1;
+    if (!fv4 || vec4) variant = (int)forced_v;
+  }
+  const int64_t cw = cols_block_width(variant);
+  const int64_t col_tiles = ceil_div(inner, cw);
+  const int64_t slots = (int64_t)st->sm_count * st->occ_cols[variant];
+  int64_t base_blocks = 0;
+  if (mul_overflows(outer, col_tiles, &base_blocks)) return LIBREDUCE_ERR_OVERFLOW;
+  int64_t splits = 1;
+  const int64_t forced = g_opt_axis_split.load();
+  if (forced > 0) {
+    splits = std::min(forced, reduce);
+  } else if (base_blocks < 2 * slots) {
+    splits = ceil_div(4 * slots, base_blocks);
+    splits = std::min(splits, std::max<int64_t>(1, reduce / 64));  // at least ~64 rows per slice
+  }
+  int64_t rows_per_split = ceil_div(reduce, splits);
+  splits = ceil_div(reduce, rows_per_split);
+  if (splits > 1 && (base_blocks > kMaxTickets || splits * base_blocks * cw > kMaxPartials)) {
+    // Shrink the split to fit the workspace.
+    const int64_t cap = kMaxPartials / (base_blocks * cw);
+    if (base_blocks > kMaxTickets || cap < 2) {
+      splits = 1;
+    } else {
+      splits = cap;
+    }
+    rows_per_split = ceil_div(reduce, splits);
+    splits = ceil_div(reduce, rows_per_split);
+  }
+  int64_t grid = 0;
+  if (mul_overflows(base_blocks, splits, &grid) || grid > INT32_MAX) return LIBREDUCE_ERR_OVERFLOW;
+  ColsParams p{x, outer, reduce, inner, (int32_t)col_tiles, (int32_t)splits, rows_per_split,
+               out, nullptr, nullptr};
+  if (splits > 1) {
+    int rc = ensure_workspace(st);
+    if (rc) return rc;
+    p.partials = st->partials;
+    p.tickets = st->tickets;
+  }
+  return launched(launch_reduce_cols(variant, p, grid, s));
+}
+
+int run_rscan_rows(DeviceState* st, const float* x, int64_t rows, int64_t N, float* y,
+                   cudaStream_t s) {
+  const bool vec4 = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
+                    ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
+  int variant = vec4 ? kRScanV4S4 : kRScanV1S4;
+  const int64_t forced_v = g_opt_rscan_variant.load();
+  if (forced_v >= 0 && forced_v < kNumRScanVariants && (forced_v == kRScanV1S4 || vec4))
+    variant = (int)forced_v;
+  (void)st;
+  const int64_t grid = std::min<int64_t>(rows, INT32_MAX);
+  RScanRowsParams p{x, y, rows, N};
+  return launched(launch_rscan_rows(variant, p, grid, s));
+}
+
+}  // namespace
+}  // namespace lr
+
+using namespace lr;
+
+extern "C" {
+
+int reduce_sum_f32(const float* x, int64_t n, float* out, libreduce_stream_t stream) {
+  if (n < 0 || out == nullptr || (x == nullptr && n > 0)) return LIBREDUCE_ERR_INVALID_ARG;
+  if (n > INT64_MAX / 4) return LIBREDUCE_ERR_OVERFLOW;
+  if (n > 0 && overlaps(x, (size_t)n * sizeof(float), out, sizeof(float))) return LIBREDUCE_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  int dev = 0;
+  int rc = device_state(&st, &dev);
+  if (rc) return rc;
+  if ((rc = check_buffer(out, sizeof(float), dev))) return rc;
+  if (n > 0 && (rc = check_buffer(x, (size_t)n * sizeof(float), dev))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (n == 0) {
+    const cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), s);
+    return e == cudaSuccess ? LIBREDUCE_OK : fail_cuda(e);
+  }
+  return run_contig(st, x, 1, n, out, s);
+}
+
+int reduce_axis_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
+                    libreduce_stream_t stream) {
+  if (outer < 0 || reduce < 0 || inner < 0) return LIBREDUCE_ERR_INVALID_ARG;
+  int64_t n_out = 0, total = 0;
+  if (mul_overflows(outer, inner, &n_out) || mul_overflows(n_out, reduce, &total) ||
+      total > INT64_MAX / 4)
+    return LIBREDUCE_ERR_OVERFLOW;
+  if (n_out == 0) return LIBREDUCE_OK;
+  if (out == nullptr || (x == nullptr && total > 0)) return LIBREDUCE_ERR_INVALID_ARG;
+  if (overlaps(x, (size_t)total * sizeof(float), out, (size_t)n_out * sizeof(float)))
+    return LIBREDUCE_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  int dev = 0;
+  int rc = device_state(&st, &dev);
+  if (rc) return rc;
+  if ((rc = check_buffer(out, (size_t)n_out * sizeof(float), dev))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (total == 0) {
+    const cudaError_t e = cudaMemsetAsync(out, 0, (size_t)n_out * sizeof(float), s);
+    return e == cudaSuccess ? LIBREDUCE_OK : fail_cuda(e);
+  }
+  if ((rc = check_buffer(x, (size_t)total * sizeof(float), dev))) return rc;
+  if (inner == 1) {
+    if (outer == 1) return run_contig(st, x, 1, reduce, out, s);
+    if (reduce <= kRowsWarpMaxLen && g_opt_axis_split.load() <= 0)
+      return run_rows_warp(st, x, outer, reduce, out, s);
+    return run_contig(st, x, outer, reduce, out, s);
+  }
+  return run_cols(st, x, outer, reduce, inner, out, s);
+}
+
+int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, float* y,
+                       libreduce_stream_t stream) {
+  if (rows < 0 || N < 0) return LIBREDUCE_ERR_INVALID_ARG;
+  int64_t total = 0;
+  if (mul_overflows(rows, N, &total) || total > INT64_MAX / 4) return LIBREDUCE_ERR_OVERFLOW;
+  if (total == 0) return LIBREDUCE_OK;
+  if (x == nullptr || y == nullptr) return LIBREDUCE_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)total * sizeof(float);
+  if (overlaps(x, bytes, y, bytes)) return LIBREDUCE_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  int dev = 0;
+  int rc = device_state(&st, &dev);
+  if (rc) return rc;
+  if ((rc = check_buffer(x, bytes, dev))) return rc;
+  if ((rc = check_buffer(y, bytes, dev))) return rc;
+  return run_rscan_rows(st, x, rows, N, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int libreduce_check(libreduce_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  DeviceState* st = nullptr;
+  int rc = device_state(&st, nullptr);
+  if (rc) return rc;
+  if (!st->ws) return LIBREDUCE_OK;
+  unsigned word = 0;
+  e = cudaMemcpyAsync(&word, st->err_word, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (word == 0) return LIBREDUCE_OK;
+  e = cudaMemsetAsync(st->err_word, 0, sizeof(unsigned), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return LIBREDUCE_ERR_TIMEOUT;
+}
+
+const char* libreduce_strerror(int status) {
+  switch (status) {
+    case LIBREDUCE_OK: return "ok";
+    case LIBREDUCE_ERR_INVALID_ARG: return "invalid argument";
+    case LIBREDUCE_ERR_OVERFLOW: return "size overflow or beyond the workspace limits";
+    case LIBREDUCE_ERR_ALIAS: return "output overlaps input";
+    case LIBREDUCE_ERR_CUDA: return "CUDA runtime error";
+    case LIBREDUCE_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    default: return "unknown status";
+  }
+}
+
+int libreduce_last_cuda_error(void) { return t_last_cuda_error; }
+
+int64_t libreduce_launch_count(void) { return g_launches.load(); }
+
+int libreduce_set_option(int option, int64_t value) {
+  switch (option) {
+    case LIBREDUCE_OPT_SCAN_STRATEGY:
+      if (value < 0 || value > 2) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_scan_strategy = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_AXIS_SPLIT:
+      if (value < 0 || value > INT32_MAX) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_axis_split = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_SPIN_LIMIT:
+      if (value < 0) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_spin_limit = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_STALL_TILE:
+      if (value < -1) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_stall_tile = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_CONTIG_VARIANT:
+      if (value < -1 || value >= kNumContigVariants) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_contig_variant = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_COLS_VARIANT:
+      if (value < -1 || value >= kNumColsVariants) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_cols_variant = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_RSCAN_VARIANT:
+      if (value < -1 || value >= kNumRScanVariants) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_rscan_variant = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_WAVES:
+      if (value < 0 || value > 64) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_waves = value;
+      return LIBREDUCE_OK;
+    default:
+      return LIBREDUCE_ERR_INVALID_ARG;
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,378 @@
+// lr_reduce.cu -- fp32 sum kernels: 1D sum, row sums (inner == 1) and axis
+// sums with inner > 1 (sm_103a).
+//
+// Design, by source:
+//  * "High-Performance Reduction Kernels" README, 'Key design decisions':
+//    float4 loads, warp-shuffle trees, one float per warp staged in shared
+//    memory, an SM-aware grid, and a contiguous chunk per block.  Its
+//    'Optimization: ILP4 accumulator' section: several independent loads in
+//    flight per thread.  Here each thread issues U independent 128-bit loads
+//    per step and sums them with a fixed tree.
+//  * "Seven-step reduction: 30x from one kernel", V7: warp shuffle first, shared
+//    memory only across warps.  Its atomicAdd(out, sum) finish is replaced by a
+//    deterministic one: block partials go to scratch and the last block (found
+//    with an integer ticket) adds them in index order, so reruns are
+//    bit-identical.
+//  * POPCORNBENCH trace l1_p47 (sum over dim=1 of [128, 4096, 4095]): threads
+//    run across the contiguous inner dim (coalesced) and loop over the reduce
+//    dim, several rows in flight; float4 columns only when inner % 4 == 0,
+//    because an odd row stride breaks 16-byte alignment of later rows.
+#include "lr_device.cuh"
+#include "lr_internal.h"
+
+namespace lr {
+namespace {
+
+constexpr int kFold = 16;  // blocked-accumulator fold length
+
+// Sum p[start], p[start + stride], ... (< n), eight loads in flight, fixed
+// order.  The data was written by other blocks of this launch, so it is read
+// from L2.
+__device__ __forceinline__ float sum_strided_cg(const float* p, int64_t n, int64_t start,
+                                                int64_t stride) {
+  BlockedAcc<kFold> acc;
+  int64_t k = start;
+  for (; k + 7 * stride < n; k += 8 * stride) {
+    float r[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) r[u] = ld_cg1(p + k + u * stride);
+    acc.add(tree_sum<8>(r));
+  }
+  for (; k < n; k += stride) acc.add(ld_cg1(p + k));
+  return acc.total();
+}
+
+// ---------------------------------------------------------------------------
+// 1D sum / long rows: one block per (segment, chunk).
+// ---------------------------------------------------------------------------
+template <int U>
+__global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
+  __shared__ float sh[kThreads / 32];
+  __shared__ int am_last;
+  const int t = threadIdx.x;
+  const int64_t unit = blockIdx.x;
+  const int64_t seg = unit / p.chunks;
+  const int64_t c = unit - seg * p.chunks;
+  const float* a = p.x + seg * p.seg_len + c * p.chunk_len;
+  const int64_t len = min(p.chunk_len, p.seg_len - c * p.chunk_len);
+
+  // Peel up to three leading floats so the body is 16-byte aligned.
+  int64_t head = (int64_t)((0u - (unsigned)(uintptr_t)a) & 15u) >> 2;
+  if (head > len) head = len;
+  const int64_t nvec = (len - head) >> 2;
+  const int tail = (int)((len - head) & 3);
+  const float* av = a + head;
+
+  BlockedAcc<kFold> acc;
+  constexpr int64_t S = kThreads;
+  int64_t i = t;
+  for (; i + (U - 1) * S < nvec; i += U * S) {
+    float4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) r[u] = ld_stream4(av + 4 * (i + u * S));
+    float s[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) s[u] = sum4(r[u]);
+    acc.add(tree_sum<U>(s));
+  }
+  for (; i < nvec; i += S) acc.add(sum4(ld_stream4(av + 4 * i)));
+  float v = acc.total();
+  if (t < head) v += a[t];
+  if (t < tail) v += av[4 * nvec + t];
+
+  v = block_sum<kThreads>(v, sh);
+  if (p.chunks == 1) {
+    if (t == 0) p.out[seg] = v;
+    return;
+  }
+  if (t == 0) {
+    p.partials[unit] = v;
+    __threadfence();
+    const unsigned prev = atomicAdd(p.tickets + seg, 1u);
+    am_last = (prev == (unsigned)(p.chunks - 1));
+  }
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+  float s = sum_strided_cg(p.partials + seg * p.chunks, p.chunks, t, kThreads);
+  s = block_sum<kThreads>(s, sh);
+  if (t == 0) {
+    p.out[seg] = s;
+    p.tickets[seg] = 0u;  // ready for the next launch
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Short rows: one warp per row, rows strided over the grid.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_reduce_rows_warp(RowsWarpParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t first = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  for (int64_t row = first; row < p.rows; row += nwarps) {
+    const float* a = p.x + row * p.len;
+    BlockedAcc<kFold> acc;
+    int64_t j = lane;
+    for (; j + 7 * 32 < p.len; j += 8 * 32) {
+      float r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) r[u] = ld_stream1(a + j + u * 32);
+      acc.add(tree_sum<8>(r));
+    }
+    for (; j < p.len; j += 32) acc.add(ld_stream1(a + j));
+    const float v = warp_sum(acc.total());
+    if (lane == 0) p.out[row] = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Axis sum, inner > 1: warps across columns, loop over the reduce dim.
+// ---------------------------------------------------------------------------
+template <int VEC, int WY>
+struct ColsShape {
+  static constexpr int WX = 8 / WY;            // warps across columns
+  static constexpr int CW = WX * 32 * VEC;     // columns per block
+};
+
+template <int VEC, int WY, int U>
+__global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
+  using Sh = ColsShape<VEC, WY>;
+  constexpr int WX = Sh::WX;
+  constexpr int CW = Sh::CW;
+  __shared__ __align__(16) float sh[1024];
+  __shared__ int am_last;
+
+  int64_t b = blockIdx.x;
+  const int64_t ct = b % p.col_tiles;
+  b /= p.col_tiles;
+  const int64_t s = b % p.splits;
+  const int64_t o = b / p.splits;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int wx = warp % WX;
+  const int wy = warp / WX;
+  const int jloc = wx * 32 * VEC + lane * VEC;
+  const int64_t col = ct * CW + jloc;
+  const int64_t r0 = s * p.rows_per_split;
+  const int64_t r1 = min(r0 + p.rows_per_split, p.reduce);
+  const int64_t inner = p.inner;
+
+  float res[VEC];
+#pragma unroll
+  for (int c = 0; c < VEC; ++c) res[c] = 0.f;
+
+  if (col < inner) {
+    const float* xc = p.x + o * p.reduce * inner + col;
+    BlockedAcc<kFold> acc[VEC];
+    int64_t r = r0 + wy;
+    for (; r + (U - 1) * WY < r1; r += U * WY) {
+      if constexpr (VEC == 4) {
+        float4 q[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) q[u] = ld_stream4(xc + (r + u * WY) * inner);
+        float e[4][U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          e[0][u] = q[u].x;
+          e[1][u] = q[u].y;
+          e[2][u] = q[u].z;
+          e[3][u] = q[u].w;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c].add(tree_sum<U>(e[c]));
+      } else {
+        float q[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) q[u] = ld_stream1(xc + (r + u * WY) * inner);
+        acc[0].add(tree_sum<U>(q));
+      }
+    }
+    for (; r < r1; r += WY) {
+      if constexpr (VEC == 4) {
+        const float4 q = ld_stream4(xc + r * inner);
+        acc[0].add(q.x);
+        acc[1].add(q.y);
+        acc[2].add(q.z);
+        acc[3].add(q.w);
+      } else {
+        acc[0].add(ld_stream1(xc + r * inner));
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) res[c] = acc[c].total();
+  }
+
+  // Combine the WY row groups of the block in a fixed tree.
+  if constexpr (WY > 1) {
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) sh[wy * CW + jloc + c] = res[c];
+    __syncthreads();
+    if (wy == 0) {
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        float v[WY];
+#pragma unroll
+        for (int k = 0; k < WY; ++k) v[k] = sh[k * CW + jloc + c];
+        res[c] = tree_sum<WY>(v);
+      }
+    }
+  }
+
+  if (p.splits == 1) {
+    if (wy == 0) {
+      float* outp = p.out + o * inner;
+#pragma unroll
+      for (int c = 0; c < VEC; ++c)
+        if (col + c < inner) outp[col + c] = res[c];
+    }
+    return;
+  }
+
+  // Split reduce: publish this slice's column sums, then let the last block of
+  // (o, ct) add the slices in slice order.
+  float* part_base = p.partials + (o * p.splits) * (int64_t)p.col_tiles * CW + ct * CW;
+  const int64_t slice_stride = (int64_t)p.col_tiles * CW;
+  if (wy == 0) {
+    float* mine = part_base + s * slice_stride;
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) mine[jloc + c] = res[c];
+    __threadfence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.tickets + o * p.col_tiles + ct, 1u);
+    am_last = (prev == (unsigned)(p.splits - 1));
+  }
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+
+  constexpr int Q = CW / 4;            // float4 columns of the tile
+  constexpr int G = kThreads / Q;      // slice groups
+  const int q = threadIdx.x % Q;
+  const int g = threadIdx.x / Q;
+  BlockedAcc<kFold> acc4[4];
+  {
+    int64_t k = g;
+    const int64_t S = p.splits;
+    for (; k + 3 * G < S; k += 4 * G) {
+      float4 r[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) r[u] = ld_cg4(part_base + (k + u * G) * slice_stride + 4 * q);
+      float e[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        e[0][u] = r[u].x;
+        e[1][u] = r[u].y;
+        e[2][u] = r[u].z;
+        e[3][u] = r[u].w;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc4[c].add(tree_sum<4>(e[c]));
+    }
+    for (; k < S; k += G) {
+      const float4 r = ld_cg4(part_base + k * slice_stride + 4 * q);
+      acc4[0].add(r.x);
+      acc4[1].add(r.y);
+      acc4[2].add(r.z);
+      acc4[3].add(r.w);
+    }
+  }
+  __syncthreads();  // sh may still be read by the row-group combine above
+#pragma unroll
+  for (int c = 0; c < 4; ++c) sh[g * CW + 4 * q + c] = acc4[c].total();
+  __syncthreads();
+  if (threadIdx.x < Q) {
+    float* outp = p.out + o * inner;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float v[G];
+#pragma unroll
+      for (int k = 0; k < G; ++k) v[k] = sh[k * CW + 4 * q + c];
+      const float tot = tree_sum<G>(v);
+      const int64_t cc = ct * CW + 4 * q + c;
+      if (cc < inner) outp[cc] = tot;
+    }
+    if (threadIdx.x == 0) p.tickets[o * p.col_tiles + ct] = 0u;
+  }
+}
+
+// Unroll depth (rows or vectors in flight per thread) of each variant.
+constexpr int kColsU = 8;
+
+template <typename K>
+int occupancy_of(K kernel) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+int cols_block_width(int variant) {
+  switch (variant) {
+    case kColsV1W1: return ColsShape<1, 1>::CW;
+    case kColsV1W4: return ColsShape<1, 4>::CW;
+    case kColsV1W8: return ColsShape<1, 8>::CW;
+    case kColsV4W1: return ColsShape<4, 1>::CW;
+    case kColsV4W4: return ColsShape<4, 4>::CW;
+    case kColsV4W8: return ColsShape<4, 8>::CW;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_reduce_contig(int variant, const ContigParams& p, int64_t grid, cudaStream_t s) {
+  const dim3 g((unsigned)grid);
+  switch (variant) {
+    case kContigU4: k_reduce_contig<4><<<g, kThreads, 0, s>>>(p); break;
+    case kContigU8: k_reduce_contig<8><<<g, kThreads, 0, s>>>(p); break;
+    case kContigU16: k_reduce_contig<16><<<g, kThreads, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_rows_warp(const RowsWarpParams& p, int64_t grid, cudaStream_t s) {
+  k_reduce_rows_warp<<<dim3((unsigned)grid), kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_cols(int variant, const ColsParams& p, int64_t grid, cudaStream_t s) {
+  const dim3 g((unsigned)grid);
+  switch (variant) {
+    case kColsV1W1: k_reduce_cols<1, 1, kColsU><<<g, kThreads, 0, s>>>(p); break;
+    case kColsV1W4: k_reduce_cols<1, 4, kColsU><<<g, kThreads, 0, s>>>(p); break;
+    case kColsV1W8: k_reduce_cols<1, 8, kColsU><<<g, kThreads, 0, s>>>(p); break;
+    case kColsV4W1: k_reduce_cols<4, 1, kColsU><<<g, kThreads, 0, s>>>(p); break;
+    case kColsV4W4: k_reduce_cols<4, 4, kColsU><<<g, kThreads, 0, s>>>(p); break;
+    case kColsV4W8: k_reduce_cols<4, 8, kColsU><<<g, kThreads, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+int occupancy_reduce_contig(int variant) {
+  switch (variant) {
+    case kContigU4: return occupancy_of(k_reduce_contig<4>);
+    case kContigU8: return occupancy_of(k_reduce_contig<8>);
+    case kContigU16: return occupancy_of(k_reduce_contig<16>);
+    default: return 0;
+  }
+}
+
+int occupancy_reduce_rows_warp() { return occupancy_of(k_reduce_rows_warp); }
+
+int occupancy_reduce_cols(int variant) {
+  switch (variant) {
+    case kColsV1W1: return occupancy_of(k_reduce_cols<1, 1, kColsU>);
+    case kColsV1W4: return occupancy_of(k_reduce_cols<1, 4, kColsU>);
+    case kColsV1W8: return occupancy_of(k_reduce_cols<1, 8, kColsU>);
+    case kColsV4W1: return occupancy_of(k_reduce_cols<4, 1, kColsU>);
+    case kColsV4W4: return occupancy_of(k_reduce_cols<4, 4, kColsU>);
+    case kColsV4W8: return occupancy_of(k_reduce_cols<4, 8, kColsU>);
+    default: return 0;
+  }
+}
+
+}  // namespace lr
