@@ -7,6 +7,7 @@ One step runs every primitive once over its full-size synthetic workload:
   axis_4096x65536_d1      reduce_axis_f32  [4096, 65536] d1      uniform[-1,1) seed 11
   axis_65536x4096_d0      reduce_axis_f32  [65536, 4096] d0      uniform[-1,1) seed 11
   rcumsum_32768x32768     reverse_cumsum   [32768, 32768]        uniform[0,1)  seed 3
+  rcumsum_1x1e9           reverse_cumsum   [1, 1e9] (look-back)  uniform[0,1)  seed 3
 
 The metric is effective HBM bandwidth: algorithmic bytes (every input read
 once, every output written once) divided by device time, in GB/s, and as a
@@ -15,6 +16,7 @@ each is larger than L2 (>= 1 GiB), so no flush is needed between launches;
 the small-n sweep of the 1D sum flushes L2 before every timed launch.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+        python bench.py --profile-case NAME [--steps K] [--warmup W]   (small case for ncu)
 Under torchrun (N > 1) each rank runs the same step on its own GPU (replicas,
 weak scaling); time is the max over ranks.
 """
@@ -42,7 +44,16 @@ from reduction_scan_primitives_gb300 import inputs  # noqa: E402
 
 METRIC = "effective HBM GB/s and % of GB300 peak per reduce/scan config (1 GPU)"
 STEP_WORKLOADS = ["sum_1e9", "axis_128x4096x4095_d1", "axis_4096x65536_d1", "axis_65536x4096_d0",
-                  "rcumsum_32768x32768"]
+                  "rcumsum_32768x32768", "rcumsum_1x1e9"]
+# Small cases of each kernel for ncu captures: larger than L2, a few GB at most.
+PROFILE_CASES = {
+    "sum_2e8": dict(op="sum", shape=(200_000_000,), dist="uniform01", seed=42),
+    "axis_16x4096x4095_d1": dict(op="axis", shape=(16, 4096, 4095), dim=1, dist="normal", seed=7),
+    "axis_4096x65536_d1": dict(inputs.WORKLOADS["axis_4096x65536_d1"]),
+    "axis_65536x4096_d0": dict(inputs.WORKLOADS["axis_65536x4096_d0"]),
+    "rcumsum_4096x32768": dict(op="rcumsum", shape=(4096, 32768), dist="uniform01", seed=3),
+    "rcumsum_1x1e8": dict(op="rcumsum", shape=(1, 100_000_000), dist="uniform01", seed=3),
+}
 FALLBACK_HBM_GBS = 6800.0
 # Context only (another machine): the page's T4 figures for the 1D sum.
 PAGES_T4 = {"sum_1e8_ms": 1.4716, "sum_1e9_ms": 14.4983}
@@ -180,9 +191,13 @@ def recorded_traffic():
 # ---------------------------------------------------------------------------
 # Workloads.
 # ---------------------------------------------------------------------------
+def workload_spec(name):
+    return inputs.WORKLOADS.get(name) or PROFILE_CASES[name]
+
+
 def make_call(name, x, out):
     from reduction_scan_primitives_gb300 import libreduce as L
-    w = inputs.WORKLOADS[name]
+    w = workload_spec(name)
     if w["op"] == "sum":
         return lambda: L.reduce_sum_f32(x, out=out)
     if w["op"] == "axis":
@@ -191,7 +206,7 @@ def make_call(name, x, out):
 
 
 def alloc_workload(name, device):
-    w = inputs.WORKLOADS[name]
+    w = workload_spec(name)
     x = inputs.make(w["shape"], w["dist"], w["seed"], device=device)
     if w["op"] == "sum":
         out = torch.empty((), dtype=torch.float32, device=device)
@@ -217,7 +232,10 @@ def time_sweep(device, reps=10):
             L.reduce_sum_f32(x, out=out)
         times = []
         for _ in range(reps):
+            # Write a buffer larger than L2, then read it back so the dirty lines
+            # are written out before the timed launch rather than during it.
             flush.fill_(1.0)
+            flush.sum()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             L.reduce_sum_f32(x, out=out)
@@ -235,47 +253,35 @@ def time_sweep(device, reps=10):
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample of each workload.
 # ---------------------------------------------------------------------------
-def oracle_sample(name, x_dev):
-    """(callable running the oracle on a sample, sample's algorithmic bytes, description)."""
+def oracle_run(name, x_dev):
+    """(callable running the oracle on the whole workload, its algorithmic bytes)."""
     import numpy as np
 
     import oracle
-    w = inputs.WORKLOADS[name]
+    w = workload_spec(name)
+    xs = np.ascontiguousarray(x_dev.cpu().numpy())
     if w["op"] == "sum":
-        m = 25_000_000
-        xs = x_dev.reshape(-1)[:m].cpu().numpy()
-        return (lambda: oracle.sum1d(xs)), 4 * m + 4, f"first {m} elements"
+        return (lambda: oracle.sum1d(xs)), 4 * xs.size + 4
     if w["op"] == "axis":
         o, r, i = inputs.canonical_axis(w["shape"], w["dim"])
-        x3 = x_dev.reshape(o, r, i)
-        if o > 1:
-            k = max(1, o // 128) if i > 1 else max(1, o // 64)
-            xs = np.ascontiguousarray(x3[:k].cpu().numpy())
-            return ((lambda: oracle.axis_sum(xs, k, r, i)), 4 * k * r * i + 4 * k * i,
-                    f"first {k} of {o} outer slices")
-        rr = max(1, r // 64)
-        xs = np.ascontiguousarray(x3[:, :rr].cpu().numpy())
-        return ((lambda: oracle.axis_sum(xs, 1, rr, i)), 4 * rr * i + 4 * i,
-                f"first {rr} of {r} reduce rows")
+        return (lambda: oracle.axis_sum(xs, o, r, i)), 4 * xs.size + 4 * o * i
     rows, n = w["shape"]
-    k = max(1, rows // 128)
-    xs = np.ascontiguousarray(x_dev[:k].cpu().numpy())
-    return (lambda: oracle.reverse_cumsum(xs, k, n)), 8 * k * n, f"first {k} of {rows} rows"
+    return (lambda: oracle.reverse_cumsum(xs, rows, n)), 8 * xs.size
 
 
-def cpu_baseline(data, device):
-    total_bytes, total_s, desc = 0, 0.0, []
+def cpu_baseline(data):
+    """The oracle, single-threaded, over every workload of one step, once."""
+    total_bytes, total_s = 0, 0.0
     for name in STEP_WORKLOADS:
-        fn, nbytes, what = oracle_sample(name, data[name][0])
-        fn()  # first touch
+        fn, nbytes = oracle_run(name, data[name][0])
         t0 = time.perf_counter()
         fn()
-        dt = time.perf_counter() - t0
+        total_s += time.perf_counter() - t0
         total_bytes += nbytes
-        total_s += dt
-        desc.append(f"{name}: {what}")
+        del fn
     return {"value": round(total_bytes / total_s / 1e9, 3), "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "sample": "; ".join(desc), "seconds": round(total_s, 2)}
+            "kind": "oracle", "sample": "one step: every workload in full, once (host copy of the "
+            "device inputs)", "seconds": round(total_s, 2)}
 
 
 # ---------------------------------------------------------------------------
@@ -299,19 +305,18 @@ def run_ours(args):
     step_bytes = sum(nbytes.values())
     torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        for name in STEP_WORKLOADS:
-            calls[name]()
-    torch.cuda.synchronize()
-    L.check(device)
-
     stream = torch.cuda.current_stream(device)
     ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                  for _ in range(args.steps)] for name in STEP_WORKLOADS}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = L.launch_count()
     with ClockSampler(local) as clocks:
         time.sleep(0.3)
+        for _ in range(args.warmup):
+            for name in STEP_WORKLOADS:
+                calls[name]()
+        torch.cuda.synchronize()
+        L.check(device)
+        launches0 = L.launch_count()
         barrier(world)
         torch.cuda.synchronize()
         start.record(stream)
@@ -351,7 +356,7 @@ def run_ours(args):
 
     e2e = run_e2e(args, data, nbytes, device, world) if not args.no_e2e else None
     sweep = time_sweep(device) if (rank == 0 and not args.no_sweep) else None
-    cpu = cpu_baseline(data, device) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    cpu = cpu_baseline(data) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     if rank == 0:
         line = {
@@ -430,8 +435,10 @@ def run_reference(args):
             o, r, i = inputs.canonical_axis(w["shape"], w["dim"])
             shape = [max(1, o // 128), r, i] if o > 1 and i > 1 else (
                 [max(1, o // 64), r, i] if o > 1 else [1, max(1, r // 64), i])
+        elif shape[0] >= 128:
+            shape = [shape[0] // 128, shape[1]]
         else:
-            shape = [max(1, shape[0] // 128), shape[1]]
+            shape = [shape[0], max(1, shape[1] // 128)]
         samples[name] = inputs.make(tuple(shape), w["dist"], w["seed"]).numpy()
     import oracle
 
@@ -472,16 +479,38 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """Run one small case a few times (for an ncu capture of its kernel)."""
+    from reduction_scan_primitives_gb300 import build as lib_build
+    from reduction_scan_primitives_gb300 import libreduce as L
+    lib_build.build()
+    L.load()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    x, out = alloc_workload(args.profile_case, device)
+    call = make_call(args.profile_case, x, out)
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    L.check(device)
+    print(json.dumps({"profile_case": args.profile_case, "launches": args.warmup + args.steps,
+                      "bytes": inputs.algorithmic_bytes(workload_spec(args.profile_case))}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES))
     args = ap.parse_args(argv)
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         print("bench: --warmup raised to 3 (minimum)", file=sys.stderr)
         args.warmup = 3

@@ -154,7 +154,8 @@ int64_t libreduce_launch_count(void);
  *                                 float4 columns (needs inner % 4 == 0, aligned x)
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
  *                                 2 float4 x 4 (float4 needs N % 4 == 0, aligned x, y)
- *   LIBREDUCE_OPT_WAVES           1D sum: blocks = waves x resident blocks (0 = 1) */
+ *   LIBREDUCE_OPT_WAVES           1D sum: blocks = waves x resident blocks (0 = automatic:
+ *                                 one wave, or more blocks of 64 Ki floats for long arrays) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6
 #define LIBREDUCE_OPT_RSCAN_VARIANT 7

@@ -23,7 +23,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxTickets = 1 << 16;       // integer tickets (per row / column tile)
 constexpr int64_t kMaxPartials = 1 << 22;      // fp32 partial sums (16 MiB)
-constexpr size_t kHeaderBytes = 256;           // device error word and spare
+constexpr size_t kHeaderBytes = 256;           // error word, abort word, tile counter
+constexpr int64_t kMaxLookbackTiles = 1 << 20; // look-back tiles per launch
 constexpr size_t kWorkspaceBytes =
     kHeaderBytes + sizeof(unsigned) * kMaxTickets + sizeof(float) * kMaxPartials;
 
@@ -39,6 +40,11 @@ struct DeviceState {
   unsigned* err_word = nullptr;
   unsigned* tickets = nullptr;
   float* partials = nullptr;
+  // Look-back region (allocated by the first look-back scan on the device).
+  unsigned long long* node_val = nullptr;
+  unsigned* node_arrive = nullptr;
+  std::atomic<unsigned> epoch{0};
+  int occ_lookback[kNumLookbackVariants] = {};
 };
 
 std::mutex g_mu;
@@ -74,6 +80,8 @@ int device_state(DeviceState** out, int* dev_out) {
     st.occ_rows_warp = std::max(1, occupancy_reduce_rows_warp());
     for (int v = 0; v < kNumColsVariants; ++v) st.occ_cols[v] = std::max(1, occupancy_reduce_cols(v));
     for (int v = 0; v < kNumRScanVariants; ++v) st.occ_rscan[v] = std::max(1, occupancy_rscan_rows(v));
+    for (int v = 0; v < kNumLookbackVariants; ++v)
+      st.occ_lookback[v] = std::max(1, occupancy_rscan_lookback(v));
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
   }
@@ -100,6 +108,30 @@ int ensure_workspace(DeviceState* st) {
   st->err_word = reinterpret_cast<unsigned*>(base);
   st->tickets = reinterpret_cast<unsigned*>(base + kHeaderBytes);
   st->partials = reinterpret_cast<float*>(base + kHeaderBytes + sizeof(unsigned) * kMaxTickets);
+  return LIBREDUCE_OK;
+}
+
+// Allocate the look-back flags once per device.  Their epochs make stale
+// contents harmless, but they start zeroed (epoch 0 is never used).
+int ensure_lookback(DeviceState* st) {
+  int rc = ensure_workspace(st);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (st->node_val) return LIBREDUCE_OK;
+  const size_t nodes = 2 * (size_t)kMaxLookbackTiles;
+  const size_t bytes = nodes * (sizeof(unsigned long long) + sizeof(unsigned));
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = cudaMemset(p, 0, bytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(p);
+    return fail_cuda(e);
+  }
+  st->node_val = static_cast<unsigned long long*>(p);
+  st->node_arrive = reinterpret_cast<unsigned*>(static_cast<char*>(p) +
+                                                nodes * sizeof(unsigned long long));
   return LIBREDUCE_OK;
 }
 
@@ -174,11 +206,12 @@ int launched(cudaError_t e) {
 // Strategies.
 // ---------------------------------------------------------------------------
 constexpr int64_t kMinChunk = 8192;         // floats per block, lower bound
+constexpr int64_t kTargetChunk = 65536;     // floats per block of a long 1D sum (256 KiB)
 constexpr int64_t kRowsWarpMaxLen = 2048;   // rows up to this length: one warp per row
 
 int contig_variant() {
   const int64_t v = g_opt_contig_variant.load();
-  return (v >= 0 && v < kNumContigVariants) ? (int)v : kContigU8;
+  return (v >= 0 && v < kNumContigVariants) ? (int)v : kContigU16;
 }
 
 // Sum of `segments` contiguous segments of seg_len floats each.
@@ -186,15 +219,20 @@ int run_contig(DeviceState* st, const float* x, int64_t segments, int64_t seg_le
                cudaStream_t s) {
   const int variant = contig_variant();
   const int64_t slots = (int64_t)st->sm_count * st->occ_contig[variant];
-  const int64_t waves = std::max<int64_t>(1, g_opt_waves.load());
+  const int64_t waves = g_opt_waves.load();
   int64_t chunks = 1;
   const int64_t forced = g_opt_axis_split.load();
   if (forced > 0) {
     chunks = std::min<int64_t>(forced, ceil_div(seg_len, 4));
+  } else if (segments == 1) {
+    // One long array: at least one full wave of blocks, and blocks of about
+    // kTargetChunk floats beyond that, so the blocks that finish first pick
+    // up more work instead of idling through a long tail.
+    chunks = waves > 0 ? waves * slots : std::max(slots, ceil_div(seg_len, kTargetChunk));
+    chunks = std::min(chunks, std::max<int64_t>(1, seg_len / kMinChunk));
   } else if (segments < 4 * slots) {
-    // Too few segments to fill the GPU: cut each into chunks.
-    const int64_t target = (segments == 1 ? waves * slots : 4 * slots);
-    chunks = ceil_div(target, segments);
+    // Too few rows to fill the GPU: cut each into chunks.
+    chunks = ceil_div(4 * slots, segments);
     chunks = std::min(chunks, std::max<int64_t>(1, seg_len / kMinChunk));
   }
   int64_t chunk_len = round_up(ceil_div(seg_len, chunks), 4);
@@ -226,7 +264,7 @@ int run_rows_warp(DeviceState* st, const float* x, int64_t rows, int64_t len, fl
 int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int64_t inner,
              float* out, cudaStream_t s) {
   const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
-  int variant = vec4 ? kColsV4W8 : kColsV1W4;
+  int variant = vec4 ? kColsV4W4 : kColsV1W4;
   const int64_t forced_v = g_opt_cols_variant.load();
   if (forced_v >= 0 && forced_v < kNumColsVariants) {
     const bool fv4 = forced_v >= kColsV4W1;
@@ -241,8 +279,10 @@ int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int
   const int64_t forced = g_opt_axis_split.load();
   if (forced > 0) {
     splits = std::min(forced, reduce);
-  } else if (base_blocks < 2 * slots) {
-    splits = ceil_div(4 * slots, base_blocks);
+  } else if (base_blocks < slots) {
+    // Too few column tiles to fill the GPU: slice the reduce axis so the grid
+    // is one full wave (measured best for a short kernel: no tail, no ramp).
+    splits = ceil_div(slots, base_blocks);
     splits = std::min(splits, std::max<int64_t>(1, reduce / 64));  // at least ~64 rows per slice
   }
   int64_t rows_per_split = ceil_div(reduce, splits);
@@ -271,6 +311,27 @@ int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int
   return launched(launch_reduce_cols(variant, p, grid, s));
 }
 
+constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with up to 1 us sleeps): about a second
+
+int run_rscan_lookback(DeviceState* st, const float* x, int64_t rows, int64_t N, float* y,
+                       cudaStream_t s, int variant) {
+  const int64_t tile = lookback_tile(variant);
+  const int64_t tiles = ceil_div(N, tile);
+  int64_t total = 0;
+  if (mul_overflows(rows, tiles, &total) || total > kMaxLookbackTiles) return LIBREDUCE_ERR_OVERFLOW;
+  int rc = ensure_lookback(st);
+  if (rc) return rc;
+  unsigned epoch = st->epoch.fetch_add(1) + 1;
+  if (epoch == 0) epoch = st->epoch.fetch_add(1) + 1;  // 0 marks "never written"
+  unsigned* counter = st->err_word + 2;
+  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const int64_t spin = g_opt_spin_limit.load();
+  RScanLookbackParams p{x, y, rows, N, tiles, st->node_val, st->node_arrive, counter, st->err_word,
+                        epoch, spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load()};
+  return launched(launch_rscan_lookback(variant, p, total, s));
+}
+
 int run_rscan_rows(DeviceState* st, const float* x, int64_t rows, int64_t N, float* y,
                    cudaStream_t s) {
   const bool vec4 = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
@@ -279,7 +340,15 @@ int run_rscan_rows(DeviceState* st, const float* x, int64_t rows, int64_t N, flo
   const int64_t forced_v = g_opt_rscan_variant.load();
   if (forced_v >= 0 && forced_v < kNumRScanVariants && (forced_v == kRScanV1S4 || vec4))
     variant = (int)forced_v;
-  (void)st;
+  // Few rows cannot fill the GPU one block per row: use the look-back scan,
+  // which spreads every row's tiles over all SMs.
+  const int64_t strategy = g_opt_scan_strategy.load();
+  const int lb_variant = vec4 ? kLookbackV4 : kLookbackV1;
+  const int64_t lb_tiles = ceil_div(N, lookback_tile(lb_variant));
+  const int64_t row_slots = (int64_t)st->sm_count * st->occ_rscan[variant];
+  const bool lookback_fits = rows <= kMaxLookbackTiles / std::max<int64_t>(1, lb_tiles);
+  if (strategy == 2 || (strategy == 0 && rows < row_slots && lb_tiles >= 4 && lookback_fits))
+    return run_rscan_lookback(st, x, rows, N, y, s, lb_variant);
   const int64_t grid = std::min<int64_t>(rows, INT32_MAX);
   RScanRowsParams p{x, y, rows, N};
   return launched(launch_rscan_rows(variant, p, grid, s));

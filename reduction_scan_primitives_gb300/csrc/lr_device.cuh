@@ -54,6 +54,33 @@ __device__ __forceinline__ float4 ld_cg4(const float* p) {
 }
 
 // ---------------------------------------------------------------------------
+// Inter-block signalling (GPU scope).  Used by the look-back scan, whose
+// blocks publish values that other blocks of the same launch wait for.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned atom_exch_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------------------
 // Summation building blocks.  Every tree below has a fixed shape, so a given
 // input always produces the same bits.
 // ---------------------------------------------------------------------------

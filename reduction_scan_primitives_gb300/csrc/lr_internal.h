@@ -58,6 +58,27 @@ struct RScanRowsParams {
   int64_t N;
 };
 
+// --- Reverse cumulative sum, single-pass decoupled look-back ----------------
+// One block per tile.  Blocks take tickets in scan order (right to left within
+// a row, row after row): ticket t is tile k = t % tiles_per_row counted from
+// the right end of row t / tiles_per_row.  Dyadic block sums of tile
+// aggregates are published as 64-bit words {epoch, fp32 bits}; a word counts
+// only if its epoch equals this launch's, so the flags never need clearing.
+struct RScanLookbackParams {
+  const float* x;
+  float* y;
+  int64_t rows;
+  int64_t N;
+  int64_t tiles_per_row;
+  unsigned long long* node_val;  // rows * 2 * tiles_per_row words
+  unsigned* node_arrive;         // same shape (levels >= 1 used)
+  unsigned* tile_counter;        // zero on entry
+  unsigned* err_word;            // bit 0 set when a wait runs out
+  unsigned epoch;                // nonzero, different for every launch on the device
+  int64_t spin_limit;            // polls before a wait gives up
+  int64_t stall_tile;            // test fault: this ticket never publishes (-1: none)
+};
+
 // Variants are small integers chosen by the dispatcher; each launcher
 // returns cudaErrorInvalidValue for a variant it does not have.
 enum ContigVariant { kContigU4 = 0, kContigU8 = 1, kContigU16 = 2, kNumContigVariants };
@@ -71,6 +92,10 @@ enum ColsVariant {
   kNumColsVariants
 };
 enum RScanVariant { kRScanV1S4 = 0, kRScanV4S2 = 1, kRScanV4S4 = 2, kNumRScanVariants };
+enum LookbackVariant { kLookbackV1 = 0, kLookbackV4 = 1, kNumLookbackVariants };
+
+// Elements per tile of each look-back variant.
+int64_t lookback_tile(int variant);
 
 // Columns covered by one block of a cols variant.
 int cols_block_width(int variant);
@@ -79,11 +104,14 @@ cudaError_t launch_reduce_contig(int variant, const ContigParams& p, int64_t gri
 cudaError_t launch_reduce_rows_warp(const RowsWarpParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_reduce_cols(int variant, const ColsParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t grid, cudaStream_t s);
+cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int64_t grid,
+                                  cudaStream_t s);
 
 // Resident 256-thread blocks per SM for each kernel variant (0 on error).
 int occupancy_reduce_contig(int variant);
 int occupancy_reduce_rows_warp();
 int occupancy_reduce_cols(int variant);
 int occupancy_rscan_rows(int variant);
+int occupancy_rscan_lookback(int variant);
 
 }  // namespace lr

@@ -69,6 +69,8 @@ WORKLOADS = {
     "axis_4096x65536_d1": dict(op="axis", shape=(4096, 65536), dim=1, dist="uniform_pm1", seed=11),
     "axis_65536x4096_d0": dict(op="axis", shape=(65536, 4096), dim=0, dist="uniform_pm1", seed=11),
     "rcumsum_32768x32768": dict(op="rcumsum", shape=(32768, 32768), dist="uniform01", seed=3),
+    # Few long rows (the look-back scan): one row of 1e9.
+    "rcumsum_1x1e9": dict(op="rcumsum", shape=(1, 1_000_000_000), dist="uniform01", seed=3),
 }
 
 # The 1D sweep sizes of the sum benchmark (uniform[0,1), seed 42).
