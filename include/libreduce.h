@@ -114,6 +114,32 @@ int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, float* y,
                        libreduce_stream_t stream);
 
 /*
+ * reduce_sum_f32_noalloc -- out[0] = sum_{i<n} x[i], allocating nothing.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory.  reduce_sum_f32 takes its scratch from a
+ * workspace the library cudaMallocs on first use; some callers cannot allow
+ * that (code inside a custom allocator or a memory-capped service, where every
+ * device byte must be accounted for up front, or a stream capture in
+ * progress).  This call runs the same kernel with its scratch (a ticket and up
+ * to 16384 partial sums, 64.25 KiB) in a fixed static device array that every
+ * GPU loading the library holds until exit.  It calls no cudaMalloc, cudaFree
+ * or other allocating routine.
+ *   x    device, n floats (may be NULL when n == 0)
+ *   n    0 <= n <= 2^36 (16384 blocks of at most 2^22 floats)
+ *   out  device, 1 float
+ * The result equals reduce_sum_f32's within the documented tolerance (the
+ * blocking can differ once more than 16384 blocks would be used).
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array, and the ticket
+ * is cleared on the stream before each launch, so calls that overlap on the
+ * GPU (different streams, or other threads) race and must be avoided.
+ * Errors: INVALID_ARG, OVERFLOW (n > 2^36), ALIAS (out inside x), CUDA.
+ */
+int reduce_sum_f32_noalloc(const float* x, int64_t n, float* out, libreduce_stream_t stream);
+
+/*
  * libreduce_check -- synchronise `stream`, then return and clear the current
  * device's error word: LIBREDUCE_OK, or LIBREDUCE_ERR_TIMEOUT if a bounded
  * device-side wait ran out since the last check (the affected outputs are then

@@ -355,6 +355,11 @@ int run_rscan_rows(DeviceState* st, const float* x, int64_t rows, int64_t N, flo
 }
 
 }  // namespace
+
+int check_device_buffer(const void* p, size_t bytes, int dev) { return check_buffer(p, bytes, dev); }
+int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace lr
 
 using namespace lr;

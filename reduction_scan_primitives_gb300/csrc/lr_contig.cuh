@@ -1,0 +1,99 @@
+// lr_contig.cuh -- the contiguous-chunk sum kernel (1D sum and long rows),
+// shared by the translation units that launch it.  Each including file gets
+// its own instantiation (internal linkage).
+//
+// Design, by source: "High-Performance Reduction Kernels" README ('Key design
+// decisions': float4 loads, warp-shuffle trees, one float per warp in shared
+// memory, contiguous block assignment; 'Optimization: ILP4 accumulator':
+// several independent loads in flight per thread) and "Seven-step reduction:
+// 30x from one kernel" (V7), with the atomicAdd finish replaced by a
+// deterministic last-block combine.
+#pragma once
+
+#include "lr_device.cuh"
+#include "lr_internal.h"
+
+namespace lr {
+namespace {
+
+constexpr int kFold = 16;  // blocked-accumulator fold length
+
+// Sum p[start], p[start + stride], ... (< n), eight loads in flight, fixed
+// order.  The data was written by other blocks of this launch, so it is read
+// from L2.
+__device__ __forceinline__ float sum_strided_cg(const float* p, int64_t n, int64_t start,
+                                                int64_t stride) {
+  BlockedAcc<kFold> acc;
+  int64_t k = start;
+  for (; k + 7 * stride < n; k += 8 * stride) {
+    float r[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) r[u] = ld_cg1(p + k + u * stride);
+    acc.add(tree_sum<8>(r));
+  }
+  for (; k < n; k += stride) acc.add(ld_cg1(p + k));
+  return acc.total();
+}
+
+// ---------------------------------------------------------------------------
+// 1D sum / long rows: one block per (segment, chunk).
+// ---------------------------------------------------------------------------
+template <int U>
+__global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
+  __shared__ float sh[kThreads / 32];
+  __shared__ int am_last;
+  const int t = threadIdx.x;
+  const int64_t unit = blockIdx.x;
+  const int64_t seg = unit / p.chunks;
+  const int64_t c = unit - seg * p.chunks;
+  const float* a = p.x + seg * p.seg_len + c * p.chunk_len;
+  const int64_t len = min(p.chunk_len, p.seg_len - c * p.chunk_len);
+
+  // Peel up to three leading floats so the body is 16-byte aligned.
+  int64_t head = (int64_t)((0u - (unsigned)(uintptr_t)a) & 15u) >> 2;
+  if (head > len) head = len;
+  const int64_t nvec = (len - head) >> 2;
+  const int tail = (int)((len - head) & 3);
+  const float* av = a + head;
+
+  BlockedAcc<kFold> acc;
+  constexpr int64_t S = kThreads;
+  int64_t i = t;
+  for (; i + (U - 1) * S < nvec; i += U * S) {
+    float4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) r[u] = ld_stream4(av + 4 * (i + u * S));
+    float s[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) s[u] = sum4(r[u]);
+    acc.add(tree_sum<U>(s));
+  }
+  for (; i < nvec; i += S) acc.add(sum4(ld_stream4(av + 4 * i)));
+  float v = acc.total();
+  if (t < head) v += a[t];
+  if (t < tail) v += av[4 * nvec + t];
+
+  v = block_sum<kThreads>(v, sh);
+  if (p.chunks == 1) {
+    if (t == 0) p.out[seg] = v;
+    return;
+  }
+  if (t == 0) {
+    p.partials[unit] = v;
+    __threadfence();
+    const unsigned prev = atomicAdd(p.tickets + seg, 1u);
+    am_last = (prev == (unsigned)(p.chunks - 1));
+  }
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+  float s = sum_strided_cg(p.partials + seg * p.chunks, p.chunks, t, kThreads);
+  s = block_sum<kThreads>(s, sh);
+  if (t == 0) {
+    p.out[seg] = s;
+    p.tickets[seg] = 0u;  // ready for the next launch
+  }
+}
+
+}  // namespace
+}  // namespace lr

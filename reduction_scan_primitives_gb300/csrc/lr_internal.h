@@ -107,6 +107,11 @@ cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t gri
 cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int64_t grid,
                                   cudaStream_t s);
 
+// Host helpers defined in lr_api.cu, for entry points in other files.
+int check_device_buffer(const void* p, size_t bytes, int dev);  // a libreduce status
+int record_cuda_error(cudaError_t e);                           // returns the CUDA status
+void count_launch();
+
 // Resident 256-thread blocks per SM for each kernel variant (0 on error).
 int occupancy_reduce_contig(int variant);
 int occupancy_reduce_rows_warp();

@@ -76,6 +76,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.reduce_sum_f32.argtypes = [vp, i64, vp, vp]
     lib.reduce_sum_f32.restype = i32
+    lib.reduce_sum_f32_noalloc.argtypes = [vp, i64, vp, vp]
+    lib.reduce_sum_f32_noalloc.restype = i32
     lib.reduce_axis_f32.argtypes = [vp, i64, i64, i64, vp, vp]
     lib.reduce_axis_f32.restype = i32
     lib.reverse_cumsum_f32.argtypes = [vp, i64, i64, vp, vp]
