@@ -51,6 +51,13 @@
 extern "C" {
 #endif
 
+/* Exported entry points (the library is built with hidden visibility). */
+#if defined(__GNUC__)
+#define LIBREDUCE_API __attribute__((visibility("default")))
+#else
+#define LIBREDUCE_API
+#endif
+
 /* Same type as cudaStream_t; declared here so callers need no CUDA header. */
 typedef struct CUstream_st* libreduce_stream_t;
 
@@ -75,7 +82,7 @@ typedef struct CUstream_st* libreduce_stream_t;
  * Errors: INVALID_ARG (n < 0, x NULL with n > 0, out NULL, bad pointer),
  *         OVERFLOW (4*n overflows int64), ALIAS (out inside x), CUDA.
  */
-int reduce_sum_f32(const float* x, int64_t n, float* out, libreduce_stream_t stream);
+LIBREDUCE_API int reduce_sum_f32(const float* x, int64_t n, float* out, libreduce_stream_t stream);
 
 /*
  * reduce_axis_f32 -- out[o*inner + i] = sum_{r<reduce} x[(o*reduce + r)*inner + i].
@@ -92,7 +99,7 @@ int reduce_sum_f32(const float* x, int64_t n, float* out, libreduce_stream_t str
  *         pointer), OVERFLOW (outer*reduce*inner overflows int64), ALIAS (out
  *         overlaps x), CUDA.
  */
-int reduce_axis_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
+LIBREDUCE_API int reduce_axis_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
                     libreduce_stream_t stream);
 
 /*
@@ -110,7 +117,7 @@ int reduce_axis_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner
  * Errors: INVALID_ARG, OVERFLOW (rows*N overflows int64, or a few-row scan
  *         larger than the look-back workspace holds), ALIAS, CUDA.
  */
-int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, float* y,
+LIBREDUCE_API int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, float* y,
                        libreduce_stream_t stream);
 
 /*
@@ -137,7 +144,7 @@ int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, float* y,
  * GPU (different streams, or other threads) race and must be avoided.
  * Errors: INVALID_ARG, OVERFLOW (n > 2^36), ALIAS (out inside x), CUDA.
  */
-int reduce_sum_f32_noalloc(const float* x, int64_t n, float* out, libreduce_stream_t stream);
+LIBREDUCE_API int reduce_sum_f32_noalloc(const float* x, int64_t n, float* out, libreduce_stream_t stream);
 
 /*
  * libreduce_check -- synchronise `stream`, then return and clear the current
@@ -145,21 +152,23 @@ int reduce_sum_f32_noalloc(const float* x, int64_t n, float* out, libreduce_stre
  * device-side wait ran out since the last check (the affected outputs are then
  * undefined), or LIBREDUCE_ERR_CUDA if the synchronisation itself failed.
  */
-int libreduce_check(libreduce_stream_t stream);
+LIBREDUCE_API int libreduce_check(libreduce_stream_t stream);
 
 /* Text for a status code (static storage, never NULL). */
-const char* libreduce_strerror(int status);
+LIBREDUCE_API const char* libreduce_strerror(int status);
 
 /* The cudaError_t of the last CUDA failure seen on this thread (0 if none). */
-int libreduce_last_cuda_error(void);
+LIBREDUCE_API int libreduce_last_cuda_error(void);
 
 /* Number of kernels this library has launched in this process (all devices). */
-int64_t libreduce_launch_count(void);
+LIBREDUCE_API int64_t libreduce_launch_count(void);
 
 /*
  * Process-wide dispatch options, for tests and benchmarks.  Not thread-safe
  * against concurrent calls; set them before queuing work.
- *   LIBREDUCE_OPT_SCAN_STRATEGY  0 auto, 1 one block per row, 2 look-back
+ *   LIBREDUCE_OPT_SCAN_STRATEGY  0 auto, 1 one block per row, 2 look-back (its fastest
+ *                                form), 3 look-back keeping each tile in registers between
+ *                                its read and its write (one HBM read, no L2 reread)
  *   LIBREDUCE_OPT_AXIS_SPLIT     0 auto, k > 0 forces k slices of the reduce axis
  *                                (inner > 1), or k chunks per row (inner == 1)
  *   LIBREDUCE_OPT_SPIN_LIMIT     0 default, else the look-back wait limit in polls
@@ -181,12 +190,15 @@ int64_t libreduce_launch_count(void);
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
  *                                 2 float4 x 4 (float4 needs N % 4 == 0, aligned x, y)
  *   LIBREDUCE_OPT_WAVES           1D sum: blocks = waves x resident blocks (0 = automatic:
- *                                 one wave, or more blocks of 64 Ki floats for long arrays) */
+ *                                 one wave, or more blocks of 64 Ki floats for long arrays)
+ *   LIBREDUCE_OPT_LOOKBACK_LAG    look-back scan: tiles between the read that publishes a
+ *                                 tile's sum and the reread that writes it (0 = automatic) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6
 #define LIBREDUCE_OPT_RSCAN_VARIANT 7
 #define LIBREDUCE_OPT_WAVES 8
-int libreduce_set_option(int option, int64_t value);
+#define LIBREDUCE_OPT_LOOKBACK_LAG 9
+LIBREDUCE_API int libreduce_set_option(int option, int64_t value);
 
 #ifdef __cplusplus
 }

@@ -42,7 +42,6 @@ struct DeviceState {
   float* partials = nullptr;
   // Look-back region (allocated by the first look-back scan on the device).
   unsigned long long* node_val = nullptr;
-  unsigned* node_arrive = nullptr;
   std::atomic<unsigned> epoch{0};
   int occ_lookback[kNumLookbackVariants] = {};
 };
@@ -58,6 +57,7 @@ std::atomic<int64_t> g_opt_contig_variant{-1};
 std::atomic<int64_t> g_opt_cols_variant{-1};
 std::atomic<int64_t> g_opt_rscan_variant{-1};
 std::atomic<int64_t> g_opt_waves{0};
+std::atomic<int64_t> g_opt_lookback_lag{0};
 thread_local int t_last_cuda_error = 0;
 
 int fail_cuda(cudaError_t e) {
@@ -119,7 +119,7 @@ int ensure_lookback(DeviceState* st) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (st->node_val) return LIBREDUCE_OK;
   const size_t nodes = 2 * (size_t)kMaxLookbackTiles;
-  const size_t bytes = nodes * (sizeof(unsigned long long) + sizeof(unsigned));
+  const size_t bytes = nodes * sizeof(unsigned long long);
   void* p = nullptr;
   cudaError_t e = cudaMalloc(&p, bytes);
   if (e != cudaSuccess) return fail_cuda(e);
@@ -130,8 +130,6 @@ int ensure_lookback(DeviceState* st) {
     return fail_cuda(e);
   }
   st->node_val = static_cast<unsigned long long*>(p);
-  st->node_arrive = reinterpret_cast<unsigned*>(static_cast<char*>(p) +
-                                                nodes * sizeof(unsigned long long));
   return LIBREDUCE_OK;
 }
 
@@ -311,7 +309,8 @@ int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int
   return launched(launch_reduce_cols(variant, p, grid, s));
 }
 
-constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with up to 1 us sleeps): about a second
+constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): well under a second
+constexpr int64_t kLookbackLag = 768;           // L2-lag form: 768 tiles (24 MiB) between touches
 
 int run_rscan_lookback(DeviceState* st, const float* x, int64_t rows, int64_t N, float* y,
                        cudaStream_t s, int variant) {
@@ -327,9 +326,13 @@ int run_rscan_lookback(DeviceState* st, const float* x, int64_t rows, int64_t N,
   cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return fail_cuda(e);
   const int64_t spin = g_opt_spin_limit.load();
-  RScanLookbackParams p{x, y, rows, N, tiles, st->node_val, st->node_arrive, counter, st->err_word,
-                        epoch, spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load()};
-  return launched(launch_rscan_lookback(variant, p, total, s));
+  const int64_t lag_opt = g_opt_lookback_lag.load();
+  const int64_t lag = variant == kLookbackL2 ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt : kLookbackLag)
+                                             : 0;
+  RScanLookbackParams p{x, y, rows, N, tiles, st->node_val, counter, st->err_word,
+                        epoch, spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag};
+  const int64_t grid = total + lag;  // one block per ticket
+  return launched(launch_rscan_lookback(variant, p, grid, s));
 }
 
 int run_rscan_rows(DeviceState* st, const float* x, int64_t rows, int64_t N, float* y,
@@ -343,11 +346,11 @@ int run_rscan_rows(DeviceState* st, const float* x, int64_t rows, int64_t N, flo
   // Few rows cannot fill the GPU one block per row: use the look-back scan,
   // which spreads every row's tiles over all SMs.
   const int64_t strategy = g_opt_scan_strategy.load();
-  const int lb_variant = vec4 ? kLookbackV4 : kLookbackV1;
+  const int lb_variant = !vec4 ? kLookbackV1 : (strategy == 3 ? kLookbackV4 : kLookbackL2);
   const int64_t lb_tiles = ceil_div(N, lookback_tile(lb_variant));
   const int64_t row_slots = (int64_t)st->sm_count * st->occ_rscan[variant];
   const bool lookback_fits = rows <= kMaxLookbackTiles / std::max<int64_t>(1, lb_tiles);
-  if (strategy == 2 || (strategy == 0 && rows < row_slots && lb_tiles >= 4 && lookback_fits))
+  if (strategy >= 2 || (strategy == 0 && 4 * rows < row_slots && lb_tiles >= 4 && lookback_fits))
     return run_rscan_lookback(st, x, rows, N, y, s, lb_variant);
   const int64_t grid = std::min<int64_t>(rows, INT32_MAX);
   RScanRowsParams p{x, y, rows, N};
@@ -471,7 +474,7 @@ int64_t libreduce_launch_count(void) { return g_launches.load(); }
 int libreduce_set_option(int option, int64_t value) {
   switch (option) {
     case LIBREDUCE_OPT_SCAN_STRATEGY:
-      if (value < 0 || value > 2) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < 0 || value > 3) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_strategy = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_AXIS_SPLIT:
@@ -497,6 +500,10 @@ int libreduce_set_option(int option, int64_t value) {
     case LIBREDUCE_OPT_RSCAN_VARIANT:
       if (value < -1 || value >= kNumRScanVariants) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_rscan_variant = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_LOOKBACK_LAG:
+      if (value < 0 || value > (1 << 20)) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_lookback_lag = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_WAVES:
       if (value < 0 || value > 64) return LIBREDUCE_ERR_INVALID_ARG;

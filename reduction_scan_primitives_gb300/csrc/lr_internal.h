@@ -61,9 +61,9 @@ struct RScanRowsParams {
 // --- Reverse cumulative sum, single-pass decoupled look-back ----------------
 // One block per tile.  Blocks take tickets in scan order (right to left within
 // a row, row after row): ticket t is tile k = t % tiles_per_row counted from
-// the right end of row t / tiles_per_row.  Dyadic block sums of tile
-// aggregates are published as 64-bit words {epoch, fp32 bits}; a word counts
-// only if its epoch equals this launch's, so the flags never need clearing.
+// the right end of row t / tiles_per_row.  Tile sums and 32-ary group sums are
+// published as 64-bit words {epoch, fp32 bits}; a word counts only if its
+// epoch equals this launch's, so the flags never need clearing.
 struct RScanLookbackParams {
   const float* x;
   float* y;
@@ -71,12 +71,12 @@ struct RScanLookbackParams {
   int64_t N;
   int64_t tiles_per_row;
   unsigned long long* node_val;  // rows * 2 * tiles_per_row words
-  unsigned* node_arrive;         // same shape (levels >= 1 used)
   unsigned* tile_counter;        // zero on entry
   unsigned* err_word;            // bit 0 set when a wait runs out
   unsigned epoch;                // nonzero, different for every launch on the device
   int64_t spin_limit;            // polls before a wait gives up
   int64_t stall_tile;            // test fault: this ticket never publishes (-1: none)
+  int64_t lag;                   // L2-lag form: tiles between a tile's two touches
 };
 
 // Variants are small integers chosen by the dispatcher; each launcher
@@ -92,7 +92,12 @@ enum ColsVariant {
   kNumColsVariants
 };
 enum RScanVariant { kRScanV1S4 = 0, kRScanV4S2 = 1, kRScanV4S4 = 2, kNumRScanVariants };
-enum LookbackVariant { kLookbackV1 = 0, kLookbackV4 = 1, kNumLookbackVariants };
+enum LookbackVariant {
+  kLookbackV1 = 0,  // scalar items, one tile per block, tile kept in registers
+  kLookbackV4 = 1,  // float4 items, one tile per block, tile kept in registers
+  kLookbackL2 = 2,  // float4 items, ticket t sums tile t and writes tile t - lag (L2 reread)
+  kNumLookbackVariants
+};
 
 // Elements per tile of each look-back variant.
 int64_t lookback_tile(int variant);

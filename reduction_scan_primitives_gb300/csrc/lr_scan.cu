@@ -64,24 +64,24 @@ __device__ __forceinline__ void store_tile(const float (&v)[SUB][VEC], float* yr
 }
 
 // Suffix scan of one tile held in registers (v[s][i]: element s*256*VEC +
-// t*VEC + i of the tile).  On return v holds each thread's local suffix, and
-// for each sub-tile s the caller adds
-//     exc[s] + (wexc[s] + (rs[s] + carry))
-// where exc is the suffix over lanes to the right, wexc over warps to the
-// right, rs over sub-tiles to the right, and carry over tiles to the right.
+// t*VEC + i of the tile).  On return v holds each thread's local suffix and
+// off[s] = exc + (wexc + rs), where exc is the suffix over lanes to the right,
+// wexc over warps to the right and rs over sub-tiles to the right inside the
+// tile; the caller adds off[s] + carry (carry: the tiles to the right).
 // `total` is the tile's sum (identical in every thread).  Contains one
 // __syncthreads(); `sh` must not be written again until every thread of the
 // block is past that barrier.
-template <int VEC, int SUB>
+template <int SUB>
 struct TileScan {
-  float exc[SUB], wexc[SUB], rs[SUB];
+  float off[SUB];
   float total;
 };
 
 template <int VEC, int SUB>
-__device__ __forceinline__ TileScan<VEC, SUB> tile_suffix(float (&v)[SUB][VEC],
-                                                         float (&sh)[SUB][kNW], int lane, int w) {
-  TileScan<VEC, SUB> r;
+__device__ __forceinline__ TileScan<SUB> tile_suffix(float (&v)[SUB][VEC], float (&sh)[SUB][kNW],
+                                                    int lane, int w) {
+  TileScan<SUB> r;
+  float exc[SUB];
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
     // 1. Suffix of each thread's VEC items, right to left.
@@ -95,38 +95,36 @@ __device__ __forceinline__ TileScan<VEC, SUB> tile_suffix(float (&v)[SUB][VEC],
       if (lane + o < 32) a += u;
     }
     const float e = __shfl_down_sync(kFullMask, a, 1);
-    r.exc[s] = (lane == 31) ? 0.f : e;
+    exc[s] = (lane == 31) ? 0.f : e;
     if (lane == 0) sh[s][w] = a;  // the warp's total
   }
   __syncthreads();
-  // 3. Warp totals -> exclusive suffix over warps, sub-tile totals.
-  float stot[SUB];
+  // 3. Warp totals -> exclusive suffix over warps and sub-tile totals;
+  // 4. sub-tiles to the right inside this tile.
+  float rs = 0.f;  // sum of the sub-tiles to the right of s
 #pragma unroll
-  for (int s = 0; s < SUB; ++s) {
+  for (int s = SUB - 1; s >= 0; --s) {
     float wt[kNW];
 #pragma unroll
     for (int q = 0; q < kNW; ++q) wt[q] = sh[s][q];
-    stot[s] = tree_sum<kNW>(wt);
-    float acc = 0.f;
+    float wexc = 0.f;
 #pragma unroll
     for (int q = kNW - 1; q >= 1; --q)
-      if (q > w) acc += wt[q];
-    r.wexc[s] = acc;
+      if (q > w) wexc += wt[q];
+    r.off[s] = exc[s] + (wexc + rs);
+    const float stot = tree_sum<kNW>(wt);
+    rs = (s == SUB - 1) ? stot : stot + rs;
   }
-  // 4. Sub-tiles to the right inside this tile.
-  r.rs[SUB - 1] = 0.f;
-#pragma unroll
-  for (int s = SUB - 2; s >= 0; --s) r.rs[s] = stot[s + 1] + r.rs[s + 1];
-  r.total = stot[0] + r.rs[0];
+  r.total = rs;
   return r;
 }
 
 template <int VEC, int SUB>
-__device__ __forceinline__ void add_offsets(float (&v)[SUB][VEC], const TileScan<VEC, SUB>& ts,
+__device__ __forceinline__ void add_offsets(float (&v)[SUB][VEC], const TileScan<SUB>& ts,
                                             float carry) {
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
-    const float off = ts.exc[s] + (ts.wexc[s] + (ts.rs[s] + carry));
+    const float off = ts.off[s] + carry;
 #pragma unroll
     for (int i = 0; i < VEC; ++i) v[s][i] += off;
   }
@@ -159,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) k_rscan_rows(RScanRowsParams p) {
     for (int64_t k = ntiles - 1; k >= 0; --k) {
       const int64_t base = k * TILE;
       if (k > 0) load_tile<VEC, SUB>(nxt, xr, base - TILE, N, t);  // prefetch the tile to the left
-      const TileScan<VEC, SUB> ts = tile_suffix<VEC, SUB>(cur, sh_w[par], lane, w);
+      const TileScan<SUB> ts = tile_suffix<VEC, SUB>(cur, sh_w[par], lane, w);
       add_offsets<VEC, SUB>(cur, ts, carry_hi + carry_lo);
       store_tile<VEC, SUB>(cur, yr, base, N, t);
       // Blocked carry: fold every kCarryFold tiles to keep chains short.
@@ -181,85 +179,77 @@ __global__ void __launch_bounds__(kThreads) k_rscan_rows(RScanRowsParams p) {
 // ---------------------------------------------------------------------------
 // Single-pass decoupled look-back, deterministic.
 //
-// Tiles of a row are numbered k = 0, 1, ... from the right end (scan order).
-// A(k) is tile k's sum.  B(l, j) = A(j*2^l) + ... + A((j+1)*2^l - 1) is a
-// dyadic block; B(0, k) = A(k), and B(l, j) = B(l-1, 2j) + B(l-1, 2j+1)
-// (lower index first) is formed by whichever of its two children is
-// published last, found with an exchange on an arrival word.  Tile k's
-// exclusive suffix (everything to its right) is the sum, over the set bits l
-// of k, of B(l, (k >> l) - 1): the binary decomposition of [0, k).  Which
-// block values exist when a tile looks back depends on timing, but every
-// value, and the way the tile combines them, does not, so the result is
-// bit-identical from run to run.
+// Tiles of a row are numbered k = 0, 1, ... from the right end (scan order),
+// A(k) is tile k's sum, and tiles are grouped 32-ary: node(0, m) = A(m) and
+// node(L+1, m) is the sum of node(L, 32m .. 32m+31), added with a fixed
+// pairwise tree (adjacent pairs first).  Writing k in base 32, the tiles to
+// the right of tile k are exactly, for every level L, the siblings that
+// precede k's level-L ancestor under the same parent, so
+//     E(k) = sum over L (from 0 up) of tree(node(L, first_L .. first_L + d_L - 1)),
+// d_L being k's base-32 digit L.  Warp L reads the d_L siblings of level L in
+// one round trip (all levels at once) and adds them with the same fixed tree,
+// so E(k) never depends on timing and reruns are bit-identical.
 //
-// Forward progress: tickets are taken in scan order, so a tile only waits
-// for tiles with smaller tickets, whose blocks are already running and never
-// wait on later tiles.  Every wait is bounded; when one runs out the block
-// records the failure (error word, plus this launch's epoch in the abort
-// word so the other waiters stop early) and finishes.
+// Publication needs no atomics: every tile publishes A(k); a tile whose level-L
+// ancestor is the last child of its parent (digits 0..L all 31) has read the
+// other 31 children, so it publishes the parent.  Values are 64-bit words
+// {epoch, fp32 bits} written and read with relaxed single-copy-atomic
+// accesses; a word counts only if its epoch is this launch's.
+//
+// Forward progress: tickets are taken in scan order and every node a tile
+// waits for is published by a tile with a smaller ticket, whose block is
+// already running and itself waits only on smaller tickets.  Every wait is
+// bounded; when one runs out the block records the failure (error word, plus
+// this launch's epoch in the abort word so the other waiters stop early) and
+// finishes.
 // ---------------------------------------------------------------------------
+constexpr int kMaxLevels = kNW;  // one warp per level: 32^8 tiles per row at most
+
 __device__ __forceinline__ unsigned long long pack_node(unsigned epoch, float v) {
   return ((unsigned long long)epoch << 32) | (unsigned long long)__float_as_uint(v);
-}
-
-__device__ __forceinline__ int64_t level_offset(int64_t tiles, int l) {
-  int64_t off = 0;
-  for (int q = 0; q < l; ++q) off += tiles >> q;
-  return off;
 }
 
 // Poll a node until it carries this launch's epoch (or give up).
 __device__ __forceinline__ float wait_node(const unsigned long long* node, unsigned epoch,
                                            int64_t limit, const unsigned* abort_word, bool* fail) {
-  unsigned ns = 32;
+  unsigned ns = 0;
   for (int64_t it = 0;; ++it) {
-    const unsigned long long word = ld_acquire_u64(node);
+    const unsigned long long word = ld_relaxed_u64(node);
     if ((unsigned)(word >> 32) == epoch) return __uint_as_float((unsigned)word);
     if (it >= limit || ld_relaxed_u32(abort_word) == epoch) {
       *fail = true;
       return 0.f;
     }
-    __nanosleep(ns);
-    if (ns < 1024) ns <<= 1;
+    if (it >= 64) {  // spin first, then back off gently
+      ns = ns ? (ns < 256 ? 2 * ns : ns) : 32;
+      __nanosleep(ns);
+    }
   }
 }
 
-// Publish A(k) and complete every dyadic block this tile is the last child of.
-__device__ void publish_up(unsigned long long* vals, unsigned* arrive, int64_t tiles, int64_t k,
-                           float a, unsigned epoch, int64_t limit, const unsigned* abort_word,
-                           bool* fail) {
-  float val = a;
-  int l = 0;
-  int64_t j = k;
-  int64_t off = 0;
-  st_release_u64(vals + j, pack_node(epoch, val));
-  while (true) {
-    const int64_t pj = j >> 1;
-    if (pj >= (tiles >> (l + 1))) break;  // the parent block runs past the row end
-    const int64_t next_off = off + (tiles >> l);
-    if (atom_exch_acq_rel(arrive + next_off + pj, epoch) != epoch) break;  // first child
-    const float sib = wait_node(vals + off + (j ^ 1), epoch, limit, abort_word, fail);
-    if (*fail) break;
-    val = (j & 1) ? (sib + val) : (val + sib);
-    ++l;
-    j = pj;
-    off = next_off;
-    st_release_u64(vals + off + j, pack_node(epoch, val));
-  }
+// Fixed pairwise tree over the 32 lanes (adjacent pairs first); lane 0 gets it.
+__device__ __forceinline__ float warp_tree_adjacent(float v) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) v += __shfl_down_sync(kFullMask, v, o);
+  return v;
 }
 
 template <int VEC, int SUB>
-__global__ void __launch_bounds__(kThreads) k_rscan_lookback(RScanLookbackParams p) {
+__global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
   __shared__ float sh_w[SUB][kNW];
+  __shared__ float s_part[kMaxLevels];
   __shared__ unsigned s_ticket;
-  __shared__ float s_excl;
+  __shared__ int s_fail;
   const int t = threadIdx.x;
   const int lane = t & 31;
   const int w = t >> 5;
   const unsigned* abort_word = p.err_word + 1;
 
-  if (t == 0) s_ticket = atomicAdd(p.tile_counter, 1u);
+  if (t == 0) {
+    s_ticket = atomicAdd(p.tile_counter, 1u);
+    s_fail = 0;
+  }
   __syncthreads();
   const int64_t ticket = s_ticket;
   const int64_t tiles = p.tiles_per_row;
@@ -268,40 +258,219 @@ __global__ void __launch_bounds__(kThreads) k_rscan_lookback(RScanLookbackParams
     return;
   }
   const int64_t row = ticket / tiles;
-  const int64_t k = ticket - row * tiles;    // from the right
+  const int64_t k = ticket - row * tiles;       // from the right
   const int64_t base = (tiles - 1 - k) * TILE;  // tiles are aligned at the row's left end
   const float* xr = p.x + row * p.N;
   float* yr = p.y + row * p.N;
+  unsigned long long* vals = p.node_val + row * 2 * tiles;
+  const bool stalled = ticket == p.stall_tile;
 
   float v[SUB][VEC];
   load_tile<VEC, SUB>(v, xr, base, p.N, t);
-  const TileScan<VEC, SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, lane, w);
+  const TileScan<SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, lane, w);
+  if (t == 0 && !stalled) st_relaxed_u64(vals + k, pack_node(p.epoch, ts.total));
 
-  if (w == 0) {
-    unsigned long long* vals = p.node_val + row * 2 * tiles;
-    unsigned* arrive = p.node_arrive + row * 2 * tiles;
-    bool fail = false;
-    if (lane == 0 && ticket != p.stall_tile)
-      publish_up(vals, arrive, tiles, k, ts.total, p.epoch, p.spin_limit, abort_word, &fail);
-    __syncwarp();
-    float e = 0.f;
-    if ((k >> lane) & 1) {
-      const int64_t j = (k >> lane) - 1;
-      e = wait_node(vals + level_offset(tiles, lane) + j, p.epoch, p.spin_limit, abort_word, &fail);
+  // Levels of this row: base-32 digits of the largest tile index.
+  int levels = 1;
+  while (levels < kMaxLevels && ((tiles - 1) >> (5 * levels)) != 0) ++levels;
+
+  // Warp L reads the level-L siblings that precede k's ancestor (all levels
+  // at once).  Warp 0 also publishes every parent this tile completes, right
+  // after the read of the level below it, so no publication waits on a level
+  // it does not need.
+  if (w < levels) {
+    int64_t off = 0, count = tiles;
+    for (int q = 0; q < w; ++q) {
+      off += count;
+      count >>= 5;
     }
-    e = warp_sum(e);  // fixed tree over the decomposition's blocks
-    const unsigned failed = __any_sync(kFullMask, fail);
-    if (lane == 0) {
-      s_excl = e;
-      if (failed) {
-        atomicOr(p.err_word, 1u);
-        atomicExch(p.err_word + 1, p.epoch);
+    int64_t m = k >> (5 * w);
+    int d = (int)(m & 31);
+    bool fail = false;
+    float sib = 0.f;
+    if (lane < d) sib = wait_node(vals + off + (m - d) + lane, p.epoch, p.spin_limit, abort_word, &fail);
+    const float part = warp_tree_adjacent(sib);
+    if (lane == 0) s_part[w] = part;
+    if (w == 0) {
+      float own = ts.total;
+      int L = 0;
+      while (d == 31 && !stalled && !__any_sync(kFullMask, fail)) {
+        const float parent = warp_tree_adjacent(lane < 31 ? sib : own);
+        own = __shfl_sync(kFullMask, parent, 0);
+        const int64_t next_off = off + count;
+        if (lane == 0) st_relaxed_u64(vals + next_off + (m >> 5), pack_node(p.epoch, own));
+        if (++L >= levels) break;
+        off = next_off;
+        count >>= 5;
+        m >>= 5;
+        d = (int)(m & 31);
+        if (d != 31) break;  // the next parent is not complete yet: someone else's job
+        sib = 0.f;
+        if (lane < 31) sib = wait_node(vals + off + (m - 31) + lane, p.epoch, p.spin_limit, abort_word, &fail);
       }
+    }
+    if (__any_sync(kFullMask, fail) && lane == 0) s_fail = 1;
+  }
+  __syncthreads();
+
+  if (t == 0) {
+    float excl = 0.f;
+    for (int L = 0; L < levels; ++L) excl += s_part[L];  // from the lowest level up
+    s_part[0] = excl;
+    if (s_fail) {
+      atomicOr(p.err_word, 1u);
+      atomicExch(p.err_word + 1, p.epoch);
     }
   }
   __syncthreads();
-  add_offsets<VEC, SUB>(v, ts, s_excl);
+  add_offsets<VEC, SUB>(v, ts, s_part[0]);
   store_tile<VEC, SUB>(v, yr, base, p.N, t);
+}
+
+// ---------------------------------------------------------------------------
+// Look-back with the two touches of each tile a fixed number of tickets apart.
+//
+// A block with ticket t (one block per ticket, tickets 0 .. tiles + lag - 1)
+//   1. starts a bulk copy (TMA engine) of tile t from HBM into shared memory;
+//   2. meanwhile writes out tile u = t - lag: looks back for u's exclusive
+//      suffix, which every tile to its right published about `lag` tickets
+//      ago, rereads u (read from HBM only about lag * 32 KiB ago, so normally
+//      served from L2), scans it and stores it;
+//   3. sums tile t from shared memory and publishes the sum, completing
+//      parents as the one-tile-per-block form does.
+// The look-back rarely waits, the HBM read of tile t overlaps step 2, and HBM
+// still sees each element read once and written once while the lag's tiles
+// stay in L2.  Every wait is on a smaller ticket, so forward progress holds as
+// in the other forms.
+// ---------------------------------------------------------------------------
+template <int SUB>
+__global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback_l2(RScanLookbackParams p) {
+  constexpr int64_t TILE = (int64_t)SUB * kThreads * 4;
+  __shared__ __align__(128) float s_tile[TILE];
+  __shared__ unsigned long long s_bar;
+  __shared__ float sh_w[SUB][kNW];
+  __shared__ float s_red[kNW];
+  __shared__ float s_part[kMaxLevels];
+  __shared__ unsigned s_ticket;
+  __shared__ int s_fail;
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int w = t >> 5;
+  const unsigned* abort_word = p.err_word + 1;
+  const int64_t tiles = p.tiles_per_row;
+  const int64_t total = p.rows * tiles;
+
+  if (t == 0) {
+    const unsigned tk = atomicAdd(p.tile_counter, 1u);
+    s_ticket = tk;
+    s_fail = 0;
+    if (tk < total) {
+      const int64_t row = tk / tiles;
+      const int64_t k = tk - row * tiles;
+      const int64_t base = (tiles - 1 - k) * TILE;
+      const int64_t len = min(TILE, p.N - base);
+      mbar_init(&s_bar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&s_bar, (unsigned)(len * 4));
+      bulk_load(s_tile, p.x + row * p.N + base, (unsigned)(len * 4), &s_bar);
+    }
+  }
+  __syncthreads();
+  const int64_t ticket = s_ticket;
+  if (ticket >= total + p.lag) {  // a stale counter: touch nothing
+    if (t == 0) atomicOr(p.err_word, 2u);
+    return;
+  }
+  int levels = 1;
+  while (levels < kMaxLevels && ((tiles - 1) >> (5 * levels)) != 0) ++levels;
+
+  // ---- write out tile `ticket - lag` ----
+  const int64_t u = ticket - p.lag;
+  if (u >= 0) {
+    const int64_t row = u / tiles;
+    const int64_t k = u - row * tiles;
+    const int64_t base = (tiles - 1 - k) * TILE;
+    float v[SUB][4];
+    load_tile<4, SUB>(v, p.x + row * p.N, base, p.N, t);  // in flight during the look-back
+    unsigned long long* vals = p.node_val + row * 2 * tiles;
+    if (w < levels) {
+      int64_t off = 0, count = tiles;
+      for (int q = 0; q < w; ++q) {
+        off += count;
+        count >>= 5;
+      }
+      const int64_t m = k >> (5 * w);
+      const int d = (int)(m & 31);
+      bool fail = false;
+      float sib = 0.f;
+      if (lane < d) sib = wait_node(vals + off + (m - d) + lane, p.epoch, p.spin_limit, abort_word, &fail);
+      const float part = warp_tree_adjacent(sib);
+      if (lane == 0) s_part[w] = part;
+      if (__any_sync(kFullMask, fail) && lane == 0) s_fail = 1;
+    }
+    const TileScan<SUB> ts = tile_suffix<4, SUB>(v, sh_w, lane, w);  // its barrier publishes s_part
+    float excl = 0.f;
+    for (int L = 0; L < levels; ++L) excl += s_part[L];  // from the lowest level up
+    add_offsets<4, SUB>(v, ts, excl);
+    store_tile<4, SUB>(v, p.y + row * p.N, base, p.N, t);
+  }
+
+  // ---- sum tile `ticket` (in shared memory) and publish it ----
+  if (ticket < total) {
+    const int64_t row = ticket / tiles;
+    const int64_t k = ticket - row * tiles;
+    const int64_t len = min(TILE, p.N - (tiles - 1 - k) * TILE);
+    bool loaded = true;
+    for (int64_t it = 0; !mbar_try_wait_parity(&s_bar, 0u); ++it)
+      if (it >= p.spin_limit) {
+        loaded = false;
+        break;
+      }
+    if (!loaded) s_fail = 1;
+    float e[SUB];
+#pragma unroll
+    for (int s = 0; s < SUB; ++s) {
+      const int64_t j = (int64_t)s * kThreads * 4 + (int64_t)t * 4;
+      float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < len) q = *reinterpret_cast<const float4*>(s_tile + j);
+      e[s] = (q.x + q.y) + (q.z + q.w);
+    }
+    const float a = block_sum<kThreads>(tree_sum<SUB>(e), s_red);  // thread 0
+    unsigned long long* vals = p.node_val + row * 2 * tiles;
+    const bool stalled = ticket == p.stall_tile;
+    if (w == 0 && !stalled) {
+      const float own0 = __shfl_sync(kFullMask, a, 0);
+      if (lane == 0) st_relaxed_u64(vals + k, pack_node(p.epoch, own0));
+      if ((k & 31) == 31) {  // publish every parent this tile completes
+        bool fail = false;
+        float own = own0;
+        int64_t off = 0, count = tiles, m = k;
+        for (int L = 0; L < levels && (m & 31) == 31; ++L) {
+          float sib = 0.f;
+          if (lane < 31) sib = wait_node(vals + off + (m - 31) + lane, p.epoch, p.spin_limit, abort_word, &fail);
+          if (__any_sync(kFullMask, fail)) break;
+          const float parent = warp_tree_adjacent(lane < 31 ? sib : own);
+          own = __shfl_sync(kFullMask, parent, 0);
+          const int64_t next_off = off + count;
+          if (lane == 0) st_relaxed_u64(vals + next_off + (m >> 5), pack_node(p.epoch, own));
+          off = next_off;
+          count >>= 5;
+          m >>= 5;
+        }
+        if (fail && lane == 0) s_fail = 1;
+      }
+    }
+    // A copy whose wait gave up may still be in flight: wait once more
+    // (bounded) before the block's shared memory is released.
+    if (!loaded && t == 0)
+      for (int64_t it = 0; !mbar_try_wait_parity(&s_bar, 0u) && it < p.spin_limit; ++it) {
+      }
+  }
+  __syncthreads();
+  if (t == 0 && s_fail) {
+    atomicOr(p.err_word, 1u);
+    atomicExch(p.err_word + 1, p.epoch);
+  }
 }
 
 template <typename K>
@@ -312,6 +481,15 @@ int occupancy_of(K kernel) {
 }
 
 }  // namespace
+
+int64_t lookback_tile(int variant) {
+  switch (variant) {
+    case kLookbackV1: return 8 * kThreads * 1;
+    case kLookbackV4:
+    case kLookbackL2: return 8 * kThreads * 4;
+    default: return 0;
+  }
+}
 
 cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
@@ -324,20 +502,13 @@ cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t gri
   return cudaGetLastError();
 }
 
-int64_t lookback_tile(int variant) {
-  switch (variant) {
-    case kLookbackV1: return 8 * kThreads * 1;
-    case kLookbackV4: return 8 * kThreads * 4;
-    default: return 0;
-  }
-}
-
 cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int64_t grid,
                                   cudaStream_t s) {
   const dim3 g((unsigned)grid);
   switch (variant) {
     case kLookbackV1: k_rscan_lookback<1, 8><<<g, kThreads, 0, s>>>(p); break;
     case kLookbackV4: k_rscan_lookback<4, 8><<<g, kThreads, 0, s>>>(p); break;
+    case kLookbackL2: k_rscan_lookback_l2<8><<<g, kThreads, 0, s>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -347,6 +518,7 @@ int occupancy_rscan_lookback(int variant) {
   switch (variant) {
     case kLookbackV1: return occupancy_of(k_rscan_lookback<1, 8>);
     case kLookbackV4: return occupancy_of(k_rscan_lookback<4, 8>);
+    case kLookbackL2: return occupancy_of(k_rscan_lookback_l2<8>);
     default: return 0;
   }
 }

@@ -32,6 +32,7 @@ OPT_CONTIG_VARIANT = 5
 OPT_COLS_VARIANT = 6
 OPT_RSCAN_VARIANT = 7
 OPT_WAVES = 8
+OPT_LOOKBACK_LAG = 9
 
 LIB_PATH = _build.LIB
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
@@ -59,8 +60,8 @@ def declared_functions() -> list[str]:
     with open(HEADER) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
-                      text, flags=re.M)
+    return re.findall(r"^\s*(?:LIBREDUCE_API\s+)?(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*"
+                      r"([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
 
 
 def load(path: str | None = None) -> ctypes.CDLL:

@@ -71,12 +71,27 @@ def test_deterministic_bitwise():
 
 
 def test_matches_block_per_row_path():
-    # Same data through both strategies: both within tolerance of the oracle.
+    # Same data through every strategy: all within tolerance of the oracle.
     x = inputs.make((4, 123_456), "uniform01", 9)
     ref, scale = oracle.reverse_cumsum(x.numpy(), 4, 123_456)
-    for strategy in (1, 2):
+    for strategy in (1, 2, 3):
         L.set_option(L.OPT_SCAN_STRATEGY, strategy)
         assert_close(run(x), ref, scale, f"strategy {strategy}")
+
+
+@pytest.mark.parametrize("lag", [1, 7, 64, 768, 5000])
+def test_lag_values(lag):
+    # Any lag gives a correct result (a small one only waits more, a large one
+    # rereads from HBM instead of L2).
+    L.set_option(L.OPT_LOOKBACK_LAG, lag)
+    check(2, 8192 * 300 + 4)
+
+
+@pytest.mark.parametrize("strategy", [2, 3])
+@pytest.mark.parametrize("n", [8192 * 6 * 152 + 8, 8192 * 40000])
+def test_long_rows_both_forms(n, strategy):
+    L.set_option(L.OPT_SCAN_STRATEGY, strategy)
+    check(1, n, force=False)
 
 
 def test_bounded_wait_reports_timeout():
@@ -87,10 +102,12 @@ def test_bounded_wait_reports_timeout():
     L.set_option(L.OPT_SCAN_STRATEGY, LOOKBACK)
     L.set_option(L.OPT_SPIN_LIMIT, 2000)
     L.set_option(L.OPT_STALL_TILE, 5)
-    L.reverse_cumsum_f32(x)
-    with pytest.raises(L.LibreduceError) as ei:
-        L.check()
-    assert ei.value.status == L.ERR_TIMEOUT
+    for strategy in (2, 3):  # L2-lag form and one tile per block
+        L.set_option(L.OPT_SCAN_STRATEGY, strategy)
+        L.reverse_cumsum_f32(x)
+        with pytest.raises(L.LibreduceError) as ei:
+            L.check()
+        assert ei.value.status == L.ERR_TIMEOUT
     L.set_option(L.OPT_STALL_TILE, -1)
     L.set_option(L.OPT_SPIN_LIMIT, 0)
     L.check()  # the error word was cleared
