@@ -223,10 +223,14 @@ int run_contig(DeviceState* st, const float* x, int64_t segments, int64_t seg_le
   if (forced > 0) {
     chunks = std::min<int64_t>(forced, ceil_div(seg_len, 4));
   } else if (segments == 1) {
-    // One long array: at least one full wave of blocks, and blocks of about
-    // kTargetChunk floats beyond that, so the blocks that finish first pick
-    // up more work instead of idling through a long tail.
-    chunks = waves > 0 ? waves * slots : std::max(slots, ceil_div(seg_len, kTargetChunk));
+    // One long array: a whole number of waves of resident blocks, each block
+    // about kTargetChunk floats.  A partial last wave would cost a whole
+    // block's duration for a few blocks (measured: 1526 blocks at 1e8 take 16%
+    // longer than 1520).
+    const int64_t w = waves > 0 ? waves
+                                : std::max<int64_t>(1, (seg_len + kTargetChunk * slots / 2) /
+                                                           (kTargetChunk * slots));
+    chunks = w * slots;
     chunks = std::min(chunks, std::max<int64_t>(1, seg_len / kMinChunk));
   } else if (segments < 4 * slots) {
     // Too few rows to fill the GPU: cut each into chunks.
@@ -322,9 +326,7 @@ int run_rscan_lookback(DeviceState* st, const float* x, int64_t rows, int64_t N,
   if (rc) return rc;
   unsigned epoch = st->epoch.fetch_add(1) + 1;
   if (epoch == 0) epoch = st->epoch.fetch_add(1) + 1;  // 0 marks "never written"
-  unsigned* counter = st->err_word + 2;
-  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned), s);
-  if (e != cudaSuccess) return fail_cuda(e);
+  unsigned* counter = st->err_word + 2;  // zero on entry; the block with the last ticket resets it
   const int64_t spin = g_opt_spin_limit.load();
   const int64_t lag_opt = g_opt_lookback_lag.load();
   const int64_t lag = variant == kLookbackL2 ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt : kLookbackLag)
@@ -449,7 +451,9 @@ int libreduce_check(libreduce_stream_t stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail_cuda(e);
   if (word == 0) return LIBREDUCE_OK;
-  e = cudaMemsetAsync(st->err_word, 0, sizeof(unsigned), s);
+  // Clear the error and abort words and the look-back ticket counter, which an
+  // interrupted launch may have left behind.
+  e = cudaMemsetAsync(st->err_word, 0, 3 * sizeof(unsigned), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail_cuda(e);
   return LIBREDUCE_ERR_TIMEOUT;

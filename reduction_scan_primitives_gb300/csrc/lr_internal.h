@@ -71,7 +71,7 @@ struct RScanLookbackParams {
   int64_t N;
   int64_t tiles_per_row;
   unsigned long long* node_val;  // rows * 2 * tiles_per_row words
-  unsigned* tile_counter;        // zero on entry
+  unsigned* tile_counter;        // zero on entry; reset by the block with the last ticket
   unsigned* err_word;            // bit 0 set when a wait runs out
   unsigned epoch;                // nonzero, different for every launch on the device
   int64_t spin_limit;            // polls before a wait gives up

@@ -247,8 +247,11 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
   const unsigned* abort_word = p.err_word + 1;
 
   if (t == 0) {
-    s_ticket = atomicAdd(p.tile_counter, 1u);
+    const unsigned tk = atomicAdd(p.tile_counter, 1u);
+    s_ticket = tk;
     s_fail = 0;
+    // Every other ticket is taken before the last one: reset for the next launch.
+    if ((int64_t)tk == p.rows * p.tiles_per_row - 1) atomicExch(p.tile_counter, 0u);
   }
   __syncthreads();
   const int64_t ticket = s_ticket;
@@ -364,6 +367,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback_l2(RScanLookback
     const unsigned tk = atomicAdd(p.tile_counter, 1u);
     s_ticket = tk;
     s_fail = 0;
+    // Every other ticket is taken before the last one: reset for the next launch.
+    if ((int64_t)tk == total + p.lag - 1) atomicExch(p.tile_counter, 0u);
     if (tk < total) {
       const int64_t row = tk / tiles;
       const int64_t k = tk - row * tiles;
