@@ -45,6 +45,8 @@ class Oracle:
         lib.oracle_reverse_cumsum.restype = None
         lib.oracle_axis_sum_at.argtypes = [_f32p, _i64, _i64, _i64, _i64p, _i64, _f64p, _f64p]
         lib.oracle_axis_sum_at.restype = None
+        lib.oracle_cumsum.argtypes = [_f32p, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _f64p, _f64p]
+        lib.oracle_cumsum.restype = None
         self._lib = lib
         self.path = lib_path
 
@@ -90,6 +92,18 @@ class Oracle:
         return y.reshape(rows, N), abs_y.reshape(rows, N)
 
 
+    def cumsum(self, x, outer, N, inner, reverse=False, exclusive=False):
+        """(y, abs_y), each fp64 [outer, N, inner]: cumulative sum along the middle
+        axis, forward (k <= j) or reverse (k >= j), inclusive or exclusive."""
+        x = _as_f32(x)
+        if x.size != outer * N * inner:
+            raise ValueError("size mismatch")
+        y = np.empty(outer * N * inner, np.float64)
+        abs_y = np.empty(outer * N * inner, np.float64)
+        self._lib.oracle_cumsum(x, outer, N, inner, int(bool(reverse)), int(bool(exclusive)), y, abs_y)
+        return y.reshape(outer, N, inner), abs_y.reshape(outer, N, inner)
+
+
 _default = None
 
 
@@ -115,6 +129,10 @@ def axis_sum_at(x, outer, reduce, inner, positions):
 
 def reverse_cumsum(x, rows, N):
     return default().reverse_cumsum(x, rows, N)
+
+
+def cumsum(x, outer, N, inner, reverse=False, exclusive=False):
+    return default().cumsum(x, outer, N, inner, reverse, exclusive)
 
 
 def tolerance(abs_scale):

@@ -36,3 +36,19 @@ def reverse_cumsum_exact(flat, rows, n):
             row.append(sum_exact(flat[i * n + k] for k in range(j, n)))
         out.append(row)
     return out
+
+
+def cumsum_exact(flat, outer, n, inner, reverse=False, exclusive=False):
+    """Exact y[o][j][i] = sum of x[o, k, i] over k <= j (forward) or k >= j
+    (reverse), with k == j left out when exclusive; one sum per output."""
+    out = []
+    for o in range(outer):
+        plane = []
+        for j in range(n):
+            if reverse:
+                ks = range(j + 1 if exclusive else j, n)
+            else:
+                ks = range(0, j if exclusive else j + 1)
+            plane.append([sum_exact(flat[(o * n + k) * inner + i] for k in ks) for i in range(inner)])
+        out.append(plane)
+    return out

@@ -13,6 +13,8 @@
  *   oracle_sum             s = sum_{i<n} x[i]                       (1D sum)
  *   oracle_axis_sum        out[o,i] = sum_r x[o,r,i], r ascending  (axis sum)
  *   oracle_reverse_cumsum  y[i,j] = sum_{k>=j} x[i,k]               (suffix sum)
+ *   oracle_cumsum          cumulative sum along the middle axis of [outer, N,
+ *                          inner], forward or reverse, inclusive or exclusive
  *
  * Each one also returns the companion sum of |x| over the same terms, which
  * is the scale of the per-element acceptance tolerance
@@ -26,7 +28,8 @@
  *     (opening problem statement).
  *   - POPCORNBENCH trace l1_p91 (reverse cumulative sum): y =
  *     cumsum(x.flip(1), 1).flip(1), i.e. y[i,j] = x[i,j] + ... + x[i,N-1]
- *     (opening problem statement).
+ *     (opening problem statement); the same trace works an exclusive
+ *     (forward) scan of 1..8 by hand, and discusses scanning other dims.
  *
  * Build with the host compiler and without -ffast-math, so the sequential
  * fp64 loops are not reassociated (oracle/build.py does this).
@@ -107,5 +110,39 @@ void oracle_axis_sum_at(const float* x, int64_t outer, int64_t reduce, int64_t i
     }
     out[k] = s;
     if (abs_out) abs_out[k] = a;
+  }
+}
+
+/* Cumulative sum along the middle axis of a contiguous [outer, N, inner]
+ * array, for every (o, i):
+ *   forward (reverse == 0):  y[o,j,i] = sum of x[o,k,i] over k <= j
+ *   reverse (reverse != 0):  y[o,j,i] = sum of x[o,k,i] over k >= j
+ * and with exclusive != 0 the element k == j itself is left out (k < j, or
+ * k > j).  Walk the axis in the scan direction with a running fp64 sum; an
+ * inclusive result is stored after adding x[o,j,i], an exclusive one before.
+ * abs_y (may be NULL) gets the running sum of |x| over the same terms. */
+void oracle_cumsum(const float* x, int64_t outer, int64_t N, int64_t inner, int reverse,
+                   int exclusive, double* y, double* abs_y) {
+  for (int64_t o = 0; o < outer; ++o) {
+    for (int64_t i = 0; i < inner; ++i) {
+      double acc = 0.0;
+      double acc_abs = 0.0;
+      for (int64_t step = 0; step < N; ++step) {
+        const int64_t j = reverse ? N - 1 - step : step;
+        const int64_t idx = (o * N + j) * inner + i;
+        const double v = (double)x[idx];
+        if (exclusive) {
+          y[idx] = acc;
+          if (abs_y) abs_y[idx] = acc_abs;
+          acc += v;
+          acc_abs += fabs(v);
+        } else {
+          acc += v;
+          acc_abs += fabs(v);
+          y[idx] = acc;
+          if (abs_y) abs_y[idx] = acc_abs;
+        }
+      }
+    }
   }
 }

@@ -197,6 +197,65 @@ def pin_scan_integers(orc):
     assert np.array_equal(ay, np.flip(np.cumsum(np.flip(np.abs(xi), 1), 1), 1).astype(np.float64))
 
 
+CUMSUM_SHAPES = [(1, 1, 1), (1, 8, 1), (2, 5, 3), (3, 4, 2), (1, 7, 4), (2, 1, 5), (4, 6, 1)]
+MODES = [(False, False), (False, True), (True, False), (True, True)]
+
+
+def pin_cumsum_bruteforce(orc):
+    """Forward / reverse, inclusive / exclusive cumulative sums along the middle
+    axis of [outer, N, inner] against exact rational sums, one per output,
+    written with their own index ranges (the POPCORNBENCH trace l1_p91
+    discusses the reverse scan along dim 1 and other dims)."""
+    rng = np.random.default_rng(21)
+    for (o, n, i) in CUMSUM_SHAPES:
+        x = _mixed_values(rng, o * n * i)
+        for rev, exc in MODES:
+            y, ay = orc.cumsum(x, o, n, i, rev, exc)
+            ex = brute.cumsum_exact(x.tolist(), o, n, i, rev, exc)
+            exa = brute.cumsum_exact([abs(v) for v in x.tolist()], o, n, i, rev, exc)
+            for a in range(o):
+                for j in range(n):
+                    for b in range(i):
+                        bound = n * U64 * float(exa[a][j][b]) + 1e-300
+                        assert abs(y[a, j, b] - float(ex[a][j][b])) <= bound, ((o, n, i), rev, exc, a, j, b)
+                        assert abs(ay[a, j, b] - float(exa[a][j][b])) <= bound
+
+
+def pin_cumsum_worked_examples(orc):
+    """The hand traces of the POPCORNBENCH trace l1_p91: reverse inclusive
+    [1..8] -> [36, ..., 8] and forward exclusive [1..8] -> [0, 1, 3, ..., 28]."""
+    with open(os.path.join(GOLDEN, "exclusive_scan_worked_example.json")) as f:
+        cases = json.load(f)["cases"]
+    with open(os.path.join(GOLDEN, "rcumsum_worked_examples.json")) as f:
+        cases += [dict(c, reverse=True, exclusive=False) for c in json.load(f)["cases"]]
+    for c in cases:
+        x = np.asarray(c["x"], dtype=np.float32)
+        y, _ = orc.cumsum(x, 1, x.size, 1, c["reverse"], c["exclusive"])
+        assert y.reshape(-1).tolist() == [float(v) for v in c["y"]], (c, y)
+
+
+def pin_cumsum_integers(orc):
+    """Exact on small integers against int64 cumsum written with numpy: forward
+    = cumsum, reverse = flip-cumsum-flip, exclusive = the inclusive result
+    shifted by one; the reverse inclusive case equals the reverse-cumsum
+    routine's result."""
+    x = _np(inputs.make((3, 50, 4), "int:-8:8", 6))
+    xi = x.astype(np.int64)
+    fwd = np.cumsum(xi, axis=1)
+    rev = np.flip(np.cumsum(np.flip(xi, 1), axis=1), 1)
+    zero = np.zeros((3, 1, 4), np.int64)
+    want = {(False, False): fwd, (True, False): rev,
+            (False, True): np.concatenate([zero, fwd[:, :-1]], axis=1),
+            (True, True): np.concatenate([rev[:, 1:], zero], axis=1)}
+    for (r, e), ref in want.items():
+        y, ay = orc.cumsum(x, 3, 50, 4, r, e)
+        assert np.array_equal(y, ref.astype(np.float64)), (r, e)
+    x2 = _np(inputs.make((5, 77), "int:0:3", 8))
+    y, _ = orc.cumsum(x2, 5, 77, 1, True, False)
+    assert np.array_equal(y[:, :, 0], orc.reverse_cumsum(x2, 5, 77)[0])
+
+
 ALL_PINS = [pin_sum_harmonic, pin_sum_constant, pin_sum_integers, pin_sum_bruteforce,
             pin_axis_bruteforce, pin_axis_integers_and_invariants, pin_scan_worked_examples,
-            pin_scan_bruteforce, pin_scan_integers]
+            pin_scan_bruteforce, pin_scan_integers, pin_cumsum_bruteforce, pin_cumsum_worked_examples,
+            pin_cumsum_integers]

@@ -28,6 +28,15 @@ MUTANTS = [
     ("scan_abs_wrong", "oracle_reverse_cumsum", "acc_abs += fabs(v);", "acc_abs += v;"),
     ("at_swapped_position", "oracle_axis_sum_at", "int64_t o = pos[k] / inner;",
      "int64_t o = pos[k] % inner;"),
+    ("cumsum_direction_ignored", "oracle_cumsum", "const int64_t j = reverse ? N - 1 - step : step;",
+     "const int64_t j = step;"),
+    ("cumsum_direction_swapped", "oracle_cumsum", "const int64_t j = reverse ? N - 1 - step : step;",
+     "const int64_t j = reverse ? step : N - 1 - step;"),
+    ("cumsum_exclusive_ignored", "oracle_cumsum", "if (exclusive) {", "if (0) {"),
+    ("cumsum_wrong_index", "oracle_cumsum", "const int64_t idx = (o * N + j) * inner + i;",
+     "const int64_t idx = (o * inner + i) * N + j;"),
+    ("cumsum_no_reset", "oracle_cumsum", "      double acc = 0.0;\n      double acc_abs = 0.0;\n      for (int64_t step",
+     "      double acc_abs = 0.0;\n      for (int64_t step"),
 ]
 
 
@@ -54,6 +63,9 @@ def test_pins_catch_mutant(tmp_path, name, func, old, new):
     mutated = _mutate(src, func, old, new)
     if name == "scan_no_row_reset":
         mutated = _hoist_acc(mutated)
+    if name == "cumsum_no_reset":
+        mutated = mutated.replace("                   int exclusive, double* y, double* abs_y) {\n",
+                                  "                   int exclusive, double* y, double* abs_y) {\n  double acc = 0.0;\n", 1)
     assert mutated != src
     csrc = tmp_path / "oracle_mutant.c"
     csrc.write_text(mutated)
