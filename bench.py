@@ -45,6 +45,8 @@ from reduction_scan_primitives_gb300 import inputs  # noqa: E402
 METRIC = "effective HBM GB/s and % of GB300 peak per reduce/scan config (1 GPU)"
 STEP_WORKLOADS = ["sum_1e9", "axis_128x4096x4095_d1", "axis_4096x65536_d1", "axis_65536x4096_d0",
                   "rcumsum_32768x32768", "rcumsum_1x1e9"]
+# Follow-on forms, timed separately from the step (reported under next_rows).
+NEXT_WORKLOADS = ["cumsum_fwd_32768x32768", "cumsum_fwd_excl_1x1e9", "cumsum_128x4096x4095_d1"]
 # Small cases of each kernel for ncu captures: larger than L2, a few GB at most.
 PROFILE_CASES = {
     "sum_2e8": dict(op="sum", shape=(200_000_000,), dist="uniform01", seed=42),
@@ -202,6 +204,8 @@ def make_call(name, x, out):
         return lambda: L.reduce_sum_f32(x, out=out)
     if w["op"] == "axis":
         return lambda: L.reduce_axis_f32(x, w["dim"], out=out)
+    if w["op"] == "cumsum":
+        return lambda: L.cumsum_f32(x, w["dim"], reverse=w["reverse"], exclusive=w["exclusive"], out=out)
     return lambda: L.reverse_cumsum_f32(x, out=out)
 
 
@@ -217,6 +221,35 @@ def alloc_workload(name, device):
     else:
         out = torch.empty_like(x)
     return x, out
+
+
+def time_next(device, reps=20):
+    """The follow-on forms, each timed alone (back-to-back launches, inputs
+    larger than L2)."""
+    from reduction_scan_primitives_gb300 import libreduce as L
+    peak, _ = hbm_peak()
+    res = {}
+    for name in NEXT_WORKLOADS:
+        x, out = alloc_workload(name, device)
+        call = make_call(name, x, out)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            call()
+            b.record()
+        torch.cuda.synchronize()
+        L.check(device)
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        nbytes = inputs.algorithmic_bytes(workload_spec(name))
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "bytes": nbytes}
+        del x, out
+    return res
 
 
 def time_sweep(device, reps=10):
@@ -356,6 +389,7 @@ def run_ours(args):
 
     e2e = run_e2e(args, data, nbytes, device, world) if not args.no_e2e else None
     sweep = time_sweep(device) if (rank == 0 and not args.no_sweep) else None
+    nxt = time_next(device) if (rank == 0 and not args.no_next) else None
     cpu = cpu_baseline(data) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     if rank == 0:
@@ -368,7 +402,7 @@ def run_ours(args):
                        "step_bytes": step_bytes, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (each >= 1 GiB); sweep flushes L2"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clocks.summary(), "per_config": per, "sum_sweep": sweep,
+            "clocks": clocks.summary(), "per_config": per, "sum_sweep": sweep, "next_rows": nxt,
             "pages_context_t4": PAGES_T4,
         }
         print(json.dumps(line), flush=True)
@@ -506,6 +540,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the follow-on forms")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES))
     args = ap.parse_args(argv)
     if args.profile_case:

@@ -121,6 +121,31 @@ LIBREDUCE_API int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, fl
                        libreduce_stream_t stream);
 
 /*
+ * cumsum_f32 -- cumulative sum along the middle axis of a contiguous
+ * [outer, N, inner] array, for every (o, i):
+ *   forward (default):              y[o,j,i] = sum_{k <= j} x[o,k,i]
+ *   LIBREDUCE_SCAN_REVERSE:         y[o,j,i] = sum_{k >= j} x[o,k,i]
+ *   with LIBREDUCE_SCAN_EXCLUSIVE:  the term k == j is left out (k < j, k > j)
+ *
+ * The generalisation the POPCORNBENCH trace l1_p91 discusses (other scan
+ * directions and dims); reverse_cumsum_f32(x, rows, N, y, s) is
+ * cumsum_f32(x, rows, N, 1, y, LIBREDUCE_SCAN_REVERSE, s).  inner == 1 scans
+ * rows with the row kernels (a forward scan runs as a reverse scan of the
+ * mirrored row); inner > 1 scans columns, coalesced across inner.  Every
+ * output is built from additions over its own terms only (no subtraction),
+ * and an exclusive output with no terms is +0.0f.
+ *   x     device, outer*N*inner floats
+ *   y     device, outer*N*inner floats; must not overlap x
+ *   flags LIBREDUCE_SCAN_REVERSE | LIBREDUCE_SCAN_EXCLUSIVE (other bits: INVALID_ARG)
+ *   Any zero extent is a no-op.
+ * Errors: as reverse_cumsum_f32.
+ */
+#define LIBREDUCE_SCAN_REVERSE 1u
+#define LIBREDUCE_SCAN_EXCLUSIVE 2u
+LIBREDUCE_API int cumsum_f32(const float* x, int64_t outer, int64_t N, int64_t inner, float* y,
+                             unsigned flags, libreduce_stream_t stream);
+
+/*
  * reduce_sum_f32_noalloc -- out[0] = sum_{i<n} x[i], allocating nothing.
  *
  * The pages have no counterpart to this call; it exists for callers that

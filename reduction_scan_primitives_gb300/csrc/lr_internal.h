@@ -50,12 +50,30 @@ struct ColsParams {
   unsigned* tickets;  // outer * col_tiles, zero on entry, left zero on exit
 };
 
-// --- Reverse cumulative sum, one block per row ------------------------------
+// --- Scan flags (internal) ---------------------------------------------------
+// The row kernels compute a reverse (suffix) scan; a forward scan is the
+// reverse scan of the mirrored row (kScanMirror), and an exclusive scan leaves
+// out each element's own term (kScanExclusive).
+constexpr int kScanMirror = 1;
+constexpr int kScanExclusive = 2;
+
+// --- Cumulative sum along rows, one block per row ----------------------------
 struct RScanRowsParams {
   const float* x;
   float* y;
   int64_t rows;
   int64_t N;
+  int flags;
+};
+
+// --- Cumulative sum along a strided axis (inner > 1) -------------------------
+// x, y: [outer, N, inner]; one thread per (o, group of VEC columns).
+struct ScanColsParams {
+  const float* x;
+  float* y;
+  int64_t outer, N, inner;
+  int reverse;
+  int exclusive;
 };
 
 // --- Reverse cumulative sum, single-pass decoupled look-back ----------------
@@ -77,6 +95,7 @@ struct RScanLookbackParams {
   int64_t spin_limit;            // polls before a wait gives up
   int64_t stall_tile;            // test fault: this ticket never publishes (-1: none)
   int64_t lag;                   // L2-lag form: tiles between a tile's two touches
+  int flags;                     // kScanMirror | kScanExclusive
 };
 
 // Variants are small integers chosen by the dispatcher; each launcher
@@ -99,6 +118,8 @@ enum LookbackVariant {
   kNumLookbackVariants
 };
 
+enum ScanColsVariant { kScanColsV1 = 0, kScanColsV4 = 1, kNumScanColsVariants };
+
 // Elements per tile of each look-back variant.
 int64_t lookback_tile(int variant);
 
@@ -111,6 +132,7 @@ cudaError_t launch_reduce_cols(int variant, const ColsParams& p, int64_t grid, c
 cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int64_t grid,
                                   cudaStream_t s);
+cudaError_t launch_scan_cols(int variant, const ScanColsParams& p, int64_t grid, cudaStream_t s);
 
 // Host helpers defined in lr_api.cu, for entry points in other files.
 int check_device_buffer(const void* p, size_t bytes, int dev);  // a libreduce status
@@ -123,5 +145,6 @@ int occupancy_reduce_rows_warp();
 int occupancy_reduce_cols(int variant);
 int occupancy_rscan_rows(int variant);
 int occupancy_rscan_lookback(int variant);
+int occupancy_scan_cols(int variant);
 
 }  // namespace lr

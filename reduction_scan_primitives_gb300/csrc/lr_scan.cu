@@ -27,37 +27,51 @@ namespace {
 constexpr int kNW = kThreads / 32;
 constexpr int kCarryFold = 32;  // tiles per fold of the blocked carry
 
+// Tile loads and stores.  Element j of the logical row is physical element j,
+// or N - 1 - j when `mirror` is set (a forward scan run as a reverse scan of
+// the mirrored row); with float4 items the four components are then taken in
+// reverse order.
 template <int VEC, int SUB>
 __device__ __forceinline__ void load_tile(float (&v)[SUB][VEC], const float* xr, int64_t base,
-                                          int64_t N, int t) {
+                                          int64_t N, int t, bool mirror) {
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
     const int64_t j = base + (int64_t)s * kThreads * VEC + (int64_t)t * VEC;
     if constexpr (VEC == 4) {
       // N % 4 == 0 on this path, so j < N means all four are in range.
       float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (j < N) q = ld_stream4(xr + j);
-      v[s][0] = q.x;
-      v[s][1] = q.y;
-      v[s][2] = q.z;
-      v[s][3] = q.w;
+      if (j < N) q = ld_stream4(xr + (mirror ? N - 4 - j : j));
+      if (mirror) {
+        v[s][0] = q.w;
+        v[s][1] = q.z;
+        v[s][2] = q.y;
+        v[s][3] = q.x;
+      } else {
+        v[s][0] = q.x;
+        v[s][1] = q.y;
+        v[s][2] = q.z;
+        v[s][3] = q.w;
+      }
     } else {
-      v[s][0] = (j < N) ? ld_stream1(xr + j) : 0.f;
+      v[s][0] = (j < N) ? ld_stream1(xr + (mirror ? N - 1 - j : j)) : 0.f;
     }
   }
 }
 
 template <int VEC, int SUB>
 __device__ __forceinline__ void store_tile(const float (&v)[SUB][VEC], float* yr, int64_t base,
-                                           int64_t N, int t) {
+                                           int64_t N, int t, bool mirror) {
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
     const int64_t j = base + (int64_t)s * kThreads * VEC + (int64_t)t * VEC;
     if (j < N) {
       if constexpr (VEC == 4) {
-        st_stream4(yr + j, make_float4(v[s][0], v[s][1], v[s][2], v[s][3]));
+        if (mirror)
+          st_stream4(yr + (N - 4 - j), make_float4(v[s][3], v[s][2], v[s][1], v[s][0]));
+        else
+          st_stream4(yr + j, make_float4(v[s][0], v[s][1], v[s][2], v[s][3]));
       } else {
-        st_stream1(yr + j, v[s][0]);
+        st_stream1(yr + (mirror ? N - 1 - j : j), v[s][0]);
       }
     }
   }
@@ -119,14 +133,24 @@ __device__ __forceinline__ TileScan<SUB> tile_suffix(float (&v)[SUB][VEC], float
   return r;
 }
 
+// Turn the local suffixes into outputs: add each sub-tile's offset and the
+// carry.  Inclusive: item i gets its own local suffix.  Exclusive: item i gets
+// the local suffix of the item to its right (none for the thread's last
+// item), so no output ever subtracts its own term.
 template <int VEC, int SUB>
-__device__ __forceinline__ void add_offsets(float (&v)[SUB][VEC], const TileScan<SUB>& ts,
-                                            float carry) {
+__device__ __forceinline__ void finalize(float (&v)[SUB][VEC], const TileScan<SUB>& ts, float carry,
+                                         bool exclusive) {
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
     const float off = ts.off[s] + carry;
+    if (exclusive) {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) v[s][i] += off;
+      for (int i = 0; i + 1 < VEC; ++i) v[s][i] = v[s][i + 1] + off;
+      v[s][VEC - 1] = off;
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) v[s][i] += off;
+    }
   }
 }
 
@@ -143,6 +167,8 @@ __global__ void __launch_bounds__(kThreads) k_rscan_rows(RScanRowsParams p) {
   const int w = t >> 5;
   const int64_t N = p.N;
   const int64_t ntiles = (N + TILE - 1) / TILE;
+  const bool mirror = (p.flags & kScanMirror) != 0;
+  const bool exclusive = (p.flags & kScanExclusive) != 0;
   int par = 0;
 
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
@@ -150,16 +176,16 @@ __global__ void __launch_bounds__(kThreads) k_rscan_rows(RScanRowsParams p) {
     float* yr = p.y + row * N;
     float cur[SUB][VEC];
     float nxt[SUB][VEC];
-    load_tile<VEC, SUB>(cur, xr, (ntiles - 1) * TILE, N, t);
+    load_tile<VEC, SUB>(cur, xr, (ntiles - 1) * TILE, N, t, mirror);
     float carry_lo = 0.f, carry_hi = 0.f;
     int ncarry = 0;
 
     for (int64_t k = ntiles - 1; k >= 0; --k) {
       const int64_t base = k * TILE;
-      if (k > 0) load_tile<VEC, SUB>(nxt, xr, base - TILE, N, t);  // prefetch the tile to the left
+      if (k > 0) load_tile<VEC, SUB>(nxt, xr, base - TILE, N, t, mirror);  // prefetch the next tile
       const TileScan<SUB> ts = tile_suffix<VEC, SUB>(cur, sh_w[par], lane, w);
-      add_offsets<VEC, SUB>(cur, ts, carry_hi + carry_lo);
-      store_tile<VEC, SUB>(cur, yr, base, N, t);
+      finalize<VEC, SUB>(cur, ts, carry_hi + carry_lo, exclusive);
+      store_tile<VEC, SUB>(cur, yr, base, N, t, mirror);
       // Blocked carry: fold every kCarryFold tiles to keep chains short.
       carry_lo += ts.total;
       if (++ncarry == kCarryFold) {
@@ -268,8 +294,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
   unsigned long long* vals = p.node_val + row * 2 * tiles;
   const bool stalled = ticket == p.stall_tile;
 
+  const bool mirror = (p.flags & kScanMirror) != 0;
   float v[SUB][VEC];
-  load_tile<VEC, SUB>(v, xr, base, p.N, t);
+  load_tile<VEC, SUB>(v, xr, base, p.N, t, mirror);
   const TileScan<SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, lane, w);
   if (t == 0 && !stalled) st_relaxed_u64(vals + k, pack_node(p.epoch, ts.total));
 
@@ -326,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
     }
   }
   __syncthreads();
-  add_offsets<VEC, SUB>(v, ts, s_part[0]);
-  store_tile<VEC, SUB>(v, yr, base, p.N, t);
+  finalize<VEC, SUB>(v, ts, s_part[0], (p.flags & kScanExclusive) != 0);
+  store_tile<VEC, SUB>(v, yr, base, p.N, t, mirror);
 }
 
 // ---------------------------------------------------------------------------
@@ -374,10 +401,12 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback_l2(RScanLookback
       const int64_t k = tk - row * tiles;
       const int64_t base = (tiles - 1 - k) * TILE;
       const int64_t len = min(TILE, p.N - base);
+      // The tile's elements in memory (mirrored rows hold them at the other end).
+      const int64_t phys = (p.flags & kScanMirror) ? p.N - base - len : base;
       mbar_init(&s_bar, 1);
       fence_mbar_init();
       mbar_arrive_expect_tx(&s_bar, (unsigned)(len * 4));
-      bulk_load(s_tile, p.x + row * p.N + base, (unsigned)(len * 4), &s_bar);
+      bulk_load(s_tile, p.x + row * p.N + phys, (unsigned)(len * 4), &s_bar);
     }
   }
   __syncthreads();
@@ -395,8 +424,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback_l2(RScanLookback
     const int64_t row = u / tiles;
     const int64_t k = u - row * tiles;
     const int64_t base = (tiles - 1 - k) * TILE;
+    const bool mirror = (p.flags & kScanMirror) != 0;
     float v[SUB][4];
-    load_tile<4, SUB>(v, p.x + row * p.N, base, p.N, t);  // in flight during the look-back
+    load_tile<4, SUB>(v, p.x + row * p.N, base, p.N, t, mirror);  // in flight during the look-back
     unsigned long long* vals = p.node_val + row * 2 * tiles;
     if (w < levels) {
       int64_t off = 0, count = tiles;
@@ -416,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback_l2(RScanLookback
     const TileScan<SUB> ts = tile_suffix<4, SUB>(v, sh_w, lane, w);  // its barrier publishes s_part
     float excl = 0.f;
     for (int L = 0; L < levels; ++L) excl += s_part[L];  // from the lowest level up
-    add_offsets<4, SUB>(v, ts, excl);
-    store_tile<4, SUB>(v, p.y + row * p.N, base, p.N, t);
+    finalize<4, SUB>(v, ts, excl, (p.flags & kScanExclusive) != 0);
+    store_tile<4, SUB>(v, p.y + row * p.N, base, p.N, t, mirror);
   }
 
   // ---- sum tile `ticket` (in shared memory) and publish it ----
@@ -478,6 +508,109 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback_l2(RScanLookback
   }
 }
 
+// ---------------------------------------------------------------------------
+// Cumulative sum along a strided axis: x, y are [outer, N, inner] with
+// inner > 1 (the POPCORNBENCH trace l1_p91 discusses scanning dims other than
+// the last).  One thread per (o, VEC adjacent columns), so a warp's loads and
+// stores cover 32*VEC consecutive floats of one row; it walks the axis in the
+// scan direction with U rows in flight.  The running sum is blocked: a chunk
+// of up to 64 terms, folded into three more levels every 32 folds, and each
+// output is carry + chunk sum, so no addition chain grows with N (up to
+// 64*32*32*32 rows per chunk level) and no output subtracts anything.
+// ---------------------------------------------------------------------------
+template <int VEC>
+struct RunningSum {
+  float l0[VEC], l1[VEC], l2[VEC], l3[VEC], carry[VEC];
+  int n0 = 0, n1 = 0, n2 = 0;
+  __device__ __forceinline__ RunningSum() {
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) l0[c] = l1[c] = l2[c] = l3[c] = carry[c] = 0.f;
+  }
+  __device__ __forceinline__ void fold() {
+    if (++n0 < 64) return;
+    n0 = 0;
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      l1[c] += l0[c];
+      l0[c] = 0.f;
+    }
+    if (++n1 == 32) {
+      n1 = 0;
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        l2[c] += l1[c];
+        l1[c] = 0.f;
+      }
+      if (++n2 == 32) {
+        n2 = 0;
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          l3[c] += l2[c];
+          l2[c] = 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) carry[c] = (l3[c] + l2[c]) + l1[c];
+  }
+};
+
+template <int VEC, int U>
+__global__ void __launch_bounds__(kThreads) k_scan_cols(ScanColsParams p) {
+  const int64_t groups = (p.inner + VEC - 1) / VEC;
+  const int64_t total = p.outer * groups;
+  for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * kThreads) {
+    const int64_t o = g / groups;
+    const int64_t c0 = (g - o * groups) * VEC;
+    const float* xc = p.x + o * p.N * p.inner + c0;
+    float* yc = p.y + o * p.N * p.inner + c0;
+    RunningSum<VEC> rs;
+    for (int64_t step = 0; step < p.N; step += U) {
+      float q[U][VEC];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t s = step + u;
+        const int64_t j = p.reverse ? p.N - 1 - s : s;
+        if (s < p.N) {
+          if constexpr (VEC == 4) {
+            const float4 f = ld_stream4(xc + j * p.inner);
+            q[u][0] = f.x;
+            q[u][1] = f.y;
+            q[u][2] = f.z;
+            q[u][3] = f.w;
+          } else {
+            q[u][0] = ld_stream1(xc + j * p.inner);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t s = step + u;
+        if (s >= p.N) break;
+        const int64_t j = p.reverse ? p.N - 1 - s : s;
+        float out[VEC];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          if (p.exclusive) {
+            out[c] = rs.carry[c] + rs.l0[c];
+            rs.l0[c] += q[u][c];
+          } else {
+            rs.l0[c] += q[u][c];
+            out[c] = rs.carry[c] + rs.l0[c];
+          }
+        }
+        rs.fold();
+        if constexpr (VEC == 4) {
+          st_stream4(yc + j * p.inner, make_float4(out[0], out[1], out[2], out[3]));
+        } else {
+          st_stream1(yc + j * p.inner, out[0]);
+        }
+      }
+    }
+  }
+}
+
 template <typename K>
 int occupancy_of(K kernel) {
   int n = 0;
@@ -524,6 +657,24 @@ int occupancy_rscan_lookback(int variant) {
     case kLookbackV1: return occupancy_of(k_rscan_lookback<1, 8>);
     case kLookbackV4: return occupancy_of(k_rscan_lookback<4, 8>);
     case kLookbackL2: return occupancy_of(k_rscan_lookback_l2<8>);
+    default: return 0;
+  }
+}
+
+cudaError_t launch_scan_cols(int variant, const ScanColsParams& p, int64_t grid, cudaStream_t s) {
+  const dim3 g((unsigned)grid);
+  switch (variant) {
+    case kScanColsV1: k_scan_cols<1, 8><<<g, kThreads, 0, s>>>(p); break;
+    case kScanColsV4: k_scan_cols<4, 8><<<g, kThreads, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+int occupancy_scan_cols(int variant) {
+  switch (variant) {
+    case kScanColsV1: return occupancy_of(k_scan_cols<1, 8>);
+    case kScanColsV4: return occupancy_of(k_scan_cols<4, 8>);
     default: return 0;
   }
 }

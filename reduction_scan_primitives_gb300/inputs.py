@@ -58,9 +58,9 @@ def make(shape, dist: str, seed: int = 0, device="cpu") -> torch.Tensor:
     raise ValueError(f"unknown distribution {dist!r}")
 
 
-# The five workloads, by what they are.  ``op`` names the primitive; ``view``
-# gives its arguments; ``bytes`` is the algorithmic traffic (every input read
-# once, every output written once).
+# The workloads, by what they are.  ``op`` names the primitive, the other
+# keys its arguments; algorithmic_bytes() gives the traffic it must move
+# (every input read once, every output written once).
 WORKLOADS = {
     "sum_1e6_harmonic": dict(op="sum", shape=(1_000_000,), dist="harmonic", seed=0),
     "sum_1e6_pm1": dict(op="sum", shape=(1_000_000,), dist="uniform_pm1", seed=42),
@@ -71,6 +71,13 @@ WORKLOADS = {
     "rcumsum_32768x32768": dict(op="rcumsum", shape=(32768, 32768), dist="uniform01", seed=3),
     # Few long rows (the look-back scan): one row of 1e9.
     "rcumsum_1x1e9": dict(op="rcumsum", shape=(1, 1_000_000_000), dist="uniform01", seed=3),
+    # Other scan forms: forward, exclusive, along a non-last axis.
+    "cumsum_fwd_32768x32768": dict(op="cumsum", shape=(32768, 32768), dim=1, reverse=False,
+                                   exclusive=False, dist="uniform01", seed=3),
+    "cumsum_fwd_excl_1x1e9": dict(op="cumsum", shape=(1, 1_000_000_000), dim=1, reverse=False,
+                                  exclusive=True, dist="uniform01", seed=3),
+    "cumsum_128x4096x4095_d1": dict(op="cumsum", shape=(128, 4096, 4095), dim=1, reverse=False,
+                                    exclusive=False, dist="normal", seed=7),
 }
 
 # The 1D sweep sizes of the sum benchmark (uniform[0,1), seed 42).
@@ -94,6 +101,6 @@ def algorithmic_bytes(w: dict) -> int:
     if w["op"] == "axis":
         outer, _, inner = canonical_axis(w["shape"], w["dim"])
         return 4 * n + 4 * outer * inner
-    if w["op"] == "rcumsum":
+    if w["op"] in ("rcumsum", "cumsum"):
         return 8 * n
     raise ValueError(w["op"])

@@ -24,6 +24,9 @@ ERR_ALIAS = 3
 ERR_CUDA = 4
 ERR_TIMEOUT = 5
 
+SCAN_REVERSE = 1
+SCAN_EXCLUSIVE = 2
+
 OPT_SCAN_STRATEGY = 1
 OPT_AXIS_SPLIT = 2
 OPT_SPIN_LIMIT = 3
@@ -83,6 +86,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.reduce_axis_f32.restype = i32
     lib.reverse_cumsum_f32.argtypes = [vp, i64, i64, vp, vp]
     lib.reverse_cumsum_f32.restype = i32
+    lib.cumsum_f32.argtypes = [vp, i64, i64, i64, vp, ctypes.c_uint, vp]
+    lib.cumsum_f32.restype = i32
     lib.libreduce_check.argtypes = [vp]
     lib.libreduce_check.restype = i32
     lib.libreduce_strerror.argtypes = [i32]
@@ -197,6 +202,28 @@ def reverse_cumsum_f32(x: torch.Tensor, out: torch.Tensor | None = None) -> torc
     return out
 
 
+def cumsum_f32(x: torch.Tensor, dim: int = -1, reverse: bool = False, exclusive: bool = False,
+               out: torch.Tensor | None = None) -> torch.Tensor:
+    """Cumulative sum of x along `dim` (float32 CUDA, contiguous): forward
+    (sum over k <= j) or reverse (k >= j), inclusive or exclusive (k != j)."""
+    _check_tensor(x, "x")
+    if x.dim() == 0:
+        raise ValueError("x must have at least one dim")
+    outer, N, inner = canonical_axis(x.shape, dim)
+    if out is None:
+        out = torch.empty_like(x)
+    else:
+        _check_tensor(out, "out")
+        if out.shape != x.shape or out.device != x.device:
+            raise ValueError("out must have x's shape and device")
+    flags = (SCAN_REVERSE if reverse else 0) | (SCAN_EXCLUSIVE if exclusive else 0)
+    lib = load()
+    with torch.cuda.device(x.device):
+        st = lib.cumsum_f32(x.data_ptr(), outer, N, inner, out.data_ptr(), flags, _stream_ptr(x.device))
+    _raise_on("cumsum_f32", st)
+    return out
+
+
 def check(device=None) -> None:
     """Synchronise the current stream and raise if a device-side wait ran out."""
     lib = load()
@@ -218,3 +245,4 @@ def launch_count() -> int:
 reduce_sum = reduce_sum_f32
 reduce_axis = reduce_axis_f32
 reverse_cumsum = reverse_cumsum_f32
+cumsum = cumsum_f32

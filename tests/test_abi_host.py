@@ -60,6 +60,17 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.reverse_cumsum_f32(FAKE, 1, 4, NULL, NULL) == E
 
 
+def test_cumsum_arguments(lib):
+    E = L.ERR_INVALID_ARG
+    assert lib.cumsum_f32(FAKE, 1, 4, 1, FAKE + 4096, 4, NULL) == E  # unknown flag bit
+    assert lib.cumsum_f32(FAKE, -1, 4, 1, FAKE + 4096, 0, NULL) == E
+    assert lib.cumsum_f32(FAKE, 1, 4, -2, FAKE + 4096, 0, NULL) == E
+    assert lib.cumsum_f32(NULL, 1, 4, 2, FAKE + 4096, 0, NULL) == E
+    assert lib.cumsum_f32(FAKE, 2, 4, 3, FAKE + 40, 1, NULL) == L.ERR_ALIAS
+    assert lib.cumsum_f32(FAKE, 1 << 62, 4, 1 << 62, FAKE, 0, NULL) == L.ERR_OVERFLOW
+    assert lib.cumsum_f32(FAKE, 3, 0, 5, FAKE, 3, NULL) == L.OK  # empty: no-op
+
+
 def test_overflow_rejected(lib):
     big = 1 << 62
     assert lib.reduce_axis_f32(FAKE, big, big, 2, FAKE, NULL) == L.ERR_OVERFLOW

@@ -1,0 +1,114 @@
+"""cumsum_f32 (forward / reverse, inclusive / exclusive, any axis) against the
+oracle (GPU)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import libreduce_defaults, on_device  # noqa: F401
+from parity import assert_close, assert_exact, bitwise_equal
+from reduction_scan_primitives_gb300 import inputs
+from reduction_scan_primitives_gb300 import libreduce as L
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+MODES = [(False, False), (False, True), (True, False), (True, True)]
+MODE_IDS = ["fwd", "fwd-excl", "rev", "rev-excl"]
+
+
+def run(x_cpu, dim, reverse, exclusive, offset=0, out_offset=0):
+    xd = on_device(x_cpu, offset)
+    y = on_device(torch.zeros_like(x_cpu), out_offset)
+    L.cumsum_f32(xd, dim, reverse=reverse, exclusive=exclusive, out=y)
+    L.check()
+    return y.cpu().numpy()
+
+
+def check(shape, dim, reverse, exclusive, dist="uniform_pm1", seed=4, offset=0, out_offset=0):
+    x = inputs.make(shape, dist, seed)
+    o, n, i = L.canonical_axis(x.shape, dim)
+    ref, scale = oracle.cumsum(x.numpy(), o, n, i, reverse, exclusive)
+    got = run(x, dim, reverse, exclusive, offset, out_offset)
+    assert_close(got.reshape(-1), ref.reshape(-1), scale.reshape(-1),
+                 f"cumsum {shape} dim={dim} rev={reverse} excl={exclusive} off={offset}/{out_offset}")
+    return got, ref
+
+
+def test_worked_examples():
+    with open(os.path.join(GOLDEN, "exclusive_scan_worked_example.json")) as f:
+        cases = json.load(f)["cases"]
+    with open(os.path.join(GOLDEN, "rcumsum_worked_examples.json")) as f:
+        cases += [dict(c, reverse=True, exclusive=False) for c in json.load(f)["cases"]]
+    for c in cases:
+        x = torch.tensor([c["x"]], dtype=torch.float32)
+        got = run(x, 1, c["reverse"], c["exclusive"])
+        assert got.reshape(-1).tolist() == [float(v) for v in c["y"]], c
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("rows,n", [(1, 1), (3, 5), (2, 4096), (5, 8193), (37, 32768), (300, 1001),
+                                    (1, 1_000_003), (3, 200_004)])
+def test_rows(rows, n, reverse, exclusive):
+    got, ref = check((rows, n), 1, reverse, exclusive)
+    if exclusive:
+        edge = 0 if not reverse else n - 1
+        assert np.all(got[:, edge] == 0.0)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("strategy", [1, 2, 3])
+def test_rows_every_strategy(strategy, reverse, exclusive):
+    L.set_option(L.OPT_SCAN_STRATEGY, strategy)
+    check((3, 100_000), 1, reverse, exclusive)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("offset,out_offset", [(1, 0), (2, 3)])
+def test_rows_misaligned(offset, out_offset, reverse, exclusive):
+    check((4, 50_001), 1, reverse, exclusive, offset=offset, out_offset=out_offset)
+    L.set_option(L.OPT_SCAN_STRATEGY, 2)
+    check((1, 300_000), 1, reverse, exclusive, offset=offset, out_offset=out_offset)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape,dim", [((4, 9, 7), 1), ((2, 1000, 64), 1), ((3, 257, 33), 1),
+                                       ((1, 5000, 4096), 1), ((600, 8), 0), ((7, 6, 5, 4), 2),
+                                       ((16, 4096, 4095), 1)])
+def test_axis(shape, dim, reverse, exclusive):
+    check(shape, dim, reverse, exclusive)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+def test_axis_misaligned_and_long(reverse, exclusive):
+    check((2, 700, 36), 1, reverse, exclusive, offset=1)
+    check((2, 300_000, 4), 1, reverse, exclusive)  # long axis: blocked running sum
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+def test_integer_inputs_exact(reverse, exclusive):
+    for shape, dim in (((64, 32768), 1), ((3, 4000, 36), 1), ((1, 1 << 20), 1)):
+        x = inputs.make(shape, "int:0:3", 3)
+        o, n, i = L.canonical_axis(x.shape, dim)
+        ref, _ = oracle.cumsum(x.numpy(), o, n, i, reverse, exclusive)
+        assert_exact(run(x, dim, reverse, exclusive).reshape(-1), ref.reshape(-1), f"int {shape}")
+
+
+def test_deterministic_bitwise():
+    for shape, dim in (((1, 1 << 24), 1), ((128, 4096, 63), 1), ((512, 32768), 1)):
+        xd = on_device(inputs.make(shape, "uniform01", 5))
+        for reverse, exclusive in MODES:
+            outs = [L.cumsum_f32(xd, dim, reverse=reverse, exclusive=exclusive).clone() for _ in range(3)]
+            L.check()
+            for o in outs[1:]:
+                assert bitwise_equal(outs[0], o), (shape, reverse, exclusive)
+
+
+def test_reverse_entry_point_matches():
+    xd = on_device(inputs.make((5, 70_000), "uniform01", 6))
+    a = L.reverse_cumsum_f32(xd)
+    b = L.cumsum_f32(xd, 1, reverse=True)
+    L.check()
+    assert bitwise_equal(a, b)
