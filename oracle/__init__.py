@@ -47,6 +47,8 @@ class Oracle:
         lib.oracle_axis_sum_at.restype = None
         lib.oracle_cumsum.argtypes = [_f32p, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _f64p, _f64p]
         lib.oracle_cumsum.restype = None
+        lib.oracle_reduce_op.argtypes = [_f32p, _i64, _i64, _i64, ctypes.c_int, _f64p, _f64p]
+        lib.oracle_reduce_op.restype = None
         self._lib = lib
         self.path = lib_path
 
@@ -104,6 +106,20 @@ class Oracle:
         return y.reshape(outer, N, inner), abs_y.reshape(outer, N, inner)
 
 
+    OPS = {"mean": 1, "max": 2, "min": 3, "norm": 4}
+
+    def reduce_op(self, x, outer, reduce, inner, op):
+        """(out, scale), each fp64 [outer, inner]: mean / max / min / norm of
+        x[o, :, i]; scale is sum|x| (mean) or sum x^2 (norm), 0 otherwise."""
+        x = _as_f32(x)
+        if x.size != outer * reduce * inner:
+            raise ValueError("size mismatch")
+        out = np.empty(outer * inner, np.float64)
+        sc = np.empty(outer * inner, np.float64)
+        self._lib.oracle_reduce_op(x, outer, reduce, inner, self.OPS[op], out, sc)
+        return out.reshape(outer, inner), sc.reshape(outer, inner)
+
+
 _default = None
 
 
@@ -133,6 +149,10 @@ def reverse_cumsum(x, rows, N):
 
 def cumsum(x, outer, N, inner, reverse=False, exclusive=False):
     return default().cumsum(x, outer, N, inner, reverse, exclusive)
+
+
+def reduce_op(x, outer, reduce, inner, op):
+    return default().reduce_op(x, outer, reduce, inner, op)
 
 
 def tolerance(abs_scale):

@@ -52,3 +52,26 @@ def cumsum_exact(flat, outer, n, inner, reverse=False, exclusive=False):
             plane.append([sum_exact(flat[(o * n + k) * inner + i] for k in ks) for i in range(inner)])
         out.append(plane)
     return out
+
+
+def reduce_op_exact(flat, outer, reduce, inner, op):
+    """mean / max / min / squared norm of x[o, :, i] with Python built-ins and
+    exact rationals (the norm is returned squared, exactly)."""
+    out = []
+    for o in range(outer):
+        row = []
+        for i in range(inner):
+            vals = [flat[(o * reduce + r) * inner + i] for r in range(reduce)]
+            if op == "mean":
+                row.append(sum_exact(vals) / len(vals) if vals else None)
+            elif op == "max":
+                row.append(max(vals) if vals else float("-inf"))
+            elif op == "min":
+                row.append(min(vals) if vals else float("inf"))
+            else:
+                total = Fraction(0)
+                for v in vals:
+                    total += Fraction(float(v)) * Fraction(float(v))
+                row.append(total)
+        out.append(row)
+    return out

@@ -15,6 +15,8 @@
  *   oracle_reverse_cumsum  y[i,j] = sum_{k>=j} x[i,k]               (suffix sum)
  *   oracle_cumsum          cumulative sum along the middle axis of [outer, N,
  *                          inner], forward or reverse, inclusive or exclusive
+ *   oracle_reduce_op       max, min, mean or Euclidean norm along the middle
+ *                          axis of [outer, reduce, inner]
  *
  * Each one also returns the companion sum of |x| over the same terms, which
  * is the scale of the per-element acceptance tolerance
@@ -30,6 +32,9 @@
  *     cumsum(x.flip(1), 1).flip(1), i.e. y[i,j] = x[i,j] + ... + x[i,N-1]
  *     (opening problem statement); the same trace works an exclusive
  *     (forward) scan of 1..8 by hand, and discusses scanning other dims.
+ *   - "Seven-step reduction: 30x from one kernel" (introduction): sum, max,
+ *     the softmax denominator, the L2 norm and row sums are all the same
+ *     reduction pattern.
  *
  * Build with the host compiler and without -ffast-math, so the sequential
  * fp64 loops are not reassociated (oracle/build.py does this).
@@ -143,6 +148,45 @@ void oracle_cumsum(const float* x, int64_t outer, int64_t N, int64_t inner, int 
           if (abs_y) abs_y[idx] = acc_abs;
         }
       }
+    }
+  }
+}
+
+/* Other reductions along the middle axis of a contiguous [outer, reduce,
+ * inner] array, one output per (o, i), taken over r = 0..reduce-1 in order:
+ *   op 1  mean:  (sum of x) / reduce                  (empty: NaN)
+ *   op 2  max:   the largest x, NaN if any x is NaN     (empty: -inf)
+ *   op 3  min:   the smallest x, NaN if any x is NaN    (empty: +inf)
+ *   op 4  norm:  sqrt(sum of x*x)                     (empty: 0)
+ * abs_out (may be NULL) gets the sum of |x| (mean) or of x*x (norm), the
+ * scale of the acceptance tolerance; max and min are compared exactly. */
+void oracle_reduce_op(const float* x, int64_t outer, int64_t reduce, int64_t inner, int op,
+                      double* out, double* abs_out) {
+  for (int64_t o = 0; o < outer; ++o) {
+    for (int64_t i = 0; i < inner; ++i) {
+      double acc = (op == 2) ? -INFINITY : (op == 3) ? INFINITY : 0.0;
+      double scale = 0.0;
+      for (int64_t r = 0; r < reduce; ++r) {
+        const double v = (double)x[(o * reduce + r) * inner + i];
+        if (op == 1) {
+          acc += v;
+          scale += fabs(v);
+        } else if (op == 2) {
+          if (isnan(v) || isnan(acc)) acc = NAN;
+          else if (v > acc) acc = v;
+        } else if (op == 3) {
+          if (isnan(v) || isnan(acc)) acc = NAN;
+          else if (v < acc) acc = v;
+        } else {
+          acc += v * v;
+          scale += v * v;
+        }
+      }
+      double res = acc;
+      if (op == 1) res = reduce > 0 ? acc / (double)reduce : NAN;
+      if (op == 4) res = sqrt(acc);
+      out[o * inner + i] = res;
+      if (abs_out) abs_out[o * inner + i] = scale;
     }
   }
 }

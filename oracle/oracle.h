@@ -19,6 +19,8 @@ void oracle_reverse_cumsum(const float* x, int64_t rows, int64_t N, double* y,
                            double* abs_y);
 void oracle_cumsum(const float* x, int64_t outer, int64_t N, int64_t inner, int reverse,
                    int exclusive, double* y, double* abs_y);
+void oracle_reduce_op(const float* x, int64_t outer, int64_t reduce, int64_t inner, int op,
+                      double* out, double* abs_out);
 void oracle_axis_sum_at(const float* x, int64_t outer, int64_t reduce, int64_t inner,
                         const int64_t* pos, int64_t m, double* out, double* abs_out);
 

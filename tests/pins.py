@@ -255,7 +255,66 @@ def pin_cumsum_integers(orc):
     assert np.array_equal(y[:, :, 0], orc.reverse_cumsum(x2, 5, 77)[0])
 
 
+OP_SHAPES = [(1, 1, 1), (2, 5, 3), (3, 1, 4), (1, 9, 1), (4, 6, 2)]
+
+
+def pin_reduce_ops_bruteforce(orc):
+    """Max and min against Python's max()/min() (exact), mean against the exact
+    rational mean, the norm squared against the exact rational sum of squares
+    (the "Seven-step reduction" page lists sum, max and the L2 norm as the same
+    reduction pattern)."""
+    rng = np.random.default_rng(31)
+    for (o, r, i) in OP_SHAPES:
+        x = _mixed_values(rng, o * r * i)
+        for op in ("mean", "max", "min", "norm"):
+            out, sc = orc.reduce_op(x, o, r, i, op)
+            ex = brute.reduce_op_exact(x.tolist(), o, r, i, op)
+            for a in range(o):
+                for b in range(i):
+                    if op in ("max", "min"):
+                        assert out[a, b] == float(ex[a][b]), (op, (o, r, i), a, b)
+                    elif op == "mean":
+                        scale = sum(abs(float(x[(a * r + k) * i + b])) for k in range(r))
+                        assert abs(out[a, b] - float(ex[a][b])) <= r * U64 * scale / r + 1e-300, (op, a, b)
+                    else:
+                        want = float(ex[a][b])
+                        assert abs(out[a, b] ** 2 - want) <= (r + 2) * U64 * want + 1e-300, (op, a, b)
+
+
+def pin_reduce_ops_closed_forms(orc):
+    """Closed forms: the mean of 1..n is (n+1)/2; a constant c has mean c,
+    max = min = c and norm |c| sqrt(n); the norms of (3, 4) and (1, 2, 2) are
+    5 and 3; NaN propagates through max and min; empty axes give -inf, +inf,
+    NaN and 0."""
+    n = 1001
+    x = np.arange(1, n + 1, dtype=np.float32)
+    assert orc.reduce_op(x, 1, n, 1, "mean")[0][0, 0] == (n + 1) / 2
+    assert orc.reduce_op(x, 1, n, 1, "max")[0][0, 0] == n
+    assert orc.reduce_op(x, 1, n, 1, "min")[0][0, 0] == 1
+    c = np.full(400, -2.5, dtype=np.float32)
+    assert orc.reduce_op(c, 1, 400, 1, "mean")[0][0, 0] == -2.5
+    assert orc.reduce_op(c, 1, 400, 1, "norm")[0][0, 0] == 2.5 * 20.0
+    assert orc.reduce_op(np.array([3, 4], np.float32), 1, 2, 1, "norm")[0][0, 0] == 5.0
+    assert orc.reduce_op(np.array([1, 2, 2], np.float32), 1, 3, 1, "norm")[0][0, 0] == 3.0
+    y = np.array([1.0, np.nan, 7.0], np.float32)
+    assert np.isnan(orc.reduce_op(y, 1, 3, 1, "max")[0][0, 0])
+    assert np.isnan(orc.reduce_op(y, 1, 3, 1, "min")[0][0, 0])
+    e = np.zeros(0, np.float32)
+    assert orc.reduce_op(e, 2, 0, 3, "max")[0].tolist() == [[-np.inf] * 3] * 2
+    assert orc.reduce_op(e, 2, 0, 3, "min")[0].tolist() == [[np.inf] * 3] * 2
+    assert np.isnan(orc.reduce_op(e, 1, 0, 1, "mean")[0][0, 0])
+    assert orc.reduce_op(e, 1, 0, 1, "norm")[0][0, 0] == 0.0
+    # Strided axis with integers: exact against int64 arithmetic.
+    z = _np(inputs.make((3, 40, 5), "int:-8:8", 12))
+    zi = z.astype(np.int64)
+    assert np.array_equal(orc.reduce_op(z, 3, 40, 5, "max")[0], zi.max(axis=1).astype(np.float64))
+    assert np.array_equal(orc.reduce_op(z, 3, 40, 5, "min")[0], zi.min(axis=1).astype(np.float64))
+    # The sum of squares of small integers is exact, and sqrt is correctly rounded.
+    assert np.array_equal(orc.reduce_op(z, 3, 40, 5, "norm")[0],
+                          np.sqrt((zi * zi).sum(axis=1).astype(np.float64)))
+
+
 ALL_PINS = [pin_sum_harmonic, pin_sum_constant, pin_sum_integers, pin_sum_bruteforce,
             pin_axis_bruteforce, pin_axis_integers_and_invariants, pin_scan_worked_examples,
             pin_scan_bruteforce, pin_scan_integers, pin_cumsum_bruteforce, pin_cumsum_worked_examples,
-            pin_cumsum_integers]
+            pin_cumsum_integers, pin_reduce_ops_bruteforce, pin_reduce_ops_closed_forms]

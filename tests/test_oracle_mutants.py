@@ -35,6 +35,14 @@ MUTANTS = [
     ("cumsum_exclusive_ignored", "oracle_cumsum", "if (exclusive) {", "if (0) {"),
     ("cumsum_wrong_index", "oracle_cumsum", "const int64_t idx = (o * N + j) * inner + i;",
      "const int64_t idx = (o * inner + i) * N + j;"),
+    ("op_max_is_min", "oracle_reduce_op", "else if (v > acc) acc = v;", "else if (v < acc) acc = v;"),
+    ("op_nan_dropped", "oracle_reduce_op", "if (isnan(v) || isnan(acc)) acc = NAN;\n          else if (v > acc)",
+     "if (0) acc = NAN;\n          else if (v > acc)"),
+    ("op_mean_not_divided", "oracle_reduce_op", "res = reduce > 0 ? acc / (double)reduce : NAN;",
+     "res = reduce > 0 ? acc : NAN;"),
+    ("op_norm_no_sqrt", "oracle_reduce_op", "if (op == 4) res = sqrt(acc);", "if (op == 4) res = acc;"),
+    ("op_norm_abs_not_square", "oracle_reduce_op", "acc += v * v;", "acc += fabs(v);"),
+    ("op_wrong_index", "oracle_reduce_op", "x[(o * reduce + r) * inner + i]", "x[(o * inner + i) * reduce + r]"),
     ("cumsum_no_reset", "oracle_cumsum", "      double acc = 0.0;\n      double acc_abs = 0.0;\n      for (int64_t step",
      "      double acc_abs = 0.0;\n      for (int64_t step"),
 ]
