@@ -46,7 +46,8 @@ METRIC = "effective HBM GB/s and % of GB300 peak per reduce/scan config (1 GPU)"
 STEP_WORKLOADS = ["sum_1e9", "axis_128x4096x4095_d1", "axis_4096x65536_d1", "axis_65536x4096_d0",
                   "rcumsum_32768x32768", "rcumsum_1x1e9"]
 # Follow-on forms, timed separately from the step (reported under next_rows).
-NEXT_WORKLOADS = ["cumsum_fwd_32768x32768", "cumsum_fwd_excl_1x1e9", "cumsum_128x4096x4095_d1"]
+NEXT_WORKLOADS = ["cumsum_fwd_32768x32768", "cumsum_fwd_excl_1x1e9", "cumsum_128x4096x4095_d1",
+                  "max_1e9", "norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0"]
 # Small cases of each kernel for ncu captures: larger than L2, a few GB at most.
 PROFILE_CASES = {
     "sum_2e8": dict(op="sum", shape=(200_000_000,), dist="uniform01", seed=42),
@@ -206,15 +207,19 @@ def make_call(name, x, out):
         return lambda: L.reduce_axis_f32(x, w["dim"], out=out)
     if w["op"] == "cumsum":
         return lambda: L.cumsum_f32(x, w["dim"], reverse=w["reverse"], exclusive=w["exclusive"], out=out)
+    if w["op"] == "reduce":
+        if "dim" in w:
+            return lambda: L.reduce_axis_op_f32(x, w["dim"], w["rop"], out=out)
+        return lambda: L.reduce_f32(x, w["rop"], out=out)
     return lambda: L.reverse_cumsum_f32(x, out=out)
 
 
 def alloc_workload(name, device):
     w = workload_spec(name)
     x = inputs.make(w["shape"], w["dist"], w["seed"], device=device)
-    if w["op"] == "sum":
+    if w["op"] == "sum" or (w["op"] == "reduce" and "dim" not in w):
         out = torch.empty((), dtype=torch.float32, device=device)
-    elif w["op"] == "axis":
+    elif w["op"] in ("axis", "reduce"):
         shp = list(w["shape"])
         del shp[w["dim"]]
         out = torch.empty(shp, dtype=torch.float32, device=device)

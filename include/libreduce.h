@@ -103,6 +103,33 @@ LIBREDUCE_API int reduce_axis_f32(const float* x, int64_t outer, int64_t reduce,
                     libreduce_stream_t stream);
 
 /*
+ * Other reductions on the same kernels (the "Seven-step reduction" page lists
+ * sum, max, the L2 norm and row sums as one pattern):
+ *   LIBREDUCE_OP_SUM   sum
+ *   LIBREDUCE_OP_MEAN  sum / count (the fp32 sum divided in double, rounded once)
+ *   LIBREDUCE_OP_MAX   largest element; NaN if any element is NaN; exact
+ *   LIBREDUCE_OP_MIN   smallest element; NaN if any element is NaN; exact
+ *   LIBREDUCE_OP_NORM  sqrt(sum of x*x) (correctly rounded square root)
+ * An empty reduction gives 0 (sum, norm), NaN (mean), -inf (max), +inf (min).
+ * Accuracy: sum as above; mean within (1e-5*sum|x| + 1e-6)/count plus one
+ * rounding; norm within 1e-5 * norm + 1e-6.
+ *
+ * reduce_f32      -- out[0] = op over x[0 .. n-1]             (reduce_sum_f32 is op SUM)
+ * reduce_axis_op_f32 -- out[o*inner + i] = op over r of x[(o*reduce + r)*inner + i]
+ *                       (reduce_axis_f32 is op SUM)
+ * Arguments, layout and errors as reduce_sum_f32 / reduce_axis_f32; an
+ * unknown op is INVALID_ARG.
+ */
+#define LIBREDUCE_OP_SUM 0
+#define LIBREDUCE_OP_MEAN 1
+#define LIBREDUCE_OP_MAX 2
+#define LIBREDUCE_OP_MIN 3
+#define LIBREDUCE_OP_NORM 4
+LIBREDUCE_API int reduce_f32(const float* x, int64_t n, float* out, int op, libreduce_stream_t stream);
+LIBREDUCE_API int reduce_axis_op_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner,
+                                     float* out, int op, libreduce_stream_t stream);
+
+/*
  * reverse_cumsum_f32 -- y[i*N + j] = sum_{k=j}^{N-1} x[i*N + k] for every row i.
  *
  * The reverse inclusive cumulative sum along the last dim of a contiguous

@@ -31,9 +31,9 @@ constexpr size_t kWorkspaceBytes =
 struct DeviceState {
   bool ready = false;
   int sm_count = 0;
-  int occ_contig[kNumContigVariants] = {};
-  int occ_rows_warp = 0;
-  int occ_cols[kNumColsVariants] = {};
+  int occ_contig[kNumContigVariants][kNumReduceOps] = {};
+  int occ_rows_warp[kNumReduceOps] = {};
+  int occ_cols[kNumColsVariants][kNumReduceOps] = {};
   int occ_rscan[kNumRScanVariants] = {};
   // Workspace (allocated by the first call that needs it).
   char* ws = nullptr;
@@ -77,9 +77,13 @@ int device_state(DeviceState** out, int* dev_out) {
   if (!st.ready) {
     e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail_cuda(e);
-    for (int v = 0; v < kNumContigVariants; ++v) st.occ_contig[v] = std::max(1, occupancy_reduce_contig(v));
-    st.occ_rows_warp = std::max(1, occupancy_reduce_rows_warp());
-    for (int v = 0; v < kNumColsVariants; ++v) st.occ_cols[v] = std::max(1, occupancy_reduce_cols(v));
+    for (int op = 0; op < kNumReduceOps; ++op) {
+      for (int v = 0; v < kNumContigVariants; ++v)
+        st.occ_contig[v][op] = std::max(1, occupancy_reduce_contig(v, op));
+      st.occ_rows_warp[op] = std::max(1, occupancy_reduce_rows_warp(op));
+      for (int v = 0; v < kNumColsVariants; ++v)
+        st.occ_cols[v][op] = std::max(1, occupancy_reduce_cols(v, op));
+    }
     for (int v = 0; v < kNumRScanVariants; ++v) st.occ_rscan[v] = std::max(1, occupancy_rscan_rows(v));
     for (int v = 0; v < kNumLookbackVariants; ++v)
       st.occ_lookback[v] = std::max(1, occupancy_rscan_lookback(v));
@@ -215,11 +219,11 @@ int contig_variant() {
   return (v >= 0 && v < kNumContigVariants) ? (int)v : kContigU16;
 }
 
-// Sum of `segments` contiguous segments of seg_len floats each.
+// Reduction of `segments` contiguous segments of seg_len floats each.
 int run_contig(DeviceState* st, const float* x, int64_t segments, int64_t seg_len, float* out,
-               cudaStream_t s) {
-  const int variant = contig_variant();
-  const int64_t slots = (int64_t)st->sm_count * st->occ_contig[variant];
+               int op, int epi, cudaStream_t s) {
+  const int variant = op == kOpSum ? contig_variant() : kContigU16;
+  const int64_t slots = (int64_t)st->sm_count * st->occ_contig[variant][op];
   const int64_t waves = g_opt_waves.load();
   int64_t chunks = 1;
   const int64_t forced = g_opt_axis_split.load();
@@ -248,36 +252,36 @@ int run_contig(DeviceState* st, const float* x, int64_t segments, int64_t seg_le
   }
   const int64_t grid = segments * chunks;
   if (grid > INT32_MAX) return LIBREDUCE_ERR_OVERFLOW;
-  ContigParams p{x, seg_len, chunk_len, (int32_t)chunks, out, nullptr, nullptr};
+  ContigParams p{x, seg_len, chunk_len, (int32_t)chunks, out, nullptr, nullptr, epi};
   if (chunks > 1) {
     int rc = ensure_workspace(st);
     if (rc) return rc;
     p.partials = st->partials;
     p.tickets = st->tickets;
   }
-  return launched(launch_reduce_contig(variant, p, grid, s));
+  return launched(launch_reduce_contig(variant, op, p, grid, s));
 }
 
-int run_rows_warp(DeviceState* st, const float* x, int64_t rows, int64_t len, float* out,
-                  cudaStream_t s) {
-  const int64_t slots = (int64_t)st->sm_count * st->occ_rows_warp;
+int run_rows_warp(DeviceState* st, const float* x, int64_t rows, int64_t len, float* out, int op,
+                  int epi, cudaStream_t s) {
+  const int64_t slots = (int64_t)st->sm_count * st->occ_rows_warp[op];
   const int64_t grid = std::max<int64_t>(1, std::min(ceil_div(rows, kThreads / 32), 8 * slots));
-  RowsWarpParams p{x, rows, len, out};
-  return launched(launch_reduce_rows_warp(p, grid, s));
+  RowsWarpParams p{x, rows, len, out, epi};
+  return launched(launch_reduce_rows_warp(op, p, grid, s));
 }
 
 int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int64_t inner,
-             float* out, cudaStream_t s) {
+             float* out, int op, int epi, cudaStream_t s) {
   const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
   int variant = vec4 ? kColsV4W4 : kColsV1W4;
   const int64_t forced_v = g_opt_cols_variant.load();
-  if (forced_v >= 0 && forced_v < kNumColsVariants) {
+  if (op == kOpSum && forced_v >= 0 && forced_v < kNumColsVariants) {
     const bool fv4 = forced_v >= kColsV4W1;
     if (!fv4 || vec4) variant = (int)forced_v;
   }
   const int64_t cw = cols_block_width(variant);
   const int64_t col_tiles = ceil_div(inner, cw);
-  const int64_t slots = (int64_t)st->sm_count * st->occ_cols[variant];
+  const int64_t slots = (int64_t)st->sm_count * st->occ_cols[variant][op];
   int64_t base_blocks = 0;
   if (mul_overflows(outer, col_tiles, &base_blocks)) return LIBREDUCE_ERR_OVERFLOW;
   int64_t splits = 1;
@@ -286,8 +290,9 @@ int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int
     splits = std::min(forced, reduce);
   } else if (base_blocks < slots) {
     // Too few column tiles to fill the GPU: slice the reduce axis so the grid
-    // is one full wave (measured best for a short kernel: no tail, no ramp).
-    splits = ceil_div(slots, base_blocks);
+    // is one wave, as full as possible without spilling into a second one
+    // (measured best for a short kernel: no tail, no ramp).
+    splits = std::max<int64_t>(1, slots / base_blocks);
     splits = std::min(splits, std::max<int64_t>(1, reduce / 64));  // at least ~64 rows per slice
   }
   int64_t rows_per_split = ceil_div(reduce, splits);
@@ -306,14 +311,69 @@ int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int
   int64_t grid = 0;
   if (mul_overflows(base_blocks, splits, &grid) || grid > INT32_MAX) return LIBREDUCE_ERR_OVERFLOW;
   ColsParams p{x, outer, reduce, inner, (int32_t)col_tiles, (int32_t)splits, rows_per_split,
-               out, nullptr, nullptr};
+               out, nullptr, nullptr, epi};
   if (splits > 1) {
     int rc = ensure_workspace(st);
     if (rc) return rc;
     p.partials = st->partials;
     p.tickets = st->tickets;
   }
-  return launched(launch_reduce_cols(variant, p, grid, s));
+  return launched(launch_reduce_cols(variant, op, p, grid, s));
+}
+
+// Public operator -> (kernel operator, epilogue, value of an empty reduction).
+struct OpPlan {
+  int op;
+  int epi;
+  float empty;
+};
+bool plan_op(int public_op, OpPlan* plan) {
+  const float inf = __builtin_inff(), nan = __builtin_nanf("");
+  switch (public_op) {
+    case LIBREDUCE_OP_SUM: *plan = {kOpSum, kEpiNone, 0.f}; return true;
+    case LIBREDUCE_OP_MEAN: *plan = {kOpSum, kEpiMean, nan}; return true;
+    case LIBREDUCE_OP_MAX: *plan = {kOpMax, kEpiNone, -inf}; return true;
+    case LIBREDUCE_OP_MIN: *plan = {kOpMin, kEpiNone, inf}; return true;
+    case LIBREDUCE_OP_NORM: *plan = {kOpSumSq, kEpiSqrt, 0.f}; return true;
+    default: return false;
+  }
+}
+
+// The reduction behind every reduce entry point: `out[o*inner + i]` is the
+// reduction of x[o, :, i] over the middle axis of [outer, reduce, inner].
+int reduce_impl(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
+                int public_op, cudaStream_t s) {
+  OpPlan plan;
+  if (!plan_op(public_op, &plan)) return LIBREDUCE_ERR_INVALID_ARG;
+  if (outer < 0 || reduce < 0 || inner < 0) return LIBREDUCE_ERR_INVALID_ARG;
+  int64_t n_out = 0, total = 0;
+  if (mul_overflows(outer, inner, &n_out) || mul_overflows(n_out, reduce, &total) ||
+      total > INT64_MAX / 4)
+    return LIBREDUCE_ERR_OVERFLOW;
+  if (n_out == 0) return LIBREDUCE_OK;
+  if (out == nullptr || (x == nullptr && total > 0)) return LIBREDUCE_ERR_INVALID_ARG;
+  if (overlaps(x, (size_t)total * sizeof(float), out, (size_t)n_out * sizeof(float)))
+    return LIBREDUCE_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  int dev = 0;
+  int rc = device_state(&st, &dev);
+  if (rc) return rc;
+  if ((rc = check_buffer(out, (size_t)n_out * sizeof(float), dev))) return rc;
+  if (total == 0) {
+    if (plan.empty == 0.f) {
+      const cudaError_t e = cudaMemsetAsync(out, 0, (size_t)n_out * sizeof(float), s);
+      return e == cudaSuccess ? LIBREDUCE_OK : fail_cuda(e);
+    }
+    return launched(launch_fill(out, n_out, plan.empty, s));
+  }
+  if ((rc = check_buffer(x, (size_t)total * sizeof(float), dev))) return rc;
+  if (inner == 1) {
+    if (outer == 1) return run_contig(st, x, 1, reduce, out, plan.op, plan.epi, s);
+    if (reduce <= kRowsWarpMaxLen && g_opt_axis_split.load() <= 0)
+      return run_rows_warp(st, x, outer, reduce, out, plan.op, plan.epi, s);
+    return run_contig(st, x, outer, reduce, out, plan.op, plan.epi, s);
+  }
+  return run_cols(st, x, outer, reduce, inner, out, plan.op, plan.epi, s);
 }
 
 constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): well under a second
@@ -423,52 +483,24 @@ using namespace lr;
 extern "C" {
 
 int reduce_sum_f32(const float* x, int64_t n, float* out, libreduce_stream_t stream) {
+  return reduce_f32(x, n, out, LIBREDUCE_OP_SUM, stream);
+}
+
+int reduce_f32(const float* x, int64_t n, float* out, int op, libreduce_stream_t stream) {
   if (n < 0 || out == nullptr || (x == nullptr && n > 0)) return LIBREDUCE_ERR_INVALID_ARG;
   if (n > INT64_MAX / 4) return LIBREDUCE_ERR_OVERFLOW;
-  if (n > 0 && overlaps(x, (size_t)n * sizeof(float), out, sizeof(float))) return LIBREDUCE_ERR_ALIAS;
-  DeviceState* st = nullptr;
-  int dev = 0;
-  int rc = device_state(&st, &dev);
-  if (rc) return rc;
-  if ((rc = check_buffer(out, sizeof(float), dev))) return rc;
-  if (n > 0 && (rc = check_buffer(x, (size_t)n * sizeof(float), dev))) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (n == 0) {
-    const cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), s);
-    return e == cudaSuccess ? LIBREDUCE_OK : fail_cuda(e);
-  }
-  return run_contig(st, x, 1, n, out, s);
+  return reduce_impl(x, 1, n, 1, out, op, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int reduce_axis_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
                     libreduce_stream_t stream) {
-  if (outer < 0 || reduce < 0 || inner < 0) return LIBREDUCE_ERR_INVALID_ARG;
-  int64_t n_out = 0, total = 0;
-  if (mul_overflows(outer, inner, &n_out) || mul_overflows(n_out, reduce, &total) ||
-      total > INT64_MAX / 4)
-    return LIBREDUCE_ERR_OVERFLOW;
-  if (n_out == 0) return LIBREDUCE_OK;
-  if (out == nullptr || (x == nullptr && total > 0)) return LIBREDUCE_ERR_INVALID_ARG;
-  if (overlaps(x, (size_t)total * sizeof(float), out, (size_t)n_out * sizeof(float)))
-    return LIBREDUCE_ERR_ALIAS;
-  DeviceState* st = nullptr;
-  int dev = 0;
-  int rc = device_state(&st, &dev);
-  if (rc) return rc;
-  if ((rc = check_buffer(out, (size_t)n_out * sizeof(float), dev))) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (total == 0) {
-    const cudaError_t e = cudaMemsetAsync(out, 0, (size_t)n_out * sizeof(float), s);
-    return e == cudaSuccess ? LIBREDUCE_OK : fail_cuda(e);
-  }
-  if ((rc = check_buffer(x, (size_t)total * sizeof(float), dev))) return rc;
-  if (inner == 1) {
-    if (outer == 1) return run_contig(st, x, 1, reduce, out, s);
-    if (reduce <= kRowsWarpMaxLen && g_opt_axis_split.load() <= 0)
-      return run_rows_warp(st, x, outer, reduce, out, s);
-    return run_contig(st, x, outer, reduce, out, s);
-  }
-  return run_cols(st, x, outer, reduce, inner, out, s);
+  return reduce_impl(x, outer, reduce, inner, out, LIBREDUCE_OP_SUM,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int reduce_axis_op_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
+                       int op, libreduce_stream_t stream) {
+  return reduce_impl(x, outer, reduce, inner, out, op, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, float* y,

@@ -1,4 +1,4 @@
-// lr_contig.cuh -- the contiguous-chunk sum kernel (1D sum and long rows),
+// lr_contig.cuh -- the contiguous-chunk reduction kernel (1D and long rows),
 // shared by the translation units that launch it.  Each including file gets
 // its own instantiation (internal linkage).
 //
@@ -18,27 +18,28 @@ namespace {
 
 constexpr int kFold = 16;  // blocked-accumulator fold length
 
-// Sum p[start], p[start + stride], ... (< n), eight loads in flight, fixed
+// Reduce p[start], p[start + stride], ... (< n), eight loads in flight, fixed
 // order.  The data was written by other blocks of this launch, so it is read
-// from L2.
-__device__ __forceinline__ float sum_strided_cg(const float* p, int64_t n, int64_t start,
-                                                int64_t stride) {
-  BlockedAcc<kFold> acc;
+// from L2.  The values are partial results, already prepped.
+template <typename Op>
+__device__ __forceinline__ float reduce_strided_cg(const float* p, int64_t n, int64_t start,
+                                                   int64_t stride) {
+  BlockedAcc<kFold, Op> acc;
   int64_t k = start;
   for (; k + 7 * stride < n; k += 8 * stride) {
     float r[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) r[u] = ld_cg1(p + k + u * stride);
-    acc.add(tree_sum<8>(r));
+    acc.add(tree_reduce<Op, 8>(r));
   }
   for (; k < n; k += stride) acc.add(ld_cg1(p + k));
   return acc.total();
 }
 
 // ---------------------------------------------------------------------------
-// 1D sum / long rows: one block per (segment, chunk).
+// 1D reduction / long rows: one block per (segment, chunk).
 // ---------------------------------------------------------------------------
-template <int U>
+template <int U, typename Op>
 __global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
   __shared__ float sh[kThreads / 32];
   __shared__ int am_last;
@@ -56,7 +57,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
   const int tail = (int)((len - head) & 3);
   const float* av = a + head;
 
-  BlockedAcc<kFold> acc;
+  BlockedAcc<kFold, Op> acc;
   constexpr int64_t S = kThreads;
   int64_t i = t;
   for (; i + (U - 1) * S < nvec; i += U * S) {
@@ -65,17 +66,17 @@ __global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
     for (int u = 0; u < U; ++u) r[u] = ld_stream4(av + 4 * (i + u * S));
     float s[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) s[u] = sum4(r[u]);
-    acc.add(tree_sum<U>(s));
+    for (int u = 0; u < U; ++u) s[u] = reduce4<Op>(r[u]);
+    acc.add(tree_reduce<Op, U>(s));
   }
-  for (; i < nvec; i += S) acc.add(sum4(ld_stream4(av + 4 * i)));
+  for (; i < nvec; i += S) acc.add(reduce4<Op>(ld_stream4(av + 4 * i)));
   float v = acc.total();
-  if (t < head) v += a[t];
-  if (t < tail) v += av[4 * nvec + t];
+  if (t < head) v = Op::combine(v, Op::prep(a[t]));
+  if (t < tail) v = Op::combine(v, Op::prep(av[4 * nvec + t]));
 
-  v = block_sum<kThreads>(v, sh);
+  v = block_reduce<Op, kThreads>(v, sh);
   if (p.chunks == 1) {
-    if (t == 0) p.out[seg] = v;
+    if (t == 0) p.out[seg] = finish(v, p.epi, p.seg_len);
     return;
   }
   if (t == 0) {
@@ -87,10 +88,10 @@ __global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
   __syncthreads();
   if (!am_last) return;
   __threadfence();
-  float s = sum_strided_cg(p.partials + seg * p.chunks, p.chunks, t, kThreads);
-  s = block_sum<kThreads>(s, sh);
+  float s = reduce_strided_cg<Op>(p.partials + seg * p.chunks, p.chunks, t, kThreads);
+  s = block_reduce<Op, kThreads>(s, sh);
   if (t == 0) {
-    p.out[seg] = s;
+    p.out[seg] = finish(s, p.epi, p.seg_len);
     p.tickets[seg] = 0u;  // ready for the next launch
   }
 }

@@ -10,6 +10,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "lr_internal.h"
+
 namespace lr {
 
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -140,78 +142,125 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, 
 }
 
 // ---------------------------------------------------------------------------
-// Summation building blocks.  Every tree below has a fixed shape, so a given
+// Reduction operators.  `prep` maps a loaded element to the value that is
+// combined (x*x for a sum of squares); `combine` is associative up to
+// rounding; `identity` is the value of an empty reduction.  Max and min
+// propagate NaN (a NaN operand wins), like the comparison-based reductions
+// of most array libraries; on ties they keep one operand, chosen by position.
+// ---------------------------------------------------------------------------
+struct OpSum {
+  static __device__ __forceinline__ float identity() { return 0.f; }
+  static __device__ __forceinline__ float prep(float x) { return x; }
+  static __device__ __forceinline__ float combine(float a, float b) { return a + b; }
+};
+struct OpSumSq {
+  static __device__ __forceinline__ float identity() { return 0.f; }
+  static __device__ __forceinline__ float prep(float x) { return x * x; }
+  static __device__ __forceinline__ float combine(float a, float b) { return a + b; }
+};
+struct OpMax {
+  static __device__ __forceinline__ float identity() { return __int_as_float(0xff800000); }  // -inf
+  static __device__ __forceinline__ float prep(float x) { return x; }
+  static __device__ __forceinline__ float combine(float a, float b) { return (a > b || a != a) ? a : b; }
+};
+struct OpMin {
+  static __device__ __forceinline__ float identity() { return __int_as_float(0x7f800000); }  // +inf
+  static __device__ __forceinline__ float prep(float x) { return x; }
+  static __device__ __forceinline__ float combine(float a, float b) { return (a < b || a != a) ? a : b; }
+};
+
+// ---------------------------------------------------------------------------
+// Reduction building blocks.  Every tree below has a fixed shape, so a given
 // input always produces the same bits.
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ float sum4(float4 v) { return (v.x + v.y) + (v.z + v.w); }
+template <typename Op>
+__device__ __forceinline__ float reduce4(float4 v) {
+  return Op::combine(Op::combine(Op::prep(v.x), Op::prep(v.y)), Op::combine(Op::prep(v.z), Op::prep(v.w)));
+}
+__device__ __forceinline__ float sum4(float4 v) { return reduce4<OpSum>(v); }
 
-// Pairwise sum of a small register array, fixed shape.
-template <int N>
-__device__ __forceinline__ float tree_sum(const float* v) {
+// Pairwise reduction of a small register array (values already prepped).
+template <typename Op, int N>
+__device__ __forceinline__ float tree_reduce(const float* v) {
   if constexpr (N == 1) {
     return v[0];
   } else {
     constexpr int H = N / 2;
-    return tree_sum<H>(v) + tree_sum<N - H>(v + H);
+    return Op::combine(tree_reduce<Op, H>(v), tree_reduce<Op, N - H>(v + H));
   }
 }
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v) { return tree_reduce<OpSum, N>(v); }
 
-// Warp sum: lane 0 receives the sum of v over the 32 lanes.
-__device__ __forceinline__ float warp_sum(float v) {
+// Warp reduction: lane 0 receives the reduction of v over the 32 lanes.
+template <typename Op>
+__device__ __forceinline__ float warp_reduce(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(kFullMask, v, o);
+  for (int o = 16; o > 0; o >>= 1) v = Op::combine(v, __shfl_down_sync(kFullMask, v, o));
   return v;
 }
+__device__ __forceinline__ float warp_sum(float v) { return warp_reduce<OpSum>(v); }
 
-// Block sum for NT threads (NT a multiple of 32, at most 1024).  `sh` holds
-// NT/32 floats.  The result is valid in thread 0.  The caller must place a
-// __syncthreads() between two uses of the same `sh`.
-template <int NT>
-__device__ __forceinline__ float block_sum(float v, float* sh) {
+// Block reduction for NT threads (NT a multiple of 32, at most 1024).  `sh`
+// holds NT/32 floats.  The result is valid in thread 0.  The caller must place
+// a __syncthreads() between two uses of the same `sh`.
+template <typename Op, int NT>
+__device__ __forceinline__ float block_reduce(float v, float* sh) {
   constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  v = warp_sum(v);
+  v = warp_reduce<Op>(v);
   if constexpr (NW == 1) {
     return v;
   } else {
     if (lane == 0) sh[warp] = v;
     __syncthreads();
-    float r = 0.f;
+    float r = Op::identity();
     if (warp == 0) {
-      r = lane < NW ? sh[lane] : 0.f;
+      r = lane < NW ? sh[lane] : Op::identity();
 #pragma unroll
-      for (int o = NW / 2; o > 0; o >>= 1) r += __shfl_down_sync(kFullMask, r, o);
+      for (int o = NW / 2; o > 0; o >>= 1) r = Op::combine(r, __shfl_down_sync(kFullMask, r, o));
     }
     return r;
   }
 }
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float* sh) { return block_reduce<OpSum, NT>(v, sh); }
 
 // Three-level accumulator.  A plain running fp32 sum over m terms has an
 // addition chain of length m, and its worst-case rounding error grows with m.
-// Folding the running sum into a second, then a third register every K terms
-// keeps every chain at most K + K + m/K^2 long, at the cost of two extra adds
-// per K terms.  The fold points depend only on the number of terms, so the
-// result is deterministic.
-template <int K>
+// Folding the running value into a second, then a third register every K
+// terms keeps every chain at most K + K + m/K^2 long, at the cost of two extra
+// combines per K terms.  The fold points depend only on the number of terms,
+// so the result is deterministic.  (For max and min the folds change nothing.)
+template <int K, typename Op = OpSum>
 struct BlockedAcc {
-  float lo = 0.f, mid = 0.f, hi = 0.f;
+  float lo = Op::identity(), mid = Op::identity(), hi = Op::identity();
   int n_lo = 0, n_mid = 0;
   __device__ __forceinline__ void add(float v) {
-    lo += v;
+    lo = Op::combine(lo, v);
     if (++n_lo == K) {
-      mid += lo;
-      lo = 0.f;
+      mid = Op::combine(mid, lo);
+      lo = Op::identity();
       n_lo = 0;
       if (++n_mid == K) {
-        hi += mid;
-        mid = 0.f;
+        hi = Op::combine(hi, mid);
+        mid = Op::identity();
         n_mid = 0;
       }
     }
   }
-  __device__ __forceinline__ float total() const { return hi + (mid + lo); }
+  __device__ __forceinline__ float total() const { return Op::combine(hi, Op::combine(mid, lo)); }
 };
+
+// Output epilogue: the mean divides by the element count (in double, then
+// rounds once to fp32); the Euclidean norm takes the square root of the sum
+// of squares (IEEE, correctly rounded).
+__device__ __forceinline__ float finish(float v, int epi, int64_t count) {
+  if (epi == kEpiMean) return (float)((double)v / (double)count);
+  if (epi == kEpiSqrt) return sqrtf(v);
+  return v;
+}
 
 }  // namespace lr

@@ -7,6 +7,10 @@
 
 namespace lr {
 
+// Output epilogue of the reduce kernels: the mean divides the sum by the
+// element count, the norm takes the square root of the sum of squares.
+enum Epilogue { kEpiNone = 0, kEpiMean = 1, kEpiSqrt = 2 };
+
 constexpr int kThreads = 256;  // every libreduce kernel runs 256-thread blocks
 
 // --- 1D sum and row sums over contiguous segments --------------------------
@@ -23,6 +27,7 @@ struct ContigParams {
   float* out;          // one float per segment
   float* partials;     // segments * chunks floats (chunks > 1)
   unsigned* tickets;   // one per segment, zero on entry, left zero on exit
+  int epi;             // output epilogue (kEpiNone, kEpiMean, kEpiSqrt)
 };
 
 // --- Row sums, one warp per row (short rows) -------------------------------
@@ -31,6 +36,7 @@ struct RowsWarpParams {
   int64_t rows;
   int64_t len;
   float* out;
+  int epi;
 };
 
 // --- Axis sum with inner > 1 ------------------------------------------------
@@ -48,6 +54,7 @@ struct ColsParams {
   float* out;
   float* partials;
   unsigned* tickets;  // outer * col_tiles, zero on entry, left zero on exit
+  int epi;
 };
 
 // --- Scan flags (internal) ---------------------------------------------------
@@ -98,8 +105,14 @@ struct RScanLookbackParams {
   int flags;                     // kScanMirror | kScanExclusive
 };
 
+// Reduction operators of the reduce kernels (the epilogue in the params turns
+// a sum into a mean and a sum of squares into a norm).
+enum ReduceOp { kOpSum = 0, kOpSumSq = 1, kOpMax = 2, kOpMin = 3, kNumReduceOps };
+
 // Variants are small integers chosen by the dispatcher; each launcher
-// returns cudaErrorInvalidValue for a variant it does not have.
+// returns cudaErrorInvalidValue for a variant it does not have.  Operators
+// other than kOpSum exist for the default variants only (kContigU16,
+// kColsV1W4, kColsV4W4).
 enum ContigVariant { kContigU4 = 0, kContigU8 = 1, kContigU16 = 2, kNumContigVariants };
 enum ColsVariant {
   kColsV1W1 = 0,   // scalar columns, 8 warps across columns
@@ -126,9 +139,11 @@ int64_t lookback_tile(int variant);
 // Columns covered by one block of a cols variant.
 int cols_block_width(int variant);
 
-cudaError_t launch_reduce_contig(int variant, const ContigParams& p, int64_t grid, cudaStream_t s);
-cudaError_t launch_reduce_rows_warp(const RowsWarpParams& p, int64_t grid, cudaStream_t s);
-cudaError_t launch_reduce_cols(int variant, const ColsParams& p, int64_t grid, cudaStream_t s);
+cudaError_t launch_reduce_contig(int variant, int op, const ContigParams& p, int64_t grid,
+                                 cudaStream_t s);
+cudaError_t launch_reduce_rows_warp(int op, const RowsWarpParams& p, int64_t grid, cudaStream_t s);
+cudaError_t launch_reduce_cols(int variant, int op, const ColsParams& p, int64_t grid, cudaStream_t s);
+cudaError_t launch_fill(float* out, int64_t n, float value, cudaStream_t s);
 cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int64_t grid,
                                   cudaStream_t s);
@@ -140,9 +155,9 @@ int record_cuda_error(cudaError_t e);                           // returns the C
 void count_launch();
 
 // Resident 256-thread blocks per SM for each kernel variant (0 on error).
-int occupancy_reduce_contig(int variant);
-int occupancy_reduce_rows_warp();
-int occupancy_reduce_cols(int variant);
+int occupancy_reduce_contig(int variant, int op);
+int occupancy_reduce_rows_warp(int op);
+int occupancy_reduce_cols(int variant, int op);
 int occupancy_rscan_rows(int variant);
 int occupancy_rscan_lookback(int variant);
 int occupancy_scan_cols(int variant);

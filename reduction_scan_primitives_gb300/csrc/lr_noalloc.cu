@@ -61,7 +61,7 @@ int setup(int dev, NoAllocDevice** out) {
     int sms = 0, occ = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return record_cuda_error(e);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_reduce_contig<16>, kThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_reduce_contig<16, OpSum>, kThreads, 0);
     if (e != cudaSuccess) return record_cuda_error(e);
     d.scratch = static_cast<unsigned char*>(p);
     d.slots = (int64_t)sms * std::max(1, occ);
@@ -110,8 +110,8 @@ extern "C" int reduce_sum_f32_noalloc(const float* x, int64_t n, float* out,
     e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
     if (e != cudaSuccess) return record_cuda_error(e);
   }
-  ContigParams p{x, n, chunk_len, (int32_t)chunks, out, partials, ticket};
-  k_reduce_contig<16><<<dim3((unsigned)chunks), kThreads, 0, s>>>(p);
+  ContigParams p{x, n, chunk_len, (int32_t)chunks, out, partials, ticket, kEpiNone};
+  k_reduce_contig<16, OpSum><<<dim3((unsigned)chunks), kThreads, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return record_cuda_error(e);
   count_launch();

@@ -1,5 +1,5 @@
-// lr_reduce.cu -- fp32 sum kernels: 1D sum, row sums (inner == 1) and axis
-// sums with inner > 1 (sm_103a).
+// lr_reduce.cu -- fp32 reduction kernels: 1D, rows (inner == 1) and strided
+// axes (inner > 1), for sum, sum of squares, max and min (sm_103a).
 //
 // Design, by source:
 //  * "High-Performance Reduction Kernels" README, 'Key design decisions':
@@ -17,6 +17,9 @@
 //    run across the contiguous inner dim (coalesced) and loop over the reduce
 //    dim, several rows in flight; float4 columns only when inner % 4 == 0,
 //    because an odd row stride breaks 16-byte alignment of later rows.
+#include <algorithm>
+#include <type_traits>
+
 #include "lr_contig.cuh"
 #include "lr_device.cuh"
 #include "lr_internal.h"
@@ -27,23 +30,24 @@ namespace {
 // ---------------------------------------------------------------------------
 // Short rows: one warp per row, rows strided over the grid.
 // ---------------------------------------------------------------------------
+template <typename Op>
 __global__ void __launch_bounds__(kThreads) k_reduce_rows_warp(RowsWarpParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t first = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
   for (int64_t row = first; row < p.rows; row += nwarps) {
     const float* a = p.x + row * p.len;
-    BlockedAcc<kFold> acc;
+    BlockedAcc<kFold, Op> acc;
     int64_t j = lane;
     for (; j + 7 * 32 < p.len; j += 8 * 32) {
       float r[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) r[u] = ld_stream1(a + j + u * 32);
-      acc.add(tree_sum<8>(r));
+      for (int u = 0; u < 8; ++u) r[u] = Op::prep(ld_stream1(a + j + u * 32));
+      acc.add(tree_reduce<Op, 8>(r));
     }
-    for (; j < p.len; j += 32) acc.add(ld_stream1(a + j));
-    const float v = warp_sum(acc.total());
-    if (lane == 0) p.out[row] = v;
+    for (; j < p.len; j += 32) acc.add(Op::prep(ld_stream1(a + j)));
+    const float v = warp_reduce<Op>(acc.total());
+    if (lane == 0) p.out[row] = finish(v, p.epi, p.len);
   }
 }
 
@@ -56,7 +60,7 @@ struct ColsShape {
   static constexpr int CW = WX * 32 * VEC;     // columns per block
 };
 
-template <int VEC, int WY, int U>
+template <int VEC, int WY, int U, typename Op>
 __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
   using Sh = ColsShape<VEC, WY>;
   constexpr int WX = Sh::WX;
@@ -81,11 +85,11 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
 
   float res[VEC];
 #pragma unroll
-  for (int c = 0; c < VEC; ++c) res[c] = 0.f;
+  for (int c = 0; c < VEC; ++c) res[c] = Op::identity();
 
   if (col < inner) {
     const float* xc = p.x + o * p.reduce * inner + col;
-    BlockedAcc<kFold> acc[VEC];
+    BlockedAcc<kFold, Op> acc[VEC];
     int64_t r = r0 + wy;
     for (; r + (U - 1) * WY < r1; r += U * WY) {
       if constexpr (VEC == 4) {
@@ -95,29 +99,29 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
         float e[4][U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          e[0][u] = q[u].x;
-          e[1][u] = q[u].y;
-          e[2][u] = q[u].z;
-          e[3][u] = q[u].w;
+          e[0][u] = Op::prep(q[u].x);
+          e[1][u] = Op::prep(q[u].y);
+          e[2][u] = Op::prep(q[u].z);
+          e[3][u] = Op::prep(q[u].w);
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[c].add(tree_sum<U>(e[c]));
+        for (int c = 0; c < 4; ++c) acc[c].add(tree_reduce<Op, U>(e[c]));
       } else {
         float q[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) q[u] = ld_stream1(xc + (r + u * WY) * inner);
-        acc[0].add(tree_sum<U>(q));
+        for (int u = 0; u < U; ++u) q[u] = Op::prep(ld_stream1(xc + (r + u * WY) * inner));
+        acc[0].add(tree_reduce<Op, U>(q));
       }
     }
     for (; r < r1; r += WY) {
       if constexpr (VEC == 4) {
         const float4 q = ld_stream4(xc + r * inner);
-        acc[0].add(q.x);
-        acc[1].add(q.y);
-        acc[2].add(q.z);
-        acc[3].add(q.w);
+        acc[0].add(Op::prep(q.x));
+        acc[1].add(Op::prep(q.y));
+        acc[2].add(Op::prep(q.z));
+        acc[3].add(Op::prep(q.w));
       } else {
-        acc[0].add(ld_stream1(xc + r * inner));
+        acc[0].add(Op::prep(ld_stream1(xc + r * inner)));
       }
     }
 #pragma unroll
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
         float v[WY];
 #pragma unroll
         for (int k = 0; k < WY; ++k) v[k] = sh[k * CW + jloc + c];
-        res[c] = tree_sum<WY>(v);
+        res[c] = tree_reduce<Op, WY>(v);
       }
     }
   }
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
       float* outp = p.out + o * inner;
 #pragma unroll
       for (int c = 0; c < VEC; ++c)
-        if (col + c < inner) outp[col + c] = res[c];
+        if (col + c < inner) outp[col + c] = finish(res[c], p.epi, p.reduce);
     }
     return;
   }
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
   constexpr int G = kThreads / Q;      // slice groups
   const int q = threadIdx.x % Q;
   const int g = threadIdx.x / Q;
-  BlockedAcc<kFold> acc4[4];
+  BlockedAcc<kFold, Op> acc4[4];
   {
     int64_t k = g;
     const int64_t S = p.splits;
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
         e[3][u] = r[u].w;
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc4[c].add(tree_sum<4>(e[c]));
+      for (int c = 0; c < 4; ++c) acc4[c].add(tree_reduce<Op, 4>(e[c]));
     }
     for (; k < S; k += G) {
       const float4 r = ld_cg4(part_base + k * slice_stride + 4 * q);
@@ -212,9 +216,9 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
       float v[G];
 #pragma unroll
       for (int k = 0; k < G; ++k) v[k] = sh[k * CW + 4 * q + c];
-      const float tot = tree_sum<G>(v);
+      const float tot = tree_reduce<Op, G>(v);
       const int64_t cc = ct * CW + 4 * q + c;
-      if (cc < inner) outp[cc] = tot;
+      if (cc < inner) outp[cc] = finish(tot, p.epi, p.reduce);
     }
     if (threadIdx.x == 0) p.tickets[o * p.col_tiles + ct] = 0u;
   }
@@ -223,11 +227,50 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
 // Unroll depth (rows or vectors in flight per thread) of each variant.
 constexpr int kColsU = 8;
 
+__global__ void k_fill(float* out, int64_t n, float value) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = value;
+}
+
 template <typename K>
 int occupancy_of(K kernel) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess) return 0;
   return n;
+}
+
+template <typename Op>
+cudaError_t contig_op(int variant, const ContigParams& p, dim3 g, cudaStream_t s) {
+  if constexpr (std::is_same<Op, OpSum>::value) {
+    switch (variant) {
+      case kContigU4: k_reduce_contig<4, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
+      case kContigU8: k_reduce_contig<8, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
+      default: break;
+    }
+  }
+  if (variant != kContigU16) return cudaErrorInvalidValue;
+  k_reduce_contig<16, Op><<<g, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename Op>
+cudaError_t cols_op(int variant, const ColsParams& p, dim3 g, cudaStream_t s) {
+  if constexpr (std::is_same<Op, OpSum>::value) {
+    switch (variant) {
+      case kColsV1W1: k_reduce_cols<1, 1, kColsU, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
+      case kColsV1W8: k_reduce_cols<1, 8, kColsU, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
+      case kColsV4W1: k_reduce_cols<4, 1, kColsU, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
+      case kColsV4W8: k_reduce_cols<4, 8, kColsU, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
+      default: break;
+    }
+  }
+  switch (variant) {
+    case kColsV1W4: k_reduce_cols<1, 4, kColsU, Op><<<g, kThreads, 0, s>>>(p); break;
+    case kColsV4W4: k_reduce_cols<4, 4, kColsU, Op><<<g, kThreads, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -244,55 +287,102 @@ int cols_block_width(int variant) {
   }
 }
 
-cudaError_t launch_reduce_contig(int variant, const ContigParams& p, int64_t grid, cudaStream_t s) {
+cudaError_t launch_reduce_contig(int variant, int op, const ContigParams& p, int64_t grid,
+                                 cudaStream_t s) {
   const dim3 g((unsigned)grid);
-  switch (variant) {
-    case kContigU4: k_reduce_contig<4><<<g, kThreads, 0, s>>>(p); break;
-    case kContigU8: k_reduce_contig<8><<<g, kThreads, 0, s>>>(p); break;
-    case kContigU16: k_reduce_contig<16><<<g, kThreads, 0, s>>>(p); break;
+  switch (op) {
+    case kOpSum: return contig_op<OpSum>(variant, p, g, s);
+    case kOpSumSq: return contig_op<OpSumSq>(variant, p, g, s);
+    case kOpMax: return contig_op<OpMax>(variant, p, g, s);
+    case kOpMin: return contig_op<OpMin>(variant, p, g, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_reduce_rows_warp(int op, const RowsWarpParams& p, int64_t grid, cudaStream_t s) {
+  const dim3 g((unsigned)grid);
+  switch (op) {
+    case kOpSum: k_reduce_rows_warp<OpSum><<<g, kThreads, 0, s>>>(p); break;
+    case kOpSumSq: k_reduce_rows_warp<OpSumSq><<<g, kThreads, 0, s>>>(p); break;
+    case kOpMax: k_reduce_rows_warp<OpMax><<<g, kThreads, 0, s>>>(p); break;
+    case kOpMin: k_reduce_rows_warp<OpMin><<<g, kThreads, 0, s>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_reduce_rows_warp(const RowsWarpParams& p, int64_t grid, cudaStream_t s) {
-  k_reduce_rows_warp<<<dim3((unsigned)grid), kThreads, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_reduce_cols(int variant, const ColsParams& p, int64_t grid, cudaStream_t s) {
+cudaError_t launch_reduce_cols(int variant, int op, const ColsParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
-  switch (variant) {
-    case kColsV1W1: k_reduce_cols<1, 1, kColsU><<<g, kThreads, 0, s>>>(p); break;
-    case kColsV1W4: k_reduce_cols<1, 4, kColsU><<<g, kThreads, 0, s>>>(p); break;
-    case kColsV1W8: k_reduce_cols<1, 8, kColsU><<<g, kThreads, 0, s>>>(p); break;
-    case kColsV4W1: k_reduce_cols<4, 1, kColsU><<<g, kThreads, 0, s>>>(p); break;
-    case kColsV4W4: k_reduce_cols<4, 4, kColsU><<<g, kThreads, 0, s>>>(p); break;
-    case kColsV4W8: k_reduce_cols<4, 8, kColsU><<<g, kThreads, 0, s>>>(p); break;
+  switch (op) {
+    case kOpSum: return cols_op<OpSum>(variant, p, g, s);
+    case kOpSumSq: return cols_op<OpSumSq>(variant, p, g, s);
+    case kOpMax: return cols_op<OpMax>(variant, p, g, s);
+    case kOpMin: return cols_op<OpMin>(variant, p, g, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_fill(float* out, int64_t n, float value, cudaStream_t s) {
+  const int64_t blocks = std::min<int64_t>((n + kThreads - 1) / kThreads, 4096);
+  k_fill<<<dim3((unsigned)std::max<int64_t>(1, blocks)), kThreads, 0, s>>>(out, n, value);
   return cudaGetLastError();
 }
 
-int occupancy_reduce_contig(int variant) {
-  switch (variant) {
-    case kContigU4: return occupancy_of(k_reduce_contig<4>);
-    case kContigU8: return occupancy_of(k_reduce_contig<8>);
-    case kContigU16: return occupancy_of(k_reduce_contig<16>);
+namespace {
+
+template <typename Op>
+int occ_contig(int variant) {
+  if constexpr (std::is_same<Op, OpSum>::value) {
+    if (variant == kContigU4) return occupancy_of(k_reduce_contig<4, Op>);
+    if (variant == kContigU8) return occupancy_of(k_reduce_contig<8, Op>);
+  }
+  return variant == kContigU16 ? occupancy_of(k_reduce_contig<16, Op>) : 0;
+}
+
+template <typename Op>
+int occ_cols(int variant) {
+  if constexpr (std::is_same<Op, OpSum>::value) {
+    switch (variant) {
+      case kColsV1W1: return occupancy_of(k_reduce_cols<1, 1, kColsU, Op>);
+      case kColsV1W8: return occupancy_of(k_reduce_cols<1, 8, kColsU, Op>);
+      case kColsV4W1: return occupancy_of(k_reduce_cols<4, 1, kColsU, Op>);
+      case kColsV4W8: return occupancy_of(k_reduce_cols<4, 8, kColsU, Op>);
+      default: break;
+    }
+  }
+  if (variant == kColsV1W4) return occupancy_of(k_reduce_cols<1, 4, kColsU, Op>);
+  if (variant == kColsV4W4) return occupancy_of(k_reduce_cols<4, 4, kColsU, Op>);
+  return 0;
+}
+
+}  // namespace
+
+int occupancy_reduce_contig(int variant, int op) {
+  switch (op) {
+    case kOpSum: return occ_contig<OpSum>(variant);
+    case kOpSumSq: return occ_contig<OpSumSq>(variant);
+    case kOpMax: return occ_contig<OpMax>(variant);
+    case kOpMin: return occ_contig<OpMin>(variant);
     default: return 0;
   }
 }
 
-int occupancy_reduce_rows_warp() { return occupancy_of(k_reduce_rows_warp); }
+int occupancy_reduce_rows_warp(int op) {
+  switch (op) {
+    case kOpSum: return occupancy_of(k_reduce_rows_warp<OpSum>);
+    case kOpSumSq: return occupancy_of(k_reduce_rows_warp<OpSumSq>);
+    case kOpMax: return occupancy_of(k_reduce_rows_warp<OpMax>);
+    case kOpMin: return occupancy_of(k_reduce_rows_warp<OpMin>);
+    default: return 0;
+  }
+}
 
-int occupancy_reduce_cols(int variant) {
-  switch (variant) {
-    case kColsV1W1: return occupancy_of(k_reduce_cols<1, 1, kColsU>);
-    case kColsV1W4: return occupancy_of(k_reduce_cols<1, 4, kColsU>);
-    case kColsV1W8: return occupancy_of(k_reduce_cols<1, 8, kColsU>);
-    case kColsV4W1: return occupancy_of(k_reduce_cols<4, 1, kColsU>);
-    case kColsV4W4: return occupancy_of(k_reduce_cols<4, 4, kColsU>);
-    case kColsV4W8: return occupancy_of(k_reduce_cols<4, 8, kColsU>);
+int occupancy_reduce_cols(int variant, int op) {
+  switch (op) {
+    case kOpSum: return occ_cols<OpSum>(variant);
+    case kOpSumSq: return occ_cols<OpSumSq>(variant);
+    case kOpMax: return occ_cols<OpMax>(variant);
+    case kOpMin: return occ_cols<OpMin>(variant);
     default: return 0;
   }
 }

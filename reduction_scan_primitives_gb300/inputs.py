@@ -78,6 +78,14 @@ WORKLOADS = {
                                   exclusive=True, dist="uniform01", seed=3),
     "cumsum_128x4096x4095_d1": dict(op="cumsum", shape=(128, 4096, 4095), dim=1, reverse=False,
                                     exclusive=False, dist="normal", seed=7),
+    # Other reductions on the same shapes.
+    "max_1e9": dict(op="reduce", rop="max", shape=(1_000_000_000,), dist="uniform01", seed=42),
+    "norm_128x4096x4095_d1": dict(op="reduce", rop="norm", shape=(128, 4096, 4095), dim=1,
+                                  dist="normal", seed=7),
+    "mean_4096x65536_d1": dict(op="reduce", rop="mean", shape=(4096, 65536), dim=1,
+                               dist="uniform_pm1", seed=11),
+    "min_65536x4096_d0": dict(op="reduce", rop="min", shape=(65536, 4096), dim=0,
+                              dist="uniform_pm1", seed=11),
 }
 
 # The 1D sweep sizes of the sum benchmark (uniform[0,1), seed 42).
@@ -98,9 +106,11 @@ def algorithmic_bytes(w: dict) -> int:
     n = math.prod(w["shape"])
     if w["op"] == "sum":
         return 4 * n + 4
-    if w["op"] == "axis":
+    if w["op"] in ("axis", "reduce") and "dim" in w:
         outer, _, inner = canonical_axis(w["shape"], w["dim"])
         return 4 * n + 4 * outer * inner
+    if w["op"] == "reduce":
+        return 4 * n + 4
     if w["op"] in ("rcumsum", "cumsum"):
         return 8 * n
     raise ValueError(w["op"])

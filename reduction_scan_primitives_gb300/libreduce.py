@@ -24,6 +24,8 @@ ERR_ALIAS = 3
 ERR_CUDA = 4
 ERR_TIMEOUT = 5
 
+OPS = {"sum": 0, "mean": 1, "max": 2, "min": 3, "norm": 4}
+
 SCAN_REVERSE = 1
 SCAN_EXCLUSIVE = 2
 
@@ -84,6 +86,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.reduce_sum_f32_noalloc.restype = i32
     lib.reduce_axis_f32.argtypes = [vp, i64, i64, i64, vp, vp]
     lib.reduce_axis_f32.restype = i32
+    lib.reduce_f32.argtypes = [vp, i64, vp, i32, vp]
+    lib.reduce_f32.restype = i32
+    lib.reduce_axis_op_f32.argtypes = [vp, i64, i64, i64, vp, i32, vp]
+    lib.reduce_axis_op_f32.restype = i32
     lib.reverse_cumsum_f32.argtypes = [vp, i64, i64, vp, vp]
     lib.reverse_cumsum_f32.restype = i32
     lib.cumsum_f32.argtypes = [vp, i64, i64, i64, vp, ctypes.c_uint, vp]
@@ -179,6 +185,56 @@ def reduce_axis_f32(x: torch.Tensor, dim: int, keepdim: bool = False,
         st = lib.reduce_axis_f32(x.data_ptr(), outer, reduce, inner, out.data_ptr(),
                                  _stream_ptr(x.device))
     _raise_on("reduce_axis_f32", st)
+    return out
+
+
+def _op_code(op) -> int:
+    if isinstance(op, str):
+        if op not in OPS:
+            raise ValueError(f"unknown reduction {op!r}; one of {sorted(OPS)}")
+        return OPS[op]
+    return int(op)
+
+
+def reduce_f32(x: torch.Tensor, op="sum", out: torch.Tensor | None = None) -> torch.Tensor:
+    """Reduction of every element of x: "sum", "mean", "max", "min" or "norm"."""
+    _check_tensor(x, "x")
+    if out is None:
+        out = torch.empty((), dtype=torch.float32, device=x.device)
+    else:
+        _check_tensor(out, "out")
+        if out.numel() != 1 or out.device != x.device:
+            raise ValueError("out must hold one float on x's device")
+    lib = load()
+    with torch.cuda.device(x.device):
+        st = lib.reduce_f32(x.data_ptr(), x.numel(), out.data_ptr(), _op_code(op), _stream_ptr(x.device))
+    _raise_on("reduce_f32", st)
+    return out
+
+
+def reduce_axis_op_f32(x: torch.Tensor, dim: int, op="sum", keepdim: bool = False,
+                       out: torch.Tensor | None = None) -> torch.Tensor:
+    """Reduction of x along `dim`: "sum", "mean", "max", "min" or "norm"."""
+    _check_tensor(x, "x")
+    outer, reduce, inner = canonical_axis(x.shape, dim)
+    shape = list(x.shape)
+    if x.dim():
+        d = dim % x.dim()
+        if keepdim:
+            shape[d] = 1
+        else:
+            del shape[d]
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=x.device)
+    else:
+        _check_tensor(out, "out")
+        if out.numel() != outer * inner or out.device != x.device:
+            raise ValueError("out has the wrong size or device")
+    lib = load()
+    with torch.cuda.device(x.device):
+        st = lib.reduce_axis_op_f32(x.data_ptr(), outer, reduce, inner, out.data_ptr(), _op_code(op),
+                                    _stream_ptr(x.device))
+    _raise_on("reduce_axis_op_f32", st)
     return out
 
 

@@ -71,6 +71,16 @@ def test_cumsum_arguments(lib):
     assert lib.cumsum_f32(FAKE, 3, 0, 5, FAKE, 3, NULL) == L.OK  # empty: no-op
 
 
+def test_reduce_op_arguments(lib):
+    E = L.ERR_INVALID_ARG
+    assert lib.reduce_f32(FAKE, 16, FAKE + 4096, 9, NULL) == E  # unknown op
+    assert lib.reduce_f32(FAKE, 16, FAKE + 4096, -1, NULL) == E
+    assert lib.reduce_axis_op_f32(FAKE, 2, 3, 4, FAKE + 4096, 5, NULL) == E
+    assert lib.reduce_axis_op_f32(FAKE, 2, 3, 4, FAKE + 4, L.OPS["max"], NULL) == L.ERR_ALIAS
+    assert lib.reduce_axis_op_f32(FAKE, 0, 3, 4, FAKE, L.OPS["min"], NULL) == L.OK  # nothing to write
+    assert lib.reduce_f32(NULL, 3, FAKE, L.OPS["mean"], NULL) == E
+
+
 def test_overflow_rejected(lib):
     big = 1 << 62
     assert lib.reduce_axis_f32(FAKE, big, big, 2, FAKE, NULL) == L.ERR_OVERFLOW

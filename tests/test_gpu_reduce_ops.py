@@ -1,0 +1,115 @@
+"""reduce_f32 / reduce_axis_op_f32 (mean, max, min, norm) against the oracle
+(GPU).  Sum is covered by test_gpu_sum / test_gpu_axis."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import libreduce_defaults, on_device  # noqa: F401
+from parity import bitwise_equal, to_np
+from reduction_scan_primitives_gb300 import inputs
+from reduction_scan_primitives_gb300 import libreduce as L
+
+pytestmark = pytest.mark.gpu
+OPS = ["mean", "max", "min", "norm"]
+
+
+def assert_op_close(gpu, ref, scale, op, count, what):
+    """mean: (1e-5 sum|x| + 1e-6) / count plus one fp32 rounding; norm:
+    1e-5 norm + 1e-6; max and min: exact (NaN for NaN)."""
+    g = np.asarray(to_np(gpu), np.float64).reshape(-1)
+    r = np.asarray(ref, np.float64).reshape(-1)
+    sc = np.asarray(scale, np.float64).reshape(-1)
+    nan = np.isnan(r)
+    assert np.array_equal(np.isnan(g), nan), f"{what}: NaN pattern differs"
+    g, r, sc = g[~nan], r[~nan], sc[~nan]
+    if op in ("max", "min"):
+        bad = np.flatnonzero(g != r)
+        assert bad.size == 0, f"{what}: {bad.size} differ, first {bad[0]}: {g[bad[0]]} vs {r[bad[0]]}"
+        return
+    if op == "mean":
+        tol = (1e-5 * sc + 1e-6) / max(count, 1) + 2.0 ** -24 * np.abs(r)
+    else:
+        tol = 1e-5 * r + 1e-6
+    fin = np.isfinite(r)
+    bad = np.flatnonzero(fin & ~(np.abs(g - r) <= tol))
+    assert bad.size == 0, f"{what}: {bad.size} out of tolerance, first {bad[0]}: {g[bad[0]]} vs {r[bad[0]]}"
+    assert np.array_equal(g[~fin], r[~fin])
+
+
+def check_axis(shape, dim, op, dist="normal", seed=5, offset=0):
+    x = inputs.make(shape, dist, seed)
+    o, r, i = L.canonical_axis(x.shape, dim)
+    ref, scale = oracle.reduce_op(x.numpy(), o, r, i, op)
+    got = L.reduce_axis_op_f32(on_device(x, offset), dim, op)
+    assert_op_close(got, ref, scale, op, r, f"{op} {shape} dim={dim} off={offset}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("n", [1, 3, 1000, 8193, 1_000_003, 50_000_000])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_1d(op, n, offset):
+    x = inputs.make((n,), "uniform_pm1", 40 + n % 7)
+    ref, scale = oracle.reduce_op(x.numpy(), 1, n, 1, op)
+    got = L.reduce_f32(on_device(x, offset), op)
+    assert_op_close(got, ref, scale, op, n, f"{op} n={n} off={offset}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("shape,dim", [((64, 1000), 1), ((300, 2049), 1), ((70, 65536), 1), ((5, 300001), 1),
+                                       ((128, 512, 257), 1), ((4, 3000, 4096), 1), ((65536, 64), 0),
+                                       ((2, 777, 4095), 1), ((6, 5, 4, 3), 2)])
+def test_axis(op, shape, dim):
+    check_axis(shape, dim, op)
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_axis_split_and_misaligned(op):
+    check_axis((1, 65536, 1024), 1, op)     # split reduce axis, last-block combine
+    check_axis((3, 2000, 36), 1, op, offset=1)  # scalar columns on a misaligned base
+
+
+@pytest.mark.parametrize("op", ["max", "min"])
+def test_nan_propagates(op):
+    x = inputs.make((4, 5000), "uniform01", 2)
+    x[2, 4321] = float("nan")
+    got = L.reduce_axis_op_f32(on_device(x), 1, op).cpu().numpy()
+    assert np.isnan(got[2]) and np.isfinite(np.delete(got, 2)).all()
+    y = inputs.make((3_000_000,), "uniform01", 2)
+    y[1_234_567] = float("nan")
+    assert math.isnan(L.reduce_f32(on_device(y), op).item())
+
+
+def test_empty_values():
+    x = torch.empty((3, 0, 2), device="cuda")
+    want = {"sum": 0.0, "mean": float("nan"), "max": -float("inf"), "min": float("inf"), "norm": 0.0}
+    for op, v in want.items():
+        got = L.reduce_axis_op_f32(x, 1, op).cpu().numpy()
+        if math.isnan(v):
+            assert np.isnan(got).all(), op
+        else:
+            assert (got == v).all(), op
+
+
+def test_integer_inputs():
+    x = inputs.make((16, 4096, 36), "int:-8:8", 9)
+    for op in ("max", "min"):
+        ref, _ = oracle.reduce_op(x.numpy(), 16, 4096, 36, op)
+        assert np.array_equal(L.reduce_axis_op_f32(on_device(x), 1, op).cpu().numpy().reshape(-1), ref.reshape(-1))
+    xi = x.numpy().astype(np.int64)
+    ss = (xi * xi).sum(axis=1).astype(np.float64)  # exact in fp32 as well (< 2^24)
+    got = L.reduce_axis_op_f32(on_device(x), 1, "norm").cpu().numpy()
+    assert np.array_equal(got, np.sqrt(ss).astype(np.float32))
+
+
+def test_deterministic_bitwise():
+    xd = on_device(inputs.make((4096, 4096), "normal", 1))
+    for op in OPS:
+        for dim in (0, 1):
+            a = L.reduce_axis_op_f32(xd, dim, op).clone()
+            b = L.reduce_axis_op_f32(xd, dim, op).clone()
+            assert bitwise_equal(a, b), (op, dim)
+        a = L.reduce_f32(xd, op).clone()
+        assert bitwise_equal(a, L.reduce_f32(xd, op)), op
