@@ -47,7 +47,8 @@ STEP_WORKLOADS = ["sum_1e9", "axis_128x4096x4095_d1", "axis_4096x65536_d1", "axi
                   "rcumsum_32768x32768", "rcumsum_1x1e9"]
 # Follow-on forms, timed separately from the step (reported under next_rows).
 NEXT_WORKLOADS = ["cumsum_fwd_32768x32768", "cumsum_fwd_excl_1x1e9", "cumsum_128x4096x4095_d1",
-                  "max_1e9", "norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0"]
+                  "max_1e9", "norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0",
+                  "rcumsum_1x1e9_ws", "axis_65536x4096_d0_ws"]
 # Small cases of each kernel for ncu captures: larger than L2, a few GB at most.
 PROFILE_CASES = {
     "sum_2e8": dict(op="sum", shape=(200_000_000,), dist="uniform01", seed=42),
@@ -205,6 +206,13 @@ def make_call(name, x, out):
         return lambda: L.reduce_sum_f32(x, out=out)
     if w["op"] == "axis":
         return lambda: L.reduce_axis_f32(x, w["dim"], out=out)
+    if w.get("ws"):
+        # Caller-provided scratch, sized by the query call and reused every step.
+        if w["op"] == "cumsum":
+            ws = L.workspace(L.cumsum_ws_f32(x, w["dim"], w["reverse"], w["exclusive"], out=out))
+            return lambda: L.cumsum_ws_f32(x, w["dim"], w["reverse"], w["exclusive"], ws=ws, out=out)
+        ws = L.workspace(L.reduce_axis_op_ws_f32(x, w["dim"], w["rop"], out=out))
+        return lambda: L.reduce_axis_op_ws_f32(x, w["dim"], w["rop"], ws=ws, out=out)
     if w["op"] == "cumsum":
         return lambda: L.cumsum_f32(x, w["dim"], reverse=w["reverse"], exclusive=w["exclusive"], out=out)
     if w["op"] == "reduce":

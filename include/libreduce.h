@@ -26,7 +26,8 @@
  *    call on that device that needs it, so that first call must not be made
  *    inside a stream capture.  Because the workspace is shared, calls on one
  *    device must not run concurrently on different streams; calls queued on
- *    one stream are always safe.
+ *    one stream are always safe.  The *_ws variants take the scratch from
+ *    the caller instead and lift this limit.
  *  - Errors: validation happens before any work is queued, and a failed call
  *    queues nothing.  LIBREDUCE_ERR_CUDA means a CUDA runtime call failed; its
  *    code is available from libreduce_last_cuda_error().  Device-side errors
@@ -171,6 +172,37 @@ LIBREDUCE_API int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, fl
 #define LIBREDUCE_SCAN_EXCLUSIVE 2u
 LIBREDUCE_API int cumsum_f32(const float* x, int64_t outer, int64_t N, int64_t inner, float* y,
                              unsigned flags, libreduce_stream_t stream);
+
+/*
+ * Workspace variants (the two-call temporary-storage idiom of the CUB
+ * DeviceReduce::Sum example on the "Seven-step reduction" page).  They compute
+ * exactly what reduce_axis_op_f32 / cumsum_f32 compute, with the same bits,
+ * but take their scratch from a caller buffer instead of the library's
+ * per-device workspace, so calls with different workspaces may run
+ * concurrently on different streams.
+ *   ws == NULL:  nothing is queued; *ws_bytes receives the bytes needed: at
+ *                least 256 (the header with the call's error word), more when
+ *                the call needs partial sums, tickets or look-back flags; 0 for
+ *                a call with nothing to compute.  x, y/out and the sizes must be
+ *                the ones of the real call (alignment picks the kernels).
+ *   ws != NULL:  device memory of the current device, 256-byte aligned, at
+ *                least *ws_bytes long (INVALID_ARG if smaller than needed).  The
+ *                call clears the parts that must start at zero on `stream`, so
+ *                the buffer needs no preparation and may be reused at once.
+ *                Its first bytes hold the call's device error word: read it
+ *                with libreduce_check_ws(ws, stream).
+ * A workspace must not be used by two calls that may overlap on the GPU.
+ * Errors: as the plain call; INVALID_ARG for ws_bytes == NULL, a misaligned
+ * or too small workspace.
+ */
+LIBREDUCE_API int reduce_axis_op_ws_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner,
+                                        float* out, int op, void* ws, size_t* ws_bytes,
+                                        libreduce_stream_t stream);
+LIBREDUCE_API int cumsum_ws_f32(const float* x, int64_t outer, int64_t N, int64_t inner, float* y,
+                                unsigned flags, void* ws, size_t* ws_bytes, libreduce_stream_t stream);
+/* libreduce_check for a workspace call: synchronise `stream`, return and clear
+ * the error word in `ws` (LIBREDUCE_OK or LIBREDUCE_ERR_TIMEOUT). */
+LIBREDUCE_API int libreduce_check_ws(void* ws, libreduce_stream_t stream);
 
 /*
  * reduce_sum_f32_noalloc -- out[0] = sum_{i<n} x[i], allocating nothing.

@@ -219,9 +219,92 @@ int contig_variant() {
   return (v >= 0 && v < kNumContigVariants) ? (int)v : kContigU16;
 }
 
+// ---------------------------------------------------------------------------
+// Scratch.  Every strategy first states what it needs; a provider then hands
+// it out from the library's per-device workspace or from a caller buffer
+// (the *_ws entry points).  The plan never depends on the provider, so both
+// give bit-identical results.
+// ---------------------------------------------------------------------------
+struct Need {
+  int64_t tickets = 0;   // u32, zero on entry
+  int64_t partials = 0;  // f32
+  int64_t nodes = 0;     // u64 look-back words, zero (or stale-epoch) on entry
+  bool header = false;   // error / abort / ticket-counter words
+};
+
+struct Scratch {
+  unsigned* header = nullptr;
+  unsigned* tickets = nullptr;
+  float* partials = nullptr;
+  unsigned long long* nodes = nullptr;
+  unsigned epoch = 0;
+};
+
+struct Provider {
+  DeviceState* st = nullptr;
+  char* ws = nullptr;        // caller workspace, or null for the library's own
+  size_t ws_bytes = 0;
+  size_t* query = nullptr;   // size query: store the bytes needed, launch nothing
+};
+
+constexpr int kQueried = -1;  // internal: a size query was answered
+
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Caller-workspace layout: [header 256 B][tickets][partials][nodes], each part
+// 256-byte aligned.
+void ws_layout(const Need& n, size_t* off_t, size_t* off_p, size_t* off_n, size_t* total) {
+  *off_t = kHeaderBytes;
+  *off_p = *off_t + align256(sizeof(unsigned) * (size_t)n.tickets);
+  *off_n = *off_p + align256(sizeof(float) * (size_t)n.partials);
+  *total = *off_n + align256(sizeof(unsigned long long) * (size_t)n.nodes);
+}
+
+int acquire(const Provider& pv, const Need& need, Scratch* sc, cudaStream_t s) {
+  const bool any = need.tickets || need.partials || need.nodes || need.header;
+  if (pv.query) {
+    // A caller workspace always holds at least the header (its error word).
+    size_t a, b, c, total = 0;
+    ws_layout(need, &a, &b, &c, &total);
+    *pv.query = total;
+    return kQueried;
+  }
+  if (!pv.ws) {
+    if (!any) return LIBREDUCE_OK;
+    DeviceState* st = pv.st;
+    int rc = need.nodes ? ensure_lookback(st) : ensure_workspace(st);
+    if (rc) return rc;
+    sc->header = st->err_word;
+    sc->tickets = st->tickets;
+    sc->partials = st->partials;
+    sc->nodes = st->node_val;
+    if (need.nodes) {
+      unsigned epoch = st->epoch.fetch_add(1) + 1;
+      if (epoch == 0) epoch = st->epoch.fetch_add(1) + 1;  // 0 marks "never written"
+      sc->epoch = epoch;
+    }
+    return LIBREDUCE_OK;
+  }
+  size_t off_t, off_p, off_n, total;
+  ws_layout(need, &off_t, &off_p, &off_n, &total);
+  if (total > pv.ws_bytes) return LIBREDUCE_ERR_INVALID_ARG;  // workspace too small
+  // A caller workspace holds anything on entry: clear what must start at zero.
+  cudaError_t e = cudaMemsetAsync(pv.ws, 0, off_p, s);
+  if (e == cudaSuccess && need.nodes)
+    e = cudaMemsetAsync(pv.ws + off_n, 0, sizeof(unsigned long long) * (size_t)need.nodes, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  sc->header = reinterpret_cast<unsigned*>(pv.ws);
+  sc->tickets = reinterpret_cast<unsigned*>(pv.ws + off_t);
+  sc->partials = reinterpret_cast<float*>(pv.ws + off_p);
+  sc->nodes = reinterpret_cast<unsigned long long*>(pv.ws + off_n);
+  sc->epoch = 1;  // every node word was just cleared
+  return LIBREDUCE_OK;
+}
+
 // Reduction of `segments` contiguous segments of seg_len floats each.
-int run_contig(DeviceState* st, const float* x, int64_t segments, int64_t seg_len, float* out,
+int run_contig(const Provider& pv, const float* x, int64_t segments, int64_t seg_len, float* out,
                int op, int epi, cudaStream_t s) {
+  DeviceState* st = pv.st;
   const int variant = op == kOpSum ? contig_variant() : kContigU16;
   const int64_t slots = (int64_t)st->sm_count * st->occ_contig[variant][op];
   const int64_t waves = g_opt_waves.load();
@@ -252,26 +335,33 @@ int run_contig(DeviceState* st, const float* x, int64_t segments, int64_t seg_le
   }
   const int64_t grid = segments * chunks;
   if (grid > INT32_MAX) return LIBREDUCE_ERR_OVERFLOW;
-  ContigParams p{x, seg_len, chunk_len, (int32_t)chunks, out, nullptr, nullptr, epi};
+  Need need;
   if (chunks > 1) {
-    int rc = ensure_workspace(st);
-    if (rc) return rc;
-    p.partials = st->partials;
-    p.tickets = st->tickets;
+    need.tickets = segments;
+    need.partials = segments * chunks;
   }
+  Scratch sc;
+  int rc = acquire(pv, need, &sc, s);
+  if (rc) return rc;
+  ContigParams p{x, seg_len, chunk_len, (int32_t)chunks, out, sc.partials, sc.tickets, epi};
   return launched(launch_reduce_contig(variant, op, p, grid, s));
 }
 
-int run_rows_warp(DeviceState* st, const float* x, int64_t rows, int64_t len, float* out, int op,
+int run_rows_warp(const Provider& pv, const float* x, int64_t rows, int64_t len, float* out, int op,
                   int epi, cudaStream_t s) {
+  DeviceState* st = pv.st;
   const int64_t slots = (int64_t)st->sm_count * st->occ_rows_warp[op];
   const int64_t grid = std::max<int64_t>(1, std::min(ceil_div(rows, kThreads / 32), 8 * slots));
+  Scratch sc;
+  int rc = acquire(pv, Need{}, &sc, s);
+  if (rc) return rc;
   RowsWarpParams p{x, rows, len, out, epi};
   return launched(launch_reduce_rows_warp(op, p, grid, s));
 }
 
-int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int64_t inner,
+int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, int64_t inner,
              float* out, int op, int epi, cudaStream_t s) {
+  DeviceState* st = pv.st;
   const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
   int variant = vec4 ? kColsV4W4 : kColsV1W4;
   const int64_t forced_v = g_opt_cols_variant.load();
@@ -310,14 +400,16 @@ int run_cols(DeviceState* st, const float* x, int64_t outer, int64_t reduce, int
   }
   int64_t grid = 0;
   if (mul_overflows(base_blocks, splits, &grid) || grid > INT32_MAX) return LIBREDUCE_ERR_OVERFLOW;
-  ColsParams p{x, outer, reduce, inner, (int32_t)col_tiles, (int32_t)splits, rows_per_split,
-               out, nullptr, nullptr, epi};
+  Need need;
   if (splits > 1) {
-    int rc = ensure_workspace(st);
-    if (rc) return rc;
-    p.partials = st->partials;
-    p.tickets = st->tickets;
+    need.tickets = base_blocks;
+    need.partials = splits * base_blocks * cw;
   }
+  Scratch sc;
+  int rc = acquire(pv, need, &sc, s);
+  if (rc) return rc;
+  ColsParams p{x, outer, reduce, inner, (int32_t)col_tiles, (int32_t)splits, rows_per_split,
+               out, sc.partials, sc.tickets, epi};
   return launched(launch_reduce_cols(variant, op, p, grid, s));
 }
 
@@ -339,10 +431,13 @@ bool plan_op(int public_op, OpPlan* plan) {
   }
 }
 
+// Turn an internal status into the public one (a size query is a success).
+int finish_status(int rc) { return rc == kQueried ? LIBREDUCE_OK : rc; }
+
 // The reduction behind every reduce entry point: `out[o*inner + i]` is the
 // reduction of x[o, :, i] over the middle axis of [outer, reduce, inner].
 int reduce_impl(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
-                int public_op, cudaStream_t s) {
+                int public_op, Provider pv, cudaStream_t s) {
   OpPlan plan;
   if (!plan_op(public_op, &plan)) return LIBREDUCE_ERR_INVALID_ARG;
   if (outer < 0 || reduce < 0 || inner < 0) return LIBREDUCE_ERR_INVALID_ARG;
@@ -350,16 +445,20 @@ int reduce_impl(const float* x, int64_t outer, int64_t reduce, int64_t inner, fl
   if (mul_overflows(outer, inner, &n_out) || mul_overflows(n_out, reduce, &total) ||
       total > INT64_MAX / 4)
     return LIBREDUCE_ERR_OVERFLOW;
-  if (n_out == 0) return LIBREDUCE_OK;
+  if (n_out == 0) {
+    if (pv.query) *pv.query = 0;
+    return LIBREDUCE_OK;
+  }
   if (out == nullptr || (x == nullptr && total > 0)) return LIBREDUCE_ERR_INVALID_ARG;
   if (overlaps(x, (size_t)total * sizeof(float), out, (size_t)n_out * sizeof(float)))
     return LIBREDUCE_ERR_ALIAS;
-  DeviceState* st = nullptr;
   int dev = 0;
-  int rc = device_state(&st, &dev);
+  int rc = device_state(&pv.st, &dev);
   if (rc) return rc;
   if ((rc = check_buffer(out, (size_t)n_out * sizeof(float), dev))) return rc;
   if (total == 0) {
+    Scratch sc;
+    if ((rc = acquire(pv, Need{}, &sc, s))) return finish_status(rc);
     if (plan.empty == 0.f) {
       const cudaError_t e = cudaMemsetAsync(out, 0, (size_t)n_out * sizeof(float), s);
       return e == cudaSuccess ? LIBREDUCE_OK : fail_cuda(e);
@@ -368,12 +467,12 @@ int reduce_impl(const float* x, int64_t outer, int64_t reduce, int64_t inner, fl
   }
   if ((rc = check_buffer(x, (size_t)total * sizeof(float), dev))) return rc;
   if (inner == 1) {
-    if (outer == 1) return run_contig(st, x, 1, reduce, out, plan.op, plan.epi, s);
+    if (outer == 1) return finish_status(run_contig(pv, x, 1, reduce, out, plan.op, plan.epi, s));
     if (reduce <= kRowsWarpMaxLen && g_opt_axis_split.load() <= 0)
-      return run_rows_warp(st, x, outer, reduce, out, plan.op, plan.epi, s);
-    return run_contig(st, x, outer, reduce, out, plan.op, plan.epi, s);
+      return finish_status(run_rows_warp(pv, x, outer, reduce, out, plan.op, plan.epi, s));
+    return finish_status(run_contig(pv, x, outer, reduce, out, plan.op, plan.epi, s));
   }
-  return run_cols(st, x, outer, reduce, inner, out, plan.op, plan.epi, s);
+  return finish_status(run_cols(pv, x, outer, reduce, inner, out, plan.op, plan.epi, s));
 }
 
 constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): well under a second
@@ -384,24 +483,26 @@ constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): we
 constexpr int64_t kLookbackLagReverse = 768;
 constexpr int64_t kLookbackLagForward = 512;
 
-int run_rscan_lookback(DeviceState* st, const float* x, int64_t rows, int64_t N, float* y,
+int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
                        cudaStream_t s, int variant, int flags) {
   const int64_t tile = lookback_tile(variant);
   const int64_t tiles = ceil_div(N, tile);
   int64_t total = 0;
   if (mul_overflows(rows, tiles, &total) || total > kMaxLookbackTiles) return LIBREDUCE_ERR_OVERFLOW;
-  int rc = ensure_lookback(st);
+  Need need;
+  need.header = true;
+  need.nodes = 2 * total;
+  Scratch sc;
+  int rc = acquire(pv, need, &sc, s);
   if (rc) return rc;
-  unsigned epoch = st->epoch.fetch_add(1) + 1;
-  if (epoch == 0) epoch = st->epoch.fetch_add(1) + 1;  // 0 marks "never written"
-  unsigned* counter = st->err_word + 2;  // zero on entry; the block with the last ticket resets it
+  unsigned* counter = sc.header + 2;  // zero on entry; the block with the last ticket resets it
   const int64_t spin = g_opt_spin_limit.load();
   const int64_t lag_opt = g_opt_lookback_lag.load();
   const int64_t lag_default = (flags & kScanMirror) ? kLookbackLagForward : kLookbackLagReverse;
   const int64_t lag = variant == kLookbackL2 ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt : lag_default)
                                              : 0;
-  RScanLookbackParams p{x, y, rows, N, tiles, st->node_val, counter, st->err_word,
-                        epoch, spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag,
+  RScanLookbackParams p{x, y, rows, N, tiles, sc.nodes, counter, sc.header,
+                        sc.epoch, spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag,
                         flags};
   const int64_t grid = total + lag;  // one block per ticket
   return launched(launch_rscan_lookback(variant, p, grid, s));
@@ -409,8 +510,9 @@ int run_rscan_lookback(DeviceState* st, const float* x, int64_t rows, int64_t N,
 
 // Scans along rows (inner == 1).  `flags`: kScanMirror for a forward scan,
 // kScanExclusive to leave out each element's own term.
-int run_rscan_rows(DeviceState* st, const float* x, int64_t rows, int64_t N, float* y,
+int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
                    cudaStream_t s, int flags) {
+  DeviceState* st = pv.st;
   const bool vec4 = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
                     ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
   int variant = vec4 ? kRScanV4S4 : kRScanV1S4;
@@ -425,49 +527,77 @@ int run_rscan_rows(DeviceState* st, const float* x, int64_t rows, int64_t N, flo
   const int64_t row_slots = (int64_t)st->sm_count * st->occ_rscan[variant];
   const bool lookback_fits = rows <= kMaxLookbackTiles / std::max<int64_t>(1, lb_tiles);
   if (strategy >= 2 || (strategy == 0 && 4 * rows < row_slots && lb_tiles >= 4 && lookback_fits))
-    return run_rscan_lookback(st, x, rows, N, y, s, lb_variant, flags);
+    return run_rscan_lookback(pv, x, rows, N, y, s, lb_variant, flags);
+  Scratch sc;
+  int rc = acquire(pv, Need{}, &sc, s);
+  if (rc) return rc;
   const int64_t grid = std::min<int64_t>(rows, INT32_MAX);
   RScanRowsParams p{x, y, rows, N, flags};
   return launched(launch_rscan_rows(variant, p, grid, s));
 }
 
 // Scans along a strided axis (inner > 1): one thread per column group.
-int run_scan_cols(DeviceState* st, const float* x, int64_t outer, int64_t N, int64_t inner,
+int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
                   float* y, bool reverse, bool exclusive, cudaStream_t s) {
+  DeviceState* st = pv.st;
   const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
                     ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
   const int variant = vec4 ? kScanColsV4 : kScanColsV1;
   const int64_t groups = outer * ceil_div(inner, vec4 ? 4 : 1);
   const int64_t slots = (int64_t)st->sm_count * st->occ_scan_cols[variant];
   const int64_t grid = std::max<int64_t>(1, std::min(ceil_div(groups, kThreads), 8 * slots));
+  Scratch sc;
+  int rc = acquire(pv, Need{}, &sc, s);
+  if (rc) return rc;
   ScanColsParams p{x, y, outer, N, inner, reverse ? 1 : 0, exclusive ? 1 : 0};
   return launched(launch_scan_cols(variant, p, grid, s));
 }
 
-// The cumulative sum behind both scan entry points.
+// The cumulative sum behind every scan entry point.
 int cumsum_impl(const float* x, int64_t outer, int64_t N, int64_t inner, float* y, unsigned flags,
-                cudaStream_t s) {
+                Provider pv, cudaStream_t s) {
   if (outer < 0 || N < 0 || inner < 0) return LIBREDUCE_ERR_INVALID_ARG;
   if (flags & ~(LIBREDUCE_SCAN_REVERSE | LIBREDUCE_SCAN_EXCLUSIVE)) return LIBREDUCE_ERR_INVALID_ARG;
   int64_t rows = 0, total = 0;
   if (mul_overflows(outer, inner, &rows) || mul_overflows(rows, N, &total) || total > INT64_MAX / 4)
     return LIBREDUCE_ERR_OVERFLOW;
-  if (total == 0) return LIBREDUCE_OK;
+  if (total == 0) {
+    if (pv.query) *pv.query = 0;
+    return LIBREDUCE_OK;
+  }
   if (x == nullptr || y == nullptr) return LIBREDUCE_ERR_INVALID_ARG;
   const size_t bytes = (size_t)total * sizeof(float);
   if (overlaps(x, bytes, y, bytes)) return LIBREDUCE_ERR_ALIAS;
-  DeviceState* st = nullptr;
   int dev = 0;
-  int rc = device_state(&st, &dev);
+  int rc = device_state(&pv.st, &dev);
   if (rc) return rc;
   if ((rc = check_buffer(x, bytes, dev))) return rc;
   if ((rc = check_buffer(y, bytes, dev))) return rc;
   const bool reverse = (flags & LIBREDUCE_SCAN_REVERSE) != 0;
   const bool exclusive = (flags & LIBREDUCE_SCAN_EXCLUSIVE) != 0;
   if (inner == 1)
-    return run_rscan_rows(st, x, outer, N, y, s,
-                          (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0));
-  return run_scan_cols(st, x, outer, N, inner, y, reverse, exclusive, s);
+    return finish_status(run_rscan_rows(
+        pv, x, outer, N, y, s, (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0)));
+  return finish_status(run_scan_cols(pv, x, outer, N, inner, y, reverse, exclusive, s));
+}
+
+// Provider for the *_ws entry points: a size query when ws is null, else the
+// caller's buffer (device memory of the current device, 256-byte aligned).
+int ws_provider(void* ws, size_t* ws_bytes, Provider* pv) {
+  if (ws_bytes == nullptr) return LIBREDUCE_ERR_INVALID_ARG;
+  if (ws == nullptr) {
+    pv->query = ws_bytes;
+    return LIBREDUCE_OK;
+  }
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return LIBREDUCE_ERR_INVALID_ARG;
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  int rc = check_buffer(ws, *ws_bytes, dev);
+  if (rc) return rc;
+  pv->ws = static_cast<char*>(ws);
+  pv->ws_bytes = *ws_bytes;
+  return LIBREDUCE_OK;
 }
 
 }  // namespace
@@ -489,28 +619,45 @@ int reduce_sum_f32(const float* x, int64_t n, float* out, libreduce_stream_t str
 int reduce_f32(const float* x, int64_t n, float* out, int op, libreduce_stream_t stream) {
   if (n < 0 || out == nullptr || (x == nullptr && n > 0)) return LIBREDUCE_ERR_INVALID_ARG;
   if (n > INT64_MAX / 4) return LIBREDUCE_ERR_OVERFLOW;
-  return reduce_impl(x, 1, n, 1, out, op, reinterpret_cast<cudaStream_t>(stream));
+  return reduce_impl(x, 1, n, 1, out, op, Provider{}, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int reduce_axis_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
                     libreduce_stream_t stream) {
-  return reduce_impl(x, outer, reduce, inner, out, LIBREDUCE_OP_SUM,
+  return reduce_impl(x, outer, reduce, inner, out, LIBREDUCE_OP_SUM, Provider{},
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 int reduce_axis_op_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
                        int op, libreduce_stream_t stream) {
-  return reduce_impl(x, outer, reduce, inner, out, op, reinterpret_cast<cudaStream_t>(stream));
+  return reduce_impl(x, outer, reduce, inner, out, op, Provider{}, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int reduce_axis_op_ws_f32(const float* x, int64_t outer, int64_t reduce, int64_t inner, float* out,
+                          int op, void* ws, size_t* ws_bytes, libreduce_stream_t stream) {
+  Provider pv;
+  int rc = ws_provider(ws, ws_bytes, &pv);
+  if (rc) return rc;
+  return reduce_impl(x, outer, reduce, inner, out, op, pv, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, float* y,
                        libreduce_stream_t stream) {
-  return cumsum_impl(x, rows, N, 1, y, LIBREDUCE_SCAN_REVERSE, reinterpret_cast<cudaStream_t>(stream));
+  return cumsum_impl(x, rows, N, 1, y, LIBREDUCE_SCAN_REVERSE, Provider{},
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 int cumsum_f32(const float* x, int64_t outer, int64_t N, int64_t inner, float* y, unsigned flags,
                libreduce_stream_t stream) {
-  return cumsum_impl(x, outer, N, inner, y, flags, reinterpret_cast<cudaStream_t>(stream));
+  return cumsum_impl(x, outer, N, inner, y, flags, Provider{}, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int cumsum_ws_f32(const float* x, int64_t outer, int64_t N, int64_t inner, float* y, unsigned flags,
+                  void* ws, size_t* ws_bytes, libreduce_stream_t stream) {
+  Provider pv;
+  int rc = ws_provider(ws, ws_bytes, &pv);
+  if (rc) return rc;
+  return cumsum_impl(x, outer, N, inner, y, flags, pv, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int libreduce_check(libreduce_stream_t stream) {
@@ -529,6 +676,22 @@ int libreduce_check(libreduce_stream_t stream) {
   // Clear the error and abort words and the look-back ticket counter, which an
   // interrupted launch may have left behind.
   e = cudaMemsetAsync(st->err_word, 0, 3 * sizeof(unsigned), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return LIBREDUCE_ERR_TIMEOUT;
+}
+
+int libreduce_check_ws(void* ws, libreduce_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (ws == nullptr) return LIBREDUCE_ERR_INVALID_ARG;
+  unsigned word = 0;
+  e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (word == 0) return LIBREDUCE_OK;
+  e = cudaMemsetAsync(ws, 0, 3 * sizeof(unsigned), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail_cuda(e);
   return LIBREDUCE_ERR_TIMEOUT;

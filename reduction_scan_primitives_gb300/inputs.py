@@ -86,6 +86,11 @@ WORKLOADS = {
                                dist="uniform_pm1", seed=11),
     "min_65536x4096_d0": dict(op="reduce", rop="min", shape=(65536, 4096), dim=0,
                               dist="uniform_pm1", seed=11),
+    # The same calls with caller-provided scratch.
+    "rcumsum_1x1e9_ws": dict(op="cumsum", shape=(1, 1_000_000_000), dim=1, reverse=True,
+                             exclusive=False, dist="uniform01", seed=3, ws=True),
+    "axis_65536x4096_d0_ws": dict(op="reduce", rop="sum", shape=(65536, 4096), dim=0,
+                                  dist="uniform_pm1", seed=11, ws=True),
 }
 
 # The 1D sweep sizes of the sum benchmark (uniform[0,1), seed 42).

@@ -96,6 +96,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.cumsum_f32.restype = i32
     lib.libreduce_check.argtypes = [vp]
     lib.libreduce_check.restype = i32
+    sz = ctypes.POINTER(ctypes.c_size_t)
+    lib.reduce_axis_op_ws_f32.argtypes = [vp, i64, i64, i64, vp, i32, vp, sz, vp]
+    lib.reduce_axis_op_ws_f32.restype = i32
+    lib.cumsum_ws_f32.argtypes = [vp, i64, i64, i64, vp, ctypes.c_uint, vp, sz, vp]
+    lib.cumsum_ws_f32.restype = i32
+    lib.libreduce_check_ws.argtypes = [vp, vp]
+    lib.libreduce_check_ws.restype = i32
     lib.libreduce_strerror.argtypes = [i32]
     lib.libreduce_strerror.restype = ctypes.c_char_p
     lib.libreduce_last_cuda_error.argtypes = []
@@ -278,6 +285,70 @@ def cumsum_f32(x: torch.Tensor, dim: int = -1, reverse: bool = False, exclusive:
         st = lib.cumsum_f32(x.data_ptr(), outer, N, inner, out.data_ptr(), flags, _stream_ptr(x.device))
     _raise_on("cumsum_f32", st)
     return out
+
+
+def _ws_ptr(ws):
+    if ws is None:
+        return None
+    if not isinstance(ws, torch.Tensor) or ws.device.type != "cuda":
+        raise ValueError("the workspace must be a CUDA tensor")
+    return ws.data_ptr()
+
+
+def _ws_nbytes(ws):
+    return ctypes.c_size_t(0 if ws is None else ws.numel() * ws.element_size())
+
+
+def reduce_axis_op_ws_f32(x: torch.Tensor, dim: int, op="sum", ws: torch.Tensor | None = None,
+                          out: torch.Tensor | None = None):
+    """reduce_axis_op_f32 with caller scratch.  ws=None: returns the bytes the
+    call needs (nothing runs); else runs with `ws` (a 256-byte aligned CUDA
+    buffer of at least that many bytes) and returns the output."""
+    _check_tensor(x, "x")
+    outer, reduce, inner = canonical_axis(x.shape, dim)
+    if out is None:
+        shape = list(x.shape)
+        del shape[dim % x.dim()]
+        out = torch.empty(shape, dtype=torch.float32, device=x.device)
+    nbytes = _ws_nbytes(ws)
+    lib = load()
+    with torch.cuda.device(x.device):
+        st = lib.reduce_axis_op_ws_f32(x.data_ptr(), outer, reduce, inner, out.data_ptr(), _op_code(op),
+                                       _ws_ptr(ws), ctypes.byref(nbytes), _stream_ptr(x.device))
+    _raise_on("reduce_axis_op_ws_f32", st)
+    return int(nbytes.value) if ws is None else out
+
+
+def cumsum_ws_f32(x: torch.Tensor, dim: int = -1, reverse: bool = False, exclusive: bool = False,
+                  ws: torch.Tensor | None = None, out: torch.Tensor | None = None):
+    """cumsum_f32 with caller scratch (see reduce_axis_op_ws_f32)."""
+    _check_tensor(x, "x")
+    outer, N, inner = canonical_axis(x.shape, dim)
+    if out is None:
+        out = torch.empty_like(x)
+    flags = (SCAN_REVERSE if reverse else 0) | (SCAN_EXCLUSIVE if exclusive else 0)
+    nbytes = _ws_nbytes(ws)
+    lib = load()
+    with torch.cuda.device(x.device):
+        st = lib.cumsum_ws_f32(x.data_ptr(), outer, N, inner, out.data_ptr(), flags, _ws_ptr(ws),
+                               ctypes.byref(nbytes), _stream_ptr(x.device))
+    _raise_on("cumsum_ws_f32", st)
+    return int(nbytes.value) if ws is None else out
+
+
+def check_ws(ws: torch.Tensor) -> None:
+    """Synchronise the current stream and raise if a wait of a workspace call ran out."""
+    with torch.cuda.device(ws.device):
+        st = load().libreduce_check_ws(ws.data_ptr(), _stream_ptr(ws.device))
+    _raise_on("libreduce_check_ws", st)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A 256-byte aligned uint8 CUDA buffer of at least `nbytes` bytes."""
+    n = max(int(nbytes), 1)
+    raw = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-raw.data_ptr()) % 256
+    return raw[off:off + n]
 
 
 def check(device=None) -> None:

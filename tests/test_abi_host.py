@@ -81,6 +81,20 @@ def test_reduce_op_arguments(lib):
     assert lib.reduce_f32(NULL, 3, FAKE, L.OPS["mean"], NULL) == E
 
 
+def test_workspace_arguments(lib):
+    import ctypes as C
+    n = C.c_size_t(1 << 20)
+    E = L.ERR_INVALID_ARG
+    # ws_bytes NULL, misaligned workspace: rejected before any CUDA call.
+    assert lib.reduce_axis_op_ws_f32(FAKE, 1, 8, 1, FAKE + 4096, 0, FAKE + 8192, None, NULL) == E
+    assert lib.cumsum_ws_f32(FAKE, 1, 8, 1, FAKE + 4096, 0, FAKE + 8192 + 16, C.byref(n), NULL) == E
+    assert lib.reduce_axis_op_ws_f32(FAKE, 1, 8, 1, FAKE + 4096, 0, FAKE + 8192 + 4, C.byref(n), NULL) == E
+    # A size query of an empty call needs nothing.
+    q = C.c_size_t(77)
+    assert lib.cumsum_ws_f32(FAKE, 0, 8, 1, FAKE, 0, NULL, C.byref(q), NULL) == L.OK and q.value == 0
+    assert lib.libreduce_check_ws(NULL, NULL) in (E, L.ERR_CUDA)
+
+
 def test_overflow_rejected(lib):
     big = 1 << 62
     assert lib.reduce_axis_f32(FAKE, big, big, 2, FAKE, NULL) == L.ERR_OVERFLOW
