@@ -252,7 +252,9 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  * against concurrent calls; set them before queuing work.
  *   LIBREDUCE_OPT_SCAN_STRATEGY  0 auto, 1 one block per row, 2 look-back (its fastest
  *                                form), 3 look-back keeping each tile in registers between
- *                                its read and its write (one HBM read, no L2 reread)
+ *                                its read and its write (one HBM read, no L2 reread),
+ *                                4 reduce-then-scan (tile sums, a scan of the sums, every
+ *                                tile scanned again with its carry: three passes)
  *   LIBREDUCE_OPT_AXIS_SPLIT     0 auto, k > 0 forces k slices of the reduce axis
  *                                (inner > 1), or k chunks per row (inner == 1)
  *   LIBREDUCE_OPT_SPIN_LIMIT     0 default, else the look-back wait limit in polls
@@ -276,12 +278,18 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *   LIBREDUCE_OPT_WAVES           1D sum: blocks = waves x resident blocks (0 = automatic:
  *                                 one wave, or more blocks of 64 Ki floats for long arrays)
  *   LIBREDUCE_OPT_LOOKBACK_LAG    look-back scan: tiles between the read that publishes a
- *                                 tile's sum and the reread that writes it (0 = automatic) */
+ *                                 tile's sum and the reread that writes it (0 = automatic)
+ *   LIBREDUCE_OPT_SCAN_COLS_VARIANT  scan along a strided axis (inner > 1), block shape:
+ *                                 0 scalar columns, 2 warps across x 4 down the axis;
+ *                                 1 float4 columns, 2 x 4; 2 scalar, 1 x 8; 3 float4,
+ *                                 1 x 8; 4 float4, 8 x 1 (float4 needs inner % 4 == 0
+ *                                 and aligned x, y) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6
 #define LIBREDUCE_OPT_RSCAN_VARIANT 7
 #define LIBREDUCE_OPT_WAVES 8
 #define LIBREDUCE_OPT_LOOKBACK_LAG 9
+#define LIBREDUCE_OPT_SCAN_COLS_VARIANT 10
 LIBREDUCE_API int libreduce_set_option(int option, int64_t value);
 
 #ifdef __cplusplus

@@ -57,6 +57,7 @@ std::atomic<int64_t> g_opt_stall_tile{-1};
 std::atomic<int64_t> g_opt_contig_variant{-1};
 std::atomic<int64_t> g_opt_cols_variant{-1};
 std::atomic<int64_t> g_opt_rscan_variant{-1};
+std::atomic<int64_t> g_opt_scan_cols_variant{-1};
 std::atomic<int64_t> g_opt_waves{0};
 std::atomic<int64_t> g_opt_lookback_lag{0};
 thread_local int t_last_cuda_error = 0;
@@ -409,7 +410,7 @@ int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, 
   int rc = acquire(pv, need, &sc, s);
   if (rc) return rc;
   ColsParams p{x, outer, reduce, inner, (int32_t)col_tiles, (int32_t)splits, rows_per_split,
-               out, sc.partials, sc.tickets, epi};
+               out, sc.partials, sc.tickets, epi, 0};
   return launched(launch_reduce_cols(variant, op, p, grid, s));
 }
 
@@ -508,6 +509,31 @@ int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t
   return launched(launch_rscan_lookback(variant, p, grid, s));
 }
 
+// Reduce-then-scan along rows: tile sums, a reverse exclusive scan of the
+// sums (one block per row), then every tile scanned again with its carry.
+int run_reduce_then_scan(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
+                         cudaStream_t s, int flags, bool vec4) {
+  const int variant = vec4 ? kTileV4 : kTileV1;
+  const int64_t tiles = ceil_div(N, tile_scan_len(variant));
+  int64_t total = 0;
+  if (mul_overflows(rows, tiles, &total) || 2 * total > kMaxPartials || total > INT32_MAX)
+    return LIBREDUCE_ERR_OVERFLOW;
+  Need need;
+  need.partials = 2 * total;
+  Scratch sc;
+  int rc = acquire(pv, need, &sc, s);
+  if (rc) return rc;
+  float* sums = sc.partials;
+  float* carries = sc.partials + total;
+  TileSumsParams p1{x, rows, N, tiles, sums, flags};
+  if ((rc = launched(launch_tile_sums(variant, p1, total, s)))) return rc;
+  RScanRowsParams p2{sums, carries, rows, tiles, kScanExclusive};
+  if ((rc = launched(launch_rscan_rows(kRScanV1S4, p2, std::min<int64_t>(rows, INT32_MAX), s))))
+    return rc;
+  TileCarryParams p3{x, y, rows, N, tiles, carries, flags};
+  return launched(launch_tile_carry_scan(variant, p3, total, s));
+}
+
 // Scans along rows (inner == 1).  `flags`: kScanMirror for a forward scan,
 // kScanExclusive to leave out each element's own term.
 int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
@@ -526,6 +552,7 @@ int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, 
   const int64_t lb_tiles = ceil_div(N, lookback_tile(lb_variant));
   const int64_t row_slots = (int64_t)st->sm_count * st->occ_rscan[variant];
   const bool lookback_fits = rows <= kMaxLookbackTiles / std::max<int64_t>(1, lb_tiles);
+  if (strategy == 4) return run_reduce_then_scan(pv, x, rows, N, y, s, flags, vec4);
   if (strategy >= 2 || (strategy == 0 && 4 * rows < row_slots && lb_tiles >= 4 && lookback_fits))
     return run_rscan_lookback(pv, x, rows, N, y, s, lb_variant, flags);
   Scratch sc;
@@ -536,21 +563,66 @@ int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, 
   return launched(launch_rscan_rows(variant, p, grid, s));
 }
 
-// Scans along a strided axis (inner > 1): one thread per column group.
+// Scans along a strided axis (inner > 1): one block per (o, column tile),
+// walking the whole axis.  When those blocks cannot fill the GPU, the axis is
+// cut into segments and scanned in three passes: segment sums (the split
+// column reduction, keeping every slice), an exclusive scan of the sums along
+// the segments (the same scan kernel, one segment), then every segment
+// scanned again from its carry.  The extra read of x costs half a pass, so
+// segments are used only where one pass would leave most SMs idle.
 int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
                   float* y, bool reverse, bool exclusive, cudaStream_t s) {
   DeviceState* st = pv.st;
   const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
                     ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
-  const int variant = vec4 ? kScanColsV4 : kScanColsV1;
-  const int64_t groups = outer * ceil_div(inner, vec4 ? 4 : 1);
-  const int64_t slots = (int64_t)st->sm_count * st->occ_scan_cols[variant];
-  const int64_t grid = std::max<int64_t>(1, std::min(ceil_div(groups, kThreads), 8 * slots));
+  int variant = vec4 ? kScanColsV4 : kScanColsV1;
+  const int64_t forced_v = g_opt_scan_cols_variant.load();
+  if (forced_v >= 0 && forced_v < kNumScanColsVariants && (!scan_cols_vec4((int)forced_v) || vec4))
+    variant = (int)forced_v;
+  const int64_t slots = (int64_t)st->sm_count * st->occ_scan_cols[variant];  // resident blocks
+  int64_t units = 0;
+  if (mul_overflows(outer, ceil_div(inner, scan_cols_block_width(variant)), &units))
+    return LIBREDUCE_ERR_OVERFLOW;
+  int64_t segs = 1;
+  const int64_t forced = g_opt_axis_split.load();
+  if (forced > 0) segs = std::min(forced, N);
+  else if (2 * units < slots)
+    segs = std::min(ceil_div(4 * slots, units), std::max<int64_t>(1, N / (4 * scan_cols_tile_rows(variant))));
+  // The segment sums come from the split column reduction, whose column tiles
+  // are padded to its block width; sums and carries must fit the library's
+  // partials: take as many segments as fit, or none.  (The sums pass keeps
+  // its slices and takes no tickets.)
+  const int cvariant = vec4 ? kColsV4W4 : kColsV1W4;
+  const int64_t cw = cols_block_width(cvariant);
+  const int64_t col_tiles = ceil_div(inner, cw);
+  const int64_t inner_pad = col_tiles * cw;
+  if (segs > 1) {
+    const int64_t cap = kMaxPartials / (2 * outer * inner_pad);
+    segs = cap < 2 ? 1 : std::min(segs, cap);
+  }
+  int64_t seg_len = ceil_div(N, segs);
+  segs = ceil_div(N, seg_len);
+  Need need;
+  if (segs > 1) need.partials = 2 * outer * segs * inner_pad;
   Scratch sc;
-  int rc = acquire(pv, Need{}, &sc, s);
+  int rc = acquire(pv, need, &sc, s);
   if (rc) return rc;
-  ScanColsParams p{x, y, outer, N, inner, reverse ? 1 : 0, exclusive ? 1 : 0};
-  return launched(launch_scan_cols(variant, p, grid, s));
+  const auto grid_for = [](int64_t blocks) { return std::max<int64_t>(1, std::min<int64_t>(blocks, INT32_MAX)); };
+  if (segs == 1) {
+    ScanColsParams p{x, y, outer, N, inner, reverse ? 1 : 0, exclusive ? 1 : 0, nullptr, 1, N, 0};
+    return launched(launch_scan_cols(variant, p, grid_for(units), s));
+  }
+  float* sums = sc.partials;                               // [outer, segs, inner_pad]
+  float* carries = sc.partials + outer * segs * inner_pad;  // same shape
+  ColsParams p1{x, outer, N, inner, (int32_t)col_tiles, (int32_t)segs, seg_len,
+                nullptr, sums, nullptr, kEpiNone, 1};
+  if ((rc = launched(launch_reduce_cols(cvariant, kOpSum, p1, outer * col_tiles * segs, s)))) return rc;
+  ScanColsParams p2{sums, carries, outer, segs, inner_pad, reverse ? 1 : 0, 1, nullptr, 1, segs, 0};
+  const int64_t units2 = outer * ceil_div(inner_pad, scan_cols_block_width(kScanColsV4));
+  if ((rc = launched(launch_scan_cols(kScanColsV4, p2, grid_for(units2), s)))) return rc;
+  ScanColsParams p3{x, y, outer, N, inner, reverse ? 1 : 0, exclusive ? 1 : 0, carries, segs, seg_len,
+                    inner_pad};
+  return launched(launch_scan_cols(variant, p3, grid_for(units * segs), s));
 }
 
 // The cumulative sum behind every scan entry point.
@@ -716,7 +788,7 @@ int64_t libreduce_launch_count(void) { return g_launches.load(); }
 int libreduce_set_option(int option, int64_t value) {
   switch (option) {
     case LIBREDUCE_OPT_SCAN_STRATEGY:
-      if (value < 0 || value > 3) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < 0 || value > 4) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_strategy = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_AXIS_SPLIT:
@@ -742,6 +814,10 @@ int libreduce_set_option(int option, int64_t value) {
     case LIBREDUCE_OPT_RSCAN_VARIANT:
       if (value < -1 || value >= kNumRScanVariants) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_rscan_variant = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_SCAN_COLS_VARIANT:
+      if (value < -1 || value >= kNumScanColsVariants) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_scan_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_LOOKBACK_LAG:
       if (value < 0 || value > (1 << 20)) return LIBREDUCE_ERR_INVALID_ARG;

@@ -55,6 +55,7 @@ struct ColsParams {
   float* partials;
   unsigned* tickets;  // outer * col_tiles, zero on entry, left zero on exit
   int epi;
+  int keep_partials;  // split only: leave every slice's column sums in `partials`
 };
 
 // --- Scan flags (internal) ---------------------------------------------------
@@ -73,14 +74,39 @@ struct RScanRowsParams {
   int flags;
 };
 
+// --- Reduce-then-scan along rows (three passes) ------------------------------
+// Rows are scanned as reverse scans of the (possibly mirrored) row, in logical
+// tiles k = [k*TILE, (k+1)*TILE).  Pass 1 writes the sum of every logical tile
+// (sums[r*tiles + k]); pass 2 is a reverse exclusive row scan of those sums,
+// giving each tile's carry (the sum of the tiles after it); pass 3 scans each
+// tile again and adds its carry.  `flags` as for the row scans.
+struct TileSumsParams {
+  const float* x;
+  int64_t rows, N, tiles;
+  float* sums;
+  int flags;
+};
+struct TileCarryParams {
+  const float* x;
+  float* y;
+  int64_t rows, N, tiles;
+  const float* carries;  // [rows, tiles], logical tile order
+  int flags;
+};
+
 // --- Cumulative sum along a strided axis (inner > 1) -------------------------
-// x, y: [outer, N, inner]; one thread per (o, group of VEC columns).
+// x, y: [outer, N, inner]; one block per (o, segment, column tile).
 struct ScanColsParams {
   const float* x;
   float* y;
   int64_t outer, N, inner;
   int reverse;
   int exclusive;
+  // Segmented form (the last pass of a column reduce-then-scan): the axis is
+  // cut into `segs` segments of seg_len rows, each scanned from
+  // carry[(o*segs + s)*carry_stride + col].
+  const float* carry;  // null: one segment, starting from zero
+  int64_t segs, seg_len, carry_stride;
 };
 
 // --- Reverse cumulative sum, single-pass decoupled look-back ----------------
@@ -131,13 +157,33 @@ enum LookbackVariant {
   kNumLookbackVariants
 };
 
-enum ScanColsVariant { kScanColsV1 = 0, kScanColsV4 = 1, kNumScanColsVariants };
+// Column scan block shapes: VEC floats per thread, WX warps across columns,
+// WY warps down the axis, U rows per warp per tile.
+enum ScanColsVariant {
+  kScanColsV1 = 0,    // VEC 1, WX 2, WY 4, U 16
+  kScanColsV4 = 1,    // VEC 4, WX 2, WY 4, U 8 (needs inner % 4 == 0, aligned x, y)
+  kScanColsV1Y8 = 2,  // VEC 1, WX 1, WY 8, U 8
+  kScanColsV4Y8 = 3,  // VEC 4, WX 1, WY 8, U 8
+  kScanColsV4Y1 = 4,  // VEC 4, WX 8, WY 1, U 8
+  kNumScanColsVariants
+};
+inline bool scan_cols_vec4(int variant) {
+  return variant == kScanColsV4 || variant == kScanColsV4Y8 || variant == kScanColsV4Y1;
+}
+enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
+
+// Elements per tile of the reduce-then-scan passes.
+int64_t tile_scan_len(int variant);
 
 // Elements per tile of each look-back variant.
 int64_t lookback_tile(int variant);
 
 // Columns covered by one block of a cols variant.
 int cols_block_width(int variant);
+
+// Columns and rows (in scan order) of one tile of a column scan variant.
+int scan_cols_block_width(int variant);
+int scan_cols_tile_rows(int variant);
 
 cudaError_t launch_reduce_contig(int variant, int op, const ContigParams& p, int64_t grid,
                                  cudaStream_t s);
@@ -148,6 +194,8 @@ cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t gri
 cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int64_t grid,
                                   cudaStream_t s);
 cudaError_t launch_scan_cols(int variant, const ScanColsParams& p, int64_t grid, cudaStream_t s);
+cudaError_t launch_tile_sums(int variant, const TileSumsParams& p, int64_t grid, cudaStream_t s);
+cudaError_t launch_tile_carry_scan(int variant, const TileCarryParams& p, int64_t grid, cudaStream_t s);
 
 // Host helpers defined in lr_api.cu, for entry points in other files.
 int check_device_buffer(const void* p, size_t bytes, int dev);  // a libreduce status

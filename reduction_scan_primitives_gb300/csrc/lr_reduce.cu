@@ -162,8 +162,10 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
     float* mine = part_base + s * slice_stride;
 #pragma unroll
     for (int c = 0; c < VEC; ++c) mine[jloc + c] = res[c];
+    if (p.keep_partials) return;  // the slice sums are the result
     __threadfence();
   }
+  if (p.keep_partials) return;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();

@@ -509,104 +509,207 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback_l2(RScanLookback
 }
 
 // ---------------------------------------------------------------------------
+// Reduce-then-scan along rows: the deterministic multi-pass alternative to the
+// look-back (each element travels three times between HBM and the SMs instead
+// of two).  Both tile passes address logical tile k of the (possibly
+// mirrored) row, and the middle pass -- a reverse exclusive row scan of the
+// tile sums -- turns the sums into each tile's carry.
+// ---------------------------------------------------------------------------
+template <int VEC, int SUB>
+__global__ void __launch_bounds__(kThreads) k_tile_sums(TileSumsParams p) {
+  constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
+  __shared__ float sh[kNW];
+  const int64_t b = blockIdx.x;
+  const int64_t row = b / p.tiles;
+  const int64_t k = b - row * p.tiles;
+  float v[SUB][VEC];
+  load_tile<VEC, SUB>(v, p.x + row * p.N, k * TILE, p.N, threadIdx.x, (p.flags & kScanMirror) != 0);
+  float e[SUB];
+#pragma unroll
+  for (int s = 0; s < SUB; ++s) e[s] = tree_sum<VEC>(v[s]);
+  const float a = block_sum<kThreads>(tree_sum<SUB>(e), sh);
+  if (threadIdx.x == 0) p.sums[b] = a;
+}
+
+template <int VEC, int SUB>
+__global__ void __launch_bounds__(kThreads) k_tile_carry_scan(TileCarryParams p) {
+  constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
+  __shared__ float sh_w[SUB][kNW];
+  const int t = threadIdx.x;
+  const int64_t b = blockIdx.x;
+  const int64_t row = b / p.tiles;
+  const int64_t k = b - row * p.tiles;
+  const bool mirror = (p.flags & kScanMirror) != 0;
+  float v[SUB][VEC];
+  load_tile<VEC, SUB>(v, p.x + row * p.N, k * TILE, p.N, t, mirror);
+  const TileScan<SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, t & 31, t >> 5);
+  finalize<VEC, SUB>(v, ts, p.carries[b], (p.flags & kScanExclusive) != 0);
+  store_tile<VEC, SUB>(v, p.y + row * p.N, k * TILE, p.N, t, mirror);
+}
+
+// ---------------------------------------------------------------------------
 // Cumulative sum along a strided axis: x, y are [outer, N, inner] with
 // inner > 1 (the POPCORNBENCH trace l1_p91 discusses scanning dims other than
-// the last).  One thread per (o, VEC adjacent columns), so a warp's loads and
-// stores cover 32*VEC consecutive floats of one row; it walks the axis in the
-// scan direction with U rows in flight.  The running sum is blocked: a chunk
-// of up to 64 terms, folded into three more levels every 32 folds, and each
-// output is carry + chunk sum, so no addition chain grows with N (up to
-// 64*32*32*32 rows per chunk level) and no output subtracts anything.
+// the last).  A block owns CW = WX*32*VEC adjacent columns of one (o, segment)
+// and walks the segment in the scan direction in tiles of T = WY*U rows: warp
+// row wy loads rows [wy*U, wy*U + U) of the tile (every warp load is 32*VEC
+// consecutive floats of one row), scans them in registers, and publishes its
+// U-row total in shared memory; each thread then adds the totals of the warp
+// rows before its own (pre) and of all WY (the tile total) in a fixed order.
+// Output = base + (pre + own prefix), with base the blocked running sum of
+// the earlier tiles' totals (starting from the segment's carry), so no
+// addition chain grows with N and no output subtracts anything.  Splitting
+// the rows of a tile over WY warps gives every column WY threads and keeps
+// U*VEC loads in flight per thread, with one barrier per tile.
 // ---------------------------------------------------------------------------
+
+// Running sum of tile totals: level 0 takes 32 tile totals, each higher level
+// 32 folds of the one below, the top one term per 32^4 tiles; hi holds the
+// levels above 0, so base() is one addition.
 template <int VEC>
-struct RunningSum {
-  float l0[VEC], l1[VEC], l2[VEC], l3[VEC], carry[VEC];
-  int n0 = 0, n1 = 0, n2 = 0;
-  __device__ __forceinline__ RunningSum() {
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) l0[c] = l1[c] = l2[c] = l3[c] = carry[c] = 0.f;
-  }
-  __device__ __forceinline__ void fold() {
-    if (++n0 < 64) return;
-    n0 = 0;
+struct TileCarry {
+  float lv[5][VEC];
+  float hi[VEC];
+  int n0 = 0, n1 = 0, n2 = 0, n3 = 0;
+  __device__ __forceinline__ explicit TileCarry(const float (&init)[VEC]) {
 #pragma unroll
     for (int c = 0; c < VEC; ++c) {
-      l1[c] += l0[c];
-      l0[c] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) lv[k][c] = 0.f;
+      lv[4][c] = hi[c] = init[c];
     }
+  }
+  __device__ __forceinline__ void fold(int k) {
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      lv[k + 1][c] += lv[k][c];
+      lv[k][c] = 0.f;
+    }
+  }
+  __device__ __forceinline__ void add(const float (&t)[VEC]) {
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) lv[0][c] += t[c];
+    if (++n0 < 32) return;
+    n0 = 0;
+    fold(0);
     if (++n1 == 32) {
       n1 = 0;
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) {
-        l2[c] += l1[c];
-        l1[c] = 0.f;
-      }
+      fold(1);
       if (++n2 == 32) {
         n2 = 0;
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-          l3[c] += l2[c];
-          l2[c] = 0.f;
+        fold(2);
+        if (++n3 == 32) {
+          n3 = 0;
+          fold(3);
         }
       }
     }
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) carry[c] = (l3[c] + l2[c]) + l1[c];
+    for (int c = 0; c < VEC; ++c) hi[c] = ((lv[4][c] + lv[3][c]) + lv[2][c]) + lv[1][c];
   }
+  __device__ __forceinline__ float base(int c) const { return hi[c] + lv[0][c]; }
 };
 
-template <int VEC, int U>
-__global__ void __launch_bounds__(kThreads) k_scan_cols(ScanColsParams p) {
-  const int64_t groups = (p.inner + VEC - 1) / VEC;
-  const int64_t total = p.outer * groups;
-  for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < total;
-       g += (int64_t)gridDim.x * kThreads) {
-    const int64_t o = g / groups;
-    const int64_t c0 = (g - o * groups) * VEC;
-    const float* xc = p.x + o * p.N * p.inner + c0;
-    float* yc = p.y + o * p.N * p.inner + c0;
-    RunningSum<VEC> rs;
-    for (int64_t step = 0; step < p.N; step += U) {
+template <int VEC, int WX, int WY, int U>
+__global__ void __launch_bounds__(kThreads, VEC == 4 ? 3 : 4) k_scan_cols(ScanColsParams p) {
+  static_assert(WX * WY * 32 == kThreads, "WX warps across columns, WY down the axis");
+  constexpr int CW = WX * 32 * VEC;
+  constexpr int T = WY * U;
+  __shared__ __align__(16) float sh[2][WY][CW];
+  const int warp = threadIdx.x >> 5;
+  const int wx = warp % WX;
+  const int wy = warp / WX;
+  const int jloc = (wx * 32 + (threadIdx.x & 31)) * VEC;
+  const int64_t col_tiles = (p.inner + CW - 1) / CW;
+  const int64_t units = p.outer * p.segs * col_tiles;
+  const int64_t step_j = p.reverse ? -p.inner : p.inner;
+  int buf = 0;
+  for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int64_t og = unit / col_tiles;  // (o, segment)
+    const int64_t col = (unit - og * col_tiles) * CW + jloc;
+    const int64_t o = og / p.segs;
+    const int64_t lo = (og - o * p.segs) * p.seg_len;
+    const int64_t len = min(p.seg_len, p.N - lo);
+    // With VEC == 4 the caller guarantees inner % 4 == 0: all four columns.
+    const bool active = col < p.inner;
+    const int64_t j0 = p.reverse ? lo + len - 1 : lo;
+    const int64_t off = (o * p.N + j0) * p.inner + (active ? col : 0);
+    const float* xp = p.x + off;
+    float* yp = p.y + off;
+    float init[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c)
+      init[c] = (p.carry != nullptr && active) ? p.carry[og * p.carry_stride + col + c] : 0.f;
+    TileCarry<VEC> tc(init);
+    for (int64_t t0 = 0; t0 < len; t0 += T) {
+      // The stride is hidden from the optimiser each tile: otherwise it hoists
+      // all U row offsets out of the loop and holds them in registers.
+      int64_t sj = step_j;
+      asm volatile("" : "+l"(sj));
+      const int64_t k0 = t0 + wy * U;  // this warp row's first row, in scan order
+      const int cnt = active ? (int)max((int64_t)0, min((int64_t)U, len - k0)) : 0;
       float q[U][VEC];
+      const float* xr = xp + k0 * sj;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t s = step + u;
-        const int64_t j = p.reverse ? p.N - 1 - s : s;
-        if (s < p.N) {
+        if (u < cnt) {
           if constexpr (VEC == 4) {
-            const float4 f = ld_stream4(xc + j * p.inner);
+            const float4 f = ld_stream4(xr);
             q[u][0] = f.x;
             q[u][1] = f.y;
             q[u][2] = f.z;
             q[u][3] = f.w;
           } else {
-            q[u][0] = ld_stream1(xc + j * p.inner);
+            q[u][0] = ld_stream1(xr);
           }
+        } else {
+#pragma unroll
+          for (int c = 0; c < VEC; ++c) q[u][c] = 0.f;
         }
+        xr += sj;
       }
+#pragma unroll
+      for (int u = 1; u < U; ++u)
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) q[u][c] += q[u - 1][c];
+      if constexpr (VEC == 4)
+        *reinterpret_cast<float4*>(&sh[buf][wy][jloc]) =
+            make_float4(q[U - 1][0], q[U - 1][1], q[U - 1][2], q[U - 1][3]);
+      else
+        sh[buf][wy][jloc] = q[U - 1][0];
+      __syncthreads();
+      float pre[VEC], tot[VEC], b[VEC];
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        float r = 0.f;
+        pre[c] = 0.f;
+#pragma unroll
+        for (int y = 0; y < WY; ++y) {
+          if (y == wy) pre[c] = r;
+          r += sh[buf][y][jloc + c];
+        }
+        tot[c] = r;
+        b[c] = tc.base(c);
+      }
+      float* yr = yp + k0 * sj;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t s = step + u;
-        if (s >= p.N) break;
-        const int64_t j = p.reverse ? p.N - 1 - s : s;
-        float out[VEC];
+        if (u < cnt) {
+          float out[VEC];
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-          if (p.exclusive) {
-            out[c] = rs.carry[c] + rs.l0[c];
-            rs.l0[c] += q[u][c];
-          } else {
-            rs.l0[c] += q[u][c];
-            out[c] = rs.carry[c] + rs.l0[c];
+          for (int c = 0; c < VEC; ++c) {
+            const float own = p.exclusive ? (u > 0 ? q[u - 1][c] : 0.f) : q[u][c];
+            out[c] = b[c] + (pre[c] + own);
           }
+          if constexpr (VEC == 4)
+            st_stream4(yr, make_float4(out[0], out[1], out[2], out[3]));
+          else
+            st_stream1(yr, out[0]);
         }
-        rs.fold();
-        if constexpr (VEC == 4) {
-          st_stream4(yc + j * p.inner, make_float4(out[0], out[1], out[2], out[3]));
-        } else {
-          st_stream1(yc + j * p.inner, out[0]);
-        }
+        yr += sj;
       }
+      tc.add(tot);
+      buf ^= 1;
     }
   }
 }
@@ -664,17 +767,61 @@ int occupancy_rscan_lookback(int variant) {
 cudaError_t launch_scan_cols(int variant, const ScanColsParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
   switch (variant) {
-    case kScanColsV1: k_scan_cols<1, 8><<<g, kThreads, 0, s>>>(p); break;
-    case kScanColsV4: k_scan_cols<4, 8><<<g, kThreads, 0, s>>>(p); break;
+    case kScanColsV1: k_scan_cols<1, 2, 4, 16><<<g, kThreads, 0, s>>>(p); break;
+    case kScanColsV4: k_scan_cols<4, 2, 4, 8><<<g, kThreads, 0, s>>>(p); break;
+    case kScanColsV1Y8: k_scan_cols<1, 1, 8, 8><<<g, kThreads, 0, s>>>(p); break;
+    case kScanColsV4Y8: k_scan_cols<4, 1, 8, 8><<<g, kThreads, 0, s>>>(p); break;
+    case kScanColsV4Y1: k_scan_cols<4, 8, 1, 8><<<g, kThreads, 0, s>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }
 
+int scan_cols_block_width(int variant) {
+  switch (variant) {
+    case kScanColsV1: return 2 * 32;
+    case kScanColsV4: return 2 * 32 * 4;
+    case kScanColsV1Y8: return 32;
+    case kScanColsV4Y8: return 32 * 4;
+    case kScanColsV4Y1: return 8 * 32 * 4;
+    default: return 0;
+  }
+}
+
+int scan_cols_tile_rows(int variant) {
+  switch (variant) {
+    case kScanColsV1: return 4 * 16;
+    case kScanColsV4: return 4 * 8;
+    case kScanColsV1Y8: return 8 * 8;
+    case kScanColsV4Y8: return 8 * 8;
+    case kScanColsV4Y1: return 8;
+    default: return 0;
+  }
+}
+
+int64_t tile_scan_len(int variant) { return variant == kTileV4 ? 8 * kThreads * 4 : 8 * kThreads; }
+
+cudaError_t launch_tile_sums(int variant, const TileSumsParams& p, int64_t grid, cudaStream_t s) {
+  const dim3 g((unsigned)grid);
+  if (variant == kTileV4) k_tile_sums<4, 8><<<g, kThreads, 0, s>>>(p);
+  else k_tile_sums<1, 8><<<g, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_carry_scan(int variant, const TileCarryParams& p, int64_t grid, cudaStream_t s) {
+  const dim3 g((unsigned)grid);
+  if (variant == kTileV4) k_tile_carry_scan<4, 8><<<g, kThreads, 0, s>>>(p);
+  else k_tile_carry_scan<1, 8><<<g, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 int occupancy_scan_cols(int variant) {
   switch (variant) {
-    case kScanColsV1: return occupancy_of(k_scan_cols<1, 8>);
-    case kScanColsV4: return occupancy_of(k_scan_cols<4, 8>);
+    case kScanColsV1: return occupancy_of(k_scan_cols<1, 2, 4, 16>);
+    case kScanColsV4: return occupancy_of(k_scan_cols<4, 2, 4, 8>);
+    case kScanColsV1Y8: return occupancy_of(k_scan_cols<1, 1, 8, 8>);
+    case kScanColsV4Y8: return occupancy_of(k_scan_cols<4, 1, 8, 8>);
+    case kScanColsV4Y1: return occupancy_of(k_scan_cols<4, 8, 1, 8>);
     default: return 0;
   }
 }

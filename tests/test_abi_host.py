@@ -132,12 +132,14 @@ def test_no_cpu_fallback_without_gpu(lib):
 
 def test_options(lib):
     assert lib.libreduce_set_option(999, 0) == L.ERR_INVALID_ARG
-    assert lib.libreduce_set_option(L.OPT_SCAN_STRATEGY, 4) == L.ERR_INVALID_ARG
+    assert lib.libreduce_set_option(L.OPT_SCAN_STRATEGY, 5) == L.ERR_INVALID_ARG
     assert lib.libreduce_set_option(L.OPT_STALL_TILE, -2) == L.ERR_INVALID_ARG
     for opt, val in ((L.OPT_SCAN_STRATEGY, 0), (L.OPT_AXIS_SPLIT, 0), (L.OPT_SPIN_LIMIT, 0),
                      (L.OPT_STALL_TILE, -1), (L.OPT_CONTIG_VARIANT, -1), (L.OPT_COLS_VARIANT, -1),
-                     (L.OPT_RSCAN_VARIANT, -1), (L.OPT_WAVES, 0), (L.OPT_LOOKBACK_LAG, 0)):
+                     (L.OPT_RSCAN_VARIANT, -1), (L.OPT_WAVES, 0), (L.OPT_LOOKBACK_LAG, 0),
+                     (L.OPT_SCAN_COLS_VARIANT, -1)):
         assert lib.libreduce_set_option(opt, val) == L.OK
+    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 5) == L.ERR_INVALID_ARG
 
 
 def test_strerror(lib):

@@ -59,7 +59,7 @@ def test_rows(rows, n, reverse, exclusive):
 
 
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
-@pytest.mark.parametrize("strategy", [1, 2, 3])
+@pytest.mark.parametrize("strategy", [1, 2, 3, 4])
 def test_rows_every_strategy(strategy, reverse, exclusive):
     L.set_option(L.OPT_SCAN_STRATEGY, strategy)
     check((3, 100_000), 1, reverse, exclusive)
@@ -69,8 +69,9 @@ def test_rows_every_strategy(strategy, reverse, exclusive):
 @pytest.mark.parametrize("offset,out_offset", [(1, 0), (2, 3)])
 def test_rows_misaligned(offset, out_offset, reverse, exclusive):
     check((4, 50_001), 1, reverse, exclusive, offset=offset, out_offset=out_offset)
-    L.set_option(L.OPT_SCAN_STRATEGY, 2)
-    check((1, 300_000), 1, reverse, exclusive, offset=offset, out_offset=out_offset)
+    for strategy in (2, 4):
+        L.set_option(L.OPT_SCAN_STRATEGY, strategy)
+        check((1, 300_000), 1, reverse, exclusive, offset=offset, out_offset=out_offset)
 
 
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
@@ -112,3 +113,31 @@ def test_reverse_entry_point_matches():
     b = L.cumsum_f32(xd, 1, reverse=True)
     L.check()
     assert bitwise_equal(a, b)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape,segs,offset", [((3, 1000, 36), 7, 0), ((2, 777, 4096), 3, 0),
+                                               ((4, 301, 33), 5, 0), ((1, 5000, 4096), 64, 1),
+                                               ((2, 130, 12), 130, 0), ((2, 100, 8), 1000, 0),
+                                               ((1, 70_001, 4), 0, 0), ((2, 3000, 5), 0, 2)])
+def test_axis_segmented(shape, segs, offset, reverse, exclusive):
+    """The column scan cut into segments: segment sums, a scan of the sums,
+    then every segment rescanned from its carry.  segs > 0 forces the count
+    (clamped to one row per segment); 0 leaves it to the library, which cuts
+    the axis when there are too few columns to fill the GPU."""
+    if segs:
+        L.set_option(L.OPT_AXIS_SPLIT, segs)
+    got, _ = check(shape, 1, reverse, exclusive, offset=offset)
+    if exclusive:
+        edge = 0 if not reverse else shape[1] - 1
+        assert np.all(got[:, edge, :] == 0.0)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+def test_axis_segmented_integers_exact(reverse, exclusive):
+    for shape, segs in (((3, 4000, 36), 9), ((2, 2048, 7), 64), ((1, 100_000, 8), 0)):
+        L.set_option(L.OPT_AXIS_SPLIT, segs)
+        x = inputs.make(shape, "int:0:3", 8)
+        o, n, i = L.canonical_axis(x.shape, 1)
+        ref, _ = oracle.cumsum(x.numpy(), o, n, i, reverse, exclusive)
+        assert_exact(run(x, 1, reverse, exclusive).reshape(-1), ref.reshape(-1), f"int {shape} segs={segs}")

@@ -74,7 +74,7 @@ def test_matches_block_per_row_path():
     # Same data through every strategy: all within tolerance of the oracle.
     x = inputs.make((4, 123_456), "uniform01", 9)
     ref, scale = oracle.reverse_cumsum(x.numpy(), 4, 123_456)
-    for strategy in (1, 2, 3):
+    for strategy in (1, 2, 3, 4):
         L.set_option(L.OPT_SCAN_STRATEGY, strategy)
         assert_close(run(x), ref, scale, f"strategy {strategy}")
 
@@ -87,7 +87,7 @@ def test_lag_values(lag):
     check(2, 8192 * 300 + 4)
 
 
-@pytest.mark.parametrize("strategy", [2, 3])
+@pytest.mark.parametrize("strategy", [2, 3, 4])
 @pytest.mark.parametrize("n", [8192 * 6 * 152 + 8, 8192 * 40000])
 def test_long_rows_both_forms(n, strategy):
     L.set_option(L.OPT_SCAN_STRATEGY, strategy)
@@ -114,3 +114,17 @@ def test_bounded_wait_reports_timeout():
     xc = x.cpu()
     ref, scale = oracle.reverse_cumsum(xc.numpy(), 1, xc.shape[1])
     assert_close(L.reverse_cumsum_f32(x).cpu().numpy(), ref, scale, "after timeout")
+
+
+@pytest.mark.parametrize("rows,n", [(1, 1), (1, 8191), (2, 8193), (3, 100_003), (1, 2_000_001)])
+def test_reduce_then_scan_shapes(rows, n):
+    L.set_option(L.OPT_SCAN_STRATEGY, 4)
+    check(rows, n, force=False)
+
+
+def test_reduce_then_scan_deterministic():
+    L.set_option(L.OPT_SCAN_STRATEGY, 4)
+    xd = on_device(inputs.make((2, 5_000_000), "uniform01", 7))
+    a = L.reverse_cumsum_f32(xd).clone()
+    b = L.reverse_cumsum_f32(xd).clone()
+    assert bitwise_equal(a, b)

@@ -112,3 +112,21 @@ def test_timeout_reported_through_workspace():
     L.check_ws(ws)
     ref = L.cumsum_f32(xd, 1, reverse=True)
     assert bitwise_equal(L.cumsum_ws_f32(xd, 1, reverse=True, ws=ws), ref)
+
+
+@pytest.mark.parametrize("shape,reverse,exclusive", [((2, 300_000, 4), True, False),
+                                                     ((1, 5000, 4096), False, True),
+                                                     ((3, 20_000, 33), True, True)])
+def test_segmented_column_scan_ws_matches_default(shape, reverse, exclusive):
+    """A column scan with few columns is cut into segments, whose sums and
+    carries live in the caller's workspace."""
+    xd = on_device(inputs.make(shape, "uniform_pm1", 5))
+    ref = L.cumsum_f32(xd, 1, reverse=reverse, exclusive=exclusive)
+    need = L.cumsum_ws_f32(xd, 1, reverse=reverse, exclusive=exclusive)
+    assert need > 256
+    ws = garbage_ws(need)
+    for _ in range(2):
+        got = L.cumsum_ws_f32(xd, 1, reverse=reverse, exclusive=exclusive, ws=ws)
+        L.check_ws(ws)
+        assert bitwise_equal(got, ref), shape
+    L.check()
