@@ -563,31 +563,68 @@ int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, 
   return launched(launch_rscan_rows(variant, p, grid, s));
 }
 
+// Predicted fraction of the copy bandwidth that a column scan reaches with
+// `units` equally long blocks, `slots` of them resident at once, a fraction
+// lane_eff of the lanes of a column tile holding columns, and `base` the
+// fraction the variant reaches on a large, well-shaped case.  Whole waves run
+// at full rate; a wave with fewer active warps than kSatFraction of the slots
+// (idle lanes counted out) no longer has enough loads in flight to cover the
+// memory latency and takes as long as one that has.  A fit to GB300 sweeps of
+// [outer, N, inner] from [1, 5000, 4096] to [4096, 256, 64].
+double predict_scan_cols(int64_t units, int64_t slots, double lane_eff, double base) {
+  constexpr double kSatFraction = 0.6;
+  const double floor_a = kSatFraction / lane_eff;
+  const int64_t full = units / slots;
+  const double rest = (double)(units - full * slots) / (double)slots;
+  const double time = (double)full * std::max(1.0, floor_a) + (rest > 0 ? std::max(rest, floor_a) : 0.0);
+  return base * ((double)units / (double)slots) / time;
+}
+
 // Scans along a strided axis (inner > 1): one block per (o, column tile),
 // walking the whole axis.  When those blocks cannot fill the GPU, the axis is
 // cut into segments and scanned in three passes: segment sums (the split
 // column reduction, keeping every slice), an exclusive scan of the sums along
 // the segments (the same scan kernel, one segment), then every segment
-// scanned again from its carry.  The extra read of x costs half a pass, so
-// segments are used only where one pass would leave most SMs idle.
+// scanned again from its carry.  The block shape and the segment count are
+// chosen by predict_scan_cols, the segmented form paying 1.5x for the extra
+// read of x.
 int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
                   float* y, bool reverse, bool exclusive, cudaStream_t s) {
   DeviceState* st = pv.st;
   const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
                     ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
-  int variant = vec4 ? kScanColsV4 : kScanColsV1;
   const int64_t forced_v = g_opt_scan_cols_variant.load();
-  if (forced_v >= 0 && forced_v < kNumScanColsVariants && (!scan_cols_vec4((int)forced_v) || vec4))
-    variant = (int)forced_v;
-  const int64_t slots = (int64_t)st->sm_count * st->occ_scan_cols[variant];  // resident blocks
-  int64_t units = 0;
-  if (mul_overflows(outer, ceil_div(inner, scan_cols_block_width(variant)), &units))
-    return LIBREDUCE_ERR_OVERFLOW;
-  int64_t segs = 1;
   const int64_t forced = g_opt_axis_split.load();
-  if (forced > 0) segs = std::min(forced, N);
-  else if (2 * units < slots)
-    segs = std::min(ceil_div(4 * slots, units), std::max<int64_t>(1, N / (4 * scan_cols_tile_rows(variant))));
+  // Fractions of the copy bandwidth each shape reaches on [128, 4096, 4096]
+  // (scalar: 0.75 when the rows are not 16-byte aligned).
+  const double base[kNumScanColsVariants] = {vec4 ? 0.906 : 0.75, 0.976, 0.977};
+  int variant = kScanColsV1;
+  int64_t segs = 1;
+  double best = -1.0;
+  for (int v = 0; v < kNumScanColsVariants; ++v) {
+    if (scan_cols_vec4(v) && !vec4) continue;
+    if (forced_v >= 0 && forced_v < kNumScanColsVariants && (!scan_cols_vec4((int)forced_v) || vec4) &&
+        v != forced_v)
+      continue;
+    const int64_t cw = scan_cols_block_width(v);
+    int64_t units = 0;
+    if (mul_overflows(outer, ceil_div(inner, cw), &units)) return LIBREDUCE_ERR_OVERFLOW;
+    const int64_t slots = (int64_t)st->sm_count * st->occ_scan_cols[v];
+    const double lane_eff = (double)inner / (double)(ceil_div(inner, cw) * cw);
+    int64_t cand[2] = {1, 1};
+    if (forced > 0) cand[0] = cand[1] = std::min(forced, N);
+    else cand[1] = std::min(ceil_div(4 * slots, units), std::max<int64_t>(1, N / (4 * scan_cols_tile_rows(v))));
+    for (int64_t sg : cand) {
+      double pred = predict_scan_cols(units * sg, slots, lane_eff, base[v]);
+      if (sg > 1) pred /= 1.5;
+      if (pred > best) {
+        best = pred;
+        variant = v;
+        segs = sg;
+      }
+    }
+  }
+  const int64_t units = outer * ceil_div(inner, scan_cols_block_width(variant));
   // The segment sums come from the split column reduction, whose column tiles
   // are padded to its block width; sums and carries must fit the library's
   // partials: take as many segments as fit, or none.  (The sums pass keeps

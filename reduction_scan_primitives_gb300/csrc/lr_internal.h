@@ -162,14 +162,10 @@ enum LookbackVariant {
 enum ScanColsVariant {
   kScanColsV1 = 0,    // VEC 1, WX 2, WY 4, U 16
   kScanColsV4 = 1,    // VEC 4, WX 2, WY 4, U 8 (needs inner % 4 == 0, aligned x, y)
-  kScanColsV1Y8 = 2,  // VEC 1, WX 1, WY 8, U 8
-  kScanColsV4Y8 = 3,  // VEC 4, WX 1, WY 8, U 8
-  kScanColsV4Y1 = 4,  // VEC 4, WX 8, WY 1, U 8
+  kScanColsV4Y8 = 2,  // VEC 4, WX 1, WY 8, U 8 (same)
   kNumScanColsVariants
 };
-inline bool scan_cols_vec4(int variant) {
-  return variant == kScanColsV4 || variant == kScanColsV4Y8 || variant == kScanColsV4Y1;
-}
+inline bool scan_cols_vec4(int variant) { return variant != kScanColsV1; }
 enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
 
 // Elements per tile of the reduce-then-scan passes.

@@ -769,9 +769,7 @@ cudaError_t launch_scan_cols(int variant, const ScanColsParams& p, int64_t grid,
   switch (variant) {
     case kScanColsV1: k_scan_cols<1, 2, 4, 16><<<g, kThreads, 0, s>>>(p); break;
     case kScanColsV4: k_scan_cols<4, 2, 4, 8><<<g, kThreads, 0, s>>>(p); break;
-    case kScanColsV1Y8: k_scan_cols<1, 1, 8, 8><<<g, kThreads, 0, s>>>(p); break;
     case kScanColsV4Y8: k_scan_cols<4, 1, 8, 8><<<g, kThreads, 0, s>>>(p); break;
-    case kScanColsV4Y1: k_scan_cols<4, 8, 1, 8><<<g, kThreads, 0, s>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -781,9 +779,7 @@ int scan_cols_block_width(int variant) {
   switch (variant) {
     case kScanColsV1: return 2 * 32;
     case kScanColsV4: return 2 * 32 * 4;
-    case kScanColsV1Y8: return 32;
     case kScanColsV4Y8: return 32 * 4;
-    case kScanColsV4Y1: return 8 * 32 * 4;
     default: return 0;
   }
 }
@@ -792,9 +788,7 @@ int scan_cols_tile_rows(int variant) {
   switch (variant) {
     case kScanColsV1: return 4 * 16;
     case kScanColsV4: return 4 * 8;
-    case kScanColsV1Y8: return 8 * 8;
     case kScanColsV4Y8: return 8 * 8;
-    case kScanColsV4Y1: return 8;
     default: return 0;
   }
 }
@@ -819,9 +813,7 @@ int occupancy_scan_cols(int variant) {
   switch (variant) {
     case kScanColsV1: return occupancy_of(k_scan_cols<1, 2, 4, 16>);
     case kScanColsV4: return occupancy_of(k_scan_cols<4, 2, 4, 8>);
-    case kScanColsV1Y8: return occupancy_of(k_scan_cols<1, 1, 8, 8>);
     case kScanColsV4Y8: return occupancy_of(k_scan_cols<4, 1, 8, 8>);
-    case kScanColsV4Y1: return occupancy_of(k_scan_cols<4, 8, 1, 8>);
     default: return 0;
   }
 }

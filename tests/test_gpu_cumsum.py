@@ -141,3 +141,16 @@ def test_axis_segmented_integers_exact(reverse, exclusive):
         o, n, i = L.canonical_axis(x.shape, 1)
         ref, _ = oracle.cumsum(x.numpy(), o, n, i, reverse, exclusive)
         assert_exact(run(x, 1, reverse, exclusive).reshape(-1), ref.reshape(-1), f"int {shape} segs={segs}")
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+def test_axis_every_block_shape(variant, reverse, exclusive):
+    """Each column-scan block shape (scalar 2x4 warps, float4 2x4, float4 1x8),
+    on shapes with ragged column tiles and ragged row tiles, single pass and
+    segmented; float4 shapes fall back to scalar where rows are not aligned."""
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, variant)
+    for shape, segs in (((3, 1001, 388), 0), ((2, 333, 132), 5), ((5, 77, 4096), 0), ((2, 900, 36), 3),
+                        ((2, 130, 37), 0)):
+        L.set_option(L.OPT_AXIS_SPLIT, segs)
+        check(shape, 1, reverse, exclusive)
