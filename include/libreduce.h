@@ -282,7 +282,7 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *   LIBREDUCE_OPT_SCAN_COLS_VARIANT  scan along a strided axis (inner > 1), block shape:
  *                                 0 scalar columns, 2 warps across x 4 down the axis;
  *                                 1 float4 columns, 2 x 4; 2 float4 columns, 1 x 8
- *                                 (float4 needs inner % 4 == 0 and aligned x, y) */
+ *                                 (float4 columns need inner % 4 == 0 and aligned x, y) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6
 #define LIBREDUCE_OPT_RSCAN_VARIANT 7

@@ -596,16 +596,15 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
   const int64_t forced_v = g_opt_scan_cols_variant.load();
   const int64_t forced = g_opt_axis_split.load();
   // Fractions of the copy bandwidth each shape reaches on [128, 4096, 4096]
-  // (scalar: 0.75 when the rows are not 16-byte aligned).
+  // (the scalar shape: 0.75 on [128, 4096, 4095], whose rows are not 16-byte
+  // aligned).
   const double base[kNumScanColsVariants] = {vec4 ? 0.906 : 0.75, 0.976, 0.977};
-  int variant = kScanColsV1;
+  const bool force = forced_v >= 0 && forced_v < kNumScanColsVariants && (!scan_cols_vec4((int)forced_v) || vec4);
+  int variant = vec4 ? kScanColsV4 : kScanColsV1;
   int64_t segs = 1;
   double best = -1.0;
   for (int v = 0; v < kNumScanColsVariants; ++v) {
-    if (scan_cols_vec4(v) && !vec4) continue;
-    if (forced_v >= 0 && forced_v < kNumScanColsVariants && (!scan_cols_vec4((int)forced_v) || vec4) &&
-        v != forced_v)
-      continue;
+    if (force ? v != forced_v : (scan_cols_vec4(v) && !vec4)) continue;
     const int64_t cw = scan_cols_block_width(v);
     int64_t units = 0;
     if (mul_overflows(outer, ceil_div(inner, cw), &units)) return LIBREDUCE_ERR_OVERFLOW;

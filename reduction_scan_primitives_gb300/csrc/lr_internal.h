@@ -165,7 +165,7 @@ enum ScanColsVariant {
   kScanColsV4Y8 = 2,  // VEC 4, WX 1, WY 8, U 8 (same)
   kNumScanColsVariants
 };
-inline bool scan_cols_vec4(int variant) { return variant != kScanColsV1; }
+inline bool scan_cols_vec4(int variant) { return variant == kScanColsV4 || variant == kScanColsV4Y8; }
 enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
 
 // Elements per tile of the reduce-then-scan passes.

@@ -701,10 +701,11 @@ __global__ void __launch_bounds__(kThreads, VEC == 4 ? 3 : 4) k_scan_cols(ScanCo
             const float own = p.exclusive ? (u > 0 ? q[u - 1][c] : 0.f) : q[u][c];
             out[c] = b[c] + (pre[c] + own);
           }
-          if constexpr (VEC == 4)
+          if constexpr (VEC == 4) {
             st_stream4(yr, make_float4(out[0], out[1], out[2], out[3]));
-          else
+          } else {
             st_stream1(yr, out[0]);
+          }
         }
         yr += sj;
       }

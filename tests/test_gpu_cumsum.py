@@ -147,10 +147,12 @@ def test_axis_segmented_integers_exact(reverse, exclusive):
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
 def test_axis_every_block_shape(variant, reverse, exclusive):
     """Each column-scan block shape (scalar 2x4 warps, float4 2x4, float4 1x8),
-    on shapes with ragged column tiles and ragged row tiles, single pass and
-    segmented; float4 shapes fall back to scalar where rows are not aligned."""
+    on shapes with ragged column tiles and ragged row tiles, rows of every
+    16-byte misalignment, single pass and segmented; float4 shapes fall back
+    to the automatic choice where rows are not aligned."""
     L.set_option(L.OPT_SCAN_COLS_VARIANT, variant)
-    for shape, segs in (((3, 1001, 388), 0), ((2, 333, 132), 5), ((5, 77, 4096), 0), ((2, 900, 36), 3),
-                        ((2, 130, 37), 0)):
+    for shape, segs, off in (((3, 1001, 388), 0, 0), ((2, 333, 132), 5, 0), ((5, 77, 4096), 0, 0),
+                             ((2, 900, 36), 3, 0), ((2, 130, 37), 0, 0), ((3, 500, 4095), 0, 0),
+                             ((2, 300, 258), 4, 1), ((2, 97, 301), 0, 3), ((4, 64, 1000), 0, 2)):
         L.set_option(L.OPT_AXIS_SPLIT, segs)
-        check(shape, 1, reverse, exclusive)
+        check(shape, 1, reverse, exclusive, offset=off, out_offset=(off * 3) % 4)
