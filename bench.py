@@ -47,6 +47,7 @@ STEP_WORKLOADS = ["sum_1e9", "axis_128x4096x4095_d1", "axis_4096x65536_d1", "axi
                   "rcumsum_32768x32768", "rcumsum_1x1e9"]
 # Follow-on forms, timed separately from the step (reported under next_rows).
 NEXT_WORKLOADS = ["cumsum_fwd_32768x32768", "cumsum_fwd_excl_1x1e9", "cumsum_128x4096x4095_d1",
+                  "cumsum_64x16384x1024_d1", "cumsum_2x8192x4096_d1", "rcumsum_1x1e9_rts",
                   "max_1e9", "norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0",
                   "rcumsum_1x1e9_ws", "axis_65536x4096_d0_ws"]
 # Small cases of each kernel for ncu captures: larger than L2, a few GB at most.
@@ -215,6 +216,14 @@ def make_call(name, x, out):
         return lambda: L.reduce_axis_op_ws_f32(x, w["dim"], w["rop"], ws=ws, out=out)
     if w["op"] == "cumsum":
         return lambda: L.cumsum_f32(x, w["dim"], reverse=w["reverse"], exclusive=w["exclusive"], out=out)
+    if w.get("strategy"):
+        def call():  # the scan strategy is a library option: set for this call only
+            L.set_option(L.OPT_SCAN_STRATEGY, w["strategy"])
+            try:
+                L.reverse_cumsum_f32(x, out=out)
+            finally:
+                L.set_option(L.OPT_SCAN_STRATEGY, 0)
+        return call
     if w["op"] == "reduce":
         if "dim" in w:
             return lambda: L.reduce_axis_op_f32(x, w["dim"], w["rop"], out=out)

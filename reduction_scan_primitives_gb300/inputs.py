@@ -86,6 +86,16 @@ WORKLOADS = {
                                dist="uniform_pm1", seed=11),
     "min_65536x4096_d0": dict(op="reduce", rop="min", shape=(65536, 4096), dim=0,
                               dist="uniform_pm1", seed=11),
+    # The reverse scan of one long row as three passes (reduce-then-scan), for
+    # comparison with the single-pass look-back on the same input.
+    "rcumsum_1x1e9_rts": dict(op="rcumsum", shape=(1, 1_000_000_000), dist="uniform01", seed=3,
+                              strategy=4),
+    # Column scans with few column tiles: one pass with warp-split blocks, and
+    # too few to fill the GPU (the axis is cut into segments, three passes).
+    "cumsum_64x16384x1024_d1": dict(op="cumsum", shape=(64, 16384, 1024), dim=1, reverse=True,
+                                    exclusive=False, dist="uniform01", seed=3),
+    "cumsum_2x8192x4096_d1": dict(op="cumsum", shape=(2, 8192, 4096), dim=1, reverse=False,
+                                  exclusive=True, dist="uniform01", seed=3),
     # The same calls with caller-provided scratch.
     "rcumsum_1x1e9_ws": dict(op="cumsum", shape=(1, 1_000_000_000), dim=1, reverse=True,
                              exclusive=False, dist="uniform01", seed=3, ws=True),

@@ -62,3 +62,26 @@ def error_ratio(gpu, ref, abs_ref):
 def bitwise_equal(a, b):
     import torch
     return torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def assert_op_close(gpu, ref, scale, op, count, what):
+    """mean: (1e-5 sum|x| + 1e-6) / count plus one fp32 rounding; norm:
+    1e-5 norm + 1e-6; max and min: exact (NaN for NaN)."""
+    g = np.asarray(to_np(gpu), np.float64).reshape(-1)
+    r = np.asarray(ref, np.float64).reshape(-1)
+    sc = np.asarray(scale, np.float64).reshape(-1)
+    nan = np.isnan(r)
+    assert np.array_equal(np.isnan(g), nan), f"{what}: NaN pattern differs"
+    g, r, sc = g[~nan], r[~nan], sc[~nan]
+    if op in ("max", "min"):
+        bad = np.flatnonzero(g != r)
+        assert bad.size == 0, f"{what}: {bad.size} differ, first {bad[0]}: {g[bad[0]]} vs {r[bad[0]]}"
+        return
+    if op == "mean":
+        tol = (1e-5 * sc + 1e-6) / max(count, 1) + 2.0 ** -24 * np.abs(r)
+    else:
+        tol = 1e-5 * r + 1e-6
+    fin = np.isfinite(r)
+    bad = np.flatnonzero(fin & ~(np.abs(g - r) <= tol))
+    assert bad.size == 0, f"{what}: {bad.size} out of tolerance, first {bad[0]}: {g[bad[0]]} vs {r[bad[0]]}"
+    assert np.array_equal(g[~fin], r[~fin])
