@@ -58,6 +58,10 @@ PROFILE_CASES = {
     "axis_65536x4096_d0": dict(inputs.WORKLOADS["axis_65536x4096_d0"]),
     "rcumsum_4096x32768": dict(op="rcumsum", shape=(4096, 32768), dist="uniform01", seed=3),
     "rcumsum_1x1e8": dict(op="rcumsum", shape=(1, 100_000_000), dist="uniform01", seed=3),
+    "cumsum_16x4096x4095_d1": dict(op="cumsum", shape=(16, 4096, 4095), dim=1, reverse=False,
+                                   exclusive=False, dist="normal", seed=7),
+    "cumsum_16x4096x4096_d1": dict(op="cumsum", shape=(16, 4096, 4096), dim=1, reverse=True,
+                                   exclusive=False, dist="uniform01", seed=3),
 }
 FALLBACK_HBM_GBS = 6800.0
 # Context only (another machine): the page's T4 figures for the 1D sum.
