@@ -477,12 +477,16 @@ int reduce_impl(const float* x, int64_t outer, int64_t reduce, int64_t inner, fl
 }
 
 constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): well under a second
-// L2-lag form: tiles between a tile's two touches.  Measured on one row of 1e9:
-// a reverse scan (descending addresses) keeps 768 tiles (24 MiB) in L2 and
-// runs at 91% of copy bandwidth; a forward scan (ascending) loses L2 hits
-// beyond ~512 tiles (78% at 768, 80% at 512).
-constexpr int64_t kLookbackLagReverse = 768;
-constexpr int64_t kLookbackLagForward = 512;
+// L2-lag form: tickets between a tile's two touches.  The lag must exceed the
+// blocks resident at once, or the write of tile t - lag waits on tiles still
+// in flight; past ~2000 tiles (64 MiB) the reread misses L2.  Measured on one
+// row of 1e9 with 608 resident blocks (4 per SM): reverse 55% at lag 384, 63%
+// at 512, 87% at 768, 94% at 1024, 87% at 1280, 76% at 1536; forward 84-85%
+// from 768 to 1152.  Default: 5/3 of the resident blocks, in steps of 64.
+int64_t lookback_lag(const DeviceState* st) {
+  const int64_t resident = (int64_t)st->sm_count * st->occ_lookback[kLookbackL2];
+  return std::max<int64_t>(64, ceil_div(resident * 5 / 3, 64) * 64);
+}
 
 int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
                        cudaStream_t s, int variant, int flags) {
@@ -499,9 +503,9 @@ int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t
   unsigned* counter = sc.header + 2;  // zero on entry; the block with the last ticket resets it
   const int64_t spin = g_opt_spin_limit.load();
   const int64_t lag_opt = g_opt_lookback_lag.load();
-  const int64_t lag_default = (flags & kScanMirror) ? kLookbackLagForward : kLookbackLagReverse;
-  const int64_t lag = variant == kLookbackL2 ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt : lag_default)
-                                             : 0;
+  const int64_t lag = variant == kLookbackL2
+                          ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt : lookback_lag(pv.st))
+                          : 0;
   RScanLookbackParams p{x, y, rows, N, tiles, sc.nodes, counter, sc.header,
                         sc.epoch, spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag,
                         flags};

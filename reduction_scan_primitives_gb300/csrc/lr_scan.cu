@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
 // in the other forms.
 // ---------------------------------------------------------------------------
 template <int SUB>
-__global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback_l2(RScanLookbackParams p) {
+__global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookbackParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * 4;
   __shared__ __align__(128) float s_tile[TILE];
   __shared__ unsigned long long s_bar;
