@@ -272,7 +272,10 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *                                 kernel: 0 -> 4, 1 -> 8, 2 -> 16 (x 16 bytes)
  *   LIBREDUCE_OPT_COLS_VARIANT    inner > 1 kernel: 0..2 scalar columns with 1, 4 or
  *                                 8 warps along the reduce dim; 3..5 the same with
- *                                 float4 columns (needs inner % 4 == 0, aligned x)
+ *                                 float4 columns (needs inner % 4 == 0, aligned x);
+ *                                 6, 7 the narrow-row kernel, a block or a warp per plane
+ *                                 (inner <= 32 scalar or 128 float4 columns: the
+ *                                 automatic choice there)
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
  *                                 2 float4 x 4 (float4 needs N % 4 == 0, aligned x, y)
  *   LIBREDUCE_OPT_WAVES           1D sum: blocks = waves x resident blocks (0 = automatic:
@@ -281,7 +284,10 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *                                 tile's sum and the reread that writes it (0 = automatic)
  *   LIBREDUCE_OPT_SCAN_COLS_VARIANT  scan along a strided axis (inner > 1), block shape:
  *                                 0 scalar columns, 2 warps across x 4 down the axis;
- *                                 1 float4 columns, 2 x 4; 2 float4 columns, 1 x 8
+ *                                 1 float4 columns, 2 x 4; 2 float4 columns, 1 x 8;
+ *                                 3, 4 the narrow-row scan, tiles in shared memory or a
+ *                                 warp per (plane, segment) (inner <= 32 scalar or 128
+ *                                 float4 columns: the automatic choice there)
  *                                 (float4 columns need inner % 4 == 0 and aligned x, y) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6

@@ -45,6 +45,9 @@ struct DeviceState {
   std::atomic<unsigned> epoch{0};
   int occ_lookback[kNumLookbackVariants] = {};
   int occ_scan_cols[kNumScanColsVariants] = {};
+  int occ_narrow[2][kNumReduceOps] = {};  // [vec4][op]
+  int occ_scan_narrow[2] = {};            // [vec4]
+  int occ_scan_narrow_warp[2] = {};       // [vec4]
 };
 
 std::mutex g_mu;
@@ -90,6 +93,12 @@ int device_state(DeviceState** out, int* dev_out) {
       st.occ_lookback[v] = std::max(1, occupancy_rscan_lookback(v));
     for (int v = 0; v < kNumScanColsVariants; ++v)
       st.occ_scan_cols[v] = std::max(1, occupancy_scan_cols(v));
+    for (int v4 = 0; v4 < 2; ++v4) {
+      for (int op = 0; op < kNumReduceOps; ++op)
+        st.occ_narrow[v4][op] = std::max(1, occupancy_reduce_narrow(v4 ? 4 : 1, op));
+      st.occ_scan_narrow[v4] = std::max(1, occupancy_scan_narrow(v4 ? 4 : 1));
+      st.occ_scan_narrow_warp[v4] = std::max(1, occupancy_scan_narrow_warp(v4 ? 4 : 1));
+    }
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
   }
@@ -360,10 +369,85 @@ int run_rows_warp(const Provider& pv, const float* x, int64_t rows, int64_t len,
   return launched(launch_reduce_rows_warp(op, p, grid, s));
 }
 
+// Narrow rows: inner is at most 32 column groups of VEC floats (VEC = 4 when
+// inner % 4 == 0 and x is 16-byte aligned).
+bool narrow_rows(const float* x, const float* y, int64_t inner, int* vec) {
+  const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
+                    ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
+  *vec = vec4 ? 4 : 1;
+  return inner > 1 && inner <= 32 * *vec;
+}
+
+// A warp per plane pays when the planes are many and small: a block per plane
+// would spend its time starting up, and there are enough planes to fill the
+// GPU with warps (measured on [100000, 100, 3]: 46% against 6% of copy
+// bandwidth; on [1024, 8192, 64] the block form is ahead, 99% against 81%).
+bool narrow_warp_reduce(const DeviceState* st, int64_t outer, int64_t reduce, int64_t inner) {
+  return outer >= (int64_t)st->sm_count * 32 && reduce * inner <= 64 * 1024;
+}
+
+// Axis reduction over narrow rows: one block per (o, slice); when outer alone
+// cannot fill the GPU the reduce axis is sliced so the grid is one full wave
+// (as run_cols does), each slice at least one step of U = 8 rows per row
+// group; the last block of o combines the slices.
+int run_narrow(const Provider& pv, const float* x, int64_t outer, int64_t reduce, int64_t inner,
+               float* out, int op, int epi, int vec, int64_t forced_splits, cudaStream_t s) {
+  DeviceState* st = pv.st;
+  const int64_t slots = (int64_t)st->sm_count * st->occ_narrow[vec == 4][op];
+  const int64_t groups = kThreads / (inner / vec);
+  int64_t splits = 1;
+  if (forced_splits > 0) {
+    splits = std::min(forced_splits, reduce);
+  } else if (outer < slots) {
+    splits = std::max<int64_t>(1, slots / outer);
+    splits = std::min(splits, std::max<int64_t>(1, reduce / (8 * groups)));
+  }
+  if (splits > 1) {  // the slices must fit the tickets and partials
+    const int64_t cap = outer > kMaxTickets ? 1 : kMaxPartials / (outer * inner);
+    splits = cap < 2 ? 1 : std::min(splits, cap);
+  }
+  int64_t rows_per_split = ceil_div(reduce, splits);
+  splits = ceil_div(reduce, rows_per_split);
+  int64_t grid = 0;
+  if (mul_overflows(outer, splits, &grid) || grid > INT32_MAX) return LIBREDUCE_ERR_OVERFLOW;
+  Need need;
+  if (splits > 1) {
+    need.tickets = outer;
+    need.partials = outer * splits * inner;
+  }
+  Scratch sc;
+  int rc = acquire(pv, need, &sc, s);
+  if (rc) return rc;
+  NarrowParams p{x, outer, reduce, inner, splits, rows_per_split, out, sc.partials, inner,
+                 sc.tickets, epi, 0};
+  return launched(launch_reduce_narrow(vec, op, p, grid, s));
+}
+
 int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, int64_t inner,
              float* out, int op, int epi, cudaStream_t s) {
   DeviceState* st = pv.st;
   const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
+  {
+    // Narrow rows take the narrow kernel unless a wide shape is forced (sums).
+    int vec = 1;
+    const int64_t fv = g_opt_cols_variant.load();
+    const bool wide_forced = op == kOpSum && fv >= 0 && fv < kNumColsVariants;
+    if (narrow_rows(x, x, inner, &vec) && !wide_forced) {
+      // Many small planes: a warp per plane; otherwise a block per (plane, slice).
+      const bool warp_form = fv == kColsNarrowWarp || (fv != kColsNarrow && narrow_warp_reduce(st, outer, reduce, inner));
+      if (warp_form) {
+        Need need;
+        Scratch sc;
+        int rc = acquire(pv, need, &sc, s);
+        if (rc) return rc;
+        const int64_t grid = ceil_div(outer, kThreads / 32);
+        if (grid > INT32_MAX) return LIBREDUCE_ERR_OVERFLOW;
+        NarrowParams p{x, outer, reduce, inner, 1, reduce, out, nullptr, inner, nullptr, epi, 0};
+        return launched(launch_reduce_narrow_warp(vec, op, p, grid, s));
+      }
+      return run_narrow(pv, x, outer, reduce, inner, out, op, epi, vec, g_opt_axis_split.load(), s);
+    }
+  }
   int variant = vec4 ? kColsV4W4 : kColsV1W4;
   const int64_t forced_v = g_opt_cols_variant.load();
   if (op == kOpSum && forced_v >= 0 && forced_v < kNumColsVariants) {
@@ -567,6 +651,9 @@ int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, 
   return launched(launch_rscan_rows(variant, p, grid, s));
 }
 
+int run_scan_narrow(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
+                    float* y, bool reverse, bool exclusive, int vec, bool warp_form, cudaStream_t s);
+
 // Predicted fraction of the copy bandwidth that a column scan reaches with
 // `units` equally long blocks, `slots` of them resident at once, a fraction
 // lane_eff of the lanes of a column tile holding columns, and `base` the
@@ -595,6 +682,20 @@ double predict_scan_cols(int64_t units, int64_t slots, double lane_eff, double b
 int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
                   float* y, bool reverse, bool exclusive, cudaStream_t s) {
   DeviceState* st = pv.st;
+  {
+    int nvec = 1;
+    const int64_t fv = g_opt_scan_cols_variant.load();
+    if (narrow_rows(x, y, inner, &nvec) && (fv < 0 || fv == kScanColsNarrow || fv == kScanColsNarrowWarp)) {
+      // The block form walks tiles of T rows; a plane of fewer than T/2 rows
+      // would leave most of its threads idle: a warp per plane instead
+      // (measured on [100000, 100, 3]: 25% against 4% of copy bandwidth; on
+      // larger planes the block form is ahead, e.g. 66% against 20% on
+      // [1000, 10000, 8]).
+      const bool warp_form =
+          fv == kScanColsNarrowWarp || (fv < 0 && 2 * N < scan_narrow_tile_rows(nvec, inner));
+      return run_scan_narrow(pv, x, outer, N, inner, y, reverse, exclusive, nvec, warp_form, s);
+    }
+  }
   const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
                     ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
   const int64_t forced_v = g_opt_scan_cols_variant.load();
@@ -663,6 +764,67 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
   ScanColsParams p3{x, y, outer, N, inner, reverse ? 1 : 0, exclusive ? 1 : 0, carries, segs, seg_len,
                     inner_pad};
   return launched(launch_scan_cols(variant, p3, grid_for(units * segs), s));
+}
+
+// Scans along a strided axis with narrow rows: one block per (o, segment),
+// walking the segment in shared-memory tiles.  When outer alone cannot fill
+// the GPU the axis is cut into segments and scanned in three passes, as in
+// run_scan_cols: segment sums from the narrow reduction (kept slices, rows
+// padded to a multiple of 4 floats with zeros), an exclusive scan of the sums
+// along the segments, then every segment rescanned from its carry.
+int run_scan_narrow(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
+                    float* y, bool reverse, bool exclusive, int vec, bool warp_form, cudaStream_t s) {
+  DeviceState* st = pv.st;
+  int64_t tpr = 1;
+  while (tpr * vec < inner) tpr <<= 1;
+  // Units are warps (warp form) or blocks; rows one unit walks per step.
+  const int64_t per_block = warp_form ? kThreads / 32 : 1;
+  const int64_t slots = (int64_t)st->sm_count * per_block *
+                        (warp_form ? st->occ_scan_narrow_warp[vec == 4] : st->occ_scan_narrow[vec == 4]);
+  const int64_t tile_rows = warp_form ? 8 * (32 / tpr) : scan_narrow_tile_rows(vec, inner);
+  const double lane_eff = (double)inner / (double)(tpr * vec);
+  const int64_t part_stride = round_up(inner, 4);
+  int64_t segs = 1;
+  const int64_t forced = g_opt_axis_split.load();
+  if (forced > 0) {
+    segs = std::min(forced, N);
+  } else {
+    const int64_t cand = std::min(ceil_div(4 * slots, outer), std::max<int64_t>(1, N / (4 * tile_rows)));
+    if (cand > 1 && predict_scan_cols(outer * cand, slots, lane_eff, 1.0) / 1.5 >
+                        predict_scan_cols(outer, slots, lane_eff, 1.0))
+      segs = cand;
+  }
+  if (segs > 1) {
+    const int64_t cap = kMaxPartials / (2 * outer * part_stride);
+    segs = cap < 2 ? 1 : std::min(segs, cap);
+  }
+  const int64_t seg_len = ceil_div(N, segs);
+  segs = ceil_div(N, seg_len);
+  int64_t units = 0;
+  if (mul_overflows(outer, segs, &units)) return LIBREDUCE_ERR_OVERFLOW;
+  const auto grid_for = [](int64_t blocks) { return std::max<int64_t>(1, std::min<int64_t>(blocks, INT32_MAX)); };
+  Need need;  // also answers a size query when nothing is needed
+  if (segs > 1) need.partials = 2 * outer * segs * part_stride;
+  Scratch sc;
+  int rc = acquire(pv, need, &sc, s);
+  if (rc) return rc;
+  const auto scan = [&](const ScanColsParams& q, int v) {
+    return warp_form ? launch_scan_narrow_warp(v, q, grid_for(ceil_div(q.outer * q.segs, per_block)), s)
+                     : launch_scan_narrow(v, q, grid_for(q.outer * q.segs), s);
+  };
+  if (segs == 1) {
+    ScanColsParams p{x, y, outer, N, inner, reverse ? 1 : 0, exclusive ? 1 : 0, nullptr, 1, N, 0};
+    return launched(scan(p, vec));
+  }
+  float* sums = sc.partials;                                 // [outer, segs, part_stride]
+  float* carries = sc.partials + outer * segs * part_stride;  // same shape
+  NarrowParams p1{x, outer, N, inner, segs, seg_len, nullptr, sums, part_stride, nullptr, kEpiNone, 1};
+  if ((rc = launched(launch_reduce_narrow(vec, kOpSum, p1, units, s)))) return rc;
+  ScanColsParams p2{sums, carries, outer, segs, part_stride, reverse ? 1 : 0, 1, nullptr, 1, segs, 0};
+  if ((rc = launched(scan(p2, 4)))) return rc;
+  ScanColsParams p3{x, y, outer, N, inner, reverse ? 1 : 0, exclusive ? 1 : 0, carries, segs, seg_len,
+                    part_stride};
+  return launched(scan(p3, vec));
 }
 
 // The cumulative sum behind every scan entry point.
@@ -848,7 +1010,7 @@ int libreduce_set_option(int option, int64_t value) {
       g_opt_contig_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_COLS_VARIANT:
-      if (value < -1 || value >= kNumColsVariants) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < -1 || value > kColsNarrowWarp) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_RSCAN_VARIANT:
@@ -856,7 +1018,7 @@ int libreduce_set_option(int option, int64_t value) {
       g_opt_rscan_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_SCAN_COLS_VARIANT:
-      if (value < -1 || value >= kNumScanColsVariants) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < -1 || value > kScanColsNarrowWarp) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_LOOKBACK_LAG:

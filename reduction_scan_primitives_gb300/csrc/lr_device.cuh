@@ -254,6 +254,53 @@ struct BlockedAcc {
   __device__ __forceinline__ float total() const { return Op::combine(hi, Op::combine(mid, lo)); }
 };
 
+// Running sum of tile totals: level 0 takes 32 tile totals, each higher level
+// 32 folds of the one below, the top one term per 32^4 tiles; hi holds the
+// levels above 0, so base() is one addition.
+template <int VEC>
+struct TileCarry {
+  float lv[5][VEC];
+  float hi[VEC];
+  int n0 = 0, n1 = 0, n2 = 0, n3 = 0;
+  __device__ __forceinline__ explicit TileCarry(const float (&init)[VEC]) {
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) lv[k][c] = 0.f;
+      lv[4][c] = hi[c] = init[c];
+    }
+  }
+  __device__ __forceinline__ void fold(int k) {
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      lv[k + 1][c] += lv[k][c];
+      lv[k][c] = 0.f;
+    }
+  }
+  __device__ __forceinline__ void add(const float (&t)[VEC]) {
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) lv[0][c] += t[c];
+    if (++n0 < 32) return;
+    n0 = 0;
+    fold(0);
+    if (++n1 == 32) {
+      n1 = 0;
+      fold(1);
+      if (++n2 == 32) {
+        n2 = 0;
+        fold(2);
+        if (++n3 == 32) {
+          n3 = 0;
+          fold(3);
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) hi[c] = ((lv[4][c] + lv[3][c]) + lv[2][c]) + lv[1][c];
+  }
+  __device__ __forceinline__ float base(int c) const { return hi[c] + lv[0][c]; }
+};
+
 // Output epilogue: the mean divides by the element count (in double, then
 // rounds once to fp32); the Euclidean norm takes the square root of the sum
 // of squares (IEEE, correctly rounded).

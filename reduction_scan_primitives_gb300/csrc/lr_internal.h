@@ -94,6 +94,22 @@ struct TileCarryParams {
   int flags;
 };
 
+// --- Axis reduction over narrow rows (inner <= 32 column groups of VEC) -----
+// x: [outer, reduce, inner]; one block per (o, slice).  With splits > 1 each
+// slice's column values go to partials[(o*splits + s)*part_stride + c] and the
+// last block of o (ticket) combines them, unless keep_partials is set.
+struct NarrowParams {
+  const float* x;
+  int64_t outer, reduce, inner;
+  int64_t splits, rows_per_split;
+  float* out;
+  float* partials;
+  int64_t part_stride;
+  unsigned* tickets;  // outer, zero on entry, left zero on exit
+  int epi;
+  int keep_partials;
+};
+
 // --- Cumulative sum along a strided axis (inner > 1) -------------------------
 // x, y: [outer, N, inner]; one block per (o, segment, column tile).
 struct ScanColsParams {
@@ -149,6 +165,10 @@ enum ColsVariant {
   kColsV4W8 = 5,
   kNumColsVariants
 };
+// Option values (not kernel shapes of the enum above): the narrow-row kernel,
+// block form (one block per (o, slice)) and warp form (one warp per o).
+constexpr int kColsNarrow = kNumColsVariants;
+constexpr int kColsNarrowWarp = kNumColsVariants + 1;
 enum RScanVariant { kRScanV1S4 = 0, kRScanV4S2 = 1, kRScanV4S4 = 2, kNumRScanVariants };
 enum LookbackVariant {
   kLookbackV1 = 0,  // scalar items, one tile per block, tile kept in registers
@@ -166,6 +186,10 @@ enum ScanColsVariant {
   kNumScanColsVariants
 };
 inline bool scan_cols_vec4(int variant) { return variant == kScanColsV4 || variant == kScanColsV4Y8; }
+// Option values: the narrow-row scan, block form (tiles in shared memory) and
+// warp form (one warp per (o, segment)).
+constexpr int kScanColsNarrow = kNumScanColsVariants;
+constexpr int kScanColsNarrowWarp = kNumScanColsVariants + 1;
 enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
 
 // Elements per tile of the reduce-then-scan passes.
@@ -191,6 +215,17 @@ cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int
                                   cudaStream_t s);
 cudaError_t launch_scan_cols(int variant, const ScanColsParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_tile_sums(int variant, const TileSumsParams& p, int64_t grid, cudaStream_t s);
+// Narrow rows: vec is 1 or 4 (4 needs inner % 4 == 0 and 16-byte aligned x, y);
+// inner <= 32 * vec.
+cudaError_t launch_reduce_narrow(int vec, int op, const NarrowParams& p, int64_t grid, cudaStream_t s);
+cudaError_t launch_scan_narrow(int vec, const ScanColsParams& p, int64_t grid, cudaStream_t s);
+int occupancy_reduce_narrow(int vec, int op);
+int occupancy_scan_narrow(int vec);
+int64_t scan_narrow_tile_rows(int vec, int64_t inner);  // rows of one tile, in scan order
+// Warp forms (one warp per (o, segment) / per o): eight units per block.
+cudaError_t launch_scan_narrow_warp(int vec, const ScanColsParams& p, int64_t grid, cudaStream_t s);
+int occupancy_scan_narrow_warp(int vec);
+cudaError_t launch_reduce_narrow_warp(int vec, int op, const NarrowParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_tile_carry_scan(int variant, const TileCarryParams& p, int64_t grid, cudaStream_t s);
 
 // Host helpers defined in lr_api.cu, for entry points in other files.

@@ -113,3 +113,49 @@ def test_nan_inf():
     got = gpu_axis(x, 4, 100, 8)
     assert np.isnan(got[1, 3]) and got[2, 4] == float("inf")
     assert np.isfinite(np.delete(got.reshape(-1), [1 * 8 + 3, 2 * 8 + 4])).all()
+
+
+NARROW = [(2, 30000, 4), (5, 777, 3), (3, 1000, 32), (2, 5000, 128), (4, 1001, 12), (1, 200000, 2),
+          (100, 300, 7), (2, 70001, 16), (64, 64, 5)]
+
+
+@pytest.mark.parametrize("shape", NARROW)
+@pytest.mark.parametrize("split", [0, 1, 5, 333])
+def test_narrow_rows(shape, split):
+    """Rows of at most 32 column groups take the narrow kernel (the plane read
+    contiguously, a fixed column group per thread, row groups joined by a
+    tree), one block per plane or sliced (forced or automatic); the wide
+    kernel forced on the same shapes agrees with the oracle too."""
+    L.set_option(L.OPT_AXIS_SPLIT, split)
+    check(*shape, what=f"narrow {shape} split={split}")
+    L.set_option(L.OPT_COLS_VARIANT, 7)  # a warp per plane
+    check(*shape, what=f"narrow warp {shape}")
+    L.set_option(L.OPT_COLS_VARIANT, 1)
+    check(*shape, what=f"wide {shape} split={split}")
+
+
+@pytest.mark.parametrize("shape", [(5000, 100, 3), (20000, 7, 4), (3000, 64, 32), (2000, 33, 128), (4864, 2, 2)])
+def test_narrow_many_small_planes(shape):
+    """Many small planes take the warp-per-plane form by default."""
+    got, ref = check(*shape, what=f"small planes {shape}")
+    x = inputs.make(shape, "int:-8:8", 4)
+    ref, _ = oracle.axis_sum(x.numpy(), *shape)
+    assert_exact(gpu_axis(x, *shape), ref, f"small planes int {shape}")
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_narrow_rows_misaligned(offset):
+    for shape in ((3, 5000, 8), (2, 3001, 32), (2, 999, 128)):
+        check(*shape, offset=offset, what=f"narrow {shape} off={offset}")
+
+
+def test_narrow_rows_integer_exact_and_bitwise():
+    for shape, split in (((4, 20000, 4), 0), ((3, 7001, 3), 7), ((2, 100003, 16), 0)):
+        L.set_option(L.OPT_AXIS_SPLIT, split)
+        x = inputs.make(shape, "int:-8:8", 9)
+        ref, _ = oracle.axis_sum(x.numpy(), *shape)
+        xd = on_device(x)
+        a = L.reduce_axis_f32(xd, 1).clone()
+        b = L.reduce_axis_f32(xd, 1).clone()
+        assert_exact(a.cpu().numpy(), ref, f"narrow int {shape}")
+        assert bitwise_equal(a, b)

@@ -156,3 +156,46 @@ def test_axis_every_block_shape(variant, reverse, exclusive):
                              ((2, 300, 258), 4, 1), ((2, 97, 301), 0, 3), ((4, 64, 1000), 0, 2)):
         L.set_option(L.OPT_AXIS_SPLIT, segs)
         check(shape, 1, reverse, exclusive, offset=off, out_offset=(off * 3) % 4)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape,segs,offset", [((2, 30000, 4), 0, 0), ((5, 777, 3), 0, 0), ((3, 1000, 32), 0, 0),
+                                               ((2, 5000, 128), 0, 0), ((4, 1001, 12), 3, 0),
+                                               ((1, 200000, 2), 0, 0), ((100, 300, 7), 0, 0),
+                                               ((2, 70001, 16), 17, 0), ((3, 5000, 8), 0, 1),
+                                               ((2, 3001, 20), 5, 2), ((1, 3, 5), 0, 0), ((2, 1, 4), 0, 0),
+                                               ((3, 4097, 31), 0, 3)])
+@pytest.mark.parametrize("form", [-1, 3, 4], ids=["auto", "block", "warp"])
+def test_axis_narrow(shape, segs, offset, reverse, exclusive, form):
+    """Rows of at most 32 column groups: the narrow scan, with tiles staged in
+    shared memory (block form) or a warp per (plane, segment) scanning row
+    groups with shuffles (warp form), one unit per plane or cut into segments
+    (forced, or automatic when outer is small)."""
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, form)
+    if segs:
+        L.set_option(L.OPT_AXIS_SPLIT, segs)
+    got, _ = check(shape, 1, reverse, exclusive, offset=offset, out_offset=(offset * 3) % 4)
+    if exclusive:
+        edge = 0 if not reverse else shape[1] - 1
+        assert np.all(got[:, edge, :] == 0.0)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("form", [3, 4], ids=["block", "warp"])
+def test_axis_narrow_integers_exact(reverse, exclusive, form):
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, form)
+    for shape, segs in (((3, 4000, 4), 0), ((2, 20001, 3), 9), ((1, 100_000, 16), 0), ((4, 999, 32), 5),
+                        ((5000, 7, 3), 0)):
+        L.set_option(L.OPT_AXIS_SPLIT, segs)
+        x = inputs.make(shape, "int:0:3", 8)
+        o, n, i = L.canonical_axis(x.shape, 1)
+        ref, _ = oracle.cumsum(x.numpy(), o, n, i, reverse, exclusive)
+        assert_exact(run(x, 1, reverse, exclusive).reshape(-1), ref.reshape(-1), f"narrow int {shape} segs={segs}")
+
+
+def test_axis_narrow_wide_forced_agree():
+    """The wide column scan forced on narrow rows also matches the oracle."""
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, 0)
+    for shape in ((2, 3000, 4), (3, 1000, 7), (2, 500, 32)):
+        check(shape, 1, True, False)
+        check(shape, 1, False, True)

@@ -90,3 +90,17 @@ def test_deterministic_bitwise():
             assert bitwise_equal(a, b), (op, dim)
         a = L.reduce_f32(xd, op).clone()
         assert bitwise_equal(a, L.reduce_f32(xd, op)), op
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("shape", [(3, 5000, 4), (2, 30001, 3), (5, 999, 32), (2, 4000, 128), (64, 100, 6)])
+@pytest.mark.parametrize("split", [0, 9])
+def test_narrow_rows_ops(op, shape, split):
+    """Mean, max, min and norm on the narrow-row kernel, with and without
+    forced slices (the last block combines them), and a warp per plane."""
+    L.set_option(L.OPT_AXIS_SPLIT, split)
+    check_axis(shape, 1, op)
+    check_axis(shape, 1, op, offset=1)
+    L.set_option(L.OPT_COLS_VARIANT, 7)
+    check_axis(shape, 1, op)
+    check_axis((3000, 50, shape[2]), 1, op, offset=1)
