@@ -369,21 +369,22 @@ int run_rows_warp(const Provider& pv, const float* x, int64_t rows, int64_t len,
   return launched(launch_reduce_rows_warp(op, p, grid, s));
 }
 
-// Narrow rows: inner is at most 32 column groups of VEC floats (VEC = 4 when
-// inner % 4 == 0 and x is 16-byte aligned).
+// Narrow rows: at most 256 scalar or 128 float4 columns (VEC = 4 when inner
+// % 4 == 0 and x, y are 16-byte aligned).  Beyond that the wide kernels keep
+// every lane busy (and reach the copy bandwidth on 16-byte aligned rows).
 bool narrow_rows(const float* x, const float* y, int64_t inner, int* vec) {
   const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
                     ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
   *vec = vec4 ? 4 : 1;
-  return inner > 1 && inner <= 32 * *vec;
+  return inner > 1 && inner <= (vec4 ? 128 : 256);
 }
 
 // A warp per plane pays when the planes are many and small: a block per plane
 // would spend its time starting up, and there are enough planes to fill the
 // GPU with warps (measured on [100000, 100, 3]: 46% against 6% of copy
 // bandwidth; on [1024, 8192, 64] the block form is ahead, 99% against 81%).
-bool narrow_warp_reduce(const DeviceState* st, int64_t outer, int64_t reduce, int64_t inner) {
-  return outer >= (int64_t)st->sm_count * 32 && reduce * inner <= 64 * 1024;
+bool narrow_warp_reduce(const DeviceState* st, int64_t outer, int64_t reduce, int64_t inner, int vec) {
+  return inner <= 32 * vec && outer >= (int64_t)st->sm_count * 32 && reduce * inner <= 64 * 1024;
 }
 
 // Axis reduction over narrow rows: one block per (o, slice); when outer alone
@@ -434,7 +435,8 @@ int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, 
     const bool wide_forced = op == kOpSum && fv >= 0 && fv < kNumColsVariants;
     if (narrow_rows(x, x, inner, &vec) && !wide_forced) {
       // Many small planes: a warp per plane; otherwise a block per (plane, slice).
-      const bool warp_form = fv == kColsNarrowWarp || (fv != kColsNarrow && narrow_warp_reduce(st, outer, reduce, inner));
+      const bool warp_form = inner <= 32 * vec && (fv == kColsNarrowWarp ||
+                                                   (fv != kColsNarrow && narrow_warp_reduce(st, outer, reduce, inner, vec)));
       if (warp_form) {
         Need need;
         Scratch sc;
@@ -691,8 +693,8 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
       // (measured on [100000, 100, 3]: 25% against 4% of copy bandwidth; on
       // larger planes the block form is ahead, e.g. 66% against 20% on
       // [1000, 10000, 8]).
-      const bool warp_form =
-          fv == kScanColsNarrowWarp || (fv < 0 && 2 * N < scan_narrow_tile_rows(nvec, inner));
+      const bool warp_form = inner <= 32 * nvec && (fv == kScanColsNarrowWarp ||
+                                                    (fv < 0 && 2 * N < scan_narrow_tile_rows(nvec, inner)));
       return run_scan_narrow(pv, x, outer, N, inner, y, reverse, exclusive, nvec, warp_form, s);
     }
   }

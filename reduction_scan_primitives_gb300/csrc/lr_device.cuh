@@ -141,6 +141,26 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, 
       : "memory");
 }
 
+// Per-thread asynchronous copies into shared memory (cp.async).  The first
+// `src_bytes` of the copy come from global memory and the rest is filled with
+// zeros, so src_bytes == 0 writes a zero item without reading anything (`src`
+// must still be a valid address).  Completion: commit_group, then wait_group.
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src, unsigned src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src, unsigned src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst_smem)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Reduction operators.  `prep` maps a loaded element to the value that is
 // combined (x*x for a sum of squares); `combine` is associative up to

@@ -160,101 +160,167 @@ __global__ void __launch_bounds__(kThreads) k_reduce_narrow(NarrowParams p) {
 
 // ---------------------------------------------------------------------------
 // Cumulative sum: block per (o, segment); tiles of T = G*U rows in scan order.
-// Thread (g, cg) owns scan-order rows [g*U, g*U + U) of the tile.  The tile
-// is staged in shared memory: the block copies it in with the reduction's
-// mapping (step k reads physical rows k*G .. k*G + G - 1: contiguous), each
-// thread scans its U rows there, the row groups are scanned with warp
-// shuffles (groups of a warp: stride tpr lanes) and warp totals, results go
-// back to the same places and the block copies the tile out contiguously.
-// Row group g's U rows sit at g*S in shared memory, S = U*inner + pad, the pad
-// chosen so that the lanes of one shared-memory access hit distinct banks.
-// tpr = threads per row, inner / VEC rounded up to a power of two (<= 32).
+// Thread (g, cg) owns scan-order rows [g*U, g*U + U) of the tile.  Tiles are
+// staged in shared memory, two buffers: while the block scans tile i, its
+// threads' cp.async copies bring tile i + 1 in, with the reduction's mapping
+// (step k copies physical rows k*G .. k*G + G - 1: contiguous in memory; rows
+// outside the segment arrive as zeros).  Each thread scans its U rows in
+// shared memory, the row groups are scanned with warp shuffles (groups of a
+// warp: stride tpr lanes) and warp totals, results go back to the same places
+// and the block stores the tile contiguously.  Row group g's U rows sit at
+// g*S, S = U*inner + pad, the pad chosen so that the lanes of one
+// shared-memory access hit distinct banks.  tpr = threads per row, inner / VEC
+// rounded up to a power of two (<= 256); from tpr = 32 on a row group spans
+// whole warps and the groups' totals meet in shared memory instead.  The
+// copies run one tile ahead across the block's planes and segments too.
 // ---------------------------------------------------------------------------
 template <int VEC, int U>
+__host__ __device__ constexpr int scan_narrow_cap() {  // floats of one tile buffer, pad included
+  return kThreads * U * VEC + (VEC == 4 ? 1024 : 4096);
+}
+
+template <int VEC, int U>
 __global__ void __launch_bounds__(kThreads) k_scan_narrow(ScanColsParams p) {
-  constexpr int kCap = kThreads * U * VEC + (VEC == 4 ? 1024 : 4096);
-  __shared__ __align__(16) float s_tile[kCap];
-  __shared__ __align__(16) float s_wt[kNW][32 * VEC];
+  constexpr int kCap = scan_narrow_cap<VEC, U>();
+  extern __shared__ __align__(16) float s_dyn[];         // two tile buffers of kCap floats
+  __shared__ __align__(16) float s_tot[kThreads * VEC];  // warp totals, or row-group totals
   const int64_t inner = p.inner;
   int tpr = 1;
-  while (tpr * VEC < inner) tpr <<= 1;
+  while (tpr * VEC < inner) tpr <<= 1;  // <= 256
   const int G = kThreads / tpr;
   const int T = G * U;
   const int pad = (VEC * tpr - (int)((U * inner) & 31) + 32) & 31;
   const int S = U * (int)inner + pad;
-  if (G * S > kCap) return;  // unreachable: inner <= 32*VEC keeps G*S within kCap
+  if (G * S > kCap) return;  // unreachable: tpr <= 256 keeps G*S within kCap
   const int t = threadIdx.x;
   const int lane = t & 31;
   const int warp = t >> 5;
   const int g = t / tpr;
   const int cg = t - g * tpr;
   const int col = cg * VEC;
-  const bool active = col < inner;  // with VEC == 4, inner % 4 == 0: all four columns
-  const int gpw = 32 / tpr;         // row groups per warp
+  const bool active = col < inner;      // with VEC == 4, inner % 4 == 0: all four columns
+  const bool wide_groups = tpr >= 32;   // a row group spans whole warps
+  const int gpw = wide_groups ? 1 : 32 / tpr;
+  const int gcols = tpr * VEC;          // row width of the row-group totals
   const int64_t units = p.outer * p.segs;
 
-  for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
-    const int64_t o = unit / p.segs;
-    const int64_t lo = (unit - o * p.segs) * p.seg_len;
-    const int64_t len = min(p.seg_len, p.N - lo);
-    const float* xo = p.x + o * p.N * inner + col;
-    float* yo = p.y + o * p.N * inner + col;
+  struct Unit {
+    int64_t lo, len, tiles;
+    const float* xo;
+    float* yo;
+  };
+  const auto unit_at = [&](int64_t u) {
+    Unit r;
+    const int64_t o = u / p.segs;
+    r.lo = (u - o * p.segs) * p.seg_len;
+    r.len = min(p.seg_len, p.N - r.lo);
+    r.tiles = (r.len + T - 1) / T;
+    r.xo = p.x + o * p.N * inner + col;
+    r.yo = p.y + o * p.N * inner + col;
+    return r;
+  };
+  // Physical rows of tile i: [phys_lo, phys_lo + T) clipped to the segment.
+  const auto phys_lo = [&](const Unit& un, int64_t i) {
+    return p.reverse ? un.lo + un.len - (i + 1) * T : un.lo + i * T;
+  };
+  // The tile geometry (G, S, inner) is hidden from the optimiser once per
+  // tile (Gt, St, It): otherwise it hoists every row's shared-memory offset
+  // out of the tile loop and holds them all in registers.
+  const auto issue = [&](float* buf, const Unit& un, int64_t i, int Gt, int St, int It) {
+    if (!active) return;
+    const int64_t pl = phys_lo(un, i);
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int pr = k * Gt + g;  // tile row; group pr / U, row pr % U within it
+      const int64_t row = pl + pr;
+      const bool ok = row >= un.lo && row < un.lo + un.len;
+      float* d = buf + (pr / U) * St + (pr % U) * It + col;
+      const float* src = ok ? un.xo + row * inner : un.xo;
+      if constexpr (VEC == 4)
+        cp_async16(d, src, ok ? 16u : 0u);
+      else
+        cp_async4(d, src, ok ? 4u : 0u);
+    }
+  };
+  const auto carry_of = [&](int64_t u) {
     float init[VEC];
 #pragma unroll
     for (int c = 0; c < VEC; ++c)
-      init[c] = (p.carry != nullptr && active) ? p.carry[unit * p.carry_stride + col + c] : 0.f;
-    TileCarry<VEC> tc(init);
-    for (int64_t t0 = 0; t0 < len; t0 += T) {
-      // Physical rows of this tile: [phys_lo, phys_lo + T) clipped to the segment.
-      const int64_t phys_lo = p.reverse ? lo + len - t0 - T : lo + t0;
-      const int64_t vlo = max(phys_lo, lo), vhi = min(phys_lo + T, lo + len);
-      // Copy in (contiguous): step k holds tile rows k*G + g.
-      float q[U][VEC];
+      init[c] = (p.carry != nullptr && active) ? p.carry[u * p.carry_stride + col + c] : 0.f;
+    return TileCarry<VEC>(init);
+  };
+
+  int64_t unit = blockIdx.x;
+  if (unit >= units) return;
+  Unit cu = unit_at(unit);
+  TileCarry<VEC> tc = carry_of(unit);
+  int cur = 0;
+  int64_t i = 0;
+  issue(s_dyn, cu, 0, G, S, (int)inner);
+  cp_async_commit();
+  while (true) {
+    int Gt = G, St = S, It = (int)inner;
+    asm volatile("" : "+r"(Gt), "+r"(St), "+r"(It));
+    // The next tile: this unit's next, or the first tile of the block's next
+    // unit, so the copies run ahead across planes and segments too.
+    int64_t nunit = unit, ni = i + 1;
+    if (ni >= cu.tiles) {
+      nunit = unit + gridDim.x;
+      ni = 0;
+    }
+    const bool more = nunit < units;
+    const Unit nu = (more && nunit != unit) ? unit_at(nunit) : cu;
+    float* buf = s_dyn + cur * kCap;
+    if (more) {
+      __syncthreads();  // the other buffer's last tile has been stored
+      issue(s_dyn + (cur ^ 1) * kCap, nu, ni, Gt, St, It);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // tile i is in shared memory for every thread
+    // Scan this thread's U rows (scan order u = 0 .. U-1).
+    float* base_p = buf + (p.reverse ? (Gt - 1 - g) : g) * St + col;
+    float q[U][VEC];
 #pragma unroll
-      for (int k = 0; k < U; ++k) {
-        const int64_t row = phys_lo + (int64_t)k * G + g;
-        if (active && g < G && row >= vlo && row < vhi) {
-          load_vec<VEC>(q[k], xo + row * inner);
-        } else {
-#pragma unroll
-          for (int c = 0; c < VEC; ++c) q[k][c] = 0.f;
-        }
+    for (int u = 0; u < U; ++u) {
+      const float* src = base_p + (p.reverse ? (U - 1 - u) : u) * It;
+      if constexpr (VEC == 4) {
+        const float4 f = active ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+        q[u][0] = f.x;
+        q[u][1] = f.y;
+        q[u][2] = f.z;
+        q[u][3] = f.w;
+      } else {
+        q[u][0] = active ? src[0] : 0.f;
       }
-      __syncthreads();  // the previous tile's copy-out has read s_tile
-      if (active) {
+    }
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-          const int pr = k * G + g;  // tile row; group pr / U, row pr % U within it
-          float* d = s_tile + (pr / U) * S + (pr % U) * (int)inner + col;
-          if constexpr (VEC == 4)
-            *reinterpret_cast<float4*>(d) = make_float4(q[k][0], q[k][1], q[k][2], q[k][3]);
-          else
-            d[0] = q[k][0];
-        }
-      }
+    for (int u = 1; u < U; ++u)
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) q[u][c] += q[u - 1][c];
+    float tot[VEC], pre[VEC], b[VEC];
+    if (wide_groups) {
+      // Row groups of whole warps: their totals through shared memory.
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) s_tot[g * gcols + col + c] = q[U - 1][c];
       __syncthreads();
-      // Scan this thread's U rows (scan order u = 0 .. U-1).
-      float* base_p = s_tile + (p.reverse ? (G - 1 - g) : g) * S + col;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const float* src = base_p + (p.reverse ? (U - 1 - u) : u) * (int)inner;
-        if constexpr (VEC == 4) {
-          const float4 f = active ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
-          q[u][0] = f.x;
-          q[u][1] = f.y;
-          q[u][2] = f.z;
-          q[u][3] = f.w;
-        } else {
-          q[u][0] = active ? src[0] : 0.f;
+      for (int c = 0; c < VEC; ++c) {
+        float r = 0.f, gp = 0.f;
+        for (int g2 = 0; g2 < Gt; ++g2) {
+          if (g2 == g) gp = r;
+          r += s_tot[g2 * gcols + col + c];
         }
+        tot[c] = r;
+        pre[c] = gp;
       }
-#pragma unroll
-      for (int u = 1; u < U; ++u)
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) q[u][c] += q[u - 1][c];
-      // Row groups of this warp: inclusive shuffle scan over them (stride tpr
-      // lanes), then the exclusive value from the group before.
-      float ex[VEC], tot[VEC], pre[VEC], b[VEC];
+    } else {
+      // Row groups of this warp: inclusive shuffle scan over them (stride
+      // tpr lanes), the exclusive value from the group before, and the warp
+      // totals in a fixed order.
+      float ex[VEC];
 #pragma unroll
       for (int c = 0; c < VEC; ++c) {
         float v = q[U - 1][c];
@@ -265,7 +331,7 @@ __global__ void __launch_bounds__(kThreads) k_scan_narrow(ScanColsParams p) {
         const float e = __shfl_up_sync(kFullMask, v, tpr);
         ex[c] = lane >= tpr ? e : 0.f;
         const float wt = __shfl_sync(kFullMask, v, (gpw - 1) * tpr + cg);
-        if (lane < tpr) s_wt[warp][col + c] = wt;
+        if (lane < tpr) s_tot[warp * 32 * VEC + col + c] = wt;
       }
       __syncthreads();
 #pragma unroll
@@ -274,54 +340,64 @@ __global__ void __launch_bounds__(kThreads) k_scan_narrow(ScanColsParams p) {
 #pragma unroll
         for (int w2 = 0; w2 < kNW; ++w2) {
           if (w2 == warp) wp = r;
-          r += s_wt[w2][col + c];
+          r += s_tot[w2 * 32 * VEC + col + c];
         }
         tot[c] = r;
         pre[c] = wp + ex[c];
-        b[c] = tc.base(c);
       }
-      // Results back to this thread's places in the tile.
-      if (active) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          float out[VEC];
-#pragma unroll
-          for (int c = 0; c < VEC; ++c) {
-            const float own = p.exclusive ? (u > 0 ? q[u - 1][c] : 0.f) : q[u][c];
-            out[c] = b[c] + (pre[c] + own);
-          }
-          float* dst = base_p + (p.reverse ? (U - 1 - u) : u) * (int)inner;
-          if constexpr (VEC == 4)
-            *reinterpret_cast<float4*>(dst) = make_float4(out[0], out[1], out[2], out[3]);
-          else
-            dst[0] = out[0];
-        }
-      }
-      __syncthreads();
-      // Copy out (contiguous), the mapping of the copy in.
-      if (active) {
-#pragma unroll
-        for (int k = 0; k < U; ++k) {
-          const int pr = k * G + g;
-          const int64_t row = phys_lo + pr;
-          if (g < G && row >= vlo && row < vhi) {
-            const float* src = s_tile + (pr / U) * S + (pr % U) * (int)inner + col;
-            float v[VEC];
-            if constexpr (VEC == 4) {
-              const float4 f = *reinterpret_cast<const float4*>(src);
-              v[0] = f.x;
-              v[1] = f.y;
-              v[2] = f.z;
-              v[3] = f.w;
-            } else {
-              v[0] = src[0];
-            }
-            store_vec<VEC>(yo + row * inner, v);
-          }
-        }
-      }
-      tc.add(tot);
     }
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) b[c] = tc.base(c);
+    // Results back to this thread's places in the tile.
+    if (active) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float out[VEC];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          const float own = p.exclusive ? (u > 0 ? q[u - 1][c] : 0.f) : q[u][c];
+          out[c] = b[c] + (pre[c] + own);
+        }
+        float* dst = base_p + (p.reverse ? (U - 1 - u) : u) * It;
+        if constexpr (VEC == 4)
+          *reinterpret_cast<float4*>(dst) = make_float4(out[0], out[1], out[2], out[3]);
+        else
+          dst[0] = out[0];
+      }
+    }
+    __syncthreads();
+    // Store the tile (contiguous), the mapping of the copy in.
+    if (active) {
+      const int64_t pl = phys_lo(cu, i);
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int pr = k * Gt + g;
+        const int64_t row = pl + pr;
+        if (row >= cu.lo && row < cu.lo + cu.len) {
+          const float* src = buf + (pr / U) * St + (pr % U) * It + col;
+          float v[VEC];
+          if constexpr (VEC == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(src);
+            v[0] = f.x;
+            v[1] = f.y;
+            v[2] = f.z;
+            v[3] = f.w;
+          } else {
+            v[0] = src[0];
+          }
+          store_vec<VEC>(cu.yo + row * inner, v);
+        }
+      }
+    }
+    tc.add(tot);
+    cur ^= 1;
+    if (!more) break;
+    if (nunit != unit) {
+      unit = nunit;
+      cu = nu;
+      tc = carry_of(unit);
+    }
+    i = ni;
   }
 }
 
@@ -518,15 +594,32 @@ int occupancy_reduce_narrow(int vec, int op) {
   }
 }
 
+// The block-form scan keeps two tile buffers in dynamic shared memory (above
+// the 48 KiB a launch gets without asking).
+template <int VEC, int U>
+cudaError_t scan_narrow_kernel(void (**k)(ScanColsParams), size_t* bytes) {
+  *k = k_scan_narrow<VEC, U>;
+  *bytes = 2 * sizeof(float) * scan_narrow_cap<VEC, U>();
+  return cudaFuncSetAttribute(*k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)*bytes);
+}
+
 cudaError_t launch_scan_narrow(int vec, const ScanColsParams& p, int64_t grid, cudaStream_t s) {
-  const dim3 g((unsigned)grid);
-  if (vec == 4) k_scan_narrow<4, 8><<<g, kThreads, 0, s>>>(p);
-  else k_scan_narrow<1, 16><<<g, kThreads, 0, s>>>(p);
+  void (*k)(ScanColsParams) = nullptr;
+  size_t bytes = 0;
+  const cudaError_t e = vec == 4 ? scan_narrow_kernel<4, 8>(&k, &bytes) : scan_narrow_kernel<1, 16>(&k, &bytes);
+  if (e != cudaSuccess) return e;
+  k<<<dim3((unsigned)grid), kThreads, bytes, s>>>(p);
   return cudaGetLastError();
 }
 
 int occupancy_scan_narrow(int vec) {
-  return vec == 4 ? occupancy_of(k_scan_narrow<4, 8>) : occupancy_of(k_scan_narrow<1, 16>);
+  void (*k)(ScanColsParams) = nullptr;
+  size_t bytes = 0;
+  if ((vec == 4 ? scan_narrow_kernel<4, 8>(&k, &bytes) : scan_narrow_kernel<1, 16>(&k, &bytes)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kThreads, bytes) != cudaSuccess) return 0;
+  return n;
 }
 
 int64_t scan_narrow_tile_rows(int vec, int64_t inner) {

@@ -116,7 +116,7 @@ def test_nan_inf():
 
 
 NARROW = [(2, 30000, 4), (5, 777, 3), (3, 1000, 32), (2, 5000, 128), (4, 1001, 12), (1, 200000, 2),
-          (100, 300, 7), (2, 70001, 16), (64, 64, 5)]
+          (100, 300, 7), (2, 70001, 16), (64, 64, 5), (1, 100000, 33), (3, 2000, 100), (2, 3000, 255)]
 
 
 @pytest.mark.parametrize("shape", NARROW)

@@ -164,7 +164,9 @@ def test_axis_every_block_shape(variant, reverse, exclusive):
                                                ((1, 200000, 2), 0, 0), ((100, 300, 7), 0, 0),
                                                ((2, 70001, 16), 17, 0), ((3, 5000, 8), 0, 1),
                                                ((2, 3001, 20), 5, 2), ((1, 3, 5), 0, 0), ((2, 1, 4), 0, 0),
-                                               ((3, 4097, 31), 0, 3)])
+                                               ((3, 4097, 31), 0, 3), ((1, 100000, 33), 0, 0),
+                                               ((3, 2000, 100), 0, 0), ((2, 3000, 255), 4, 0),
+                                               ((4, 1000, 256), 0, 1), ((600, 50, 64), 0, 0)])
 @pytest.mark.parametrize("form", [-1, 3, 4], ids=["auto", "block", "warp"])
 def test_axis_narrow(shape, segs, offset, reverse, exclusive, form):
     """Rows of at most 32 column groups: the narrow scan, with tiles staged in
