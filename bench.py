@@ -47,7 +47,8 @@ STEP_WORKLOADS = ["sum_1e9", "axis_128x4096x4095_d1", "axis_4096x65536_d1", "axi
                   "rcumsum_32768x32768", "rcumsum_1x1e9"]
 # Follow-on forms, timed separately from the step (reported under next_rows).
 NEXT_WORKLOADS = ["cumsum_fwd_32768x32768", "cumsum_fwd_excl_1x1e9", "cumsum_128x4096x4095_d1",
-                  "cumsum_64x16384x1024_d1", "cumsum_2x8192x4096_d1", "rcumsum_1x1e9_rts",
+                  "cumsum_64x16384x1024_d1", "cumsum_2x8192x4096_d1", "cumsum_1024x8192x64_d1",
+                  "sum_16x1000000x12_d1", "rcumsum_1x1e9_rts",
                   "max_1e9", "norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0",
                   "rcumsum_1x1e9_ws", "axis_65536x4096_d0_ws"]
 # Small cases of each kernel for ncu captures: larger than L2, a few GB at most.

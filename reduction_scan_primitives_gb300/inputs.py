@@ -86,6 +86,11 @@ WORKLOADS = {
                                dist="uniform_pm1", seed=11),
     "min_65536x4096_d0": dict(op="reduce", rop="min", shape=(65536, 4096), dim=0,
                               dist="uniform_pm1", seed=11),
+    # Narrow rows (few columns): the reduction and the scan along dim 1.
+    "sum_16x1000000x12_d1": dict(op="reduce", rop="sum", shape=(16, 1_000_000, 12), dim=1,
+                                 dist="uniform_pm1", seed=13),
+    "cumsum_1024x8192x64_d1": dict(op="cumsum", shape=(1024, 8192, 64), dim=1, reverse=False,
+                                   exclusive=False, dist="uniform01", seed=13),
     # The reverse scan of one long row as three passes (reduce-then-scan), for
     # comparison with the single-pass look-back on the same input.
     "rcumsum_1x1e9_rts": dict(op="rcumsum", shape=(1, 1_000_000_000), dist="uniform01", seed=3,

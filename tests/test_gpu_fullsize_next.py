@@ -86,7 +86,7 @@ def test_rcumsum_1e9_reduce_then_scan():
 
 
 @pytest.mark.parametrize("name", ["cumsum_128x4096x4095_d1", "cumsum_64x16384x1024_d1",
-                                  "cumsum_2x8192x4096_d1"])
+                                  "cumsum_2x8192x4096_d1", "cumsum_1024x8192x64_d1"])
 def test_column_scans(name):
     column_scan_check(name)
 
@@ -98,11 +98,16 @@ def test_max_1e9():
     assert_op_close(np.array([got]), ref, scale, "max", w["shape"][0], "max 1e9")
 
 
-@pytest.mark.parametrize("name", ["norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0"])
+@pytest.mark.parametrize("name", ["norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0",
+                                  "sum_16x1000000x12_d1"])
 def test_axis_ops(name):
     w, x = workload(name)
     outer, r, inner = L.canonical_axis(w["shape"], w["dim"])
     out = L.reduce_axis_op_f32(x, w["dim"], w["rop"]).reshape(outer, inner)
+    if w["rop"] == "sum":  # the sum's oracle and tolerance
+        ref, scale = oracle.axis_sum(x.cpu().numpy(), outer, r, inner)
+        assert_close(out.cpu().numpy(), ref, scale, name)
+        return
     if outer * r * inner <= 300_000_000:
         ref, scale = oracle.reduce_op(x.cpu().numpy(), outer, r, inner, w["rop"])
         assert_op_close(out, ref, scale, w["rop"], r, name)
