@@ -1,6 +1,7 @@
 // lr_narrow.cu -- reductions and cumulative sums along a strided axis whose
-// rows are narrow: x is [outer, N, inner] with inner at most 32 column groups
-// of VEC floats (sm_103a).
+// rows are narrow: x is [outer, N, inner] with inner at most 256 column groups
+// of VEC floats (the library routes up to 256 scalar or 128 float4 columns
+// here) (sm_103a).
 //
 // The wide-row kernels put a warp across 32*VEC adjacent columns and loop down
 // the axis (POPCORNBENCH trace l1_p47: coalesced across the contiguous inner
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_narrow(NarrowParams p) {
   __syncthreads();
   if (!am_last) return;
   __threadfence();
-  const int Gs = kThreads / (int)inner;  // slice groups (inner <= 32*VEC <= 128 here, so Gs >= 2)
+  const int Gs = kThreads / (int)inner;  // slice groups (inner <= 256 here, so Gs >= 1)
   const int gs = threadIdx.x / (int)inner;
   const int c = threadIdx.x - gs * (int)inner;
   float v = Op::identity();

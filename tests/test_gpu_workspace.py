@@ -13,7 +13,8 @@ from reduction_scan_primitives_gb300 import libreduce as L
 pytestmark = pytest.mark.gpu
 
 REDUCE_CASES = [((1, 50_000_000), 1, "sum"), ((65536, 4096), 0, "sum"), ((65536, 4096), 0, "max"),
-                ((300, 70_000), 1, "mean"), ((128, 512, 257), 1, "norm"), ((4096, 300), 1, "min")]
+                ((300, 70_000), 1, "mean"), ((128, 512, 257), 1, "norm"), ((4096, 300), 1, "min"),
+                ((4, 100_000, 12), 1, "sum"), ((2, 300_000, 33), 1, "mean"), ((6000, 50, 3), 1, "max")]
 SCAN_CASES = [((1, 30_000_000), True, False), ((2, 5_000_000), False, True), ((512, 32768), True, False),
               ((3, 100_003), False, False)]
 
@@ -41,6 +42,10 @@ def test_query_sizes():
     assert L.reduce_axis_op_ws_f32(x, 1, "sum") == 256        # one warp per row: the header only
     y = on_device(inputs.make((65536, 64), "uniform01", 1))
     assert L.reduce_axis_op_ws_f32(y, 0, "sum") > 0           # split reduce axis
+    nr = on_device(inputs.make((4, 100_000, 12), "uniform01", 1))
+    assert L.reduce_axis_op_ws_f32(nr, 1, "sum") > 256         # narrow rows, sliced
+    sp = on_device(inputs.make((6000, 50, 3), "uniform01", 1))
+    assert L.reduce_axis_op_ws_f32(sp, 1, "sum") == 256        # a warp per small plane: the header only
     z = on_device(inputs.make((1, 10_000_000), "uniform01", 1))
     assert L.cumsum_ws_f32(z, 1, reverse=True) > 0            # look-back flags
     w = on_device(inputs.make((4096, 8192), "uniform01", 1))
