@@ -1,6 +1,8 @@
 /*
- * libreduce.h -- C ABI of libreduce, fp32 sum reductions and the reverse
- * cumulative sum on NVIDIA GB300 (sm_103a).
+ * libreduce.h -- C ABI of libreduce on NVIDIA GB300 (sm_103a): fp32
+ * reductions (sum, mean, max, min, Euclidean norm; 1D or along one axis) and
+ * cumulative sums (forward or reverse, inclusive or exclusive, along any
+ * axis), with library or caller-provided scratch.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -18,9 +20,11 @@
  *  - Results are deterministic: the same input on the same device gives
  *    bit-identical output on every call.  No floating-point atomics are used;
  *    partial sums are combined in a fixed order.
- *  - Accuracy: each output is within 1e-5 * (sum of |x| over its terms) +
- *    1e-6 of the exact sum, and exact when every partial sum is an integer of
- *    magnitude below 2^24.  NaN and Inf propagate as IEEE addition does.
+ *  - Accuracy: each sum or scan output is within 1e-5 * (sum of |x| over its
+ *    terms) + 1e-6 of the exact sum, and exact when every partial sum is an
+ *    integer of magnitude below 2^24 (max and min are exact; mean and norm as
+ *    documented with their op codes).  NaN and Inf propagate as IEEE addition
+ *    does.
  *  - Scratch: the library keeps one workspace per device for partial sums,
  *    tickets and look-back flags.  It is allocated (cudaMalloc) by the first
  *    call on that device that needs it, so that first call must not be made
