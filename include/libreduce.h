@@ -32,6 +32,10 @@
  *    device must not run concurrently on different streams; calls queued on
  *    one stream are always safe.  The *_ws variants take the scratch from
  *    the caller instead and lift this limit.
+ *  - CUDA graphs: after that first call, every call may be captured and the
+ *    graph replayed any number of times (tickets are reset on the device, and
+ *    the look-back scan takes its launch epoch from a device word that every
+ *    launch advances, so a replay never reads an earlier replay's flags).
  *  - Errors: validation happens before any work is queued, and a failed call
  *    queues nothing.  LIBREDUCE_ERR_CUDA means a CUDA runtime call failed; its
  *    code is available from libreduce_last_cuda_error().  Device-side errors

@@ -23,7 +23,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxTickets = 1 << 16;       // integer tickets (per row / column tile)
 constexpr int64_t kMaxPartials = 1 << 22;      // fp32 partial sums (16 MiB)
-constexpr size_t kHeaderBytes = 256;           // error word, abort word, tile counter
+constexpr size_t kHeaderBytes = 256;           // error word, abort word, {ticket counter, epoch}
 constexpr int64_t kMaxLookbackTiles = 1 << 20; // look-back tiles per launch
 constexpr size_t kWorkspaceBytes =
     kHeaderBytes + sizeof(unsigned) * kMaxTickets + sizeof(float) * kMaxPartials;
@@ -42,7 +42,6 @@ struct DeviceState {
   float* partials = nullptr;
   // Look-back region (allocated by the first look-back scan on the device).
   unsigned long long* node_val = nullptr;
-  std::atomic<unsigned> epoch{0};
   int occ_lookback[kNumLookbackVariants] = {};
   int occ_scan_cols[kNumScanColsVariants] = {};
   int occ_narrow[2][kNumReduceOps] = {};  // [vec4][op]
@@ -128,8 +127,9 @@ int ensure_workspace(DeviceState* st) {
   return LIBREDUCE_OK;
 }
 
-// Allocate the look-back flags once per device.  Their epochs make stale
-// contents harmless, but they start zeroed (epoch 0 is never used).
+// Allocate the look-back flags once per device.  Their epochs (a device word
+// in the header, advanced by every look-back launch) make stale contents
+// harmless, but they start zeroed (epoch 0 is never used).
 int ensure_lookback(DeviceState* st) {
   int rc = ensure_workspace(st);
   if (rc) return rc;
@@ -247,7 +247,6 @@ struct Scratch {
   unsigned* tickets = nullptr;
   float* partials = nullptr;
   unsigned long long* nodes = nullptr;
-  unsigned epoch = 0;
 };
 
 struct Provider {
@@ -288,11 +287,6 @@ int acquire(const Provider& pv, const Need& need, Scratch* sc, cudaStream_t s) {
     sc->tickets = st->tickets;
     sc->partials = st->partials;
     sc->nodes = st->node_val;
-    if (need.nodes) {
-      unsigned epoch = st->epoch.fetch_add(1) + 1;
-      if (epoch == 0) epoch = st->epoch.fetch_add(1) + 1;  // 0 marks "never written"
-      sc->epoch = epoch;
-    }
     return LIBREDUCE_OK;
   }
   size_t off_t, off_p, off_n, total;
@@ -307,7 +301,6 @@ int acquire(const Provider& pv, const Need& need, Scratch* sc, cudaStream_t s) {
   sc->tickets = reinterpret_cast<unsigned*>(pv.ws + off_t);
   sc->partials = reinterpret_cast<float*>(pv.ws + off_p);
   sc->nodes = reinterpret_cast<unsigned long long*>(pv.ws + off_n);
-  sc->epoch = 1;  // every node word was just cleared
   return LIBREDUCE_OK;
 }
 
@@ -586,15 +579,16 @@ int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t
   Scratch sc;
   int rc = acquire(pv, need, &sc, s);
   if (rc) return rc;
-  unsigned* counter = sc.header + 2;  // zero on entry; the block with the last ticket resets it
+  // Header words 2-3: {ticket counter, epoch} as one 64-bit word; the block
+  // with the last ticket resets the counter and advances the epoch.
+  auto* ticket_word = reinterpret_cast<unsigned long long*>(sc.header + 2);
   const int64_t spin = g_opt_spin_limit.load();
   const int64_t lag_opt = g_opt_lookback_lag.load();
   const int64_t lag = variant == kLookbackL2
                           ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt : lookback_lag(pv.st))
                           : 0;
-  RScanLookbackParams p{x, y, rows, N, tiles, sc.nodes, counter, sc.header,
-                        sc.epoch, spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag,
-                        flags};
+  RScanLookbackParams p{x, y, rows, N, tiles, sc.nodes, ticket_word, sc.header,
+                        spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag, flags};
   const int64_t grid = total + lag;  // one block per ticket
   return launched(launch_rscan_lookback(variant, p, grid, s));
 }

@@ -138,9 +138,9 @@ struct RScanLookbackParams {
   int64_t N;
   int64_t tiles_per_row;
   unsigned long long* node_val;  // rows * 2 * tiles_per_row words
-  unsigned* tile_counter;        // zero on entry; reset by the block with the last ticket
-  unsigned* err_word;            // bit 0 set when a wait runs out
-  unsigned epoch;                // nonzero, different for every launch on the device
+  unsigned long long* ticket_word;  // {epoch:32, ticket counter:32}; counter zero on entry,
+                                   // reset (epoch advanced) by the block with the last ticket
+  unsigned* err_word;              // bit 0 set when a wait runs out
   int64_t spin_limit;            // polls before a wait gives up
   int64_t stall_tile;            // test fault: this ticket never publishes (-1: none)
   int64_t lag;                   // L2-lag form: tiles between a tile's two touches

@@ -260,12 +260,31 @@ __device__ __forceinline__ float warp_tree_adjacent(float v) {
   return v;
 }
 
+// Tickets and the launch's epoch (the tag that tells this launch's node words
+// from older ones) share one 64-bit device word: epoch in the high half, the
+// ticket counter in the low half.  One atomicAdd gives a block both; the
+// block with the last ticket -- every other block has taken its ticket --
+// resets the counter and advances the epoch (0 is reserved for "never
+// written").  Kept on the device rather than passed by the host, so a launch
+// captured in a CUDA graph gets a new epoch at every replay.
+struct Ticket {
+  unsigned ticket, epoch;
+};
+__device__ __forceinline__ Ticket take_ticket(unsigned long long* word) {
+  const unsigned long long old = atomicAdd(word, 1ull);
+  const unsigned e = (unsigned)(old >> 32);
+  return Ticket{(unsigned)old, e == 0 ? 1u : e};
+}
+__device__ __forceinline__ void next_launch(unsigned long long* word, unsigned epoch) {
+  atomicExch(word, (unsigned long long)(epoch + 1 == 0 ? 1u : epoch + 1) << 32);
+}
+
 template <int VEC, int SUB>
 __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
   __shared__ float sh_w[SUB][kNW];
   __shared__ float s_part[kMaxLevels];
-  __shared__ unsigned s_ticket;
+  __shared__ unsigned s_ticket, s_epoch;
   __shared__ int s_fail;
   const int t = threadIdx.x;
   const int lane = t & 31;
@@ -273,14 +292,16 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
   const unsigned* abort_word = p.err_word + 1;
 
   if (t == 0) {
-    const unsigned tk = atomicAdd(p.tile_counter, 1u);
-    s_ticket = tk;
+    const Ticket tk = take_ticket(p.ticket_word);
+    s_ticket = tk.ticket;
+    s_epoch = tk.epoch;
     s_fail = 0;
     // Every other ticket is taken before the last one: reset for the next launch.
-    if ((int64_t)tk == p.rows * p.tiles_per_row - 1) atomicExch(p.tile_counter, 0u);
+    if ((int64_t)tk.ticket == p.rows * p.tiles_per_row - 1) next_launch(p.ticket_word, tk.epoch);
   }
   __syncthreads();
   const int64_t ticket = s_ticket;
+  const unsigned epoch = s_epoch;
   const int64_t tiles = p.tiles_per_row;
   if (ticket >= p.rows * tiles) {  // a stale counter: touch nothing
     if (t == 0) atomicOr(p.err_word, 2u);
@@ -298,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
   float v[SUB][VEC];
   load_tile<VEC, SUB>(v, xr, base, p.N, t, mirror);
   const TileScan<SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, lane, w);
-  if (t == 0 && !stalled) st_relaxed_u64(vals + k, pack_node(p.epoch, ts.total));
+  if (t == 0 && !stalled) st_relaxed_u64(vals + k, pack_node(epoch, ts.total));
 
   // Levels of this row: base-32 digits of the largest tile index.
   int levels = 1;
@@ -318,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
     int d = (int)(m & 31);
     bool fail = false;
     float sib = 0.f;
-    if (lane < d) sib = wait_node(vals + off + (m - d) + lane, p.epoch, p.spin_limit, abort_word, &fail);
+    if (lane < d) sib = wait_node(vals + off + (m - d) + lane, epoch, p.spin_limit, abort_word, &fail);
     const float part = warp_tree_adjacent(sib);
     if (lane == 0) s_part[w] = part;
     if (w == 0) {
@@ -328,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
         const float parent = warp_tree_adjacent(lane < 31 ? sib : own);
         own = __shfl_sync(kFullMask, parent, 0);
         const int64_t next_off = off + count;
-        if (lane == 0) st_relaxed_u64(vals + next_off + (m >> 5), pack_node(p.epoch, own));
+        if (lane == 0) st_relaxed_u64(vals + next_off + (m >> 5), pack_node(epoch, own));
         if (++L >= levels) break;
         off = next_off;
         count >>= 5;
@@ -336,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
         d = (int)(m & 31);
         if (d != 31) break;  // the next parent is not complete yet: someone else's job
         sib = 0.f;
-        if (lane < 31) sib = wait_node(vals + off + (m - 31) + lane, p.epoch, p.spin_limit, abort_word, &fail);
+        if (lane < 31) sib = wait_node(vals + off + (m - 31) + lane, epoch, p.spin_limit, abort_word, &fail);
       }
     }
     if (__any_sync(kFullMask, fail) && lane == 0) s_fail = 1;
@@ -349,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
     s_part[0] = excl;
     if (s_fail) {
       atomicOr(p.err_word, 1u);
-      atomicExch(p.err_word + 1, p.epoch);
+      atomicExch(p.err_word + 1, epoch);
     }
   }
   __syncthreads();
@@ -381,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
   __shared__ float sh_w[SUB][kNW];
   __shared__ float s_red[kNW];
   __shared__ float s_part[kMaxLevels];
-  __shared__ unsigned s_ticket;
+  __shared__ unsigned s_ticket, s_epoch;
   __shared__ int s_fail;
   const int t = threadIdx.x;
   const int lane = t & 31;
@@ -391,11 +412,13 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
   const int64_t total = p.rows * tiles;
 
   if (t == 0) {
-    const unsigned tk = atomicAdd(p.tile_counter, 1u);
+    const Ticket tkt = take_ticket(p.ticket_word);
+    const unsigned tk = tkt.ticket;
     s_ticket = tk;
+    s_epoch = tkt.epoch;
     s_fail = 0;
     // Every other ticket is taken before the last one: reset for the next launch.
-    if ((int64_t)tk == total + p.lag - 1) atomicExch(p.tile_counter, 0u);
+    if ((int64_t)tk == total + p.lag - 1) next_launch(p.ticket_word, tkt.epoch);
     if (tk < total) {
       const int64_t row = tk / tiles;
       const int64_t k = tk - row * tiles;
@@ -411,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
   }
   __syncthreads();
   const int64_t ticket = s_ticket;
+  const unsigned epoch = s_epoch;
   if (ticket >= total + p.lag) {  // a stale counter: touch nothing
     if (t == 0) atomicOr(p.err_word, 2u);
     return;
@@ -438,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
       const int d = (int)(m & 31);
       bool fail = false;
       float sib = 0.f;
-      if (lane < d) sib = wait_node(vals + off + (m - d) + lane, p.epoch, p.spin_limit, abort_word, &fail);
+      if (lane < d) sib = wait_node(vals + off + (m - d) + lane, epoch, p.spin_limit, abort_word, &fail);
       const float part = warp_tree_adjacent(sib);
       if (lane == 0) s_part[w] = part;
       if (__any_sync(kFullMask, fail) && lane == 0) s_fail = 1;
@@ -475,19 +499,19 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
     const bool stalled = ticket == p.stall_tile;
     if (w == 0 && !stalled) {
       const float own0 = __shfl_sync(kFullMask, a, 0);
-      if (lane == 0) st_relaxed_u64(vals + k, pack_node(p.epoch, own0));
+      if (lane == 0) st_relaxed_u64(vals + k, pack_node(epoch, own0));
       if ((k & 31) == 31) {  // publish every parent this tile completes
         bool fail = false;
         float own = own0;
         int64_t off = 0, count = tiles, m = k;
         for (int L = 0; L < levels && (m & 31) == 31; ++L) {
           float sib = 0.f;
-          if (lane < 31) sib = wait_node(vals + off + (m - 31) + lane, p.epoch, p.spin_limit, abort_word, &fail);
+          if (lane < 31) sib = wait_node(vals + off + (m - 31) + lane, epoch, p.spin_limit, abort_word, &fail);
           if (__any_sync(kFullMask, fail)) break;
           const float parent = warp_tree_adjacent(lane < 31 ? sib : own);
           own = __shfl_sync(kFullMask, parent, 0);
           const int64_t next_off = off + count;
-          if (lane == 0) st_relaxed_u64(vals + next_off + (m >> 5), pack_node(p.epoch, own));
+          if (lane == 0) st_relaxed_u64(vals + next_off + (m >> 5), pack_node(epoch, own));
           off = next_off;
           count >>= 5;
           m >>= 5;
@@ -504,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
   __syncthreads();
   if (t == 0 && s_fail) {
     atomicOr(p.err_word, 1u);
-    atomicExch(p.err_word + 1, p.epoch);
+    atomicExch(p.err_word + 1, epoch);
   }
 }
 
