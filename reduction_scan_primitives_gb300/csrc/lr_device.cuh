@@ -60,16 +60,6 @@ __device__ __forceinline__ float4 ld_cg4(const float* p) {
 // blocks publish values that other blocks of the same launch wait for.
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
 // A 64-bit word that carries its own validity (an epoch next to the value)
 // needs no ordering with other data, so relaxed single-copy-atomic accesses
 // suffice and no fence is paid on either side.
@@ -104,11 +94,6 @@ __device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned coun
 // Make mbarrier initialisation visible to the async (bulk-copy) proxy.
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// Order this thread's earlier shared-memory accesses before later bulk copies.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, unsigned bytes) {
@@ -198,7 +183,6 @@ template <typename Op>
 __device__ __forceinline__ float reduce4(float4 v) {
   return Op::combine(Op::combine(Op::prep(v.x), Op::prep(v.y)), Op::combine(Op::prep(v.z), Op::prep(v.w)));
 }
-__device__ __forceinline__ float sum4(float4 v) { return reduce4<OpSum>(v); }
 
 // Pairwise reduction of a small register array (values already prepped).
 template <typename Op, int N>
@@ -220,7 +204,6 @@ __device__ __forceinline__ float warp_reduce(float v) {
   for (int o = 16; o > 0; o >>= 1) v = Op::combine(v, __shfl_down_sync(kFullMask, v, o));
   return v;
 }
-__device__ __forceinline__ float warp_sum(float v) { return warp_reduce<OpSum>(v); }
 
 // Block reduction for NT threads (NT a multiple of 32, at most 1024).  `sh`
 // holds NT/32 floats.  The result is valid in thread 0.  The caller must place
