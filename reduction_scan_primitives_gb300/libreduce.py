@@ -170,6 +170,23 @@ def reduce_sum_f32(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Te
     return out
 
 
+def reduce_sum_f32_noalloc(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """reduce_sum_f32 that allocates no device memory: its scratch is a fixed
+    static device array (n <= 2**36; calls must not overlap on the GPU)."""
+    _check_tensor(x, "x")
+    if out is None:
+        out = torch.empty((), dtype=torch.float32, device=x.device)
+    else:
+        _check_tensor(out, "out")
+        if out.numel() != 1 or out.device != x.device:
+            raise ValueError("out must hold one float on x's device")
+    lib = load()
+    with torch.cuda.device(x.device):
+        st = lib.reduce_sum_f32_noalloc(x.data_ptr(), x.numel(), out.data_ptr(), _stream_ptr(x.device))
+    _raise_on("reduce_sum_f32_noalloc", st)
+    return out
+
+
 def reduce_axis_f32(x: torch.Tensor, dim: int, keepdim: bool = False,
                     out: torch.Tensor | None = None) -> torch.Tensor:
     """Sum of x along `dim` (float32 CUDA, contiguous)."""

@@ -59,3 +59,11 @@ def test_empty_and_limits(lib):
     assert lib.reduce_sum_f32_noalloc(ctypes.c_void_p(x1.data_ptr()), (1 << 36) + 1,
                                       ctypes.c_void_p(out.data_ptr()), None) == L.ERR_OVERFLOW
     assert lib.reduce_sum_f32_noalloc(None, 5, ctypes.c_void_p(out.data_ptr()), None) == L.ERR_INVALID_ARG
+
+
+def test_python_binding_matches(lib):
+    x = inputs.make((2_000_003,), "uniform_pm1", 19, device="cuda")
+    a = L.reduce_sum_f32_noalloc(x).clone()
+    b = L.reduce_sum_f32(x)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
