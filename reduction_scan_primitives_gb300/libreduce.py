@@ -9,6 +9,7 @@ work is queued on the current torch stream of the tensor's device.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import re
@@ -133,8 +134,23 @@ def _check_tensor(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
+# The current stream's raw handle without building a Stream object (the
+# public route costs about a microsecond per call).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_ptr(device) -> int:
-    return torch.cuda.current_stream(device).cuda_stream
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    if _raw_stream is not None:
+        return _raw_stream(index)
+    return torch.cuda.current_stream(index).cuda_stream
+
+
+def _on(device):
+    """Make `device` current for the call, entering it only when it is not."""
+    if device.index is None or device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def canonical_axis(shape, dim: int):
@@ -164,7 +180,7 @@ def reduce_sum_f32(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Te
         if out.numel() != 1 or out.device != x.device:
             raise ValueError("out must hold one float on x's device")
     lib = load()
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.reduce_sum_f32(x.data_ptr(), x.numel(), out.data_ptr(), _stream_ptr(x.device))
     _raise_on("reduce_sum_f32", st)
     return out
@@ -181,7 +197,7 @@ def reduce_sum_f32_noalloc(x: torch.Tensor, out: torch.Tensor | None = None) -> 
         if out.numel() != 1 or out.device != x.device:
             raise ValueError("out must hold one float on x's device")
     lib = load()
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.reduce_sum_f32_noalloc(x.data_ptr(), x.numel(), out.data_ptr(), _stream_ptr(x.device))
     _raise_on("reduce_sum_f32_noalloc", st)
     return out
@@ -206,7 +222,7 @@ def reduce_axis_f32(x: torch.Tensor, dim: int, keepdim: bool = False,
         if out.numel() != outer * inner or out.device != x.device:
             raise ValueError("out has the wrong size or device")
     lib = load()
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.reduce_axis_f32(x.data_ptr(), outer, reduce, inner, out.data_ptr(),
                                  _stream_ptr(x.device))
     _raise_on("reduce_axis_f32", st)
@@ -231,7 +247,7 @@ def reduce_f32(x: torch.Tensor, op="sum", out: torch.Tensor | None = None) -> to
         if out.numel() != 1 or out.device != x.device:
             raise ValueError("out must hold one float on x's device")
     lib = load()
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.reduce_f32(x.data_ptr(), x.numel(), out.data_ptr(), _op_code(op), _stream_ptr(x.device))
     _raise_on("reduce_f32", st)
     return out
@@ -256,7 +272,7 @@ def reduce_axis_op_f32(x: torch.Tensor, dim: int, op="sum", keepdim: bool = Fals
         if out.numel() != outer * inner or out.device != x.device:
             raise ValueError("out has the wrong size or device")
     lib = load()
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.reduce_axis_op_f32(x.data_ptr(), outer, reduce, inner, out.data_ptr(), _op_code(op),
                                     _stream_ptr(x.device))
     _raise_on("reduce_axis_op_f32", st)
@@ -277,7 +293,7 @@ def reverse_cumsum_f32(x: torch.Tensor, out: torch.Tensor | None = None) -> torc
         if out.shape != x.shape or out.device != x.device:
             raise ValueError("out must have x's shape and device")
     lib = load()
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.reverse_cumsum_f32(x.data_ptr(), rows, N, out.data_ptr(), _stream_ptr(x.device))
     _raise_on("reverse_cumsum_f32", st)
     return out
@@ -299,7 +315,7 @@ def cumsum_f32(x: torch.Tensor, dim: int = -1, reverse: bool = False, exclusive:
             raise ValueError("out must have x's shape and device")
     flags = (SCAN_REVERSE if reverse else 0) | (SCAN_EXCLUSIVE if exclusive else 0)
     lib = load()
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.cumsum_f32(x.data_ptr(), outer, N, inner, out.data_ptr(), flags, _stream_ptr(x.device))
     _raise_on("cumsum_f32", st)
     return out
@@ -330,7 +346,7 @@ def reduce_axis_op_ws_f32(x: torch.Tensor, dim: int, op="sum", ws: torch.Tensor 
         out = torch.empty(shape, dtype=torch.float32, device=x.device)
     nbytes = _ws_nbytes(ws)
     lib = load()
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.reduce_axis_op_ws_f32(x.data_ptr(), outer, reduce, inner, out.data_ptr(), _op_code(op),
                                        _ws_ptr(ws), ctypes.byref(nbytes), _stream_ptr(x.device))
     _raise_on("reduce_axis_op_ws_f32", st)
@@ -347,7 +363,7 @@ def cumsum_ws_f32(x: torch.Tensor, dim: int = -1, reverse: bool = False, exclusi
     flags = (SCAN_REVERSE if reverse else 0) | (SCAN_EXCLUSIVE if exclusive else 0)
     nbytes = _ws_nbytes(ws)
     lib = load()
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.cumsum_ws_f32(x.data_ptr(), outer, N, inner, out.data_ptr(), flags, _ws_ptr(ws),
                                ctypes.byref(nbytes), _stream_ptr(x.device))
     _raise_on("cumsum_ws_f32", st)
@@ -356,7 +372,7 @@ def cumsum_ws_f32(x: torch.Tensor, dim: int = -1, reverse: bool = False, exclusi
 
 def check_ws(ws: torch.Tensor) -> None:
     """Synchronise the current stream and raise if a wait of a workspace call ran out."""
-    with torch.cuda.device(ws.device):
+    with _on(ws.device):
         st = load().libreduce_check_ws(ws.data_ptr(), _stream_ptr(ws.device))
     _raise_on("libreduce_check_ws", st)
 
