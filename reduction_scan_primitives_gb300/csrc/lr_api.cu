@@ -556,15 +556,18 @@ int reduce_impl(const float* x, int64_t outer, int64_t reduce, int64_t inner, fl
 }
 
 constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): well under a second
-// L2-lag form: tickets between a tile's two touches.  The lag must exceed the
-// blocks resident at once, or the write of tile t - lag waits on tiles still
-// in flight; past ~2000 tiles (64 MiB) the reread misses L2.  Measured on one
-// row of 1e9 with 608 resident blocks (4 per SM): reverse 55% at lag 384, 63%
-// at 512, 87% at 768, 94% at 1024, 87% at 1280, 76% at 1536; forward 84-85%
-// from 768 to 1152.  Default: 5/3 of the resident blocks, in steps of 64.
-int64_t lookback_lag(const DeviceState* st) {
+// L2-lag form: tickets between a tile's two touches.  In the reverse scan's
+// order (write, then publish) the lag must exceed the blocks resident at
+// once, or the write of tile t - lag waits on tiles still in flight; past
+// ~2000 tiles (64 MiB) the reread misses L2.  Measured on one row of 1e9 with
+// 608 resident blocks (4 per SM): reverse 55% at lag 384, 63% at 512, 87% at
+// 768, 94-96% at 1024, 87% at 1280, 76% at 1536: 5/3 of the resident blocks.
+// The forward scan publishes first and reaches 92% at 640-768 (89% at 1024):
+// 5/4 of the resident blocks.  Both in steps of 64.
+int64_t lookback_lag(const DeviceState* st, bool mirror) {
   const int64_t resident = (int64_t)st->sm_count * st->occ_lookback[kLookbackL2];
-  return std::max<int64_t>(64, ceil_div(resident * 5 / 3, 64) * 64);
+  const int64_t lag = mirror ? resident * 5 / 4 : resident * 5 / 3;
+  return std::max<int64_t>(64, ceil_div(lag, 64) * 64);
 }
 
 int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
@@ -585,7 +588,8 @@ int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t
   const int64_t spin = g_opt_spin_limit.load();
   const int64_t lag_opt = g_opt_lookback_lag.load();
   const int64_t lag = variant == kLookbackL2
-                          ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt : lookback_lag(pv.st))
+                          ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt
+                                                                 : lookback_lag(pv.st, (flags & kScanMirror) != 0))
                           : 0;
   RScanLookbackParams p{x, y, rows, N, tiles, sc.nodes, ticket_word, sc.header,
                         spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag, flags};

@@ -18,6 +18,8 @@
 // The trace's formula tile_total - prefix_before(j) + carry is not used: it
 // subtracts two large numbers to get a small one, which loses the accuracy
 // the per-element tolerance (relative to that element's own suffix) asks for.
+#include <algorithm>
+
 #include "lr_device.cuh"
 #include "lr_internal.h"
 
@@ -392,9 +394,13 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
 // The look-back rarely waits, the HBM read of tile t overlaps step 2, and HBM
 // still sees each element read once and written once while the lag's tiles
 // stay in L2.  Every wait is on a smaller ticket, so forward progress holds as
-// in the other forms.
+// in the other forms.  EARLY takes the steps as 1, reread of u, 3, then the
+// rest of 2: the sum of tile t is out as soon as its copy lands, so a shorter
+// lag suffices.  Measured on one row of 1e9: the reverse scan is faster in
+// the plain order (96% of copy bandwidth against 94%), the forward (mirrored)
+// scan with EARLY (92% against 85%).
 // ---------------------------------------------------------------------------
-template <int SUB>
+template <int SUB, bool EARLY>
 __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookbackParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * 4;
   __shared__ __align__(128) float s_tile[TILE];
@@ -442,15 +448,22 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
   int levels = 1;
   while (levels < kMaxLevels && ((tiles - 1) >> (5 * levels)) != 0) ++levels;
 
-  // ---- write out tile `ticket - lag` ----
+  // ---- reread tile `ticket - lag` (from L2), in flight while tile `ticket` lands ----
   const int64_t u = ticket - p.lag;
+  const bool mirror = (p.flags & kScanMirror) != 0;
+  float v[SUB][4];
   if (u >= 0) {
     const int64_t row = u / tiles;
     const int64_t k = u - row * tiles;
+    load_tile<4, SUB>(v, p.x + row * p.N, (tiles - 1 - k) * TILE, p.N, t, mirror);
+  }
+
+  // ---- write out tile `ticket - lag` ----
+  const auto write_out = [&]() {
+    if (u < 0) return;
+    const int64_t row = u / tiles;
+    const int64_t k = u - row * tiles;
     const int64_t base = (tiles - 1 - k) * TILE;
-    const bool mirror = (p.flags & kScanMirror) != 0;
-    float v[SUB][4];
-    load_tile<4, SUB>(v, p.x + row * p.N, base, p.N, t, mirror);  // in flight during the look-back
     unsigned long long* vals = p.node_val + row * 2 * tiles;
     if (w < levels) {
       int64_t off = 0, count = tiles;
@@ -472,8 +485,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
     for (int L = 0; L < levels; ++L) excl += s_part[L];  // from the lowest level up
     finalize<4, SUB>(v, ts, excl, (p.flags & kScanExclusive) != 0);
     store_tile<4, SUB>(v, p.y + row * p.N, base, p.N, t, mirror);
-  }
+  };
 
+  // The reverse scan writes first (its reread overlaps tile `ticket`'s copy),
+  // then publishes; the forward (mirrored) scan publishes as soon as its copy
+  // lands and writes last (measured faster in each direction).
+  if constexpr (!EARLY) write_out();
   // ---- sum tile `ticket` (in shared memory) and publish it ----
   if (ticket < total) {
     const int64_t row = ticket / tiles;
@@ -525,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
       for (int64_t it = 0; !mbar_try_wait_parity(&s_bar, 0u) && it < p.spin_limit; ++it) {
       }
   }
+  if constexpr (EARLY) write_out();
   __syncthreads();
   if (t == 0 && s_fail) {
     atomicOr(p.err_word, 1u);
@@ -727,7 +745,10 @@ cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int
   switch (variant) {
     case kLookbackV1: k_rscan_lookback<1, 8><<<g, kThreads, 0, s>>>(p); break;
     case kLookbackV4: k_rscan_lookback<4, 8><<<g, kThreads, 0, s>>>(p); break;
-    case kLookbackL2: k_rscan_lookback_l2<8><<<g, kThreads, 0, s>>>(p); break;
+    case kLookbackL2:
+      if (p.flags & kScanMirror) k_rscan_lookback_l2<8, true><<<g, kThreads, 0, s>>>(p);
+      else k_rscan_lookback_l2<8, false><<<g, kThreads, 0, s>>>(p);
+      break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -737,7 +758,8 @@ int occupancy_rscan_lookback(int variant) {
   switch (variant) {
     case kLookbackV1: return occupancy_of(k_rscan_lookback<1, 8>);
     case kLookbackV4: return occupancy_of(k_rscan_lookback<4, 8>);
-    case kLookbackL2: return occupancy_of(k_rscan_lookback_l2<8>);
+    case kLookbackL2:
+      return std::min(occupancy_of(k_rscan_lookback_l2<8, false>), occupancy_of(k_rscan_lookback_l2<8, true>));
     default: return 0;
   }
 }
