@@ -11,7 +11,10 @@
  *    allocator, or managed memory).  The caller owns them.  Host pointers are
  *    rejected with LIBREDUCE_ERR_INVALID_ARG before any work is queued.
  *  - Every float* must be 4-byte aligned.  Any 4-byte alignment is accepted;
- *    16-byte aligned buffers take the vectorised (128-bit) paths.
+ *    16-byte aligned buffers take the vectorised (128-bit) paths, and so do
+ *    row scans whose x and y sit at the same offset mod 16 bytes (rows of
+ *    any length: the float4 items at a row's two edges are masked, and a
+ *    masked item's load stays within the 16-byte granule of a row element).
  *  - Arrays are contiguous and row-major.  Sizes are element counts (int64).
  *  - `stream` is a cudaStream_t (NULL means the legacy default stream).  A
  *    call only enqueues work on `stream`: it never synchronises the host and
@@ -285,7 +288,8 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *                                 (inner <= 32 scalar or 128 float4 columns: the
  *                                 automatic choice there)
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
- *                                 2 float4 x 4 (float4 needs N % 4 == 0, aligned x, y)
+ *                                 2 float4 x 4 (float4 needs x and y at the same
+ *                                 offset mod 16 bytes; any N)
  *   LIBREDUCE_OPT_WAVES           1D sum: blocks = waves x resident blocks (0 = automatic:
  *                                 one wave, or more blocks of 64 Ki floats for long arrays)
  *   LIBREDUCE_OPT_LOOKBACK_LAG    look-back scan: tiles between the read that publishes a

@@ -570,10 +570,29 @@ int64_t lookback_lag(const DeviceState* st, bool mirror) {
   return std::max<int64_t>(64, ceil_div(lag, 64) * 64);
 }
 
+// Row scans with float4 tiles read any row as a 16-byte aligned "virtual
+// row" (the scan kernels' RowView): they need x and y to share their 16-byte
+// misalignment.  The longest virtual row is the row padded by its
+// misalignment (the same for every row when N % 4 == 0, else up to 3) and
+// rounded up to a multiple of 4.
+bool rows_vec4(const float* x, const float* y) {
+  return ((reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+}
+// Float4 rows that are not whole aligned float4s run the kernel forms that
+// mask the row edges.
+bool has_row_edges(const float* x, int64_t N) {
+  return N % 4 != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0;
+}
+int64_t virtual_row_len(const float* x, int64_t N, bool vec4) {
+  if (!vec4) return N;
+  const int64_t m0 = (int64_t)((reinterpret_cast<uintptr_t>(x) >> 2) & 3);
+  return round_up(N + (N % 4 == 0 ? m0 : 3), 4);
+}
+
 int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
                        cudaStream_t s, int variant, int flags) {
   const int64_t tile = lookback_tile(variant);
-  const int64_t tiles = ceil_div(N, tile);
+  const int64_t tiles = ceil_div(virtual_row_len(x, N, variant != kLookbackV1), tile);
   int64_t total = 0;
   if (mul_overflows(rows, tiles, &total) || total > kMaxLookbackTiles) return LIBREDUCE_ERR_OVERFLOW;
   Need need;
@@ -591,6 +610,7 @@ int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t
                           ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt
                                                                  : lookback_lag(pv.st, (flags & kScanMirror) != 0))
                           : 0;
+  if (variant == kLookbackL2 && has_row_edges(x, N)) flags |= kScanRowEdges;
   RScanLookbackParams p{x, y, rows, N, tiles, sc.nodes, ticket_word, sc.header,
                         spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag, flags};
   const int64_t grid = total + lag;  // one block per ticket
@@ -602,7 +622,7 @@ int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t
 int run_reduce_then_scan(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
                          cudaStream_t s, int flags, bool vec4) {
   const int variant = vec4 ? kTileV4 : kTileV1;
-  const int64_t tiles = ceil_div(N, tile_scan_len(variant));
+  const int64_t tiles = ceil_div(virtual_row_len(x, N, vec4), tile_scan_len(variant));
   int64_t total = 0;
   if (mul_overflows(rows, tiles, &total) || 2 * total > kMaxPartials || total > INT32_MAX)
     return LIBREDUCE_ERR_OVERFLOW;
@@ -627,8 +647,7 @@ int run_reduce_then_scan(const Provider& pv, const float* x, int64_t rows, int64
 int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
                    cudaStream_t s, int flags) {
   DeviceState* st = pv.st;
-  const bool vec4 = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
-                    ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
+  const bool vec4 = rows_vec4(x, y);
   int variant = vec4 ? kRScanV4S4 : kRScanV1S4;
   const int64_t forced_v = g_opt_rscan_variant.load();
   if (forced_v >= 0 && forced_v < kNumRScanVariants && (forced_v == kRScanV1S4 || vec4))
@@ -637,7 +656,7 @@ int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, 
   // which spreads every row's tiles over all SMs.
   const int64_t strategy = g_opt_scan_strategy.load();
   const int lb_variant = !vec4 ? kLookbackV1 : (strategy == 3 ? kLookbackV4 : kLookbackL2);
-  const int64_t lb_tiles = ceil_div(N, lookback_tile(lb_variant));
+  const int64_t lb_tiles = ceil_div(virtual_row_len(x, N, vec4), lookback_tile(lb_variant));
   const int64_t row_slots = (int64_t)st->sm_count * st->occ_rscan[variant];
   const bool lookback_fits = rows <= kMaxLookbackTiles / std::max<int64_t>(1, lb_tiles);
   if (strategy == 4) return run_reduce_then_scan(pv, x, rows, N, y, s, flags, vec4);
@@ -647,6 +666,7 @@ int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, 
   int rc = acquire(pv, Need{}, &sc, s);
   if (rc) return rc;
   const int64_t grid = std::min<int64_t>(rows, INT32_MAX);
+  if (variant != kRScanV1S4 && has_row_edges(x, N)) flags |= kScanRowEdges;
   RScanRowsParams p{x, y, rows, N, flags};
   return launched(launch_rscan_rows(variant, p, grid, s));
 }

@@ -64,6 +64,10 @@ struct ColsParams {
 // out each element's own term (kScanExclusive).
 constexpr int kScanMirror = 1;
 constexpr int kScanExclusive = 2;
+// Set by the host for float4 row scans whose rows are not whole aligned
+// float4s (N % 4 != 0 or x not 16-byte aligned): selects the kernel form that
+// masks the row edges.
+constexpr int kScanRowEdges = 4;
 
 // --- Cumulative sum along rows, one block per row ----------------------------
 struct RScanRowsParams {

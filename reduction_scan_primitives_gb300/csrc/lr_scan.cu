@@ -29,20 +29,78 @@ namespace {
 constexpr int kNW = kThreads / 32;
 constexpr int kCarryFold = 32;  // tiles per fold of the blocked carry
 
-// Tile loads and stores.  Element j of the logical row is physical element j,
-// or N - 1 - j when `mirror` is set (a forward scan run as a reverse scan of
-// the mirrored row); with float4 items the four components are then taken in
-// reverse order.
+// A row as the tile kernels see it.  With float4 items a row of any length
+// and any 4-byte alignment is read as a "virtual row" that starts at the
+// 16-byte boundary at or before its first element and is padded to a multiple
+// of 4: its elements are virtual indices [lo, hi), the rest read as zeros and
+// are never written.  Only 16-byte chunks that hold some of the row's
+// elements are read, so every read stays inside the row's memory pages.  y
+// must share x's 16-byte misalignment (the caller checks).  With scalar items
+// the view is the row itself.
+struct RowView {
+  const float* x;  // virtual index 0 (16-byte aligned for float4 items)
+  float* y;
+  int64_t V;       // virtual length (a multiple of 4 for float4 items)
+  int64_t lo, hi;  // the row's elements
+};
+
+// EDGES = false: the caller guarantees whole aligned float4 rows (N % 4 == 0,
+// x 16-byte aligned), so the view is the row itself.
+template <int VEC, bool EDGES = true>
+__device__ __forceinline__ RowView row_view(const float* x, float* y, int64_t row, int64_t N) {
+  const float* xr = x + row * N;
+  int64_t m = 0;
+  if constexpr (VEC == 4 && EDGES) m = (int64_t)((reinterpret_cast<uintptr_t>(xr) >> 2) & 3);
+  RowView r;
+  r.x = xr - m;
+  r.y = y != nullptr ? y + row * N - m : nullptr;
+  r.lo = m;
+  r.hi = m + N;
+  r.V = (VEC == 4 && EDGES) ? ((m + N + 3) & ~(int64_t)3) : N;
+  return r;
+}
+
+// One tile of a row: virtual elements [base, base + len) of the row, or the
+// mirrored ones [V - base - len, V - base) when `mirror` is set (a forward
+// scan run as a reverse scan of the mirrored row).  x and y point at the
+// tile's lowest element in memory; element jj of the tile (in scan order) is
+// x[jj], or x[len - VEC - jj] mirrored, with float4 items' components then
+// taken in reverse order.  lo and hi bound the row's own elements relative to
+// x.  All tile-relative indices fit 32 bits.
+struct TileView {
+  const float* x;
+  float* y;
+  int len, lo, hi;
+};
+
+__device__ __forceinline__ TileView tile_view(const RowView& rv, int64_t base, int64_t tile, bool mirror) {
+  TileView tv;
+  const int64_t len = max((int64_t)0, min(tile, rv.V - base));  // 0: a tile past the row's end
+  const int64_t phys = len > 0 ? (mirror ? rv.V - base - len : base) : 0;
+  tv.x = rv.x + phys;
+  tv.y = rv.y != nullptr ? rv.y + phys : nullptr;
+  tv.len = (int)len;
+  tv.lo = (int)min(max(rv.lo - phys, (int64_t)0), len);
+  tv.hi = (int)min(max(rv.hi - phys, (int64_t)0), len);
+  return tv;
+}
+
+// Tile loads and stores.  Every float4 item of a virtual row holds at least
+// one row element (lo <= 3 and hi > V - 4), so the loads need no edge test: an
+// item at the row's edge reads its whole 16-byte granule, which lies in the
+// same page as the row element it holds.  The elements outside the row are
+// zeroed by mask_tile, called where the tile is consumed: masking right after
+// the loads would wait on them and stall a prefetch.  Stores write the row's
+// own elements only.
 template <int VEC, int SUB>
-__device__ __forceinline__ void load_tile(float (&v)[SUB][VEC], const float* xr, int64_t base,
-                                          int64_t N, int t, bool mirror) {
+__device__ __forceinline__ void load_tile(float (&v)[SUB][VEC], const TileView& tv, int t, bool mirror) {
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
-    const int64_t j = base + (int64_t)s * kThreads * VEC + (int64_t)t * VEC;
+    const int jj = s * kThreads * VEC + t * VEC;
     if constexpr (VEC == 4) {
-      // N % 4 == 0 on this path, so j < N means all four are in range.
+      // len % 4 == 0 and jj % 4 == 0, so jj < len means all four are in the tile.
       float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (j < N) q = ld_stream4(xr + (mirror ? N - 4 - j : j));
+      if (jj < tv.len) q = ld_stream4(tv.x + (mirror ? tv.len - 4 - jj : jj));
       if (mirror) {
         v[s][0] = q.w;
         v[s][1] = q.z;
@@ -55,25 +113,53 @@ __device__ __forceinline__ void load_tile(float (&v)[SUB][VEC], const float* xr,
         v[s][3] = q.w;
       }
     } else {
-      v[s][0] = (j < N) ? ld_stream1(xr + (mirror ? N - 1 - j : j)) : 0.f;
+      v[s][0] = (jj < tv.len) ? ld_stream1(tv.x + (mirror ? tv.len - 1 - jj : jj)) : 0.f;
     }
   }
 }
 
+// True when the tile holds an edge of its row (the same in every thread).
+__device__ __forceinline__ bool tile_has_edge(const TileView& tv) { return tv.lo > 0 || tv.hi < tv.len; }
+
+// Zeroes the loaded items' components that lie outside the row.
 template <int VEC, int SUB>
-__device__ __forceinline__ void store_tile(const float (&v)[SUB][VEC], float* yr, int64_t base,
-                                           int64_t N, int t, bool mirror) {
+__device__ __forceinline__ void mask_tile(float (&v)[SUB][VEC], const TileView& tv, int t, bool mirror) {
+  if constexpr (VEC == 4) {  // scalar tiles hold row elements only
+    if (!tile_has_edge(tv)) return;
+#pragma unroll
+    for (int s = 0; s < SUB; ++s) {
+      const int jj = s * kThreads * 4 + t * 4;
+      const int r = mirror ? tv.len - 4 - jj : jj;  // memory offset of the item
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int e = mirror ? r + 3 - c : r + c;  // memory offset of v[s][c]
+        if (e < tv.lo || e >= tv.hi) v[s][c] = 0.f;
+      }
+    }
+  }
+}
+
+template <int VEC, int SUB, bool EDGES = true>
+__device__ __forceinline__ void store_tile(const float (&v)[SUB][VEC], const TileView& tv, int t, bool mirror) {
+  const bool edge = EDGES && VEC == 4 && tile_has_edge(tv);
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
-    const int64_t j = base + (int64_t)s * kThreads * VEC + (int64_t)t * VEC;
-    if (j < N) {
+    const int jj = s * kThreads * VEC + t * VEC;
+    if (jj < tv.len) {
       if constexpr (VEC == 4) {
-        if (mirror)
-          st_stream4(yr + (N - 4 - j), make_float4(v[s][3], v[s][2], v[s][1], v[s][0]));
-        else
-          st_stream4(yr + j, make_float4(v[s][0], v[s][1], v[s][2], v[s][3]));
+        const int r = mirror ? tv.len - 4 - jj : jj;
+        float q[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) q[c] = mirror ? v[s][3 - c] : v[s][c];
+        if (!edge || (r >= tv.lo && r + 4 <= tv.hi)) {
+          st_stream4(tv.y + r, make_float4(q[0], q[1], q[2], q[3]));
+        } else {  // an edge of the row: its own elements only
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (r + c >= tv.lo && r + c < tv.hi) st_stream1(tv.y + r + c, q[c]);
+        }
       } else {
-        st_stream1(yr + (mirror ? N - 1 - j : j), v[s][0]);
+        st_stream1(tv.y + (mirror ? tv.len - 1 - jj : jj), v[s][0]);
       }
     }
   }
@@ -160,34 +246,34 @@ __device__ __forceinline__ void finalize(float (&v)[SUB][VEC], const TileScan<SU
 // Block per row: tiles right to left, carry in registers, next tile
 // prefetched into registers while the current one is scanned.
 // ---------------------------------------------------------------------------
-template <int VEC, int SUB>
+template <int VEC, int SUB, bool EDGES>
 __global__ void __launch_bounds__(kThreads) k_rscan_rows(RScanRowsParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
   __shared__ float sh_w[2][SUB][kNW];  // warp totals, double-buffered by tile parity
   const int t = threadIdx.x;
   const int lane = t & 31;
   const int w = t >> 5;
-  const int64_t N = p.N;
-  const int64_t ntiles = (N + TILE - 1) / TILE;
   const bool mirror = (p.flags & kScanMirror) != 0;
   const bool exclusive = (p.flags & kScanExclusive) != 0;
   int par = 0;
 
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-    const float* xr = p.x + row * N;
-    float* yr = p.y + row * N;
+    const RowView rv = row_view<VEC, EDGES>(p.x, p.y, row, p.N);
+    const int64_t ntiles = (rv.V + TILE - 1) / TILE;
     float cur[SUB][VEC];
     float nxt[SUB][VEC];
-    load_tile<VEC, SUB>(cur, xr, (ntiles - 1) * TILE, N, t, mirror);
+    load_tile<VEC, SUB>(cur, tile_view(rv, (ntiles - 1) * TILE, TILE, mirror), t, mirror);
     float carry_lo = 0.f, carry_hi = 0.f;
     int ncarry = 0;
 
     for (int64_t k = ntiles - 1; k >= 0; --k) {
       const int64_t base = k * TILE;
-      if (k > 0) load_tile<VEC, SUB>(nxt, xr, base - TILE, N, t, mirror);  // prefetch the next tile
+      if (k > 0) load_tile<VEC, SUB>(nxt, tile_view(rv, base - TILE, TILE, mirror), t, mirror);  // prefetch
+      const TileView tv = tile_view(rv, base, TILE, mirror);
+      if constexpr (EDGES) mask_tile<VEC, SUB>(cur, tv, t, mirror);
       const TileScan<SUB> ts = tile_suffix<VEC, SUB>(cur, sh_w[par], lane, w);
       finalize<VEC, SUB>(cur, ts, carry_hi + carry_lo, exclusive);
-      store_tile<VEC, SUB>(cur, yr, base, N, t, mirror);
+      store_tile<VEC, SUB, EDGES>(cur, tv, t, mirror);
       // Blocked carry: fold every kCarryFold tiles to keep chains short.
       carry_lo += ts.total;
       if (++ncarry == kCarryFold) {
@@ -312,14 +398,14 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
   const int64_t row = ticket / tiles;
   const int64_t k = ticket - row * tiles;       // from the right
   const int64_t base = (tiles - 1 - k) * TILE;  // tiles are aligned at the row's left end
-  const float* xr = p.x + row * p.N;
-  float* yr = p.y + row * p.N;
   unsigned long long* vals = p.node_val + row * 2 * tiles;
   const bool stalled = ticket == p.stall_tile;
 
   const bool mirror = (p.flags & kScanMirror) != 0;
+  const TileView tv = tile_view(row_view<VEC>(p.x, p.y, row, p.N), base, TILE, mirror);
   float v[SUB][VEC];
-  load_tile<VEC, SUB>(v, xr, base, p.N, t, mirror);
+  load_tile<VEC, SUB>(v, tv, t, mirror);
+  mask_tile<VEC, SUB>(v, tv, t, mirror);
   const TileScan<SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, lane, w);
   if (t == 0 && !stalled) st_relaxed_u64(vals + k, pack_node(epoch, ts.total));
 
@@ -377,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
   }
   __syncthreads();
   finalize<VEC, SUB>(v, ts, s_part[0], (p.flags & kScanExclusive) != 0);
-  store_tile<VEC, SUB>(v, yr, base, p.N, t, mirror);
+  store_tile<VEC, SUB>(v, tv, t, mirror);
 }
 
 // ---------------------------------------------------------------------------
@@ -400,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
 // the plain order (96% of copy bandwidth against 94%), the forward (mirrored)
 // scan with EARLY (92% against 85%).
 // ---------------------------------------------------------------------------
-template <int SUB, bool EARLY>
+template <int SUB, bool EARLY, bool EDGES>
 __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookbackParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * 4;
   __shared__ __align__(128) float s_tile[TILE];
@@ -428,14 +514,14 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
     if (tk < total) {
       const int64_t row = tk / tiles;
       const int64_t k = tk - row * tiles;
-      const int64_t base = (tiles - 1 - k) * TILE;
-      const int64_t len = min(TILE, p.N - base);
-      // The tile's elements in memory (mirrored rows hold them at the other end).
-      const int64_t phys = (p.flags & kScanMirror) ? p.N - base - len : base;
-      mbar_init(&s_bar, 1);
-      fence_mbar_init();
-      mbar_arrive_expect_tx(&s_bar, (unsigned)(len * 4));
-      bulk_load(s_tile, p.x + row * p.N + phys, (unsigned)(len * 4), &s_bar);
+      const TileView tv = tile_view(row_view<4, EDGES>(p.x, nullptr, row, p.N), (tiles - 1 - k) * TILE, TILE,
+                                    (p.flags & kScanMirror) != 0);
+      if (!EDGES || tv.len > 0) {  // 0: a tile past this row's end
+        mbar_init(&s_bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&s_bar, (unsigned)tv.len * 4u);
+        bulk_load(s_tile, tv.x, (unsigned)tv.len * 4u, &s_bar);
+      }
     }
   }
   __syncthreads();
@@ -452,10 +538,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
   const int64_t u = ticket - p.lag;
   const bool mirror = (p.flags & kScanMirror) != 0;
   float v[SUB][4];
+  TileView tv_u{};
   if (u >= 0) {
     const int64_t row = u / tiles;
     const int64_t k = u - row * tiles;
-    load_tile<4, SUB>(v, p.x + row * p.N, (tiles - 1 - k) * TILE, p.N, t, mirror);
+    tv_u = tile_view(row_view<4, EDGES>(p.x, p.y, row, p.N), (tiles - 1 - k) * TILE, TILE, mirror);
+    load_tile<4, SUB>(v, tv_u, t, mirror);
   }
 
   // ---- write out tile `ticket - lag` ----
@@ -463,7 +551,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
     if (u < 0) return;
     const int64_t row = u / tiles;
     const int64_t k = u - row * tiles;
-    const int64_t base = (tiles - 1 - k) * TILE;
     unsigned long long* vals = p.node_val + row * 2 * tiles;
     if (w < levels) {
       int64_t off = 0, count = tiles;
@@ -480,11 +567,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
       if (lane == 0) s_part[w] = part;
       if (__any_sync(kFullMask, fail) && lane == 0) s_fail = 1;
     }
+    if constexpr (EDGES) mask_tile<4, SUB>(v, tv_u, t, mirror);
     const TileScan<SUB> ts = tile_suffix<4, SUB>(v, sh_w, lane, w);  // its barrier publishes s_part
     float excl = 0.f;
     for (int L = 0; L < levels; ++L) excl += s_part[L];  // from the lowest level up
     finalize<4, SUB>(v, ts, excl, (p.flags & kScanExclusive) != 0);
-    store_tile<4, SUB>(v, p.y + row * p.N, base, p.N, t, mirror);
+    store_tile<4, SUB, EDGES>(v, tv_u, t, mirror);
   };
 
   // The reverse scan writes first (its reread overlaps tile `ticket`'s copy),
@@ -495,21 +583,35 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
   if (ticket < total) {
     const int64_t row = ticket / tiles;
     const int64_t k = ticket - row * tiles;
-    const int64_t len = min(TILE, p.N - (tiles - 1 - k) * TILE);
+    // The copy's layout: shared element jj is tv.x[jj], whatever the direction.
+    const TileView tv = tile_view(row_view<4, EDGES>(p.x, nullptr, row, p.N), (tiles - 1 - k) * TILE, TILE,
+                                  (p.flags & kScanMirror) != 0);
     bool loaded = true;
-    for (int64_t it = 0; !mbar_try_wait_parity(&s_bar, 0u); ++it)
-      if (it >= p.spin_limit) {
-        loaded = false;
-        break;
-      }
+    if (!EDGES || tv.len > 0)
+      for (int64_t it = 0; !mbar_try_wait_parity(&s_bar, 0u); ++it)
+        if (it >= p.spin_limit) {
+          loaded = false;
+          break;
+        }
     if (!loaded) s_fail = 1;
     float e[SUB];
 #pragma unroll
     for (int s = 0; s < SUB; ++s) {
-      const int64_t j = (int64_t)s * kThreads * 4 + (int64_t)t * 4;
-      float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (j < len) q = *reinterpret_cast<const float4*>(s_tile + j);
-      e[s] = (q.x + q.y) + (q.z + q.w);
+      const int jj = s * kThreads * 4 + t * 4;
+      float q[4] = {0.f, 0.f, 0.f, 0.f};
+      if (jj < tv.len) {
+        const float4 f = *reinterpret_cast<const float4*>(s_tile + jj);
+        q[0] = f.x;
+        q[1] = f.y;
+        q[2] = f.z;
+        q[3] = f.w;
+        if (EDGES && tile_has_edge(tv) && (jj < tv.lo || jj + 4 > tv.hi)) {  // an edge of the row
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (jj + c < tv.lo || jj + c >= tv.hi) q[c] = 0.f;
+        }
+      }
+      e[s] = (q[0] + q[1]) + (q[2] + q[3]);
     }
     const float a = block_sum<kThreads>(tree_sum<SUB>(e), s_red);  // thread 0
     unsigned long long* vals = p.node_val + row * 2 * tiles;
@@ -565,7 +667,10 @@ __global__ void __launch_bounds__(kThreads) k_tile_sums(TileSumsParams p) {
   const int64_t row = b / p.tiles;
   const int64_t k = b - row * p.tiles;
   float v[SUB][VEC];
-  load_tile<VEC, SUB>(v, p.x + row * p.N, k * TILE, p.N, threadIdx.x, (p.flags & kScanMirror) != 0);
+  const bool mirror = (p.flags & kScanMirror) != 0;
+  const TileView tv = tile_view(row_view<VEC>(p.x, nullptr, row, p.N), k * TILE, TILE, mirror);
+  load_tile<VEC, SUB>(v, tv, threadIdx.x, mirror);
+  mask_tile<VEC, SUB>(v, tv, threadIdx.x, mirror);
   float e[SUB];
 #pragma unroll
   for (int s = 0; s < SUB; ++s) e[s] = tree_sum<VEC>(v[s]);
@@ -583,10 +688,12 @@ __global__ void __launch_bounds__(kThreads) k_tile_carry_scan(TileCarryParams p)
   const int64_t k = b - row * p.tiles;
   const bool mirror = (p.flags & kScanMirror) != 0;
   float v[SUB][VEC];
-  load_tile<VEC, SUB>(v, p.x + row * p.N, k * TILE, p.N, t, mirror);
+  const TileView tv = tile_view(row_view<VEC>(p.x, p.y, row, p.N), k * TILE, TILE, mirror);
+  load_tile<VEC, SUB>(v, tv, t, mirror);
+  mask_tile<VEC, SUB>(v, tv, t, mirror);
   const TileScan<SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, t & 31, t >> 5);
   finalize<VEC, SUB>(v, ts, p.carries[b], (p.flags & kScanExclusive) != 0);
-  store_tile<VEC, SUB>(v, p.y + row * p.N, k * TILE, p.N, t, mirror);
+  store_tile<VEC, SUB>(v, tv, t, mirror);
 }
 
 // ---------------------------------------------------------------------------
@@ -731,9 +838,15 @@ int64_t lookback_tile(int variant) {
 cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
   switch (variant) {
-    case kRScanV1S4: k_rscan_rows<1, 4><<<g, kThreads, 0, s>>>(p); break;
-    case kRScanV4S2: k_rscan_rows<4, 2><<<g, kThreads, 0, s>>>(p); break;
-    case kRScanV4S4: k_rscan_rows<4, 4><<<g, kThreads, 0, s>>>(p); break;
+    case kRScanV1S4: k_rscan_rows<1, 4, false><<<g, kThreads, 0, s>>>(p); break;
+    case kRScanV4S2:
+      if (p.flags & kScanRowEdges) k_rscan_rows<4, 2, true><<<g, kThreads, 0, s>>>(p);
+      else k_rscan_rows<4, 2, false><<<g, kThreads, 0, s>>>(p);
+      break;
+    case kRScanV4S4:
+      if (p.flags & kScanRowEdges) k_rscan_rows<4, 4, true><<<g, kThreads, 0, s>>>(p);
+      else k_rscan_rows<4, 4, false><<<g, kThreads, 0, s>>>(p);
+      break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -746,8 +859,13 @@ cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int
     case kLookbackV1: k_rscan_lookback<1, 8><<<g, kThreads, 0, s>>>(p); break;
     case kLookbackV4: k_rscan_lookback<4, 8><<<g, kThreads, 0, s>>>(p); break;
     case kLookbackL2:
-      if (p.flags & kScanMirror) k_rscan_lookback_l2<8, true><<<g, kThreads, 0, s>>>(p);
-      else k_rscan_lookback_l2<8, false><<<g, kThreads, 0, s>>>(p);
+      if (p.flags & kScanRowEdges) {
+        if (p.flags & kScanMirror) k_rscan_lookback_l2<8, true, true><<<g, kThreads, 0, s>>>(p);
+        else k_rscan_lookback_l2<8, false, true><<<g, kThreads, 0, s>>>(p);
+      } else {
+        if (p.flags & kScanMirror) k_rscan_lookback_l2<8, true, false><<<g, kThreads, 0, s>>>(p);
+        else k_rscan_lookback_l2<8, false, false><<<g, kThreads, 0, s>>>(p);
+      }
       break;
     default: return cudaErrorInvalidValue;
   }
@@ -759,7 +877,10 @@ int occupancy_rscan_lookback(int variant) {
     case kLookbackV1: return occupancy_of(k_rscan_lookback<1, 8>);
     case kLookbackV4: return occupancy_of(k_rscan_lookback<4, 8>);
     case kLookbackL2:
-      return std::min(occupancy_of(k_rscan_lookback_l2<8, false>), occupancy_of(k_rscan_lookback_l2<8, true>));
+      return std::min({occupancy_of(k_rscan_lookback_l2<8, false, false>),
+                       occupancy_of(k_rscan_lookback_l2<8, true, false>),
+                       occupancy_of(k_rscan_lookback_l2<8, false, true>),
+                       occupancy_of(k_rscan_lookback_l2<8, true, true>)});
     default: return 0;
   }
 }
@@ -820,9 +941,9 @@ int occupancy_scan_cols(int variant) {
 
 int occupancy_rscan_rows(int variant) {
   switch (variant) {
-    case kRScanV1S4: return occupancy_of(k_rscan_rows<1, 4>);
-    case kRScanV4S2: return occupancy_of(k_rscan_rows<4, 2>);
-    case kRScanV4S4: return occupancy_of(k_rscan_rows<4, 4>);
+    case kRScanV1S4: return occupancy_of(k_rscan_rows<1, 4, false>);
+    case kRScanV4S2: return std::min(occupancy_of(k_rscan_rows<4, 2, false>), occupancy_of(k_rscan_rows<4, 2, true>));
+    case kRScanV4S4: return std::min(occupancy_of(k_rscan_rows<4, 4, false>), occupancy_of(k_rscan_rows<4, 4, true>));
     default: return 0;
   }
 }

@@ -74,6 +74,55 @@ def test_rows_misaligned(offset, out_offset, reverse, exclusive):
         check((1, 300_000), 1, reverse, exclusive, offset=offset, out_offset=out_offset)
 
 
+# Rows of any length and any 4-byte offset (shared by x and y) run on the
+# float4 paths as aligned "virtual rows": the float4 items at a row's two
+# edges are masked.  N = 3 * 8192 - 1 over 4 rows gives rows whose virtual
+# lengths differ by one float4 across a tile boundary, so some rows end
+# with a tile that holds none of their elements.
+VIRTUAL_ROWS = [(4, 3 * 8192 - 1), (5, 8192 + 2), (3, 100_003), (2, 32767), (9, 4097), (1, 5), (6, 3)]
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("strategy", [1, 2, 3, 4])
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
+def test_rows_virtual_float4(strategy, offset, reverse, exclusive):
+    L.set_option(L.OPT_SCAN_STRATEGY, strategy)
+    for rows, n in VIRTUAL_ROWS:
+        got, _ = check((rows, n), 1, reverse, exclusive, offset=offset, out_offset=offset)
+        if exclusive:
+            assert np.all(got[:, n - 1 if reverse else 0] == 0.0)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("strategy", [1, 2, 3, 4])
+def test_rows_virtual_integers_exact(strategy, reverse, exclusive):
+    """Small integers sum exactly, so a masked edge item that leaked into a
+    tile total (or a dropped element) changes some output bit."""
+    L.set_option(L.OPT_SCAN_STRATEGY, strategy)
+    for rows, n in [(4, 3 * 8192 - 1), (3, 20_001)]:
+        for offset in (1, 3):
+            x = inputs.make((rows, n), "int:0:3", 17 + offset)
+            ref, _ = oracle.cumsum(x.numpy(), rows, n, 1, reverse, exclusive)
+            got = run(x, 1, reverse, exclusive, offset, offset)
+            assert_exact(got.reshape(-1), ref.reshape(-1), f"[{rows},{n}] s={strategy} off={offset}")
+
+
+def test_rows_virtual_neighbours_untouched():
+    """Stores at a row's edges write only the row's own elements: the floats
+    around a misaligned output keep their values."""
+    for strategy in (1, 2, 3, 4):
+        L.set_option(L.OPT_SCAN_STRATEGY, strategy)
+        for reverse in (False, True):
+            x = inputs.make((3, 8192 + 2), "uniform01", 5)
+            n = x.numel()
+            buf = torch.full((n + 8,), 7.0, device="cuda")
+            y = buf[1:1 + n].view(x.shape)
+            L.cumsum_f32(on_device(x, 1), 1, reverse=reverse, out=y)
+            L.check()
+            rest = torch.cat([buf[:1], buf[1 + n:]]).cpu()
+            assert torch.all(rest == 7.0), (strategy, reverse)
+
+
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("shape,dim", [((4, 9, 7), 1), ((2, 1000, 64), 1), ((3, 257, 33), 1),
                                        ((1, 5000, 4096), 1), ((600, 8), 0), ((7, 6, 5, 4), 2),
