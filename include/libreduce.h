@@ -299,7 +299,11 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *                                 1 float4 columns, 2 x 4; 2 float4 columns, 1 x 8;
  *                                 3, 4 the narrow-row scan, tiles in shared memory or a
  *                                 warp per (plane, segment) (inner <= 32 scalar or 128
- *                                 float4 columns: the automatic choice there)
+ *                                 float4 columns: the automatic choice there);
+ *                                 5 the single-pass look-back over 256-row x 32-column
+ *                                 tiles (the automatic choice where one block per
+ *                                 (o, column tile) cannot fill the GPU; falls back to
+ *                                 the automatic choice when its tiles exceed 32768)
  *                                 (float4 columns need inner % 4 == 0 and aligned x, y) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6

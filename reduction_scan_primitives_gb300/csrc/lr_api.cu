@@ -47,6 +47,7 @@ struct DeviceState {
   int occ_narrow[2][kNumReduceOps] = {};  // [vec4][op]
   int occ_scan_narrow[2] = {};            // [vec4]
   int occ_scan_narrow_warp[2] = {};       // [vec4]
+  int occ_scan_cols_lb = 0;
 };
 
 std::mutex g_mu;
@@ -98,6 +99,7 @@ int device_state(DeviceState** out, int* dev_out) {
       st.occ_scan_narrow[v4] = std::max(1, occupancy_scan_narrow(v4 ? 4 : 1));
       st.occ_scan_narrow_warp[v4] = std::max(1, occupancy_scan_narrow_warp(v4 ? 4 : 1));
     }
+    st.occ_scan_cols_lb = std::max(1, occupancy_scan_cols_lookback());
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
   }
@@ -699,6 +701,37 @@ double predict_scan_cols(int64_t units, int64_t slots, double lane_eff, double b
 // scanned again from its carry.  The block shape and the segment count are
 // chosen by predict_scan_cols, the segmented form paying 1.5x for the extra
 // read of x.
+// Single-pass column scan with a look-back over 256-row x 32-column tiles
+// (k_scan_cols_lookback).  Returns kColLbNoFit, before touching anything,
+// when the tiles' node words would not fit the look-back region.
+constexpr int kColLbNoFit = -2;  // distinct from kQueried
+int run_scan_cols_lookback(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
+                           float* y, bool reverse, bool exclusive, cudaStream_t s) {
+  const int64_t col_tiles = ceil_div(inner, kColLbCols);
+  const int64_t tiles = ceil_div(N, kColLbRows);
+  int64_t units = 0, total = 0;
+  if (mul_overflows(outer, col_tiles, &units) || mul_overflows(units, tiles, &total) ||
+      total > kMaxLookbackTiles / kColLbCols)
+    return kColLbNoFit;
+  Need need;
+  need.header = true;
+  need.nodes = 2 * total * kColLbCols;
+  Scratch sc;
+  int rc = acquire(pv, need, &sc, s);
+  if (rc) return rc;
+  auto* ticket_word = reinterpret_cast<unsigned long long*>(sc.header + 2);
+  const int64_t spin = g_opt_spin_limit.load();
+  const int64_t lag_opt = g_opt_lookback_lag.load();
+  const int64_t resident = (int64_t)pv.st->sm_count * pv.st->occ_scan_cols_lb;
+  const int64_t lag = std::min<int64_t>(total, lag_opt > 0 ? lag_opt : std::max<int64_t>(64, ceil_div(resident * 5 / 3, 64) * 64));
+  ScanColsLookbackParams p{x, y, outer, N, inner, col_tiles, tiles, sc.nodes, ticket_word, sc.header,
+                           spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag,
+                           reverse ? 1 : 0, exclusive ? 1 : 0};
+  // float4 items need whole aligned float4s in every row of x and y.
+  const bool vec4 = inner % 4 == 0 && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+  return launched(launch_scan_cols_lookback(vec4 ? 4 : 1, p, total + lag, s));
+}
+
 int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
                   float* y, bool reverse, bool exclusive, cudaStream_t s) {
   DeviceState* st = pv.st;
@@ -747,6 +780,13 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
         segs = sg;
       }
     }
+  }
+  // Where the blocks of one unit each would not fill the GPU, the single-pass
+  // look-back replaces the three-pass segmented form (unless a variant or a
+  // split is forced).
+  if (forced_v == kScanColsLookback || (segs > 1 && forced_v < 0 && forced <= 0)) {
+    const int rc = run_scan_cols_lookback(pv, x, outer, N, inner, y, reverse, exclusive, s);
+    if (rc != kColLbNoFit) return rc;
   }
   const int64_t units = outer * ceil_div(inner, scan_cols_block_width(variant));
   // The segment sums come from the split column reduction, whose column tiles
@@ -1038,7 +1078,7 @@ int libreduce_set_option(int option, int64_t value) {
       g_opt_rscan_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_SCAN_COLS_VARIANT:
-      if (value < -1 || value > kScanColsNarrowWarp) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < -1 || value > kScanColsLookback) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_LOOKBACK_LAG:

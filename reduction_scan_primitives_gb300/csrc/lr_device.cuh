@@ -79,6 +79,56 @@ __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
   return v;
 }
 
+// Look-back node words: {epoch:32, fp32 bits:32}.  A word counts only if its
+// epoch is the current launch's, so node buffers never need clearing.
+__device__ __forceinline__ unsigned long long pack_node(unsigned epoch, float v) {
+  return ((unsigned long long)epoch << 32) | (unsigned long long)__float_as_uint(v);
+}
+
+// Poll a node until it carries this launch's epoch (or give up).
+__device__ __forceinline__ float wait_node(const unsigned long long* node, unsigned epoch,
+                                           int64_t limit, const unsigned* abort_word, bool* fail) {
+  unsigned ns = 0;
+  for (int64_t it = 0;; ++it) {
+    const unsigned long long word = ld_relaxed_u64(node);
+    if ((unsigned)(word >> 32) == epoch) return __uint_as_float((unsigned)word);
+    if (it >= limit || ld_relaxed_u32(abort_word) == epoch) {
+      *fail = true;
+      return 0.f;
+    }
+    if (it >= 64) {  // spin first, then back off gently
+      ns = ns ? (ns < 256 ? 2 * ns : ns) : 32;
+      __nanosleep(ns);
+    }
+  }
+}
+
+// Fixed pairwise tree over the 32 lanes (adjacent pairs first); lane 0 gets it.
+__device__ __forceinline__ float warp_tree_adjacent(float v) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) v += __shfl_down_sync(kFullMask, v, o);
+  return v;
+}
+
+// Tickets and the launch's epoch (the tag that tells this launch's node words
+// from older ones) share one 64-bit device word: epoch in the high half, the
+// ticket counter in the low half.  One atomicAdd gives a block both; the
+// block with the last ticket -- every other block has taken its ticket --
+// resets the counter and advances the epoch (0 is reserved for "never
+// written").  Kept on the device rather than passed by the host, so a launch
+// captured in a CUDA graph gets a new epoch at every replay.
+struct Ticket {
+  unsigned ticket, epoch;
+};
+__device__ __forceinline__ Ticket take_ticket(unsigned long long* word) {
+  const unsigned long long old = atomicAdd(word, 1ull);
+  const unsigned e = (unsigned)(old >> 32);
+  return Ticket{(unsigned)old, e == 0 ? 1u : e};
+}
+__device__ __forceinline__ void next_launch(unsigned long long* word, unsigned epoch) {
+  atomicExch(word, (unsigned long long)(epoch + 1 == 0 ? 1u : epoch + 1) << 32);
+}
+
 // ---------------------------------------------------------------------------
 // Bulk copies (TMA engine, 1D) into shared memory, completed on an mbarrier.
 // ---------------------------------------------------------------------------
@@ -123,6 +173,20 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, 
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst_smem)),
       "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Tiled tensor copy (TMA engine) of one 3-D box into shared memory, completed
+// on an mbarrier.  `tmap` is the generic address of a tensor map held in
+// kernel parameter space (__grid_constant__); c0 is the innermost coordinate
+// (c0 * element size must be a multiple of 16 bytes), c1 and c2 may lie
+// outside the tensor, whose elements there arrive as zeros.
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, int c0, int c1, int c2,
+                                            unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
 

@@ -151,6 +151,31 @@ struct RScanLookbackParams {
   int flags;                     // kScanMirror | kScanExclusive
 };
 
+// --- Scan along a strided axis, single-pass look-back over column tiles -----
+// x, y are [outer, N, inner], scanned along N.  A unit is (o, column tile ct)
+// of kColLbCols columns; its tile k holds scan positions [k*kColLbRows,
+// (k+1)*kColLbRows) (position n is row N-1-n when reverse).  Tickets run over
+// (o, k, ct) with ct fastest, so blocks in flight cover whole rows.  Node
+// words {epoch, fp32} per column: unit u's level-L node m, column c, is
+// node_val[((u*2*tiles) + off_L + m) * kColLbCols + c].
+constexpr int kColLbRows = 256;
+constexpr int kColLbCols = 32;
+constexpr int kColLbMaxLevels = 3;  // 32^3 tiles per unit at most
+struct ScanColsLookbackParams {
+  const float* x;
+  float* y;
+  int64_t outer, N, inner;
+  int64_t col_tiles;                // ceil(inner / kColLbCols)
+  int64_t tiles;                    // per unit: ceil(N / kColLbRows)
+  unsigned long long* node_val;     // outer * col_tiles * 2 * tiles * kColLbCols words
+  unsigned long long* ticket_word;  // as in RScanLookbackParams
+  unsigned* err_word;               // as in RScanLookbackParams
+  int64_t spin_limit;
+  int64_t stall_tile;               // test fault: this ticket never publishes (-1: none)
+  int64_t lag;                      // tickets between a tile's two touches
+  int reverse, exclusive;
+};
+
 // Reduction operators of the reduce kernels (the epilogue in the params turns
 // a sum into a mean and a sum of squares into a norm).
 enum ReduceOp { kOpSum = 0, kOpSumSq = 1, kOpMax = 2, kOpMin = 3, kNumReduceOps };
@@ -194,6 +219,7 @@ inline bool scan_cols_vec4(int variant) { return variant == kScanColsV4 || varia
 // warp form (one warp per (o, segment)).
 constexpr int kScanColsNarrow = kNumScanColsVariants;
 constexpr int kScanColsNarrowWarp = kNumScanColsVariants + 1;
+constexpr int kScanColsLookback = kNumScanColsVariants + 2;  // k_scan_cols_lookback
 enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
 
 // Elements per tile of the reduce-then-scan passes.
@@ -231,6 +257,8 @@ cudaError_t launch_scan_narrow_warp(int vec, const ScanColsParams& p, int64_t gr
 int occupancy_scan_narrow_warp(int vec);
 cudaError_t launch_reduce_narrow_warp(int vec, int op, const NarrowParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_tile_carry_scan(int variant, const TileCarryParams& p, int64_t grid, cudaStream_t s);
+cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, int64_t grid, cudaStream_t s);
+int occupancy_scan_cols_lookback();
 
 // Host helpers defined in lr_api.cu, for entry points in other files.
 int check_device_buffer(const void* p, size_t bytes, int dev);  // a libreduce status

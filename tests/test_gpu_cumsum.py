@@ -250,3 +250,95 @@ def test_axis_narrow_wide_forced_agree():
     for shape in ((2, 3000, 4), (3, 1000, 7), (2, 500, 32)):
         check(shape, 1, True, False)
         check(shape, 1, False, True)
+
+
+# The single-pass column look-back (OPT_SCAN_COLS_VARIANT 5): 256-row x
+# 32-column tiles, tickets column tile fastest, a 32-ary look-back per column.
+COL_LB = 5
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape,offset", [((2, 1000, 64), 0), ((3, 257, 33), 1), ((1, 9000, 40), 2),
+                                          ((2, 600, 4095), 3), ((1, 256, 32), 0), ((4, 255, 5), 0),
+                                          ((1, 1, 70), 0), ((2, 20, 3), 1), ((1, 270_000, 3), 0)])
+def test_axis_lookback(shape, offset, reverse, exclusive):
+    """Several tiles per unit, ragged row and column tiles, fewer rows than a
+    tile, one to three look-back levels (9000 rows: 36 tiles, two levels;
+    270000 rows: 1055 tiles, three), any 4-byte offset of x and of y."""
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, COL_LB)
+    got, _ = check(shape, 1, reverse, exclusive, offset=offset, out_offset=(offset + 1) % 4)
+    if exclusive:
+        assert np.all(got[:, shape[1] - 1 if reverse else 0, :] == 0.0)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+def test_axis_lookback_integers_exact(reverse, exclusive):
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, COL_LB)
+    for shape in ((2, 9000, 40), (1, 2000, 4095), (3, 300, 7)):
+        x = inputs.make(shape, "int:0:3", 9)
+        o, n, i = L.canonical_axis(x.shape, 1)
+        ref, _ = oracle.cumsum(x.numpy(), o, n, i, reverse, exclusive)
+        assert_exact(run(x, 1, reverse, exclusive).reshape(-1), ref.reshape(-1), f"look-back int {shape}")
+
+
+def test_axis_lookback_bitwise_any_lag():
+    """Every sum runs in a fixed order, so the result does not depend on the
+    lag between a tile's two touches (which changes the timing and which
+    waits happen) and is bit-identical across runs."""
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, COL_LB)
+    x = on_device(inputs.make((2, 9000, 100), "normal", 12))
+    first = L.cumsum_f32(x, 1, reverse=True)
+    for lag in (0, 1, 7, 64, 5000, 0):
+        L.set_option(L.OPT_LOOKBACK_LAG, lag)
+        assert bitwise_equal(L.cumsum_f32(x, 1, reverse=True), first), lag
+    L.check()
+
+
+def test_axis_lookback_bounded_wait_reports_timeout():
+    """A tile that never publishes (chosen on the host) makes the waits behind
+    it run out: the kernel returns, the host reads TIMEOUT, and the library
+    keeps working afterwards."""
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, COL_LB)
+    x = on_device(inputs.make((1, 4096, 64), "uniform01", 3))
+    L.set_option(L.OPT_SPIN_LIMIT, 2000)
+    L.set_option(L.OPT_STALL_TILE, 3)
+    L.cumsum_f32(x, 1)
+    with pytest.raises(L.LibreduceError) as ei:
+        L.check()
+    assert ei.value.status == L.ERR_TIMEOUT
+    L.set_option(L.OPT_STALL_TILE, -1)
+    L.set_option(L.OPT_SPIN_LIMIT, 0)
+    L.check()  # the error word was cleared
+    xc = x.cpu()
+    ref, scale = oracle.cumsum(xc.numpy(), 1, 4096, 64, False, False)
+    assert_close(L.cumsum_f32(x, 1).cpu().numpy().reshape(-1), ref.reshape(-1), scale.reshape(-1), "after timeout")
+
+
+def test_axis_lookback_is_the_automatic_choice_for_few_units():
+    """[1, 5000, 4096] has 16 column tiles of the wide kernel: the library
+    takes the one-launch look-back instead of the three-pass segmented scan,
+    and both match the oracle."""
+    x = inputs.make((1, 5000, 4096), "uniform_pm1", 5)
+    ref, scale = oracle.cumsum(x.numpy(), 1, 5000, 4096, True, False)
+    xd = on_device(x)
+    n0 = L.launch_count()
+    auto = L.cumsum_f32(xd, 1, reverse=True)
+    L.check()
+    assert L.launch_count() - n0 == 1
+    assert_close(auto.cpu().numpy().reshape(-1), ref.reshape(-1), scale.reshape(-1), "automatic")
+    L.set_option(L.OPT_AXIS_SPLIT, 8)  # a forced split keeps the three-pass form
+    n0 = L.launch_count()
+    three = L.cumsum_f32(xd, 1, reverse=True)
+    L.check()
+    assert L.launch_count() - n0 == 3
+    assert_close(three.cpu().numpy().reshape(-1), ref.reshape(-1), scale.reshape(-1), "three passes")
+
+
+def test_axis_lookback_caller_workspace_matches():
+    x = on_device(inputs.make((2, 3000, 300), "normal", 6))
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, COL_LB)
+    plain = L.cumsum_f32(x, 1, exclusive=True)
+    ws = L.workspace(L.cumsum_ws_f32(x, 1, exclusive=True))
+    got = L.cumsum_ws_f32(x, 1, exclusive=True, ws=ws)
+    L.check_ws(ws)
+    assert bitwise_equal(got, plain)

@@ -24,7 +24,10 @@ def calls(x1, xa, xl, xn, xc, outs, ws):
     L.reverse_cumsum_f32(xl, out=outs["lookback"])           # few long rows: the look-back scan
     L.cumsum_f32(xl, 1, exclusive=True, out=outs["forward"])  # the look-back, mirrored
     L.cumsum_f32(xn, 1, out=outs["narrow"])                   # narrow rows, segmented
-    L.cumsum_f32(xc, 1, reverse=True, out=outs["cols"])       # column tiles, segmented
+    L.cumsum_f32(xc, 1, reverse=True, out=outs["cols"])       # few column tiles: the column look-back
+    L.set_option(L.OPT_AXIS_SPLIT, 6)
+    L.cumsum_f32(xc, 1, exclusive=True, out=outs["cols3"])     # the same, forced into three passes
+    L.set_option(L.OPT_AXIS_SPLIT, 0)
     L.cumsum_ws_f32(xl, 1, reverse=True, ws=ws, out=outs["lookback_ws"])
 
 
@@ -35,7 +38,8 @@ def test_capture_and_replay():
     outs = {"sum": torch.empty((), device="cuda"), "axis": torch.empty(8, 300, device="cuda"),
             "max": torch.empty(8, 300, device="cuda"), "lookback": torch.empty_like(xs["xl"]),
             "forward": torch.empty_like(xs["xl"]), "narrow": torch.empty_like(xs["xn"]),
-            "cols": torch.empty_like(xs["xc"]), "lookback_ws": torch.empty_like(xs["xl"])}
+            "cols": torch.empty_like(xs["xc"]), "cols3": torch.empty_like(xs["xc"]),
+            "lookback_ws": torch.empty_like(xs["xl"])}
     ws = L.workspace(L.cumsum_ws_f32(xs["xl"], 1, reverse=True))
     args = (xs["x1"], xs["xa"], xs["xl"], xs["xn"], xs["xc"], outs, ws)
     calls(*args)  # the first calls allocate the library workspace
