@@ -67,6 +67,7 @@ PROFILE_CASES = {
     "cumsum_256x8192x64_d1": dict(op="cumsum", shape=(256, 8192, 64), dim=1, reverse=False,
                                   exclusive=False, dist="uniform01", seed=13),
     "sum_16x1000000x12_d1": dict(inputs.WORKLOADS["sum_16x1000000x12_d1"]),
+    "cumsum_2x8192x4096_d1": dict(inputs.WORKLOADS["cumsum_2x8192x4096_d1"]),
 }
 FALLBACK_HBM_GBS = 6800.0
 # Context only (another machine): the page's T4 figures for the 1D sum.

@@ -635,6 +635,7 @@ int run_reduce_then_scan(const Provider& pv, const float* x, int64_t rows, int64
   if (rc) return rc;
   float* sums = sc.partials;
   float* carries = sc.partials + total;
+  if (vec4 && has_row_edges(x, N)) flags |= kScanRowEdges;
   TileSumsParams p1{x, rows, N, tiles, sums, flags};
   if ((rc = launched(launch_tile_sums(variant, p1, total, s)))) return rc;
   RScanRowsParams p2{sums, carries, rows, tiles, kScanExclusive};

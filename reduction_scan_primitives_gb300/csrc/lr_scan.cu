@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
 // mirrored) row, and the middle pass -- a reverse exclusive row scan of the
 // tile sums -- turns the sums into each tile's carry.
 // ---------------------------------------------------------------------------
-template <int VEC, int SUB>
+template <int VEC, int SUB, bool EDGES>
 __global__ void __launch_bounds__(kThreads) k_tile_sums(TileSumsParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
   __shared__ float sh[kNW];
@@ -622,9 +622,9 @@ __global__ void __launch_bounds__(kThreads) k_tile_sums(TileSumsParams p) {
   const int64_t k = b - row * p.tiles;
   float v[SUB][VEC];
   const bool mirror = (p.flags & kScanMirror) != 0;
-  const TileView tv = tile_view(row_view<VEC>(p.x, nullptr, row, p.N), k * TILE, TILE, mirror);
+  const TileView tv = tile_view(row_view<VEC, EDGES>(p.x, nullptr, row, p.N), k * TILE, TILE, mirror);
   load_tile<VEC, SUB>(v, tv, threadIdx.x, mirror);
-  mask_tile<VEC, SUB>(v, tv, threadIdx.x, mirror);
+  if constexpr (EDGES) mask_tile<VEC, SUB>(v, tv, threadIdx.x, mirror);
   float e[SUB];
 #pragma unroll
   for (int s = 0; s < SUB; ++s) e[s] = tree_sum<VEC>(v[s]);
@@ -632,8 +632,8 @@ __global__ void __launch_bounds__(kThreads) k_tile_sums(TileSumsParams p) {
   if (threadIdx.x == 0) p.sums[b] = a;
 }
 
-template <int VEC, int SUB>
-__global__ void __launch_bounds__(kThreads) k_tile_carry_scan(TileCarryParams p) {
+template <int VEC, int SUB, bool EDGES>
+__global__ void __launch_bounds__(kThreads, 3) k_tile_carry_scan(TileCarryParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
   __shared__ float sh_w[SUB][kNW];
   const int t = threadIdx.x;
@@ -642,12 +642,12 @@ __global__ void __launch_bounds__(kThreads) k_tile_carry_scan(TileCarryParams p)
   const int64_t k = b - row * p.tiles;
   const bool mirror = (p.flags & kScanMirror) != 0;
   float v[SUB][VEC];
-  const TileView tv = tile_view(row_view<VEC>(p.x, p.y, row, p.N), k * TILE, TILE, mirror);
+  const TileView tv = tile_view(row_view<VEC, EDGES>(p.x, p.y, row, p.N), k * TILE, TILE, mirror);
   load_tile<VEC, SUB>(v, tv, t, mirror);
-  mask_tile<VEC, SUB>(v, tv, t, mirror);
+  if constexpr (EDGES) mask_tile<VEC, SUB>(v, tv, t, mirror);
   const TileScan<SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, t & 31, t >> 5);
   finalize<VEC, SUB>(v, ts, p.carries[b], (p.flags & kScanExclusive) != 0);
-  store_tile<VEC, SUB>(v, tv, t, mirror);
+  store_tile<VEC, SUB, EDGES>(v, tv, t, mirror);
 }
 
 // ---------------------------------------------------------------------------
@@ -872,15 +872,23 @@ int64_t tile_scan_len(int variant) { return variant == kTileV4 ? 8 * kThreads * 
 
 cudaError_t launch_tile_sums(int variant, const TileSumsParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
-  if (variant == kTileV4) k_tile_sums<4, 8><<<g, kThreads, 0, s>>>(p);
-  else k_tile_sums<1, 8><<<g, kThreads, 0, s>>>(p);
+  if (variant == kTileV4) {
+    if (p.flags & kScanRowEdges) k_tile_sums<4, 8, true><<<g, kThreads, 0, s>>>(p);
+    else k_tile_sums<4, 8, false><<<g, kThreads, 0, s>>>(p);
+  } else {
+    k_tile_sums<1, 8, false><<<g, kThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_tile_carry_scan(int variant, const TileCarryParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
-  if (variant == kTileV4) k_tile_carry_scan<4, 8><<<g, kThreads, 0, s>>>(p);
-  else k_tile_carry_scan<1, 8><<<g, kThreads, 0, s>>>(p);
+  if (variant == kTileV4) {
+    if (p.flags & kScanRowEdges) k_tile_carry_scan<4, 8, true><<<g, kThreads, 0, s>>>(p);
+    else k_tile_carry_scan<4, 8, false><<<g, kThreads, 0, s>>>(p);
+  } else {
+    k_tile_carry_scan<1, 8, false><<<g, kThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
