@@ -303,7 +303,7 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *                                 5 the single-pass look-back over 256-row x 32-column
  *                                 tiles (the automatic choice where one block per
  *                                 (o, column tile) cannot fill the GPU; falls back to
- *                                 the automatic choice when its tiles exceed 32768)
+ *                                 the automatic choice when its tiles exceed 262144)
  *                                 (float4 columns need inner % 4 == 0 and aligned x, y) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6

@@ -24,7 +24,11 @@ constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxTickets = 1 << 16;       // integer tickets (per row / column tile)
 constexpr int64_t kMaxPartials = 1 << 22;      // fp32 partial sums (16 MiB)
 constexpr size_t kHeaderBytes = 256;           // error word, abort word, {ticket counter, epoch}
-constexpr int64_t kMaxLookbackTiles = 1 << 20; // look-back tiles per launch
+// Look-back node words (allocated on the first look-back of a device, 128 MB):
+// a row look-back takes 2 words per tile, a column look-back 2 per tile and
+// column.
+constexpr int64_t kLookbackWords = int64_t(1) << 24;
+constexpr int64_t kMaxLookbackTiles = kLookbackWords / 2;  // row look-back tiles per launch
 constexpr size_t kWorkspaceBytes =
     kHeaderBytes + sizeof(unsigned) * kMaxTickets + sizeof(float) * kMaxPartials;
 
@@ -137,7 +141,7 @@ int ensure_lookback(DeviceState* st) {
   if (rc) return rc;
   std::lock_guard<std::mutex> lk(g_mu);
   if (st->node_val) return LIBREDUCE_OK;
-  const size_t nodes = 2 * (size_t)kMaxLookbackTiles;
+  const size_t nodes = (size_t)kLookbackWords;
   const size_t bytes = nodes * sizeof(unsigned long long);
   void* p = nullptr;
   cudaError_t e = cudaMalloc(&p, bytes);
@@ -712,7 +716,7 @@ int run_scan_cols_lookback(const Provider& pv, const float* x, int64_t outer, in
   const int64_t tiles = ceil_div(N, kColLbRows);
   int64_t units = 0, total = 0;
   if (mul_overflows(outer, col_tiles, &units) || mul_overflows(units, tiles, &total) ||
-      total > kMaxLookbackTiles / kColLbCols)
+      total > kLookbackWords / (2 * kColLbCols))
     return kColLbNoFit;
   Need need;
   need.header = true;
@@ -856,6 +860,17 @@ int run_scan_narrow(const Provider& pv, const float* x, int64_t outer, int64_t N
     if (cand > 1 && predict_scan_cols(outer * cand, slots, lane_eff, 1.0) / 1.5 >
                         predict_scan_cols(outer, slots, lane_eff, 1.0))
       segs = cand;
+  }
+  // Where the planes must be cut into segments and the float4 columns (x, y
+  // aligned) fill 32-column tiles (at least 90% of their lanes), the
+  // single-pass column look-back
+  // beats the three passes (measured: [2, 4e6, 128] 0.70 against 0.62,
+  // [2, 2e6, 96] 0.66 against 0.50, [8, 2e6, 32] 0.67 against 0.65; with
+  // idle lanes it loses, e.g. [2, 4e6, 36] 0.40 against 0.44).
+  if (segs > 1 && forced <= 0 && !warp_form && vec == 4 && g_opt_scan_cols_variant.load() < 0 &&
+      10 * inner >= 9 * kColLbCols * ceil_div(inner, kColLbCols)) {
+    const int rc = run_scan_cols_lookback(pv, x, outer, N, inner, y, reverse, exclusive, s);
+    if (rc != kColLbNoFit) return rc;
   }
   if (segs > 1) {
     const int64_t cap = kMaxPartials / (2 * outer * part_stride);

@@ -342,3 +342,27 @@ def test_axis_lookback_caller_workspace_matches():
     got = L.cumsum_ws_f32(x, 1, exclusive=True, ws=ws)
     L.check_ws(ws)
     assert bitwise_equal(got, plain)
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+def test_narrow_few_planes_take_the_lookback(reverse, exclusive):
+    """Few planes of narrow float4 rows whose columns fill 32-column tiles are
+    scanned by the single-pass column look-back (one launch) instead of the
+    three-pass segmented narrow scan; both agree with the oracle."""
+    for shape in ((1, 200_000, 32), (2, 60_000, 96)):
+        x = inputs.make(shape, "uniform_pm1", 21)
+        o, n, i = L.canonical_axis(x.shape, 1)
+        ref, scale = oracle.cumsum(x.numpy(), o, n, i, reverse, exclusive)
+        xd = on_device(x)
+        n0 = L.launch_count()
+        got = L.cumsum_f32(xd, 1, reverse=reverse, exclusive=exclusive)
+        L.check()
+        assert L.launch_count() - n0 == 1, shape
+        assert_close(got.cpu().numpy().reshape(-1), ref.reshape(-1), scale.reshape(-1), f"look-back {shape}")
+        L.set_option(L.OPT_SCAN_COLS_VARIANT, 3)  # the narrow kernel, segmented
+        n0 = L.launch_count()
+        three = L.cumsum_f32(xd, 1, reverse=reverse, exclusive=exclusive)
+        L.check()
+        assert L.launch_count() - n0 == 3, shape
+        assert_close(three.cpu().numpy().reshape(-1), ref.reshape(-1), scale.reshape(-1), f"narrow {shape}")
+        L.set_option(L.OPT_SCAN_COLS_VARIANT, -1)
