@@ -42,17 +42,17 @@ static_assert(kColLbCols == 32 && kColsPerWarp == 4, "a 32-column tile, 4 column
 static_assert(TR == 32 * kNW, "a warp covers 32 rows of a tile");
 
 struct TilePos {
-  int64_t o, k, ct;
+  int o, k, ct;  // tickets and tile counts fit 31 bits (the host caps the tiles of a launch)
 };
 
 // Tickets and tile counts fit 32 bits (the host caps the tiles of a launch),
 // so the divisions are 32-bit; one thread computes them for the block.
-__device__ __forceinline__ TilePos tile_pos(int64_t ticket, int64_t tiles, int64_t col_tiles) {
-  const unsigned tk = (unsigned)ticket, per_o = (unsigned)(tiles * col_tiles), ct = (unsigned)col_tiles;
+__device__ __forceinline__ TilePos tile_pos(int ticket, int tiles, int col_tiles) {
+  const unsigned tk = (unsigned)ticket, per_o = (unsigned)tiles * (unsigned)col_tiles, ct = (unsigned)col_tiles;
   const unsigned o = tk / per_o;
   const unsigned r = tk - o * per_o;
   const unsigned k = r / ct;
-  return TilePos{(int64_t)o, (int64_t)k, (int64_t)(r - k * ct)};
+  return TilePos{(int)o, (int)k, (int)(r - k * ct)};
 }
 
 // Offset in x and y of scan position n (< N) of column col of outer index o.
@@ -62,7 +62,7 @@ __device__ __forceinline__ int64_t elem_off(const ScanColsLookbackParams& p, int
 }
 
 __device__ __forceinline__ unsigned long long* unit_nodes(const ScanColsLookbackParams& p, const TilePos& q) {
-  return p.node_val + (q.o * p.col_tiles + q.ct) * 2 * p.tiles * kColLbCols;
+  return p.node_val + ((int64_t)q.o * p.col_tiles + q.ct) * 2 * p.tiles * kColLbCols;
 }
 
 // Thread layout of a 256 x 32 tile with VEC-wide items: LPR = 32 / VEC lanes
@@ -83,8 +83,8 @@ template <int VEC>
 __device__ __forceinline__ const float* tile_ptr(const ScanColsLookbackParams& p, const float* base,
                                                  const TilePos& q, int w, int lane, int* rows, bool* cok) {
   using Ly = Layout<VEC>;
-  const int64_t col = q.ct * kColLbCols + (lane % Ly::LPR) * VEC;
-  const int64_t n0 = q.k * TR + w * 32 + (lane / Ly::LPR) * Ly::R;
+  const int64_t col = (int64_t)q.ct * kColLbCols + (lane % Ly::LPR) * VEC;
+  const int64_t n0 = (int64_t)q.k * TR + w * 32 + (lane / Ly::LPR) * Ly::R;
   *rows = (int)max((int64_t)0, min((int64_t)Ly::R, p.N - n0));
   *cok = col < p.inner;  // with VEC 4, inner % 4 == 0: all four columns or none
   return (*rows > 0 && *cok) ? base + elem_off(p, q.o, n0, col) : base;
@@ -146,7 +146,7 @@ __device__ __forceinline__ float pick4(const float (&a)[4], int i) {
 // VEC 4 (inner % 4 == 0, x and y 16-byte aligned) copies tiles with the
 // tensor map `tmap` ([outer, N, inner] fp32, box 32 x 256 x 1); VEC 1 ignores it.
 template <int VEC>
-__global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLookbackParams p,
+__global__ void __launch_bounds__(kThreads, 4) k_scan_cols_lookback(ScanColsLookbackParams p,
                                                                     const __grid_constant__ CUtensorMap tmap) {
   using Ly = Layout<VEC>;
   constexpr int R = Ly::R;
@@ -164,23 +164,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLook
   const int cg = lane % Ly::LPR;
   const int rq = lane / Ly::LPR;
   const unsigned* abort_word = p.err_word + 1;
-  const int64_t K = p.tiles;
-  const int64_t total = p.outer * K * p.col_tiles;
+  const int K = (int)p.tiles;
+  const int CT = (int)p.col_tiles;
+  const int lag = (int)p.lag;
+  const int total = (int)(p.outer * p.tiles * p.col_tiles);
 
   if (t == 0) {
     const Ticket tkt = take_ticket(p.ticket_word);
     s_ticket = tkt.ticket;
     s_epoch = tkt.epoch;
     // Every other ticket is taken before the last one: reset for the next launch.
-    if ((int64_t)tkt.ticket == total + p.lag - 1) next_launch(p.ticket_word, tkt.epoch);
-    const int64_t tk = tkt.ticket;
-    const TilePos q = tk < total ? tile_pos(tk, K, p.col_tiles) : TilePos{0, 0, 0};
+    if ((int64_t)tkt.ticket == (int64_t)total + lag - 1) next_launch(p.ticket_word, tkt.epoch);
+    const int tk = (int)tkt.ticket;
+    const TilePos q = tk < total ? tile_pos(tk, K, CT) : TilePos{0, 0, 0};
     s_pos[0] = q;
-    s_pos[1] = (tk >= p.lag && tk - p.lag < total) ? tile_pos(tk - p.lag, K, p.col_tiles) : TilePos{0, 0, 0};
+    s_pos[1] = (tk >= lag && tk - lag < total) ? tile_pos(tk - lag, K, CT) : TilePos{0, 0, 0};
     if (kTma && tk < total) {
       // The box's first row in memory: scan positions k*256 .. k*256+255 are
       // rows N-1-k*256 down to N-256-k*256 when reverse (possibly negative).
-      const int64_t row0 = p.reverse ? p.N - (q.k + 1) * TR : q.k * TR;
+      const int64_t row0 = p.reverse ? p.N - (int64_t)(q.k + 1) * TR : (int64_t)q.k * TR;
       mbar_init(&s_bar, 1);
       fence_mbar_init();
       mbar_arrive_expect_tx(&s_bar, (unsigned)sizeof(s_tile));
@@ -188,12 +190,12 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLook
     }
   }
   __syncthreads();
-  const int64_t ticket = s_ticket;
   const unsigned epoch = s_epoch;
-  if (ticket >= total + p.lag) {  // a stale counter: touch nothing
+  if ((int64_t)s_ticket >= (int64_t)total + lag) {  // a stale counter: touch nothing
     if (t == 0) atomicOr(p.err_word, 2u);
     return;
   }
+  const int ticket = (int)s_ticket;
   const int64_t step = p.reverse ? -p.inner : p.inner;  // from one scan position to the next
   int levels = 1;
   while (levels < kColLbMaxLevels && ((K - 1) >> (5 * levels)) != 0) ++levels;
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLook
   }
 
   // ---- 2. reread tile u = ticket - lag (from L2) ----
-  const int64_t u = ticket - p.lag;
+  const int u = ticket - lag;
   float v[R][VEC];
   int rows_u = 0;
   bool cok_u = false;
@@ -241,9 +243,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLook
     // leaves its per-level partial sums (siblings in order) in s_part ----
     const TilePos qu = s_pos[1];
     const unsigned long long* vals = unit_nodes(p, qu);
-    int64_t off = 0, count = K;
+    int off = 0, count = K;
     for (int L = 0; L < levels; ++L) {
-      const int64_t m = qu.k >> (5 * L);
+      const int m = qu.k >> (5 * L);
       const int d = (int)(m & 31);
       const unsigned long long* sib = vals + (off + m - d) * kColLbCols + lane;
       unsigned long long word[4];
@@ -269,9 +271,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLook
   }
 
   // ---- 4. scan tile u and write it ----
-  // Sequential prefix over my R rows, then the row groups before mine in this
-  // warp and the warps before mine (fixed orders), then the carry.
-  float pre[VEC];
+  // Sequential prefix over my R rows, to which the row groups before mine in
+  // this warp are added before the barrier; after it the carry and the warps
+  // before mine (fixed orders).
 #pragma unroll
   for (int c = 0; c < VEC; ++c) {
     float run = 0.f;
@@ -288,13 +290,14 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLook
       if (g < rq) acc += tg;
       wt += tg;
     }
-    pre[c] = acc;
+#pragma unroll
+    for (int i = 0; i < R; ++i) v[i][c] = acc + v[i][c];
     if (rq == 0) s_tot[w][cg * VEC + c] = wt;  // the warp's column totals
   }
   __syncthreads();  // s_tot and s_part complete
   if (u >= 0 && cok_u) {
     // carry = sum over levels (lowest first) of the warp partials in warp
-    // order; base = carry + (warps before mine + row groups before mine).
+    // order; base = carry + warps before mine.
     float carry[VEC], wsum[VEC];
 #pragma unroll
     for (int c = 0; c < VEC; ++c) carry[c] = wsum[c] = 0.f;
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLook
     }
     float basev[VEC];
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) basev[c] = carry[c] + (wsum[c] + pre[c]);
+    for (int c = 0; c < VEC; ++c) basev[c] = carry[c] + wsum[c];
     // The stride is hidden from the optimiser here: otherwise it reuses the
     // row addresses of the reread and holds them all in registers.
     int64_t st = step;
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLook
     if (!stalled) {
       if (lane < kColsPerWarp)
         st_relaxed_u64(vals + q.k * kColLbCols + col0 + lane, pack_node(epoch, pick4(own, lane)));
-      int64_t off = 0, count = K, m = q.k;
+      int off = 0, count = K, m = q.k;
       for (int L = 0; L + 1 < levels && (m & 31) == 31; ++L) {
         float val[kColsPerWarp];
         bool f2 = false;
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan_cols_lookback(ScanColsLook
           fail = true;
           break;
         }
-        const int64_t next_off = off + count;
+        const int next_off = off + count;
         if (lane < kColsPerWarp)
           st_relaxed_u64(vals + (next_off + (m >> 5)) * kColLbCols + col0 + lane, pack_node(epoch, pick4(own, lane)));
         off = next_off;
