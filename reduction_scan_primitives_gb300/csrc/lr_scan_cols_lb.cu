@@ -39,7 +39,8 @@ constexpr int kNW = kThreads / 32;
 constexpr int TR = kColLbRows;
 constexpr int kColsPerWarp = kColLbCols / kNW;  // look-back and publication: warp w owns 4 columns
 static_assert(kColLbCols == 32 && kColsPerWarp == 4, "a 32-column tile, 4 columns per warp");
-static_assert(TR == 32 * kNW, "a warp covers 32 rows of a tile");
+constexpr int kRowsPerWarp = TR / kNW;  // a warp covers this many consecutive rows of a tile
+static_assert(TR % (4 * kNW) == 0, "every thread owns whole rows");
 
 struct TilePos {
   int o, k, ct;  // tickets and tile counts fit 31 bits (the host caps the tiles of a launch)
@@ -65,16 +66,17 @@ __device__ __forceinline__ unsigned long long* unit_nodes(const ScanColsLookback
   return p.node_val + ((int64_t)q.o * p.col_tiles + q.ct) * 2 * p.tiles * kColLbCols;
 }
 
-// Thread layout of a 256 x 32 tile with VEC-wide items: LPR = 32 / VEC lanes
-// across a row, RG = VEC row groups per warp, R = 32 / VEC consecutive rows
-// (in scan order) per thread.  Thread (w, lane) owns columns cg*VEC ..
-// cg*VEC + VEC-1 (cg = lane % LPR) of rows w*32 + rq*R .. + R-1 (rq = lane /
-// LPR); it copies, sums, rereads, scans and writes exactly those.
+// Thread layout of a TR x 32 tile with VEC-wide items: LPR = 32 / VEC lanes
+// across a row, RG = VEC row groups per warp, R = kRowsPerWarp / VEC
+// consecutive rows (in scan order) per thread.  Thread (w, lane) owns columns
+// cg*VEC .. cg*VEC + VEC-1 (cg = lane % LPR) of rows w*kRowsPerWarp + rq*R ..
+// + R-1 (rq = lane / LPR); it copies, sums, rereads, scans and writes exactly
+// those.
 template <int VEC>
 struct Layout {
   static constexpr int LPR = 32 / VEC;
   static constexpr int RG = VEC;
-  static constexpr int R = 32 / VEC;
+  static constexpr int R = kRowsPerWarp / VEC;
 };
 
 // Pointer to the thread's first element of tile q (scan position
@@ -84,7 +86,7 @@ __device__ __forceinline__ const float* tile_ptr(const ScanColsLookbackParams& p
                                                  const TilePos& q, int w, int lane, int* rows, bool* cok) {
   using Ly = Layout<VEC>;
   const int64_t col = (int64_t)q.ct * kColLbCols + (lane % Ly::LPR) * VEC;
-  const int64_t n0 = (int64_t)q.k * TR + w * 32 + (lane / Ly::LPR) * Ly::R;
+  const int64_t n0 = (int64_t)q.k * TR + w * kRowsPerWarp + (lane / Ly::LPR) * Ly::R;
   *rows = (int)max((int64_t)0, min((int64_t)Ly::R, p.N - n0));
   *cok = col < p.inner;  // with VEC 4, inner % 4 == 0: all four columns or none
   return (*rows > 0 && *cok) ? base + elem_off(p, q.o, n0, col) : base;
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_scan_cols_lookback(ScanColsLook
   const int64_t step = p.reverse ? -p.inner : p.inner;  // from one scan position to the next
   int levels = 1;
   while (levels < kColLbMaxLevels && ((K - 1) >> (5 * levels)) != 0) ++levels;
-  float* my_tile = &s_tile[w * 32 + rq * R][cg * VEC];  // row i of mine: my_tile + i * 32
+  float* my_tile = &s_tile[w * kRowsPerWarp + rq * R][cg * VEC];  // row i of mine: my_tile + i * 32
   const int col0 = w * kColsPerWarp;                    // this warp's look-back columns
   bool fail = false;
 
