@@ -138,3 +138,55 @@ def test_workspace_calls_match_default():
     got = L.reduce_axis_op_ws_f32(x, 0, "sum", ws=ws)
     L.check_ws(ws)
     assert bitwise_equal(got, ref)
+
+
+def offset_pair(shape, offset, dist, seed):
+    """x and y of `shape` at the same 4-byte offset from 16-byte aligned
+    allocations, x filled from the seeded generator."""
+    n = int(np.prod(shape))
+    xb = torch.empty(n + 4, dtype=torch.float32, device=DEV)
+    yb = torch.empty(n + 4, dtype=torch.float32, device=DEV)
+    x = xb[offset:offset + n].view(shape)
+    x.copy_(inputs.make(shape, dist, seed, device=DEV))
+    return x, yb[offset:offset + n].view(shape)
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+def test_odd_long_row_both_directions(offset):
+    """One row of 999,999,999 (not a whole number of float4s), at a 4-byte
+    offset or not: the float4 look-back with masked row edges, reverse and
+    forward exclusive, against the oracle's sums of sampled suffixes and
+    prefixes; the end outputs are exact."""
+    n = 999_999_999
+    x, y = offset_pair((1, n), offset, "uniform01", 23)
+    xh = x.cpu().numpy().reshape(-1)
+    js = pick(n, 3, 6, edges=(0, 1, 2, 3, 4, 4095, 4096, 8191, 8192))
+    L.reverse_cumsum_f32(x, out=y)
+    L.check()
+    assert y[0, -1].item() == x[0, -1].item()
+    got = y[0, torch.as_tensor(js, device=DEV)].cpu().numpy()
+    for j, g in zip(js, got):
+        ref, scale = oracle.sum1d(xh[j:])
+        assert_close(g, ref, scale, f"suffix {j} (offset {offset})")
+    L.cumsum_f32(x, 1, exclusive=True, out=y)
+    L.check()
+    assert y[0, 0].item() == 0.0
+    got = y[0, torch.as_tensor(js, device=DEV)].cpu().numpy()
+    for j, g in zip(js, got):
+        ref, scale = oracle.sum1d(xh[:j])
+        assert_close(g, ref, scale, f"prefix {j} (offset {offset})")
+
+
+@pytest.mark.parametrize("reverse", [True, False])
+def test_odd_rows_at_offset(reverse):
+    """[32768, 32767] at a 4-byte offset: one block per row with masked row
+    edges.  Sampled rows against the oracle, the end column exactly x."""
+    x, y = offset_pair((32768, 32767), 3, "uniform01", 29)
+    L.cumsum_f32(x, 1, reverse=reverse, out=y)
+    L.check()
+    end = -1 if reverse else 0
+    assert torch.equal(y[:, end], x[:, end])
+    rows = torch.as_tensor(pick(32768, 40, 7, edges=(0, 1, 2, 3)), device=DEV)
+    xs = x.index_select(0, rows).cpu().numpy()
+    ref, scale = oracle.cumsum(xs, len(rows), 32767, 1, reverse, False)
+    assert_close(y.index_select(0, rows).cpu().numpy(), ref, scale, f"odd rows reverse={reverse}")
