@@ -158,7 +158,8 @@ struct RScanLookbackParams {
 // (o, k, ct) with ct fastest, so blocks in flight cover whole rows.  Node
 // words {epoch, fp32} per column: unit u's level-L node m, column c, is
 // node_val[((u*2*tiles) + off_L + m) * kColLbCols + c].
-constexpr int kColLbRows = 256;
+constexpr int kColLbWarps = 8;                // warps per block; a warp covers 32 rows of a tile
+constexpr int kColLbRows = 32 * kColLbWarps;  // rows per tile
 constexpr int kColLbCols = 32;
 constexpr int kColLbMaxLevels = 3;  // 32^3 tiles per unit at most
 struct ScanColsLookbackParams {

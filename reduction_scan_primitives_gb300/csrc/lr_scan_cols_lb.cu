@@ -35,12 +35,16 @@
 namespace lr {
 namespace {
 
-constexpr int kNW = kThreads / 32;
+constexpr int kNW = kColLbWarps;
+constexpr int kLbThreads = 32 * kNW;
 constexpr int TR = kColLbRows;
-constexpr int kColsPerWarp = kColLbCols / kNW;  // look-back and publication: warp w owns 4 columns
-static_assert(kColLbCols == 32 && kColsPerWarp == 4, "a 32-column tile, 4 columns per warp");
+constexpr int kColsPerWarp = kColLbCols / kNW;  // publication: warp w owns these columns
+constexpr int kSibPerWarp = (31 + kNW - 1) / kNW;  // look-back siblings a warp reads per level
+static_assert(kColLbCols == 32 && kColLbCols % kNW == 0, "a 32-column tile, whole columns per warp");
 constexpr int kRowsPerWarp = TR / kNW;  // a warp covers this many consecutive rows of a tile
-static_assert(TR % (4 * kNW) == 0, "every thread owns whole rows");
+static_assert(kRowsPerWarp == 32, "every thread owns whole rows");
+constexpr int kBoxRows = 256;  // a tensor copy moves at most 256 rows
+static_assert(TR % kBoxRows == 0, "whole boxes per tile");
 
 struct TilePos {
   int o, k, ct;  // tickets and tile counts fit 31 bits (the host caps the tiles of a launch)
@@ -105,7 +109,7 @@ __device__ __forceinline__ void load_item(float (&d)[VEC], const float* src) {
   }
 }
 
-// The four node words of one lane (columns col0 .. col0+3 of one node):
+// The node words of one lane (columns col0 .. col0+kColsPerWarp-1 of one node):
 // read them, then poll the ones that do not yet carry this launch's epoch
 // until they do (bounded: on giving up *fail is set and they read as 0).
 __device__ __forceinline__ void read_words(const unsigned long long* src, bool active, unsigned epoch,
@@ -141,19 +145,25 @@ __device__ __forceinline__ void read_words(const unsigned long long* src, bool a
     out[c] = (active && (unsigned)(word[c] >> 32) == epoch) ? __uint_as_float((unsigned)word[c]) : 0.f;
 }
 
-__device__ __forceinline__ float pick4(const float (&a)[4], int i) {
-  return i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : a[3];
+__device__ __forceinline__ float pick(const float (&a)[kColsPerWarp], int i) {
+  float r = a[0];
+#pragma unroll
+  for (int c = 1; c < kColsPerWarp; ++c)
+    if (i == c) r = a[c];
+  return r;
 }
 
 // VEC 4 (inner % 4 == 0, x and y 16-byte aligned) copies tiles with the
 // tensor map `tmap` ([outer, N, inner] fp32, box 32 x 256 x 1); VEC 1 ignores it.
+// The tile lands in dynamic shared memory (TR x 32 floats).
 template <int VEC>
-__global__ void __launch_bounds__(kThreads, 4) k_scan_cols_lookback(ScanColsLookbackParams p,
-                                                                    const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(kLbThreads, 32 / kNW) k_scan_cols_lookback(
+    ScanColsLookbackParams p, const __grid_constant__ CUtensorMap tmap) {
   using Ly = Layout<VEC>;
   constexpr int R = Ly::R;
   constexpr bool kTma = VEC == 4;
-  __shared__ __align__(128) float s_tile[TR][kColLbCols];
+  extern __shared__ __align__(128) float s_tile_mem[];
+  float(*s_tile)[kColLbCols] = reinterpret_cast<float(*)[kColLbCols]>(s_tile_mem);
   __shared__ unsigned long long s_bar;
   __shared__ __align__(16) float s_tot[kNW][kColLbCols];  // warp totals of the reread tile
   __shared__ __align__(16) float s_sum[kNW][kColLbCols];  // warp sums of the copied tile
@@ -182,13 +192,16 @@ __global__ void __launch_bounds__(kThreads, 4) k_scan_cols_lookback(ScanColsLook
     s_pos[0] = q;
     s_pos[1] = (tk >= lag && tk - lag < total) ? tile_pos(tk - lag, K, CT) : TilePos{0, 0, 0};
     if (kTma && tk < total) {
-      // The box's first row in memory: scan positions k*256 .. k*256+255 are
-      // rows N-1-k*256 down to N-256-k*256 when reverse (possibly negative).
+      // The tile's first row in memory: scan positions k*TR .. k*TR+TR-1 are
+      // rows N-1-k*TR down to N-TR-k*TR when reverse (possibly negative).
       const int64_t row0 = p.reverse ? p.N - (int64_t)(q.k + 1) * TR : (int64_t)q.k * TR;
       mbar_init(&s_bar, 1);
       fence_mbar_init();
-      mbar_arrive_expect_tx(&s_bar, (unsigned)sizeof(s_tile));
-      tma_load_3d(&s_tile[0][0], &tmap, (int)(q.ct * kColLbCols), (int)row0, (int)q.o, &s_bar);
+      mbar_arrive_expect_tx(&s_bar, (unsigned)(TR * kColLbCols * sizeof(float)));
+#pragma unroll
+      for (int b = 0; b < TR / kBoxRows; ++b)
+        tma_load_3d(&s_tile[b * kBoxRows][0], &tmap, (int)(q.ct * kColLbCols), (int)(row0 + b * kBoxRows),
+                    (int)q.o, &s_bar);
     }
   }
   __syncthreads();
@@ -250,16 +263,17 @@ __global__ void __launch_bounds__(kThreads, 4) k_scan_cols_lookback(ScanColsLook
       const int m = qu.k >> (5 * L);
       const int d = (int)(m & 31);
       const unsigned long long* sib = vals + (off + m - d) * kColLbCols + lane;
-      unsigned long long word[4];
+      unsigned long long word[kSibPerWarp];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) word[i] = w + 8 * i < d ? ld_relaxed_u64(sib + (w + 8 * i) * kColLbCols) : 0ull;
+      for (int i = 0; i < kSibPerWarp; ++i)
+        word[i] = w + kNW * i < d ? ld_relaxed_u64(sib + (w + kNW * i) * kColLbCols) : 0ull;
       float part = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (w + 8 * i < d)
+      for (int i = 0; i < kSibPerWarp; ++i) {
+        if (w + kNW * i < d)
           part += (unsigned)(word[i] >> 32) == epoch
                       ? __uint_as_float((unsigned)word[i])
-                      : wait_node(sib + (w + 8 * i) * kColLbCols, epoch, p.spin_limit, abort_word, &fail);
+                      : wait_node(sib + (w + kNW * i) * kColLbCols, epoch, p.spin_limit, abort_word, &fail);
       }
       s_part[L][w][lane] = part;
       off += count;
@@ -414,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_scan_cols_lookback(ScanColsLook
     }
     if (!stalled) {
       if (lane < kColsPerWarp)
-        st_relaxed_u64(vals + q.k * kColLbCols + col0 + lane, pack_node(epoch, pick4(own, lane)));
+        st_relaxed_u64(vals + q.k * kColLbCols + col0 + lane, pack_node(epoch, pick(own, lane)));
       int off = 0, count = K, m = q.k;
       for (int L = 0; L + 1 < levels && (m & 31) == 31; ++L) {
         float val[kColsPerWarp];
@@ -429,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_scan_cols_lookback(ScanColsLook
         }
         const int next_off = off + count;
         if (lane < kColsPerWarp)
-          st_relaxed_u64(vals + (next_off + (m >> 5)) * kColLbCols + col0 + lane, pack_node(epoch, pick4(own, lane)));
+          st_relaxed_u64(vals + (next_off + (m >> 5)) * kColLbCols + col0 + lane, pack_node(epoch, pick(own, lane)));
         off = next_off;
         count >>= 5;
         m >>= 5;
@@ -476,25 +490,34 @@ bool encode_cols_map(CUtensorMap* m, const ScanColsLookbackParams& p) {
     return false;
   const cuuint64_t dims[3] = {(cuuint64_t)p.inner, (cuuint64_t)p.N, (cuuint64_t)p.outer};
   const cuuint64_t strides[2] = {(cuuint64_t)p.inner * 4, (cuuint64_t)p.N * (cuuint64_t)p.inner * 4};
-  const cuuint32_t box[3] = {kColLbCols, TR, 1};
+  const cuuint32_t box[3] = {kColLbCols, kBoxRows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p.x), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr size_t kTileBytes = (size_t)TR * kColLbCols * sizeof(float);  // dynamic shared memory
+
 cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, int64_t grid, cudaStream_t s) {
   CUtensorMap m;
   std::memset(&m, 0, sizeof(m));
-  if (vec == 4 && encode_cols_map(&m, p)) k_scan_cols_lookback<4><<<dim3((unsigned)grid), kThreads, 0, s>>>(p, m);
-  else k_scan_cols_lookback<1><<<dim3((unsigned)grid), kThreads, 0, s>>>(p, m);
+  if (vec == 4 && encode_cols_map(&m, p))
+    k_scan_cols_lookback<4><<<dim3((unsigned)grid), kLbThreads, kTileBytes, s>>>(p, m);
+  else
+    k_scan_cols_lookback<1><<<dim3((unsigned)grid), kLbThreads, kTileBytes, s>>>(p, m);
   return cudaGetLastError();
 }
 
 int occupancy_scan_cols_lookback() {
   int n1 = 0, n4 = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, k_scan_cols_lookback<1>, kThreads, 0) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n4, k_scan_cols_lookback<4>, kThreads, 0) != cudaSuccess)
+  if (cudaFuncSetAttribute(k_scan_cols_lookback<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTileBytes) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(k_scan_cols_lookback<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTileBytes) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, k_scan_cols_lookback<1>, kLbThreads, kTileBytes) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n4, k_scan_cols_lookback<4>, kLbThreads, kTileBytes) != cudaSuccess)
     return 0;
   return n1 < n4 ? n1 : n4;
 }
