@@ -29,9 +29,10 @@
  *    documented with their op codes).  NaN and Inf propagate as IEEE addition
  *    does.
  *  - Scratch: the library keeps one workspace per device for partial sums,
- *    tickets and look-back flags.  It is allocated (cudaMalloc) by the first
- *    call on that device that needs it, so that first call must not be made
- *    inside a stream capture.  Because the workspace is shared, calls on one
+ *    tickets and look-back flags (about 17 MB, plus 128 MB of look-back node
+ *    words once a look-back scan has run).  It is allocated (cudaMalloc) by
+ *    the first call on that device that needs it, so that first call must not
+ *    be made inside a stream capture.  Because the workspace is shared, calls on one
  *    device must not run concurrently on different streams; calls queued on
  *    one stream are always safe.  The *_ws variants take the scratch from
  *    the caller instead and lift this limit.
@@ -170,7 +171,9 @@ LIBREDUCE_API int reverse_cumsum_f32(const float* x, int64_t rows, int64_t N, fl
  * directions and dims); reverse_cumsum_f32(x, rows, N, y, s) is
  * cumsum_f32(x, rows, N, 1, y, LIBREDUCE_SCAN_REVERSE, s).  inner == 1 scans
  * rows with the row kernels (a forward scan runs as a reverse scan of the
- * mirrored row); inner > 1 scans columns, coalesced across inner.  Every
+ * mirrored row); inner > 1 scans columns, coalesced across inner (where the
+ * (o, column tile) units are too few to fill the GPU, by a single-pass
+ * look-back over 256-row x 32-column tiles).  Every
  * output is built from additions over its own terms only (no subtraction),
  * and an exclusive output with no terms is +0.0f.
  *   x     device, outer*N*inner floats
