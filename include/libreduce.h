@@ -268,7 +268,10 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *                                form), 3 look-back keeping each tile in registers between
  *                                its read and its write (one HBM read, no L2 reread),
  *                                4 reduce-then-scan (tile sums, a scan of the sums, every
- *                                tile scanned again with its carry: three passes)
+ *                                tile scanned again with its carry: three passes),
+ *                                5 many short rows (N <= 2048; the automatic choice
+ *                                there): chunks of whole rows staged in shared memory,
+ *                                each row scanned by a group of 1 to 32 lanes
  *   LIBREDUCE_OPT_AXIS_SPLIT     0 auto, k > 0 forces k slices of the reduce axis
  *                                (inner > 1), or k chunks per row (inner == 1)
  *   LIBREDUCE_OPT_SPIN_LIMIT     0 default, else the look-back wait limit in polls

@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "lib", "libreduce.so")
-SOURCES = ["lr_api.cu", "lr_reduce.cu", "lr_scan.cu", "lr_scan_cols_lb.cu", "lr_narrow.cu", "lr_noalloc.cu"]
+SOURCES = ["lr_api.cu", "lr_reduce.cu", "lr_scan.cu", "lr_scan_cols_lb.cu", "lr_rows_short.cu", "lr_narrow.cu",
+           "lr_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-Wall,-fvisibility=hidden",
               "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]

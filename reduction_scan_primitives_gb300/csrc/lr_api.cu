@@ -52,6 +52,7 @@ struct DeviceState {
   int occ_scan_narrow[2] = {};            // [vec4]
   int occ_scan_narrow_warp[2] = {};       // [vec4]
   int occ_scan_cols_lb = 0;
+  int occ_rscan_short = 0;
 };
 
 std::mutex g_mu;
@@ -104,6 +105,7 @@ int device_state(DeviceState** out, int* dev_out) {
       st.occ_scan_narrow_warp[v4] = std::max(1, occupancy_scan_narrow_warp(v4 ? 4 : 1));
     }
     st.occ_scan_cols_lb = std::max(1, occupancy_scan_cols_lookback());
+    st.occ_rscan_short = std::max(1, occupancy_rscan_short());
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
   }
@@ -649,6 +651,37 @@ int run_reduce_then_scan(const Provider& pv, const float* x, int64_t rows, int64
   return launched(launch_tile_carry_scan(variant, p3, total, s));
 }
 
+// Scans of many short rows (N <= kShortRowMax): chunks of whole rows staged in
+// shared memory, each row scanned by a group of G lanes (G = 1 up to 32
+// elements, else the power of two with about 8 elements per lane, at most 32).
+int run_rscan_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y, cudaStream_t s,
+                    int flags) {
+  int lanes = 1, run = (int)N, stride = (int)(N | 1);
+  if (N > 32) {
+    lanes = 2;
+    while (lanes < 32 && lanes * 8 < N) lanes <<= 1;
+    run = (int)ceil_div(N, lanes) | 1;  // odd: the lanes of a row on distinct banks
+    // The rows of a warp on distinct banks too: stride = run * lanes (mod 32).
+    stride = (int)N;
+    if (lanes < 32)
+      while (stride % 32 != (run * lanes) % 32) ++stride;
+  }
+  // At least 8 rows per chunk where they fit, so every warp has a row.
+  const int rpc = (int)std::max<int64_t>(
+      1, std::min<int64_t>(kShortSmem / stride, std::max<int64_t>(8, kShortChunk / N)));
+  const unsigned long long magic = ((1ull << 32) + (unsigned long long)N - 1) / (unsigned long long)N;
+  // float4 loads and stores need whole float4s per row and aligned pointers.
+  const bool vec4 = N % 4 == 0 && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+  Scratch sc;
+  int rc = acquire(pv, Need{}, &sc, s);
+  if (rc) return rc;
+  const int64_t chunks = ceil_div(rows, rpc);
+  const int64_t grid =
+      std::max<int64_t>(1, std::min<int64_t>(chunks, 4 * (int64_t)pv.st->sm_count * pv.st->occ_rscan_short));
+  ShortRowsParams p{x, y, rows, (int)N, rpc, stride, run, magic, flags};
+  return launched(launch_rscan_short(lanes, vec4 ? 4 : 1, p, grid, s));
+}
+
 // Scans along rows (inner == 1).  `flags`: kScanMirror for a forward scan,
 // kScanExclusive to leave out each element's own term.
 int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
@@ -661,12 +694,14 @@ int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, 
     variant = (int)forced_v;
   // Few rows cannot fill the GPU one block per row: use the look-back scan,
   // which spreads every row's tiles over all SMs.
-  const int64_t strategy = g_opt_scan_strategy.load();
+  int64_t strategy = g_opt_scan_strategy.load();
+  if (strategy == 5 && N > kShortRowMax) strategy = 0;  // rows too long for the short-row form
   const int lb_variant = !vec4 ? kLookbackV1 : (strategy == 3 ? kLookbackV4 : kLookbackL2);
   const int64_t lb_tiles = ceil_div(virtual_row_len(x, N, vec4), lookback_tile(lb_variant));
   const int64_t row_slots = (int64_t)st->sm_count * st->occ_rscan[variant];
   const bool lookback_fits = rows <= kMaxLookbackTiles / std::max<int64_t>(1, lb_tiles);
   if (strategy == 4) return run_reduce_then_scan(pv, x, rows, N, y, s, flags, vec4);
+  if (strategy == 5 || (strategy == 0 && N <= kShortRowMax)) return run_rscan_short(pv, x, rows, N, y, s, flags);
   if (strategy >= 2 || (strategy == 0 && 4 * rows < row_slots && lb_tiles >= 4 && lookback_fits))
     return run_rscan_lookback(pv, x, rows, N, y, s, lb_variant, flags);
   Scratch sc;
@@ -1068,7 +1103,7 @@ int64_t libreduce_launch_count(void) { return g_launches.load(); }
 int libreduce_set_option(int option, int64_t value) {
   switch (option) {
     case LIBREDUCE_OPT_SCAN_STRATEGY:
-      if (value < 0 || value > 4) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < 0 || value > 5) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_strategy = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_AXIS_SPLIT:

@@ -78,6 +78,28 @@ struct RScanRowsParams {
   int flags;
 };
 
+// --- Scans of many short rows (N <= kShortRowMax) -----------------------------
+// A block stages a chunk of rows_per_chunk whole rows in shared memory (row r
+// of the chunk at r*stride floats), scans each row with a group of `lanes`
+// lanes (a power of two, 1..32; the kernel's template parameter), each lane
+// taking a run of run_len consecutive elements, and stores the chunk back.
+// magic = ceil(2^32 / N): the row of flat index e of a chunk is
+// (e*magic) >> 32, exact for every e < kShortSmem and N <= 4096.
+constexpr int kShortRowMax = 2048;    // longest row this form takes
+constexpr int kShortChunk = 6144;     // data floats per chunk (about; at least 8 rows where they fit)
+constexpr int kShortSmem = 12288;     // shared floats per block (48 KB)
+struct ShortRowsParams {
+  const float* x;
+  float* y;
+  int64_t rows;
+  int N;
+  int rows_per_chunk;
+  int stride;
+  int run_len;
+  unsigned long long magic;
+  int flags;  // kScanMirror | kScanExclusive
+};
+
 // --- Reduce-then-scan along rows (three passes) ------------------------------
 // Rows are scanned as reverse scans of the (possibly mirrored) row, in logical
 // tiles k = [k*TILE, (k+1)*TILE).  Pass 1 writes the sum of every logical tile
@@ -258,6 +280,10 @@ cudaError_t launch_scan_narrow_warp(int vec, const ScanColsParams& p, int64_t gr
 int occupancy_scan_narrow_warp(int vec);
 cudaError_t launch_reduce_narrow_warp(int vec, int op, const NarrowParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_tile_carry_scan(int variant, const TileCarryParams& p, int64_t grid, cudaStream_t s);
+// lanes: 1, 2, 4, 8, 16 or 32; vec: 4 for float4 loads and stores (N % 4 == 0,
+// x and y 16-byte aligned), else 1.
+cudaError_t launch_rscan_short(int lanes, int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s);
+int occupancy_rscan_short();
 cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, int64_t grid, cudaStream_t s);
 int occupancy_scan_cols_lookback();
 

@@ -1,0 +1,178 @@
+// lr_rows_short.cu -- cumulative sums of many short rows (inner == 1, N up
+// to kShortRowMax).
+//
+// One block per row would leave most of its threads idle and pay a whole
+// tile's work for a few hundred bytes.  Instead a block stages a chunk of
+// whole rows (about kShortChunk floats, and at least 8 rows where they fit,
+// so every warp has one; contiguous in memory) in shared memory with
+// coalesced loads, scans every row there, and stores the chunk back with
+// coalesced stores.  A row is scanned by a group of G lanes:
+//   G == 1: one thread walks the row in the scan direction;
+//   G > 1:  lane g takes the g-th run of L (odd) consecutive elements from
+//           the scan's start: a sequential prefix over its run in place,
+//           then the sum of the runs before it from a shuffle scan of the
+//           run totals across the group, added to each of its outputs.
+// Every output is a sum over its own terms (an exclusive output leaves its
+// own term out of its run's prefix), so nothing is subtracted, and all orders
+// are fixed: reruns are bit-identical.  Rows are padded in shared memory so
+// that the lanes of a warp hit distinct banks: an odd row stride for G == 1;
+// for G > 1 an odd run length (the lanes of a row are L apart) and a row
+// stride congruent to L*G modulo 32 (the rows of a warp then cover distinct
+// banks too).
+#include "lr_device.cuh"
+#include "lr_internal.h"
+
+namespace lr {
+namespace {
+
+// Coalesced loads of a chunk into shared memory.  VEC 4 loads 16 bytes at a
+// time (N % 4 == 0: a float4 never straddles two rows).
+template <int VEC>
+__device__ __forceinline__ void stage_in(const ShortRowsParams& p, const float* src, float* s, int ne) {
+  const int t = threadIdx.x;
+  if constexpr (VEC == 4) {
+#pragma unroll 4
+    for (int e = 4 * t; e < ne; e += 4 * kThreads) {
+      const float4 f = ld_stream4(src + e);
+      const int r = (int)(((unsigned long long)e * p.magic) >> 32);
+      float* d = s + r * p.stride + (e - r * p.N);
+      d[0] = f.x;
+      d[1] = f.y;
+      d[2] = f.z;
+      d[3] = f.w;
+    }
+  } else {
+#pragma unroll 8
+    for (int e = t; e < ne; e += kThreads) {
+      const int r = (int)(((unsigned long long)e * p.magic) >> 32);
+      s[r * p.stride + (e - r * p.N)] = ld_stream1(src + e);
+    }
+  }
+}
+
+template <int VEC>
+__device__ __forceinline__ void stage_out(const ShortRowsParams& p, const float* s, float* dst, int ne) {
+  const int t = threadIdx.x;
+  if constexpr (VEC == 4) {
+#pragma unroll 4
+    for (int e = 4 * t; e < ne; e += 4 * kThreads) {
+      const int r = (int)(((unsigned long long)e * p.magic) >> 32);
+      const float* d = s + r * p.stride + (e - r * p.N);
+      st_stream4(dst + e, make_float4(d[0], d[1], d[2], d[3]));
+    }
+  } else {
+#pragma unroll 8
+    for (int e = t; e < ne; e += kThreads) {
+      const int r = (int)(((unsigned long long)e * p.magic) >> 32);
+      st_stream1(dst + e, s[r * p.stride + (e - r * p.N)]);
+    }
+  }
+}
+
+// Scan one row in place with G lanes (g = this lane's index in its group).
+// G == 1: the lane walks the row in the scan direction.  G > 1: lane g takes
+// the g-th run of L consecutive elements counted from the scan's start,
+// writes the run's own prefix sums in place, and then adds the sum of the
+// runs before it (an exclusive scan of the run totals across the group).
+// `active` is false for the lanes of a group past the chunk's last row: they
+// still take part in the shuffles, with zeros, and touch nothing.
+template <int G>
+__device__ __forceinline__ void scan_row(float* row, int N, int L, int g, bool active, bool mirror,
+                                         bool exclusive) {
+  if constexpr (G == 1) {
+    if (!active) return;
+    float acc = 0.f;
+    if (mirror) {
+      for (int j = 0; j < N; ++j) {
+        const float before = acc;
+        acc += row[j];
+        row[j] = exclusive ? before : acc;
+      }
+    } else {
+      for (int j = N - 1; j >= 0; --j) {
+        const float before = acc;
+        acc += row[j];
+        row[j] = exclusive ? before : acc;
+      }
+    }
+  } else {
+    // Element i of run g in memory: g*L + i (forward) or N-1 - (g*L + i)
+    // (reverse); positions outside [0, N) belong to no element.
+    const int first = g * L;
+    const int n_run = active ? max(0, min(L, N - first)) : 0;
+    float* base = mirror ? row + first : row + (N - 1 - first);
+    const int dir = mirror ? 1 : -1;
+    float acc = 0.f;
+    for (int i = 0; i < n_run; ++i) {
+      const float before = acc;
+      acc += base[dir * i];
+      base[dir * i] = exclusive ? before : acc;
+    }
+    float incl = acc;  // prefix of the run totals over lanes 0..g
+#pragma unroll
+    for (int d = 1; d < G; d <<= 1) {
+      const float o = __shfl_up_sync(kFullMask, incl, d, G);
+      if (g >= d) incl += o;
+    }
+    float off = __shfl_up_sync(kFullMask, incl, 1, G);  // the runs before this one
+    if (g == 0) off = 0.f;
+    for (int i = 0; i < n_run; ++i) base[dir * i] = off + base[dir * i];
+  }
+}
+
+template <int G, int VEC>
+__global__ void __launch_bounds__(kThreads) k_rscan_short(ShortRowsParams p) {
+  __shared__ __align__(16) float s[kShortSmem];
+  const int t = threadIdx.x;
+  const int gi = t / G;  // this thread's group
+  const int g = t % G;   // its lane in the group
+  constexpr int kGroups = kThreads / G;
+  const bool mirror = (p.flags & kScanMirror) != 0;
+  const bool exclusive = (p.flags & kScanExclusive) != 0;
+  const int64_t chunks = (p.rows + p.rows_per_chunk - 1) / p.rows_per_chunk;
+  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
+    const int64_t r0 = c * p.rows_per_chunk;
+    const int nr = (int)min((int64_t)p.rows_per_chunk, p.rows - r0);
+    const int ne = nr * p.N;
+    stage_in<VEC>(p, p.x + r0 * p.N, s, ne);
+    __syncthreads();
+    // Whole warps stay in the loop (the groups' shuffles), so the bound is
+    // the same for every thread.
+    for (int rb = 0; rb < nr; rb += kGroups) {
+      const int r = rb + gi;
+      scan_row<G>(s + (r < nr ? r : 0) * p.stride, p.N, p.run_len, g, r < nr, mirror, exclusive);
+    }
+    __syncthreads();
+    stage_out<VEC>(p, s, p.y + r0 * p.N, ne);
+    __syncthreads();  // the next chunk overwrites s
+  }
+}
+
+template <int G>
+cudaError_t launch_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
+  if (vec == 4) k_rscan_short<G, 4><<<dim3((unsigned)grid), kThreads, 0, s>>>(p);
+  else k_rscan_short<G, 1><<<dim3((unsigned)grid), kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_rscan_short(int lanes, int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
+  switch (lanes) {
+    case 1: return launch_g<1>(vec, p, grid, s);
+    case 2: return launch_g<2>(vec, p, grid, s);
+    case 4: return launch_g<4>(vec, p, grid, s);
+    case 8: return launch_g<8>(vec, p, grid, s);
+    case 16: return launch_g<16>(vec, p, grid, s);
+    case 32: return launch_g<32>(vec, p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int occupancy_rscan_short() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_rscan_short<32, 4>, kThreads, 0) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace lr

@@ -132,7 +132,7 @@ def test_no_cpu_fallback_without_gpu(lib):
 
 def test_options(lib):
     assert lib.libreduce_set_option(999, 0) == L.ERR_INVALID_ARG
-    assert lib.libreduce_set_option(L.OPT_SCAN_STRATEGY, 5) == L.ERR_INVALID_ARG
+    assert lib.libreduce_set_option(L.OPT_SCAN_STRATEGY, 6) == L.ERR_INVALID_ARG
     assert lib.libreduce_set_option(L.OPT_STALL_TILE, -2) == L.ERR_INVALID_ARG
     for opt, val in ((L.OPT_SCAN_STRATEGY, 0), (L.OPT_AXIS_SPLIT, 0), (L.OPT_SPIN_LIMIT, 0),
                      (L.OPT_STALL_TILE, -1), (L.OPT_CONTIG_VARIANT, -1), (L.OPT_COLS_VARIANT, -1),

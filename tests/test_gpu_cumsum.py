@@ -366,3 +366,40 @@ def test_narrow_few_planes_take_the_lookback(reverse, exclusive):
         assert L.launch_count() - n0 == 3, shape
         assert_close(three.cpu().numpy().reshape(-1), ref.reshape(-1), scale.reshape(-1), f"narrow {shape}")
         L.set_option(L.OPT_SCAN_COLS_VARIANT, -1)
+
+
+# Many short rows (N <= 2048): chunks of whole rows staged in shared memory,
+# each row scanned by a group of 1..32 lanes (OPT_SCAN_STRATEGY 5 forces it;
+# the automatic choice for such rows).
+SHORT_N = [1, 2, 3, 5, 8, 16, 31, 32, 33, 40, 64, 100, 255, 256, 257, 1000, 1024, 2047, 2048]
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("strategy", [0, 5])
+def test_short_rows(strategy, reverse, exclusive):
+    """Every lane-group size and its boundaries; row counts that leave a
+    partial last chunk; float4 (aligned, N % 4 == 0) and scalar staging (x and
+    y at an odd offset)."""
+    L.set_option(L.OPT_SCAN_STRATEGY, strategy)
+    for n in SHORT_N:
+        rows = 3 * max(1, 6144 // n) + 7
+        for offset in (0, 1):
+            got, _ = check((rows, n), 1, reverse, exclusive, offset=offset, out_offset=offset)
+            if exclusive:
+                assert np.all(got[:, n - 1 if reverse else 0] == 0.0), n
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+def test_short_rows_integers_exact(reverse, exclusive):
+    for n in (7, 32, 100, 1024):
+        x = inputs.make((5000, n), "int:0:3", 31)
+        ref, _ = oracle.cumsum(x.numpy(), 5000, n, 1, reverse, exclusive)
+        assert_exact(run(x, 1, reverse, exclusive).reshape(-1), ref.reshape(-1), f"short rows int N={n}")
+
+
+def test_short_rows_deterministic_bitwise():
+    x = on_device(inputs.make((100_000, 100), "normal", 33))
+    first = L.cumsum_f32(x, 1, reverse=True)
+    for _ in range(3):
+        assert bitwise_equal(L.cumsum_f32(x, 1, reverse=True), first)
+    L.check()
