@@ -86,8 +86,8 @@ struct RScanRowsParams {
 // magic = ceil(2^32 / N): the row of flat index e of a chunk is
 // (e*magic) >> 32, exact for every e < kShortSmem and N <= 4096.
 constexpr int kShortRowMax = 2048;    // longest row this form takes
-constexpr int kShortChunk = 6144;     // data floats per chunk (about; at least 8 rows where they fit)
-constexpr int kShortSmem = 12288;     // shared floats per block (48 KB)
+constexpr int kShortChunk = 3072;     // data floats per chunk (about; at least 8 rows where they fit)
+constexpr int kShortSmem = 6144;      // shared floats per block (24 KB)
 struct ShortRowsParams {
   const float* x;
   float* y;

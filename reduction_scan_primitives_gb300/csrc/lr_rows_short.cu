@@ -25,55 +25,69 @@
 namespace lr {
 namespace {
 
+constexpr int kShortThreads = 128;  // 8 blocks per SM at 64 registers
+
 // Coalesced loads of a chunk into shared memory.  VEC 4 loads 16 bytes at a
 // time (N % 4 == 0: a float4 never straddles two rows).
-template <int VEC>
+// SMEM4: 16-byte shared-memory accesses (the row stride is a multiple of 4,
+// as for every group of more than one lane); else four 4-byte ones.
+template <int VEC, bool SMEM4>
 __device__ __forceinline__ void stage_in(const ShortRowsParams& p, const float* src, float* s, int ne) {
   const int t = threadIdx.x;
   if constexpr (VEC == 4) {
 #pragma unroll 4
-    for (int e = 4 * t; e < ne; e += 4 * kThreads) {
+    for (int e = 4 * t; e < ne; e += 4 * kShortThreads) {
       const float4 f = ld_stream4(src + e);
       const int r = (int)(((unsigned long long)e * p.magic) >> 32);
       float* d = s + r * p.stride + (e - r * p.N);
-      d[0] = f.x;
-      d[1] = f.y;
-      d[2] = f.z;
-      d[3] = f.w;
+      if constexpr (SMEM4) {  // one 16-byte store: no bank conflicts
+        *reinterpret_cast<float4*>(d) = f;
+      } else {
+        d[0] = f.x;
+        d[1] = f.y;
+        d[2] = f.z;
+        d[3] = f.w;
+      }
     }
   } else {
 #pragma unroll 8
-    for (int e = t; e < ne; e += kThreads) {
+    for (int e = t; e < ne; e += kShortThreads) {
       const int r = (int)(((unsigned long long)e * p.magic) >> 32);
       s[r * p.stride + (e - r * p.N)] = ld_stream1(src + e);
     }
   }
 }
 
-template <int VEC>
+template <int VEC, bool SMEM4>
 __device__ __forceinline__ void stage_out(const ShortRowsParams& p, const float* s, float* dst, int ne) {
   const int t = threadIdx.x;
   if constexpr (VEC == 4) {
 #pragma unroll 4
-    for (int e = 4 * t; e < ne; e += 4 * kThreads) {
+    for (int e = 4 * t; e < ne; e += 4 * kShortThreads) {
       const int r = (int)(((unsigned long long)e * p.magic) >> 32);
       const float* d = s + r * p.stride + (e - r * p.N);
-      st_stream4(dst + e, make_float4(d[0], d[1], d[2], d[3]));
+      if constexpr (SMEM4) st_stream4(dst + e, *reinterpret_cast<const float4*>(d));
+      else st_stream4(dst + e, make_float4(d[0], d[1], d[2], d[3]));
     }
   } else {
 #pragma unroll 8
-    for (int e = t; e < ne; e += kThreads) {
+    for (int e = t; e < ne; e += kShortThreads) {
       const int r = (int)(((unsigned long long)e * p.magic) >> 32);
       st_stream1(dst + e, s[r * p.stride + (e - r * p.N)]);
     }
   }
 }
 
+constexpr int kRegRun = 16;  // elements a lane holds in registers at a time
+
 // Scan one row in place with G lanes (g = this lane's index in its group).
 // G == 1: the lane walks the row in the scan direction.  G > 1: lane g takes
-// the g-th run of L consecutive elements counted from the scan's start,
-// writes the run's own prefix sums in place, and then adds the sum of the
-// runs before it (an exclusive scan of the run totals across the group).
+// the g-th run of L consecutive elements counted from the scan's start; the
+// sum of the runs before it (an exclusive scan of the run totals across the
+// group) is added to each of its prefix sums.  A run of at most kRegRun
+// elements stays in registers between its load and its store; a longer one
+// is scanned in place first and offset in a second pass.  Both compute
+// off + (prefix within the run) with the same additions.
 // `active` is false for the lanes of a group past the chunk's last row: they
 // still take part in the shuffles, with zeros, and touch nothing.
 template <int G>
@@ -82,18 +96,12 @@ __device__ __forceinline__ void scan_row(float* row, int N, int L, int g, bool a
   if constexpr (G == 1) {
     if (!active) return;
     float acc = 0.f;
-    if (mirror) {
-      for (int j = 0; j < N; ++j) {
-        const float before = acc;
-        acc += row[j];
-        row[j] = exclusive ? before : acc;
-      }
-    } else {
-      for (int j = N - 1; j >= 0; --j) {
-        const float before = acc;
-        acc += row[j];
-        row[j] = exclusive ? before : acc;
-      }
+    const int dir = mirror ? 1 : -1;
+    float* p0 = mirror ? row : row + (N - 1);
+    for (int i = 0; i < N; ++i) {
+      const float before = acc;
+      acc += p0[dir * i];
+      p0[dir * i] = exclusive ? before : acc;
     }
   } else {
     // Element i of run g in memory: g*L + i (forward) or N-1 - (g*L + i)
@@ -102,31 +110,54 @@ __device__ __forceinline__ void scan_row(float* row, int N, int L, int g, bool a
     const int n_run = active ? max(0, min(L, N - first)) : 0;
     float* base = mirror ? row + first : row + (N - 1 - first);
     const int dir = mirror ? 1 : -1;
-    float acc = 0.f;
-    for (int i = 0; i < n_run; ++i) {
-      const float before = acc;
-      acc += base[dir * i];
-      base[dir * i] = exclusive ? before : acc;
-    }
-    float incl = acc;  // prefix of the run totals over lanes 0..g
+    const auto offset_of = [&](float total) {
+      float incl = total;  // prefix of the run totals over lanes 0..g
 #pragma unroll
-    for (int d = 1; d < G; d <<= 1) {
-      const float o = __shfl_up_sync(kFullMask, incl, d, G);
-      if (g >= d) incl += o;
+      for (int d = 1; d < G; d <<= 1) {
+        const float o = __shfl_up_sync(kFullMask, incl, d, G);
+        if (g >= d) incl += o;
+      }
+      const float off = __shfl_up_sync(kFullMask, incl, 1, G);  // the runs before this one
+      return g == 0 ? 0.f : off;
+    };
+    if (L <= kRegRun) {  // the same for every lane of the warp
+      float v[kRegRun];
+#pragma unroll
+      for (int i = 0; i < kRegRun; ++i) v[i] = i < n_run ? base[dir * i] : 0.f;
+      float total = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRegRun; ++i) total += v[i];
+      const float off = offset_of(total);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRegRun; ++i) {
+        const float before = acc;
+        acc += v[i];
+        v[i] = off + (exclusive ? before : acc);
+      }
+#pragma unroll
+      for (int i = 0; i < kRegRun; ++i)
+        if (i < n_run) base[dir * i] = v[i];
+    } else {
+      float acc = 0.f;
+      for (int i = 0; i < n_run; ++i) {
+        const float before = acc;
+        acc += base[dir * i];
+        base[dir * i] = exclusive ? before : acc;
+      }
+      const float off = offset_of(acc);
+      for (int i = 0; i < n_run; ++i) base[dir * i] = off + base[dir * i];
     }
-    float off = __shfl_up_sync(kFullMask, incl, 1, G);  // the runs before this one
-    if (g == 0) off = 0.f;
-    for (int i = 0; i < n_run; ++i) base[dir * i] = off + base[dir * i];
   }
 }
 
 template <int G, int VEC>
-__global__ void __launch_bounds__(kThreads) k_rscan_short(ShortRowsParams p) {
+__global__ void __launch_bounds__(kShortThreads) k_rscan_short(ShortRowsParams p) {
   __shared__ __align__(16) float s[kShortSmem];
   const int t = threadIdx.x;
   const int gi = t / G;  // this thread's group
   const int g = t % G;   // its lane in the group
-  constexpr int kGroups = kThreads / G;
+  constexpr int kGroups = kShortThreads / G;
   const bool mirror = (p.flags & kScanMirror) != 0;
   const bool exclusive = (p.flags & kScanExclusive) != 0;
   const int64_t chunks = (p.rows + p.rows_per_chunk - 1) / p.rows_per_chunk;
@@ -134,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) k_rscan_short(ShortRowsParams p) {
     const int64_t r0 = c * p.rows_per_chunk;
     const int nr = (int)min((int64_t)p.rows_per_chunk, p.rows - r0);
     const int ne = nr * p.N;
-    stage_in<VEC>(p, p.x + r0 * p.N, s, ne);
+    stage_in<VEC, (G > 1)>(p, p.x + r0 * p.N, s, ne);
     __syncthreads();
     // Whole warps stay in the loop (the groups' shuffles), so the bound is
     // the same for every thread.
@@ -143,15 +174,15 @@ __global__ void __launch_bounds__(kThreads) k_rscan_short(ShortRowsParams p) {
       scan_row<G>(s + (r < nr ? r : 0) * p.stride, p.N, p.run_len, g, r < nr, mirror, exclusive);
     }
     __syncthreads();
-    stage_out<VEC>(p, s, p.y + r0 * p.N, ne);
+    stage_out<VEC, (G > 1)>(p, s, p.y + r0 * p.N, ne);
     __syncthreads();  // the next chunk overwrites s
   }
 }
 
 template <int G>
 cudaError_t launch_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
-  if (vec == 4) k_rscan_short<G, 4><<<dim3((unsigned)grid), kThreads, 0, s>>>(p);
-  else k_rscan_short<G, 1><<<dim3((unsigned)grid), kThreads, 0, s>>>(p);
+  if (vec == 4) k_rscan_short<G, 4><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+  else k_rscan_short<G, 1><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -171,7 +202,7 @@ cudaError_t launch_rscan_short(int lanes, int vec, const ShortRowsParams& p, int
 
 int occupancy_rscan_short() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_rscan_short<32, 4>, kThreads, 0) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_rscan_short<32, 4>, kShortThreads, 0) != cudaSuccess) return 0;
   return n;
 }
 
