@@ -317,6 +317,11 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
 #define LIBREDUCE_OPT_WAVES 8
 #define LIBREDUCE_OPT_LOOKBACK_LAG 9
 #define LIBREDUCE_OPT_SCAN_COLS_VARIANT 10
+/* LIBREDUCE_OPT_ROWS_FORM  reductions along rows of at most 2048 elements (inner == 1):
+ *                          0 automatic (2 up to 128 elements, else 1), 1 one warp per
+ *                          row, 2 chunks of whole rows staged in shared memory, a
+ *                          group of 1 to 32 lanes per row */
+#define LIBREDUCE_OPT_ROWS_FORM 11
 LIBREDUCE_API int libreduce_set_option(int option, int64_t value);
 
 #ifdef __cplusplus

@@ -66,6 +66,7 @@ std::atomic<int64_t> g_opt_contig_variant{-1};
 std::atomic<int64_t> g_opt_cols_variant{-1};
 std::atomic<int64_t> g_opt_rscan_variant{-1};
 std::atomic<int64_t> g_opt_scan_cols_variant{-1};
+std::atomic<int64_t> g_opt_rows_form{0};
 std::atomic<int64_t> g_opt_waves{0};
 std::atomic<int64_t> g_opt_lookback_lag{0};
 thread_local int t_last_cuda_error = 0;
@@ -231,6 +232,9 @@ int launched(cudaError_t e) {
 constexpr int64_t kMinChunk = 8192;         // floats per block, lower bound
 constexpr int64_t kTargetChunk = 65536;     // floats per block of a long 1D sum (256 KiB)
 constexpr int64_t kRowsWarpMaxLen = 2048;   // rows up to this length: one warp per row
+constexpr int64_t kShortReduceMax = 128;    // rows up to this length: staged chunks (automatic choice;
+                                            // measured 0.75 against 0.21 at N = 32, 0.54 against
+                                            // 0.31 at 100, and behind one warp per row from 256)
 
 int contig_variant() {
   const int64_t v = g_opt_contig_variant.load();
@@ -357,6 +361,9 @@ int run_contig(const Provider& pv, const float* x, int64_t segments, int64_t seg
   ContigParams p{x, seg_len, chunk_len, (int32_t)chunks, out, sc.partials, sc.tickets, epi};
   return launched(launch_reduce_contig(variant, op, p, grid, s));
 }
+
+int run_rows_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* out, int op, int epi,
+                   cudaStream_t s);
 
 int run_rows_warp(const Provider& pv, const float* x, int64_t rows, int64_t len, float* out, int op,
                   int epi, cudaStream_t s) {
@@ -556,8 +563,12 @@ int reduce_impl(const float* x, int64_t outer, int64_t reduce, int64_t inner, fl
   if ((rc = check_buffer(x, (size_t)total * sizeof(float), dev))) return rc;
   if (inner == 1) {
     if (outer == 1) return finish_status(run_contig(pv, x, 1, reduce, out, plan.op, plan.epi, s));
-    if (reduce <= kRowsWarpMaxLen && g_opt_axis_split.load() <= 0)
+    if (reduce <= kRowsWarpMaxLen && g_opt_axis_split.load() <= 0) {
+      const int64_t form = g_opt_rows_form.load();
+      if (form == 2 || (form == 0 && reduce <= kShortReduceMax))
+        return finish_status(run_rows_short(pv, x, outer, reduce, out, plan.op, plan.epi, s));
       return finish_status(run_rows_warp(pv, x, outer, reduce, out, plan.op, plan.epi, s));
+    }
     return finish_status(run_contig(pv, x, outer, reduce, out, plan.op, plan.epi, s));
   }
   return finish_status(run_cols(pv, x, outer, reduce, inner, out, plan.op, plan.epi, s));
@@ -654,32 +665,55 @@ int run_reduce_then_scan(const Provider& pv, const float* x, int64_t rows, int64
 // Scans of many short rows (N <= kShortRowMax): chunks of whole rows staged in
 // shared memory, each row scanned by a group of G lanes (G = 1 up to 32
 // elements, else the power of two with about 8 elements per lane, at most 32).
-int run_rscan_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y, cudaStream_t s,
-                    int flags) {
-  int lanes = 1, run = (int)N, stride = (int)(N | 1);
+struct ShortPlan {
+  int lanes, run, stride, rows_per_chunk;
+  unsigned long long magic;
+};
+ShortPlan short_plan(int64_t N) {
+  ShortPlan q{1, (int)N, (int)(N | 1), 1, 0};
   if (N > 32) {
-    lanes = 2;
-    while (lanes < 32 && lanes * 8 < N) lanes <<= 1;
-    run = (int)ceil_div(N, lanes) | 1;  // odd: the lanes of a row on distinct banks
+    q.lanes = 2;
+    while (q.lanes < 32 && q.lanes * 8 < N) q.lanes <<= 1;
+    q.run = (int)ceil_div(N, q.lanes) | 1;  // odd: the lanes of a row on distinct banks
     // The rows of a warp on distinct banks too: stride = run * lanes (mod 32).
-    stride = (int)N;
-    if (lanes < 32)
-      while (stride % 32 != (run * lanes) % 32) ++stride;
+    q.stride = (int)N;
+    if (q.lanes < 32)
+      while (q.stride % 32 != (q.run * q.lanes) % 32) ++q.stride;
   }
   // At least 8 rows per chunk where they fit, so every warp has a row.
-  const int rpc = (int)std::max<int64_t>(
-      1, std::min<int64_t>(kShortSmem / stride, std::max<int64_t>(8, kShortChunk / N)));
-  const unsigned long long magic = ((1ull << 32) + (unsigned long long)N - 1) / (unsigned long long)N;
+  q.rows_per_chunk = (int)std::max<int64_t>(
+      1, std::min<int64_t>(kShortSmem / q.stride, std::max<int64_t>(8, kShortChunk / N)));
+  q.magic = ((1ull << 32) + (unsigned long long)N - 1) / (unsigned long long)N;
+  return q;
+}
+int64_t short_grid(const DeviceState* st, int64_t rows, const ShortPlan& q) {
+  return std::max<int64_t>(1, std::min<int64_t>(ceil_div(rows, q.rows_per_chunk),
+                                                4 * (int64_t)st->sm_count * st->occ_rscan_short));
+}
+
+int run_rscan_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y, cudaStream_t s,
+                    int flags) {
+  const ShortPlan q = short_plan(N);
   // float4 loads and stores need whole float4s per row and aligned pointers.
   const bool vec4 = N % 4 == 0 && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
   Scratch sc;
   int rc = acquire(pv, Need{}, &sc, s);
   if (rc) return rc;
-  const int64_t chunks = ceil_div(rows, rpc);
-  const int64_t grid =
-      std::max<int64_t>(1, std::min<int64_t>(chunks, 4 * (int64_t)pv.st->sm_count * pv.st->occ_rscan_short));
-  ShortRowsParams p{x, y, rows, (int)N, rpc, stride, run, magic, flags};
-  return launched(launch_rscan_short(lanes, vec4 ? 4 : 1, p, grid, s));
+  ShortRowsParams p{x, y, rows, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, flags};
+  return launched(launch_rscan_short(q.lanes, vec4 ? 4 : 1, p, short_grid(pv.st, rows, q), s));
+}
+
+// Reductions of many short rows (inner == 1, reduce <= kShortRowMax) with the
+// same chunks: one float per row.
+int run_rows_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* out, int op, int epi,
+                   cudaStream_t s) {
+  const ShortPlan q = short_plan(N);
+  const bool vec4 = N % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  Scratch sc;
+  int rc = acquire(pv, Need{}, &sc, s);
+  if (rc) return rc;
+  ShortRowsParams p{x, out, rows, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, epi};
+  return launched(launch_reduce_short(op, q.lanes, vec4 ? 4 : 1, p, short_grid(pv.st, rows, q), s));
 }
 
 // Scans along rows (inner == 1).  `flags`: kScanMirror for a forward scan,
@@ -1133,6 +1167,10 @@ int libreduce_set_option(int option, int64_t value) {
     case LIBREDUCE_OPT_SCAN_COLS_VARIANT:
       if (value < -1 || value > kScanColsLookback) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_cols_variant = value;
+      return LIBREDUCE_OK;
+    case LIBREDUCE_OPT_ROWS_FORM:
+      if (value < 0 || value > 2) return LIBREDUCE_ERR_INVALID_ARG;
+      g_opt_rows_form = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_LOOKBACK_LAG:
       if (value < 0 || value > (1 << 20)) return LIBREDUCE_ERR_INVALID_ARG;

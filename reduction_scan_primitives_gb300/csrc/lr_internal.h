@@ -283,6 +283,10 @@ cudaError_t launch_tile_carry_scan(int variant, const TileCarryParams& p, int64_
 // lanes: 1, 2, 4, 8, 16 or 32; vec: 4 for float4 loads and stores (N % 4 == 0,
 // x and y 16-byte aligned), else 1.
 cudaError_t launch_rscan_short(int lanes, int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s);
+// The same chunks for reductions of short rows: p.y receives one float per
+// row and p.flags holds the epilogue (kEpiNone, kEpiMean, kEpiSqrt).  lanes:
+// 1, 8, 16 or 32.
+cudaError_t launch_reduce_short(int op, int lanes, int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s);
 int occupancy_rscan_short();
 cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, int64_t grid, cudaStream_t s);
 int occupancy_scan_cols_lookback();

@@ -179,6 +179,66 @@ __global__ void __launch_bounds__(kShortThreads) k_rscan_short(ShortRowsParams p
   }
 }
 
+// Reductions of many short rows: the same chunks and lane groups.  Lane g of
+// a row's group combines its run (elements g*L .. g*L+L-1 in order), the
+// group's lanes are then combined by a fixed shuffle tree, and lane 0 writes
+// the row's result (with the epilogue: mean or square root).  p.y is the
+// output (one float per row) and p.flags the epilogue.
+template <int G, int VEC, typename Op>
+__global__ void __launch_bounds__(kShortThreads) k_reduce_short(ShortRowsParams p) {
+  __shared__ __align__(16) float s[kShortSmem];
+  const int t = threadIdx.x;
+  const int gi = t / G;
+  const int g = t % G;
+  constexpr int kGroups = kShortThreads / G;
+  const int64_t chunks = (p.rows + p.rows_per_chunk - 1) / p.rows_per_chunk;
+  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
+    const int64_t r0 = c * p.rows_per_chunk;
+    const int nr = (int)min((int64_t)p.rows_per_chunk, p.rows - r0);
+    stage_in<VEC, (G > 1)>(p, p.x + r0 * p.N, s, nr * p.N);
+    __syncthreads();
+    for (int rb = 0; rb < nr; rb += kGroups) {
+      const int r = rb + gi;
+      const bool active = r < nr;
+      const float* row = s + (active ? r : 0) * p.stride;
+      const int first = G == 1 ? 0 : g * p.run_len;
+      const int n_run = active ? max(0, min(G == 1 ? p.N : p.run_len, p.N - first)) : 0;
+      float v = Op::identity();
+      for (int i0 = 0; i0 < n_run; i0 += kRegRun) {
+        float a[kRegRun];
+#pragma unroll
+        for (int i = 0; i < kRegRun; ++i) a[i] = i0 + i < n_run ? Op::prep(row[first + i0 + i]) : Op::identity();
+#pragma unroll
+        for (int i = 0; i < kRegRun; ++i) v = Op::combine(v, a[i]);
+      }
+      if constexpr (G > 1) {
+#pragma unroll
+        for (int d = G / 2; d > 0; d >>= 1) v = Op::combine(v, __shfl_down_sync(kFullMask, v, d, G));
+      }
+      if (active && g == 0) p.y[r0 + r] = finish(v, p.flags, p.N);
+    }
+    __syncthreads();  // the next chunk overwrites s
+  }
+}
+
+template <int G, typename Op>
+cudaError_t launch_reduce_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
+  if (vec == 4) k_reduce_short<G, 4, Op><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+  else k_reduce_short<G, 1, Op><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename Op>
+cudaError_t launch_reduce_op(int lanes, int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
+  switch (lanes) {
+    case 1: return launch_reduce_g<1, Op>(vec, p, grid, s);
+    case 8: return launch_reduce_g<8, Op>(vec, p, grid, s);
+    case 16: return launch_reduce_g<16, Op>(vec, p, grid, s);
+    case 32: return launch_reduce_g<32, Op>(vec, p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <int G>
 cudaError_t launch_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
   if (vec == 4) k_rscan_short<G, 4><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
@@ -196,6 +256,16 @@ cudaError_t launch_rscan_short(int lanes, int vec, const ShortRowsParams& p, int
     case 8: return launch_g<8>(vec, p, grid, s);
     case 16: return launch_g<16>(vec, p, grid, s);
     case 32: return launch_g<32>(vec, p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_reduce_short(int op, int lanes, int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
+  switch (op) {
+    case kOpSum: return launch_reduce_op<OpSum>(lanes, vec, p, grid, s);
+    case kOpSumSq: return launch_reduce_op<OpSumSq>(lanes, vec, p, grid, s);
+    case kOpMax: return launch_reduce_op<OpMax>(lanes, vec, p, grid, s);
+    case kOpMin: return launch_reduce_op<OpMin>(lanes, vec, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

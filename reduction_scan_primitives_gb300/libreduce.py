@@ -40,6 +40,7 @@ OPT_RSCAN_VARIANT = 7
 OPT_WAVES = 8
 OPT_LOOKBACK_LAG = 9
 OPT_SCAN_COLS_VARIANT = 10
+OPT_ROWS_FORM = 11
 
 LIB_PATH = _build.LIB
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",

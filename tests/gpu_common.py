@@ -8,7 +8,7 @@ from reduction_scan_primitives_gb300 import libreduce as L
 DEFAULT_OPTIONS = ((L.OPT_SCAN_STRATEGY, 0), (L.OPT_AXIS_SPLIT, 0), (L.OPT_SPIN_LIMIT, 0),
                    (L.OPT_STALL_TILE, -1), (L.OPT_CONTIG_VARIANT, -1), (L.OPT_COLS_VARIANT, -1),
                    (L.OPT_RSCAN_VARIANT, -1), (L.OPT_WAVES, 0), (L.OPT_LOOKBACK_LAG, 0),
-                   (L.OPT_SCAN_COLS_VARIANT, -1))
+                   (L.OPT_SCAN_COLS_VARIANT, -1), (L.OPT_ROWS_FORM, 0))
 
 
 def reset_options():

@@ -143,6 +143,10 @@ def test_options(lib):
     assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 6) == L.ERR_INVALID_ARG
     assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, -1) == L.OK
     assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 8) == L.ERR_INVALID_ARG
+    for v in (0, 1, 2):
+        assert lib.libreduce_set_option(L.OPT_ROWS_FORM, v) == L.OK
+    assert lib.libreduce_set_option(L.OPT_ROWS_FORM, 3) == L.ERR_INVALID_ARG
+    assert lib.libreduce_set_option(L.OPT_ROWS_FORM, 0) == L.OK
 
 
 def test_strerror(lib):

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from gpu_common import libreduce_defaults, on_device  # noqa: F401
-from parity import assert_op_close, bitwise_equal, to_np
+from parity import assert_close, assert_op_close, bitwise_equal, to_np
 from reduction_scan_primitives_gb300 import inputs
 from reduction_scan_primitives_gb300 import libreduce as L
 
@@ -104,3 +104,44 @@ def test_narrow_rows_ops(op, shape, split):
     L.set_option(L.OPT_COLS_VARIANT, 7)
     check_axis(shape, 1, op)
     check_axis((3000, 50, shape[2]), 1, op, offset=1)
+
+
+# Reductions along rows of at most 2048 elements (inner == 1): one warp per
+# row (OPT_ROWS_FORM 1) or chunks of whole rows staged in shared memory with a
+# group of 1-32 lanes per row (2, the automatic choice).
+SHORT_N = [1, 2, 3, 7, 8, 31, 32, 33, 64, 100, 255, 256, 257, 1000, 1024, 2047, 2048]
+
+
+@pytest.mark.parametrize("op", OPS + ["sum"])
+@pytest.mark.parametrize("form", [1, 2])
+def test_short_rows_both_forms(op, form):
+    L.set_option(L.OPT_ROWS_FORM, form)
+    for n in SHORT_N:
+        rows = 3 * max(1, 3072 // n) + 5
+        for offset in (0, 1):
+            x = inputs.make((rows, n), "normal", 50 + n % 11)
+            got = L.reduce_axis_op_f32(on_device(x, offset), 1, op)
+            what = f"{op} [{rows},{n}] form={form} off={offset}"
+            if op == "sum":
+                ref, scale = oracle.axis_sum(x.numpy(), rows, n, 1)
+                assert_close(to_np(got).reshape(-1), ref.reshape(-1), scale.reshape(-1), what)
+            else:
+                ref, scale = oracle.reduce_op(x.numpy(), rows, n, 1, op)
+                assert_op_close(got, ref, scale, op, n, what)
+
+
+def test_short_rows_forms_exact_and_deterministic():
+    """Small integers sum exactly in both forms (so they agree bit for bit),
+    and max / min pick the same elements; reruns are bit-identical."""
+    for n in (5, 32, 100, 1000):
+        x = on_device(inputs.make((20_000, n), "int:-8:8", 61))
+        outs = {}
+        for form in (1, 2):
+            L.set_option(L.OPT_ROWS_FORM, form)
+            for op in ("sum", "max", "min"):
+                a = L.reduce_axis_op_f32(x, 1, op)
+                assert bitwise_equal(L.reduce_axis_op_f32(x, 1, op), a)
+                outs[(form, op)] = a
+        for op in ("sum", "max", "min"):
+            assert bitwise_equal(outs[(1, op)], outs[(2, op)]), (n, op)
+    L.check()
