@@ -669,7 +669,9 @@ struct ShortPlan {
   int lanes, run, stride, rows_per_chunk;
   unsigned long long magic;
 };
-ShortPlan short_plan(int64_t N) {
+// `target`: the data floats a chunk aims at (kShortChunk for scans, whose
+// chunks also go back out; kShortSmem for reductions, which only read).
+ShortPlan short_plan(int64_t N, int64_t target) {
   ShortPlan q{1, (int)N, (int)(N | 1), 1, 0};
   if (N > 32) {
     q.lanes = 2;
@@ -682,7 +684,7 @@ ShortPlan short_plan(int64_t N) {
   }
   // At least 8 rows per chunk where they fit, so every warp has a row.
   q.rows_per_chunk = (int)std::max<int64_t>(
-      1, std::min<int64_t>(kShortSmem / q.stride, std::max<int64_t>(8, kShortChunk / N)));
+      1, std::min<int64_t>(kShortSmem / q.stride, std::max<int64_t>(8, target / N)));
   q.magic = ((1ull << 32) + (unsigned long long)N - 1) / (unsigned long long)N;
   return q;
 }
@@ -693,7 +695,7 @@ int64_t short_grid(const DeviceState* st, int64_t rows, const ShortPlan& q) {
 
 int run_rscan_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y, cudaStream_t s,
                     int flags) {
-  const ShortPlan q = short_plan(N);
+  const ShortPlan q = short_plan(N, kShortChunk);
   // float4 loads and stores need whole float4s per row and aligned pointers.
   const bool vec4 = N % 4 == 0 && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
   Scratch sc;
@@ -707,7 +709,7 @@ int run_rscan_short(const Provider& pv, const float* x, int64_t rows, int64_t N,
 // same chunks: one float per row.
 int run_rows_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* out, int op, int epi,
                    cudaStream_t s) {
-  const ShortPlan q = short_plan(N);
+  const ShortPlan q = short_plan(N, kShortSmem);
   const bool vec4 = N % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   Scratch sc;
   int rc = acquire(pv, Need{}, &sc, s);
