@@ -51,7 +51,7 @@ NEXT_WORKLOADS = ["cumsum_fwd_32768x32768", "cumsum_fwd_excl_1x1e9", "cumsum_128
                   "cumsum_64x16384x1024_d1", "cumsum_2x8192x4096_d1", "cumsum_1024x8192x64_d1",
                   "sum_16x1000000x12_d1", "rcumsum_1x1e9_rts",
                   "max_1e9", "norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0",
-                  "rcumsum_1x1e9_ws", "axis_65536x4096_d0_ws"]
+                  "rcumsum_1x1e9_ws", "axis_65536x4096_d0_ws", "rcumsum_2000000x100", "sum_4000000x32_d1"]
 # Small cases of each kernel for ncu captures: larger than L2, a few GB at most.
 PROFILE_CASES = {
     "sum_2e8": dict(op="sum", shape=(200_000_000,), dist="uniform01", seed=42),
@@ -68,6 +68,8 @@ PROFILE_CASES = {
                                   exclusive=False, dist="uniform01", seed=13),
     "sum_16x1000000x12_d1": dict(inputs.WORKLOADS["sum_16x1000000x12_d1"]),
     "cumsum_2x8192x4096_d1": dict(inputs.WORKLOADS["cumsum_2x8192x4096_d1"]),
+    "rcumsum_2000000x100": dict(inputs.WORKLOADS["rcumsum_2000000x100"]),
+    "sum_4000000x32_d1": dict(inputs.WORKLOADS["sum_4000000x32_d1"]),
 }
 FALLBACK_HBM_GBS = 6800.0
 # Context only (another machine): the page's T4 figures for the 1D sum.

@@ -101,6 +101,12 @@ WORKLOADS = {
                                     exclusive=False, dist="uniform01", seed=3),
     "cumsum_2x8192x4096_d1": dict(op="cumsum", shape=(2, 8192, 4096), dim=1, reverse=False,
                                   exclusive=True, dist="uniform01", seed=3),
+    # Many short rows: the reverse scan of 100-element rows and the sum of
+    # 32-element rows (chunks of whole rows staged in shared memory).
+    "rcumsum_2000000x100": dict(op="cumsum", shape=(2_000_000, 100), dim=1, reverse=True,
+                                exclusive=False, dist="uniform01", seed=3),
+    "sum_4000000x32_d1": dict(op="reduce", rop="sum", shape=(4_000_000, 32), dim=1,
+                              dist="uniform_pm1", seed=11),
     # The same calls with caller-provided scratch.
     "rcumsum_1x1e9_ws": dict(op="cumsum", shape=(1, 1_000_000_000), dim=1, reverse=True,
                              exclusive=False, dist="uniform01", seed=3, ws=True),

@@ -190,3 +190,23 @@ def test_odd_rows_at_offset(reverse):
     xs = x.index_select(0, rows).cpu().numpy()
     ref, scale = oracle.cumsum(xs, len(rows), 32767, 1, reverse, False)
     assert_close(y.index_select(0, rows).cpu().numpy(), ref, scale, f"odd rows reverse={reverse}")
+
+
+def test_short_rows_full_size():
+    """The two short-row workloads of the bench, in its launch configuration:
+    sampled rows of the reverse scan of [2e6, 100] and of the row sums of
+    [4e6, 32] against the oracle; the scan's last column is exactly x."""
+    w, x = workload("rcumsum_2000000x100")
+    rows, n = w["shape"]
+    y = L.cumsum_f32(x, 1, reverse=True)
+    L.check()
+    assert torch.equal(y[:, -1], x[:, -1])
+    pick_rows = torch.as_tensor(pick(rows, 60, 8, edges=(0, 1, 2, 63, 64)), device=DEV)
+    ref, scale = oracle.cumsum(x.index_select(0, pick_rows).cpu().numpy(), len(pick_rows), n, 1, True, False)
+    assert_close(y.index_select(0, pick_rows).cpu().numpy(), ref, scale, "short rows scan")
+    w, x = workload("sum_4000000x32_d1")
+    rows, n = w["shape"]
+    s = L.reduce_axis_f32(x, 1)
+    L.check()
+    ref, scale = oracle.axis_sum(x.cpu().numpy(), rows, n, 1)
+    assert_close(s.cpu().numpy(), ref[:, 0], scale[:, 0], "short rows sum")
