@@ -235,6 +235,9 @@ constexpr int64_t kRowsWarpMaxLen = 2048;   // rows up to this length: one warp 
 constexpr int64_t kShortReduceMax = 128;    // rows up to this length: staged chunks (automatic choice;
                                             // measured 0.75 against 0.21 at N = 32, 0.54 against
                                             // 0.31 at 100, and behind one warp per row from 256)
+// Short-row plans (short_plan): rows up to these lengths take one lane each.
+constexpr int64_t kShortScanSolo = 64;
+constexpr int64_t kShortReduceSolo = 64;
 
 int contig_variant() {
   const int64_t v = g_opt_contig_variant.load();
@@ -662,29 +665,64 @@ int run_reduce_then_scan(const Provider& pv, const float* x, int64_t rows, int64
   return launched(launch_tile_carry_scan(variant, p3, total, s));
 }
 
-// Scans of many short rows (N <= kShortRowMax): chunks of whole rows staged in
-// shared memory, each row scanned by a group of G lanes (G = 1 up to 32
-// elements, else the power of two with about 8 elements per lane, at most 32).
+// Scans and reductions of many short rows (N <= kShortRowMax): chunks of whole
+// rows staged in shared memory, each row handled by a group of G lanes.
 struct ShortPlan {
   int lanes, run, stride, rows_per_chunk;
   unsigned long long magic;
 };
-// `target`: the data floats a chunk aims at (kShortChunk for scans, whose
-// chunks also go back out; kShortSmem for reductions, which only read).
-ShortPlan short_plan(int64_t N, int64_t target) {
+// Rows of at most `solo` elements: one lane per row, chunks of about
+// `target` floats with at least 8 rows where they fit.  Longer rows: groups of
+// G lanes (a power of two, 4 to 32) with lane runs of L = ceil(N/G) | 1, and
+// chunks that the prefetch covers (at most kShortChunk floats; a longer chunk
+// loads its remainder at staging) and that the block's 128/G groups cover in
+// one pass at least 3/4 full:
+//   rows = kShortChunk / N, at least 4 (one pass of 32-lane groups) and at
+//          most 32 (one pass of 4-lane groups), within the shared memory;
+//   G    = the largest with rows <= 128/G; if that pass would be less than
+//          3/4 full, G doubles and rows = 128/G.
+// Measured on scans of 2e8 floats (fraction of copy bandwidth, [rows, N]):
+// runs of 25-33 elements in one pass beat runs of 7-17 over two partly idle
+// passes ([., 100] 0.96 at G = 4 against 0.69 at G = 16; [., 256] 0.96
+// against 0.91), a full pass beats a 3/5 one ([., 160] 0.97 at G = 8 with 16
+// rows against 0.88 at G = 4 with 19), chunks of up to 3072 floats beat
+// larger ones with a remainder ([., 128] 0.96 against 0.93), and one lane per
+// row stays best up to 64 elements (0.97-0.98).
+// Where a chunk holds at least the rows that span a whole number of 128-byte
+// lines, it is rounded down to a multiple of them, so every chunk starts on a
+// line boundary and no line is shared by two blocks.
+ShortPlan short_plan(int64_t N, int64_t target, int64_t solo) {
   ShortPlan q{1, (int)N, (int)(N | 1), 1, 0};
-  if (N > 32) {
-    q.lanes = 2;
-    while (q.lanes < 32 && q.lanes * 8 < N) q.lanes <<= 1;
+  int64_t a = N, b = 32;  // rows per whole number of lines: 32 / gcd(N, 32)
+  while (b) {
+    const int64_t r = a % b;
+    a = b;
+    b = r;
+  }
+  const int64_t line_rows = 32 / a;
+  const auto line_round = [&](int64_t rows) { return rows >= line_rows ? rows - rows % line_rows : rows; };
+  if (N <= solo) {
+    q.rows_per_chunk = (int)line_round(
+        std::max<int64_t>(1, std::min<int64_t>(kShortSmem / q.stride, std::max<int64_t>(8, target / N))));
+  } else {
+    const int64_t fit = kShortSmem / (N + 31);  // rows that fit at the widest stride a group needs
+    int64_t rows = std::min<int64_t>(fit, std::min<int64_t>(32, std::max<int64_t>(4, kShortChunk / N)));
+    rows = line_round(std::max<int64_t>(1, rows));
+    q.lanes = 4;
+    while (q.lanes < 32 && 2 * q.lanes * rows <= kShortThreads) q.lanes <<= 1;
+    if (q.lanes < 32 && 4 * rows * q.lanes < 3 * kShortThreads) {
+      q.lanes <<= 1;
+      rows = line_round(kShortThreads / q.lanes);
+    }
     q.run = (int)ceil_div(N, q.lanes) | 1;  // odd: the lanes of a row on distinct banks
     // The rows of a warp on distinct banks too: stride = run * lanes (mod 32).
     q.stride = (int)N;
     if (q.lanes < 32)
       while (q.stride % 32 != (q.run * q.lanes) % 32) ++q.stride;
+    // 32-lane groups keep stride N: up to a full pass of them where it fits.
+    if (q.lanes == 32) rows = std::max<int64_t>(rows, line_round(std::min<int64_t>(4, kShortSmem / q.stride)));
+    q.rows_per_chunk = (int)rows;
   }
-  // At least 8 rows per chunk where they fit, so every warp has a row.
-  q.rows_per_chunk = (int)std::max<int64_t>(
-      1, std::min<int64_t>(kShortSmem / q.stride, std::max<int64_t>(8, target / N)));
   q.magic = ((1ull << 32) + (unsigned long long)N - 1) / (unsigned long long)N;
   return q;
 }
@@ -695,7 +733,7 @@ int64_t short_grid(const DeviceState* st, int64_t rows, const ShortPlan& q) {
 
 int run_rscan_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y, cudaStream_t s,
                     int flags) {
-  const ShortPlan q = short_plan(N, kShortChunk);
+  const ShortPlan q = short_plan(N, kShortChunk, kShortScanSolo);
   // float4 loads and stores need whole float4s per row and aligned pointers.
   const bool vec4 = N % 4 == 0 && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
   Scratch sc;
@@ -709,7 +747,7 @@ int run_rscan_short(const Provider& pv, const float* x, int64_t rows, int64_t N,
 // same chunks: one float per row.
 int run_rows_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* out, int op, int epi,
                    cudaStream_t s) {
-  const ShortPlan q = short_plan(N, kShortSmem);
+  const ShortPlan q = short_plan(N, kShortChunk, kShortReduceSolo);
   const bool vec4 = N % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   Scratch sc;
   int rc = acquire(pv, Need{}, &sc, s);

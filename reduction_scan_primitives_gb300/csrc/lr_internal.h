@@ -88,6 +88,7 @@ struct RScanRowsParams {
 constexpr int kShortRowMax = 2048;    // longest row this form takes
 constexpr int kShortChunk = 3072;     // data floats per chunk (about; at least 8 rows where they fit)
 constexpr int kShortSmem = 6144;      // shared floats per block (24 KB)
+constexpr int kShortThreads = 128;    // threads per block
 struct ShortRowsParams {
   const float* x;
   float* y;

@@ -1,12 +1,14 @@
-// lr_rows_short.cu -- cumulative sums of many short rows (inner == 1, N up
-// to kShortRowMax).
+// lr_rows_short.cu -- cumulative sums and reductions of many short rows
+// (inner == 1, N up to kShortRowMax).
 //
 // One block per row would leave most of its threads idle and pay a whole
 // tile's work for a few hundred bytes.  Instead a block stages a chunk of
-// whole rows (about kShortChunk floats, and at least 8 rows where they fit,
-// so every warp has one; contiguous in memory) in shared memory with
-// coalesced loads, scans every row there, and stores the chunk back with
-// coalesced stores.  A row is scanned by a group of G lanes:
+// whole rows (contiguous in memory; the host sizes it and starts every chunk
+// on a 128-byte boundary where the rows allow) in shared memory with
+// coalesced loads, scans or reduces every row there, and (scans) stores the
+// chunk back with coalesced stores.  With 16-byte loads the blocks run a
+// software pipeline: the next chunk's loads are issued into registers before
+// the current chunk is processed.  A row is handled by a group of G lanes:
 //   G == 1: one thread walks the row in the scan direction;
 //   G > 1:  lane g takes the g-th run of L (odd) consecutive elements from
 //           the scan's start: a sequential prefix over its run in place,
@@ -25,39 +27,16 @@
 namespace lr {
 namespace {
 
-constexpr int kShortThreads = 128;  // 8 blocks per SM at 64 registers
+// With 16-byte loads (N % 4 == 0) the row stride is a multiple of 4 for every
+// group of at least 4 lanes (stride = L*G mod 32, or N itself for G == 32),
+// so staging can use 16-byte shared-memory accesses.
+template <int G>
+constexpr bool kSmem4 = G >= 4;
 
-// Coalesced loads of a chunk into shared memory.  VEC 4 loads 16 bytes at a
-// time (N % 4 == 0: a float4 never straddles two rows).
-// SMEM4: 16-byte shared-memory accesses (the row stride is a multiple of 4,
-// as for every group of more than one lane); else four 4-byte ones.
-template <int VEC, bool SMEM4>
-__device__ __forceinline__ void stage_in(const ShortRowsParams& p, const float* src, float* s, int ne) {
-  const int t = threadIdx.x;
-  if constexpr (VEC == 4) {
-#pragma unroll 4
-    for (int e = 4 * t; e < ne; e += 4 * kShortThreads) {
-      const float4 f = ld_stream4(src + e);
-      const int r = (int)(((unsigned long long)e * p.magic) >> 32);
-      float* d = s + r * p.stride + (e - r * p.N);
-      if constexpr (SMEM4) {  // one 16-byte store: no bank conflicts
-        *reinterpret_cast<float4*>(d) = f;
-      } else {
-        d[0] = f.x;
-        d[1] = f.y;
-        d[2] = f.z;
-        d[3] = f.w;
-      }
-    }
-  } else {
-#pragma unroll 8
-    for (int e = t; e < ne; e += kShortThreads) {
-      const int r = (int)(((unsigned long long)e * p.magic) >> 32);
-      s[r * p.stride + (e - r * p.N)] = ld_stream1(src + e);
-    }
-  }
-}
-
+// Coalesced stores of a chunk back to memory.  VEC 4 stores 16 bytes at a
+// time (N % 4 == 0: a float4 never straddles two rows).  SMEM4: 16-byte
+// shared-memory reads (the row stride is a multiple of 4: see kSmem4); else
+// four 4-byte ones.
 template <int VEC, bool SMEM4>
 __device__ __forceinline__ void stage_out(const ShortRowsParams& p, const float* s, float* dst, int ne) {
   const int t = threadIdx.x;
@@ -151,8 +130,87 @@ __device__ __forceinline__ void scan_row(float* row, int N, int L, int g, bool a
   }
 }
 
+// The software pipeline: a thread loads its share of the first kShortChunk
+// floats of chunk c + gridDim.x into registers (kPrefetch loads of VEC
+// floats) while chunk c is being processed, and writes them to shared memory
+// when that chunk is staged.  A longer chunk loads the rest at staging.
+template <int VEC>
+struct ChunkRegs;
+template <>
+struct ChunkRegs<4> {
+  static constexpr int kPrefetch = kShortChunk / (4 * kShortThreads);  // 6
+  float4 v[kPrefetch];
+};
+template <>
+struct ChunkRegs<1> {
+  static constexpr int kPrefetch = kShortChunk / kShortThreads;  // 24
+  float v[kPrefetch];
+};
+static_assert(ChunkRegs<4>::kPrefetch * 4 * kShortThreads == kShortChunk &&
+                  ChunkRegs<1>::kPrefetch * kShortThreads == kShortChunk,
+              "a prefetch covers kShortChunk floats");
+
+template <int VEC>
+__device__ __forceinline__ auto ld_vec(const float* p) {
+  if constexpr (VEC == 4) return ld_stream4(p);
+  else return ld_stream1(p);
+}
+
+template <int VEC>
+__device__ __forceinline__ void prefetch_chunk(const ShortRowsParams& p, int64_t c, ChunkRegs<VEC>& f) {
+  const int64_t r0 = c * p.rows_per_chunk;
+  const int ne = (int)min((int64_t)p.rows_per_chunk, p.rows - r0) * p.N;
+  const float* src = p.x + r0 * p.N;
+#pragma unroll
+  for (int k = 0; k < ChunkRegs<VEC>::kPrefetch; ++k) {
+    const int e = VEC * (threadIdx.x + k * kShortThreads);
+    if (e < ne) f.v[k] = ld_vec<VEC>(src + e);
+  }
+}
+
+// Shared-memory address of flat chunk index e (row r at r*stride).
+__device__ __forceinline__ float* chunk_slot(const ShortRowsParams& p, float* s, int e) {
+  const int r = (int)(((unsigned long long)e * p.magic) >> 32);
+  return s + r * p.stride + (e - r * p.N);
+}
+
+// One load's worth of a chunk into shared memory: a 16-byte store (SMEM4),
+// four 4-byte ones, or one float.
+template <bool SMEM4>
+__device__ __forceinline__ void put(float* d, float4 v) {
+  if constexpr (SMEM4) {
+    *reinterpret_cast<float4*>(d) = v;
+  } else {
+    d[0] = v.x;
+    d[1] = v.y;
+    d[2] = v.z;
+    d[3] = v.w;
+  }
+}
+template <bool SMEM4>
+__device__ __forceinline__ void put(float* d, float v) {
+  *d = v;
+}
+
+// Stage the ne floats of the chunk starting at row r0 from the prefetched
+// registers, plus the rest of a chunk longer than the prefetch.
 template <int G, int VEC>
-__global__ void __launch_bounds__(kShortThreads) k_rscan_short(ShortRowsParams p) {
+__device__ __forceinline__ void stage_chunk(const ShortRowsParams& p, float* s, int64_t r0, int ne,
+                                            const ChunkRegs<VEC>& f) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int k = 0; k < ChunkRegs<VEC>::kPrefetch; ++k) {
+    const int e = VEC * (t + k * kShortThreads);
+    if (e < ne) put<kSmem4<G>>(chunk_slot(p, s, e), f.v[k]);
+  }
+  const float* src = p.x + r0 * p.N;
+#pragma unroll 2
+  for (int e = VEC * (t + ChunkRegs<VEC>::kPrefetch * kShortThreads); e < ne; e += VEC * kShortThreads)
+    put<kSmem4<G>>(chunk_slot(p, s, e), ld_vec<VEC>(src + e));
+}
+
+template <int G, int VEC>
+__global__ void __launch_bounds__(kShortThreads, 7) k_rscan_short(ShortRowsParams p) {
   __shared__ __align__(16) float s[kShortSmem];
   const int t = threadIdx.x;
   const int gi = t / G;  // this thread's group
@@ -161,12 +219,15 @@ __global__ void __launch_bounds__(kShortThreads) k_rscan_short(ShortRowsParams p
   const bool mirror = (p.flags & kScanMirror) != 0;
   const bool exclusive = (p.flags & kScanExclusive) != 0;
   const int64_t chunks = (p.rows + p.rows_per_chunk - 1) / p.rows_per_chunk;
+  ChunkRegs<VEC> f;
+  if (blockIdx.x < chunks) prefetch_chunk<VEC>(p, blockIdx.x, f);
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
     const int64_t r0 = c * p.rows_per_chunk;
     const int nr = (int)min((int64_t)p.rows_per_chunk, p.rows - r0);
     const int ne = nr * p.N;
-    stage_in<VEC, (G > 1)>(p, p.x + r0 * p.N, s, ne);
+    stage_chunk<G, VEC>(p, s, r0, ne, f);
     __syncthreads();
+    if (c + gridDim.x < chunks) prefetch_chunk<VEC>(p, c + gridDim.x, f);
     // Whole warps stay in the loop (the groups' shuffles), so the bound is
     // the same for every thread.
     for (int rb = 0; rb < nr; rb += kGroups) {
@@ -174,7 +235,7 @@ __global__ void __launch_bounds__(kShortThreads) k_rscan_short(ShortRowsParams p
       scan_row<G>(s + (r < nr ? r : 0) * p.stride, p.N, p.run_len, g, r < nr, mirror, exclusive);
     }
     __syncthreads();
-    stage_out<VEC, (G > 1)>(p, s, p.y + r0 * p.N, ne);
+    stage_out<VEC, kSmem4<G>>(p, s, p.y + r0 * p.N, ne);
     __syncthreads();  // the next chunk overwrites s
   }
 }
@@ -185,18 +246,21 @@ __global__ void __launch_bounds__(kShortThreads) k_rscan_short(ShortRowsParams p
 // the row's result (with the epilogue: mean or square root).  p.y is the
 // output (one float per row) and p.flags the epilogue.
 template <int G, int VEC, typename Op>
-__global__ void __launch_bounds__(kShortThreads) k_reduce_short(ShortRowsParams p) {
+__global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsParams p) {
   __shared__ __align__(16) float s[kShortSmem];
   const int t = threadIdx.x;
   const int gi = t / G;
   const int g = t % G;
   constexpr int kGroups = kShortThreads / G;
   const int64_t chunks = (p.rows + p.rows_per_chunk - 1) / p.rows_per_chunk;
+  ChunkRegs<VEC> f;
+  if (blockIdx.x < chunks) prefetch_chunk<VEC>(p, blockIdx.x, f);
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
     const int64_t r0 = c * p.rows_per_chunk;
     const int nr = (int)min((int64_t)p.rows_per_chunk, p.rows - r0);
-    stage_in<VEC, (G > 1)>(p, p.x + r0 * p.N, s, nr * p.N);
+    stage_chunk<G, VEC>(p, s, r0, nr * p.N, f);
     __syncthreads();
+    if (c + gridDim.x < chunks) prefetch_chunk<VEC>(p, c + gridDim.x, f);
     for (int rb = 0; rb < nr; rb += kGroups) {
       const int r = rb + gi;
       const bool active = r < nr;
@@ -232,6 +296,8 @@ template <typename Op>
 cudaError_t launch_reduce_op(int lanes, int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
   switch (lanes) {
     case 1: return launch_reduce_g<1, Op>(vec, p, grid, s);
+    case 2: return launch_reduce_g<2, Op>(vec, p, grid, s);
+    case 4: return launch_reduce_g<4, Op>(vec, p, grid, s);
     case 8: return launch_reduce_g<8, Op>(vec, p, grid, s);
     case 16: return launch_reduce_g<16, Op>(vec, p, grid, s);
     case 32: return launch_reduce_g<32, Op>(vec, p, grid, s);
