@@ -235,9 +235,12 @@ constexpr int64_t kRowsWarpMaxLen = 2048;   // rows up to this length: one warp 
 constexpr int64_t kShortReduceMax = 128;    // rows up to this length: staged chunks (automatic choice;
                                             // measured 0.75 against 0.21 at N = 32, 0.54 against
                                             // 0.31 at 100, and behind one warp per row from 256)
-// Short-row plans (short_plan): rows up to these lengths take one lane each.
+// Short-row plans (short_form): rows up to these lengths (odd lengths: *Odd)
+// take one lane each.
 constexpr int64_t kShortScanSolo = 64;
+constexpr int64_t kShortScanSoloOdd = 256;
 constexpr int64_t kShortReduceSolo = 64;
+constexpr int64_t kShortReduceSoloOdd = kShortReduceMax;
 
 int contig_variant() {
   const int64_t v = g_opt_contig_variant.load();
@@ -731,29 +734,45 @@ int64_t short_grid(const DeviceState* st, int64_t rows, const ShortPlan& q) {
                                                 4 * (int64_t)st->sm_count * st->occ_rscan_short));
 }
 
+// The load form and plan of a short-row launch: 16-byte loads need whole
+// float4 rows (N % 4 == 0) and 16-byte aligned pointers; other rows take
+// 4-byte loads.  (Copying 16-byte aligned chunks of such rows as float4s was
+// measured and was slower: [., 33] 0.69 against 0.82 for scans, 0.49 against
+// 0.75 for sums.)  Odd rows up to solo_odd take one lane each: their chunks
+// then lie unpadded in shared memory (stride N), so staging needs no row
+// index, where lane groups pad every row (scans of [., 99] 0.78 against 0.66,
+// [., 255] 0.70 against 0.64; from 500 one lane per row is slower).
+struct ShortForm {
+  ShortPlan q;
+  int vec;
+};
+ShortForm short_form(int64_t N, int64_t solo, int64_t solo_odd, bool aligned16) {
+  return {short_plan(N, kShortChunk, N % 2 ? solo_odd : solo), aligned16 && N % 4 == 0 ? kShortLd4 : kShortLd1};
+}
+
 int run_rscan_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y, cudaStream_t s,
                     int flags) {
-  const ShortPlan q = short_plan(N, kShortChunk, kShortScanSolo);
-  // float4 loads and stores need whole float4s per row and aligned pointers.
-  const bool vec4 = N % 4 == 0 && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+  const ShortForm f = short_form(N, kShortScanSolo, kShortScanSoloOdd,
+                                 ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0);
+  const ShortPlan& q = f.q;
   Scratch sc;
   int rc = acquire(pv, Need{}, &sc, s);
   if (rc) return rc;
   ShortRowsParams p{x, y, rows, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, flags};
-  return launched(launch_rscan_short(q.lanes, vec4 ? 4 : 1, p, short_grid(pv.st, rows, q), s));
+  return launched(launch_rscan_short(q.lanes, f.vec, p, short_grid(pv.st, rows, q), s));
 }
 
 // Reductions of many short rows (inner == 1, reduce <= kShortRowMax) with the
 // same chunks: one float per row.
 int run_rows_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* out, int op, int epi,
                    cudaStream_t s) {
-  const ShortPlan q = short_plan(N, kShortChunk, kShortReduceSolo);
-  const bool vec4 = N % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  const ShortForm f = short_form(N, kShortReduceSolo, kShortReduceSoloOdd, (reinterpret_cast<uintptr_t>(x) & 15u) == 0);
+  const ShortPlan& q = f.q;
   Scratch sc;
   int rc = acquire(pv, Need{}, &sc, s);
   if (rc) return rc;
   ShortRowsParams p{x, out, rows, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, epi};
-  return launched(launch_reduce_short(op, q.lanes, vec4 ? 4 : 1, p, short_grid(pv.st, rows, q), s));
+  return launched(launch_reduce_short(op, q.lanes, f.vec, p, short_grid(pv.st, rows, q), s));
 }
 
 // Scans along rows (inner == 1).  `flags`: kScanMirror for a forward scan,

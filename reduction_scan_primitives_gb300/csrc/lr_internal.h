@@ -89,6 +89,9 @@ constexpr int kShortRowMax = 2048;    // longest row this form takes
 constexpr int kShortChunk = 3072;     // data floats per chunk (about; at least 8 rows where they fit)
 constexpr int kShortSmem = 6144;      // shared floats per block (24 KB)
 constexpr int kShortThreads = 128;    // threads per block
+// Load forms of the short-row kernels (the launchers' `vec`):
+constexpr int kShortLd1 = 1;  // 4-byte loads (any 4-byte alignment)
+constexpr int kShortLd4 = 4;  // 16-byte loads; every row is whole float4s (N % 4 == 0)
 struct ShortRowsParams {
   const float* x;
   float* y;

@@ -33,31 +33,90 @@ namespace {
 template <int G>
 constexpr bool kSmem4 = G >= 4;
 
+// Shared-memory address of flat chunk index e (row r at r*stride).  An
+// unpadded chunk (stride == N: one lane per row with N odd) needs no row.
+__device__ __forceinline__ float* chunk_slot(const ShortRowsParams& p, float* s, int e) {
+  if (p.stride == p.N) return s + e;
+  const int r = (int)(((unsigned long long)e * p.magic) >> 32);
+  return s + r * p.stride + (e - r * p.N);
+}
+
 // Coalesced stores of a chunk back to memory.  VEC 4 stores 16 bytes at a
 // time (N % 4 == 0: a float4 never straddles two rows).  SMEM4: 16-byte
 // shared-memory reads (the row stride is a multiple of 4: see kSmem4); else
 // four 4-byte ones.
 template <int VEC, bool SMEM4>
-__device__ __forceinline__ void stage_out(const ShortRowsParams& p, const float* s, float* dst, int ne) {
+__device__ __forceinline__ void stage_out(const ShortRowsParams& p, float* s, float* dst, int ne) {
   const int t = threadIdx.x;
-  if constexpr (VEC == 4) {
+  if constexpr (VEC == kShortLd4) {
 #pragma unroll 4
     for (int e = 4 * t; e < ne; e += 4 * kShortThreads) {
-      const int r = (int)(((unsigned long long)e * p.magic) >> 32);
-      const float* d = s + r * p.stride + (e - r * p.N);
+      const float* d = chunk_slot(p, s, e);
       if constexpr (SMEM4) st_stream4(dst + e, *reinterpret_cast<const float4*>(d));
       else st_stream4(dst + e, make_float4(d[0], d[1], d[2], d[3]));
     }
   } else {
 #pragma unroll 8
-    for (int e = t; e < ne; e += kShortThreads) {
-      const int r = (int)(((unsigned long long)e * p.magic) >> 32);
-      st_stream1(dst + e, s[r * p.stride + (e - r * p.N)]);
-    }
+    for (int e = t; e < ne; e += kShortThreads) st_stream1(dst + e, *chunk_slot(p, s, e));
   }
 }
 
-constexpr int kRegRun = 16;  // elements a lane holds in registers at a time
+constexpr int kRegRun = 16;   // elements a lane holds in registers at a time
+constexpr int kRunBlock = 8;  // elements per register block of a long run
+
+// Scan the n elements at base[dir*i], i = 0..n-1, in place from zero
+// (inclusive, or exclusive: each output leaves its own term out); returns
+// their sum.  The additions are the sequential ones: acc += x[0], x[1], ...
+// BLOCKED moves kRunBlock elements at a time through registers (all loads of
+// a block issued together; the zeros that pad the last block leave acc
+// unchanged), which pays where few lanes hold long runs (32-lane groups:
+// rows of 500-2048, 0.84-0.86 -> 0.87-0.94 of copy bandwidth); with many
+// groups in flight the element-by-element walk, with fewer instructions, is
+// faster (rows of 100-256: 0.96 against 0.93).
+template <bool BLOCKED>
+__device__ __forceinline__ float scan_run(float* base, int dir, int n, bool exclusive) {
+  float acc = 0.f;
+  if constexpr (!BLOCKED) {
+    for (int i = 0; i < n; ++i) {
+      const float before = acc;
+      acc += base[dir * i];
+      base[dir * i] = exclusive ? before : acc;
+    }
+    return acc;
+  }
+  for (int i0 = 0; i0 < n; i0 += kRunBlock) {
+    float v[kRunBlock];
+#pragma unroll
+    for (int i = 0; i < kRunBlock; ++i) v[i] = i0 + i < n ? base[dir * (i0 + i)] : 0.f;
+#pragma unroll
+    for (int i = 0; i < kRunBlock; ++i) {
+      const float before = acc;
+      acc += v[i];
+      v[i] = exclusive ? before : acc;
+    }
+#pragma unroll
+    for (int i = 0; i < kRunBlock; ++i)
+      if (i0 + i < n) base[dir * (i0 + i)] = v[i];
+  }
+  return acc;
+}
+
+// base[dir*i] = off + base[dir*i] for i = 0..n-1 (BLOCKED: kRunBlock at a time).
+template <bool BLOCKED>
+__device__ __forceinline__ void offset_run(float* base, int dir, int n, float off) {
+  if constexpr (!BLOCKED) {
+    for (int i = 0; i < n; ++i) base[dir * i] = off + base[dir * i];
+    return;
+  }
+  for (int i0 = 0; i0 < n; i0 += kRunBlock) {
+    float v[kRunBlock];
+#pragma unroll
+    for (int i = 0; i < kRunBlock; ++i) v[i] = i0 + i < n ? base[dir * (i0 + i)] : 0.f;
+#pragma unroll
+    for (int i = 0; i < kRunBlock; ++i)
+      if (i0 + i < n) base[dir * (i0 + i)] = off + v[i];
+  }
+}
 
 // Scan one row in place with G lanes (g = this lane's index in its group).
 // G == 1: the lane walks the row in the scan direction.  G > 1: lane g takes
@@ -65,8 +124,8 @@ constexpr int kRegRun = 16;  // elements a lane holds in registers at a time
 // sum of the runs before it (an exclusive scan of the run totals across the
 // group) is added to each of its prefix sums.  A run of at most kRegRun
 // elements stays in registers between its load and its store; a longer one
-// is scanned in place first and offset in a second pass.  Both compute
-// off + (prefix within the run) with the same additions.
+// is scanned in place first and offset in a second pass (see scan_run).
+// Both compute off + (prefix within the run) with the same additions.
 // `active` is false for the lanes of a group past the chunk's last row: they
 // still take part in the shuffles, with zeros, and touch nothing.
 template <int G>
@@ -74,14 +133,7 @@ __device__ __forceinline__ void scan_row(float* row, int N, int L, int g, bool a
                                          bool exclusive) {
   if constexpr (G == 1) {
     if (!active) return;
-    float acc = 0.f;
-    const int dir = mirror ? 1 : -1;
-    float* p0 = mirror ? row : row + (N - 1);
-    for (int i = 0; i < N; ++i) {
-      const float before = acc;
-      acc += p0[dir * i];
-      p0[dir * i] = exclusive ? before : acc;
-    }
+    scan_run<false>(mirror ? row : row + (N - 1), mirror ? 1 : -1, N, exclusive);
   } else {
     // Element i of run g in memory: g*L + i (forward) or N-1 - (g*L + i)
     // (reverse); positions outside [0, N) belong to no element.
@@ -118,42 +170,37 @@ __device__ __forceinline__ void scan_row(float* row, int N, int L, int g, bool a
       for (int i = 0; i < kRegRun; ++i)
         if (i < n_run) base[dir * i] = v[i];
     } else {
-      float acc = 0.f;
-      for (int i = 0; i < n_run; ++i) {
-        const float before = acc;
-        acc += base[dir * i];
-        base[dir * i] = exclusive ? before : acc;
-      }
-      const float off = offset_of(acc);
-      for (int i = 0; i < n_run; ++i) base[dir * i] = off + base[dir * i];
+      const float off = offset_of(scan_run<(G == 32)>(base, dir, n_run, exclusive));
+      offset_run<(G == 32)>(base, dir, n_run, off);
     }
   }
 }
 
 // The software pipeline: a thread loads its share of the first kShortChunk
-// floats of chunk c + gridDim.x into registers (kPrefetch loads of VEC
-// floats) while chunk c is being processed, and writes them to shared memory
+// floats of chunk c + gridDim.x into registers (kPrefetch loads of 16 or 4
+// bytes) while chunk c is being processed, and writes them to shared memory
 // when that chunk is staged.  A longer chunk loads the rest at staging.
 template <int VEC>
-struct ChunkRegs;
-template <>
-struct ChunkRegs<4> {
+struct ChunkRegs {  // kShortLd4
+  static constexpr int kWidth = 4;
   static constexpr int kPrefetch = kShortChunk / (4 * kShortThreads);  // 6
   float4 v[kPrefetch];
 };
 template <>
-struct ChunkRegs<1> {
+struct ChunkRegs<kShortLd1> {
+  static constexpr int kWidth = 1;
   static constexpr int kPrefetch = kShortChunk / kShortThreads;  // 24
   float v[kPrefetch];
 };
-static_assert(ChunkRegs<4>::kPrefetch * 4 * kShortThreads == kShortChunk &&
-                  ChunkRegs<1>::kPrefetch * kShortThreads == kShortChunk,
+static_assert(ChunkRegs<kShortLd4>::kPrefetch * 4 * kShortThreads == kShortChunk &&
+                  ChunkRegs<kShortLd1>::kPrefetch * kShortThreads == kShortChunk,
               "a prefetch covers kShortChunk floats");
 
+// One load at chunk index e of src: 16 bytes or 4.
 template <int VEC>
-__device__ __forceinline__ auto ld_vec(const float* p) {
-  if constexpr (VEC == 4) return ld_stream4(p);
-  else return ld_stream1(p);
+__device__ __forceinline__ auto ld_chunk(const float* src, int e) {
+  if constexpr (VEC == kShortLd4) return ld_stream4(src + e);
+  else return ld_stream1(src + e);
 }
 
 template <int VEC>
@@ -163,21 +210,16 @@ __device__ __forceinline__ void prefetch_chunk(const ShortRowsParams& p, int64_t
   const float* src = p.x + r0 * p.N;
 #pragma unroll
   for (int k = 0; k < ChunkRegs<VEC>::kPrefetch; ++k) {
-    const int e = VEC * (threadIdx.x + k * kShortThreads);
-    if (e < ne) f.v[k] = ld_vec<VEC>(src + e);
+    const int e = ChunkRegs<VEC>::kWidth * (threadIdx.x + k * kShortThreads);
+    if (e < ne) f.v[k] = ld_chunk<VEC>(src, e);
   }
 }
 
-// Shared-memory address of flat chunk index e (row r at r*stride).
-__device__ __forceinline__ float* chunk_slot(const ShortRowsParams& p, float* s, int e) {
-  const int r = (int)(((unsigned long long)e * p.magic) >> 32);
-  return s + r * p.stride + (e - r * p.N);
-}
-
-// One load's worth of a chunk into shared memory: a 16-byte store (SMEM4),
-// four 4-byte ones, or one float.
-template <bool SMEM4>
-__device__ __forceinline__ void put(float* d, float4 v) {
+// One load's worth (chunk index e) into shared memory: a 16-byte store
+// (SMEM4), four 4-byte ones, or one float.
+template <int VEC, bool SMEM4>
+__device__ __forceinline__ void put(const ShortRowsParams& p, float* s, int e, float4 v) {
+  float* d = chunk_slot(p, s, e);
   if constexpr (SMEM4) {
     *reinterpret_cast<float4*>(d) = v;
   } else {
@@ -187,9 +229,9 @@ __device__ __forceinline__ void put(float* d, float4 v) {
     d[3] = v.w;
   }
 }
-template <bool SMEM4>
-__device__ __forceinline__ void put(float* d, float v) {
-  *d = v;
+template <int VEC, bool SMEM4>
+__device__ __forceinline__ void put(const ShortRowsParams& p, float* s, int e, float v) {
+  *chunk_slot(p, s, e) = v;
 }
 
 // Stage the ne floats of the chunk starting at row r0 from the prefetched
@@ -197,16 +239,17 @@ __device__ __forceinline__ void put(float* d, float v) {
 template <int G, int VEC>
 __device__ __forceinline__ void stage_chunk(const ShortRowsParams& p, float* s, int64_t r0, int ne,
                                             const ChunkRegs<VEC>& f) {
+  constexpr int W = ChunkRegs<VEC>::kWidth;
   const int t = threadIdx.x;
 #pragma unroll
   for (int k = 0; k < ChunkRegs<VEC>::kPrefetch; ++k) {
-    const int e = VEC * (t + k * kShortThreads);
-    if (e < ne) put<kSmem4<G>>(chunk_slot(p, s, e), f.v[k]);
+    const int e = W * (t + k * kShortThreads);
+    if (e < ne) put<VEC, kSmem4<G>>(p, s, e, f.v[k]);
   }
   const float* src = p.x + r0 * p.N;
 #pragma unroll 2
-  for (int e = VEC * (t + ChunkRegs<VEC>::kPrefetch * kShortThreads); e < ne; e += VEC * kShortThreads)
-    put<kSmem4<G>>(chunk_slot(p, s, e), ld_vec<VEC>(src + e));
+  for (int e = W * (t + ChunkRegs<VEC>::kPrefetch * kShortThreads); e < ne; e += W * kShortThreads)
+    put<VEC, kSmem4<G>>(p, s, e, ld_chunk<VEC>(src, e));
 }
 
 template <int G, int VEC>
@@ -287,8 +330,11 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsPara
 
 template <int G, typename Op>
 cudaError_t launch_reduce_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
-  if (vec == 4) k_reduce_short<G, 4, Op><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
-  else k_reduce_short<G, 1, Op><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+  if (vec == kShortLd4) {
+    k_reduce_short<G, kShortLd4, Op><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+  } else {
+    k_reduce_short<G, kShortLd1, Op><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
@@ -307,8 +353,11 @@ cudaError_t launch_reduce_op(int lanes, int vec, const ShortRowsParams& p, int64
 
 template <int G>
 cudaError_t launch_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
-  if (vec == 4) k_rscan_short<G, 4><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
-  else k_rscan_short<G, 1><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+  if (vec == kShortLd4) {
+    k_rscan_short<G, kShortLd4><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+  } else {
+    k_rscan_short<G, kShortLd1><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
@@ -338,7 +387,7 @@ cudaError_t launch_reduce_short(int op, int lanes, int vec, const ShortRowsParam
 
 int occupancy_rscan_short() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_rscan_short<32, 4>, kShortThreads, 0) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_rscan_short<32, kShortLd4>, kShortThreads, 0) != cudaSuccess) return 0;
   return n;
 }
 

@@ -371,15 +371,17 @@ def test_narrow_few_planes_take_the_lookback(reverse, exclusive):
 # Many short rows (N <= 2048): chunks of whole rows staged in shared memory,
 # each row scanned by a group of 1..32 lanes (OPT_SCAN_STRATEGY 5 forces it;
 # the automatic choice for such rows).
-SHORT_N = [1, 2, 3, 5, 8, 16, 31, 32, 33, 40, 64, 100, 255, 256, 257, 1000, 1024, 2047, 2048]
+SHORT_N = [1, 2, 3, 5, 6, 8, 16, 31, 32, 33, 40, 50, 64, 65, 99, 100, 127, 130, 255, 256, 257, 258, 1000, 1002,
+           1024, 2046, 2047, 2048]
 
 
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("strategy", [0, 5])
 def test_short_rows(strategy, reverse, exclusive):
     """Every lane-group size and its boundaries; row counts that leave a
-    partial last chunk; float4 (aligned, N % 4 == 0) and scalar staging (x and
-    y at an odd offset)."""
+    partial last chunk; 16-byte loads (aligned, N % 4 == 0) and 4-byte loads
+    (N % 4 != 0, or x and y at an odd offset); rows unpadded in shared memory
+    (one lane per row, N odd)."""
     L.set_option(L.OPT_SCAN_STRATEGY, strategy)
     for n in SHORT_N:
         rows = 3 * max(1, 6144 // n) + 7
@@ -391,7 +393,7 @@ def test_short_rows(strategy, reverse, exclusive):
 
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
 def test_short_rows_integers_exact(reverse, exclusive):
-    for n in (7, 32, 100, 1024):
+    for n in (7, 32, 66, 100, 1024):
         x = inputs.make((5000, n), "int:0:3", 31)
         ref, _ = oracle.cumsum(x.numpy(), 5000, n, 1, reverse, exclusive)
         assert_exact(run(x, 1, reverse, exclusive).reshape(-1), ref.reshape(-1), f"short rows int N={n}")

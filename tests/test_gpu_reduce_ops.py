@@ -109,7 +109,7 @@ def test_narrow_rows_ops(op, shape, split):
 # Reductions along rows of at most 2048 elements (inner == 1): one warp per
 # row (OPT_ROWS_FORM 1) or chunks of whole rows staged in shared memory with a
 # group of 1-32 lanes per row (2, the automatic choice).
-SHORT_N = [1, 2, 3, 7, 8, 31, 32, 33, 64, 100, 255, 256, 257, 1000, 1024, 2047, 2048]
+SHORT_N = [1, 2, 3, 6, 7, 8, 31, 32, 33, 50, 64, 65, 99, 100, 127, 130, 255, 256, 257, 1000, 1024, 2047, 2048]
 
 
 @pytest.mark.parametrize("op", OPS + ["sum"])
@@ -133,7 +133,7 @@ def test_short_rows_both_forms(op, form):
 def test_short_rows_forms_exact_and_deterministic():
     """Small integers sum exactly in both forms (so they agree bit for bit),
     and max / min pick the same elements; reruns are bit-identical."""
-    for n in (5, 32, 100, 1000):
+    for n in (5, 32, 66, 100, 1000):
         x = on_device(inputs.make((20_000, n), "int:-8:8", 61))
         outs = {}
         for form in (1, 2):
