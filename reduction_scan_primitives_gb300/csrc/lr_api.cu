@@ -737,7 +737,7 @@ int64_t short_grid(const DeviceState* st, int64_t rows, const ShortPlan& q) {
 // The load form and plan of a short-row launch: 16-byte loads need whole
 // float4 rows (N % 4 == 0) and 16-byte aligned pointers; other rows take
 // 4-byte loads.  (Copying 16-byte aligned chunks of such rows as float4s was
-// measured and was slower: [., 33] 0.69 against 0.82 for scans, 0.49 against
+// measured and was slower: [., 33] 0.69 against 0.96 for scans, 0.49 against
 // 0.75 for sums.)  Odd rows up to solo_odd take one lane each: their chunks
 // then lie unpadded in shared memory (stride N), so staging needs no row
 // index, where lane groups pad every row (scans of [., 99] 0.78 against 0.66,
