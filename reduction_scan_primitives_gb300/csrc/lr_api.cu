@@ -236,9 +236,14 @@ constexpr int64_t kShortReduceMax = 128;    // rows up to this length: staged ch
                                             // measured 0.75 against 0.21 at N = 32, 0.54 against
                                             // 0.31 at 100, and behind one warp per row from 256)
 // Short-row plans (short_form): rows up to these lengths (odd lengths: *Odd)
-// take one lane each.
+// take one lane each.  A lane walks its row with sequential additions, so
+// an output can end a chain of N - 1 roundings; at most 158 keeps the
+// worst case, 158 * 2^-24 * sum|x| (to first order), inside the tolerance
+// 1e-5 * sum|x| for any data.  (Odd rows up to 255 scanned 0.70-0.81 walked
+// against 0.64 in lane groups; a walk with a carry folded every 16 elements,
+// which would bound the chain, cost 15-20% at every length.)
 constexpr int64_t kShortScanSolo = 64;
-constexpr int64_t kShortScanSoloOdd = 256;
+constexpr int64_t kShortScanSoloOdd = 159;
 constexpr int64_t kShortReduceSolo = 64;
 constexpr int64_t kShortReduceSoloOdd = kShortReduceMax;
 
@@ -740,8 +745,8 @@ int64_t short_grid(const DeviceState* st, int64_t rows, const ShortPlan& q) {
 // measured and was slower: [., 33] 0.69 against 0.96 for scans, 0.49 against
 // 0.75 for sums.)  Odd rows up to solo_odd take one lane each: their chunks
 // then lie unpadded in shared memory (stride N), so staging needs no row
-// index, where lane groups pad every row (scans of [., 99] 0.78 against 0.66,
-// [., 255] 0.70 against 0.64; from 500 one lane per row is slower).
+// index, where lane groups pad every row (scans of [., 99] 0.78 against 0.66;
+// from 500 one lane per row is slower).
 struct ShortForm {
   ShortPlan q;
   int vec;

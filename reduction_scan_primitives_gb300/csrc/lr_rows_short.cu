@@ -66,13 +66,15 @@ constexpr int kRunBlock = 8;  // elements per register block of a long run
 
 // Scan the n elements at base[dir*i], i = 0..n-1, in place from zero
 // (inclusive, or exclusive: each output leaves its own term out); returns
-// their sum.  The additions are the sequential ones: acc += x[0], x[1], ...
-// BLOCKED moves kRunBlock elements at a time through registers (all loads of
-// a block issued together; the zeros that pad the last block leave acc
-// unchanged), which pays where few lanes hold long runs (32-lane groups:
-// rows of 500-2048, 0.84-0.86 -> 0.87-0.94 of copy bandwidth); with many
-// groups in flight the element-by-element walk, with fewer instructions, is
-// faster (rows of 100-256: 0.96 against 0.93).
+// their sum.  The additions are the sequential ones: acc += x[0], x[1], ...,
+// so an output is at most n - 1 roundings deep (the host keeps walked rows
+// to at most 159 elements and lane runs to at most 65).  BLOCKED moves
+// kRunBlock elements at a time through
+// registers (all loads of a block issued together; the zeros that pad the
+// last block leave acc unchanged), which pays where few lanes hold long
+// runs (32-lane groups: rows of 500-2048, 0.84-0.86 -> 0.87-0.94 of copy
+// bandwidth); with many groups in flight the element-by-element walk, with
+// fewer instructions, is faster (rows of 100-256: 0.96 against 0.93).
 template <bool BLOCKED>
 __device__ __forceinline__ float scan_run(float* base, int dir, int n, bool exclusive) {
   float acc = 0.f;
@@ -310,13 +312,15 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsPara
       const float* row = s + (active ? r : 0) * p.stride;
       const int first = G == 1 ? 0 : g * p.run_len;
       const int n_run = active ? max(0, min(G == 1 ? p.N : p.run_len, p.N - first)) : 0;
+      // Blocks of kRegRun elements, each combined by a fixed tree, then
+      // folded in order: a row of up to 128 elements is at most
+      // log2(kRegRun) + 8 roundings deep.
       float v = Op::identity();
       for (int i0 = 0; i0 < n_run; i0 += kRegRun) {
         float a[kRegRun];
 #pragma unroll
         for (int i = 0; i < kRegRun; ++i) a[i] = i0 + i < n_run ? Op::prep(row[first + i0 + i]) : Op::identity();
-#pragma unroll
-        for (int i = 0; i < kRegRun; ++i) v = Op::combine(v, a[i]);
+        v = Op::combine(v, tree_reduce<Op, kRegRun>(a));
       }
       if constexpr (G > 1) {
 #pragma unroll
