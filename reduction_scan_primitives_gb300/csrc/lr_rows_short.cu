@@ -312,16 +312,20 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsPara
       const float* row = s + (active ? r : 0) * p.stride;
       const int first = G == 1 ? 0 : g * p.run_len;
       const int n_run = active ? max(0, min(G == 1 ? p.N : p.run_len, p.N - first)) : 0;
-      // Blocks of kRegRun elements, each combined by a fixed tree, then
-      // folded in order: a row of up to 128 elements is at most
-      // log2(kRegRun) + 8 roundings deep.
+      // Whole blocks of kRegRun elements, each combined by a fixed tree, then
+      // the remaining elements, all folded in order: a row of up to 128
+      // elements is at most log2(kRegRun) + 8 + 15 roundings deep.
       float v = Op::identity();
-      for (int i0 = 0; i0 < n_run; i0 += kRegRun) {
+      const float* rp = row + first;
+      int i0 = 0;
+      for (; i0 + kRegRun <= n_run; i0 += kRegRun) {
         float a[kRegRun];
 #pragma unroll
-        for (int i = 0; i < kRegRun; ++i) a[i] = i0 + i < n_run ? Op::prep(row[first + i0 + i]) : Op::identity();
+        for (int i = 0; i < kRegRun; ++i) a[i] = Op::prep(rp[i0 + i]);
         v = Op::combine(v, tree_reduce<Op, kRegRun>(a));
       }
+#pragma unroll 4
+      for (; i0 < n_run; ++i0) v = Op::combine(v, Op::prep(rp[i0]));
       if constexpr (G > 1) {
 #pragma unroll
         for (int d = G / 2; d > 0; d >>= 1) v = Op::combine(v, __shfl_down_sync(kFullMask, v, d, G));
