@@ -6,9 +6,9 @@
 // whole rows (contiguous in memory; the host sizes it and starts every chunk
 // on a 128-byte boundary where the rows allow) in shared memory with
 // coalesced loads, scans or reduces every row there, and (scans) stores the
-// chunk back with coalesced stores.  With 16-byte loads the blocks run a
-// software pipeline: the next chunk's loads are issued into registers before
-// the current chunk is processed.  A row is handled by a group of G lanes:
+// chunk back with coalesced stores.  The blocks run a software pipeline: the
+// next chunk's loads are issued into registers before the current chunk is
+// processed.  A row is handled by a group of G lanes:
 //   G == 1: one thread walks the row in the scan direction;
 //   G > 1:  lane g takes the g-th run of L (odd) consecutive elements from
 //           the scan's start: a sequential prefix over its run in place,
@@ -69,12 +69,12 @@ constexpr int kRunBlock = 8;  // elements per register block of a long run
 // their sum.  The additions are the sequential ones: acc += x[0], x[1], ...,
 // so an output is at most n - 1 roundings deep (the host keeps walked rows
 // to at most 159 elements and lane runs to at most 65).  BLOCKED moves
-// kRunBlock elements at a time through
-// registers (all loads of a block issued together; the zeros that pad the
-// last block leave acc unchanged), which pays where few lanes hold long
-// runs (32-lane groups: rows of 500-2048, 0.84-0.86 -> 0.87-0.94 of copy
-// bandwidth); with many groups in flight the element-by-element walk, with
-// fewer instructions, is faster (rows of 100-256: 0.96 against 0.93).
+// kRunBlock elements at a time through registers (all loads of a block
+// issued together; the zeros that pad the last block leave acc unchanged),
+// which pays where few lanes hold long runs (32-lane groups: rows of
+// 500-2048, 0.84-0.86 -> 0.87-0.94 of copy bandwidth); with many groups in
+// flight the element-by-element walk, with fewer instructions, is faster
+// (rows of 100-256: 0.96 against 0.93).
 template <bool BLOCKED>
 __device__ __forceinline__ float scan_run(float* base, int dir, int n, bool exclusive) {
   float acc = 0.f;
