@@ -17,8 +17,9 @@
  *    masked item's load stays within the 16-byte granule of a row element).
  *  - Arrays are contiguous and row-major.  Sizes are element counts (int64).
  *  - `stream` is a cudaStream_t (NULL means the legacy default stream).  A
- *    call only enqueues work on `stream`: it never synchronises the host and
- *    never copies results back.  The caller keeps the inputs alive and
+ *    call only enqueues work on `stream` and never copies results back; apart
+ *    from the one-time workspace set-up described under "Scratch" below, it
+ *    never synchronises the host.  The caller keeps the inputs alive and
  *    unmodified until that work completes.
  *  - Results are deterministic: the same input on the same device gives
  *    bit-identical output on every call.  No floating-point atomics are used;
@@ -29,13 +30,18 @@
  *    documented with their op codes).  NaN and Inf propagate as IEEE addition
  *    does.
  *  - Scratch: the library keeps one workspace per device for partial sums,
- *    tickets and look-back flags (about 17 MB, plus 128 MB of look-back node
- *    words once a look-back scan has run).  It is allocated (cudaMalloc) by
- *    the first call on that device that needs it, so that first call must not
- *    be made inside a stream capture.  Because the workspace is shared, calls on one
- *    device must not run concurrently on different streams; calls queued on
- *    one stream are always safe.  The *_ws variants take the scratch from
- *    the caller instead and lift this limit.
+ *    tickets and error words (17,039,616 bytes) and, once a look-back scan
+ *    has run, a second one for look-back node words (2^24 x 8 bytes =
+ *    128 MiB).  Each is allocated (cudaMalloc), zeroed (cudaMemset) and
+ *    followed by a cudaDeviceSynchronize by the first call on that device that
+ *    needs it -- the only time a call synchronises -- so that first call must
+ *    not be made inside a stream capture.  Later calls reuse them and
+ *    allocate nothing.  Calls that need no scratch (e.g. 1D reductions of at
+ *    most 2^18 floats, scans of rows one block per row) never create them.
+ *    Because the workspace is shared, calls on one device must not run
+ *    concurrently on different streams; calls queued on one stream are always
+ *    safe.  The *_ws variants take the scratch from the caller instead and
+ *    lift this limit.
  *  - CUDA graphs: after that first call, every call may be captured and the
  *    graph replayed any number of times (tickets are reset on the device, and
  *    the look-back scan takes its launch epoch from a device word that every
@@ -224,22 +230,25 @@ LIBREDUCE_API int libreduce_check_ws(void* ws, libreduce_stream_t stream);
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory.  reduce_sum_f32 takes its scratch from a
  * workspace the library cudaMallocs on first use; some callers cannot allow
- * that (code inside a custom allocator or a memory-capped service, where every
- * device byte must be accounted for up front, or a stream capture in
- * progress).  This call runs the same kernel with its scratch (a ticket and up
- * to 16384 partial sums, 64.25 KiB) in a fixed static device array that every
- * GPU loading the library holds until exit.  It calls no cudaMalloc, cudaFree
- * or other allocating routine.
+ * that (code inside a custom allocator, or a service whose device memory is
+ * capped and every byte budgeted up front).  This call runs the multi-block
+ * sum kernel with its scratch (a ticket and up to 16384 partial sums,
+ * 64.25 KiB) in a fixed static device array that every GPU loading the
+ * library holds until exit.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
  *   x    device, n floats (may be NULL when n == 0)
  *   n    0 <= n <= 2^36 (16384 blocks of at most 2^22 floats)
  *   out  device, 1 float
- * The result equals reduce_sum_f32's within the documented tolerance (the
- * blocking can differ once more than 16384 blocks would be used).
- * Set-up: the first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call shares the one array, and the ticket
- * is cleared on the stream before each launch, so calls that overlap on the
- * GPU (different streams, or other threads) race and must be avoided.
+ * The result is within the documented tolerance of the exact sum, like
+ * reduce_sum_f32's, and the same on every call; the two calls need not give
+ * the same bits (reduce_sum_f32 sums arrays of at most 2^18 floats in one
+ * thread-block cluster, and this call caps its blocks at 16384).
+ * Set-up: the first call on a device (and the first after that device's
+ * context was replaced, e.g. by cudaDeviceReset) looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Every call shares the one array, and the
+ * ticket is cleared on the stream before each launch, so calls that overlap
+ * on the GPU (different streams, or other threads) race and must be avoided.
  * Errors: INVALID_ARG, OVERFLOW (n > 2^36), ALIAS (out inside x), CUDA.
  */
 LIBREDUCE_API int reduce_sum_f32_noalloc(const float* x, int64_t n, float* out, libreduce_stream_t stream);

@@ -230,6 +230,7 @@ int launched(cudaError_t e) {
 // Strategies.
 // ---------------------------------------------------------------------------
 constexpr int64_t kMinChunk = 8192;         // floats per block, lower bound
+constexpr int64_t kClusterSlice = 16384;    // floats per CTA of a short 1D array (one cluster)
 constexpr int64_t kTargetChunk = 65536;     // floats per block of a long 1D sum (256 KiB)
 constexpr int64_t kRowsWarpMaxLen = 2048;   // rows up to this length: one warp per row
 constexpr int64_t kShortReduceMax = 128;    // rows up to this length: staged chunks (automatic choice;
@@ -336,6 +337,20 @@ int run_contig(const Provider& pv, const float* x, int64_t segments, int64_t seg
   const int64_t waves = g_opt_waves.load();
   int64_t chunks = 1;
   const int64_t forced = g_opt_axis_split.load();
+  if (segments == 1 && seg_len <= kClusterMaxN && forced <= 0 && waves <= 0 &&
+      g_opt_contig_variant.load() < 0) {
+    // A short array: one cluster of CTAs, about kClusterSlice floats each
+    // (all of a CTA's loads in one round trip), combined in distributed
+    // shared memory: one launch, no scratch, no ticket.
+    Scratch sc;
+    int rc = acquire(pv, Need{}, &sc, s);
+    if (rc) return rc;
+    int64_t ctas = std::min<int64_t>(kClusterMaxCtas, std::max<int64_t>(1, ceil_div(seg_len, kClusterSlice)));
+    const int64_t len = round_up(ceil_div(seg_len, ctas), 4);
+    ctas = ceil_div(seg_len, len);
+    ContigParams p{x, seg_len, len, (int32_t)ctas, out, nullptr, nullptr, epi};
+    return launched(launch_reduce_cluster(op, p, (int)ctas, s));
+  }
   if (forced > 0) {
     chunks = std::min<int64_t>(forced, ceil_div(seg_len, 4));
   } else if (segments == 1) {

@@ -69,7 +69,18 @@ __global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
     for (int u = 0; u < U; ++u) s[u] = reduce4<Op>(r[u]);
     acc.add(tree_reduce<Op, U>(s));
   }
-  for (; i < nvec; i += S) acc.add(reduce4<Op>(ld_stream4(av + 4 * i)));
+  if (i < nvec) {
+    // The remainder (fewer than U loads per thread) is issued all at once, so
+    // a short chunk costs one memory round trip rather than one per load.
+    float4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i + u * S < nvec) r[u] = ld_stream4(av + 4 * (i + u * S));
+    float s[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) s[u] = i + u * S < nvec ? reduce4<Op>(r[u]) : Op::identity();
+    acc.add(tree_reduce<Op, U>(s));
+  }
   float v = acc.total();
   if (t < head) v = Op::combine(v, Op::prep(a[t]));
   if (t < tail) v = Op::combine(v, Op::prep(av[4 * nvec + t]));

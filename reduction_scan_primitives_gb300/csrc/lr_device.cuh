@@ -165,6 +165,29 @@ __device__ __forceinline__ bool mbar_try_wait_parity(unsigned long long* bar, un
   return ok != 0;
 }
 
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for this block's own bulk or tensor copy (from this GPU's memory) to
+// complete phase `parity` of `bar`.  Such a copy lands within microseconds
+// and depends on no other block, so this wait is bounded by time -- two
+// seconds of the global timer, far beyond any copy -- and not by the
+// adjustable poll limit of the flag waits: a short poll limit (as the timeout
+// tests set) must never let a block leave while its copy still writes into
+// its shared memory.  Returns false only if the copy never completed.
+constexpr unsigned long long kCopyWaitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait_copy(unsigned long long* bar, unsigned parity) {
+  if (mbar_try_wait_parity(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait_parity(bar, parity))
+    if (global_ns() - t0 > kCopyWaitNs) return false;
+  return true;
+}
+
 // Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
 // to shared memory; completion is signalled as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, unsigned bytes,

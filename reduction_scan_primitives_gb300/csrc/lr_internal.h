@@ -30,6 +30,17 @@ struct ContigParams {
   int epi;             // output epilogue (kEpiNone, kEpiMean, kEpiSqrt)
 };
 
+// --- 1D reduction of a short array by one thread-block cluster ---------------
+// CTA r of a cluster of `chunks` CTAs (kClusterThreads threads each) reduces
+// x[r*chunk_len, min((r+1)*chunk_len, seg_len)) with all of its loads in
+// flight at once; CTA 0 combines the CTAs' results in rank order through
+// distributed shared memory and writes out[0].  No scratch, no ticket, one
+// launch.  The host keeps chunk_len <= kClusterThreads * kClusterLoads * 4.
+constexpr int kClusterThreads = 512;
+constexpr int kClusterLoads = 16;   // float4 loads per thread
+constexpr int kClusterMaxCtas = 8;  // the portable cluster size
+constexpr int64_t kClusterMaxN = (int64_t)kClusterMaxCtas * kClusterThreads * kClusterLoads * 4;  // 2^18
+
 // --- Row sums, one warp per row (short rows) -------------------------------
 struct RowsWarpParams {
   const float* x;
@@ -264,6 +275,8 @@ int scan_cols_tile_rows(int variant);
 
 cudaError_t launch_reduce_contig(int variant, int op, const ContigParams& p, int64_t grid,
                                  cudaStream_t s);
+// One cluster of `ctas` CTAs (1..kClusterMaxCtas); p.chunks == ctas.
+cudaError_t launch_reduce_cluster(int op, const ContigParams& p, int ctas, cudaStream_t s);
 cudaError_t launch_reduce_rows_warp(int op, const RowsWarpParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_reduce_cols(int variant, int op, const ColsParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_fill(float* out, int64_t n, float value, cudaStream_t s);

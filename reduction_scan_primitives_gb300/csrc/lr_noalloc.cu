@@ -4,16 +4,18 @@
 // reduce_sum_f32 takes its partial sums and ticket from a workspace the
 // library allocates with cudaMalloc on first use.  Some callers cannot let
 // that happen: code running where device allocation is forbidden or must be
-// accounted for up front (inside a custom allocator, a memory-capped service,
-// or a stream capture in progress).  This entry point runs the same kernel
-// with its scratch in a fixed static device array, so a call allocates
-// nothing.
+// accounted for up front (inside a custom allocator, or a service whose
+// device memory is capped and budgeted before it starts).  This entry point
+// runs the same kernel with its scratch in a fixed static device array, so a
+// call allocates nothing.
 //
 // The array (g_noalloc_scratch) lives in this file.  Host code cannot use its
 // name as a device address, so set-up asks the runtime for the address with
-// cudaGetSymbolAddress, once per device with that device current, and passes
-// it to the kernel.  The first call on a device does this set-up; make that
-// first call before any stream capture.
+// cudaGetSymbolAddress, once per device (and again if that device's context
+// was replaced, e.g. after cudaDeviceReset) with that device current, and
+// passes it to the kernel.  The first call on a device does this set-up; make
+// that first call before any stream capture.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -36,12 +38,13 @@ constexpr int64_t kMinChunkNA = 8192;
 constexpr int64_t kTargetChunkNA = 65536;
 constexpr int kMaxDevicesNA = 64;
 
-// Scratch shared by every call on a device: [ticket | 255 bytes spare |
+// Scratch shared by every call on a device: [ticket (4 B) | 252 bytes spare |
 // partial sums].  Every GPU that loads the library holds it until exit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 struct NoAllocDevice {
   bool ready = false;
+  CUcontext ctx = nullptr;           // the context the address belongs to
   unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
   int64_t slots = 0;                 // resident blocks of the kernel
 };
@@ -49,12 +52,35 @@ struct NoAllocDevice {
 std::mutex g_na_mu;
 NoAllocDevice g_na_dev[kMaxDevicesNA];
 
+// The driver's cuCtxGetCurrent through the runtime (no link against the
+// driver library); null where unavailable.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static const CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  return fn;
+}
+
 // Per-device set-up, with `dev` current: the array's device address and the
-// kernel's occupancy.  Allocates nothing.
+// kernel's occupancy.  A context replaced since (the device was reset) loads
+// the module again, possibly at another address, so set-up runs again then.
+// Allocates nothing.
 int setup(int dev, NoAllocDevice** out) {
   std::lock_guard<std::mutex> lk(g_na_mu);
   NoAllocDevice& d = g_na_dev[dev];
-  if (!d.ready) {
+  CUcontext ctx = nullptr;
+  if (CtxGetCurrentFn get = ctx_get_current()) {
+    if (get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  }
+  if (!d.ready || ctx != d.ctx) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return record_cuda_error(e);
@@ -65,6 +91,7 @@ int setup(int dev, NoAllocDevice** out) {
     if (e != cudaSuccess) return record_cuda_error(e);
     d.scratch = static_cast<unsigned char*>(p);
     d.slots = (int64_t)sms * std::max(1, occ);
+    d.ctx = ctx;
     d.ready = true;
   }
   *out = &d;

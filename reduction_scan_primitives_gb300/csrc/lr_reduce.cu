@@ -28,6 +28,74 @@ namespace lr {
 namespace {
 
 // ---------------------------------------------------------------------------
+// Short 1D arrays: one thread-block cluster, combined in distributed shared
+// memory.  A short sum is bound by latency, not bandwidth: every load of the
+// array is issued at once (one memory round trip), and the CTAs' results meet
+// through the cluster's shared memory instead of a global ticket, so the
+// launch pays no atomic and no second round trip through L2.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned cluster_ctarank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster: release this CTA's shared-memory
+// writes, then wait for all CTAs (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The float at the same shared-memory offset as `local`, in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(const float* local, unsigned rank) {
+  unsigned remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+template <typename Op>
+__global__ void __launch_bounds__(kClusterThreads) k_reduce_cluster(ContigParams p) {
+  constexpr int U = kClusterLoads;
+  constexpr int64_t S = kClusterThreads;
+  __shared__ float sh[kClusterThreads / 32];
+  __shared__ float s_part;
+  const int t = threadIdx.x;
+  const unsigned rank = cluster_ctarank();  // the grid is one cluster
+  const int64_t start = (int64_t)rank * p.chunk_len;
+  const int64_t len = max((int64_t)0, min(p.chunk_len, p.seg_len - start));
+  const float* a = p.x + start;
+  // Peel up to three leading floats so the body is 16-byte aligned.
+  int64_t head = (int64_t)((0u - (unsigned)(uintptr_t)a) & 15u) >> 2;
+  if (head > len) head = len;
+  const int64_t nvec = (len - head) >> 2;  // at most U * S
+  const int tail = (int)((len - head) & 3);
+  const float* av = a + head;
+  float4 r[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (t + u * S < nvec) r[u] = ld_stream4(av + 4 * (t + u * S));
+  float sv[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) sv[u] = t + u * S < nvec ? reduce4<Op>(r[u]) : Op::identity();
+  float v = tree_reduce<Op, U>(sv);
+  if (t < head) v = Op::combine(v, Op::prep(a[t]));
+  if (t < tail) v = Op::combine(v, Op::prep(av[4 * nvec + t]));
+  v = block_reduce<Op, kClusterThreads>(v, sh);
+  if (t == 0) s_part = v;
+  cluster_sync();
+  if (rank == 0 && t < 32) {
+    float q = t < p.chunks ? ld_cluster_f32(&s_part, (unsigned)t) : Op::identity();
+    q = warp_reduce<Op>(q);  // the CTAs' results in a fixed tree
+    if (t == 0) p.out[0] = finish(q, p.epi, p.seg_len);
+  }
+  cluster_sync();  // every CTA's shared memory stays alive until CTA 0 has read it
+}
+
+// ---------------------------------------------------------------------------
 // Short rows: one warp per row, rows strided over the grid.
 // ---------------------------------------------------------------------------
 template <typename Op>
@@ -297,6 +365,36 @@ cudaError_t launch_reduce_contig(int variant, int op, const ContigParams& p, int
     case kOpSumSq: return contig_op<OpSumSq>(variant, p, g, s);
     case kOpMax: return contig_op<OpMax>(variant, p, g, s);
     case kOpMin: return contig_op<OpMin>(variant, p, g, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename Op>
+cudaError_t cluster_op(const ContigParams& p, int ctas, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kClusterThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_reduce_cluster<Op>, p);
+}
+
+cudaError_t launch_reduce_cluster(int op, const ContigParams& p, int ctas, cudaStream_t s) {
+  if (ctas < 1 || ctas > kClusterMaxCtas || p.chunks != ctas ||
+      p.chunk_len > (int64_t)kClusterThreads * kClusterLoads * 4)
+    return cudaErrorInvalidValue;
+  switch (op) {
+    case kOpSum: return cluster_op<OpSum>(p, ctas, s);
+    case kOpSumSq: return cluster_op<OpSumSq>(p, ctas, s);
+    case kOpMax: return cluster_op<OpMax>(p, ctas, s);
+    case kOpMin: return cluster_op<OpMin>(p, ctas, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -540,14 +540,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
     // The copy's layout: shared element jj is tv.x[jj], whatever the direction.
     const TileView tv = tile_view(row_view<4, EDGES>(p.x, nullptr, row, p.N), (tiles - 1 - k) * TILE, TILE,
                                   (p.flags & kScanMirror) != 0);
-    bool loaded = true;
-    if (!EDGES || tv.len > 0)
-      for (int64_t it = 0; !mbar_try_wait_parity(&s_bar, 0u); ++it)
-        if (it >= p.spin_limit) {
-          loaded = false;
-          break;
-        }
-    if (!loaded) s_fail = 1;
+    // The copy of this tile (time-bounded wait, independent of the poll limit).
+    if ((!EDGES || tv.len > 0) && !mbar_wait_copy(&s_bar, 0u)) s_fail = 1;
     float e[SUB];
 #pragma unroll
     for (int s = 0; s < SUB; ++s) {
@@ -592,11 +586,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
         if (fail && lane == 0) s_fail = 1;
       }
     }
-    // A copy whose wait gave up may still be in flight: wait once more
-    // (bounded) before the block's shared memory is released.
-    if (!loaded && t == 0)
-      for (int64_t it = 0; !mbar_try_wait_parity(&s_bar, 0u) && it < p.spin_limit; ++it) {
-      }
   }
   if constexpr (EARLY) write_out();
   __syncthreads();

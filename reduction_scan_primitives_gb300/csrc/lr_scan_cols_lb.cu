@@ -369,16 +369,12 @@ __global__ void __launch_bounds__(kLbThreads, 32 / kNW) k_scan_cols_lookback(
   }
 
   // ---- 5. sum tile `ticket`, publish it and the group sums it completes ----
-  bool loaded = true;
   if (ticket < total) {
     if constexpr (kTma) {
       // The whole box, zeros outside the tensor: every thread sums its rows.
-      for (int64_t it = 0; !mbar_try_wait_parity(&s_bar, 0u); ++it)
-        if (it >= p.spin_limit) {
-          loaded = false;
-          fail = true;
-          break;
-        }
+      // The copy is waited for with a time bound independent of the poll
+      // limit, so the block never leaves while it is in flight.
+      if (!mbar_wait_copy(&s_bar, 0u)) fail = true;
       rows_t = R;
       cok_t = true;
     } else {
@@ -454,11 +450,6 @@ __global__ void __launch_bounds__(kLbThreads, 32 / kNW) k_scan_cols_lookback(
     atomicOr(p.err_word, 1u);
     atomicExch(p.err_word + 1, epoch);
   }
-  // A copy whose wait gave up may still be in flight: wait once more
-  // (bounded) before the block's shared memory is released.
-  if (kTma && !loaded)
-    for (int64_t it = 0; !mbar_try_wait_parity(&s_bar, 0u) && it < p.spin_limit; ++it) {
-    }
 }
 
 }  // namespace

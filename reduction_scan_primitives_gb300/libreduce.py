@@ -322,11 +322,15 @@ def cumsum_f32(x: torch.Tensor, dim: int = -1, reverse: bool = False, exclusive:
     return out
 
 
-def _ws_ptr(ws):
+def _ws_ptr(ws, device=None):
     if ws is None:
         return None
     if not isinstance(ws, torch.Tensor) or ws.device.type != "cuda":
         raise ValueError("the workspace must be a CUDA tensor")
+    if device is not None and ws.device != device:
+        raise ValueError("the workspace must be on x's device")
+    if not ws.is_contiguous():
+        raise ValueError("the workspace must be contiguous")
     return ws.data_ptr()
 
 
@@ -343,13 +347,18 @@ def reduce_axis_op_ws_f32(x: torch.Tensor, dim: int, op="sum", ws: torch.Tensor 
     outer, reduce, inner = canonical_axis(x.shape, dim)
     if out is None:
         shape = list(x.shape)
-        del shape[dim % x.dim()]
+        if x.dim():
+            del shape[dim % x.dim()]
         out = torch.empty(shape, dtype=torch.float32, device=x.device)
+    else:
+        _check_tensor(out, "out")
+        if out.numel() != outer * inner or out.device != x.device:
+            raise ValueError("out has the wrong size or device")
     nbytes = _ws_nbytes(ws)
     lib = load()
     with _on(x.device):
         st = lib.reduce_axis_op_ws_f32(x.data_ptr(), outer, reduce, inner, out.data_ptr(), _op_code(op),
-                                       _ws_ptr(ws), ctypes.byref(nbytes), _stream_ptr(x.device))
+                                       _ws_ptr(ws, x.device), ctypes.byref(nbytes), _stream_ptr(x.device))
     _raise_on("reduce_axis_op_ws_f32", st)
     return int(nbytes.value) if ws is None else out
 
@@ -358,14 +367,20 @@ def cumsum_ws_f32(x: torch.Tensor, dim: int = -1, reverse: bool = False, exclusi
                   ws: torch.Tensor | None = None, out: torch.Tensor | None = None):
     """cumsum_f32 with caller scratch (see reduce_axis_op_ws_f32)."""
     _check_tensor(x, "x")
+    if x.dim() == 0:
+        raise ValueError("x must have at least one dim")
     outer, N, inner = canonical_axis(x.shape, dim)
     if out is None:
         out = torch.empty_like(x)
+    else:
+        _check_tensor(out, "out")
+        if out.shape != x.shape or out.device != x.device:
+            raise ValueError("out must have x's shape and device")
     flags = (SCAN_REVERSE if reverse else 0) | (SCAN_EXCLUSIVE if exclusive else 0)
     nbytes = _ws_nbytes(ws)
     lib = load()
     with _on(x.device):
-        st = lib.cumsum_ws_f32(x.data_ptr(), outer, N, inner, out.data_ptr(), flags, _ws_ptr(ws),
+        st = lib.cumsum_ws_f32(x.data_ptr(), outer, N, inner, out.data_ptr(), flags, _ws_ptr(ws, x.device),
                                ctypes.byref(nbytes), _stream_ptr(x.device))
     _raise_on("cumsum_ws_f32", st)
     return int(nbytes.value) if ws is None else out

@@ -135,3 +135,23 @@ def test_segmented_column_scan_ws_matches_default(shape, reverse, exclusive):
         L.check_ws(ws)
         assert bitwise_equal(got, ref), shape
     L.check()
+
+
+def test_binding_rejects_bad_out_and_workspace():
+    """The workspace forms check `out` and `ws` in Python as the other
+    bindings do: a wrong size, dtype, device or layout raises before any call."""
+    x = on_device(inputs.make((64, 300), "uniform01", 2))
+    with pytest.raises(ValueError):
+        L.reduce_axis_op_ws_f32(x, 1, "sum", out=torch.empty(63, device="cuda"))
+    with pytest.raises(TypeError):
+        L.reduce_axis_op_ws_f32(x, 1, "sum", out=torch.empty(64, dtype=torch.float64, device="cuda"))
+    with pytest.raises(ValueError):
+        L.reduce_axis_op_ws_f32(x, 1, "sum", out=torch.empty(64))
+    with pytest.raises(ValueError):
+        L.cumsum_ws_f32(x, 1, out=torch.empty(64, 299, device="cuda"))
+    with pytest.raises(ValueError):
+        L.cumsum_ws_f32(x, 1, out=torch.empty(300, 64, device="cuda").t())
+    with pytest.raises(ValueError):
+        L.cumsum_ws_f32(x, 1, ws=torch.empty(4096, dtype=torch.uint8))
+    ok = L.cumsum_ws_f32(x, 1, ws=L.workspace(L.cumsum_ws_f32(x, 1)))
+    assert ok.shape == x.shape
