@@ -51,7 +51,9 @@ NEXT_WORKLOADS = ["cumsum_fwd_32768x32768", "cumsum_fwd_excl_1x1e9", "cumsum_128
                   "cumsum_64x16384x1024_d1", "cumsum_2x8192x4096_d1", "cumsum_1024x8192x64_d1",
                   "sum_16x1000000x12_d1", "rcumsum_1x1e9_rts",
                   "max_1e9", "norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0",
-                  "rcumsum_1x1e9_ws", "axis_65536x4096_d0_ws", "rcumsum_2000000x100", "sum_4000000x32_d1"]
+                  "rcumsum_1x1e9_ws", "axis_65536x4096_d0_ws", "rcumsum_2000000x100", "sum_4000000x32_d1",
+                  "cumsum_100000x100x3_d1", "sum_100000x100x3_d1", "cumsum_4096x4096x2_d1",
+                  "cumsum_1x40000000x4_d1"]
 # Small cases of each kernel for ncu captures: larger than L2, a few GB at most.
 PROFILE_CASES = {
     "sum_2e8": dict(op="sum", shape=(200_000_000,), dist="uniform01", seed=42),
@@ -70,6 +72,11 @@ PROFILE_CASES = {
     "cumsum_2x8192x4096_d1": dict(inputs.WORKLOADS["cumsum_2x8192x4096_d1"]),
     "rcumsum_2000000x100": dict(inputs.WORKLOADS["rcumsum_2000000x100"]),
     "sum_4000000x32_d1": dict(inputs.WORKLOADS["sum_4000000x32_d1"]),
+    "cumsum_100000x100x3_d1": dict(inputs.WORKLOADS["cumsum_100000x100x3_d1"]),
+    "sum_100000x100x3_d1": dict(inputs.WORKLOADS["sum_100000x100x3_d1"]),
+    "cumsum_4096x4096x2_d1": dict(inputs.WORKLOADS["cumsum_4096x4096x2_d1"]),
+    "cumsum_1x40000000x4_d1": dict(inputs.WORKLOADS["cumsum_1x40000000x4_d1"]),
+    "sum_1e5": dict(op="sum", shape=(100_000,), dist="uniform01", seed=42),
 }
 FALLBACK_HBM_GBS = 6800.0
 # Context only (another machine): the page's T4 figures for the 1D sum.
@@ -291,10 +298,50 @@ def time_next(device, reps=20):
     return res
 
 
+def _graph_per_launch_us(calls, device):
+    """Device time per launch of `calls` (one graph, replayed after a warm
+    replay), timed with CUDA events around the replay."""
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        for c in calls[:3]:
+            c()
+    torch.cuda.current_stream(device).wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+    g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        t = a.elapsed_time(b) * 1e3 / len(calls)
+        best = t if best is None else min(best, t)
+    del g
+    return best
+
+
 def time_sweep(device, reps=10):
-    """1D sum sweep n = 1e4 .. 1e9, L2 flushed before every timed launch."""
+    """1D sum sweep n = 1e4 .. 1e9, L2 cold for every launch.
+
+    ms: CUDA events around one launch, after writing and reading a buffer
+    larger than L2.  This GPU's event timestamps advance in steps of 2.048 us,
+    and two events with nothing between them read about 2 us apart, so below
+    ~1e7 elements this is coarse.  us_graph: for n <= 1e7, the same call
+    captured K times in one CUDA graph, launch k reading slice k of a pool
+    larger than 4x L2 (so no launch finds its input in L2), replayed and timed
+    with events: device time per launch, no host cost and no event step.
+    GB/s is taken from us_graph where present."""
     from reduction_scan_primitives_gb300 import libreduce as L
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    pool_floats = (5 * l2) // 4 + (1 << 20)
     res = {}
     peak, _ = hbm_peak()
     for n in inputs.SUM_SWEEP:
@@ -315,23 +362,34 @@ def time_sweep(device, reps=10):
             b.synchronize()
             times.append(a.elapsed_time(b))
         ms = statistics.median(times)
-        gbs = (4 * n + 4) / (ms * 1e-3) / 1e9
-        res[str(n)] = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        entry = {"ms": round(ms, 5)}
+        seconds = ms * 1e-3
+        if n <= 10_000_000:
+            k = max(8, -(-pool_floats // n))
+            pool = torch.empty(k * n, dtype=torch.float32, device=device)
+            pool.uniform_()
+            outs = torch.empty(k, dtype=torch.float32, device=device)
+            calls = [(lambda i=i: L.reduce_sum_f32(pool[i * n:(i + 1) * n], out=outs[i])) for i in range(k)]
+            us = _graph_per_launch_us(calls, device)
+            entry.update({"us_graph": round(us, 3), "graph_launches": k})
+            seconds = us * 1e-6
+            del pool, outs, calls
+        gbs = (4 * n + 4) / seconds / 1e9
+        entry.update({"GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)})
+        res[str(n)] = entry
         del x
     del flush
+    L.check(device)
     return res
 
 
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample of each workload.
 # ---------------------------------------------------------------------------
-def oracle_run(name, x_dev):
+def oracle_run(name, xs):
     """(callable running the oracle on the whole workload, its algorithmic bytes)."""
-    import numpy as np
-
     import oracle
     w = workload_spec(name)
-    xs = np.ascontiguousarray(x_dev.cpu().numpy())
     if w["op"] == "sum":
         return (lambda: oracle.sum1d(xs)), 4 * xs.size + 4
     if w["op"] == "axis":
@@ -341,19 +399,48 @@ def oracle_run(name, x_dev):
     return (lambda: oracle.reverse_cumsum(xs, rows, n)), 8 * xs.size
 
 
+def threaded_run(name, xs):
+    """The all-core fp64 baseline (cpu_baseline/) on the whole workload."""
+    import cpu_baseline
+    w = workload_spec(name)
+    if w["op"] == "sum":
+        return lambda: cpu_baseline.sum1d(xs)
+    if w["op"] == "axis":
+        o, r, i = inputs.canonical_axis(w["shape"], w["dim"])
+        return lambda: cpu_baseline.axis_sum(xs, o, r, i)
+    rows, n = w["shape"]
+    return lambda: cpu_baseline.reverse_cumsum(xs, rows, n)
+
+
 def cpu_baseline(data):
-    """The oracle, single-threaded, over every workload of one step, once."""
-    total_bytes, total_s = 0, 0.0
+    """Two CPU figures over every workload of one step, once, on this host:
+    the oracle (single-threaded fp64, the parity reference) and the all-core
+    fp64 baseline (threads over independent outputs or row segments)."""
+    import numpy as np
+
+    import cpu_baseline as cb
+    cb.build()
+    total_bytes, t_oracle, t_threads = 0, 0.0, 0.0
     for name in STEP_WORKLOADS:
-        fn, nbytes = oracle_run(name, data[name][0])
+        xs = np.ascontiguousarray(data[name][0].cpu().numpy())
+        fn, nbytes = oracle_run(name, xs)
         t0 = time.perf_counter()
         fn()
-        total_s += time.perf_counter() - t0
-        total_bytes += nbytes
+        t_oracle += time.perf_counter() - t0
         del fn
-    return {"value": round(total_bytes / total_s / 1e9, 3), "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "sample": "one step: every workload in full, once (host copy of the "
-            "device inputs)", "seconds": round(total_s, 2)}
+        fn = threaded_run(name, xs)
+        t0 = time.perf_counter()
+        fn()
+        t_threads += time.perf_counter() - t0
+        total_bytes += nbytes
+        del fn, xs
+    model = cb.cpu_model()
+    return {"value": round(total_bytes / t_oracle / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "one step: every workload in full, once (host copy of the device inputs)",
+            "seconds": round(t_oracle, 2), "cpu_model": model,
+            "threaded": {"value": round(total_bytes / t_threads / 1e9, 3), "unit": "GB/s", "cores": cb.cores(),
+                         "kind": "fp64 on every core (fp32 in and out; independent outputs or row "
+                                 "segments per thread)", "seconds": round(t_threads, 3), "cpu_model": model}}
 
 
 # ---------------------------------------------------------------------------

@@ -301,7 +301,11 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *                                 float4 columns (needs inner % 4 == 0, aligned x);
  *                                 6, 7 the narrow-row kernel, a block or a warp per plane
  *                                 (inner <= 32 scalar or 128 float4 columns: the
- *                                 automatic choice there)
+ *                                 automatic choice there); 8 chunks of whole narrow
+ *                                 planes (reduce <= 2048, inner <= 256, a plane in
+ *                                 24 KB of shared memory), each column reduced as a
+ *                                 short row (the automatic choice for planes of at
+ *                                 most 768 floats)
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
  *                                 2 float4 x 4 (float4 needs x and y at the same
  *                                 offset mod 16 bytes; any N)
@@ -318,7 +322,11 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *                                 5 the single-pass look-back over 256-row x 32-column
  *                                 tiles (the automatic choice where one block per
  *                                 (o, column tile) cannot fill the GPU; falls back to
- *                                 the automatic choice when its tiles exceed 262144)
+ *                                 the automatic choice when its tiles exceed 262144);
+ *                                 6 chunks of whole narrow planes (N <= 2048,
+ *                                 inner <= 256, a plane in 24 KB of shared memory),
+ *                                 each column scanned as a short row (the automatic
+ *                                 choice wherever a plane fits)
  *                                 (float4 columns need inner % 4 == 0 and aligned x, y) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6

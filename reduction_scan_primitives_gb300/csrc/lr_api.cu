@@ -337,11 +337,15 @@ int run_contig(const Provider& pv, const float* x, int64_t segments, int64_t seg
   const int64_t waves = g_opt_waves.load();
   int64_t chunks = 1;
   const int64_t forced = g_opt_axis_split.load();
-  if (segments == 1 && seg_len <= kClusterMaxN && forced <= 0 && waves <= 0 &&
+  if (segments == 1 && seg_len > kClusterSlice && seg_len <= kClusterMaxN && forced <= 0 && waves <= 0 &&
       g_opt_contig_variant.load() < 0) {
     // A short array: one cluster of CTAs, about kClusterSlice floats each
     // (all of a CTA's loads in one round trip), combined in distributed
-    // shared memory: one launch, no scratch, no ticket.
+    // shared memory: one launch, no scratch, no ticket.  Up to kClusterSlice
+    // floats one plain block does it (below, chunks == 1), which launches
+    // faster than a cluster (measured per launch in a graph: 1.95 against
+    // 2.7 us at 1e4; at 1e5 the cluster takes 2.95 against 3.54 us for 12
+    // blocks and a ticket).
     Scratch sc;
     int rc = acquire(pv, Need{}, &sc, s);
     if (rc) return rc;
@@ -363,6 +367,7 @@ int run_contig(const Provider& pv, const float* x, int64_t segments, int64_t seg
                                                            (kTargetChunk * slots));
     chunks = w * slots;
     chunks = std::min(chunks, std::max<int64_t>(1, seg_len / kMinChunk));
+    if (seg_len <= kClusterSlice && waves <= 0) chunks = 1;  // one block, one round trip, no ticket
   } else if (segments < 4 * slots) {
     // Too few rows to fill the GPU: cut each into chunks.
     chunks = ceil_div(4 * slots, segments);
@@ -390,6 +395,12 @@ int run_contig(const Provider& pv, const float* x, int64_t segments, int64_t seg
 
 int run_rows_short(const Provider& pv, const float* x, int64_t rows, int64_t N, float* out, int op, int epi,
                    cudaStream_t s);
+// Reductions of narrow planes by the short-row kernels (defined with them
+// below); kNoPlanes when the planes do not fit a chunk.
+constexpr int kNoPlanes = -3;  // distinct from kQueried and kColLbNoFit
+constexpr int64_t kShortPlaneInnerMax = 256;  // widest plane the short-row kernels take
+int try_reduce_short_planes(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
+                            float* out, int op, int epi, bool forced, cudaStream_t s);
 
 int run_rows_warp(const Provider& pv, const float* x, int64_t rows, int64_t len, float* out, int op,
                   int epi, cudaStream_t s) {
@@ -467,6 +478,11 @@ int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, 
     int vec = 1;
     const int64_t fv = g_opt_cols_variant.load();
     const bool wide_forced = op == kOpSum && fv >= 0 && fv < kNumColsVariants;
+    if ((fv < 0 || fv == kColsShortPlanes) && g_opt_axis_split.load() <= 0) {
+      // Narrow planes of at most kShortRowMax rows, many to a chunk.
+      const int rc = try_reduce_short_planes(pv, x, outer, reduce, inner, out, op, epi, fv == kColsShortPlanes, s);
+      if (rc != kNoPlanes) return rc;
+    }
     if (narrow_rows(x, x, inner, &vec) && !wide_forced) {
       // Many small planes: a warp per plane; otherwise a block per (plane, slice).
       const bool warp_form = inner <= 32 * vec && (fv == kColsNarrowWarp ||
@@ -778,8 +794,89 @@ int run_rscan_short(const Provider& pv, const float* x, int64_t rows, int64_t N,
   Scratch sc;
   int rc = acquire(pv, Need{}, &sc, s);
   if (rc) return rc;
-  ShortRowsParams p{x, y, rows, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, flags};
+  ShortRowsParams p{x, y, rows, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, flags, 1, 0};
   return launched(launch_rscan_short(q.lanes, f.vec, p, short_grid(pv.st, rows, q), s));
+}
+
+// Narrow planes ([outer, N, inner] along N, N <= kShortRowMax): the short-row
+// kernels over chunks of whole planes, each staged transposed so that every
+// column is a row of N (see lr_rows_short.cu).  The plan is the rows' plan
+// for rows of N, its chunk counted in planes (inner rows each) and kept inside
+// the shared memory.  ok == false: not even one plane fits.  (A form that
+// staged planes in their own layout, a column read `inner` floats apart,
+// raised an illegal-address fault on its first 16-byte-load case; the cause
+// was not found, and that form is not used.)
+struct PlaneForm {
+  ShortForm f;
+  bool ok;
+};
+PlaneForm plane_form(int64_t N, int64_t inner, int64_t solo, int64_t solo_odd, bool aligned16) {
+  PlaneForm r{short_form(N, solo, solo_odd, false), false};
+  ShortPlan& q = r.f.q;
+  if (N > kShortRowMax || inner < 2 || inner > kShortPlaneInnerMax) return r;
+  int64_t planes = std::max<int64_t>(1, std::min<int64_t>(q.rows_per_chunk / inner, kShortChunk / (N * inner)));
+  while (planes > 1 && planes * inner * q.stride > kShortSmem) --planes;
+  if (planes * inner * q.stride > kShortSmem) return r;
+  // Chunks of whole 128-byte lines where the planes allow (see short_plan).
+  int64_t a = N * inner, b = 32;
+  while (b) {
+    const int64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  const int64_t line_planes = 32 / a;
+  if (planes >= line_planes) planes -= planes % line_planes;
+  q.rows_per_chunk = (int)planes;
+  r.f.vec = aligned16 && (N * inner) % 4 == 0 ? kShortLd4 : kShortLd1;
+  r.ok = true;
+  return r;
+}
+int64_t plane_grid(const DeviceState* st, int64_t planes, const ShortPlan& q) {
+  return std::max<int64_t>(1, std::min<int64_t>(ceil_div(planes, q.rows_per_chunk),
+                                                4 * (int64_t)st->sm_count * st->occ_rscan_short));
+}
+unsigned long long magic_of(int64_t d) { return ((1ull << 32) + (unsigned long long)d - 1) / (unsigned long long)d; }
+
+int run_scan_short_planes(const Provider& pv, const PlaneForm& pf, const float* x, int64_t outer, int64_t N,
+                          int64_t inner, float* y, cudaStream_t s, int flags) {
+  const ShortPlan& q = pf.f.q;
+  Scratch sc;
+  int rc = acquire(pv, Need{}, &sc, s);
+  if (rc) return rc;
+  ShortRowsParams p{x, y, outer, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, flags, (int)inner,
+                    magic_of(inner)};
+  return launched(launch_rscan_short(q.lanes, pf.f.vec, p, plane_grid(pv.st, outer, q), s));
+}
+
+int run_reduce_short_planes(const Provider& pv, const PlaneForm& pf, const float* x, int64_t outer, int64_t N,
+                            int64_t inner, float* out, int op, int epi, cudaStream_t s);
+
+// The automatic choice: planes of at most kShortReducePlaneMax floats; above
+// that a warp per plane (or the narrow block kernel) is ahead.  Measured
+// (fraction of copy bandwidth, planes against a warp per plane): [400000,
+// 100, 3] 0.59 / 0.55, [1e6, 16, 8] 0.67 / 0.21, [100000, 33, 16] 0.57 /
+// 0.47; [50000, 512, 2] 0.58 / 0.84, [20000, 1024, 3] 0.60 / 0.73.  `forced`
+// takes any plane that fits the shared memory.
+constexpr int64_t kShortReducePlaneMax = 768;
+int try_reduce_short_planes(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
+                            float* out, int op, int epi, bool forced, cudaStream_t s) {
+  if (N > kShortRowMax || inner < 2 || inner > kShortPlaneInnerMax || (!forced && N * inner > kShortReducePlaneMax))
+    return kNoPlanes;
+  const PlaneForm pf = plane_form(N, inner, kShortReduceSolo, kShortReduceSoloOdd,
+                                  (reinterpret_cast<uintptr_t>(x) & 15u) == 0);
+  if (!pf.ok) return kNoPlanes;
+  return run_reduce_short_planes(pv, pf, x, outer, N, inner, out, op, epi, s);
+}
+
+int run_reduce_short_planes(const Provider& pv, const PlaneForm& pf, const float* x, int64_t outer, int64_t N,
+                            int64_t inner, float* out, int op, int epi, cudaStream_t s) {
+  const ShortPlan& q = pf.f.q;
+  Scratch sc;
+  int rc = acquire(pv, Need{}, &sc, s);
+  if (rc) return rc;
+  ShortRowsParams p{x, out, outer, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, epi, (int)inner,
+                    magic_of(inner)};
+  return launched(launch_reduce_short(op, q.lanes, pf.f.vec, p, plane_grid(pv.st, outer, q), s));
 }
 
 // Reductions of many short rows (inner == 1, reduce <= kShortRowMax) with the
@@ -791,7 +888,7 @@ int run_rows_short(const Provider& pv, const float* x, int64_t rows, int64_t N, 
   Scratch sc;
   int rc = acquire(pv, Need{}, &sc, s);
   if (rc) return rc;
-  ShortRowsParams p{x, out, rows, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, epi};
+  ShortRowsParams p{x, out, rows, (int)N, q.rows_per_chunk, q.stride, q.run, q.magic, epi, 1, 0};
   return launched(launch_reduce_short(op, q.lanes, f.vec, p, short_grid(pv.st, rows, q), s));
 }
 
@@ -893,7 +990,21 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
   {
     int nvec = 1;
     const int64_t fv = g_opt_scan_cols_variant.load();
-    if (narrow_rows(x, y, inner, &nvec) && (fv < 0 || fv == kScanColsNarrow || fv == kScanColsNarrowWarp)) {
+    if ((fv < 0 || fv == kScanColsShortPlanes) && g_opt_axis_split.load() <= 0 && N <= kShortRowMax &&
+        inner <= kShortPlaneInnerMax) {
+      // Narrow planes of at most kShortRowMax rows, whole planes to a chunk:
+      // ahead of the narrow kernels wherever a plane fits (fraction of copy
+      // bandwidth, planes against the better narrow form: [400000, 100, 3]
+      // 0.52 / 0.26, [50000, 512, 2] 0.54 / 0.40, [12000, 2048, 2] 0.49 /
+      // 0.46, [30000, 100, 32] 0.53 / 0.45).
+      const PlaneForm pf = plane_form(N, inner, kShortScanSolo, kShortScanSoloOdd,
+                                      ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0);
+      if (pf.ok)
+        return run_scan_short_planes(pv, pf, x, outer, N, inner, y, s,
+                                     (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0));
+    }
+    if (narrow_rows(x, y, inner, &nvec) &&
+        (fv < 0 || fv == kScanColsNarrow || fv == kScanColsNarrowWarp || fv == kScanColsShortPlanes)) {
       // The block form walks tiles of T rows; a plane of fewer than T/2 rows
       // would leave most of its threads idle: a warp per plane instead
       // (measured on [100000, 100, 3]: 25% against 4% of copy bandwidth; on
@@ -1236,7 +1347,7 @@ int libreduce_set_option(int option, int64_t value) {
       g_opt_contig_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_COLS_VARIANT:
-      if (value < -1 || value > kColsNarrowWarp) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < -1 || value > kColsShortPlanes) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_RSCAN_VARIANT:
@@ -1244,7 +1355,7 @@ int libreduce_set_option(int option, int64_t value) {
       g_opt_rscan_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_SCAN_COLS_VARIANT:
-      if (value < -1 || value > kScanColsLookback) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < -1 || value > kScanColsShortPlanes) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_ROWS_FORM:

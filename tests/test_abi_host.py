@@ -139,10 +139,12 @@ def test_options(lib):
                      (L.OPT_RSCAN_VARIANT, -1), (L.OPT_WAVES, 0), (L.OPT_LOOKBACK_LAG, 0),
                      (L.OPT_SCAN_COLS_VARIANT, -1)):
         assert lib.libreduce_set_option(opt, val) == L.OK
-    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 5) == L.OK
-    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 6) == L.ERR_INVALID_ARG
+    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 6) == L.OK
+    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 7) == L.ERR_INVALID_ARG
     assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, -1) == L.OK
-    assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 8) == L.ERR_INVALID_ARG
+    assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 8) == L.OK
+    assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 9) == L.ERR_INVALID_ARG
+    assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, -1) == L.OK
     for v in (0, 1, 2):
         assert lib.libreduce_set_option(L.OPT_ROWS_FORM, v) == L.OK
     assert lib.libreduce_set_option(L.OPT_ROWS_FORM, 3) == L.ERR_INVALID_ARG
@@ -177,3 +179,14 @@ def test_product_path_never_imports_the_oracle():
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "oracle.h" not in text, f
+
+
+def test_short_row_index_division_is_exact():
+    """The short-row kernels divide a chunk index e by a row length or a plane
+    width d with a multiply and a shift, (e * ceil(2^32 / d)) >> 32; that is
+    e // d for every index a chunk holds and every d they are given."""
+    import numpy as np
+    e = np.arange(0, 8192, dtype=np.uint64)
+    for d in range(1, 4097):
+        magic = np.uint64(((1 << 32) + d - 1) // d)
+        assert np.array_equal((e * magic) >> np.uint64(32), e // np.uint64(d)), d

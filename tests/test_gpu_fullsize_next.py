@@ -210,3 +210,26 @@ def test_short_rows_full_size():
     L.check()
     ref, scale = oracle.axis_sum(x.cpu().numpy(), rows, n, 1)
     assert_close(s.cpu().numpy(), ref[:, 0], scale[:, 0], "short rows sum")
+
+
+@pytest.mark.parametrize("name", ["cumsum_100000x100x3_d1", "cumsum_4096x4096x2_d1", "cumsum_1x40000000x4_d1"])
+def test_narrow_plane_scans_every_output(name):
+    """The bench's narrow-plane scans at full size, every output against the
+    oracle, and a rerun bit for bit."""
+    w, x = workload(name)
+    outer, n, inner = w["shape"]
+    y = L.cumsum_f32(x, 1, reverse=w["reverse"], exclusive=w["exclusive"]).clone()
+    again = L.cumsum_f32(x, 1, reverse=w["reverse"], exclusive=w["exclusive"])
+    L.check()
+    assert bitwise_equal(y, again)
+    ref, scale = oracle.cumsum(x.cpu().numpy(), outer, n, inner, w["reverse"], w["exclusive"])
+    assert_close(y.cpu().numpy(), ref, scale, name)
+
+
+def test_narrow_plane_sum_every_output():
+    w, x = workload("sum_100000x100x3_d1")
+    outer, n, inner = w["shape"]
+    out = L.reduce_axis_op_f32(x, 1, "sum")
+    L.check()
+    ref, scale = oracle.axis_sum(x.cpu().numpy(), outer, n, inner)
+    assert_close(out.cpu().numpy(), ref, scale, "sum [100000, 100, 3]")
