@@ -333,10 +333,12 @@ def time_sweep(device, reps=10):
     ms: CUDA events around one launch, after writing and reading a buffer
     larger than L2.  This GPU's event timestamps advance in steps of 2.048 us,
     and two events with nothing between them read about 2 us apart, so below
-    ~1e7 elements this is coarse.  us_graph: for n <= 1e7, the same call
+    ~1e7 elements this is coarse.  us_graph: for n <= 1e8, the same call
     captured K times in one CUDA graph, launch k reading slice k of a pool
     larger than 4x L2 (so no launch finds its input in L2), replayed and timed
     with events: device time per launch, no host cost and no event step.
+    Applied up to 1e8 elements (whose single-launch time is still only ~30
+    event steps).
     GB/s is taken from us_graph where present."""
     from reduction_scan_primitives_gb300 import libreduce as L
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
@@ -364,7 +366,7 @@ def time_sweep(device, reps=10):
         ms = statistics.median(times)
         entry = {"ms": round(ms, 5)}
         seconds = ms * 1e-3
-        if n <= 10_000_000:
+        if n <= 100_000_000:
             k = max(8, -(-pool_floats // n))
             pool = torch.empty(k * n, dtype=torch.float32, device=device)
             pool.uniform_()

@@ -326,7 +326,12 @@ LIBREDUCE_API int64_t libreduce_launch_count(void);
  *                                 6 chunks of whole narrow planes (N <= 2048,
  *                                 inner <= 256, a plane in 24 KB of shared memory),
  *                                 each column scanned as a short row (the automatic
- *                                 choice wherever a plane fits)
+ *                                 choice wherever a plane fits); 7 planes of 2 or 4
+ *                                 columns read flat as rows (x and y at the same
+ *                                 offset mod 16 bytes), each column a class of
+ *                                 every 2nd or 4th element, by the row kernels
+ *                                 (the automatic choice for 2-column planes of at
+ *                                 least 4096 floats)
  *                                 (float4 columns need inner % 4 == 0 and aligned x, y) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6

@@ -53,7 +53,12 @@ struct DeviceState {
   int occ_scan_narrow_warp[2] = {};       // [vec4]
   int occ_scan_cols_lb = 0;
   int occ_rscan_short = 0;
+  int occ_rscan_period[3] = {};     // float4 block per row, period 1, 2, 4
+  int occ_lookback_period[3] = {};  // L2 look-back, period 1, 2, 4
 };
+
+// Index of a period (1, 2, 4) in the per-period tables.
+int period_slot(int period) { return period == 4 ? 2 : period == 2 ? 1 : 0; }
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -106,6 +111,10 @@ int device_state(DeviceState** out, int* dev_out) {
       st.occ_scan_narrow_warp[v4] = std::max(1, occupancy_scan_narrow_warp(v4 ? 4 : 1));
     }
     st.occ_scan_cols_lb = std::max(1, occupancy_scan_cols_lookback());
+    for (int pi = 0; pi < 3; ++pi) {
+      st.occ_rscan_period[pi] = std::max(1, occupancy_rscan_rows_period(1 << pi));
+      st.occ_lookback_period[pi] = std::max(1, occupancy_rscan_lookback_period(1 << pi));
+    }
     st.occ_rscan_short = std::max(1, occupancy_rscan_short());
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
@@ -231,6 +240,7 @@ int launched(cudaError_t e) {
 // ---------------------------------------------------------------------------
 constexpr int64_t kMinChunk = 8192;         // floats per block, lower bound
 constexpr int64_t kClusterSlice = 16384;    // floats per CTA of a short 1D array (one cluster)
+constexpr int64_t kPeriodRowsMin = 4096;    // planes of 2 or 4 columns from this many floats: flat rows
 constexpr int64_t kTargetChunk = 65536;     // floats per block of a long 1D sum (256 KiB)
 constexpr int64_t kRowsWarpMaxLen = 2048;   // rows up to this length: one warp per row
 constexpr int64_t kShortReduceMax = 128;    // rows up to this length: staged chunks (automatic choice;
@@ -625,8 +635,8 @@ constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): we
 // 768, 94-96% at 1024, 87% at 1280, 76% at 1536: 5/3 of the resident blocks.
 // The forward scan publishes first and reaches 92% at 640-768 (89% at 1024):
 // 5/4 of the resident blocks.  Both in steps of 64.
-int64_t lookback_lag(const DeviceState* st, bool mirror) {
-  const int64_t resident = (int64_t)st->sm_count * st->occ_lookback[kLookbackL2];
+int64_t lookback_lag(const DeviceState* st, bool mirror, int period = 1) {
+  const int64_t resident = (int64_t)st->sm_count * st->occ_lookback_period[period_slot(period)];
   const int64_t lag = mirror ? resident * 5 / 4 : resident * 5 / 3;
   return std::max<int64_t>(64, ceil_div(lag, 64) * 64);
 }
@@ -651,14 +661,14 @@ int64_t virtual_row_len(const float* x, int64_t N, bool vec4) {
 }
 
 int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
-                       cudaStream_t s, int variant, int flags) {
-  const int64_t tile = lookback_tile(variant);
+                       cudaStream_t s, int variant, int flags, int period = 1) {
+  const int64_t tile = period == 1 ? lookback_tile(variant) : lookback_tile_period(period);
   const int64_t tiles = ceil_div(virtual_row_len(x, N, variant != kLookbackV1), tile);
   int64_t total = 0;
-  if (mul_overflows(rows, tiles, &total) || total > kMaxLookbackTiles) return LIBREDUCE_ERR_OVERFLOW;
+  if (mul_overflows(rows, tiles, &total) || total > kMaxLookbackTiles / period) return LIBREDUCE_ERR_OVERFLOW;
   Need need;
   need.header = true;
-  need.nodes = 2 * total;
+  need.nodes = 2 * total * period;
   Scratch sc;
   int rc = acquire(pv, need, &sc, s);
   if (rc) return rc;
@@ -669,11 +679,11 @@ int run_rscan_lookback(const Provider& pv, const float* x, int64_t rows, int64_t
   const int64_t lag_opt = g_opt_lookback_lag.load();
   const int64_t lag = variant == kLookbackL2
                           ? std::min<int64_t>(total, lag_opt > 0 ? lag_opt
-                                                                 : lookback_lag(pv.st, (flags & kScanMirror) != 0))
+                                                                 : lookback_lag(pv.st, (flags & kScanMirror) != 0, period))
                           : 0;
   if (variant == kLookbackL2 && has_row_edges(x, N)) flags |= kScanRowEdges;
   RScanLookbackParams p{x, y, rows, N, tiles, sc.nodes, ticket_word, sc.header,
-                        spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag, flags};
+                        spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag, flags, period};
   const int64_t grid = total + lag;  // one block per ticket
   return launched(launch_rscan_lookback(variant, p, grid, s));
 }
@@ -893,33 +903,41 @@ int run_rows_short(const Provider& pv, const float* x, int64_t rows, int64_t N, 
 }
 
 // Scans along rows (inner == 1).  `flags`: kScanMirror for a forward scan,
-// kScanExclusive to leave out each element's own term.
+// kScanExclusive to leave out each element's own term.  period 2 or 4: each
+// row is a narrow plane of that many columns read flat (N = its floats; the
+// caller checks that x and y share their 16-byte offset): float4 tiles one
+// block per plane, or the L2 look-back for few planes.
 int run_rscan_rows(const Provider& pv, const float* x, int64_t rows, int64_t N, float* y,
-                   cudaStream_t s, int flags) {
+                   cudaStream_t s, int flags, int period = 1) {
   DeviceState* st = pv.st;
   const bool vec4 = rows_vec4(x, y);
   int variant = vec4 ? kRScanV4S4 : kRScanV1S4;
   const int64_t forced_v = g_opt_rscan_variant.load();
-  if (forced_v >= 0 && forced_v < kNumRScanVariants && (forced_v == kRScanV1S4 || vec4))
+  if (period == 1 && forced_v >= 0 && forced_v < kNumRScanVariants && (forced_v == kRScanV1S4 || vec4))
     variant = (int)forced_v;
   // Few rows cannot fill the GPU one block per row: use the look-back scan,
   // which spreads every row's tiles over all SMs.
   int64_t strategy = g_opt_scan_strategy.load();
   if (strategy == 5 && N > kShortRowMax) strategy = 0;  // rows too long for the short-row form
+  if (period != 1 && strategy != 1 && strategy != 2) strategy = 0;  // only these forms take a period
   const int lb_variant = !vec4 ? kLookbackV1 : (strategy == 3 ? kLookbackV4 : kLookbackL2);
-  const int64_t lb_tiles = ceil_div(virtual_row_len(x, N, vec4), lookback_tile(lb_variant));
-  const int64_t row_slots = (int64_t)st->sm_count * st->occ_rscan[variant];
-  const bool lookback_fits = rows <= kMaxLookbackTiles / std::max<int64_t>(1, lb_tiles);
+  const int64_t lb_tiles = ceil_div(virtual_row_len(x, N, vec4),
+                                    period == 1 ? lookback_tile(lb_variant) : lookback_tile_period(period));
+  const int64_t row_slots =
+      (int64_t)st->sm_count * (period == 1 ? st->occ_rscan[variant] : st->occ_rscan_period[period_slot(period)]);
+  const bool lookback_fits = rows <= kMaxLookbackTiles / period / std::max<int64_t>(1, lb_tiles);
   if (strategy == 4) return run_reduce_then_scan(pv, x, rows, N, y, s, flags, vec4);
-  if (strategy == 5 || (strategy == 0 && N <= kShortRowMax)) return run_rscan_short(pv, x, rows, N, y, s, flags);
-  if (strategy >= 2 || (strategy == 0 && 4 * rows < row_slots && lb_tiles >= 4 && lookback_fits))
-    return run_rscan_lookback(pv, x, rows, N, y, s, lb_variant, flags);
+  if (period == 1 && (strategy == 5 || (strategy == 0 && N <= kShortRowMax)))
+    return run_rscan_short(pv, x, rows, N, y, s, flags);
+  if ((strategy >= 2 || (strategy == 0 && 4 * rows < row_slots && lb_tiles >= 4)) && lookback_fits)
+    return run_rscan_lookback(pv, x, rows, N, y, s, lb_variant, flags, period);
+  if (strategy >= 2 && period == 1) return run_rscan_lookback(pv, x, rows, N, y, s, lb_variant, flags);
   Scratch sc;
   int rc = acquire(pv, Need{}, &sc, s);
   if (rc) return rc;
   const int64_t grid = std::min<int64_t>(rows, INT32_MAX);
   if (variant != kRScanV1S4 && has_row_edges(x, N)) flags |= kScanRowEdges;
-  RScanRowsParams p{x, y, rows, N, flags};
+  RScanRowsParams p{x, y, rows, N, flags, period};
   return launched(launch_rscan_rows(variant, p, grid, s));
 }
 
@@ -990,6 +1008,21 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
   {
     int nvec = 1;
     const int64_t fv = g_opt_scan_cols_variant.load();
+    if ((inner == 2 || inner == 4) && rows_vec4(x, y) && g_opt_axis_split.load() <= 0 &&
+        (fv == kScanColsPeriodRows || (fv < 0 && inner == 2 && N * inner >= kPeriodRowsMin))) {
+      // Planes of 2 or 4 columns: each plane read flat as a row whose
+      // elements fall into `inner` column classes, scanned by the row
+      // kernels (float4 tiles one block per plane, or the L2 look-back).
+      // The automatic choice for 2 columns (fraction of copy bandwidth
+      // against the best other form: [16384, 4096, 2] 0.79 / 0.50, [12000,
+      // 2048, 2] 0.73 / 0.49, [1, 1e8, 2] 0.55 / 0.38, [64, 1e6, 2] 0.57 /
+      // 0.35).  With 4 columns every float4 holds one row, the per-class
+      // lane scans (4 per item) bound it by shuffle throughput, and the
+      // other forms are ahead ([1, 4e7, 4] 0.43 / 0.53, [8192, 1024, 4] 0.48
+      // / 0.50): forced only.
+      return run_rscan_rows(pv, x, outer, N * inner, y, s,
+                            (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0), (int)inner);
+    }
     if ((fv < 0 || fv == kScanColsShortPlanes) && g_opt_axis_split.load() <= 0 && N <= kShortRowMax &&
         inner <= kShortPlaneInnerMax) {
       // Narrow planes of at most kShortRowMax rows, whole planes to a chunk:
@@ -1003,8 +1036,8 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
         return run_scan_short_planes(pv, pf, x, outer, N, inner, y, s,
                                      (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0));
     }
-    if (narrow_rows(x, y, inner, &nvec) &&
-        (fv < 0 || fv == kScanColsNarrow || fv == kScanColsNarrowWarp || fv == kScanColsShortPlanes)) {
+    if (narrow_rows(x, y, inner, &nvec) && (fv < 0 || fv == kScanColsNarrow || fv == kScanColsNarrowWarp ||
+                                            fv == kScanColsShortPlanes || fv == kScanColsPeriodRows)) {
       // The block form walks tiles of T rows; a plane of fewer than T/2 rows
       // would leave most of its threads idle: a warp per plane instead
       // (measured on [100000, 100, 3]: 25% against 4% of copy bandwidth; on
@@ -1355,7 +1388,7 @@ int libreduce_set_option(int option, int64_t value) {
       g_opt_rscan_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_SCAN_COLS_VARIANT:
-      if (value < -1 || value > kScanColsShortPlanes) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < -1 || value > kScanColsPeriodRows) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_ROWS_FORM:

@@ -81,12 +81,16 @@ constexpr int kScanExclusive = 2;
 constexpr int kScanRowEdges = 4;
 
 // --- Cumulative sum along rows, one block per row ----------------------------
+// period P (1, 2 or 4): the row is a narrow plane of P columns read flat,
+// element e in column class e % P, and each class is scanned on its own
+// (float4 tiles only).
 struct RScanRowsParams {
   const float* x;
   float* y;
   int64_t rows;
   int64_t N;
   int flags;
+  int period = 1;
 };
 
 // --- Scans of many short rows (N <= kShortRowMax) -----------------------------
@@ -196,6 +200,7 @@ struct RScanLookbackParams {
   int64_t stall_tile;            // test fault: this ticket never publishes (-1: none)
   int64_t lag;                   // L2-lag form: tiles between a tile's two touches
   int flags;                     // kScanMirror | kScanExclusive
+  int period = 1;                // as in RScanRowsParams (L2-lag form only); node words x period
 };
 
 // --- Scan along a strided axis, single-pass look-back over column tiles -----
@@ -270,6 +275,7 @@ constexpr int kScanColsNarrow = kNumScanColsVariants;
 constexpr int kScanColsNarrowWarp = kNumScanColsVariants + 1;
 constexpr int kScanColsLookback = kNumScanColsVariants + 2;  // k_scan_cols_lookback
 constexpr int kScanColsShortPlanes = kNumScanColsVariants + 3;  // chunks of whole narrow planes (short-row kernels)
+constexpr int kScanColsPeriodRows = kNumScanColsVariants + 4;   // planes of 2 or 4 columns as flat rows
 enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
 
 // Elements per tile of the reduce-then-scan passes.
@@ -331,6 +337,9 @@ int occupancy_reduce_rows_warp(int op);
 int occupancy_reduce_cols(int variant, int op);
 int occupancy_rscan_rows(int variant);
 int occupancy_rscan_lookback(int variant);
+int occupancy_rscan_rows_period(int period);      // float4 block per row, period 1, 2 or 4
+int occupancy_rscan_lookback_period(int period);  // L2-lag look-back, period 1, 2 or 4
+int64_t lookback_tile_period(int period);         // its tile (floats) at that period
 int occupancy_scan_cols(int variant);
 
 }  // namespace lr

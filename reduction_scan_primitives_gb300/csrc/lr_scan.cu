@@ -166,90 +166,227 @@ __device__ __forceinline__ void store_tile(const float (&v)[SUB][VEC], const Til
 }
 
 // Suffix scan of one tile held in registers (v[s][i]: element s*256*VEC +
-// t*VEC + i of the tile).  On return v holds each thread's local suffix and
-// off[s] = exc + (wexc + rs), where exc is the suffix over lanes to the right,
-// wexc over warps to the right and rs over sub-tiles to the right inside the
-// tile; the caller adds off[s] + carry (carry: the tiles to the right).
-// `total` is the tile's sum (identical in every thread).  Contains one
-// __syncthreads(); `sh` must not be written again until every thread of the
-// block is past that barrier.
-template <int SUB>
+// t*VEC + i of the tile).  The elements fall into P classes, element e in
+// class e % P (P divides VEC, so item component i is in class i % P), and
+// each class is scanned on its own: a narrow plane of P columns read as one
+// flat row has column c of every row in one class.  P = 1 is the plain row
+// scan.  On return v holds each thread's local suffix within each class and
+// off[s][c] = exc + (wexc + rs), where exc is the class-c suffix over lanes to
+// the right, wexc over warps to the right and rs over sub-tiles to the right
+// inside the tile; the caller adds off[s][c] + carry[c] (carry: the tiles to
+// the right).  total[c] is the tile's class-c sum (identical in every
+// thread).  Contains one __syncthreads(); `sh` must not be written again until
+// every thread of the block is past that barrier.
+template <int SUB, int P = 1>
 struct TileScan {
-  float off[SUB];
-  float total;
+  float off[SUB][P];
+  float total[P];
 };
 
-template <int VEC, int SUB>
-__device__ __forceinline__ TileScan<SUB> tile_suffix(float (&v)[SUB][VEC], float (&sh)[SUB][kNW],
-                                                    int lane, int w) {
-  TileScan<SUB> r;
-  float exc[SUB];
+template <int VEC, int SUB, int P = 1>
+__device__ __forceinline__ TileScan<SUB, P> tile_suffix(float (&v)[SUB][VEC], float (&sh)[SUB][kNW][P],
+                                                       int lane, int w) {
+  static_assert(VEC % P == 0, "every item holds whole classes");
+  TileScan<SUB, P> r;
+  float exc[SUB][P];
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
-    // 1. Suffix of each thread's VEC items, right to left.
+    // 1. Suffix of each thread's VEC items within each class, right to left.
 #pragma unroll
-    for (int i = VEC - 2; i >= 0; --i) v[s][i] += v[s][i + 1];
+    for (int i = VEC - 1 - P; i >= 0; --i) v[s][i] += v[s][i + P];
     // 2. Inclusive suffix over lanes: lane l gets the sum over lanes >= l.
-    float a = v[s][0];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float u = __shfl_down_sync(kFullMask, a, o);
-      if (lane + o < 32) a += u;
+    for (int c = 0; c < P; ++c) {
+      float a = v[s][c];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_down_sync(kFullMask, a, o);
+        if (lane + o < 32) a += u;
+      }
+      const float e = __shfl_down_sync(kFullMask, a, 1);
+      exc[s][c] = (lane == 31) ? 0.f : e;
+      if (lane == 0) sh[s][w][c] = a;  // the warp's class-c total
     }
-    const float e = __shfl_down_sync(kFullMask, a, 1);
-    exc[s] = (lane == 31) ? 0.f : e;
-    if (lane == 0) sh[s][w] = a;  // the warp's total
   }
   __syncthreads();
   // 3. Warp totals -> exclusive suffix over warps and sub-tile totals;
   // 4. sub-tiles to the right inside this tile.
-  float rs = 0.f;  // sum of the sub-tiles to the right of s
+  float rs[P];  // sum of the sub-tiles to the right of s
+#pragma unroll
+  for (int c = 0; c < P; ++c) rs[c] = 0.f;
 #pragma unroll
   for (int s = SUB - 1; s >= 0; --s) {
-    float wt[kNW];
 #pragma unroll
-    for (int q = 0; q < kNW; ++q) wt[q] = sh[s][q];
-    float wexc = 0.f;
+    for (int c = 0; c < P; ++c) {
+      float wt[kNW];
 #pragma unroll
-    for (int q = kNW - 1; q >= 1; --q)
-      if (q > w) wexc += wt[q];
-    r.off[s] = exc[s] + (wexc + rs);
-    const float stot = tree_sum<kNW>(wt);
-    rs = (s == SUB - 1) ? stot : stot + rs;
+      for (int q = 0; q < kNW; ++q) wt[q] = sh[s][q][c];
+      float wexc = 0.f;
+#pragma unroll
+      for (int q = kNW - 1; q >= 1; --q)
+        if (q > w) wexc += wt[q];
+      r.off[s][c] = exc[s][c] + (wexc + rs[c]);
+      const float stot = tree_sum<kNW>(wt);
+      rs[c] = (s == SUB - 1) ? stot : stot + rs[c];
+    }
   }
-  r.total = rs;
+#pragma unroll
+  for (int c = 0; c < P; ++c) r.total[c] = rs[c];
   return r;
 }
 
 // Turn the local suffixes into outputs: add each sub-tile's offset and the
-// carry.  Inclusive: item i gets its own local suffix.  Exclusive: item i gets
-// the local suffix of the item to its right (none for the thread's last
-// item), so no output ever subtracts its own term.
-template <int VEC, int SUB>
-__device__ __forceinline__ void finalize(float (&v)[SUB][VEC], const TileScan<SUB>& ts, float carry,
-                                         bool exclusive) {
+// carry of the item's class.  Inclusive: item i gets its own local suffix.
+// Exclusive: item i gets the local suffix of the next item of its class to
+// its right (none for the thread's last item of each class), so no output
+// ever subtracts its own term.
+template <int VEC, int SUB, int P>
+__device__ __forceinline__ void finalize_p(float (&v)[SUB][VEC], const TileScan<SUB, P>& ts,
+                                           const float (&carry)[P], bool exclusive) {
 #pragma unroll
   for (int s = 0; s < SUB; ++s) {
-    const float off = ts.off[s] + carry;
+    float off[P];
+#pragma unroll
+    for (int c = 0; c < P; ++c) off[c] = ts.off[s][c] + carry[c];
     if (exclusive) {
 #pragma unroll
-      for (int i = 0; i + 1 < VEC; ++i) v[s][i] = v[s][i + 1] + off;
-      v[s][VEC - 1] = off;
+      for (int i = 0; i + P < VEC; ++i) v[s][i] = v[s][i + P] + off[i % P];
+#pragma unroll
+      for (int i = VEC - P; i < VEC; ++i) v[s][i] = off[i % P];
     } else {
 #pragma unroll
-      for (int i = 0; i < VEC; ++i) v[s][i] += off;
+      for (int i = 0; i < VEC; ++i) v[s][i] += off[i % P];
     }
   }
+}
+template <int VEC, int SUB>
+__device__ __forceinline__ void finalize(float (&v)[SUB][VEC], const TileScan<SUB, 1>& ts, float carry,
+                                         bool exclusive) {
+  const float c1[1] = {carry};
+  finalize_p<VEC, SUB, 1>(v, ts, c1, exclusive);
+}
+
+// tile_suffix and finalize_p in one pass, for P > 1 (narrow planes read flat):
+// each sub-tile's offsets are applied as soon as they are formed, so no
+// SUB x P array of them is held (the same additions in the same order as the
+// two calls).  carry_of(c) is evaluated after the barrier, where look-back
+// partials published before it are complete.  total[c] gets the tile's
+// class sums.
+template <int VEC, int SUB, int P, typename CarryFn>
+__device__ __forceinline__ void tile_scan_apply(float (&v)[SUB][VEC], float (&sh)[SUB][kNW][P], int lane, int w,
+                                                CarryFn carry_of, bool exclusive, float (&total)[P]) {
+  static_assert(VEC % P == 0, "every item holds whole classes");
+  float exc[SUB][P];
+#pragma unroll
+  for (int s = 0; s < SUB; ++s) {
+#pragma unroll
+    for (int i = VEC - 1 - P; i >= 0; --i) v[s][i] += v[s][i + P];
+#pragma unroll
+    for (int c = 0; c < P; ++c) {
+      float a = v[s][c];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_down_sync(kFullMask, a, o);
+        if (lane + o < 32) a += u;
+      }
+      const float e = __shfl_down_sync(kFullMask, a, 1);
+      exc[s][c] = (lane == 31) ? 0.f : e;
+      if (lane == 0) sh[s][w][c] = a;
+    }
+  }
+  __syncthreads();
+  float carry[P], rs[P];
+#pragma unroll
+  for (int c = 0; c < P; ++c) {
+    carry[c] = carry_of(c);
+    rs[c] = 0.f;
+  }
+#pragma unroll
+  for (int s = SUB - 1; s >= 0; --s) {
+    float off[P];
+#pragma unroll
+    for (int c = 0; c < P; ++c) {
+      float wt[kNW];
+#pragma unroll
+      for (int q = 0; q < kNW; ++q) wt[q] = sh[s][q][c];
+      float wexc = 0.f;
+#pragma unroll
+      for (int q = kNW - 1; q >= 1; --q)
+        if (q > w) wexc += wt[q];
+      off[c] = (exc[s][c] + (wexc + rs[c])) + carry[c];
+      const float stot = tree_sum<kNW>(wt);
+      rs[c] = (s == SUB - 1) ? stot : stot + rs[c];
+    }
+    if (exclusive) {
+#pragma unroll
+      for (int i = 0; i + P < VEC; ++i) v[s][i] = v[s][i + P] + off[i % P];
+#pragma unroll
+      for (int i = VEC - P; i < VEC; ++i) v[s][i] = off[i % P];
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) v[s][i] += off[i % P];
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < P; ++c) total[c] = rs[c];
+}
+
+// Per-class block sums (fixed trees: warp shuffles, then the warp totals in
+// warp 0); the results are valid in warp 0, lane 0.  sh holds kNW x P floats.
+template <int P>
+__device__ __forceinline__ void block_sum_p(float (&v)[P], float (&sh)[kNW][P]) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int c = 0; c < P; ++c) {
+    v[c] = warp_reduce<OpSum>(v[c]);
+    if (lane == 0) sh[warp][c] = v[c];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int c = 0; c < P; ++c) {
+      float r = lane < kNW ? sh[lane][c] : 0.f;
+#pragma unroll
+      for (int o = kNW / 2; o > 0; o >>= 1) r += __shfl_down_sync(kFullMask, r, o);
+      v[c] = r;
+    }
+  }
+}
+
+// The P class words of one look-back node (consecutive words from `node`):
+// all P loads are issued at once, then only the words not yet carrying this
+// launch's epoch are polled (bounded, as wait_node).
+template <int P>
+__device__ __forceinline__ void wait_node_classes(const unsigned long long* node, unsigned epoch, int64_t limit,
+                                                  const unsigned* abort_word, bool* fail, float (&out)[P]) {
+  unsigned long long word[P];
+#pragma unroll
+  for (int c = 0; c < P; ++c) word[c] = ld_relaxed_u64(node + c);
+#pragma unroll
+  for (int c = 0; c < P; ++c)
+    out[c] = (unsigned)(word[c] >> 32) == epoch ? __uint_as_float((unsigned)word[c])
+                                                : wait_node(node + c, epoch, limit, abort_word, fail);
+}
+
+// a[i] selected by a run-time index (registers cannot be indexed at run time).
+template <int P>
+__device__ __forceinline__ float pick_class(const float (&a)[P], int i) {
+  float r = a[0];
+#pragma unroll
+  for (int c = 1; c < P; ++c)
+    if (i == c) r = a[c];
+  return r;
 }
 
 // ---------------------------------------------------------------------------
 // Block per row: tiles right to left, carry in registers, next tile
 // prefetched into registers while the current one is scanned.
 // ---------------------------------------------------------------------------
-template <int VEC, int SUB, bool EDGES>
+template <int VEC, int SUB, bool EDGES, int P = 1>
 __global__ void __launch_bounds__(kThreads) k_rscan_rows(RScanRowsParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
-  __shared__ float sh_w[2][SUB][kNW];  // warp totals, double-buffered by tile parity
+  __shared__ float sh_w[2][SUB][kNW][P];  // warp totals, double-buffered by tile parity
   const int t = threadIdx.x;
   const int lane = t & 31;
   const int w = t >> 5;
@@ -263,7 +400,9 @@ __global__ void __launch_bounds__(kThreads) k_rscan_rows(RScanRowsParams p) {
     float cur[SUB][VEC];
     float nxt[SUB][VEC];
     load_tile<VEC, SUB>(cur, tile_view(rv, (ntiles - 1) * TILE, TILE, mirror), t, mirror);
-    float carry_lo = 0.f, carry_hi = 0.f;
+    float carry_lo[P], carry_hi[P];
+#pragma unroll
+    for (int c = 0; c < P; ++c) carry_lo[c] = carry_hi[c] = 0.f;
     int ncarry = 0;
 
     for (int64_t k = ntiles - 1; k >= 0; --k) {
@@ -271,14 +410,25 @@ __global__ void __launch_bounds__(kThreads) k_rscan_rows(RScanRowsParams p) {
       if (k > 0) load_tile<VEC, SUB>(nxt, tile_view(rv, base - TILE, TILE, mirror), t, mirror);  // prefetch
       const TileView tv = tile_view(rv, base, TILE, mirror);
       if constexpr (EDGES) mask_tile<VEC, SUB>(cur, tv, t, mirror);
-      const TileScan<SUB> ts = tile_suffix<VEC, SUB>(cur, sh_w[par], lane, w);
-      finalize<VEC, SUB>(cur, ts, carry_hi + carry_lo, exclusive);
+      float tot[P];
+      if constexpr (P == 1) {
+        const TileScan<SUB, P> ts = tile_suffix<VEC, SUB, P>(cur, sh_w[par], lane, w);
+        finalize<VEC, SUB>(cur, ts, carry_hi[0] + carry_lo[0], exclusive);
+        tot[0] = ts.total[0];
+      } else {
+        tile_scan_apply<VEC, SUB, P>(cur, sh_w[par], lane, w, [&](int c) { return carry_hi[c] + carry_lo[c]; },
+                                     exclusive, tot);
+      }
       store_tile<VEC, SUB, EDGES>(cur, tv, t, mirror);
       // Blocked carry: fold every kCarryFold tiles to keep chains short.
-      carry_lo += ts.total;
+#pragma unroll
+      for (int c = 0; c < P; ++c) carry_lo[c] += tot[c];
       if (++ncarry == kCarryFold) {
-        carry_hi += carry_lo;
-        carry_lo = 0.f;
+#pragma unroll
+        for (int c = 0; c < P; ++c) {
+          carry_hi[c] += carry_lo[c];
+          carry_lo[c] = 0.f;
+        }
         ncarry = 0;
       }
       par ^= 1;
@@ -324,7 +474,7 @@ constexpr int kMaxLevels = kNW;  // one warp per level: 32^8 tiles per row at mo
 template <int VEC, int SUB>
 __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
-  __shared__ float sh_w[SUB][kNW];
+  __shared__ float sh_w[SUB][kNW][1];
   __shared__ float s_part[kMaxLevels];
   __shared__ unsigned s_ticket, s_epoch;
   __shared__ int s_fail;
@@ -361,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
   load_tile<VEC, SUB>(v, tv, t, mirror);
   mask_tile<VEC, SUB>(v, tv, t, mirror);
   const TileScan<SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, lane, w);
-  if (t == 0 && !stalled) st_relaxed_u64(vals + k, pack_node(epoch, ts.total));
+  if (t == 0 && !stalled) st_relaxed_u64(vals + k, pack_node(epoch, ts.total[0]));
 
   // Levels of this row: base-32 digits of the largest tile index.
   int levels = 1;
@@ -385,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
     const float part = warp_tree_adjacent(sib);
     if (lane == 0) s_part[w] = part;
     if (w == 0) {
-      float own = ts.total;
+      float own = ts.total[0];
       int L = 0;
       while (d == 31 && !stalled && !__any_sync(kFullMask, fail)) {
         const float parent = warp_tree_adjacent(lane < 31 ? sib : own);
@@ -440,14 +590,19 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
 // the plain order (96% of copy bandwidth against 94%), the forward (mirrored)
 // scan with EARLY (92% against 85%).
 // ---------------------------------------------------------------------------
-template <int SUB, bool EARLY, bool EDGES>
-__global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookbackParams p) {
+//
+// With P > 1 the row is a narrow plane of P columns read flat (see
+// tile_suffix): every tile publishes P node words, one per class (node (L, m)
+// of class c at word (off_L + m)*P + c), and every sum above is taken per
+// class.
+template <int SUB, bool EARLY, bool EDGES, int P = 1>
+__global__ void __launch_bounds__(kThreads, P == 1 ? 4 : 3) k_rscan_lookback_l2(RScanLookbackParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * 4;
   __shared__ __align__(128) float s_tile[TILE];
   __shared__ unsigned long long s_bar;
-  __shared__ float sh_w[SUB][kNW];
-  __shared__ float s_red[kNW];
-  __shared__ float s_part[kMaxLevels];
+  __shared__ float sh_w[SUB][kNW][P];
+  __shared__ float s_red[kNW][P];
+  __shared__ float s_part[kMaxLevels][P];
   __shared__ unsigned s_ticket, s_epoch;
   __shared__ int s_fail;
   const int t = threadIdx.x;
@@ -505,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
     if (u < 0) return;
     const int64_t row = u / tiles;
     const int64_t k = u - row * tiles;
-    unsigned long long* vals = p.node_val + row * 2 * tiles;
+    unsigned long long* vals = p.node_val + row * 2 * tiles * P;
     if (w < levels) {
       int64_t off = 0, count = tiles;
       for (int q = 0; q < w; ++q) {
@@ -515,17 +670,37 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
       const int64_t m = k >> (5 * w);
       const int d = (int)(m & 31);
       bool fail = false;
-      float sib = 0.f;
-      if (lane < d) sib = wait_node(vals + off + (m - d) + lane, epoch, p.spin_limit, abort_word, &fail);
-      const float part = warp_tree_adjacent(sib);
-      if (lane == 0) s_part[w] = part;
+      float sib[P];
+#pragma unroll
+      for (int c = 0; c < P; ++c) sib[c] = 0.f;
+      if (lane < d) {
+        if constexpr (P == 1)
+          sib[0] = wait_node(vals + off + (m - d) + lane, epoch, p.spin_limit, abort_word, &fail);
+        else
+          wait_node_classes<P>(vals + (off + (m - d) + lane) * P, epoch, p.spin_limit, abort_word, &fail, sib);
+      }
+#pragma unroll
+      for (int c = 0; c < P; ++c) {
+        const float part = warp_tree_adjacent(sib[c]);
+        if (lane == 0) s_part[w][c] = part;
+      }
       if (__any_sync(kFullMask, fail) && lane == 0) s_fail = 1;
     }
     if constexpr (EDGES) mask_tile<4, SUB>(v, tv_u, t, mirror);
-    const TileScan<SUB> ts = tile_suffix<4, SUB>(v, sh_w, lane, w);  // its barrier publishes s_part
-    float excl = 0.f;
-    for (int L = 0; L < levels; ++L) excl += s_part[L];  // from the lowest level up
-    finalize<4, SUB>(v, ts, excl, (p.flags & kScanExclusive) != 0);
+    // The tile scan's barrier publishes s_part; each class's carry is its
+    // look-back partials from the lowest level up.
+    const auto excl_of = [&](int c) {
+      float excl = 0.f;
+      for (int L = 0; L < levels; ++L) excl += s_part[L][c];
+      return excl;
+    };
+    if constexpr (P == 1) {
+      const TileScan<SUB, P> ts = tile_suffix<4, SUB, P>(v, sh_w, lane, w);
+      finalize<4, SUB>(v, ts, excl_of(0), (p.flags & kScanExclusive) != 0);
+    } else {
+      float unused[P];
+      tile_scan_apply<4, SUB, P>(v, sh_w, lane, w, excl_of, (p.flags & kScanExclusive) != 0, unused);
+    }
     store_tile<4, SUB, EDGES>(v, tv_u, t, mirror);
   };
 
@@ -542,7 +717,16 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
                                   (p.flags & kScanMirror) != 0);
     // The copy of this tile (time-bounded wait, independent of the poll limit).
     if ((!EDGES || tv.len > 0) && !mbar_wait_copy(&s_bar, 0u)) s_fail = 1;
-    float e[SUB];
+    // Class sums of the copied tile.  Shared element jj is memory element
+    // jj of the tile; in scan order it is jj (reverse scan) or len-1-jj
+    // (mirrored), so with P > 1 component c of a float4 is in class c % P,
+    // or (3 - c) % P mirrored (len and jj are multiples of 4).  P == 1 sums
+    // the sub-tiles by a tree; P > 1 adds them in order as they are read (a
+    // fixed order too, and no SUB x P values held).
+    float e[P == 1 ? SUB : 1][P];
+    float a[P];
+#pragma unroll
+    for (int c = 0; c < P; ++c) a[c] = 0.f;
 #pragma unroll
     for (int s = 0; s < SUB; ++s) {
       const int jj = s * kThreads * 4 + t * 4;
@@ -559,26 +743,54 @@ __global__ void __launch_bounds__(kThreads, 4) k_rscan_lookback_l2(RScanLookback
             if (jj + c < tv.lo || jj + c >= tv.hi) q[c] = 0.f;
         }
       }
-      e[s] = (q[0] + q[1]) + (q[2] + q[3]);
+      if constexpr (P == 1) {
+        e[s][0] = (q[0] + q[1]) + (q[2] + q[3]);
+      } else if constexpr (P == 2) {
+        const float even = q[0] + q[2], odd = q[1] + q[3];
+        a[0] += mirror ? odd : even;
+        a[1] += mirror ? even : odd;
+      } else {
+        static_assert(P == 4, "P is 1, 2 or 4");
+#pragma unroll
+        for (int c = 0; c < 4; ++c) a[c] += mirror ? q[3 - c] : q[c];
+      }
     }
-    const float a = block_sum<kThreads>(tree_sum<SUB>(e), s_red);  // thread 0
-    unsigned long long* vals = p.node_val + row * 2 * tiles;
+    if constexpr (P == 1) {
+      float ec[SUB];
+#pragma unroll
+      for (int s = 0; s < SUB; ++s) ec[s] = e[s][0];
+      a[0] = tree_sum<SUB>(ec);
+    }
+    block_sum_p<P>(a, s_red);  // warp 0, lane 0
+    unsigned long long* vals = p.node_val + row * 2 * tiles * P;
     const bool stalled = ticket == p.stall_tile;
     if (w == 0 && !stalled) {
-      const float own0 = __shfl_sync(kFullMask, a, 0);
-      if (lane == 0) st_relaxed_u64(vals + k, pack_node(epoch, own0));
+      float own[P];
+#pragma unroll
+      for (int c = 0; c < P; ++c) own[c] = __shfl_sync(kFullMask, a[c], 0);
+      if (lane < P) st_relaxed_u64(vals + k * P + lane, pack_node(epoch, pick_class<P>(own, lane)));
       if ((k & 31) == 31) {  // publish every parent this tile completes
         bool fail = false;
-        float own = own0;
         int64_t off = 0, count = tiles, m = k;
         for (int L = 0; L < levels && (m & 31) == 31; ++L) {
-          float sib = 0.f;
-          if (lane < 31) sib = wait_node(vals + off + (m - 31) + lane, epoch, p.spin_limit, abort_word, &fail);
+          float sib[P];
+#pragma unroll
+          for (int c = 0; c < P; ++c) sib[c] = 0.f;
+          if (lane < 31) {
+            if constexpr (P == 1)
+              sib[0] = wait_node(vals + off + (m - 31) + lane, epoch, p.spin_limit, abort_word, &fail);
+            else
+              wait_node_classes<P>(vals + (off + (m - 31) + lane) * P, epoch, p.spin_limit, abort_word, &fail, sib);
+          }
           if (__any_sync(kFullMask, fail)) break;
-          const float parent = warp_tree_adjacent(lane < 31 ? sib : own);
-          own = __shfl_sync(kFullMask, parent, 0);
+#pragma unroll
+          for (int c = 0; c < P; ++c) {
+            const float parent = warp_tree_adjacent(lane < 31 ? sib[c] : own[c]);
+            own[c] = __shfl_sync(kFullMask, parent, 0);
+          }
           const int64_t next_off = off + count;
-          if (lane == 0) st_relaxed_u64(vals + next_off + (m >> 5), pack_node(epoch, own));
+          if (lane < P)
+            st_relaxed_u64(vals + (next_off + (m >> 5)) * P + lane, pack_node(epoch, pick_class<P>(own, lane)));
           off = next_off;
           count >>= 5;
           m >>= 5;
@@ -624,7 +836,7 @@ __global__ void __launch_bounds__(kThreads) k_tile_sums(TileSumsParams p) {
 template <int VEC, int SUB, bool EDGES>
 __global__ void __launch_bounds__(kThreads, 3) k_tile_carry_scan(TileCarryParams p) {
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
-  __shared__ float sh_w[SUB][kNW];
+  __shared__ float sh_w[SUB][kNW][1];
   const int t = threadIdx.x;
   const int64_t b = blockIdx.x;
   const int64_t row = b / p.tiles;
@@ -780,6 +992,20 @@ int64_t lookback_tile(int variant) {
 
 cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
+  if (p.period != 1) {  // narrow planes read flat: float4 tiles of 4 sub-tiles
+    if (variant != kRScanV4S4) return cudaErrorInvalidValue;
+    const bool edges = (p.flags & kScanRowEdges) != 0;
+    if (p.period == 2) {
+      if (edges) k_rscan_rows<4, 4, true, 2><<<g, kThreads, 0, s>>>(p);
+      else k_rscan_rows<4, 4, false, 2><<<g, kThreads, 0, s>>>(p);
+    } else if (p.period == 4) {
+      if (edges) k_rscan_rows<4, 4, true, 4><<<g, kThreads, 0, s>>>(p);
+      else k_rscan_rows<4, 4, false, 4><<<g, kThreads, 0, s>>>(p);
+    } else {
+      return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+  }
   switch (variant) {
     case kRScanV1S4: k_rscan_rows<1, 4, false><<<g, kThreads, 0, s>>>(p); break;
     case kRScanV4S2:
@@ -795,21 +1021,37 @@ cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t gri
   return cudaGetLastError();
 }
 
+// Sub-tiles of the L2 look-back: 8 (8192-float tiles) for plain rows; 4 for
+// planes read flat, whose per-class arrays would not fit the registers of 3
+// blocks per SM at 8.
+template <int P>
+constexpr int kL2Sub = P == 1 ? 8 : 4;
+
+template <int P>
+cudaError_t launch_l2_p(const RScanLookbackParams& p, dim3 g, cudaStream_t s) {
+  constexpr int SUB = kL2Sub<P>;
+  if (p.flags & kScanRowEdges) {
+    if (p.flags & kScanMirror) k_rscan_lookback_l2<SUB, true, true, P><<<g, kThreads, 0, s>>>(p);
+    else k_rscan_lookback_l2<SUB, false, true, P><<<g, kThreads, 0, s>>>(p);
+  } else {
+    if (p.flags & kScanMirror) k_rscan_lookback_l2<SUB, true, false, P><<<g, kThreads, 0, s>>>(p);
+    else k_rscan_lookback_l2<SUB, false, false, P><<<g, kThreads, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int64_t grid,
                                   cudaStream_t s) {
+  if (variant != kLookbackL2 && p.period != 1) return cudaErrorInvalidValue;
   const dim3 g((unsigned)grid);
   switch (variant) {
     case kLookbackV1: k_rscan_lookback<1, 8><<<g, kThreads, 0, s>>>(p); break;
     case kLookbackV4: k_rscan_lookback<4, 8><<<g, kThreads, 0, s>>>(p); break;
     case kLookbackL2:
-      if (p.flags & kScanRowEdges) {
-        if (p.flags & kScanMirror) k_rscan_lookback_l2<8, true, true><<<g, kThreads, 0, s>>>(p);
-        else k_rscan_lookback_l2<8, false, true><<<g, kThreads, 0, s>>>(p);
-      } else {
-        if (p.flags & kScanMirror) k_rscan_lookback_l2<8, true, false><<<g, kThreads, 0, s>>>(p);
-        else k_rscan_lookback_l2<8, false, false><<<g, kThreads, 0, s>>>(p);
-      }
-      break;
+      if (p.period == 2) return launch_l2_p<2>(p, g, s);
+      if (p.period == 4) return launch_l2_p<4>(p, g, s);
+      if (p.period != 1) return cudaErrorInvalidValue;
+      return launch_l2_p<1>(p, g, s);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -888,6 +1130,28 @@ int occupancy_scan_cols(int variant) {
     case kScanColsV4Y8: return occupancy_of(k_scan_cols<4, 1, 8, 8>);
     default: return 0;
   }
+}
+
+// Narrow planes read flat (period 2 or 4): the L2 look-back and the float4
+// block-per-row kernel.
+template <int P>
+int occupancy_l2_p() {
+  constexpr int SUB = kL2Sub<P>;
+  return std::min({occupancy_of(k_rscan_lookback_l2<SUB, false, false, P>),
+                   occupancy_of(k_rscan_lookback_l2<SUB, true, false, P>),
+                   occupancy_of(k_rscan_lookback_l2<SUB, false, true, P>),
+                   occupancy_of(k_rscan_lookback_l2<SUB, true, true, P>)});
+}
+int occupancy_rscan_lookback_period(int period) {
+  if (period == 2) return occupancy_l2_p<2>();
+  if (period == 4) return occupancy_l2_p<4>();
+  return occupancy_rscan_lookback(kLookbackL2);
+}
+int64_t lookback_tile_period(int period) { return (int64_t)(period == 1 ? kL2Sub<1> : kL2Sub<2>) * kThreads * 4; }
+int occupancy_rscan_rows_period(int period) {
+  if (period == 2) return std::min(occupancy_of(k_rscan_rows<4, 4, false, 2>), occupancy_of(k_rscan_rows<4, 4, true, 2>));
+  if (period == 4) return std::min(occupancy_of(k_rscan_rows<4, 4, false, 4>), occupancy_of(k_rscan_rows<4, 4, true, 4>));
+  return occupancy_rscan_rows(kRScanV4S4);
 }
 
 int occupancy_rscan_rows(int variant) {

@@ -38,7 +38,7 @@ def draw_case(rng):
                 seed=int(rng.integers(0, 1 << 30)),
                 split=int(rng.choice([0, 0, 0, 1, 2, 7, 64])),
                 cols_variant=int(rng.choice([-1, -1, 0, 1, 2, 3, 4, 5, 6, 7, 8])),
-                scan_cols_variant=int(rng.choice([-1, -1, 0, 1, 2, 3, 4, 5, 6])),
+                scan_cols_variant=int(rng.choice([-1, -1, 0, 1, 2, 3, 4, 5, 6, 7])),
                 strategy=int(rng.choice([0, 0, 1, 2, 3, 4])))
     if case["dist"] == "int:-8:8" and case["kind"] == "scan":
         case["dist"] = "int:0:3"  # partial sums stay exact in fp32
