@@ -89,6 +89,9 @@ typedef struct CUstream_st* libreduce_stream_t;
 #define LIBREDUCE_ERR_ALIAS 3       /* output overlaps input (the scan is out-of-place only) */
 #define LIBREDUCE_ERR_CUDA 4        /* a CUDA runtime call failed (see libreduce_last_cuda_error) */
 #define LIBREDUCE_ERR_TIMEOUT 5     /* a bounded device-side wait ran out (from libreduce_check) */
+#define LIBREDUCE_ERR_BOUNDS 6      /* debug build only (libreduce_check): a kernel formed an
+                                       address outside its call's buffers, or a misaligned
+                                       one; the access was skipped (see libreduce_debug_build) */
 
 /*
  * reduce_sum_f32 -- out[0] = sum_{i<n} x[i].
@@ -269,6 +272,26 @@ LIBREDUCE_API int libreduce_last_cuda_error(void);
 
 /* Number of kernels this library has launched in this process (all devices). */
 LIBREDUCE_API int64_t libreduce_launch_count(void);
+
+/*
+ * Debug build.  The library can also be built with device-side checks
+ * (reduction_scan_primitives_gb300.build.build(debug=True) -> libreduce_debug.so,
+ * same entry points; no counterpart on the pages): every global access the
+ * kernels make through their load/store helpers, their plain output and
+ * scratch accesses, and the shared-memory slots of the short-row kernels are
+ * checked against the byte ranges of the call's buffers (registered on the
+ * call's stream before its launches).  A bad or misaligned access is recorded
+ * and skipped -- a load reads zeros, a store is dropped -- never trapped, and
+ * libreduce_check / libreduce_check_ws then return LIBREDUCE_ERR_BOUNDS.  The
+ * checks are slow, the registration is a host-to-device copy per call (not
+ * for stream capture), and concurrent calls on different streams share one
+ * registration.
+ *   libreduce_debug_build()        1 for the debug build, 0 for the release library
+ *   libreduce_debug_bad_address()  the first bad address the last
+ *                                  LIBREDUCE_ERR_BOUNDS report found (0: none)
+ */
+LIBREDUCE_API int libreduce_debug_build(void);
+LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
 
 /*
  * Process-wide dispatch options, for tests and benchmarks.  Not thread-safe

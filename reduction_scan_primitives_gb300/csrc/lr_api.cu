@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -15,6 +16,11 @@
 #include "lr_internal.h"
 
 namespace lr {
+
+#ifdef LR_DEBUG
+__device__ LrDebug g_lr_debug;  // the debug build's registered ranges and findings
+#endif
+
 namespace {
 
 // ---------------------------------------------------------------------------
@@ -75,6 +81,18 @@ std::atomic<int64_t> g_opt_rows_form{0};
 std::atomic<int64_t> g_opt_waves{0};
 std::atomic<int64_t> g_opt_lookback_lag{0};
 thread_local int t_last_cuda_error = 0;
+// Debug builds: the current call's input and output byte ranges (set by the
+// entry point, registered with the scratch when the call acquires it), and
+// the first bad address the last check found.
+thread_local const void* t_dbg_buf[2] = {nullptr, nullptr};
+thread_local size_t t_dbg_bytes[2] = {0, 0};
+std::atomic<unsigned long long> g_dbg_last_bad{0};
+void dbg_call_buffers(const void* in, size_t in_bytes, const void* out, size_t out_bytes) {
+  t_dbg_buf[0] = in;
+  t_dbg_bytes[0] = in_bytes;
+  t_dbg_buf[1] = out;
+  t_dbg_bytes[1] = out_bytes;
+}
 
 int fail_cuda(cudaError_t e) {
   t_last_cuda_error = (int)e;
@@ -303,7 +321,31 @@ void ws_layout(const Need& n, size_t* off_t, size_t* off_p, size_t* off_n, size_
   *total = *off_n + align256(sizeof(unsigned long long) * (size_t)n.nodes);
 }
 
-int acquire(const Provider& pv, const Need& need, Scratch* sc, cudaStream_t s) {
+// Debug builds: register the call's buffers and every scratch region it may
+// touch, on the call's stream, before its launches.
+int register_call(const Provider& pv, cudaStream_t s) {
+#ifdef LR_DEBUG
+  const void* p[kDbgRanges] = {t_dbg_buf[0], t_dbg_buf[1], nullptr, nullptr, nullptr, nullptr};
+  size_t b[kDbgRanges] = {t_dbg_bytes[0], t_dbg_bytes[1], 0, 0, 0, 0};
+  if (pv.ws) {
+    p[2] = pv.ws;
+    b[2] = pv.ws_bytes;
+  } else if (pv.st) {
+    p[2] = pv.st->ws;
+    b[2] = pv.st->ws ? kWorkspaceBytes : 0;
+    p[3] = pv.st->node_val;
+    b[3] = pv.st->node_val ? sizeof(unsigned long long) * (size_t)kLookbackWords : 0;
+  }
+  const cudaError_t e = dbg_register_ranges(s, p, b, kDbgRanges);
+  if (e != cudaSuccess) return fail_cuda(e);
+#else
+  (void)pv;
+  (void)s;
+#endif
+  return LIBREDUCE_OK;
+}
+
+int acquire_impl(const Provider& pv, const Need& need, Scratch* sc, cudaStream_t s) {
   const bool any = need.tickets || need.partials || need.nodes || need.header;
   if (pv.query) {
     // A caller workspace always holds at least the header (its error word).
@@ -336,6 +378,14 @@ int acquire(const Provider& pv, const Need& need, Scratch* sc, cudaStream_t s) {
   sc->partials = reinterpret_cast<float*>(pv.ws + off_p);
   sc->nodes = reinterpret_cast<unsigned long long*>(pv.ws + off_n);
   return LIBREDUCE_OK;
+}
+
+// Every strategy takes its scratch here before launching: the scratch first
+// (so its ranges exist), then, in debug builds, the call's registration.
+int acquire(const Provider& pv, const Need& need, Scratch* sc, cudaStream_t s) {
+  const int rc = acquire_impl(pv, need, sc, s);
+  if (rc || pv.query) return rc;
+  return register_call(pv, s);
 }
 
 // Reduction of `segments` contiguous segments of seg_len floats each.
@@ -599,6 +649,7 @@ int reduce_impl(const float* x, int64_t outer, int64_t reduce, int64_t inner, fl
   if (out == nullptr || (x == nullptr && total > 0)) return LIBREDUCE_ERR_INVALID_ARG;
   if (overlaps(x, (size_t)total * sizeof(float), out, (size_t)n_out * sizeof(float)))
     return LIBREDUCE_ERR_ALIAS;
+  dbg_call_buffers(x, (size_t)total * sizeof(float), out, (size_t)n_out * sizeof(float));
   int dev = 0;
   int rc = device_state(&pv.st, &dev);
   if (rc) return rc;
@@ -971,10 +1022,17 @@ double predict_scan_cols(int64_t units, int64_t slots, double lane_eff, double b
 // read of x.
 // Single-pass column scan with a look-back over 256-row x 32-column tiles
 // (k_scan_cols_lookback).  Returns kColLbNoFit, before touching anything,
-// when the tiles' node words would not fit the look-back region.
+// when the tiles' node words would not fit the look-back region.  The debug
+// build never takes it (kColLbNoFit): its checked form of this kernel, with
+// the TMA tensor copies, raised a GPU fault whose cause was not found, so it
+// stays off the GPU; the three-pass form serves instead.
 constexpr int kColLbNoFit = -2;  // distinct from kQueried
 int run_scan_cols_lookback(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
                            float* y, bool reverse, bool exclusive, cudaStream_t s) {
+#ifdef LR_DEBUG
+  (void)pv, (void)x, (void)outer, (void)N, (void)inner, (void)y, (void)reverse, (void)exclusive, (void)s;
+  return kColLbNoFit;
+#endif
   const int64_t col_tiles = ceil_div(inner, kColLbCols);
   const int64_t tiles = ceil_div(N, kColLbRows);
   int64_t units = 0, total = 0;
@@ -1212,6 +1270,7 @@ int cumsum_impl(const float* x, int64_t outer, int64_t N, int64_t inner, float* 
   if (x == nullptr || y == nullptr) return LIBREDUCE_ERR_INVALID_ARG;
   const size_t bytes = (size_t)total * sizeof(float);
   if (overlaps(x, bytes, y, bytes)) return LIBREDUCE_ERR_ALIAS;
+  dbg_call_buffers(x, bytes, y, bytes);
   int dev = 0;
   int rc = device_state(&pv.st, &dev);
   if (rc) return rc;
@@ -1247,6 +1306,45 @@ int ws_provider(void* ws, size_t* ws_bytes, Provider* pv) {
 }  // namespace
 
 int check_device_buffer(const void* p, size_t bytes, int dev) { return check_buffer(p, bytes, dev); }
+
+cudaError_t dbg_register_ranges(cudaStream_t s, const void* const* p, const size_t* bytes, int n) {
+#ifdef LR_DEBUG
+  LrDebug h{};
+  for (int i = 0; i < kDbgRanges && i < n; ++i) {
+    if (p[i] == nullptr || bytes[i] == 0) continue;
+    h.lo[i] = reinterpret_cast<unsigned long long>(p[i]);
+    h.hi[i] = h.lo[i] + bytes[i];
+  }
+  // The ranges only (the findings stay until libreduce_check reads them).
+  return cudaMemcpyToSymbolAsync(g_lr_debug, &h, offsetof(LrDebug, flags), 0, cudaMemcpyHostToDevice, s);
+#else
+  (void)s;
+  (void)p;
+  (void)bytes;
+  (void)n;
+  return cudaSuccess;
+#endif
+}
+
+// Debug builds: read and clear the findings after a synchronisation; returns
+// LIBREDUCE_ERR_BOUNDS when a check failed since the last read.
+int dbg_take_findings() {
+#ifdef LR_DEBUG
+  LrDebug h{};
+  cudaError_t e = cudaMemcpyFromSymbol(&h, g_lr_debug, sizeof(h));
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (h.flags == 0) return LIBREDUCE_OK;
+  g_dbg_last_bad = h.first_bad & ~1ull;
+  const unsigned zero[4] = {0, 0, 0, 0};
+  static_assert(offsetof(LrDebug, first_bad) + sizeof(unsigned long long) - offsetof(LrDebug, flags) <= sizeof(zero),
+                "findings fit the cleared words");
+  e = cudaMemcpyToSymbol(g_lr_debug, zero, sizeof(LrDebug) - offsetof(LrDebug, flags), offsetof(LrDebug, flags));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return LIBREDUCE_ERR_BOUNDS;
+#else
+  return LIBREDUCE_OK;
+#endif
+}
 int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
@@ -1311,6 +1409,7 @@ int libreduce_check(libreduce_stream_t stream) {
   DeviceState* st = nullptr;
   int rc = device_state(&st, nullptr);
   if (rc) return rc;
+  if ((rc = dbg_take_findings())) return rc;
   if (!st->ws) return LIBREDUCE_OK;
   unsigned word = 0;
   e = cudaMemcpyAsync(&word, st->err_word, sizeof(word), cudaMemcpyDeviceToHost, s);
@@ -1330,6 +1429,7 @@ int libreduce_check_ws(void* ws, libreduce_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail_cuda(e);
   if (ws == nullptr) return LIBREDUCE_ERR_INVALID_ARG;
+  if (const int rc = dbg_take_findings()) return rc;
   unsigned word = 0;
   e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -1349,6 +1449,7 @@ const char* libreduce_strerror(int status) {
     case LIBREDUCE_ERR_ALIAS: return "output overlaps input";
     case LIBREDUCE_ERR_CUDA: return "CUDA runtime error";
     case LIBREDUCE_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    case LIBREDUCE_ERR_BOUNDS: return "debug build: a kernel access outside its call's buffers was skipped";
     default: return "unknown status";
   }
 }
@@ -1356,6 +1457,16 @@ const char* libreduce_strerror(int status) {
 int libreduce_last_cuda_error(void) { return t_last_cuda_error; }
 
 int64_t libreduce_launch_count(void) { return g_launches.load(); }
+
+int libreduce_debug_build(void) {
+#ifdef LR_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+uint64_t libreduce_debug_bad_address(void) { return g_dbg_last_bad.load(); }
 
 int libreduce_set_option(int option, int64_t value) {
   switch (option) {

@@ -84,18 +84,18 @@ __global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
     acc.add(tree_reduce<Op, U>(s));
   }
   float v = acc.total();
-  if (t < head) v = Op::combine(v, Op::prep(a[t]));
-  if (t < tail) v = Op::combine(v, Op::prep(av[4 * nvec + t]));
+  if (t < head) v = Op::combine(v, Op::prep(ld_plain(a + t)));
+  if (t < tail) v = Op::combine(v, Op::prep(ld_plain(av + 4 * nvec + t)));
 
   v = block_reduce<Op, kThreads>(v, sh);
   if (p.chunks == 1) {
-    if (t == 0) p.out[seg] = finish(v, p.epi, p.seg_len);
+    if (t == 0) st_plain(p.out + seg, finish(v, p.epi, p.seg_len));
     return;
   }
   if (t == 0) {
-    p.partials[unit] = v;
+    st_plain(p.partials + unit, v);
     __threadfence();
-    const unsigned prev = atomicAdd(p.tickets + seg, 1u);
+    const unsigned prev = take_count(p.tickets + seg);
     am_last = (prev == (unsigned)(p.chunks - 1));
   }
   __syncthreads();
@@ -104,8 +104,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
   float s = reduce_strided_cg<Op>(p.partials + seg * p.chunks, p.chunks, t, kThreads);
   s = block_reduce<Op, kThreads>(s, sh);
   if (t == 0) {
-    p.out[seg] = finish(s, p.epi, p.seg_len);
-    p.tickets[seg] = 0u;  // ready for the next launch
+    st_plain(p.out + seg, finish(s, p.epi, p.seg_len));
+    st_plain(p.tickets + seg, 0u);  // ready for the next launch
   }
 }
 

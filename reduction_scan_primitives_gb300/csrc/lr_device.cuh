@@ -17,6 +17,58 @@ namespace lr {
 constexpr unsigned kFullMask = 0xffffffffu;
 
 // ---------------------------------------------------------------------------
+// Debug builds (LR_DEBUG, the library's separate debug build): every global
+// access made through the helpers below, and the shared-memory slots of the
+// short-row kernels, is checked before it happens.  The host registers the
+// byte ranges [lo, hi) of each call's buffers (inputs, outputs, scratch);
+// an access outside all of them, a shared-memory index outside its buffer,
+// or a misaligned vector access is recorded (flag bits and the first
+// offending address) and skipped -- a load reads zeros -- never trapped.
+// libreduce_check() reports it.  Release builds compile none of this.
+// ---------------------------------------------------------------------------
+#ifdef LR_DEBUG
+extern __device__ LrDebug g_lr_debug;
+
+__device__ __forceinline__ void dbg_record(unsigned bit, unsigned long long addr) {
+  atomicOr(&g_lr_debug.flags, bit);
+  atomicCAS(&g_lr_debug.first_bad, 0ull, addr | 1ull);  // | 1: a recorded zero address stays visible
+}
+// True when [p, p + bytes) lies inside one registered range (and p is aligned
+// to `align` bytes); else records the access.  A load may cover the rest of
+// the 16-byte granules at a range's two ends: the float4 kernels read a row
+// edge's whole granule by design (it lies in the same page as the element it
+// holds) and mask the elements outside; a store must stay inside the range.
+__device__ __forceinline__ bool dbg_global(const void* p, unsigned bytes, unsigned align, bool load) {
+  const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+  if (a & (align - 1)) {
+    dbg_record(kDbgMisaligned, a);
+    return false;
+  }
+#pragma unroll
+  for (int i = 0; i < kDbgRanges; ++i) {
+    const unsigned long long lo = load ? g_lr_debug.lo[i] & ~15ull : g_lr_debug.lo[i];
+    const unsigned long long hi = load ? (g_lr_debug.hi[i] + 15) & ~15ull : g_lr_debug.hi[i];
+    if (g_lr_debug.hi[i] > g_lr_debug.lo[i] && a >= lo && a + bytes <= hi) return true;
+  }
+  dbg_record(kDbgGlobal, a);
+  return false;
+}
+// True when element index i (width w elements) lies inside a shared buffer of n elements.
+__device__ __forceinline__ bool dbg_shared(long long i, int w, long long n, const void* p) {
+  if (i >= 0 && i + w <= n) return true;
+  dbg_record(kDbgShared, reinterpret_cast<unsigned long long>(p));
+  return false;
+}
+#define LR_DBG_GLOBAL(p, bytes, align) ::lr::dbg_global((p), (bytes), (align), true)
+#define LR_DBG_GLOBAL_ST(p, bytes, align) ::lr::dbg_global((p), (bytes), (align), false)
+#define LR_DBG_SHARED(i, w, n, p) ::lr::dbg_shared((i), (w), (n), (p))
+#else
+#define LR_DBG_GLOBAL(p, bytes, align) true
+#define LR_DBG_GLOBAL_ST(p, bytes, align) true
+#define LR_DBG_SHARED(i, w, n, p) true
+#endif
+
+// ---------------------------------------------------------------------------
 // Global memory access (hand-written PTX).
 // ---------------------------------------------------------------------------
 
@@ -24,6 +76,7 @@ constexpr unsigned kFullMask = 0xffffffffu;
 // allocating in L1 (the stream is touched once).  p must be 16-byte aligned.
 __device__ __forceinline__ float4 ld_stream4(const float* p) {
   float4 v;
+  if (!LR_DBG_GLOBAL(p, 16, 16)) return make_float4(0.f, 0.f, 0.f, 0.f);
   asm("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
       : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
       : "l"(p));
@@ -33,26 +86,46 @@ __device__ __forceinline__ float4 ld_stream4(const float* p) {
 // 32-bit load of read-only data, no L1 allocation.
 __device__ __forceinline__ float ld_stream1(const float* p) {
   float v;
+  if (!LR_DBG_GLOBAL(p, 4, 4)) return 0.f;
   asm("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
 
 // 128-bit store with the evict-first (streaming) hint.  p must be 16-byte aligned.
 __device__ __forceinline__ void st_stream4(float* p, float4 v) {
+  if (!LR_DBG_GLOBAL_ST(p, 16, 16)) return;
   asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y),
                "f"(v.z), "f"(v.w)
                : "memory");
 }
 
 __device__ __forceinline__ void st_stream1(float* p, float v) {
+  if (!LR_DBG_GLOBAL_ST(p, 4, 4)) return;
   asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 // Load from L2 (bypassing L1), used for partial sums written by other blocks
 // of the same launch.
-__device__ __forceinline__ float ld_cg1(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ float ld_cg1(const float* p) {
+  if (!LR_DBG_GLOBAL(p, 4, 4)) return 0.f;
+  return __ldcg(p);
+}
 __device__ __forceinline__ float4 ld_cg4(const float* p) {
+  if (!LR_DBG_GLOBAL(p, 16, 16)) return make_float4(0.f, 0.f, 0.f, 0.f);
   return __ldcg(reinterpret_cast<const float4*>(p));
+}
+
+// Plain global accesses of the kernels (outputs, partials, carries, edge
+// elements), checked in debug builds like the helpers above.
+template <typename T>
+__device__ __forceinline__ T ld_plain(const T* p) {
+  if (!LR_DBG_GLOBAL(p, sizeof(T), sizeof(T))) return T(0);
+  return *p;
+}
+template <typename T>
+__device__ __forceinline__ void st_plain(T* p, T v) {
+  if (!LR_DBG_GLOBAL_ST(p, sizeof(T), sizeof(T))) return;
+  *p = v;
 }
 
 // ---------------------------------------------------------------------------
@@ -65,16 +138,19 @@ __device__ __forceinline__ float4 ld_cg4(const float* p) {
 // suffice and no fence is paid on either side.
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
   unsigned long long v;
+  if (!LR_DBG_GLOBAL(p, 8, 8)) return 0ull;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  if (!LR_DBG_GLOBAL_ST(p, 8, 8)) return;
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
   unsigned v;
+  if (!LR_DBG_GLOBAL(p, 4, 4)) return 0u;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
@@ -110,6 +186,14 @@ __device__ __forceinline__ float warp_tree_adjacent(float v) {
   return v;
 }
 
+// An integer ticket: atomicAdd(p, 1) (debug builds: a ticket outside the
+// call's scratch is recorded and reads as ~0u, the caller then takes no part
+// in the combine).
+__device__ __forceinline__ unsigned take_count(unsigned* p) {
+  if (!LR_DBG_GLOBAL_ST(p, 4, 4)) return ~0u;
+  return atomicAdd(p, 1u);
+}
+
 // Tickets and the launch's epoch (the tag that tells this launch's node words
 // from older ones) share one 64-bit device word: epoch in the high half, the
 // ticket counter in the low half.  One atomicAdd gives a block both; the
@@ -121,6 +205,10 @@ struct Ticket {
   unsigned ticket, epoch;
 };
 __device__ __forceinline__ Ticket take_ticket(unsigned long long* word) {
+  // Debug builds: a ticket word outside the call's scratch gives a ticket past
+  // every launch's range (and below 2^31, so no kernel mistakes it for a
+  // tile of its own), and the block leaves without starting a copy.
+  if (!LR_DBG_GLOBAL_ST(word, 8, 8)) return Ticket{0x7fffffffu, 1u};
   const unsigned long long old = atomicAdd(word, 1ull);
   const unsigned e = (unsigned)(old >> 32);
   return Ticket{(unsigned)old, e == 0 ? 1u : e};
@@ -192,6 +280,15 @@ __device__ __forceinline__ bool mbar_wait_copy(unsigned long long* bar, unsigned
 // to shared memory; completion is signalled as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, unsigned bytes,
                                           unsigned long long* bar) {
+#ifdef LR_DEBUG
+  // A source range outside the call's buffers: no copy; the expected bytes
+  // are completed on the barrier by hand, so its waiters still finish.
+  if (!LR_DBG_GLOBAL(src_gmem, bytes, 16)) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+    return;
+  }
+#endif
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst_smem)),
@@ -218,11 +315,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, in
 // zeros, so src_bytes == 0 writes a zero item without reading anything (`src`
 // must still be a valid address).  Completion: commit_group, then wait_group.
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src, unsigned src_bytes) {
+  if (src_bytes && !LR_DBG_GLOBAL(src, 16, 16)) src_bytes = 0;  // debug: a bad source fills zeros
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)), "l"(src),
                "r"(src_bytes)
                : "memory");
 }
 __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src, unsigned src_bytes) {
+  if (src_bytes && !LR_DBG_GLOBAL(src, 4, 4)) src_bytes = 0;  // debug: a bad source fills zeros
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst_smem)), "l"(src),
                "r"(src_bytes)
                : "memory");

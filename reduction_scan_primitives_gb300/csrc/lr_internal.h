@@ -326,6 +326,23 @@ int occupancy_rscan_short();
 cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, int64_t grid, cudaStream_t s);
 int occupancy_scan_cols_lookback();
 
+// --- Debug builds (LR_DEBUG) -------------------------------------------------
+// The address ranges a call's kernels may touch, registered by the host in
+// g_lr_debug (defined in lr_api.cu) before the call's launches; the device
+// helpers check every access against them and record what falls outside.
+constexpr int kDbgRanges = 6;
+constexpr unsigned kDbgGlobal = 1u;      // a global access outside every registered range
+constexpr unsigned kDbgShared = 2u;      // a shared-memory index outside its buffer
+constexpr unsigned kDbgMisaligned = 4u;  // a vector access not aligned to its width
+struct LrDebug {
+  unsigned long long lo[kDbgRanges], hi[kDbgRanges];
+  unsigned flags;
+  unsigned long long first_bad;
+};
+// Register up to kDbgRanges byte ranges [p[i], p[i] + bytes[i]) on stream s
+// (debug builds; a no-op returning cudaSuccess otherwise).
+cudaError_t dbg_register_ranges(cudaStream_t s, const void* const* p, const size_t* bytes, int n);
+
 // Host helpers defined in lr_api.cu, for entry points in other files.
 int check_device_buffer(const void* p, size_t bytes, int dev);  // a libreduce status
 int record_cuda_error(cudaError_t e);                           // returns the CUDA status

@@ -125,20 +125,20 @@ __global__ void __launch_bounds__(kThreads) k_reduce_narrow(NarrowParams p) {
   combine_groups<Op>(sh, G, inner);
 
   if (p.splits == 1) {
-    if (threadIdx.x < inner) p.out[o * inner + threadIdx.x] = finish(sh[threadIdx.x], p.epi, p.reduce);
+    if (threadIdx.x < inner) st_plain(p.out + o * inner + threadIdx.x, finish(sh[threadIdx.x], p.epi, p.reduce));
     return;
   }
   float* part = p.partials + o * p.splits * p.part_stride;
   if (threadIdx.x < p.part_stride)  // part_stride >= inner; the padding columns hold nothing
-    part[s * p.part_stride + threadIdx.x] = threadIdx.x < inner ? sh[threadIdx.x] : Op::identity();
+    st_plain(part + s * p.part_stride + threadIdx.x, threadIdx.x < inner ? sh[threadIdx.x] : Op::identity());
   if (p.keep_partials) return;  // the slice values are the result
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned prev = atomicAdd(p.tickets + o, 1u);
+    const unsigned prev = take_count(p.tickets + o);
     am_last = (prev == (unsigned)(p.splits - 1));
-    if (am_last) p.tickets[o] = 0u;  // every other block of o has taken its ticket
+    if (am_last) st_plain(p.tickets + o, 0u);  // every other block of o has taken its ticket
   }
   __syncthreads();
   if (!am_last) return;
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_narrow(NarrowParams p) {
   if (gs < Gs) sh[threadIdx.x] = v;  // = sh[gs * inner + c]
   __syncthreads();
   combine_groups<Op>(sh, Gs, inner);
-  if (threadIdx.x < inner) p.out[o * inner + threadIdx.x] = finish(sh[threadIdx.x], p.epi, p.reduce);
+  if (threadIdx.x < inner) st_plain(p.out + o * inner + threadIdx.x, finish(sh[threadIdx.x], p.epi, p.reduce));
 }
 
 // ---------------------------------------------------------------------------
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kThreads) k_scan_narrow(ScanColsParams p) {
     float init[VEC];
 #pragma unroll
     for (int c = 0; c < VEC; ++c)
-      init[c] = (p.carry != nullptr && active) ? p.carry[u * p.carry_stride + col + c] : 0.f;
+      init[c] = (p.carry != nullptr && active) ? ld_plain(p.carry + u * p.carry_stride + col + c) : 0.f;
     return TileCarry<VEC>(init);
   };
 
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kThreads) k_scan_narrow_warp(ScanColsParams p)
     float init[VEC];
 #pragma unroll
     for (int c = 0; c < VEC; ++c)
-      init[c] = (p.carry != nullptr && active) ? p.carry[unit * p.carry_stride + col + c] : 0.f;
+      init[c] = (p.carry != nullptr && active) ? ld_plain(p.carry + unit * p.carry_stride + col + c) : 0.f;
     TileCarry<VEC> tc(init);
     for (int64_t s0 = 0; s0 < len; s0 += (int64_t)U * gw) {
       int64_t step = dir * inner;  // hidden from the optimiser: see k_scan_cols
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_narrow_warp(NarrowParams p)
   }
   if (g == 0) {
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) p.out[o * inner + cg * VEC + c] = finish(res[c], p.epi, p.reduce);
+    for (int c = 0; c < VEC; ++c) st_plain(p.out + o * inner + cg * VEC + c, finish(res[c], p.epi, p.reduce));
   }
 }
 

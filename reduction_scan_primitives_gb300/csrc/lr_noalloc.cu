@@ -137,6 +137,12 @@ extern "C" int reduce_sum_f32_noalloc(const float* x, int64_t n, float* out,
     e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
     if (e != cudaSuccess) return record_cuda_error(e);
   }
+  {  // debug builds: the call's buffers and the array (a no-op otherwise)
+    const void* rp[3] = {x, out, d->scratch};
+    const size_t rb[3] = {(size_t)n * sizeof(float), sizeof(float), kScratchBytes};
+    e = dbg_register_ranges(s, rp, rb, 3);
+    if (e != cudaSuccess) return record_cuda_error(e);
+  }
   ContigParams p{x, n, chunk_len, (int32_t)chunks, out, partials, ticket, kEpiNone};
   k_reduce_contig<16, OpSum><<<dim3((unsigned)chunks), kThreads, 0, s>>>(p);
   e = cudaGetLastError();

@@ -82,15 +82,15 @@ __global__ void __launch_bounds__(kClusterThreads) k_reduce_cluster(ContigParams
 #pragma unroll
   for (int u = 0; u < U; ++u) sv[u] = t + u * S < nvec ? reduce4<Op>(r[u]) : Op::identity();
   float v = tree_reduce<Op, U>(sv);
-  if (t < head) v = Op::combine(v, Op::prep(a[t]));
-  if (t < tail) v = Op::combine(v, Op::prep(av[4 * nvec + t]));
+  if (t < head) v = Op::combine(v, Op::prep(ld_plain(a + t)));
+  if (t < tail) v = Op::combine(v, Op::prep(ld_plain(av + 4 * nvec + t)));
   v = block_reduce<Op, kClusterThreads>(v, sh);
   if (t == 0) s_part = v;
   cluster_sync();
   if (rank == 0 && t < 32) {
     float q = t < p.chunks ? ld_cluster_f32(&s_part, (unsigned)t) : Op::identity();
     q = warp_reduce<Op>(q);  // the CTAs' results in a fixed tree
-    if (t == 0) p.out[0] = finish(q, p.epi, p.seg_len);
+    if (t == 0) st_plain(p.out, finish(q, p.epi, p.seg_len));
   }
   cluster_sync();  // every CTA's shared memory stays alive until CTA 0 has read it
 }
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_rows_warp(RowsWarpParams p)
     }
     for (; j < p.len; j += 32) acc.add(Op::prep(ld_stream1(a + j)));
     const float v = warp_reduce<Op>(acc.total());
-    if (lane == 0) p.out[row] = finish(v, p.epi, p.len);
+    if (lane == 0) st_plain(p.out + row, finish(v, p.epi, p.len));
   }
 }
 
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
       float* outp = p.out + o * inner;
 #pragma unroll
       for (int c = 0; c < VEC; ++c)
-        if (col + c < inner) outp[col + c] = finish(res[c], p.epi, p.reduce);
+        if (col + c < inner) st_plain(outp + col + c, finish(res[c], p.epi, p.reduce));
     }
     return;
   }
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
   if (wy == 0) {
     float* mine = part_base + s * slice_stride;
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) mine[jloc + c] = res[c];
+    for (int c = 0; c < VEC; ++c) st_plain(mine + jloc + c, res[c]);
     if (p.keep_partials) return;  // the slice sums are the result
     __threadfence();
   }
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned prev = atomicAdd(p.tickets + o * p.col_tiles + ct, 1u);
+    const unsigned prev = take_count(p.tickets + o * p.col_tiles + ct);
     am_last = (prev == (unsigned)(p.splits - 1));
   }
   __syncthreads();
@@ -288,9 +288,9 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
       for (int k = 0; k < G; ++k) v[k] = sh[k * CW + 4 * q + c];
       const float tot = tree_reduce<Op, G>(v);
       const int64_t cc = ct * CW + 4 * q + c;
-      if (cc < inner) outp[cc] = finish(tot, p.epi, p.reduce);
+      if (cc < inner) st_plain(outp + cc, finish(tot, p.epi, p.reduce));
     }
-    if (threadIdx.x == 0) p.tickets[o * p.col_tiles + ct] = 0u;
+    if (threadIdx.x == 0) st_plain(p.tickets + o * p.col_tiles + ct, 0u);
   }
 }
 
@@ -300,7 +300,7 @@ constexpr int kColsU = 8;
 __global__ void k_fill(float* out, int64_t n, float value) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
-    out[i] = value;
+    st_plain(out + i, value);
 }
 
 template <typename K>

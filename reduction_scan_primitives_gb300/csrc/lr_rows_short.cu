@@ -48,7 +48,7 @@ __device__ __forceinline__ int unit_len(const ShortRowsParams& p) {
 // unpadded chunk (stride == N: one lane per row with N odd) needs no row.
 // PLANES: e = (q*N + j)*inner + c lands in row q*inner + c at column j.
 template <bool PLANES>
-__device__ __forceinline__ float* chunk_slot(const ShortRowsParams& p, float* s, int e) {
+__device__ __forceinline__ float* chunk_slot_raw(const ShortRowsParams& p, float* s, int e) {
   if constexpr (PLANES) {
     const int qj = (int)(((unsigned long long)e * p.magic_inner) >> 32);  // e / inner
     const int c = e - qj * p.inner;
@@ -60,6 +60,20 @@ __device__ __forceinline__ float* chunk_slot(const ShortRowsParams& p, float* s,
     return s + r * p.stride + (e - r * p.N);
   }
 }
+#ifdef LR_DEBUG
+// Debug builds: a slot outside the shared buffer is recorded and replaced by
+// slot 0 (its contents are then wrong, and reported).
+template <bool PLANES>
+__device__ __forceinline__ float* chunk_slot(const ShortRowsParams& p, float* s, int e) {
+  float* d = chunk_slot_raw<PLANES>(p, s, e);
+  return LR_DBG_SHARED(d - s, 1, kShortSmem, d) ? d : s;
+}
+#else
+template <bool PLANES>
+__device__ __forceinline__ float* chunk_slot(const ShortRowsParams& p, float* s, int e) {
+  return chunk_slot_raw<PLANES>(p, s, e);
+}
+#endif
 
 // Coalesced stores of a chunk back to memory.  VEC 4 stores 16 bytes at a
 // time (rows: N % 4 == 0, a float4 never straddles two rows; planes: N*inner
@@ -311,7 +325,10 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_rscan_short(ShortRowsParam
     // the same for every thread.
     for (int rb = 0; rb < nr; rb += kGroups) {
       const int r = rb + gi;
-      scan_row<G>(s + (r < nr ? r : 0) * p.stride, p.N, p.run_len, g, r < nr, mirror, exclusive);
+      float* row = s + (r < nr ? r : 0) * p.stride;
+      // Debug builds: a row reaching outside the shared buffer is recorded and skipped.
+      const bool in_smem = LR_DBG_SHARED(row - s, p.N, kShortSmem, row);
+      scan_row<G>(row, p.N, p.run_len, g, r < nr && in_smem, mirror, exclusive);
     }
     __syncthreads();
     stage_out<VEC, kSmem4<G>, PLANES>(p, s, p.y + r0 * unit_len<PLANES>(p), ne);
@@ -343,8 +360,8 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsPara
     if (c + gridDim.x < chunks) prefetch_chunk<VEC, PLANES>(p, c + gridDim.x, f);
     for (int rb = 0; rb < nr; rb += kGroups) {
       const int r = rb + gi;
-      const bool active = r < nr;
-      const float* row = s + (active ? r : 0) * p.stride;
+      const float* row = s + (r < nr ? r : 0) * p.stride;
+      const bool active = r < nr && LR_DBG_SHARED(row - s, p.N, kShortSmem, row);
       const int first = G == 1 ? 0 : g * p.run_len;
       const int n_run = active ? max(0, min(G == 1 ? p.N : p.run_len, p.N - first)) : 0;
       // Whole blocks of kRegRun elements, each combined by a fixed tree, then
@@ -365,7 +382,7 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsPara
 #pragma unroll
         for (int d = G / 2; d > 0; d >>= 1) v = Op::combine(v, __shfl_down_sync(kFullMask, v, d, G));
       }
-      if (active && g == 0) p.y[r0 * inner + r] = finish(v, p.flags, p.N);  // output (plane, column)
+      if (active && g == 0) st_plain(p.y + r0 * inner + r, finish(v, p.flags, p.N));  // output (plane, column)
     }
     __syncthreads();  // the next chunk overwrites s
   }

@@ -830,7 +830,7 @@ __global__ void __launch_bounds__(kThreads) k_tile_sums(TileSumsParams p) {
 #pragma unroll
   for (int s = 0; s < SUB; ++s) e[s] = tree_sum<VEC>(v[s]);
   const float a = block_sum<kThreads>(tree_sum<SUB>(e), sh);
-  if (threadIdx.x == 0) p.sums[b] = a;
+  if (threadIdx.x == 0) st_plain(p.sums + b, a);
 }
 
 template <int VEC, int SUB, bool EDGES>
@@ -847,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_tile_carry_scan(TileCarryParams
   load_tile<VEC, SUB>(v, tv, t, mirror);
   if constexpr (EDGES) mask_tile<VEC, SUB>(v, tv, t, mirror);
   const TileScan<SUB> ts = tile_suffix<VEC, SUB>(v, sh_w, t & 31, t >> 5);
-  finalize<VEC, SUB>(v, ts, p.carries[b], (p.flags & kScanExclusive) != 0);
+  finalize<VEC, SUB>(v, ts, ld_plain(p.carries + b), (p.flags & kScanExclusive) != 0);
   store_tile<VEC, SUB, EDGES>(v, tv, t, mirror);
 }
 
@@ -896,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, VEC == 4 ? 3 : 4) k_scan_cols(ScanCo
     float init[VEC];
 #pragma unroll
     for (int c = 0; c < VEC; ++c)
-      init[c] = (p.carry != nullptr && active) ? p.carry[og * p.carry_stride + col + c] : 0.f;
+      init[c] = (p.carry != nullptr && active) ? ld_plain(p.carry + og * p.carry_stride + col + c) : 0.f;
     TileCarry<VEC> tc(init);
     for (int64_t t0 = 0; t0 < len; t0 += T) {
       // The stride is hidden from the optimiser each tile: otherwise it hoists

@@ -24,6 +24,7 @@ ERR_OVERFLOW = 2
 ERR_ALIAS = 3
 ERR_CUDA = 4
 ERR_TIMEOUT = 5
+ERR_BOUNDS = 6  # debug build only: a kernel access outside its call's buffers was skipped
 
 OPS = {"sum": 0, "mean": 1, "max": 2, "min": 3, "norm": 4}
 
@@ -42,7 +43,9 @@ OPT_LOOKBACK_LAG = 9
 OPT_SCAN_COLS_VARIANT = 10
 OPT_ROWS_FORM = 11
 
-LIB_PATH = _build.LIB
+# The library this binding loads: the release build, or another build of the
+# same C ABI named by LIBREDUCE_LIB (e.g. the debug build, _build.DEBUG_LIB).
+LIB_PATH = os.environ.get("LIBREDUCE_LIB") or _build.LIB
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
                       "libreduce.h")
 
@@ -114,6 +117,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.libreduce_launch_count.restype = i64
     lib.libreduce_set_option.argtypes = [i32, i64]
     lib.libreduce_set_option.restype = i32
+    lib.libreduce_debug_build.argtypes = []
+    lib.libreduce_debug_build.restype = i32
+    lib.libreduce_debug_bad_address.argtypes = []
+    lib.libreduce_debug_bad_address.restype = ctypes.c_uint64
     if path is None:
         _lib = lib
     return lib
@@ -416,6 +423,16 @@ def set_option(option: int, value: int) -> None:
 
 def launch_count() -> int:
     return int(load().libreduce_launch_count())
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the debug build (checked kernel accesses)."""
+    return bool(load().libreduce_debug_build())
+
+
+def debug_bad_address() -> int:
+    """The first bad address the last ERR_BOUNDS report found (0: none)."""
+    return int(load().libreduce_debug_bad_address())
 
 
 # Short aliases.
