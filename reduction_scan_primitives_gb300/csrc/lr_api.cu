@@ -61,6 +61,7 @@ struct DeviceState {
   int occ_rscan_short = 0;
   int occ_rscan_period[3] = {};     // float4 block per row, period 1, 2, 4
   int occ_lookback_period[3] = {};  // L2 look-back, period 1, 2, 4
+  int occ_planes[3][2] = {};        // narrow planes read flat: [P - 2][scan]
 };
 
 // Index of a period (1, 2, 4) in the per-period tables.
@@ -134,6 +135,8 @@ int device_state(DeviceState** out, int* dev_out) {
       st.occ_lookback_period[pi] = std::max(1, occupancy_rscan_lookback_period(1 << pi));
     }
     st.occ_rscan_short = std::max(1, occupancy_rscan_short());
+    for (int pi = 0; pi < 3; ++pi)
+      for (int sc = 0; sc < 2; ++sc) st.occ_planes[pi][sc] = std::max(1, occupancy_planes(pi + 2, sc != 0));
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
   }
@@ -529,6 +532,49 @@ int run_narrow(const Provider& pv, const float* x, int64_t outer, int64_t reduce
   return launched(launch_reduce_narrow(vec, op, p, grid, s));
 }
 
+// Narrow planes of 2, 3 or 4 columns read flat as segmented class runs
+// (lr_planes.cu): planes per item and items, or false when the shape does not
+// fit (planes of at most kPlanesRun floats).  Short planes go k >= 2 to a
+// tile (the item's start is rounded down to a multiple of 4 floats, 12 for
+// three columns); longer ones one to an item.
+struct PlaneRunPlan {
+  int64_t k = 1, items = 0;
+  unsigned long long magic = 0;
+};
+bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl) {
+  int64_t L = 0;
+  if (inner < 2 || inner > 4 || outer <= 0 || mul_overflows(N, inner, &L) || L <= kPlanesRun) return false;
+  const int64_t align = inner == 3 ? 12 : 4;
+  const int64_t k = (kPlanesTile - align + 1) / L;
+  pl->k = k >= 2 ? k : 1;
+  pl->items = ceil_div(outer, pl->k);
+  pl->magic = pl->k >= 2 ? ((1ull << 32) + (unsigned long long)L - 1) / (unsigned long long)L : 0;
+  return true;
+}
+// The automatic choice takes the flat runs when there is at least one item
+// per SM.  A block streams about 33 GB/s of a scan, so from ~150 items on the
+// runs pass the forms that split a plane across blocks (fractions of copy
+// bandwidth, runs against the automatic choice before them: [512, 3000, 3]
+// 0.93 / 0.27, [400, 10000, 3] 0.80 / 0.30, [300, 5000, 4] 0.80 / 0.65,
+// [200, 50000, 4] 0.83 / 0.56, [100, 20000, 2] 0.49 / 0.31; sums [512, 3000,
+// 3] 0.69 / 0.37, [300, 5000, 4] 0.64 / 0.38); with only tens of planes a
+// block per plane leaves most SMs idle.
+bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl) { return pl.items >= st->sm_count; }
+int run_planes(const Provider& pv, const PlaneRunPlan& pl, const float* x, int64_t outer, int64_t N,
+               int64_t inner, float* y, int flags, bool scan, int op, cudaStream_t s) {
+  DeviceState* st = pv.st;
+  Need need;
+  need.header = true;  // the error word (a copy that never lands)
+  Scratch sc;
+  const int rc = acquire(pv, need, &sc, s);
+  if (rc) return rc;
+  const int64_t slots = (int64_t)st->sm_count * st->occ_planes[inner - 2][scan ? 1 : 0];
+  const int64_t grid = std::max<int64_t>(1, std::min(pl.items, slots));
+  PlaneRunParams p{x, y, outer, N, pl.k, pl.items, pl.magic, flags, sc.header};
+  return launched(scan ? launch_planes_scan((int)inner, p, grid, s)
+                       : launch_planes_reduce((int)inner, op, p, grid, s));
+}
+
 int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, int64_t inner,
              float* out, int op, int epi, cudaStream_t s) {
   DeviceState* st = pv.st;
@@ -536,8 +582,14 @@ int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, 
   {
     // Narrow rows take the narrow kernel unless a wide shape is forced (sums).
     int vec = 1;
-    const int64_t fv = g_opt_cols_variant.load();
+    int64_t fv = g_opt_cols_variant.load();
     const bool wide_forced = op == kOpSum && fv >= 0 && fv < kNumColsVariants;
+    PlaneRunPlan pl;
+    if ((fv < 0 || fv == kColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
+        (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && plane_run_plan(outer, reduce, inner, &pl) &&
+        (fv == kColsPlaneRuns || plane_runs_fill(st, pl)))
+      return run_planes(pv, pl, x, outer, reduce, inner, out, epi, false, op, s);
+    if (fv == kColsPlaneRuns) fv = -1;  // forced on a shape it does not take: the automatic choice
     if ((fv < 0 || fv == kColsShortPlanes) && g_opt_axis_split.load() <= 0) {
       // Narrow planes of at most kShortRowMax rows, many to a chunk.
       const int rc = try_reduce_short_planes(pv, x, outer, reduce, inner, out, op, epi, fv == kColsShortPlanes, s);
@@ -1065,7 +1117,14 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
   DeviceState* st = pv.st;
   {
     int nvec = 1;
-    const int64_t fv = g_opt_scan_cols_variant.load();
+    int64_t fv = g_opt_scan_cols_variant.load();
+    PlaneRunPlan pl;
+    if ((fv < 0 || fv == kScanColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
+        ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+        plane_run_plan(outer, N, inner, &pl) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl)))
+      return run_planes(pv, pl, x, outer, N, inner, y, (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0),
+                        true, kOpSum, s);
+    if (fv == kScanColsPlaneRuns) fv = -1;  // forced on a shape it does not take: the automatic choice
     if ((inner == 2 || inner == 4) && rows_vec4(x, y) && g_opt_axis_split.load() <= 0 &&
         (fv == kScanColsPeriodRows || (fv < 0 && inner == 2 && N * inner >= kPeriodRowsMin))) {
       // Planes of 2 or 4 columns: each plane read flat as a row whose
@@ -1491,7 +1550,7 @@ int libreduce_set_option(int option, int64_t value) {
       g_opt_contig_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_COLS_VARIANT:
-      if (value < -1 || value > kColsShortPlanes) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < -1 || value > kColsPlaneRuns) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_RSCAN_VARIANT:
@@ -1499,7 +1558,7 @@ int libreduce_set_option(int option, int64_t value) {
       g_opt_rscan_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_SCAN_COLS_VARIANT:
-      if (value < -1 || value > kScanColsPeriodRows) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < -1 || value > kScanColsPlaneRuns) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_ROWS_FORM:

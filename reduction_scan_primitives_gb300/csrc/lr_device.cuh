@@ -276,6 +276,14 @@ __device__ __forceinline__ bool mbar_wait_copy(unsigned long long* bar, unsigned
   return true;
 }
 
+// Orders this thread's earlier shared-memory accesses (generic proxy) before
+// bulk copies issued after the next block barrier (async proxy): a buffer
+// that threads have read or written is refilled by the TMA engine only after
+// every thread has fenced and the block has synchronised.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
 // to shared memory; completion is signalled as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, unsigned bytes,
@@ -295,6 +303,26 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, 
       "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from shared
+// to global memory as one bulk copy of the issuing thread's current bulk
+// group.  The shared source may be written again only after
+// bulk_store_wait_read; the issuing thread waits with bulk_store_wait_all
+// before its block leaves.  Writers of the source fence with
+// fence_proxy_async_smem and synchronise with the issuer first.
+__device__ __forceinline__ void bulk_store(void* dst_gmem, const void* src_smem, unsigned bytes) {
+  if (!LR_DBG_GLOBAL_ST(dst_gmem, bytes, 16)) return;  // debug: a destination outside the call's buffers
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
+               "r"(smem_u32(src_smem)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's bulk stores have read their shared sources.
+__device__ __forceinline__ void bulk_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Tiled tensor copy (TMA engine) of one 3-D box into shared memory, completed
 // on an mbarrier.  `tmap` is the generic address of a tensor map held in

@@ -129,6 +129,28 @@ struct ShortRowsParams {
   unsigned long long magic_inner;
 };
 
+// --- Narrow planes of 2, 3 or 4 columns, read flat (segmented class runs) ----
+// x is [outer, N, P] (P = 2, 3 or 4 columns), scanned or reduced along N.
+// Plane o is the L = N*P floats from o*L; the float at flat index f is in
+// column f % P.  Work is cut into items of k whole planes: k >= 2 planes fit
+// one tile of kPlanesTile floats (with the item's start rounded down to a
+// 16-byte boundary); k = 1 covers a plane in one or more tiles.  x (and y for
+// scans) must be 16-byte aligned and L > kPlanesRun.
+constexpr int kPlanesThreads = 128;                       // threads per block (this kernel only)
+constexpr int kPlanesRun = 36;                            // consecutive floats per thread
+constexpr int kPlanesTile = kPlanesThreads * kPlanesRun;  // floats per tile
+struct PlaneRunParams {
+  const float* x;
+  float* y;            // scans: [outer, N, P]; reductions: [outer, P]
+  int64_t outer;
+  int64_t N;
+  int64_t k;           // planes per item
+  int64_t items;       // ceil(outer / k)
+  unsigned long long magic;  // ceil(2^32 / L) when k >= 2 (then L < kPlanesTile)
+  int flags;           // scans: kScanMirror | kScanExclusive; reductions: the epilogue
+  unsigned* err_word;  // bit 0 set if a tile's copy never lands
+};
+
 // --- Reduce-then-scan along rows (three passes) ------------------------------
 // Rows are scanned as reverse scans of the (possibly mirrored) row, in logical
 // tiles k = [k*TILE, (k+1)*TILE).  Pass 1 writes the sum of every logical tile
@@ -252,6 +274,7 @@ enum ColsVariant {
 constexpr int kColsNarrow = kNumColsVariants;
 constexpr int kColsNarrowWarp = kNumColsVariants + 1;
 constexpr int kColsShortPlanes = kNumColsVariants + 2;  // chunks of whole narrow planes (short-row kernels)
+constexpr int kColsPlaneRuns = kNumColsVariants + 3;    // planes of 2-4 columns, segmented class runs
 enum RScanVariant { kRScanV1S4 = 0, kRScanV4S2 = 1, kRScanV4S4 = 2, kNumRScanVariants };
 enum LookbackVariant {
   kLookbackV1 = 0,  // scalar items, one tile per block, tile kept in registers
@@ -276,6 +299,7 @@ constexpr int kScanColsNarrowWarp = kNumScanColsVariants + 1;
 constexpr int kScanColsLookback = kNumScanColsVariants + 2;  // k_scan_cols_lookback
 constexpr int kScanColsShortPlanes = kNumScanColsVariants + 3;  // chunks of whole narrow planes (short-row kernels)
 constexpr int kScanColsPeriodRows = kNumScanColsVariants + 4;   // planes of 2 or 4 columns as flat rows
+constexpr int kScanColsPlaneRuns = kNumScanColsVariants + 5;    // planes of 2-4 columns, segmented class runs
 enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
 
 // Elements per tile of the reduce-then-scan passes.
@@ -324,6 +348,11 @@ cudaError_t launch_rscan_short(int lanes, int vec, const ShortRowsParams& p, int
 cudaError_t launch_reduce_short(int op, int lanes, int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s);
 int occupancy_rscan_short();
 cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, int64_t grid, cudaStream_t s);
+// Narrow planes read flat: P = 2, 3 or 4; reductions take any ReduceOp.
+cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
+cudaError_t launch_planes_reduce(int P, int op, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
+int occupancy_planes(int P, bool scan);  // resident kPlanesThreads-thread blocks per SM
+
 int occupancy_scan_cols_lookback();
 
 // --- Debug builds (LR_DEBUG) -------------------------------------------------

@@ -139,11 +139,11 @@ def test_options(lib):
                      (L.OPT_RSCAN_VARIANT, -1), (L.OPT_WAVES, 0), (L.OPT_LOOKBACK_LAG, 0),
                      (L.OPT_SCAN_COLS_VARIANT, -1)):
         assert lib.libreduce_set_option(opt, val) == L.OK
-    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 7) == L.OK
-    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 8) == L.ERR_INVALID_ARG
+    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 8) == L.OK
+    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 9) == L.ERR_INVALID_ARG
     assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, -1) == L.OK
-    assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 8) == L.OK
-    assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 9) == L.ERR_INVALID_ARG
+    assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 9) == L.OK
+    assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 10) == L.ERR_INVALID_ARG
     assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, -1) == L.OK
     for v in (0, 1, 2):
         assert lib.libreduce_set_option(L.OPT_ROWS_FORM, v) == L.OK
@@ -188,5 +188,16 @@ def test_short_row_index_division_is_exact():
     import numpy as np
     e = np.arange(0, 8192, dtype=np.uint64)
     for d in range(1, 4097):
+        magic = np.uint64(((1 << 32) + d - 1) // d)
+        assert np.array_equal((e * magic) >> np.uint64(32), e // np.uint64(d)), d
+
+
+def test_plane_run_division_is_exact():
+    """The plane-run kernel finds plane boundaries in a tile holding k >= 2
+    planes of L floats (37 <= L <= 2302) by (e * ceil(2^32 / L)) >> 32 for e
+    up to a tile and a run past it (4608 + 72); that is e // L there."""
+    import numpy as np
+    e = np.arange(0, 4608 + 72, dtype=np.uint64)
+    for d in range(37, (4608 - 3) // 2 + 1):
         magic = np.uint64(((1 << 32) + d - 1) // d)
         assert np.array_equal((e * magic) >> np.uint64(32), e // np.uint64(d)), d

@@ -1,0 +1,154 @@
+"""Narrow planes of 2, 3 or 4 columns read flat as segmented class runs (GPU):
+[outer, N, P] scanned or reduced along N by k_planes, which reads each tile of
+the flat array into shared memory and scans 12-float runs per thread, the
+column classes fixed and the segments restarting at plane boundaries.
+Against the oracle element by element: short planes many to a tile (plane
+boundaries at and inside runs), planes of about one tile, planes over many
+tiles, both directions, inclusive and exclusive, every reduction operator,
+integer inputs exactly, reruns bit for bit, neighbours of the output left
+alone, and the automatic choice on the shapes it takes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import libreduce_defaults, on_device  # noqa: F401
+from parity import assert_close, assert_exact, assert_op_close, bitwise_equal
+from reduction_scan_primitives_gb300 import inputs
+from reduction_scan_primitives_gb300 import libreduce as L
+
+pytestmark = pytest.mark.gpu
+MODES = [(False, False), (False, True), (True, False), (True, True)]
+MODE_IDS = ["fwd", "fwd-excl", "rev", "rev-excl"]
+SCAN_RUNS = 8    # LIBREDUCE_OPT_SCAN_COLS_VARIANT: narrow planes as segmented class runs
+REDUCE_RUNS = 9  # LIBREDUCE_OPT_COLS_VARIANT: the same for reductions
+# (outer, N, P): plane lengths L = N*P of 38 to 30003 floats: many planes to
+# a 4608-float tile (k >= 2, boundaries inside runs unless L % 36 == 0), one
+# plane to a tile, planes over 2 to 7 tiles; plane counts leaving a ragged
+# last item; the two bench shapes.
+SHAPES = [(100_000, 100, 3), (4096, 4096, 2), (20_001, 19, 2), (30_001, 13, 4), (9000, 767, 3),
+          (5000, 2305, 2), (3000, 1537, 3), (2000, 3001, 4), (700, 10_001, 3), (7, 13, 3),
+          (3, 333_333, 2), (12_345, 250, 4), (40_000, 9, 4)]
+
+
+def scan(x, reverse, exclusive, forced=True, out=None):
+    if forced:
+        L.set_option(L.OPT_SCAN_COLS_VARIANT, SCAN_RUNS)
+    xd = on_device(x)
+    y = out if out is not None else on_device(torch.zeros_like(x))
+    L.cumsum_f32(xd, 1, reverse=reverse, exclusive=exclusive, out=y)
+    L.check()
+    return y
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_scan_against_oracle(shape, reverse, exclusive):
+    x = inputs.make(shape, "uniform_pm1", 31)
+    y = scan(x, reverse, exclusive)
+    ref, scale = oracle.cumsum(x.numpy(), *shape, reverse, exclusive)
+    assert_close(y.cpu().numpy(), ref, scale, f"plane runs {shape} rev={reverse} excl={exclusive}")
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape", [(40_000, 25, 3), (3000, 2401, 2), (1000, 2500, 4)])
+def test_scan_integers_exact_and_bitwise(shape, reverse, exclusive):
+    """{0..3} inputs: every prefix is an integer below 2^24, so exact."""
+    x = inputs.make(shape, "int:0:3", 32)
+    a = scan(x, reverse, exclusive).clone()
+    b = scan(x, reverse, exclusive)
+    assert bitwise_equal(a, b), "reruns differ"
+    ref, _ = oracle.cumsum(x.numpy(), *shape, reverse, exclusive)
+    assert_exact(a.cpu().numpy(), ref, f"plane runs integers {shape}")
+
+
+@pytest.mark.parametrize("op", ["sum", "mean", "max", "min", "norm"])
+@pytest.mark.parametrize("shape", [(100_000, 100, 3), (20_001, 19, 2), (9000, 767, 3), (2000, 3001, 4),
+                                   (7, 13, 3), (4096, 2305, 2), (40_000, 9, 4)])
+def test_reduce_against_oracle(shape, op):
+    L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
+    x = inputs.make(shape, "uniform_pm1", 33)
+    out = L.reduce_axis_op_f32(on_device(x), 1, op)
+    L.check()
+    o, n, i = shape
+    if op == "sum":
+        ref, scale = oracle.axis_sum(x.numpy(), o, n, i)
+        assert_close(out.cpu().numpy(), ref, scale, f"plane runs sum {shape}")
+    else:
+        ref, scale = oracle.reduce_op(x.numpy(), o, n, i, op)
+        assert_op_close(out, ref, scale, op, n, f"plane runs {op} {shape}")
+
+
+@pytest.mark.parametrize("op", ["max", "min", "sum"])
+def test_reduce_nan_stays_in_its_plane(op):
+    shape = (5000, 37, 3)  # L = 111: plane ends inside runs
+    x = inputs.make(shape, "uniform_pm1", 34)
+    x[17, 5, 1] = float("nan")
+    x[4999, 36, 2] = float("nan")
+    L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
+    out = L.reduce_axis_op_f32(on_device(x), 1, op).cpu().numpy()
+    L.check()
+    nan = np.isnan(out.reshape(shape[0], 3))
+    assert nan[17, 1] and nan[4999, 2] and nan.sum() == 2
+    if op == "sum":
+        ref, scale = oracle.axis_sum(x.numpy(), *shape)
+        keep = ~np.isnan(ref)
+        assert_close(out[keep], ref[keep], scale[keep], "plane runs sum beside NaN")
+    else:
+        ref, scale = oracle.reduce_op(x.numpy(), *shape, op)
+        assert_op_close(out, ref, scale, op, shape[1], f"plane runs {op} with NaN")
+
+
+@pytest.mark.parametrize("shape", [(6000, 100, 3), (300, 3001, 4)])
+def test_reduce_integers_exact_and_bitwise(shape):
+    x = inputs.make(shape, "int:-8:8", 35)
+    L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
+    xd = on_device(x)
+    a = L.reduce_axis_f32(xd, 1).clone()
+    b = L.reduce_axis_f32(xd, 1)
+    L.check()
+    assert bitwise_equal(a, b)
+    ref, _ = oracle.axis_sum(x.numpy(), *shape)
+    assert_exact(a.cpu().numpy(), ref, f"plane runs sum integers {shape}")
+
+
+@pytest.mark.parametrize("reverse", [False, True])
+def test_neighbours_untouched(reverse):
+    """Output at a 16-byte offset inside a larger buffer of sentinels; planes
+    whose boundaries fall inside float4 granules (L = 6002 and L = 38)."""
+    for shape in [(7, 3001, 2), (5001, 19, 2)]:
+        x = inputs.make(shape, "uniform01", 36)
+        n = x.numel()
+        buf = torch.full((n + 12,), 5.0, device="cuda")
+        y = buf[4:4 + n].view(shape)
+        scan(x, reverse, False, out=y)
+        assert torch.all(buf[:4] == 5.0) and torch.all(buf[4 + n:] == 5.0)
+        ref, scale = oracle.cumsum(x.numpy(), *shape, reverse, False)
+        assert_close(y.cpu().numpy(), ref, scale, f"neighbours {shape}")
+
+
+@pytest.mark.parametrize("shape", [(100_000, 100, 3), (4096, 4096, 2), (50_000, 40, 4)])
+def test_automatic_choice_takes_plane_runs(shape):
+    """Aligned planes whose items fill the GPU take this form without options:
+    the automatic result is the forced one bit for bit."""
+    x = inputs.make(shape, "uniform_pm1", 37)
+    auto = scan(x, False, False, forced=False).clone()
+    forced = scan(x, False, False)
+    assert bitwise_equal(auto, forced)
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, -1)
+    xd = on_device(x)
+    auto_sum = L.reduce_axis_f32(xd, 1).clone()
+    L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
+    assert bitwise_equal(auto_sum, L.reduce_axis_f32(xd, 1))
+
+
+def test_misaligned_falls_back():
+    """x or y off a 16-byte boundary: another form, still against the oracle."""
+    shape = (20_000, 100, 3)
+    x = inputs.make(shape, "uniform_pm1", 38)
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, SCAN_RUNS)
+    xd = on_device(x, 1)
+    y = L.cumsum_f32(xd, 1)
+    L.check()
+    ref, scale = oracle.cumsum(x.numpy(), *shape, False, False)
+    assert_close(y.cpu().numpy(), ref, scale, "misaligned plane runs")

@@ -41,7 +41,8 @@ def scan_check(shape, reverse, exclusive, offset=0, out_offset=0, dist="uniform_
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("shape", SHAPES)
 def test_scan(shape, reverse, exclusive):
-    y, ref, scale = scan_check(shape, reverse, exclusive)
+    # Forced: some of these shapes take the plane-run kernel by default.
+    y, ref, scale = scan_check(shape, reverse, exclusive, forced=True)
     assert_close(y.cpu().numpy(), ref, scale, f"planes scan {shape} rev={reverse} excl={exclusive}")
 
 
@@ -91,6 +92,7 @@ def test_scan_neighbours_untouched():
 @pytest.mark.parametrize("shape", [(100_000, 100, 3), (4097, 5, 2), (999, 159, 3), (257, 1024, 2),
                                    (513, 33, 7), (129, 11, 256), (2000, 3, 33)])
 def test_reduce(shape, op):
+    L.set_option(L.OPT_COLS_VARIANT, 8)  # some of these shapes take the plane-run kernel by default
     x = inputs.make(shape, "uniform_pm1", 8)
     out = L.reduce_axis_op_f32(on_device(x), 1, op)
     L.check()
