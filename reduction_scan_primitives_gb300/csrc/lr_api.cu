@@ -62,6 +62,7 @@ struct DeviceState {
   int occ_rscan_period[3] = {};     // float4 block per row, period 1, 2, 4
   int occ_lookback_period[3] = {};  // L2 look-back, period 1, 2, 4
   int occ_planes[3][2] = {};        // narrow planes read flat: [P - 2][scan]
+  int occ_planes_lb[3] = {};        // the same, look-back form: [P - 2]
 };
 
 // Index of a period (1, 2, 4) in the per-period tables.
@@ -137,6 +138,7 @@ int device_state(DeviceState** out, int* dev_out) {
     st.occ_rscan_short = std::max(1, occupancy_rscan_short());
     for (int pi = 0; pi < 3; ++pi)
       for (int sc = 0; sc < 2; ++sc) st.occ_planes[pi][sc] = std::max(1, occupancy_planes(pi + 2, sc != 0));
+    for (int pi = 0; pi < 3; ++pi) st.occ_planes_lb[pi] = std::max(1, occupancy_planes_lookback(pi + 2));
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
   }
@@ -460,6 +462,8 @@ int run_rows_short(const Provider& pv, const float* x, int64_t rows, int64_t N, 
                    cudaStream_t s);
 // Reductions of narrow planes by the short-row kernels (defined with them
 // below); kNoPlanes when the planes do not fit a chunk.
+constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): well under a second
+constexpr int kColLbNoFit = -2;  // distinct from kQueried
 constexpr int kNoPlanes = -3;  // distinct from kQueried and kColLbNoFit
 constexpr int64_t kShortPlaneInnerMax = 256;  // widest plane the short-row kernels take
 int try_reduce_short_planes(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
@@ -560,6 +564,12 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl) {
 // 3] 0.69 / 0.37, [300, 5000, 4] 0.64 / 0.38); with only tens of planes a
 // block per plane leaves most SMs idle.
 bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl) { return pl.items >= st->sm_count; }
+// Fewer items than SMs: the look-back form, whose blocks take single tiles,
+// when the planes hold at least two tiles each (measured in the plane-run
+// tests; below that the items' blocks are few and short either way).
+bool plane_runs_split(const DeviceState* st, const PlaneRunPlan& pl, int64_t N, int64_t inner) {
+  return pl.items < st->sm_count && N * inner >= 2 * kPlanesTile;
+}
 int run_planes(const Provider& pv, const PlaneRunPlan& pl, const float* x, int64_t outer, int64_t N,
                int64_t inner, float* y, int flags, bool scan, int op, cudaStream_t s) {
   DeviceState* st = pv.st;
@@ -573,6 +583,38 @@ int run_planes(const Provider& pv, const PlaneRunPlan& pl, const float* x, int64
   PlaneRunParams p{x, y, outer, N, pl.k, pl.items, pl.magic, flags, sc.header};
   return launched(scan ? launch_planes_scan((int)inner, p, grid, s)
                        : launch_planes_reduce((int)inner, op, p, grid, s));
+}
+
+// Scans of few long planes of 2-4 columns by the look-back form of the
+// segmented class runs: one block per tile, the tiles of a plane in scan
+// order, each plane's carries from its own look-back tree.  kColLbNoFit when
+// its tiles exceed the node words.
+int run_planes_lookback(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner, float* y,
+                        int flags, cudaStream_t s) {
+  DeviceState* st = pv.st;
+  const int64_t align = inner == 3 ? 12 : 4;
+  const int64_t tiles = ceil_div(N * inner + align - 1, kPlanesTile);  // the most any plane covers
+  int64_t total = 0;
+  if (mul_overflows(outer, tiles, &total) || total > kMaxLookbackTiles / inner ||
+      tiles > (int64_t(1) << (5 * kPlanesLbLevels)))
+    return kColLbNoFit;
+  Need need;
+  need.header = true;
+  need.nodes = 2 * total * inner;
+  Scratch sc;
+  const int rc = acquire(pv, need, &sc, s);
+  if (rc) return rc;
+  auto* ticket_word = reinterpret_cast<unsigned long long*>(sc.header + 2);
+  const int64_t spin = g_opt_spin_limit.load();
+  const int64_t lag_opt = g_opt_lookback_lag.load();
+  // The lag as for the row look-back, from this kernel's resident blocks.
+  const int64_t resident = (int64_t)st->sm_count * st->occ_planes_lb[inner - 2];
+  const int64_t lag_auto =
+      std::max<int64_t>(64, ceil_div((flags & kScanMirror) ? resident * 5 / 4 : resident * 5 / 3, 64) * 64);
+  const int64_t lag = std::min<int64_t>(total, lag_opt > 0 ? lag_opt : lag_auto);
+  PlaneLbParams p{x, y, outer, N, tiles, sc.nodes, ticket_word, sc.header,
+                  spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag, flags};
+  return launched(launch_planes_lookback((int)inner, p, total + lag, s));  // one block per ticket
 }
 
 int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, int64_t inner,
@@ -729,7 +771,6 @@ int reduce_impl(const float* x, int64_t outer, int64_t reduce, int64_t inner, fl
   return finish_status(run_cols(pv, x, outer, reduce, inner, out, plan.op, plan.epi, s));
 }
 
-constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): well under a second
 // L2-lag form: tickets between a tile's two touches.  In the reverse scan's
 // order (write, then publish) the lag must exceed the blocks resident at
 // once, or the write of tile t - lag waits on tiles still in flight; past
@@ -1078,7 +1119,6 @@ double predict_scan_cols(int64_t units, int64_t slots, double lane_eff, double b
 // build never takes it (kColLbNoFit): its checked form of this kernel, with
 // the TMA tensor copies, raised a GPU fault whose cause was not found, so it
 // stays off the GPU; the three-pass form serves instead.
-constexpr int kColLbNoFit = -2;  // distinct from kQueried
 int run_scan_cols_lookback(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
                            float* y, bool reverse, bool exclusive, cudaStream_t s) {
 #ifdef LR_DEBUG
@@ -1124,7 +1164,15 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
         plane_run_plan(outer, N, inner, &pl) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl)))
       return run_planes(pv, pl, x, outer, N, inner, y, (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0),
                         true, kOpSum, s);
-    if (fv == kScanColsPlaneRuns) fv = -1;  // forced on a shape it does not take: the automatic choice
+    if ((fv < 0 || fv == kScanColsPlaneLookback) && g_opt_axis_split.load() <= 0 &&
+        ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+        plane_run_plan(outer, N, inner, &pl) && (fv == kScanColsPlaneLookback || plane_runs_split(st, pl, N, inner))) {
+      // Few long planes: each plane's tiles over blocks, carries by look-back.
+      const int rc = run_planes_lookback(pv, x, outer, N, inner, y,
+                                         (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0), s);
+      if (rc != kColLbNoFit) return rc;
+    }
+    if (fv == kScanColsPlaneRuns || fv == kScanColsPlaneLookback) fv = -1;  // forced on a shape it does not take
     if ((inner == 2 || inner == 4) && rows_vec4(x, y) && g_opt_axis_split.load() <= 0 &&
         (fv == kScanColsPeriodRows || (fv < 0 && inner == 2 && N * inner >= kPeriodRowsMin))) {
       // Planes of 2 or 4 columns: each plane read flat as a row whose
@@ -1558,7 +1606,7 @@ int libreduce_set_option(int option, int64_t value) {
       g_opt_rscan_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_SCAN_COLS_VARIANT:
-      if (value < -1 || value > kScanColsPlaneRuns) return LIBREDUCE_ERR_INVALID_ARG;
+      if (value < -1 || value > kScanColsPlaneLookback) return LIBREDUCE_ERR_INVALID_ARG;
       g_opt_scan_cols_variant = value;
       return LIBREDUCE_OK;
     case LIBREDUCE_OPT_ROWS_FORM:

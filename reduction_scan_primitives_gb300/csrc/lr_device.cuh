@@ -179,6 +179,31 @@ __device__ __forceinline__ float wait_node(const unsigned long long* node, unsig
   }
 }
 
+// The P class words of one look-back node (consecutive words from `node`):
+// all P loads are issued at once, then only the words not yet carrying this
+// launch's epoch are polled (bounded, as wait_node).
+template <int P>
+__device__ __forceinline__ void wait_node_classes(const unsigned long long* node, unsigned epoch, int64_t limit,
+                                                  const unsigned* abort_word, bool* fail, float (&out)[P]) {
+  unsigned long long word[P];
+#pragma unroll
+  for (int c = 0; c < P; ++c) word[c] = ld_relaxed_u64(node + c);
+#pragma unroll
+  for (int c = 0; c < P; ++c)
+    out[c] = (unsigned)(word[c] >> 32) == epoch ? __uint_as_float((unsigned)word[c])
+                                                : wait_node(node + c, epoch, limit, abort_word, fail);
+}
+
+// a[i] selected by a run-time index (registers cannot be indexed at run time).
+template <int P>
+__device__ __forceinline__ float pick_class(const float (&a)[P], int i) {
+  float r = a[0];
+#pragma unroll
+  for (int c = 1; c < P; ++c)
+    if (i == c) r = a[c];
+  return r;
+}
+
 // Fixed pairwise tree over the 32 lanes (adjacent pairs first); lane 0 gets it.
 __device__ __forceinline__ float warp_tree_adjacent(float v) {
 #pragma unroll
@@ -238,6 +263,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, u
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
+}
+
+// A plain arrival (no transaction bytes): completes the current phase of a
+// barrier initialised with count 1 when no copy is started for it.
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // One non-blocking probe of phase `parity` of the barrier.

@@ -151,6 +151,27 @@ struct PlaneRunParams {
   unsigned* err_word;  // bit 0 set if a tile's copy never lands
 };
 
+// Scans of few long planes of 2-4 columns, a plane's tiles spread over
+// blocks: scan-order tile j of plane o is ticket o * tiles + j, and each
+// tile's P class sums go through the deterministic 32-ary look-back of the
+// row scans (node words {epoch, fp32}, class c of node (L, m) of plane o at
+// word (o * 2 * tiles + off_L + m) * P + c).  tiles is the most tiles any
+// plane covers; a plane with one fewer publishes an empty last tile.
+constexpr int kPlanesLbLevels = kPlanesThreads / 32;  // one warp per level: 32^4 tiles per plane at most
+struct PlaneLbParams {
+  const float* x;
+  float* y;
+  int64_t outer, N;
+  int64_t tiles;                    // tiles per plane
+  unsigned long long* node_val;     // outer * 2 * tiles * P words
+  unsigned long long* ticket_word;  // as in RScanLookbackParams
+  unsigned* err_word;               // as in RScanLookbackParams
+  int64_t spin_limit;               // polls before a wait gives up
+  int64_t stall_tile;               // test fault: this ticket never publishes (-1: none)
+  int64_t lag;                      // tickets between a tile's two touches
+  int flags;                        // kScanMirror | kScanExclusive
+};
+
 // --- Reduce-then-scan along rows (three passes) ------------------------------
 // Rows are scanned as reverse scans of the (possibly mirrored) row, in logical
 // tiles k = [k*TILE, (k+1)*TILE).  Pass 1 writes the sum of every logical tile
@@ -300,6 +321,7 @@ constexpr int kScanColsLookback = kNumScanColsVariants + 2;  // k_scan_cols_look
 constexpr int kScanColsShortPlanes = kNumScanColsVariants + 3;  // chunks of whole narrow planes (short-row kernels)
 constexpr int kScanColsPeriodRows = kNumScanColsVariants + 4;   // planes of 2 or 4 columns as flat rows
 constexpr int kScanColsPlaneRuns = kNumScanColsVariants + 5;    // planes of 2-4 columns, segmented class runs
+constexpr int kScanColsPlaneLookback = kNumScanColsVariants + 6;  // the same tiles, a plane over blocks (look-back)
 enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
 
 // Elements per tile of the reduce-then-scan passes.
@@ -352,6 +374,8 @@ cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, 
 cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_planes_reduce(int P, int op, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes(int P, bool scan);  // resident kPlanesThreads-thread blocks per SM
+cudaError_t launch_planes_lookback(int P, const PlaneLbParams& p, int64_t grid, cudaStream_t s);
+int occupancy_planes_lookback(int P);
 
 int occupancy_scan_cols_lookback();
 

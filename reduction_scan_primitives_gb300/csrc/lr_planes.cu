@@ -54,6 +54,7 @@ constexpr int kRun = kPlanesRun;
 constexpr int kTile = kPlanesTile;
 constexpr int kChunks = kRun / 4;  // float4 chunks per run
 constexpr int kStages = 3;
+constexpr int kLbBlocks = 6;  // resident look-back blocks per SM: 6 x 37 KB of tiles, <= 85 registers
 static_assert(kRun % 4 == 0 && kRun % 3 == 0 && (kChunks & 1) == 1,
               "runs hold whole float4 chunks, a multiple of every P, an odd number of chunks");
 // Runs and tiles start on multiples of this many floats: 16 bytes and P.
@@ -121,6 +122,216 @@ __device__ __forceinline__ int rel_sat(int64_t a, int64_t b) {
   return (int)max(min(a - b, kFar), -kFar);
 }
 
+// ---------------------------------------------------------------------------
+// The scan of one tile in shared memory, shared by both kernels.
+// ---------------------------------------------------------------------------
+
+// One thread's share of a tile between the two phases.
+template <int P>
+struct RunState {
+  float v[kRun];     // my run in scan order: inputs, then running values, then outputs
+  float pre[P];      // class totals of my floats before the head
+  float ex[P];       // segmented totals of the lanes before mine in the warp
+  int hp;            // the head: scan position in my run where a plane starts (kRun: none)
+  bool head_before;  // a lane before mine in the warp holds a head
+};
+
+// The head of my run (first float at a in the tile) and, for a reduction,
+// dd: my floats before the end of plane q - 1 of the item (1..kRun), else -1.
+// Forward: boundaries at lo + q*L, q = 0 .. planes (the one at hi splits a
+// reduction's last run); reverse: a plane starts (in scan order) at its last
+// float, lo + q*L - 1, q >= 1.  Boundaries past the item only split floats
+// that are never stored.  rlo, rhi: the item's bounds relative to the tile.
+// one_plane: the item is one plane (boundaries at lo and hi only); else the
+// item's planes, shorter than a tile, all lie in this one (0 <= rlo <
+// kPlaneAlign) and Li, magic give L and ceil(2^32 / L).
+template <bool REV>
+__device__ __forceinline__ void find_head(int a, int rlo, int rhi, bool one_plane, int Li, unsigned long long magic,
+                                          int& hp, int& dd, int& q) {
+  hp = kRun;
+  dd = -1;
+  q = 0;
+  if (one_plane) {
+    if constexpr (!REV) {
+      const int d1 = rlo - a, d2 = rhi - a;
+      if (d1 >= 0 && d1 < kRun) hp = d1;
+      else if (d2 >= 0 && d2 < kRun) hp = d2;
+      if (d2 >= 1 && d2 <= kRun) {
+        dd = d2;
+        q = 1;
+      }
+    } else {
+      const int e = a + kRun - rhi;
+      if (e >= 0 && e < kRun) hp = e;
+    }
+  } else {
+    const int rr = a - rlo;
+    if constexpr (!REV) {
+      q = rr <= 0 ? 0 : (int)(((unsigned long long)(rr - 1) * magic) >> 32) + 1;
+      const int d = q * Li - rr;  // >= 0
+      if (d < kRun) hp = d;
+      if (d >= 1 && d <= kRun) dd = d;
+    } else {
+      const int g = rr + kRun;  // > 0
+      const int qr = (int)(((unsigned long long)g * magic) >> 32);
+      const int e = g - qr * Li;
+      if (qr >= 1 && e < kRun) hp = e;
+    }
+  }
+}
+
+// Phase 1: read my run (memory order reversed for a reverse scan), scan it
+// per class, then the warp's segmented scan of the run totals; lane 31
+// writes the warp's last-segment totals and head flag.  st.hp must be set.
+template <int P, bool SCAN, bool REV, bool EXCL, typename Op>
+__device__ __forceinline__ void runs_phase1(RunState<P>& st, const float* buf, int a, float (&wagg)[kNW][P],
+                                            int (&wflag)[kNW]) {
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const int hp = st.hp;
+  {
+    const float4* src = reinterpret_cast<const float4*>(buf + a);
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k) {
+      const float4 q = src[k];
+      const float e4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = 4 * k + c;
+        st.v[REV ? kRun - 1 - i : i] = SCAN ? e4[c] : Op::prep(e4[c]);
+      }
+    }
+  }
+  // 1. Sequential per-class scan of the run.  acc[c] runs over class c; the
+  // first float of each class at or after the head starts it again.  v[e]
+  // becomes the float's running value (inclusive, or the value before it
+  // when exclusive); pre[c] ends as class c's total before the head.
+  float acc[P];
+#pragma unroll
+  for (int c = 0; c < P; ++c) acc[c] = st.pre[c] = Op::identity();
+  if (!__any_sync(kFullMask, hp > 0 && hp < kRun)) {
+    // No head inside a run of this warp (hp is 0 or kRun everywhere).
+#pragma unroll
+    for (int e = 0; e < kRun; ++e) {
+      const int c = e % P;
+      const float before = acc[c];
+      acc[c] = Op::combine(acc[c], st.v[e]);
+      if constexpr (SCAN) st.v[e] = EXCL ? before : acc[c];
+    }
+    if (hp == kRun) {
+#pragma unroll
+      for (int c = 0; c < P; ++c) st.pre[c] = acc[c];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < kRun; ++e) {
+      const int c = e % P;
+      const bool restart = (unsigned)(e - hp) < (unsigned)P;  // first of its class in the new plane
+      const float before = restart ? Op::identity() : acc[c];
+      acc[c] = restart ? st.v[e] : Op::combine(acc[c], st.v[e]);
+      if constexpr (SCAN) st.v[e] = EXCL ? before : acc[c];
+      if (e < hp) st.pre[c] = acc[c];
+    }
+    // A class with no float after a head near the run's end (positions
+    // kRun - P + c hold class c) keeps nothing for the new plane.
+#pragma unroll
+    for (int c = 0; c < P; ++c)
+      if (kRun - P + c < hp && hp < kRun) acc[c] = Op::identity();
+  }
+  // 2. Segmented inclusive scan of the runs' last-segment totals across the
+  // warp: lane l adds only lanes at or after hh, its last lane with a head
+  // (every lane between hh and l has the same hh, so the Hillis-Steele steps
+  // stay inside the segment).
+  const unsigned hmask = __ballot_sync(kFullMask, hp < kRun);
+  const unsigned upto = hmask & (kFullMask >> (31 - lane));
+  const int hh = upto ? 31 - __clz((int)upto) : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const bool take = lane - o >= hh;
+#pragma unroll
+    for (int c = 0; c < P; ++c) {
+      const float u = __shfl_up_sync(kFullMask, acc[c], o);
+      if (take) acc[c] = Op::combine(u, acc[c]);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < P; ++c) st.ex[c] = __shfl_up_sync(kFullMask, acc[c], 1);
+  st.head_before = (hmask & ((1u << lane) - 1u)) != 0;
+  if (lane == 31) {
+#pragma unroll
+    for (int c = 0; c < P; ++c) wagg[w][c] = acc[c];
+    wflag[w] = hmask != 0;
+  }
+}
+
+// Phase 2, after a barrier that published the warps' totals: cl gets the
+// carry into my run's floats before its head, from `carry` (into the tile)
+// and the warps before mine in order (a warp with a head restarts it); a
+// scan adds it to those floats.  With `next` set, the last warp's lane 0
+// writes there the carry out of the tile.
+template <int P, bool SCAN, typename Op>
+__device__ __forceinline__ void runs_phase2(RunState<P>& st, const float (&carry)[P], const float (&wagg)[kNW][P],
+                                            const int (&wflag)[kNW], float* next, float (&cl)[P]) {
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  float cw[P];
+#pragma unroll
+  for (int c = 0; c < P; ++c) cw[c] = carry[c];
+#pragma unroll
+  for (int q = 0; q < kNW - 1; ++q) {
+    if (q < w) {
+      const bool f = wflag[q] != 0;
+#pragma unroll
+      for (int c = 0; c < P; ++c) cw[c] = f ? wagg[q][c] : Op::combine(cw[c], wagg[q][c]);
+    }
+  }
+  if (next != nullptr && w == kNW - 1 && lane == 0) {
+    const bool f = wflag[kNW - 1] != 0;
+#pragma unroll
+    for (int c = 0; c < P; ++c) next[c] = f ? wagg[kNW - 1][c] : Op::combine(cw[c], wagg[kNW - 1][c]);
+  }
+#pragma unroll
+  for (int c = 0; c < P; ++c)
+    cl[c] = lane == 0 ? cw[c] : (st.head_before ? st.ex[c] : Op::combine(cw[c], st.ex[c]));
+  if constexpr (SCAN) {
+#pragma unroll
+    for (int e = 0; e < kRun; ++e)
+      if (e < st.hp) st.v[e] = Op::combine(cl[e % P], st.v[e]);
+  }
+}
+
+// A scan's run back to its place in the tile (memory order).
+template <bool REV>
+__device__ __forceinline__ void put_run(const float (&v)[kRun], float* buf, int a) {
+  float4* dst = reinterpret_cast<float4*>(buf + a);
+#pragma unroll
+  for (int k = 0; k < kChunks; ++k) {
+    float e4[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = 4 * k + c;
+      e4[c] = v[REV ? kRun - 1 - i : i];
+    }
+    dst[k] = make_float4(e4[0], e4[1], e4[2], e4[3]);
+  }
+}
+
+// The floats [lo, hi) of a tile (relative to its first float, clamped to
+// the tile) from shared memory to yt: one bulk store of the whole 16-byte
+// granules [ga, gb) (thread 0), plain stores of the partial granules at the
+// two ends (threads 0-7).  After a barrier that follows every thread's
+// writes into buf and its fence_proxy_async_smem.
+__device__ __forceinline__ void store_tile_out(const float* buf, float* yt, int lo, int hi) {
+  const int t = threadIdx.x;
+  const int ga = (lo + 3) & ~3;
+  const int gb = hi & ~3;
+  if (t == 0 && ga < gb) bulk_store(yt + ga, buf + ga, (unsigned)(gb - ga) * 4u);
+  if (t < 8) {
+    const int f = t < 4 ? lo + t : max(gb, ga) + (t - 4);
+    if (f < (t < 4 ? min(ga, hi) : hi)) st_stream1(yt + f, buf[f]);
+  }
+}
+
 template <int P, bool SCAN, bool REV, bool EXCL, typename Op>
 __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
   __shared__ __align__(128) float s_buf[kStages][kTile];
@@ -132,9 +343,8 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
   __shared__ float s_carry[2][P];      // carry into the next tile
   __shared__ Cursor s_pc;              // the producer's cursor (thread 0 only)
   const int t = threadIdx.x;
-  const int lane = t & 31;
-  const int w = t >> 5;
   const int a = (REV ? kT - 1 - t : t) * kRun;  // my run's first float in a tile
+  const int Li = (int)min(p.N * P, (int64_t)INT32_MAX);
 
   int outstanding = 0;  // thread 0: copies issued and not yet consumed
   if (t == 0) {
@@ -166,129 +376,13 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
       const bool landed = mbar_wait_copy(&s_bar[stage], phase);
       const int64_t ts = tile_start(it, j, REV);
       float* buf = s_buf[stage];
-
-      // My run in scan order (memory order reversed for a reverse scan).
-      float v[kRun];
-      {
-        const float4* src = reinterpret_cast<const float4*>(buf + a);
-#pragma unroll
-        for (int k = 0; k < kChunks; ++k) {
-          const float4 q = src[k];
-          const float e4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int i = 4 * k + c;
-            v[REV ? kRun - 1 - i : i] = SCAN ? e4[c] : Op::prep(e4[c]);
-          }
-        }
-      }
-      if constexpr (!SCAN) fence_proxy_async_smem();  // the buffer is refilled after barrier 1
-
-      // The head: the scan position in my run where a plane starts (kRun:
-      // none).  Forward: boundaries at lo + q*L, q = 0 .. planes (the one at
-      // hi splits a reduction's last run); reverse: a plane starts (in scan
-      // order) at its last float, lo + q*L - 1, q >= 1.  Boundaries past the
-      // item only split floats that are never stored.  For a reduction, dd
-      // counts my floats before the end of plane first + qf - 1 (1..kRun),
-      // or is -1.
       const int rlo = rel_sat(it.lo, ts);
       const int rhi = rel_sat(it.hi, ts);
-      int hp = kRun, dd = -1, qf = 0;
-      if (p.k == 1) {  // one plane: boundaries at lo and hi only
-        if constexpr (!REV) {
-          const int d1 = rlo - a, d2 = rhi - a;
-          if (d1 >= 0 && d1 < kRun) hp = d1;
-          else if (d2 >= 0 && d2 < kRun) hp = d2;
-          if (d2 >= 1 && d2 <= kRun) {
-            dd = d2;
-            qf = 1;
-          }
-        } else {
-          const int e = a + kRun - rhi;
-          if (e >= 0 && e < kRun) hp = e;
-        }
-      } else {  // planes shorter than a tile, all in this one: 0 <= rlo < kPlaneAlign
-        const int rr = a - rlo;
-        const int Li = (int)(p.N * P);
-        if constexpr (!REV) {
-          qf = rr <= 0 ? 0 : (int)(((unsigned long long)(rr - 1) * p.magic) >> 32) + 1;
-          const int d = qf * Li - rr;  // >= 0
-          if (d < kRun) hp = d;
-          if (d >= 1 && d <= kRun) dd = d;
-        } else {
-          const int g = rr + kRun;  // > 0
-          const int qr = (int)(((unsigned long long)g * p.magic) >> 32);
-          const int e = g - qr * Li;
-          if (qr >= 1 && e < kRun) hp = e;
-        }
-      }
-
-      // 1. Sequential per-class scan of the run.  acc[c] runs over class c;
-      // the first float of each class at or after the head starts it again.
-      // v[e] becomes the float's running value (inclusive, or the value
-      // before it when exclusive); pre[c] ends as class c's total over the
-      // floats before the head.
-      float acc[P], pre[P];
-#pragma unroll
-      for (int c = 0; c < P; ++c) acc[c] = pre[c] = Op::identity();
-      if (!__any_sync(kFullMask, hp > 0 && hp < kRun)) {
-        // No head inside a run of this warp (hp is 0 or kRun everywhere).
-#pragma unroll
-        for (int e = 0; e < kRun; ++e) {
-          const int c = e % P;
-          const float before = acc[c];
-          acc[c] = Op::combine(acc[c], v[e]);
-          if constexpr (SCAN) v[e] = EXCL ? before : acc[c];
-        }
-        if (hp == kRun) {
-#pragma unroll
-          for (int c = 0; c < P; ++c) pre[c] = acc[c];
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < kRun; ++e) {
-          const int c = e % P;
-          const bool restart = (unsigned)(e - hp) < (unsigned)P;  // first of its class in the new plane
-          const float before = restart ? Op::identity() : acc[c];
-          acc[c] = restart ? v[e] : Op::combine(acc[c], v[e]);
-          if constexpr (SCAN) v[e] = EXCL ? before : acc[c];
-          if (e < hp) pre[c] = acc[c];
-        }
-        // A class with no float after a head near the run's end (positions
-        // kRun - P + c hold class c) keeps nothing for the new plane.
-#pragma unroll
-        for (int c = 0; c < P; ++c)
-          if (kRun - P + c < hp && hp < kRun) acc[c] = Op::identity();
-      }
-
-      // 2. Segmented inclusive scan of the runs' last-segment totals across
-      // the warp: lane l adds only lanes at or after hh, its last lane with a
-      // head (every lane between hh and l has the same hh, so the
-      // Hillis-Steele steps stay inside the segment).
-      const unsigned hmask = __ballot_sync(kFullMask, hp < kRun);
-      const unsigned upto = hmask & (kFullMask >> (31 - lane));
-      const int hh = upto ? 31 - __clz((int)upto) : 0;
-      float inc[P];
-#pragma unroll
-      for (int c = 0; c < P; ++c) inc[c] = acc[c];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const bool take = lane - o >= hh;
-#pragma unroll
-        for (int c = 0; c < P; ++c) {
-          const float u = __shfl_up_sync(kFullMask, inc[c], o);
-          if (take) inc[c] = Op::combine(u, inc[c]);
-        }
-      }
-      float ex[P];  // the lanes before mine, within my first float's segment
-#pragma unroll
-      for (int c = 0; c < P; ++c) ex[c] = __shfl_up_sync(kFullMask, inc[c], 1);
-      const bool head_before = (hmask & ((1u << lane) - 1u)) != 0;
-      if (lane == 31) {
-#pragma unroll
-        for (int c = 0; c < P; ++c) s_wagg[par][w][c] = inc[c];
-        s_wflag[par][w] = hmask != 0;
-      }
+      RunState<P> st;
+      int dd, qf;
+      find_head<REV>(a, rlo, rhi, p.k == 1, Li, p.magic, st.hp, dd, qf);
+      runs_phase1<P, SCAN, REV, EXCL, Op>(st, buf, a, s_wagg[par], s_wflag[par]);
+      if constexpr (!SCAN) fence_proxy_async_smem();  // the buffer is refilled after barrier 1
       // Barrier 1: warp totals visible; every thread is past its wait for
       // this tile and done with the previous tile's buffer.
       if (__syncthreads_or(!landed)) {
@@ -308,70 +402,24 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
           ++outstanding;
         }
       }
-
-      // 3. Carry into my warp: the previous tile's carry, then the warps
-      // before mine in order (a warp with a head restarts it).
-      float cw[P];
+      float carry[P], cl[P];
 #pragma unroll
-      for (int c = 0; c < P; ++c) cw[c] = j == 0 ? Op::identity() : s_carry[par][c];
-#pragma unroll
-      for (int q = 0; q < kNW - 1; ++q) {
-        if (q < w) {
-          const bool f = s_wflag[par][q] != 0;
-#pragma unroll
-          for (int c = 0; c < P; ++c) cw[c] = f ? s_wagg[par][q][c] : Op::combine(cw[c], s_wagg[par][q][c]);
-        }
-      }
-      if (w == kNW - 1 && lane == 0) {
-        const bool f = s_wflag[par][kNW - 1] != 0;
-#pragma unroll
-        for (int c = 0; c < P; ++c)
-          s_carry[par ^ 1][c] = f ? s_wagg[par][kNW - 1][c] : Op::combine(cw[c], s_wagg[par][kNW - 1][c]);
-      }
-      float cl[P];  // carry into my run's floats before its head
-#pragma unroll
-      for (int c = 0; c < P; ++c)
-        cl[c] = lane == 0 ? cw[c] : (head_before ? ex[c] : Op::combine(cw[c], ex[c]));
-
+      for (int c = 0; c < P; ++c) carry[c] = j == 0 ? Op::identity() : s_carry[par][c];
+      runs_phase2<P, SCAN, Op>(st, carry, s_wagg[par], s_wflag[par], s_carry[par ^ 1], cl);
       if constexpr (SCAN) {
-        // 4. Outputs: the floats before the head take the carry; the run
-        // goes back to its place, and the item's floats in the tile leave by
-        // one bulk store of their whole granules [ga, gb) plus plain stores
-        // of the partial granules at the item's two ends.
-#pragma unroll
-        for (int e = 0; e < kRun; ++e)
-          if (e < hp) v[e] = Op::combine(cl[e % P], v[e]);
-        float4* dst = reinterpret_cast<float4*>(buf + a);
-#pragma unroll
-        for (int k = 0; k < kChunks; ++k) {
-          float e4[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int i = 4 * k + c;
-            e4[c] = v[REV ? kRun - 1 - i : i];
-          }
-          dst[k] = make_float4(e4[0], e4[1], e4[2], e4[3]);
-        }
+        // The item's floats in the tile leave by one bulk store.
+        put_run<REV>(st.v, buf, a);
         fence_proxy_async_smem();
         __syncthreads();
-        const int lo = min(max(rlo, 0), kTile);
-        const int hi = min(max(rhi, 0), kTile);
-        const int ga = (lo + 3) & ~3;
-        const int gb = hi & ~3;
-        float* yt = p.y + ts;
-        if (t == 0 && ga < gb) bulk_store(yt + ga, buf + ga, (unsigned)(gb - ga) * 4u);
-        if (t < 8) {
-          const int f = t < 4 ? lo + t : max(gb, ga) + (t - 4);
-          if (f < (t < 4 ? min(ga, hi) : hi)) st_stream1(yt + f, buf[f]);
-        }
-      }
-      else {
-        // 4. A plane ending in my run: its class totals are my carry plus my
+        store_tile_out(buf, p.y + ts, min(max(rlo, 0), kTile), min(max(rhi, 0), kTile));
+        fence_proxy_async_smem();
+      } else {
+        // A plane ending in my run: its class totals are my carry plus my
         // floats before the boundary.
         if (dd >= 1 && qf >= 1 && qf <= it.planes) {
           float* out = p.y + (it.first + qf - 1) * P;
 #pragma unroll
-          for (int c = 0; c < P; ++c) st_plain(out + c, finish(Op::combine(cl[c], pre[c]), p.flags, p.N));
+          for (int c = 0; c < P; ++c) st_plain(out + c, finish(Op::combine(cl[c], st.pre[c]), p.flags, p.N));
         }
       }
       started = true;
@@ -397,6 +445,262 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
       }
     }
     if constexpr (SCAN) bulk_store_wait_all();  // the stores read shared memory until done
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Few long planes: one tile per block, the carry by look-back.
+//
+// The block with ticket t (tickets in scan order, plane after plane)
+//   1. starts bulk copies of tile t and of tile u = t - lag (the second
+//      normally served from L2: u was first read lag tiles ago);
+//   2. writes out tile u: its carry is the sum of the tiles before it in its
+//      plane, read from the 32-ary look-back tree (warp L reads level L;
+//      every node it needs was published about lag tickets ago), then the
+//      tile scan of both kernels with that carry, and a bulk store;
+//   3. sums tile t per class (a fixed tree) and publishes the sums, and every
+//      parent node this tile completes, as the row look-back does.
+// A forward scan takes 3 before 2, a reverse scan 2 before 3 (as the row
+// look-back measured best).  Tickets are taken in order by running blocks
+// and a block waits only on tiles of smaller tickets, so every wait ends;
+// each is bounded all the same.  (A persistent form, each block taking its
+// next ticket and starting its copies while it works on the current one, ran
+// at a third of this speed: the ticket's round trip and the wait for the
+// previous store's shared-memory reads stalled the whole block every tile.)
+// ---------------------------------------------------------------------------
+template <int P>
+struct LbTile {
+  int64_t plane, j;  // plane and scan-order tile index
+  int64_t lo, hi;    // the plane's floats
+  int64_t ts;        // the tile's first float
+  bool real;         // the plane has tile j
+};
+
+// Tickets are below 2^31 (the host bounds them by the node words).
+template <int P, bool REV>
+__device__ __forceinline__ LbTile<P> lb_tile(const PlaneLbParams& p, int64_t q) {
+  const int64_t L = p.N * P;
+  LbTile<P> g;
+  g.plane = (unsigned)q / (unsigned)p.tiles;
+  g.j = q - g.plane * p.tiles;
+  g.lo = g.plane * L;
+  g.hi = g.lo + L;
+  const int64_t vlo = g.lo - g.lo % kPlaneAlign<P>;
+  const int64_t nt = (g.hi - vlo + kTile - 1) / kTile;
+  g.real = g.j < nt;
+  g.ts = vlo + (REV ? nt - 1 - g.j : g.j) * kTile;
+  return g;
+}
+
+template <int P>
+__device__ __forceinline__ void lb_copy(const PlaneLbParams& p, const LbTile<P>& g, float* buf,
+                                        unsigned long long* bar) {
+  const int64_t te = min(g.ts + kTile, (g.hi + 3) & ~(int64_t)3);
+  const unsigned bytes = (unsigned)(te - g.ts) * 4u;
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_load(buf, p.x + g.ts, bytes, bar);
+}
+
+template <int P, bool REV, bool EXCL>
+__global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
+  __shared__ __align__(128) float s_new[kTile];  // tile `ticket`
+  __shared__ __align__(128) float s_old[kTile];  // tile `ticket - lag`
+  __shared__ __align__(8) unsigned long long s_bar[2];
+  __shared__ float s_wagg[kNW][P];
+  __shared__ int s_wflag[kNW];
+  __shared__ float s_red[kNW][P];
+  __shared__ float s_part[kPlanesLbLevels][P];
+  __shared__ unsigned s_ticket, s_epoch;
+  __shared__ int s_fail, s_copies;
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int w = t >> 5;
+  const unsigned* abort_word = p.err_word + 1;
+  const int64_t total = p.outer * p.tiles;
+  const int a = (REV ? kT - 1 - t : t) * kRun;  // my run's first float in a tile
+
+  if (t == 0) {
+    const Ticket tk = take_ticket(p.ticket_word);
+    s_ticket = tk.ticket;
+    s_epoch = tk.epoch;
+    s_fail = 0;
+    // Every other ticket is taken before the last one: reset for the next launch.
+    if ((int64_t)tk.ticket == total + p.lag - 1) next_launch(p.ticket_word, tk.epoch);
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    fence_mbar_init();
+    int copies = 0;
+    if ((int64_t)tk.ticket < total) {
+      const LbTile<P> g = lb_tile<P, REV>(p, tk.ticket);
+      if (g.real) {
+        lb_copy<P>(p, g, s_new, &s_bar[0]);
+        copies |= 1;
+      }
+    }
+    const int64_t u = (int64_t)tk.ticket - p.lag;
+    if (u >= 0 && u < total) {
+      const LbTile<P> g = lb_tile<P, REV>(p, u);
+      if (g.real) {
+        lb_copy<P>(p, g, s_old, &s_bar[1]);
+        copies |= 2;
+      }
+    }
+    s_copies = copies;
+  }
+  __syncthreads();
+  const int64_t ticket = s_ticket;
+  const unsigned epoch = s_epoch;
+  if (ticket >= total + p.lag) {  // a stale counter: no copy was started, touch nothing
+    if (t == 0) atomicOr(p.err_word, 2u);
+    return;
+  }
+  int levels = 1;
+  while (levels < kPlanesLbLevels && ((p.tiles - 1) >> (5 * levels)) != 0) ++levels;
+
+  // ---- write out tile u = ticket - lag ----
+  const auto write_out = [&]() {
+    const int64_t u = ticket - p.lag;
+    if (u < 0) return;
+    const LbTile<P> g = lb_tile<P, REV>(p, u);
+    if (!g.real) return;
+    const unsigned long long* vals = p.node_val + g.plane * 2 * p.tiles * P;
+    if (w < levels) {
+      int64_t off = 0, count = p.tiles;
+      for (int q = 0; q < w; ++q) {
+        off += count;
+        count >>= 5;
+      }
+      const int64_t m = g.j >> (5 * w);
+      const int d = (int)(m & 31);
+      bool fail = false;
+      float sib[P];
+#pragma unroll
+      for (int c = 0; c < P; ++c) sib[c] = 0.f;
+      if (lane < d) wait_node_classes<P>(vals + (off + (m - d) + lane) * P, epoch, p.spin_limit, abort_word, &fail, sib);
+#pragma unroll
+      for (int c = 0; c < P; ++c) {
+        const float part = warp_tree_adjacent(sib[c]);
+        if (lane == 0) s_part[w][c] = part;
+      }
+      if (__any_sync(kFullMask, fail) && lane == 0) s_fail = 1;
+    }
+    const bool landed = mbar_wait_copy(&s_bar[1], 0u);
+    const int rlo = rel_sat(g.lo, g.ts);
+    const int rhi = rel_sat(g.hi, g.ts);
+    RunState<P> st;
+    int dd, qf;
+    find_head<REV>(a, rlo, rhi, true, 0, 0ull, st.hp, dd, qf);
+    runs_phase1<P, true, REV, EXCL, OpSum>(st, s_old, a, s_wagg, s_wflag);
+    // The barrier also publishes s_part: each class's carry is its
+    // look-back partials from the lowest level up.
+    if (__syncthreads_or(!landed)) {
+      if (t == 0) s_fail = 1;
+      return;  // the copy never landed: no outputs
+    }
+    float carry[P], cl[P];
+#pragma unroll
+    for (int c = 0; c < P; ++c) {
+      float e = 0.f;
+      for (int L = 0; L < levels; ++L) e += s_part[L][c];
+      carry[c] = e;
+    }
+    runs_phase2<P, true, OpSum>(st, carry, s_wagg, s_wflag, nullptr, cl);
+    put_run<REV>(st.v, s_old, a);
+    fence_proxy_async_smem();
+    __syncthreads();
+    store_tile_out(s_old, p.y + g.ts, min(max(rlo, 0), kTile), min(max(rhi, 0), kTile));
+  };
+
+  // ---- sum tile `ticket` per class and publish it ----
+  const auto publish = [&]() {
+    if (ticket >= total) return;
+    const LbTile<P> g = lb_tile<P, REV>(p, ticket);
+    float own[P];
+#pragma unroll
+    for (int c = 0; c < P; ++c) own[c] = 0.f;
+    if (g.real) {  // an empty last tile publishes zeros
+      const bool landed = mbar_wait_copy(&s_bar[0], 0u);
+      // My run's class sums in scan order (the classes as the tile scan
+      // numbers them), only the plane's own floats.
+      const int rlo = rel_sat(g.lo, g.ts);
+      const int rhi = rel_sat(g.hi, g.ts);
+      const float4* src = reinterpret_cast<const float4*>(s_new + a);
+      const bool edge = rlo > a || rhi < a + kRun;
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k) {
+        const float4 q = src[k];
+        const float e4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int i = 4 * k + c;  // memory position a + i
+          const int e = REV ? kRun - 1 - i : i;
+          const bool in = !edge || (a + i >= rlo && a + i < rhi);
+          own[e % P] += in ? e4[c] : 0.f;
+        }
+      }
+      // Block sums per class: warp trees, then the warp totals in order.
+#pragma unroll
+      for (int c = 0; c < P; ++c) {
+        own[c] = warp_reduce<OpSum>(own[c]);
+        if (lane == 0) s_red[w][c] = own[c];
+      }
+      if (__syncthreads_or(!landed)) {
+        if (t == 0) s_fail = 1;
+        return;  // nothing published: the tiles behind it wait out and fail
+      }
+#pragma unroll
+      for (int c = 0; c < P; ++c) {
+        float r = s_red[0][c];
+#pragma unroll
+        for (int q = 1; q < kNW; ++q) r += s_red[q][c];
+        own[c] = r;
+      }
+    }
+    unsigned long long* vals = p.node_val + g.plane * 2 * p.tiles * P;
+    if (w == 0 && ticket != p.stall_tile) {
+      if (lane < P) st_relaxed_u64(vals + g.j * P + lane, pack_node(epoch, pick_class<P>(own, lane)));
+      if ((g.j & 31) == 31) {  // publish every parent this tile completes
+        bool fail = false;
+        int64_t off = 0, count = p.tiles, m = g.j;
+        for (int L = 0; L < levels && (m & 31) == 31; ++L) {
+          float sib[P];
+#pragma unroll
+          for (int c = 0; c < P; ++c) sib[c] = 0.f;
+          if (lane < 31)
+            wait_node_classes<P>(vals + (off + (m - 31) + lane) * P, epoch, p.spin_limit, abort_word, &fail, sib);
+          if (__any_sync(kFullMask, fail)) break;
+#pragma unroll
+          for (int c = 0; c < P; ++c) {
+            const float parent = warp_tree_adjacent(lane < 31 ? sib[c] : own[c]);
+            own[c] = __shfl_sync(kFullMask, parent, 0);
+          }
+          const int64_t next_off = off + count;
+          if (lane < P)
+            st_relaxed_u64(vals + (next_off + (m >> 5)) * P + lane, pack_node(epoch, pick_class<P>(own, lane)));
+          off = next_off;
+          count >>= 5;
+          m >>= 5;
+        }
+        if (fail && lane == 0) s_fail = 1;
+      }
+    }
+  };
+
+  if constexpr (!REV) publish();
+  write_out();
+  if constexpr (REV) publish();
+  __syncthreads();
+  if (t == 0) {
+    if (s_fail) {
+      atomicOr(p.err_word, 1u);
+      atomicExch(p.err_word + 1, epoch);
+    }
+    // No copy may still write into this block's shared memory, and the bulk
+    // store must have read it, when the block leaves (bounded waits; a
+    // landed copy returns at once).
+    if (s_copies & 1) mbar_wait_copy(&s_bar[0], 0u);
+    if (s_copies & 2) mbar_wait_copy(&s_bar[1], 0u);
+    bulk_store_wait_all();
   }
 }
 
@@ -440,6 +744,26 @@ int occupancy_p(bool scan) {
                    occupancy_of(k_planes<P, true, true, true, OpSum>)});
 }
 
+template <int P>
+cudaError_t launch_lb_p(const PlaneLbParams& p, dim3 g, cudaStream_t s) {
+  const bool rev = (p.flags & kScanMirror) == 0;
+  const bool excl = (p.flags & kScanExclusive) != 0;
+  if (rev) {
+    if (excl) k_planes_lb<P, true, true><<<g, kT, 0, s>>>(p);
+    else k_planes_lb<P, true, false><<<g, kT, 0, s>>>(p);
+  } else {
+    if (excl) k_planes_lb<P, false, true><<<g, kT, 0, s>>>(p);
+    else k_planes_lb<P, false, false><<<g, kT, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+template <int P>
+int occupancy_lb_p() {
+  return std::min({occupancy_of(k_planes_lb<P, false, false>), occupancy_of(k_planes_lb<P, false, true>),
+                   occupancy_of(k_planes_lb<P, true, false>), occupancy_of(k_planes_lb<P, true, true>)});
+}
+
 }  // namespace
 
 cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cudaStream_t s) {
@@ -459,6 +783,25 @@ cudaError_t launch_planes_reduce(int P, int op, const PlaneRunParams& p, int64_t
     case 3: return launch_reduce_p<3>(op, p, g, s);
     case 4: return launch_reduce_p<4>(op, p, g, s);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_planes_lookback(int P, const PlaneLbParams& p, int64_t grid, cudaStream_t s) {
+  const dim3 g((unsigned)grid);
+  switch (P) {
+    case 2: return launch_lb_p<2>(p, g, s);
+    case 3: return launch_lb_p<3>(p, g, s);
+    case 4: return launch_lb_p<4>(p, g, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int occupancy_planes_lookback(int P) {
+  switch (P) {
+    case 2: return occupancy_lb_p<2>();
+    case 3: return occupancy_lb_p<3>();
+    case 4: return occupancy_lb_p<4>();
+    default: return 0;
   }
 }
 

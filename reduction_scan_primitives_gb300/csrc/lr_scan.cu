@@ -354,31 +354,6 @@ __device__ __forceinline__ void block_sum_p(float (&v)[P], float (&sh)[kNW][P]) 
   }
 }
 
-// The P class words of one look-back node (consecutive words from `node`):
-// all P loads are issued at once, then only the words not yet carrying this
-// launch's epoch are polled (bounded, as wait_node).
-template <int P>
-__device__ __forceinline__ void wait_node_classes(const unsigned long long* node, unsigned epoch, int64_t limit,
-                                                  const unsigned* abort_word, bool* fail, float (&out)[P]) {
-  unsigned long long word[P];
-#pragma unroll
-  for (int c = 0; c < P; ++c) word[c] = ld_relaxed_u64(node + c);
-#pragma unroll
-  for (int c = 0; c < P; ++c)
-    out[c] = (unsigned)(word[c] >> 32) == epoch ? __uint_as_float((unsigned)word[c])
-                                                : wait_node(node + c, epoch, limit, abort_word, fail);
-}
-
-// a[i] selected by a run-time index (registers cannot be indexed at run time).
-template <int P>
-__device__ __forceinline__ float pick_class(const float (&a)[P], int i) {
-  float r = a[0];
-#pragma unroll
-  for (int c = 1; c < P; ++c)
-    if (i == c) r = a[c];
-  return r;
-}
-
 // ---------------------------------------------------------------------------
 // Block per row: tiles right to left, carry in registers, next tile
 // prefetched into registers while the current one is scanned.

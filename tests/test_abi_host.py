@@ -139,8 +139,8 @@ def test_options(lib):
                      (L.OPT_RSCAN_VARIANT, -1), (L.OPT_WAVES, 0), (L.OPT_LOOKBACK_LAG, 0),
                      (L.OPT_SCAN_COLS_VARIANT, -1)):
         assert lib.libreduce_set_option(opt, val) == L.OK
-    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 8) == L.OK
-    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 9) == L.ERR_INVALID_ARG
+    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 9) == L.OK
+    assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, 10) == L.ERR_INVALID_ARG
     assert lib.libreduce_set_option(L.OPT_SCAN_COLS_VARIANT, -1) == L.OK
     assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 9) == L.OK
     assert lib.libreduce_set_option(L.OPT_COLS_VARIANT, 10) == L.ERR_INVALID_ARG

@@ -152,3 +152,80 @@ def test_misaligned_falls_back():
     L.check()
     ref, scale = oracle.cumsum(x.numpy(), *shape, False, False)
     assert_close(y.cpu().numpy(), ref, scale, "misaligned plane runs")
+
+
+# ---- few long planes: the look-back form (one tile per block) ----------------------
+
+SCAN_LOOKBACK = 9  # LIBREDUCE_OPT_SCAN_COLS_VARIANT: the same tiles, a plane over blocks
+# One plane of ~650 tiles (two levels of the 32-ary tree), planes of 7, 3 and
+# one tile, plane lengths that are and are not multiples of the 16-byte
+# granule (and of 12 floats for 3 columns), a plane of 33 tiles (a level-1
+# parent completed by its 32nd tile).
+LB_SHAPES = [(1, 1_000_003, 3), (3, 400_000, 4), (5, 250_001, 2), (7, 10_001, 3), (4, 4609, 2),
+             (3, 50, 3), (2, 38_017, 4), (1, 76_033, 2)]
+
+
+def scan_lb(x, reverse, exclusive, forced=True):
+    if forced:
+        L.set_option(L.OPT_SCAN_COLS_VARIANT, SCAN_LOOKBACK)
+    y = L.cumsum_f32(on_device(x), 1, reverse=reverse, exclusive=exclusive)
+    L.check()
+    return y
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape", LB_SHAPES)
+def test_lookback_against_oracle(shape, reverse, exclusive):
+    x = inputs.make(shape, "uniform_pm1", 41)
+    y = scan_lb(x, reverse, exclusive)
+    ref, scale = oracle.cumsum(x.numpy(), *shape, reverse, exclusive)
+    assert_close(y.cpu().numpy(), ref, scale, f"plane look-back {shape} rev={reverse} excl={exclusive}")
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+def test_lookback_integers_exact_and_bitwise(reverse, exclusive):
+    """{0..3}: every prefix below 2^24 (at most 3 * 1.3e6), so exact."""
+    shape = (2, 1_300_001, 2)
+    x = inputs.make(shape, "int:0:3", 42)
+    a = scan_lb(x, reverse, exclusive).clone()
+    b = scan_lb(x, reverse, exclusive)
+    assert bitwise_equal(a, b), "reruns differ"
+    ref, _ = oracle.cumsum(x.numpy(), *shape, reverse, exclusive)
+    assert_exact(a.cpu().numpy(), ref, "plane look-back integers")
+
+
+@pytest.mark.parametrize("lag", [64, 640, 4096])
+def test_lookback_lags(lag):
+    """Any lag gives the same bits (the carries never depend on timing)."""
+    shape = (1, 3_000_001, 3)
+    x = inputs.make(shape, "uniform_pm1", 43)
+    base = scan_lb(x, False, False).clone()
+    L.set_option(L.OPT_LOOKBACK_LAG, lag)
+    assert bitwise_equal(base, scan_lb(x, False, False))
+
+
+def test_lookback_is_the_automatic_choice_for_few_long_planes():
+    shape = (1, 40_000_000, 4)
+    x = inputs.make(shape, "uniform_pm1", 44)
+    auto = scan_lb(x, False, False, forced=False).clone()
+    assert bitwise_equal(auto, scan_lb(x, False, False))
+
+
+def test_lookback_bounded_wait_reports_timeout():
+    """A tile that never publishes (chosen on the host) makes the waits
+    behind it run out: the host reads TIMEOUT, and the next call is right."""
+    shape = (1, 2_000_000, 3)
+    x = inputs.make(shape, "uniform01", 45)
+    xd = on_device(x)
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, SCAN_LOOKBACK)
+    L.set_option(L.OPT_SPIN_LIMIT, 2000)
+    L.set_option(L.OPT_STALL_TILE, 5)
+    L.cumsum_f32(xd, 1)
+    with pytest.raises(L.LibreduceError) as ei:
+        L.check()
+    assert ei.value.status == L.ERR_TIMEOUT
+    L.set_option(L.OPT_STALL_TILE, -1)
+    L.set_option(L.OPT_SPIN_LIMIT, 0)
+    L.check()
+    ref, scale = oracle.cumsum(x.numpy(), *shape, False, False)
+    assert_close(L.cumsum_f32(xd, 1).cpu().numpy(), ref, scale, "after timeout")
