@@ -328,9 +328,10 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 planes (reduce <= 2048, inner <= 256, a plane in
  *                                 24 KB of shared memory), each column reduced as a
  *                                 short row (the automatic choice for planes of at
- *                                 most 768 floats); 9 planes of 2, 3 or 4 columns
+ *                                 most 768 floats); 9 planes of 2 to 8 columns
  *                                 read flat as segmented class runs (x 16-byte
- *                                 aligned, planes of more than 36 floats; the
+ *                                 aligned, planes longer than a thread's run of
+ *                                 20 to 36 floats; the
  *                                 automatic choice from one item of planes per SM
  *                                 on)
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
@@ -358,12 +359,16 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 offset mod 16 bytes), each column a class of
  *                                 every 2nd or 4th element, by the row kernels
  *                                 (the automatic choice for 2-column planes of at
- *                                 least 4096 floats, after form 8); 8 planes of 2, 3
- *                                 or 4 columns read flat as segmented class runs
- *                                 (x and y 16-byte aligned, planes of more than 36
- *                                 floats; the automatic choice from one item per SM
- *                                 on, an item being one plane or as many short
- *                                 planes as fit a 4608-float tile)
+ *                                 least 4096 floats, after forms 8 and 9); 8 planes
+ *                                 of 2 to 8 columns read flat as segmented class
+ *                                 runs (x and y 16-byte aligned, planes longer than
+ *                                 a thread's run of 20 to 36 floats; the automatic
+ *                                 choice from one item per SM on, an item being one
+ *                                 plane or as many short planes as fit a tile of
+ *                                 2560 to 4608 floats); 9 the same tiles with a
+ *                                 plane's tiles spread over blocks and their carries
+ *                                 from a look-back (the automatic choice for fewer
+ *                                 items than SMs when planes hold two tiles or more)
  *                                 (float4 columns need inner % 4 == 0 and aligned x, y) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6

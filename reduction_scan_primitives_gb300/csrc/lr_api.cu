@@ -61,8 +61,8 @@ struct DeviceState {
   int occ_rscan_short = 0;
   int occ_rscan_period[3] = {};     // float4 block per row, period 1, 2, 4
   int occ_lookback_period[3] = {};  // L2 look-back, period 1, 2, 4
-  int occ_planes[3][2] = {};        // narrow planes read flat: [P - 2][scan]
-  int occ_planes_lb[3] = {};        // the same, look-back form: [P - 2]
+  int occ_planes[kPlanesMaxP - 1][2] = {};  // narrow planes read flat: [P - 2][scan]
+  int occ_planes_lb[kPlanesMaxP - 1] = {};  // the same, look-back form: [P - 2]
 };
 
 // Index of a period (1, 2, 4) in the per-period tables.
@@ -136,9 +136,10 @@ int device_state(DeviceState** out, int* dev_out) {
       st.occ_lookback_period[pi] = std::max(1, occupancy_rscan_lookback_period(1 << pi));
     }
     st.occ_rscan_short = std::max(1, occupancy_rscan_short());
-    for (int pi = 0; pi < 3; ++pi)
+    for (int pi = 0; pi < kPlanesMaxP - 1; ++pi) {
       for (int sc = 0; sc < 2; ++sc) st.occ_planes[pi][sc] = std::max(1, occupancy_planes(pi + 2, sc != 0));
-    for (int pi = 0; pi < 3; ++pi) st.occ_planes_lb[pi] = std::max(1, occupancy_planes_lookback(pi + 2));
+      st.occ_planes_lb[pi] = std::max(1, occupancy_planes_lookback(pi + 2));
+    }
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
   }
@@ -536,20 +537,22 @@ int run_narrow(const Provider& pv, const float* x, int64_t outer, int64_t reduce
   return launched(launch_reduce_narrow(vec, op, p, grid, s));
 }
 
-// Narrow planes of 2, 3 or 4 columns read flat as segmented class runs
+// Narrow planes of 2-8 columns read flat as segmented class runs
 // (lr_planes.cu): planes per item and items, or false when the shape does not
-// fit (planes of at most kPlanesRun floats).  Short planes go k >= 2 to a
-// tile (the item's start is rounded down to a multiple of 4 floats, 12 for
-// three columns); longer ones one to an item.
+// fit (planes of at most one thread run).  Short planes go k >= 2 to a tile
+// (the item's start is rounded down to planes_align floats); longer ones one
+// to an item.
 struct PlaneRunPlan {
   int64_t k = 1, items = 0;
   unsigned long long magic = 0;
 };
 bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl) {
   int64_t L = 0;
-  if (inner < 2 || inner > 4 || outer <= 0 || mul_overflows(N, inner, &L) || L <= kPlanesRun) return false;
-  const int64_t align = inner == 3 ? 12 : 4;
-  const int64_t k = (kPlanesTile - align + 1) / L;
+  if (inner < 2 || inner > kPlanesMaxP || outer <= 0 || mul_overflows(N, inner, &L) ||
+      L <= planes_run_len((int)inner))
+    return false;
+  const int64_t align = planes_align((int)inner);
+  const int64_t k = (planes_tile_len((int)inner) - align + 1) / L;
   pl->k = k >= 2 ? k : 1;
   pl->items = ceil_div(outer, pl->k);
   pl->magic = pl->k >= 2 ? ((1ull << 32) + (unsigned long long)L - 1) / (unsigned long long)L : 0;
@@ -563,12 +566,23 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl) {
 // [200, 50000, 4] 0.83 / 0.56, [100, 20000, 2] 0.49 / 0.31; sums [512, 3000,
 // 3] 0.69 / 0.37, [300, 5000, 4] 0.64 / 0.38); with only tens of planes a
 // block per plane leaves most SMs idle.
-bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl) { return pl.items >= st->sm_count; }
+// Eight columns (two float4s a row) keep the narrow kernels for planes of a
+// tile or more and for reductions, which those read as whole float4 rows
+// (fractions, runs against them: scans [1000, 10000, 8] 0.72 / 0.83, sums
+// [100000, 100, 8] 0.57 / 0.60; short-plane scans [100000, 100, 8] 0.89 /
+// 0.54 take the runs).
+bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t inner, bool scan) {
+  if (inner == 8 && (!scan || pl.k < 2)) return false;
+  return pl.items >= st->sm_count;
+}
 // Fewer items than SMs: the look-back form, whose blocks take single tiles,
 // when the planes hold at least two tiles each (measured in the plane-run
 // tests; below that the items' blocks are few and short either way).
+// Only with runs of 36 floats (2, 3, 4, 6 columns): the shorter tiles of 5,
+// 7 and 8 columns leave one block per 10-12 KB tile too little to do
+// ([1, 3e7, 5] 0.48, [2, 2e7, 8] 0.39 of copy bandwidth).
 bool plane_runs_split(const DeviceState* st, const PlaneRunPlan& pl, int64_t N, int64_t inner) {
-  return pl.items < st->sm_count && N * inner >= 2 * kPlanesTile;
+  return planes_run_len((int)inner) == 36 && pl.items < st->sm_count && N * inner >= 2 * planes_tile_len((int)inner);
 }
 int run_planes(const Provider& pv, const PlaneRunPlan& pl, const float* x, int64_t outer, int64_t N,
                int64_t inner, float* y, int flags, bool scan, int op, cudaStream_t s) {
@@ -585,15 +599,15 @@ int run_planes(const Provider& pv, const PlaneRunPlan& pl, const float* x, int64
                        : launch_planes_reduce((int)inner, op, p, grid, s));
 }
 
-// Scans of few long planes of 2-4 columns by the look-back form of the
+// Scans of few long planes of 2-8 columns by the look-back form of the
 // segmented class runs: one block per tile, the tiles of a plane in scan
 // order, each plane's carries from its own look-back tree.  kColLbNoFit when
 // its tiles exceed the node words.
 int run_planes_lookback(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner, float* y,
                         int flags, cudaStream_t s) {
   DeviceState* st = pv.st;
-  const int64_t align = inner == 3 ? 12 : 4;
-  const int64_t tiles = ceil_div(N * inner + align - 1, kPlanesTile);  // the most any plane covers
+  const int64_t align = planes_align((int)inner);
+  const int64_t tiles = ceil_div(N * inner + align - 1, planes_tile_len((int)inner));  // the most any plane covers
   int64_t total = 0;
   if (mul_overflows(outer, tiles, &total) || total > kMaxLookbackTiles / inner ||
       tiles > (int64_t(1) << (5 * kPlanesLbLevels)))
@@ -629,7 +643,7 @@ int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, 
     PlaneRunPlan pl;
     if ((fv < 0 || fv == kColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
         (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && plane_run_plan(outer, reduce, inner, &pl) &&
-        (fv == kColsPlaneRuns || plane_runs_fill(st, pl)))
+        (fv == kColsPlaneRuns || plane_runs_fill(st, pl, inner, false)))
       return run_planes(pv, pl, x, outer, reduce, inner, out, epi, false, op, s);
     if (fv == kColsPlaneRuns) fv = -1;  // forced on a shape it does not take: the automatic choice
     if ((fv < 0 || fv == kColsShortPlanes) && g_opt_axis_split.load() <= 0) {
@@ -1161,7 +1175,7 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
     PlaneRunPlan pl;
     if ((fv < 0 || fv == kScanColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
         ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
-        plane_run_plan(outer, N, inner, &pl) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl)))
+        plane_run_plan(outer, N, inner, &pl) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl, inner, true)))
       return run_planes(pv, pl, x, outer, N, inner, y, (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0),
                         true, kOpSum, s);
     if ((fv < 0 || fv == kScanColsPlaneLookback) && g_opt_axis_split.load() <= 0 &&

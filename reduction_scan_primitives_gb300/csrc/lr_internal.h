@@ -129,16 +129,22 @@ struct ShortRowsParams {
   unsigned long long magic_inner;
 };
 
-// --- Narrow planes of 2, 3 or 4 columns, read flat (segmented class runs) ----
-// x is [outer, N, P] (P = 2, 3 or 4 columns), scanned or reduced along N.
+// --- Narrow planes of 2-8 columns, read flat (segmented class runs) -----------
+// x is [outer, N, P] (P = 2 .. kPlanesMaxP columns), scanned or reduced along N.
 // Plane o is the L = N*P floats from o*L; the float at flat index f is in
 // column f % P.  Work is cut into items of k whole planes: k >= 2 planes fit
-// one tile of kPlanesTile floats (with the item's start rounded down to a
-// 16-byte boundary); k = 1 covers a plane in one or more tiles.  x (and y for
-// scans) must be 16-byte aligned and L > kPlanesRun.
-constexpr int kPlanesThreads = 128;                       // threads per block (this kernel only)
-constexpr int kPlanesRun = 36;                            // consecutive floats per thread
-constexpr int kPlanesTile = kPlanesThreads * kPlanesRun;  // floats per tile
+// one tile of planes_tile_len(P) floats (with the item's start rounded down
+// to planes_align(P)); k = 1 covers a plane in one or more tiles.  x (and y
+// for scans) must be 16-byte aligned and L > planes_run_len(P).
+constexpr int kPlanesThreads = 128;  // threads per block (these kernels only)
+constexpr int kPlanesMaxP = 8;       // columns: 2 .. kPlanesMaxP
+// Consecutive floats per thread (whole rows of P columns), the alignment of
+// runs and tiles (16 bytes and P), and floats per tile.
+__host__ __device__ constexpr int planes_run_len(int P) { return P == 5 ? 20 : P == 7 ? 28 : P == 8 ? 24 : 36; }
+__host__ __device__ constexpr int planes_align(int P) {
+  return P == 3 || P == 6 ? 12 : P == 5 ? 20 : P == 7 ? 28 : P == 8 ? 8 : 4;
+}
+__host__ __device__ constexpr int planes_tile_len(int P) { return kPlanesThreads * planes_run_len(P); }
 struct PlaneRunParams {
   const float* x;
   float* y;            // scans: [outer, N, P]; reductions: [outer, P]
@@ -146,12 +152,12 @@ struct PlaneRunParams {
   int64_t N;
   int64_t k;           // planes per item
   int64_t items;       // ceil(outer / k)
-  unsigned long long magic;  // ceil(2^32 / L) when k >= 2 (then L < kPlanesTile)
+  unsigned long long magic;  // ceil(2^32 / L) when k >= 2 (then L < planes_tile_len(P) / 2)
   int flags;           // scans: kScanMirror | kScanExclusive; reductions: the epilogue
   unsigned* err_word;  // bit 0 set if a tile's copy never lands
 };
 
-// Scans of few long planes of 2-4 columns, a plane's tiles spread over
+// Scans of few long planes of 2-8 columns, a plane's tiles spread over
 // blocks: scan-order tile j of plane o is ticket o * tiles + j, and each
 // tile's P class sums go through the deterministic 32-ary look-back of the
 // row scans (node words {epoch, fp32}, class c of node (L, m) of plane o at
@@ -370,7 +376,7 @@ cudaError_t launch_rscan_short(int lanes, int vec, const ShortRowsParams& p, int
 cudaError_t launch_reduce_short(int op, int lanes, int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s);
 int occupancy_rscan_short();
 cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, int64_t grid, cudaStream_t s);
-// Narrow planes read flat: P = 2, 3 or 4; reductions take any ReduceOp.
+// Narrow planes read flat: P = 2 .. kPlanesMaxP; reductions take any ReduceOp.
 cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_planes_reduce(int P, int op, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes(int P, bool scan);  // resident kPlanesThreads-thread blocks per SM

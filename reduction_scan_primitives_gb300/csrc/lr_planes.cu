@@ -1,5 +1,5 @@
 // lr_planes.cu -- cumulative sums and reductions along the middle axis of
-// [outer, N, P] for narrow planes of P = 2, 3 or 4 columns (sm_103a).
+// [outer, N, P] for narrow planes of P = 2 .. 8 columns (sm_103a).
 //
 // The POPCORNBENCH trace l1_p91 discusses scanning a dimension other than the
 // last; here that dimension has stride P.  Read flat, plane o is the L = N*P
@@ -12,18 +12,17 @@
 // Work is cut into items of k whole planes (k >= 2 short planes in one tile,
 // or one plane over one or more tiles).  A block takes items in turn and
 // processes an item's tiles in scan order, with a per-class carry from tile
-// to tile.  A tile of kPlanesTile floats lands in shared memory by one bulk
-// copy (TMA engine), three tiles in flight per block; its start is the
-// item's start rounded down to a 16-byte boundary (and to a multiple of P).
+// to tile.  A tile lands in shared memory by one bulk copy (TMA engine),
+// three tiles in flight per block; its start is the item's start rounded
+// down to a 16-byte boundary and a multiple of P.
 //
-// Thread t of the 128 owns run m of kPlanesRun = 36 consecutive floats of the
-// tile (m = t; m = 127 - t for a reverse scan, whose scan order runs down
-// memory).  36 is a multiple of every P and every run starts at a multiple of
-// P, so the column class of each of a thread's floats is known at compile
-// time; as L > 36, a run holds at most one plane boundary (its "head": the
-// scan position where a plane starts, in scan order).  A run is 9 float4
-// chunks, an odd number, so the runs of 8 consecutive threads fall in
-// distinct shared-memory banks.  The steps:
+// Thread t of the 128 owns run m of R consecutive floats of the tile (m = t;
+// m = 127 - t for a reverse scan, whose scan order runs down memory): R = 36
+// for 2, 3, 4 and 6 columns, 20 for 5, 28 for 7, 24 for 8 (kRunOf).  R holds
+// whole rows and every run starts at a multiple of P, so the column class of
+// each of a thread's floats is known at compile time; as L > R, a run holds
+// at most one plane boundary (its "head": the scan position where a plane
+// starts, in scan order).  The steps:
 //   1. a sequential per-class scan over the run, restarting at the head;
 //   2. a segmented shuffle scan of the run totals across the warp (per class,
 //      the lanes before a lane's last head excluded);
@@ -50,16 +49,22 @@ namespace {
 
 constexpr int kT = kPlanesThreads;
 constexpr int kNW = kT / 32;
-constexpr int kRun = kPlanesRun;
-constexpr int kTile = kPlanesTile;
-constexpr int kChunks = kRun / 4;  // float4 chunks per run
+// Floats per thread run for P columns: whole rows, a multiple of 4 (float4
+// chunks) and, where P allows, an odd number of chunks, so that the runs of
+// 8 consecutive threads fall in distinct shared-memory banks (8 columns: 6
+// chunks, two threads to a bank).  At most 36, so that three tiles of four
+// blocks fit an SM.
+template <int P>
+constexpr int kRunOf = planes_run_len(P);
+template <int P>
+constexpr int kTileOf = kT * kRunOf<P>;
+template <int P>
+constexpr int kChunksOf = kRunOf<P> / 4;
 constexpr int kStages = 3;
 constexpr int kLbBlocks = 6;  // resident look-back blocks per SM: 6 x 37 KB of tiles, <= 85 registers
-static_assert(kRun % 4 == 0 && kRun % 3 == 0 && (kChunks & 1) == 1,
-              "runs hold whole float4 chunks, a multiple of every P, an odd number of chunks");
 // Runs and tiles start on multiples of this many floats: 16 bytes and P.
 template <int P>
-constexpr int kPlaneAlign = P == 3 ? 12 : 4;
+constexpr int kPlaneAlign = planes_align(P);
 
 struct PlaneItem {
   int64_t lo, hi;  // the item's floats [lo, hi): planes first .. first + planes - 1
@@ -79,7 +84,7 @@ __device__ __forceinline__ PlaneItem plane_item(const PlaneRunParams& p, int64_t
   it.lo = it.first * L;
   it.hi = it.lo + planes * L;
   it.vlo = it.lo - it.lo % kPlaneAlign<P>;
-  it.tiles = (int)((it.hi - it.vlo + kTile - 1) / kTile);
+  it.tiles = (int)((it.hi - it.vlo + kTileOf<P> - 1) / kTileOf<P>);
   return it;
 }
 
@@ -93,18 +98,19 @@ struct Cursor {
 };
 
 // The first float of scan-order tile j of an item.
+template <int P>
 __device__ __forceinline__ int64_t tile_start(const PlaneItem& it, int j, bool rev) {
-  return it.vlo + (int64_t)(rev ? it.tiles - 1 - j : j) * kTile;
+  return it.vlo + (int64_t)(rev ? it.tiles - 1 - j : j) * kTileOf<P>;
 }
 
 template <int P>
 __device__ __forceinline__ void issue_tile(const PlaneRunParams& p, Cursor& c, bool rev, float* buf,
                                            unsigned long long* bar) {
   if (c.item >= p.items) return;
-  const int64_t ts = tile_start(c.it, c.tile, rev);
+  const int64_t ts = tile_start<P>(c.it, c.tile, rev);
   // Whole 16-byte granules up to the item's end: the last one lies in the
   // same page as the item's last float.
-  const int64_t te = min(ts + kTile, (c.it.hi + 3) & ~(int64_t)3);
+  const int64_t te = min(ts + kTileOf<P>, (c.it.hi + 3) & ~(int64_t)3);
   const unsigned bytes = (unsigned)(te - ts) * 4u;
   mbar_arrive_expect_tx(bar, bytes);
   bulk_load(buf, p.x + ts, bytes, bar);
@@ -129,15 +135,15 @@ __device__ __forceinline__ int rel_sat(int64_t a, int64_t b) {
 // One thread's share of a tile between the two phases.
 template <int P>
 struct RunState {
-  float v[kRun];     // my run in scan order: inputs, then running values, then outputs
+  float v[kRunOf<P>];     // my run in scan order: inputs, then running values, then outputs
   float pre[P];      // class totals of my floats before the head
   float ex[P];       // segmented totals of the lanes before mine in the warp
-  int hp;            // the head: scan position in my run where a plane starts (kRun: none)
+  int hp;            // the head: scan position in my run where a plane starts (kRunOf<P>: none)
   bool head_before;  // a lane before mine in the warp holds a head
 };
 
 // The head of my run (first float at a in the tile) and, for a reduction,
-// dd: my floats before the end of plane q - 1 of the item (1..kRun), else -1.
+// dd: my floats before the end of plane q - 1 of the item (1..kRunOf<P>), else -1.
 // Forward: boundaries at lo + q*L, q = 0 .. planes (the one at hi splits a
 // reduction's last run); reverse: a plane starts (in scan order) at its last
 // float, lo + q*L - 1, q >= 1.  Boundaries past the item only split floats
@@ -145,37 +151,37 @@ struct RunState {
 // one_plane: the item is one plane (boundaries at lo and hi only); else the
 // item's planes, shorter than a tile, all lie in this one (0 <= rlo <
 // kPlaneAlign) and Li, magic give L and ceil(2^32 / L).
-template <bool REV>
+template <int P, bool REV>
 __device__ __forceinline__ void find_head(int a, int rlo, int rhi, bool one_plane, int Li, unsigned long long magic,
                                           int& hp, int& dd, int& q) {
-  hp = kRun;
+  hp = kRunOf<P>;
   dd = -1;
   q = 0;
   if (one_plane) {
     if constexpr (!REV) {
       const int d1 = rlo - a, d2 = rhi - a;
-      if (d1 >= 0 && d1 < kRun) hp = d1;
-      else if (d2 >= 0 && d2 < kRun) hp = d2;
-      if (d2 >= 1 && d2 <= kRun) {
+      if (d1 >= 0 && d1 < kRunOf<P>) hp = d1;
+      else if (d2 >= 0 && d2 < kRunOf<P>) hp = d2;
+      if (d2 >= 1 && d2 <= kRunOf<P>) {
         dd = d2;
         q = 1;
       }
     } else {
-      const int e = a + kRun - rhi;
-      if (e >= 0 && e < kRun) hp = e;
+      const int e = a + kRunOf<P> - rhi;
+      if (e >= 0 && e < kRunOf<P>) hp = e;
     }
   } else {
     const int rr = a - rlo;
     if constexpr (!REV) {
       q = rr <= 0 ? 0 : (int)(((unsigned long long)(rr - 1) * magic) >> 32) + 1;
       const int d = q * Li - rr;  // >= 0
-      if (d < kRun) hp = d;
-      if (d >= 1 && d <= kRun) dd = d;
+      if (d < kRunOf<P>) hp = d;
+      if (d >= 1 && d <= kRunOf<P>) dd = d;
     } else {
-      const int g = rr + kRun;  // > 0
+      const int g = rr + kRunOf<P>;  // > 0
       const int qr = (int)(((unsigned long long)g * magic) >> 32);
       const int e = g - qr * Li;
-      if (qr >= 1 && e < kRun) hp = e;
+      if (qr >= 1 && e < kRunOf<P>) hp = e;
     }
   }
 }
@@ -192,13 +198,13 @@ __device__ __forceinline__ void runs_phase1(RunState<P>& st, const float* buf, i
   {
     const float4* src = reinterpret_cast<const float4*>(buf + a);
 #pragma unroll
-    for (int k = 0; k < kChunks; ++k) {
+    for (int k = 0; k < kChunksOf<P>; ++k) {
       const float4 q = src[k];
       const float e4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int i = 4 * k + c;
-        st.v[REV ? kRun - 1 - i : i] = SCAN ? e4[c] : Op::prep(e4[c]);
+        st.v[REV ? kRunOf<P> - 1 - i : i] = SCAN ? e4[c] : Op::prep(e4[c]);
       }
     }
   }
@@ -209,22 +215,22 @@ __device__ __forceinline__ void runs_phase1(RunState<P>& st, const float* buf, i
   float acc[P];
 #pragma unroll
   for (int c = 0; c < P; ++c) acc[c] = st.pre[c] = Op::identity();
-  if (!__any_sync(kFullMask, hp > 0 && hp < kRun)) {
-    // No head inside a run of this warp (hp is 0 or kRun everywhere).
+  if (!__any_sync(kFullMask, hp > 0 && hp < kRunOf<P>)) {
+    // No head inside a run of this warp (hp is 0 or kRunOf<P> everywhere).
 #pragma unroll
-    for (int e = 0; e < kRun; ++e) {
+    for (int e = 0; e < kRunOf<P>; ++e) {
       const int c = e % P;
       const float before = acc[c];
       acc[c] = Op::combine(acc[c], st.v[e]);
       if constexpr (SCAN) st.v[e] = EXCL ? before : acc[c];
     }
-    if (hp == kRun) {
+    if (hp == kRunOf<P>) {
 #pragma unroll
       for (int c = 0; c < P; ++c) st.pre[c] = acc[c];
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < kRun; ++e) {
+    for (int e = 0; e < kRunOf<P>; ++e) {
       const int c = e % P;
       const bool restart = (unsigned)(e - hp) < (unsigned)P;  // first of its class in the new plane
       const float before = restart ? Op::identity() : acc[c];
@@ -233,16 +239,16 @@ __device__ __forceinline__ void runs_phase1(RunState<P>& st, const float* buf, i
       if (e < hp) st.pre[c] = acc[c];
     }
     // A class with no float after a head near the run's end (positions
-    // kRun - P + c hold class c) keeps nothing for the new plane.
+    // kRunOf<P> - P + c hold class c) keeps nothing for the new plane.
 #pragma unroll
     for (int c = 0; c < P; ++c)
-      if (kRun - P + c < hp && hp < kRun) acc[c] = Op::identity();
+      if (kRunOf<P> - P + c < hp && hp < kRunOf<P>) acc[c] = Op::identity();
   }
   // 2. Segmented inclusive scan of the runs' last-segment totals across the
   // warp: lane l adds only lanes at or after hh, its last lane with a head
   // (every lane between hh and l has the same hh, so the Hillis-Steele steps
   // stay inside the segment).
-  const unsigned hmask = __ballot_sync(kFullMask, hp < kRun);
+  const unsigned hmask = __ballot_sync(kFullMask, hp < kRunOf<P>);
   const unsigned upto = hmask & (kFullMask >> (31 - lane));
   const int hh = upto ? 31 - __clz((int)upto) : 0;
 #pragma unroll
@@ -295,22 +301,22 @@ __device__ __forceinline__ void runs_phase2(RunState<P>& st, const float (&carry
     cl[c] = lane == 0 ? cw[c] : (st.head_before ? st.ex[c] : Op::combine(cw[c], st.ex[c]));
   if constexpr (SCAN) {
 #pragma unroll
-    for (int e = 0; e < kRun; ++e)
+    for (int e = 0; e < kRunOf<P>; ++e)
       if (e < st.hp) st.v[e] = Op::combine(cl[e % P], st.v[e]);
   }
 }
 
 // A scan's run back to its place in the tile (memory order).
-template <bool REV>
-__device__ __forceinline__ void put_run(const float (&v)[kRun], float* buf, int a) {
+template <int P, bool REV>
+__device__ __forceinline__ void put_run(const float (&v)[kRunOf<P>], float* buf, int a) {
   float4* dst = reinterpret_cast<float4*>(buf + a);
 #pragma unroll
-  for (int k = 0; k < kChunks; ++k) {
+  for (int k = 0; k < kChunksOf<P>; ++k) {
     float e4[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int i = 4 * k + c;
-      e4[c] = v[REV ? kRun - 1 - i : i];
+      e4[c] = v[REV ? kRunOf<P> - 1 - i : i];
     }
     dst[k] = make_float4(e4[0], e4[1], e4[2], e4[3]);
   }
@@ -334,7 +340,7 @@ __device__ __forceinline__ void store_tile_out(const float* buf, float* yt, int 
 
 template <int P, bool SCAN, bool REV, bool EXCL, typename Op>
 __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
-  __shared__ __align__(128) float s_buf[kStages][kTile];
+  __shared__ __align__(128) float s_buf[kStages][kTileOf<P>];
   __shared__ __align__(8) unsigned long long s_bar[kStages];
   // By tile parity (a reduction has no second barrier per tile, so a fast
   // warp may write the next tile's entries while others read these):
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
   __shared__ float s_carry[2][P];      // carry into the next tile
   __shared__ Cursor s_pc;              // the producer's cursor (thread 0 only)
   const int t = threadIdx.x;
-  const int a = (REV ? kT - 1 - t : t) * kRun;  // my run's first float in a tile
+  const int a = (REV ? kT - 1 - t : t) * kRunOf<P>;  // my run's first float in a tile
   const int Li = (int)min(p.N * P, (int64_t)INT32_MAX);
 
   int outstanding = 0;  // thread 0: copies issued and not yet consumed
@@ -374,13 +380,13 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
     const PlaneItem it = plane_item<P>(p, item);
     for (int j = 0; j < it.tiles; ++j) {
       const bool landed = mbar_wait_copy(&s_bar[stage], phase);
-      const int64_t ts = tile_start(it, j, REV);
+      const int64_t ts = tile_start<P>(it, j, REV);
       float* buf = s_buf[stage];
       const int rlo = rel_sat(it.lo, ts);
       const int rhi = rel_sat(it.hi, ts);
       RunState<P> st;
       int dd, qf;
-      find_head<REV>(a, rlo, rhi, p.k == 1, Li, p.magic, st.hp, dd, qf);
+      find_head<P, REV>(a, rlo, rhi, p.k == 1, Li, p.magic, st.hp, dd, qf);
       runs_phase1<P, SCAN, REV, EXCL, Op>(st, buf, a, s_wagg[par], s_wflag[par]);
       if constexpr (!SCAN) fence_proxy_async_smem();  // the buffer is refilled after barrier 1
       // Barrier 1: warp totals visible; every thread is past its wait for
@@ -408,10 +414,10 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
       runs_phase2<P, SCAN, Op>(st, carry, s_wagg[par], s_wflag[par], s_carry[par ^ 1], cl);
       if constexpr (SCAN) {
         // The item's floats in the tile leave by one bulk store.
-        put_run<REV>(st.v, buf, a);
+        put_run<P, REV>(st.v, buf, a);
         fence_proxy_async_smem();
         __syncthreads();
-        store_tile_out(buf, p.y + ts, min(max(rlo, 0), kTile), min(max(rhi, 0), kTile));
+        store_tile_out(buf, p.y + ts, min(max(rlo, 0), kTileOf<P>), min(max(rhi, 0), kTileOf<P>));
         fence_proxy_async_smem();
       } else {
         // A plane ending in my run: its class totals are my carry plus my
@@ -486,16 +492,16 @@ __device__ __forceinline__ LbTile<P> lb_tile(const PlaneLbParams& p, int64_t q) 
   g.lo = g.plane * L;
   g.hi = g.lo + L;
   const int64_t vlo = g.lo - g.lo % kPlaneAlign<P>;
-  const int64_t nt = (g.hi - vlo + kTile - 1) / kTile;
+  const int64_t nt = (g.hi - vlo + kTileOf<P> - 1) / kTileOf<P>;
   g.real = g.j < nt;
-  g.ts = vlo + (REV ? nt - 1 - g.j : g.j) * kTile;
+  g.ts = vlo + (REV ? nt - 1 - g.j : g.j) * kTileOf<P>;
   return g;
 }
 
 template <int P>
 __device__ __forceinline__ void lb_copy(const PlaneLbParams& p, const LbTile<P>& g, float* buf,
                                         unsigned long long* bar) {
-  const int64_t te = min(g.ts + kTile, (g.hi + 3) & ~(int64_t)3);
+  const int64_t te = min(g.ts + kTileOf<P>, (g.hi + 3) & ~(int64_t)3);
   const unsigned bytes = (unsigned)(te - g.ts) * 4u;
   mbar_arrive_expect_tx(bar, bytes);
   bulk_load(buf, p.x + g.ts, bytes, bar);
@@ -503,8 +509,8 @@ __device__ __forceinline__ void lb_copy(const PlaneLbParams& p, const LbTile<P>&
 
 template <int P, bool REV, bool EXCL>
 __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
-  __shared__ __align__(128) float s_new[kTile];  // tile `ticket`
-  __shared__ __align__(128) float s_old[kTile];  // tile `ticket - lag`
+  __shared__ __align__(128) float s_new[kTileOf<P>];  // tile `ticket`
+  __shared__ __align__(128) float s_old[kTileOf<P>];  // tile `ticket - lag`
   __shared__ __align__(8) unsigned long long s_bar[2];
   __shared__ float s_wagg[kNW][P];
   __shared__ int s_wflag[kNW];
@@ -517,7 +523,7 @@ __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
   const int w = t >> 5;
   const unsigned* abort_word = p.err_word + 1;
   const int64_t total = p.outer * p.tiles;
-  const int a = (REV ? kT - 1 - t : t) * kRun;  // my run's first float in a tile
+  const int a = (REV ? kT - 1 - t : t) * kRunOf<P>;  // my run's first float in a tile
 
   if (t == 0) {
     const Ticket tk = take_ticket(p.ticket_word);
@@ -589,7 +595,7 @@ __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
     const int rhi = rel_sat(g.hi, g.ts);
     RunState<P> st;
     int dd, qf;
-    find_head<REV>(a, rlo, rhi, true, 0, 0ull, st.hp, dd, qf);
+    find_head<P, REV>(a, rlo, rhi, true, 0, 0ull, st.hp, dd, qf);
     runs_phase1<P, true, REV, EXCL, OpSum>(st, s_old, a, s_wagg, s_wflag);
     // The barrier also publishes s_part: each class's carry is its
     // look-back partials from the lowest level up.
@@ -605,10 +611,10 @@ __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
       carry[c] = e;
     }
     runs_phase2<P, true, OpSum>(st, carry, s_wagg, s_wflag, nullptr, cl);
-    put_run<REV>(st.v, s_old, a);
+    put_run<P, REV>(st.v, s_old, a);
     fence_proxy_async_smem();
     __syncthreads();
-    store_tile_out(s_old, p.y + g.ts, min(max(rlo, 0), kTile), min(max(rhi, 0), kTile));
+    store_tile_out(s_old, p.y + g.ts, min(max(rlo, 0), kTileOf<P>), min(max(rhi, 0), kTileOf<P>));
   };
 
   // ---- sum tile `ticket` per class and publish it ----
@@ -625,15 +631,15 @@ __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
       const int rlo = rel_sat(g.lo, g.ts);
       const int rhi = rel_sat(g.hi, g.ts);
       const float4* src = reinterpret_cast<const float4*>(s_new + a);
-      const bool edge = rlo > a || rhi < a + kRun;
+      const bool edge = rlo > a || rhi < a + kRunOf<P>;
 #pragma unroll
-      for (int k = 0; k < kChunks; ++k) {
+      for (int k = 0; k < kChunksOf<P>; ++k) {
         const float4 q = src[k];
         const float e4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int i = 4 * k + c;  // memory position a + i
-          const int e = REV ? kRun - 1 - i : i;
+          const int e = REV ? kRunOf<P> - 1 - i : i;
           const bool in = !edge || (a + i >= rlo && a + i < rhi);
           own[e % P] += in ? e4[c] : 0.f;
         }
@@ -772,6 +778,10 @@ cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cud
     case 2: return launch_scan_p<2>(p, g, s);
     case 3: return launch_scan_p<3>(p, g, s);
     case 4: return launch_scan_p<4>(p, g, s);
+    case 5: return launch_scan_p<5>(p, g, s);
+    case 6: return launch_scan_p<6>(p, g, s);
+    case 7: return launch_scan_p<7>(p, g, s);
+    case 8: return launch_scan_p<8>(p, g, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -782,6 +792,10 @@ cudaError_t launch_planes_reduce(int P, int op, const PlaneRunParams& p, int64_t
     case 2: return launch_reduce_p<2>(op, p, g, s);
     case 3: return launch_reduce_p<3>(op, p, g, s);
     case 4: return launch_reduce_p<4>(op, p, g, s);
+    case 5: return launch_reduce_p<5>(op, p, g, s);
+    case 6: return launch_reduce_p<6>(op, p, g, s);
+    case 7: return launch_reduce_p<7>(op, p, g, s);
+    case 8: return launch_reduce_p<8>(op, p, g, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -792,6 +806,10 @@ cudaError_t launch_planes_lookback(int P, const PlaneLbParams& p, int64_t grid, 
     case 2: return launch_lb_p<2>(p, g, s);
     case 3: return launch_lb_p<3>(p, g, s);
     case 4: return launch_lb_p<4>(p, g, s);
+    case 5: return launch_lb_p<5>(p, g, s);
+    case 6: return launch_lb_p<6>(p, g, s);
+    case 7: return launch_lb_p<7>(p, g, s);
+    case 8: return launch_lb_p<8>(p, g, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -801,6 +819,10 @@ int occupancy_planes_lookback(int P) {
     case 2: return occupancy_lb_p<2>();
     case 3: return occupancy_lb_p<3>();
     case 4: return occupancy_lb_p<4>();
+    case 5: return occupancy_lb_p<5>();
+    case 6: return occupancy_lb_p<6>();
+    case 7: return occupancy_lb_p<7>();
+    case 8: return occupancy_lb_p<8>();
     default: return 0;
   }
 }
@@ -810,6 +832,10 @@ int occupancy_planes(int P, bool scan) {
     case 2: return occupancy_p<2>(scan);
     case 3: return occupancy_p<3>(scan);
     case 4: return occupancy_p<4>(scan);
+    case 5: return occupancy_p<5>(scan);
+    case 6: return occupancy_p<6>(scan);
+    case 7: return occupancy_p<7>(scan);
+    case 8: return occupancy_p<8>(scan);
     default: return 0;
   }
 }

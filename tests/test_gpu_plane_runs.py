@@ -1,6 +1,6 @@
-"""Narrow planes of 2, 3 or 4 columns read flat as segmented class runs (GPU):
+"""Narrow planes of 2 to 8 columns read flat as segmented class runs (GPU):
 [outer, N, P] scanned or reduced along N by k_planes, which reads each tile of
-the flat array into shared memory and scans 12-float runs per thread, the
+the flat array into shared memory and scans runs of whole rows per thread, the
 column classes fixed and the segments restarting at plane boundaries.
 Against the oracle element by element: short planes many to a tile (plane
 boundaries at and inside runs), planes of about one tile, planes over many
@@ -28,7 +28,10 @@ REDUCE_RUNS = 9  # LIBREDUCE_OPT_COLS_VARIANT: the same for reductions
 # last item; the two bench shapes.
 SHAPES = [(100_000, 100, 3), (4096, 4096, 2), (20_001, 19, 2), (30_001, 13, 4), (9000, 767, 3),
           (5000, 2305, 2), (3000, 1537, 3), (2000, 3001, 4), (700, 10_001, 3), (7, 13, 3),
-          (3, 333_333, 2), (12_345, 250, 4), (40_000, 9, 4)]
+          (3, 333_333, 2), (12_345, 250, 4), (40_000, 9, 4),
+          # 5-8 columns (runs of 20, 36, 28 and 24 floats)
+          (30_000, 101, 5), (20_001, 5, 5), (3000, 999, 6), (10_000, 7, 6), (7000, 77, 7), (500, 3001, 7),
+          (100_000, 100, 8), (9999, 4, 8), (64, 50_001, 5), (3, 200_000, 8)]
 
 
 def scan(x, reverse, exclusive, forced=True, out=None):
@@ -64,7 +67,8 @@ def test_scan_integers_exact_and_bitwise(shape, reverse, exclusive):
 
 @pytest.mark.parametrize("op", ["sum", "mean", "max", "min", "norm"])
 @pytest.mark.parametrize("shape", [(100_000, 100, 3), (20_001, 19, 2), (9000, 767, 3), (2000, 3001, 4),
-                                   (7, 13, 3), (4096, 2305, 2), (40_000, 9, 4)])
+                                   (7, 13, 3), (4096, 2305, 2), (40_000, 9, 4), (30_000, 101, 5),
+                                   (10_000, 7, 6), (500, 3001, 7), (100_000, 100, 8)])
 def test_reduce_against_oracle(shape, op):
     L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
     x = inputs.make(shape, "uniform_pm1", 33)
@@ -162,7 +166,8 @@ SCAN_LOOKBACK = 9  # LIBREDUCE_OPT_SCAN_COLS_VARIANT: the same tiles, a plane ov
 # granule (and of 12 floats for 3 columns), a plane of 33 tiles (a level-1
 # parent completed by its 32nd tile).
 LB_SHAPES = [(1, 1_000_003, 3), (3, 400_000, 4), (5, 250_001, 2), (7, 10_001, 3), (4, 4609, 2),
-             (3, 50, 3), (2, 38_017, 4), (1, 76_033, 2)]
+             (3, 50, 3), (2, 38_017, 4), (1, 76_033, 2),
+             (1, 300_001, 5), (2, 100_003, 6), (3, 90_001, 7), (1, 500_000, 8), (5, 2000, 7)]
 
 
 def scan_lb(x, reverse, exclusive, forced=True):
