@@ -4,7 +4,8 @@ oracle (GPU).
 Each case draws a shape (1 to 3 dims, total size log-uniform), an axis, the scan
 direction and exclusivity, a pointer offset of 0-3 floats, and the library
 options that steer the kernel choice (reduce-axis split, column-kernel and
-column-scan shapes, the narrow-row forms, the row-scan strategy), so the
+column-scan shapes, the narrow-row and narrow-plane forms, the row-scan
+strategy), so the
 many paths and their ragged edges meet inputs nobody picked by hand.  A
 failure names the case's parameters."""
 import numpy as np
@@ -37,8 +38,8 @@ def draw_case(rng):
                 offset=int(rng.integers(0, 4)), dist=str(rng.choice(["uniform_pm1", "normal", "int:-8:8"])),
                 seed=int(rng.integers(0, 1 << 30)),
                 split=int(rng.choice([0, 0, 0, 1, 2, 7, 64])),
-                cols_variant=int(rng.choice([-1, -1, 0, 1, 2, 3, 4, 5, 6, 7, 8])),
-                scan_cols_variant=int(rng.choice([-1, -1, 0, 1, 2, 3, 4, 5, 6, 7])),
+                cols_variant=int(rng.choice([-1, -1, 0, 1, 2, 3, 4, 5, 6, 7, 8, 9])),
+                scan_cols_variant=int(rng.choice([-1, -1, 0, 1, 2, 3, 4, 5, 6, 7, 8, 9])),
                 strategy=int(rng.choice([0, 0, 1, 2, 3, 4])))
     if case["dist"] == "int:-8:8" and case["kind"] == "scan":
         case["dist"] = "int:0:3"  # partial sums stay exact in fp32
