@@ -26,7 +26,7 @@ LIB = os.path.join(HERE, "lib", "libreduce.so")
 DEBUG_LIB = os.path.join(HERE, "lib", "libreduce_debug.so")
 BUILD_DEBUG = os.path.join(HERE, "_build_debug")
 SOURCES = ["lr_api.cu", "lr_reduce.cu", "lr_scan.cu", "lr_scan_cols_lb.cu", "lr_rows_short.cu", "lr_narrow.cu",
-           "lr_planes.cu",
+           "lr_planes_scan.cu", "lr_planes_reduce.cu", "lr_planes_lb.cu",
            "lr_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-Wall,-fvisibility=hidden",

@@ -539,23 +539,23 @@ int run_narrow(const Provider& pv, const float* x, int64_t outer, int64_t reduce
 
 // Narrow planes of 2-8 columns read flat as segmented class runs
 // (lr_planes.cu): planes per item and items, or false when the shape does not
-// fit (planes of at most one thread run).  Short planes go k >= 2 to a tile
-// (the item's start is rounded down to planes_align floats); longer ones one
-// to an item.
+// fit (planes of one row).  Short planes go k >= 2 to a tile (the item's
+// start is rounded down to planes_align floats), planes no longer than a
+// thread's run with several boundaries in a run; longer ones one to an item.
 struct PlaneRunPlan {
   int64_t k = 1, items = 0;
   unsigned long long magic = 0;
+  bool multi = false;  // planes no longer than a thread's run: several boundaries in a run
 };
 bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl) {
   int64_t L = 0;
-  if (inner < 2 || inner > kPlanesMaxP || outer <= 0 || mul_overflows(N, inner, &L) ||
-      L <= planes_run_len((int)inner))
-    return false;
+  if (inner < 2 || inner > kPlanesMaxP || outer <= 0 || N < 2 || mul_overflows(N, inner, &L)) return false;
   const int64_t align = planes_align((int)inner);
   const int64_t k = (planes_tile_len((int)inner) - align + 1) / L;
   pl->k = k >= 2 ? k : 1;
   pl->items = ceil_div(outer, pl->k);
   pl->magic = pl->k >= 2 ? ((1ull << 32) + (unsigned long long)L - 1) / (unsigned long long)L : 0;
+  pl->multi = L <= planes_run_len((int)inner);
   return true;
 }
 // The automatic choice takes the flat runs when there is at least one item
@@ -571,8 +571,14 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl) {
 // (fractions, runs against them: scans [1000, 10000, 8] 0.72 / 0.83, sums
 // [100000, 100, 8] 0.57 / 0.60; short-plane scans [100000, 100, 8] 0.89 /
 // 0.54 take the runs).
+// Reductions of planes no longer than a thread's run write every plane's
+// totals from scattered threads and stay with the short-row planes form
+// ([2e6, 8, 2] 0.41 against 0.62, [1e6, 5, 4] 0.35 against 0.56); their
+// scans take the runs ([500000, 7, 3] 0.87 against 0.53, [2e6, 8, 2] 0.88
+// against 0.64, [1e6, 4, 8] 0.84 against 0.62).
 bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t inner, bool scan) {
   if (inner == 8 && (!scan || pl.k < 2)) return false;
+  if (!scan && pl.multi) return false;
   return pl.items >= st->sm_count;
 }
 // Fewer items than SMs: the look-back form, whose blocks take single tiles,
@@ -594,7 +600,7 @@ int run_planes(const Provider& pv, const PlaneRunPlan& pl, const float* x, int64
   if (rc) return rc;
   const int64_t slots = (int64_t)st->sm_count * st->occ_planes[inner - 2][scan ? 1 : 0];
   const int64_t grid = std::max<int64_t>(1, std::min(pl.items, slots));
-  PlaneRunParams p{x, y, outer, N, pl.k, pl.items, pl.magic, flags, sc.header};
+  PlaneRunParams p{x, y, outer, N, pl.k, pl.items, pl.magic, flags, sc.header, pl.multi ? 1 : 0};
   return launched(scan ? launch_planes_scan((int)inner, p, grid, s)
                        : launch_planes_reduce((int)inner, op, p, grid, s));
 }
@@ -1180,7 +1186,8 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
                         true, kOpSum, s);
     if ((fv < 0 || fv == kScanColsPlaneLookback) && g_opt_axis_split.load() <= 0 &&
         ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
-        plane_run_plan(outer, N, inner, &pl) && (fv == kScanColsPlaneLookback || plane_runs_split(st, pl, N, inner))) {
+        plane_run_plan(outer, N, inner, &pl) && !pl.multi &&
+        (fv == kScanColsPlaneLookback || plane_runs_split(st, pl, N, inner))) {
       // Few long planes: each plane's tiles over blocks, carries by look-back.
       const int rc = run_planes_lookback(pv, x, outer, N, inner, y,
                                          (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0), s);

@@ -135,7 +135,8 @@ struct ShortRowsParams {
 // column f % P.  Work is cut into items of k whole planes: k >= 2 planes fit
 // one tile of planes_tile_len(P) floats (with the item's start rounded down
 // to planes_align(P)); k = 1 covers a plane in one or more tiles.  x (and y
-// for scans) must be 16-byte aligned and L > planes_run_len(P).
+// for scans) must be 16-byte aligned and N >= 2 (with L <= planes_run_len(P)
+// the kernels take the form for several plane boundaries in one thread's run).
 constexpr int kPlanesThreads = 128;  // threads per block (these kernels only)
 constexpr int kPlanesMaxP = 8;       // columns: 2 .. kPlanesMaxP
 // Consecutive floats per thread (whole rows of P columns), the alignment of
@@ -155,6 +156,7 @@ struct PlaneRunParams {
   unsigned long long magic;  // ceil(2^32 / L) when k >= 2 (then L < planes_tile_len(P) / 2)
   int flags;           // scans: kScanMirror | kScanExclusive; reductions: the epilogue
   unsigned* err_word;  // bit 0 set if a tile's copy never lands
+  int multi = 0;       // planes of 2P .. planes_run_len(P) floats: several boundaries in a run
 };
 
 // Scans of few long planes of 2-8 columns, a plane's tiles spread over
@@ -380,6 +382,7 @@ cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, 
 cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_planes_reduce(int P, int op, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes(int P, bool scan);  // resident kPlanesThreads-thread blocks per SM
+int occupancy_planes_reduce(int P);
 cudaError_t launch_planes_lookback(int P, const PlaneLbParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes_lookback(int P);
 

@@ -1,4 +1,4 @@
-// lr_planes.cu -- cumulative sums and reductions along the middle axis of
+// lr_planes.cuh -- cumulative sums and reductions along the middle axis of
 // [outer, N, P] for narrow planes of P = 2 .. 8 columns (sm_103a).
 //
 // The POPCORNBENCH trace l1_p91 discusses scanning a dimension other than the
@@ -39,6 +39,12 @@
 // item (before its start, after its end) are loaded but fall in other
 // segments, so they never reach an output; only the item's own floats are
 // stored.
+//
+// The kernels are templates here; lr_planes_scan.cu, lr_planes_reduce.cu and
+// lr_planes_lb.cu instantiate and launch the scans, the reductions and the
+// look-back form (three translation units, compiled in parallel).
+#pragma once
+
 #include <algorithm>
 
 #include "lr_device.cuh"
@@ -140,7 +146,30 @@ struct RunState {
   float ex[P];       // segmented totals of the lanes before mine in the warp
   int hp;            // the head: scan position in my run where a plane starts (kRunOf<P>: none)
   bool head_before;  // a lane before mine in the warp holds a head
+  // Planes no longer than a run (several boundaries in it): the position of
+  // my first float (in scan order) within its plane, the last head, and for a
+  // reduction the scan positions where a plane ends and the item-relative
+  // plane of my first float.
+  int pos0, hlast, qfirst;
+  unsigned long long ends;
 };
+
+// Planes of L <= kRunOf<P> floats (every run holds a boundary): the head
+// (first plane start in scan order), the last one, my first float's position
+// in its plane and, forward, the item-relative plane it lies in.  rr is my
+// run's first float relative to the item's start (> -kPlaneAlign), magic is
+// ceil(2^32 / L); every dividend stays below 2^32 / L.
+template <int P, bool REV>
+__device__ __forceinline__ void find_heads_short(int rr, int L, unsigned long long magic, RunState<P>& st) {
+  constexpr int R = kRunOf<P>;
+  const unsigned u = (unsigned)(rr + (REV ? R - 1 : 0) + 64 * L);  // > 0: 64 L exceeds any negative rr
+  const int q = (int)(((unsigned long long)u * magic) >> 32);
+  st.pos0 = (int)u - q * L;
+  st.qfirst = q - 64;
+  const int first = REV ? (st.pos0 + 1 == L ? 0 : st.pos0 + 1) : (st.pos0 == 0 ? 0 : L - st.pos0);
+  st.hp = first;
+  st.hlast = first + L * (int)(((unsigned long long)(unsigned)(R - 1 - first) * magic) >> 32);
+}
 
 // The head of my run (first float at a in the tile) and, for a reduction,
 // dd: my floats before the end of plane q - 1 of the item (1..kRunOf<P>), else -1.
@@ -189,9 +218,9 @@ __device__ __forceinline__ void find_head(int a, int rlo, int rhi, bool one_plan
 // Phase 1: read my run (memory order reversed for a reverse scan), scan it
 // per class, then the warp's segmented scan of the run totals; lane 31
 // writes the warp's last-segment totals and head flag.  st.hp must be set.
-template <int P, bool SCAN, bool REV, bool EXCL, typename Op>
+template <int P, bool SCAN, bool REV, bool EXCL, typename Op, bool MULTI = false>
 __device__ __forceinline__ void runs_phase1(RunState<P>& st, const float* buf, int a, float (&wagg)[kNW][P],
-                                            int (&wflag)[kNW]) {
+                                            int (&wflag)[kNW], int L = 0) {
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
   const int hp = st.hp;
@@ -215,7 +244,36 @@ __device__ __forceinline__ void runs_phase1(RunState<P>& st, const float* buf, i
   float acc[P];
 #pragma unroll
   for (int c = 0; c < P; ++c) acc[c] = st.pre[c] = Op::identity();
-  if (!__any_sync(kFullMask, hp > 0 && hp < kRunOf<P>)) {
+  if constexpr (MULTI) {
+    // Planes no longer than a run: a float restarts its class when it lies
+    // in its plane's first row in scan order (position < P forward, >= L - P
+    // reverse); the position walks with the float.  A reduction keeps every
+    // running value and notes where planes end (position L - 1, forward).
+    int pos = st.pos0;
+    unsigned long long ends = 0;
+#pragma unroll
+    for (int e = 0; e < kRunOf<P>; ++e) {
+      const int c = e % P;
+      const bool restart = REV ? pos >= L - P : pos < P;
+      const float before = restart ? Op::identity() : acc[c];
+      acc[c] = restart ? st.v[e] : Op::combine(acc[c], st.v[e]);
+      if constexpr (SCAN) {
+        st.v[e] = EXCL ? before : acc[c];
+      } else {
+        st.v[e] = acc[c];
+        if (pos == L - 1) ends |= 1ull << e;
+      }
+      if constexpr (REV) pos = pos == 0 ? L - 1 : pos - 1;
+      else pos = pos + 1 == L ? 0 : pos + 1;
+    }
+    st.ends = ends;
+    // A class with no float after the last head keeps nothing for the new
+    // plane (class c first appears hlast + ((c - hlast) mod P) floats in).
+    const int hl = st.hlast;
+#pragma unroll
+    for (int c = 0; c < P; ++c)
+      if (hl + ((c - hl % P + P) % P) >= kRunOf<P>) acc[c] = Op::identity();
+  } else if (!__any_sync(kFullMask, hp > 0 && hp < kRunOf<P>)) {
     // No head inside a run of this warp (hp is 0 or kRunOf<P> everywhere).
 #pragma unroll
     for (int e = 0; e < kRunOf<P>; ++e) {
@@ -248,11 +306,13 @@ __device__ __forceinline__ void runs_phase1(RunState<P>& st, const float* buf, i
   // warp: lane l adds only lanes at or after hh, its last lane with a head
   // (every lane between hh and l has the same hh, so the Hillis-Steele steps
   // stay inside the segment).
-  const unsigned hmask = __ballot_sync(kFullMask, hp < kRunOf<P>);
+  // (Planes no longer than a run: every lane holds a head, so lane l takes
+  // only its own last segment and the steps are skipped.)
+  const unsigned hmask = MULTI ? kFullMask : __ballot_sync(kFullMask, hp < kRunOf<P>);
   const unsigned upto = hmask & (kFullMask >> (31 - lane));
   const int hh = upto ? 31 - __clz((int)upto) : 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
+  for (int o = 1; o < (MULTI ? 1 : 32); o <<= 1) {
     const bool take = lane - o >= hh;
 #pragma unroll
     for (int c = 0; c < P; ++c) {
@@ -338,7 +398,7 @@ __device__ __forceinline__ void store_tile_out(const float* buf, float* yt, int 
   }
 }
 
-template <int P, bool SCAN, bool REV, bool EXCL, typename Op>
+template <int P, bool SCAN, bool REV, bool EXCL, typename Op, bool MULTI>
 __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
   __shared__ __align__(128) float s_buf[kStages][kTileOf<P>];
   __shared__ __align__(8) unsigned long long s_bar[kStages];
@@ -385,9 +445,10 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
       const int rlo = rel_sat(it.lo, ts);
       const int rhi = rel_sat(it.hi, ts);
       RunState<P> st;
-      int dd, qf;
-      find_head<P, REV>(a, rlo, rhi, p.k == 1, Li, p.magic, st.hp, dd, qf);
-      runs_phase1<P, SCAN, REV, EXCL, Op>(st, buf, a, s_wagg[par], s_wflag[par]);
+      int dd = -1, qf = 0;
+      if constexpr (MULTI) find_heads_short<P, REV>(a - rlo, Li, p.magic, st);
+      else find_head<P, REV>(a, rlo, rhi, p.k == 1, Li, p.magic, st.hp, dd, qf);
+      runs_phase1<P, SCAN, REV, EXCL, Op, MULTI>(st, buf, a, s_wagg[par], s_wflag[par], Li);
       if constexpr (!SCAN) fence_proxy_async_smem();  // the buffer is refilled after barrier 1
       // Barrier 1: warp totals visible; every thread is past its wait for
       // this tile and done with the previous tile's buffer.
@@ -419,6 +480,29 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
         __syncthreads();
         store_tile_out(buf, p.y + ts, min(max(rlo, 0), kTileOf<P>), min(max(rhi, 0), kTileOf<P>));
         fence_proxy_async_smem();
+      } else if constexpr (MULTI) {
+        // Every plane ending in my run (forward, where class c of a plane
+        // ends on its last row): its class totals are the running values
+        // there, with my carry for the plane that began before my run (a
+        // class that ended in an earlier run: the carry alone).
+        int q = st.qfirst;
+#pragma unroll
+        for (int e = 0; e < kRunOf<P>; ++e) {
+          if ((st.ends >> e) & 1ull) {
+            if (q >= 0 && q < it.planes) {
+              float* out = p.y + (it.first + q) * P;
+#pragma unroll
+              for (int c = 0; c < P; ++c) {
+                const int idx = e - ((e % P - c + P) % P);  // class c's last float of this plane
+                float val;
+                if (idx < 0) val = cl[c];
+                else val = idx < st.hp ? Op::combine(cl[c], st.v[idx < 0 ? 0 : idx]) : st.v[idx < 0 ? 0 : idx];
+                st_plain(out + c, finish(val, p.flags, p.N));
+              }
+            }
+            ++q;
+          }
+        }
       } else {
         // A plane ending in my run: its class totals are my carry plus my
         // floats before the boundary.
@@ -717,127 +801,5 @@ int occupancy_of(K kernel) {
   return n;
 }
 
-template <int P, bool REV>
-cudaError_t launch_scan_dir(const PlaneRunParams& p, dim3 g, cudaStream_t s) {
-  if (p.flags & kScanExclusive) k_planes<P, true, REV, true, OpSum><<<g, kT, 0, s>>>(p);
-  else k_planes<P, true, REV, false, OpSum><<<g, kT, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
-template <int P>
-cudaError_t launch_scan_p(const PlaneRunParams& p, dim3 g, cudaStream_t s) {
-  return (p.flags & kScanMirror) ? launch_scan_dir<P, false>(p, g, s) : launch_scan_dir<P, true>(p, g, s);
-}
-
-template <int P>
-cudaError_t launch_reduce_p(int op, const PlaneRunParams& p, dim3 g, cudaStream_t s) {
-  switch (op) {
-    case kOpSum: k_planes<P, false, false, false, OpSum><<<g, kT, 0, s>>>(p); break;
-    case kOpSumSq: k_planes<P, false, false, false, OpSumSq><<<g, kT, 0, s>>>(p); break;
-    case kOpMax: k_planes<P, false, false, false, OpMax><<<g, kT, 0, s>>>(p); break;
-    case kOpMin: k_planes<P, false, false, false, OpMin><<<g, kT, 0, s>>>(p); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
-}
-
-template <int P>
-int occupancy_p(bool scan) {
-  if (!scan) return occupancy_of(k_planes<P, false, false, false, OpSum>);
-  return std::min({occupancy_of(k_planes<P, true, false, false, OpSum>),
-                   occupancy_of(k_planes<P, true, false, true, OpSum>),
-                   occupancy_of(k_planes<P, true, true, false, OpSum>),
-                   occupancy_of(k_planes<P, true, true, true, OpSum>)});
-}
-
-template <int P>
-cudaError_t launch_lb_p(const PlaneLbParams& p, dim3 g, cudaStream_t s) {
-  const bool rev = (p.flags & kScanMirror) == 0;
-  const bool excl = (p.flags & kScanExclusive) != 0;
-  if (rev) {
-    if (excl) k_planes_lb<P, true, true><<<g, kT, 0, s>>>(p);
-    else k_planes_lb<P, true, false><<<g, kT, 0, s>>>(p);
-  } else {
-    if (excl) k_planes_lb<P, false, true><<<g, kT, 0, s>>>(p);
-    else k_planes_lb<P, false, false><<<g, kT, 0, s>>>(p);
-  }
-  return cudaGetLastError();
-}
-
-template <int P>
-int occupancy_lb_p() {
-  return std::min({occupancy_of(k_planes_lb<P, false, false>), occupancy_of(k_planes_lb<P, false, true>),
-                   occupancy_of(k_planes_lb<P, true, false>), occupancy_of(k_planes_lb<P, true, true>)});
-}
-
 }  // namespace
-
-cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cudaStream_t s) {
-  const dim3 g((unsigned)grid);
-  switch (P) {
-    case 2: return launch_scan_p<2>(p, g, s);
-    case 3: return launch_scan_p<3>(p, g, s);
-    case 4: return launch_scan_p<4>(p, g, s);
-    case 5: return launch_scan_p<5>(p, g, s);
-    case 6: return launch_scan_p<6>(p, g, s);
-    case 7: return launch_scan_p<7>(p, g, s);
-    case 8: return launch_scan_p<8>(p, g, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-cudaError_t launch_planes_reduce(int P, int op, const PlaneRunParams& p, int64_t grid, cudaStream_t s) {
-  const dim3 g((unsigned)grid);
-  switch (P) {
-    case 2: return launch_reduce_p<2>(op, p, g, s);
-    case 3: return launch_reduce_p<3>(op, p, g, s);
-    case 4: return launch_reduce_p<4>(op, p, g, s);
-    case 5: return launch_reduce_p<5>(op, p, g, s);
-    case 6: return launch_reduce_p<6>(op, p, g, s);
-    case 7: return launch_reduce_p<7>(op, p, g, s);
-    case 8: return launch_reduce_p<8>(op, p, g, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-cudaError_t launch_planes_lookback(int P, const PlaneLbParams& p, int64_t grid, cudaStream_t s) {
-  const dim3 g((unsigned)grid);
-  switch (P) {
-    case 2: return launch_lb_p<2>(p, g, s);
-    case 3: return launch_lb_p<3>(p, g, s);
-    case 4: return launch_lb_p<4>(p, g, s);
-    case 5: return launch_lb_p<5>(p, g, s);
-    case 6: return launch_lb_p<6>(p, g, s);
-    case 7: return launch_lb_p<7>(p, g, s);
-    case 8: return launch_lb_p<8>(p, g, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-int occupancy_planes_lookback(int P) {
-  switch (P) {
-    case 2: return occupancy_lb_p<2>();
-    case 3: return occupancy_lb_p<3>();
-    case 4: return occupancy_lb_p<4>();
-    case 5: return occupancy_lb_p<5>();
-    case 6: return occupancy_lb_p<6>();
-    case 7: return occupancy_lb_p<7>();
-    case 8: return occupancy_lb_p<8>();
-    default: return 0;
-  }
-}
-
-int occupancy_planes(int P, bool scan) {
-  switch (P) {
-    case 2: return occupancy_p<2>(scan);
-    case 3: return occupancy_p<3>(scan);
-    case 4: return occupancy_p<4>(scan);
-    case 5: return occupancy_p<5>(scan);
-    case 6: return occupancy_p<6>(scan);
-    case 7: return occupancy_p<7>(scan);
-    case 8: return occupancy_p<8>(scan);
-    default: return 0;
-  }
-}
-
 }  // namespace lr

@@ -1,0 +1,60 @@
+// lr_planes_reduce.cu -- the reductions of narrow planes (lr_planes.cuh):
+// instantiations, launch and occupancy.
+#include "lr_planes.cuh"
+
+namespace lr {
+namespace {
+
+template <int P, bool MULTI>
+cudaError_t launch_reduce_pm(int op, const PlaneRunParams& p, dim3 g, cudaStream_t s) {
+  switch (op) {
+    case kOpSum: k_planes<P, false, false, false, OpSum, MULTI><<<g, kT, 0, s>>>(p); break;
+    case kOpSumSq: k_planes<P, false, false, false, OpSumSq, MULTI><<<g, kT, 0, s>>>(p); break;
+    case kOpMax: k_planes<P, false, false, false, OpMax, MULTI><<<g, kT, 0, s>>>(p); break;
+    case kOpMin: k_planes<P, false, false, false, OpMin, MULTI><<<g, kT, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <int P>
+cudaError_t launch_reduce_p(int op, const PlaneRunParams& p, dim3 g, cudaStream_t s) {
+  return p.multi ? launch_reduce_pm<P, true>(op, p, g, s) : launch_reduce_pm<P, false>(op, p, g, s);
+}
+
+template <int P>
+int occupancy_reduce_p() {
+  return std::min(occupancy_of(k_planes<P, false, false, false, OpSum, false>),
+                  occupancy_of(k_planes<P, false, false, false, OpSum, true>));
+}
+
+}  // namespace
+
+cudaError_t launch_planes_reduce(int P, int op, const PlaneRunParams& p, int64_t grid, cudaStream_t s) {
+  const dim3 g((unsigned)grid);
+  switch (P) {
+    case 2: return launch_reduce_p<2>(op, p, g, s);
+    case 3: return launch_reduce_p<3>(op, p, g, s);
+    case 4: return launch_reduce_p<4>(op, p, g, s);
+    case 5: return launch_reduce_p<5>(op, p, g, s);
+    case 6: return launch_reduce_p<6>(op, p, g, s);
+    case 7: return launch_reduce_p<7>(op, p, g, s);
+    case 8: return launch_reduce_p<8>(op, p, g, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int occupancy_planes_reduce(int P) {
+  switch (P) {
+    case 2: return occupancy_reduce_p<2>();
+    case 3: return occupancy_reduce_p<3>();
+    case 4: return occupancy_reduce_p<4>();
+    case 5: return occupancy_reduce_p<5>();
+    case 6: return occupancy_reduce_p<6>();
+    case 7: return occupancy_reduce_p<7>();
+    case 8: return occupancy_reduce_p<8>();
+    default: return 0;
+  }
+}
+
+}  // namespace lr

@@ -194,11 +194,11 @@ def test_short_row_index_division_is_exact():
 
 def test_plane_run_division_is_exact():
     """The plane-run kernel finds plane boundaries in a tile holding k >= 2
-    planes of L floats (L above the thread run of 20 to 36 floats, at most
-    half the largest tile of 4608) by (e * ceil(2^32 / L)) >> 32 for e up to a
-    tile and a run past it (4608 + 72); that is e // L there."""
+    planes of L floats (4 <= L <= 2302: at most half the largest tile of 4608)
+    by (e * ceil(2^32 / L)) >> 32 for e up to a tile and a run past it, plus
+    64 L where a run start is shifted to stay positive; that is e // L there."""
     import numpy as np
-    e = np.arange(0, 4608 + 72, dtype=np.uint64)
-    for d in range(21, (4608 - 3) // 2 + 1):
+    for d in range(4, (4608 - 3) // 2 + 1):
+        e = np.arange(0, 4608 + 72 + 64 * d, dtype=np.uint64)
         magic = np.uint64(((1 << 32) + d - 1) // d)
         assert np.array_equal((e * magic) >> np.uint64(32), e // np.uint64(d)), d

@@ -2,7 +2,8 @@
 [outer, N, P] scanned or reduced along N by k_planes, which reads each tile of
 the flat array into shared memory and scans runs of whole rows per thread, the
 column classes fixed and the segments restarting at plane boundaries.
-Against the oracle element by element: short planes many to a tile (plane
+Against the oracle element by element: planes no longer than a thread's run
+(several boundaries in a run), short planes many to a tile (plane
 boundaries at and inside runs), planes of about one tile, planes over many
 tiles, both directions, inclusive and exclusive, every reduction operator,
 integer inputs exactly, reruns bit for bit, neighbours of the output left
@@ -31,7 +32,10 @@ SHAPES = [(100_000, 100, 3), (4096, 4096, 2), (20_001, 19, 2), (30_001, 13, 4), 
           (3, 333_333, 2), (12_345, 250, 4), (40_000, 9, 4),
           # 5-8 columns (runs of 20, 36, 28 and 24 floats)
           (30_000, 101, 5), (20_001, 5, 5), (3000, 999, 6), (10_000, 7, 6), (7000, 77, 7), (500, 3001, 7),
-          (100_000, 100, 8), (9999, 4, 8), (64, 50_001, 5), (3, 200_000, 8)]
+          (100_000, 100, 8), (9999, 4, 8), (64, 50_001, 5), (3, 200_000, 8),
+          # planes no longer than a thread's run: several boundaries in a run
+          (500_000, 7, 3), (300_001, 2, 2), (200_000, 5, 4), (100_000, 3, 8), (100_001, 9, 4),
+          (70_000, 18, 2), (7, 4, 5), (40_000, 4, 7), (33_333, 12, 3), (50_000, 6, 6)]
 
 
 def scan(x, reverse, exclusive, forced=True, out=None):
@@ -54,7 +58,7 @@ def test_scan_against_oracle(shape, reverse, exclusive):
 
 
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
-@pytest.mark.parametrize("shape", [(40_000, 25, 3), (3000, 2401, 2), (1000, 2500, 4)])
+@pytest.mark.parametrize("shape", [(40_000, 25, 3), (3000, 2401, 2), (1000, 2500, 4), (200_000, 7, 3)])
 def test_scan_integers_exact_and_bitwise(shape, reverse, exclusive):
     """{0..3} inputs: every prefix is an integer below 2^24, so exact."""
     x = inputs.make(shape, "int:0:3", 32)
@@ -68,7 +72,9 @@ def test_scan_integers_exact_and_bitwise(shape, reverse, exclusive):
 @pytest.mark.parametrize("op", ["sum", "mean", "max", "min", "norm"])
 @pytest.mark.parametrize("shape", [(100_000, 100, 3), (20_001, 19, 2), (9000, 767, 3), (2000, 3001, 4),
                                    (7, 13, 3), (4096, 2305, 2), (40_000, 9, 4), (30_000, 101, 5),
-                                   (10_000, 7, 6), (500, 3001, 7), (100_000, 100, 8)])
+                                   (10_000, 7, 6), (500, 3001, 7), (100_000, 100, 8),
+                                   (500_000, 7, 3), (300_001, 2, 2), (100_000, 3, 8), (40_000, 4, 7),
+                                   (33_333, 12, 3)])
 def test_reduce_against_oracle(shape, op):
     L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
     x = inputs.make(shape, "uniform_pm1", 33)
@@ -103,7 +109,7 @@ def test_reduce_nan_stays_in_its_plane(op):
         assert_op_close(out, ref, scale, op, shape[1], f"plane runs {op} with NaN")
 
 
-@pytest.mark.parametrize("shape", [(6000, 100, 3), (300, 3001, 4)])
+@pytest.mark.parametrize("shape", [(6000, 100, 3), (300, 3001, 4), (100_000, 5, 3)])
 def test_reduce_integers_exact_and_bitwise(shape):
     x = inputs.make(shape, "int:-8:8", 35)
     L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
@@ -131,7 +137,7 @@ def test_neighbours_untouched(reverse):
         assert_close(y.cpu().numpy(), ref, scale, f"neighbours {shape}")
 
 
-@pytest.mark.parametrize("shape", [(100_000, 100, 3), (4096, 4096, 2), (50_000, 40, 4)])
+@pytest.mark.parametrize("shape", [(100_000, 100, 3), (4096, 4096, 2), (50_000, 40, 4), (500_000, 7, 3)])
 def test_automatic_choice_takes_plane_runs(shape):
     """Aligned planes whose items fill the GPU take this form without options:
     the automatic result is the forced one bit for bit."""
