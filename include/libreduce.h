@@ -20,7 +20,11 @@
  *    call only enqueues work on `stream` and never copies results back; apart
  *    from the one-time workspace set-up described under "Scratch" below, it
  *    never synchronises the host.  The caller keeps the inputs alive and
- *    unmodified until that work completes.
+ *    unmodified until that work completes.  Kernels are launched with
+ *    programmatic stream serialization: a call's kernel may begin launching
+ *    while the previous kernel on `stream` finishes, but waits for it to
+ *    complete (its writes visible) before touching any memory, so stream
+ *    order holds as for a plain launch; only launch latency is overlapped.
  *  - Results are deterministic: the same input on the same device gives
  *    bit-identical output on every call.  No floating-point atomics are used;
  *    partial sums are combined in a fixed order.

@@ -41,6 +41,7 @@ __device__ __forceinline__ float reduce_strided_cg(const float* p, int64_t n, in
 // ---------------------------------------------------------------------------
 template <int U, typename Op>
 __global__ void __launch_bounds__(kThreads) k_reduce_contig(ContigParams p) {
+  pdl_begin();
   __shared__ float sh[kThreads / 32];
   __shared__ int am_last;
   const int t = threadIdx.x;

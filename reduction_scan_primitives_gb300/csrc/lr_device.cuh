@@ -69,6 +69,20 @@ __device__ __forceinline__ bool dbg_shared(long long i, int w, long long n, cons
 #endif
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel is launched so that it may
+// start while the previous kernel in its stream is still finishing; its first
+// statement waits until that kernel has completed and its memory operations
+// are visible (a no-op after a plain launch), so no access of this kernel
+// overlaps the previous one.  It then lets the next kernel of the stream
+// begin its launch, which completes once every block of this grid has begun.
+// What overlaps is launch processing and block start-up, nothing else.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Global memory access (hand-written PTX).
 // ---------------------------------------------------------------------------
 

@@ -7,6 +7,25 @@
 
 namespace lr {
 
+// Launch `kernel` with programmatic stream serialization (see pdl_begin in
+// lr_device.cuh: the kernel waits for its predecessor before touching memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, unsigned block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+
 // Output epilogue of the reduce kernels: the mean divides the sum by the
 // element count, the norm takes the square root of the sum of squares.
 enum Epilogue { kEpiNone = 0, kEpiMean = 1, kEpiSqrt = 2 };

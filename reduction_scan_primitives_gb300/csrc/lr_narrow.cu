@@ -78,6 +78,7 @@ __device__ __forceinline__ void combine_groups(float* sh, int G, int64_t inner) 
 // ---------------------------------------------------------------------------
 template <int VEC, int U, typename Op>
 __global__ void __launch_bounds__(kThreads) k_reduce_narrow(NarrowParams p) {
+  pdl_begin();
   __shared__ __align__(16) float sh[kThreads * VEC];
   __shared__ int am_last;
   const int64_t inner = p.inner;
@@ -182,6 +183,7 @@ __host__ __device__ constexpr int scan_narrow_cap() {  // floats of one tile buf
 
 template <int VEC, int U>
 __global__ void __launch_bounds__(kThreads) k_scan_narrow(ScanColsParams p) {
+  pdl_begin();
   constexpr int kCap = scan_narrow_cap<VEC, U>();
   extern __shared__ __align__(16) float s_dyn[];         // two tile buffers of kCap floats
   __shared__ __align__(16) float s_tot[kThreads * VEC];  // warp totals, or row-group totals
@@ -413,6 +415,7 @@ __global__ void __launch_bounds__(kThreads) k_scan_narrow(ScanColsParams p) {
 // ---------------------------------------------------------------------------
 template <int VEC, int U>
 __global__ void __launch_bounds__(kThreads) k_scan_narrow_warp(ScanColsParams p) {
+  pdl_begin();
   const int64_t inner = p.inner;
   int tpr = 1;
   while (tpr * VEC < inner) tpr <<= 1;
@@ -478,6 +481,7 @@ __global__ void __launch_bounds__(kThreads) k_scan_narrow_warp(ScanColsParams p)
 
 template <int VEC, int U, typename Op>
 __global__ void __launch_bounds__(kThreads) k_reduce_narrow_warp(NarrowParams p) {
+  pdl_begin();
   const int64_t inner = p.inner;
   const int tpr = (int)(inner / VEC);  // <= 32; inner % VEC == 0
   const int gw = 32 / tpr;
@@ -535,8 +539,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce_narrow_warp(NarrowParams p)
 
 cudaError_t launch_scan_narrow_warp(int vec, const ScanColsParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
-  if (vec == 4) k_scan_narrow_warp<4, 8><<<g, kThreads, 0, s>>>(p);
-  else k_scan_narrow_warp<1, 8><<<g, kThreads, 0, s>>>(p);
+  if (vec == 4) launch_pdl(k_scan_narrow_warp<4, 8>, g, kThreads, 0, s, p);
+  else launch_pdl(k_scan_narrow_warp<1, 8>, g, kThreads, 0, s, p);
   return cudaGetLastError();
 }
 
@@ -549,7 +553,7 @@ cudaError_t launch_reduce_narrow_warp(int vec, int op, const NarrowParams& p, in
   constexpr int U = 8;
 #define LR_NARROW_WARP_CASE(V, OP)                                 \
   if (vec == V && op == k##OP) {                                   \
-    k_reduce_narrow_warp<V, U, OP><<<g, kThreads, 0, s>>>(p);      \
+    launch_pdl(k_reduce_narrow_warp<V, U, OP>, g, kThreads, 0, s, p);      \
     return cudaGetLastError();                                     \
   }
   LR_NARROW_WARP_CASE(1, OpSum)
@@ -569,7 +573,7 @@ cudaError_t launch_reduce_narrow(int vec, int op, const NarrowParams& p, int64_t
   constexpr int U = 8;
 #define LR_NARROW_CASE(V, OP)                                      \
   if (vec == V && op == k##OP) {                                   \
-    k_reduce_narrow<V, U, OP><<<g, kThreads, 0, s>>>(p);           \
+    launch_pdl(k_reduce_narrow<V, U, OP>, g, kThreads, 0, s, p);           \
     return cudaGetLastError();                                     \
   }
   LR_NARROW_CASE(1, OpSum)
@@ -609,7 +613,7 @@ cudaError_t launch_scan_narrow(int vec, const ScanColsParams& p, int64_t grid, c
   size_t bytes = 0;
   const cudaError_t e = vec == 4 ? scan_narrow_kernel<4, 8>(&k, &bytes) : scan_narrow_kernel<1, 16>(&k, &bytes);
   if (e != cudaSuccess) return e;
-  k<<<dim3((unsigned)grid), kThreads, bytes, s>>>(p);
+  launch_pdl(k, dim3((unsigned)grid), kThreads, bytes, s, p);
   return cudaGetLastError();
 }
 

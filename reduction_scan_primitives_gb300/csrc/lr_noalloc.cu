@@ -144,7 +144,7 @@ extern "C" int reduce_sum_f32_noalloc(const float* x, int64_t n, float* out,
     if (e != cudaSuccess) return record_cuda_error(e);
   }
   ContigParams p{x, n, chunk_len, (int32_t)chunks, out, partials, ticket, kEpiNone};
-  k_reduce_contig<16, OpSum><<<dim3((unsigned)chunks), kThreads, 0, s>>>(p);
+  launch_pdl(k_reduce_contig<16, OpSum>, dim3((unsigned)chunks), kThreads, 0, s, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return record_cuda_error(e);
   count_launch();

@@ -400,6 +400,7 @@ __device__ __forceinline__ void store_tile_out(const float* buf, float* yt, int 
 
 template <int P, bool SCAN, bool REV, bool EXCL, typename Op, bool MULTI>
 __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
+  pdl_begin();
   __shared__ __align__(128) float s_buf[kStages][kTileOf<P>];
   __shared__ __align__(8) unsigned long long s_bar[kStages];
   // By tile parity (a reduction has no second barrier per tile, so a fast
@@ -593,6 +594,7 @@ __device__ __forceinline__ void lb_copy(const PlaneLbParams& p, const LbTile<P>&
 
 template <int P, bool REV, bool EXCL>
 __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
+  pdl_begin();
   __shared__ __align__(128) float s_new[kTileOf<P>];  // tile `ticket`
   __shared__ __align__(128) float s_old[kTileOf<P>];  // tile `ticket - lag`
   __shared__ __align__(8) unsigned long long s_bar[2];

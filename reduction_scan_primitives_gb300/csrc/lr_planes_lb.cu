@@ -10,11 +10,11 @@ cudaError_t launch_lb_p(const PlaneLbParams& p, dim3 g, cudaStream_t s) {
   const bool rev = (p.flags & kScanMirror) == 0;
   const bool excl = (p.flags & kScanExclusive) != 0;
   if (rev) {
-    if (excl) k_planes_lb<P, true, true><<<g, kT, 0, s>>>(p);
-    else k_planes_lb<P, true, false><<<g, kT, 0, s>>>(p);
+    if (excl) launch_pdl(k_planes_lb<P, true, true>, g, kT, 0, s, p);
+    else launch_pdl(k_planes_lb<P, true, false>, g, kT, 0, s, p);
   } else {
-    if (excl) k_planes_lb<P, false, true><<<g, kT, 0, s>>>(p);
-    else k_planes_lb<P, false, false><<<g, kT, 0, s>>>(p);
+    if (excl) launch_pdl(k_planes_lb<P, false, true>, g, kT, 0, s, p);
+    else launch_pdl(k_planes_lb<P, false, false>, g, kT, 0, s, p);
   }
   return cudaGetLastError();
 }

@@ -8,10 +8,10 @@ namespace {
 template <int P, bool MULTI>
 cudaError_t launch_reduce_pm(int op, const PlaneRunParams& p, dim3 g, cudaStream_t s) {
   switch (op) {
-    case kOpSum: k_planes<P, false, false, false, OpSum, MULTI><<<g, kT, 0, s>>>(p); break;
-    case kOpSumSq: k_planes<P, false, false, false, OpSumSq, MULTI><<<g, kT, 0, s>>>(p); break;
-    case kOpMax: k_planes<P, false, false, false, OpMax, MULTI><<<g, kT, 0, s>>>(p); break;
-    case kOpMin: k_planes<P, false, false, false, OpMin, MULTI><<<g, kT, 0, s>>>(p); break;
+    case kOpSum: launch_pdl(k_planes<P, false, false, false, OpSum, MULTI>, g, kT, 0, s, p); break;
+    case kOpSumSq: launch_pdl(k_planes<P, false, false, false, OpSumSq, MULTI>, g, kT, 0, s, p); break;
+    case kOpMax: launch_pdl(k_planes<P, false, false, false, OpMax, MULTI>, g, kT, 0, s, p); break;
+    case kOpMin: launch_pdl(k_planes<P, false, false, false, OpMin, MULTI>, g, kT, 0, s, p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

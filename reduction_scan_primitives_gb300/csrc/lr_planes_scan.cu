@@ -7,8 +7,8 @@ namespace {
 
 template <int P, bool REV, bool MULTI>
 cudaError_t launch_scan_dir(const PlaneRunParams& p, dim3 g, cudaStream_t s) {
-  if (p.flags & kScanExclusive) k_planes<P, true, REV, true, OpSum, MULTI><<<g, kT, 0, s>>>(p);
-  else k_planes<P, true, REV, false, OpSum, MULTI><<<g, kT, 0, s>>>(p);
+  if (p.flags & kScanExclusive) launch_pdl(k_planes<P, true, REV, true, OpSum, MULTI>, g, kT, 0, s, p);
+  else launch_pdl(k_planes<P, true, REV, false, OpSum, MULTI>, g, kT, 0, s, p);
   return cudaGetLastError();
 }
 

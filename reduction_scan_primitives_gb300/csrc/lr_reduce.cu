@@ -59,6 +59,7 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, unsigned ran
 
 template <typename Op>
 __global__ void __launch_bounds__(kClusterThreads) k_reduce_cluster(ContigParams p) {
+  pdl_begin();
   constexpr int U = kClusterLoads;
   constexpr int64_t S = kClusterThreads;
   __shared__ float sh[kClusterThreads / 32];
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(kClusterThreads) k_reduce_cluster(ContigParams
 // ---------------------------------------------------------------------------
 template <typename Op>
 __global__ void __launch_bounds__(kThreads) k_reduce_rows_warp(RowsWarpParams p) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int64_t first = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
@@ -130,6 +132,7 @@ struct ColsShape {
 
 template <int VEC, int WY, int U, typename Op>
 __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
+  pdl_begin();
   using Sh = ColsShape<VEC, WY>;
   constexpr int WX = Sh::WX;
   constexpr int CW = Sh::CW;
@@ -298,6 +301,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_cols(ColsParams p) {
 constexpr int kColsU = 8;
 
 __global__ void k_fill(float* out, int64_t n, float value) {
+  pdl_begin();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
     st_plain(out + i, value);
@@ -314,13 +318,13 @@ template <typename Op>
 cudaError_t contig_op(int variant, const ContigParams& p, dim3 g, cudaStream_t s) {
   if constexpr (std::is_same<Op, OpSum>::value) {
     switch (variant) {
-      case kContigU4: k_reduce_contig<4, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
-      case kContigU8: k_reduce_contig<8, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
+      case kContigU4: launch_pdl(k_reduce_contig<4, Op>, g, kThreads, 0, s, p); return cudaGetLastError();
+      case kContigU8: launch_pdl(k_reduce_contig<8, Op>, g, kThreads, 0, s, p); return cudaGetLastError();
       default: break;
     }
   }
   if (variant != kContigU16) return cudaErrorInvalidValue;
-  k_reduce_contig<16, Op><<<g, kThreads, 0, s>>>(p);
+  launch_pdl(k_reduce_contig<16, Op>, g, kThreads, 0, s, p);
   return cudaGetLastError();
 }
 
@@ -328,16 +332,16 @@ template <typename Op>
 cudaError_t cols_op(int variant, const ColsParams& p, dim3 g, cudaStream_t s) {
   if constexpr (std::is_same<Op, OpSum>::value) {
     switch (variant) {
-      case kColsV1W1: k_reduce_cols<1, 1, kColsU, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
-      case kColsV1W8: k_reduce_cols<1, 8, kColsU, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
-      case kColsV4W1: k_reduce_cols<4, 1, kColsU, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
-      case kColsV4W8: k_reduce_cols<4, 8, kColsU, Op><<<g, kThreads, 0, s>>>(p); return cudaGetLastError();
+      case kColsV1W1: launch_pdl(k_reduce_cols<1, 1, kColsU, Op>, g, kThreads, 0, s, p); return cudaGetLastError();
+      case kColsV1W8: launch_pdl(k_reduce_cols<1, 8, kColsU, Op>, g, kThreads, 0, s, p); return cudaGetLastError();
+      case kColsV4W1: launch_pdl(k_reduce_cols<4, 1, kColsU, Op>, g, kThreads, 0, s, p); return cudaGetLastError();
+      case kColsV4W8: launch_pdl(k_reduce_cols<4, 8, kColsU, Op>, g, kThreads, 0, s, p); return cudaGetLastError();
       default: break;
     }
   }
   switch (variant) {
-    case kColsV1W4: k_reduce_cols<1, 4, kColsU, Op><<<g, kThreads, 0, s>>>(p); break;
-    case kColsV4W4: k_reduce_cols<4, 4, kColsU, Op><<<g, kThreads, 0, s>>>(p); break;
+    case kColsV1W4: launch_pdl(k_reduce_cols<1, 4, kColsU, Op>, g, kThreads, 0, s, p); break;
+    case kColsV4W4: launch_pdl(k_reduce_cols<4, 4, kColsU, Op>, g, kThreads, 0, s, p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -376,13 +380,15 @@ cudaError_t cluster_op(const ContigParams& p, int ctas, cudaStream_t s) {
   cfg.blockDim = dim3(kClusterThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)ctas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_begin
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_reduce_cluster<Op>, p);
 }
 
@@ -402,10 +408,10 @@ cudaError_t launch_reduce_cluster(int op, const ContigParams& p, int ctas, cudaS
 cudaError_t launch_reduce_rows_warp(int op, const RowsWarpParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
   switch (op) {
-    case kOpSum: k_reduce_rows_warp<OpSum><<<g, kThreads, 0, s>>>(p); break;
-    case kOpSumSq: k_reduce_rows_warp<OpSumSq><<<g, kThreads, 0, s>>>(p); break;
-    case kOpMax: k_reduce_rows_warp<OpMax><<<g, kThreads, 0, s>>>(p); break;
-    case kOpMin: k_reduce_rows_warp<OpMin><<<g, kThreads, 0, s>>>(p); break;
+    case kOpSum: launch_pdl(k_reduce_rows_warp<OpSum>, g, kThreads, 0, s, p); break;
+    case kOpSumSq: launch_pdl(k_reduce_rows_warp<OpSumSq>, g, kThreads, 0, s, p); break;
+    case kOpMax: launch_pdl(k_reduce_rows_warp<OpMax>, g, kThreads, 0, s, p); break;
+    case kOpMin: launch_pdl(k_reduce_rows_warp<OpMin>, g, kThreads, 0, s, p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -424,7 +430,7 @@ cudaError_t launch_reduce_cols(int variant, int op, const ColsParams& p, int64_t
 
 cudaError_t launch_fill(float* out, int64_t n, float value, cudaStream_t s) {
   const int64_t blocks = std::min<int64_t>((n + kThreads - 1) / kThreads, 4096);
-  k_fill<<<dim3((unsigned)std::max<int64_t>(1, blocks)), kThreads, 0, s>>>(out, n, value);
+  launch_pdl(k_fill, dim3((unsigned)std::max<int64_t>(1, blocks)), kThreads, 0, s, out, n, value);
   return cudaGetLastError();
 }
 

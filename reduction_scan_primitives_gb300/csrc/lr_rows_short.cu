@@ -303,6 +303,7 @@ __device__ __forceinline__ void stage_chunk(const ShortRowsParams& p, float* s, 
 
 template <int G, int VEC, bool PLANES>
 __global__ void __launch_bounds__(kShortThreads, 7) k_rscan_short(ShortRowsParams p) {
+  pdl_begin();
   __shared__ __align__(16) float s[kShortSmem];
   const int t = threadIdx.x;
   const int gi = t / G;  // this thread's group
@@ -343,6 +344,7 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_rscan_short(ShortRowsParam
 // output (one float per row) and p.flags the epilogue.
 template <int G, int VEC, typename Op, bool PLANES>
 __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsParams p) {
+  pdl_begin();
   __shared__ __align__(16) float s[kShortSmem];
   const int t = threadIdx.x;
   const int gi = t / G;
@@ -391,9 +393,9 @@ __global__ void __launch_bounds__(kShortThreads, 7) k_reduce_short(ShortRowsPara
 template <int G, typename Op, bool PLANES>
 cudaError_t launch_reduce_gp(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
   if (vec == kShortLd4) {
-    k_reduce_short<G, kShortLd4, Op, PLANES><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+    launch_pdl(k_reduce_short<G, kShortLd4, Op, PLANES>, dim3((unsigned)grid), kShortThreads, 0, s, p);
   } else {
-    k_reduce_short<G, kShortLd1, Op, PLANES><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+    launch_pdl(k_reduce_short<G, kShortLd1, Op, PLANES>, dim3((unsigned)grid), kShortThreads, 0, s, p);
   }
   return cudaGetLastError();
 }
@@ -418,9 +420,9 @@ cudaError_t launch_reduce_op(int lanes, int vec, const ShortRowsParams& p, int64
 template <int G, bool PLANES>
 cudaError_t launch_gp(int vec, const ShortRowsParams& p, int64_t grid, cudaStream_t s) {
   if (vec == kShortLd4) {
-    k_rscan_short<G, kShortLd4, PLANES><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+    launch_pdl(k_rscan_short<G, kShortLd4, PLANES>, dim3((unsigned)grid), kShortThreads, 0, s, p);
   } else {
-    k_rscan_short<G, kShortLd1, PLANES><<<dim3((unsigned)grid), kShortThreads, 0, s>>>(p);
+    launch_pdl(k_rscan_short<G, kShortLd1, PLANES>, dim3((unsigned)grid), kShortThreads, 0, s, p);
   }
   return cudaGetLastError();
 }

@@ -360,6 +360,7 @@ __device__ __forceinline__ void block_sum_p(float (&v)[P], float (&sh)[kNW][P]) 
 // ---------------------------------------------------------------------------
 template <int VEC, int SUB, bool EDGES, int P = 1>
 __global__ void __launch_bounds__(kThreads) k_rscan_rows(RScanRowsParams p) {
+  pdl_begin();
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
   __shared__ float sh_w[2][SUB][kNW][P];  // warp totals, double-buffered by tile parity
   const int t = threadIdx.x;
@@ -448,6 +449,7 @@ constexpr int kMaxLevels = kNW;  // one warp per level: 32^8 tiles per row at mo
 
 template <int VEC, int SUB>
 __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackParams p) {
+  pdl_begin();
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
   __shared__ float sh_w[SUB][kNW][1];
   __shared__ float s_part[kMaxLevels];
@@ -572,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_rscan_lookback(RScanLookbackPar
 // class.
 template <int SUB, bool EARLY, bool EDGES, int P = 1>
 __global__ void __launch_bounds__(kThreads, P == 1 ? 4 : 3) k_rscan_lookback_l2(RScanLookbackParams p) {
+  pdl_begin();
   constexpr int64_t TILE = (int64_t)SUB * kThreads * 4;
   __shared__ __align__(128) float s_tile[TILE];
   __shared__ unsigned long long s_bar;
@@ -791,6 +794,7 @@ __global__ void __launch_bounds__(kThreads, P == 1 ? 4 : 3) k_rscan_lookback_l2(
 // ---------------------------------------------------------------------------
 template <int VEC, int SUB, bool EDGES>
 __global__ void __launch_bounds__(kThreads) k_tile_sums(TileSumsParams p) {
+  pdl_begin();
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
   __shared__ float sh[kNW];
   const int64_t b = blockIdx.x;
@@ -810,6 +814,7 @@ __global__ void __launch_bounds__(kThreads) k_tile_sums(TileSumsParams p) {
 
 template <int VEC, int SUB, bool EDGES>
 __global__ void __launch_bounds__(kThreads, 3) k_tile_carry_scan(TileCarryParams p) {
+  pdl_begin();
   constexpr int64_t TILE = (int64_t)SUB * kThreads * VEC;
   __shared__ float sh_w[SUB][kNW][1];
   const int t = threadIdx.x;
@@ -844,6 +849,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_tile_carry_scan(TileCarryParams
 
 template <int VEC, int WX, int WY, int U>
 __global__ void __launch_bounds__(kThreads, VEC == 4 ? 3 : 4) k_scan_cols(ScanColsParams p) {
+  pdl_begin();
   static_assert(WX * WY * 32 == kThreads, "WX warps across columns, WY down the axis");
   constexpr int CW = WX * 32 * VEC;
   constexpr int T = WY * U;
@@ -971,25 +977,25 @@ cudaError_t launch_rscan_rows(int variant, const RScanRowsParams& p, int64_t gri
     if (variant != kRScanV4S4) return cudaErrorInvalidValue;
     const bool edges = (p.flags & kScanRowEdges) != 0;
     if (p.period == 2) {
-      if (edges) k_rscan_rows<4, 4, true, 2><<<g, kThreads, 0, s>>>(p);
-      else k_rscan_rows<4, 4, false, 2><<<g, kThreads, 0, s>>>(p);
+      if (edges) launch_pdl(k_rscan_rows<4, 4, true, 2>, g, kThreads, 0, s, p);
+      else launch_pdl(k_rscan_rows<4, 4, false, 2>, g, kThreads, 0, s, p);
     } else if (p.period == 4) {
-      if (edges) k_rscan_rows<4, 4, true, 4><<<g, kThreads, 0, s>>>(p);
-      else k_rscan_rows<4, 4, false, 4><<<g, kThreads, 0, s>>>(p);
+      if (edges) launch_pdl(k_rscan_rows<4, 4, true, 4>, g, kThreads, 0, s, p);
+      else launch_pdl(k_rscan_rows<4, 4, false, 4>, g, kThreads, 0, s, p);
     } else {
       return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
   }
   switch (variant) {
-    case kRScanV1S4: k_rscan_rows<1, 4, false><<<g, kThreads, 0, s>>>(p); break;
+    case kRScanV1S4: launch_pdl(k_rscan_rows<1, 4, false>, g, kThreads, 0, s, p); break;
     case kRScanV4S2:
-      if (p.flags & kScanRowEdges) k_rscan_rows<4, 2, true><<<g, kThreads, 0, s>>>(p);
-      else k_rscan_rows<4, 2, false><<<g, kThreads, 0, s>>>(p);
+      if (p.flags & kScanRowEdges) launch_pdl(k_rscan_rows<4, 2, true>, g, kThreads, 0, s, p);
+      else launch_pdl(k_rscan_rows<4, 2, false>, g, kThreads, 0, s, p);
       break;
     case kRScanV4S4:
-      if (p.flags & kScanRowEdges) k_rscan_rows<4, 4, true><<<g, kThreads, 0, s>>>(p);
-      else k_rscan_rows<4, 4, false><<<g, kThreads, 0, s>>>(p);
+      if (p.flags & kScanRowEdges) launch_pdl(k_rscan_rows<4, 4, true>, g, kThreads, 0, s, p);
+      else launch_pdl(k_rscan_rows<4, 4, false>, g, kThreads, 0, s, p);
       break;
     default: return cudaErrorInvalidValue;
   }
@@ -1006,11 +1012,11 @@ template <int P>
 cudaError_t launch_l2_p(const RScanLookbackParams& p, dim3 g, cudaStream_t s) {
   constexpr int SUB = kL2Sub<P>;
   if (p.flags & kScanRowEdges) {
-    if (p.flags & kScanMirror) k_rscan_lookback_l2<SUB, true, true, P><<<g, kThreads, 0, s>>>(p);
-    else k_rscan_lookback_l2<SUB, false, true, P><<<g, kThreads, 0, s>>>(p);
+    if (p.flags & kScanMirror) launch_pdl(k_rscan_lookback_l2<SUB, true, true, P>, g, kThreads, 0, s, p);
+    else launch_pdl(k_rscan_lookback_l2<SUB, false, true, P>, g, kThreads, 0, s, p);
   } else {
-    if (p.flags & kScanMirror) k_rscan_lookback_l2<SUB, true, false, P><<<g, kThreads, 0, s>>>(p);
-    else k_rscan_lookback_l2<SUB, false, false, P><<<g, kThreads, 0, s>>>(p);
+    if (p.flags & kScanMirror) launch_pdl(k_rscan_lookback_l2<SUB, true, false, P>, g, kThreads, 0, s, p);
+    else launch_pdl(k_rscan_lookback_l2<SUB, false, false, P>, g, kThreads, 0, s, p);
   }
   return cudaGetLastError();
 }
@@ -1020,8 +1026,8 @@ cudaError_t launch_rscan_lookback(int variant, const RScanLookbackParams& p, int
   if (variant != kLookbackL2 && p.period != 1) return cudaErrorInvalidValue;
   const dim3 g((unsigned)grid);
   switch (variant) {
-    case kLookbackV1: k_rscan_lookback<1, 8><<<g, kThreads, 0, s>>>(p); break;
-    case kLookbackV4: k_rscan_lookback<4, 8><<<g, kThreads, 0, s>>>(p); break;
+    case kLookbackV1: launch_pdl(k_rscan_lookback<1, 8>, g, kThreads, 0, s, p); break;
+    case kLookbackV4: launch_pdl(k_rscan_lookback<4, 8>, g, kThreads, 0, s, p); break;
     case kLookbackL2:
       if (p.period == 2) return launch_l2_p<2>(p, g, s);
       if (p.period == 4) return launch_l2_p<4>(p, g, s);
@@ -1048,9 +1054,9 @@ int occupancy_rscan_lookback(int variant) {
 cudaError_t launch_scan_cols(int variant, const ScanColsParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
   switch (variant) {
-    case kScanColsV1: k_scan_cols<1, 2, 4, 16><<<g, kThreads, 0, s>>>(p); break;
-    case kScanColsV4: k_scan_cols<4, 2, 4, 8><<<g, kThreads, 0, s>>>(p); break;
-    case kScanColsV4Y8: k_scan_cols<4, 1, 8, 8><<<g, kThreads, 0, s>>>(p); break;
+    case kScanColsV1: launch_pdl(k_scan_cols<1, 2, 4, 16>, g, kThreads, 0, s, p); break;
+    case kScanColsV4: launch_pdl(k_scan_cols<4, 2, 4, 8>, g, kThreads, 0, s, p); break;
+    case kScanColsV4Y8: launch_pdl(k_scan_cols<4, 1, 8, 8>, g, kThreads, 0, s, p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -1079,10 +1085,10 @@ int64_t tile_scan_len(int variant) { return variant == kTileV4 ? 8 * kThreads * 
 cudaError_t launch_tile_sums(int variant, const TileSumsParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
   if (variant == kTileV4) {
-    if (p.flags & kScanRowEdges) k_tile_sums<4, 8, true><<<g, kThreads, 0, s>>>(p);
-    else k_tile_sums<4, 8, false><<<g, kThreads, 0, s>>>(p);
+    if (p.flags & kScanRowEdges) launch_pdl(k_tile_sums<4, 8, true>, g, kThreads, 0, s, p);
+    else launch_pdl(k_tile_sums<4, 8, false>, g, kThreads, 0, s, p);
   } else {
-    k_tile_sums<1, 8, false><<<g, kThreads, 0, s>>>(p);
+    launch_pdl(k_tile_sums<1, 8, false>, g, kThreads, 0, s, p);
   }
   return cudaGetLastError();
 }
@@ -1090,10 +1096,10 @@ cudaError_t launch_tile_sums(int variant, const TileSumsParams& p, int64_t grid,
 cudaError_t launch_tile_carry_scan(int variant, const TileCarryParams& p, int64_t grid, cudaStream_t s) {
   const dim3 g((unsigned)grid);
   if (variant == kTileV4) {
-    if (p.flags & kScanRowEdges) k_tile_carry_scan<4, 8, true><<<g, kThreads, 0, s>>>(p);
-    else k_tile_carry_scan<4, 8, false><<<g, kThreads, 0, s>>>(p);
+    if (p.flags & kScanRowEdges) launch_pdl(k_tile_carry_scan<4, 8, true>, g, kThreads, 0, s, p);
+    else launch_pdl(k_tile_carry_scan<4, 8, false>, g, kThreads, 0, s, p);
   } else {
-    k_tile_carry_scan<1, 8, false><<<g, kThreads, 0, s>>>(p);
+    launch_pdl(k_tile_carry_scan<1, 8, false>, g, kThreads, 0, s, p);
   }
   return cudaGetLastError();
 }

@@ -159,6 +159,7 @@ __device__ __forceinline__ float pick(const float (&a)[kColsPerWarp], int i) {
 template <int VEC>
 __global__ void __launch_bounds__(kLbThreads, 32 / kNW) k_scan_cols_lookback(
     ScanColsLookbackParams p, const __grid_constant__ CUtensorMap tmap) {
+  pdl_begin();
   using Ly = Layout<VEC>;
   constexpr int R = Ly::R;
   constexpr bool kTma = VEC == 4;
@@ -494,9 +495,9 @@ cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, 
   CUtensorMap m;
   std::memset(&m, 0, sizeof(m));
   if (vec == 4 && encode_cols_map(&m, p))
-    k_scan_cols_lookback<4><<<dim3((unsigned)grid), kLbThreads, kTileBytes, s>>>(p, m);
+    launch_pdl(k_scan_cols_lookback<4>, dim3((unsigned)grid), kLbThreads, kTileBytes, s, p, m);
   else
-    k_scan_cols_lookback<1><<<dim3((unsigned)grid), kLbThreads, kTileBytes, s>>>(p, m);
+    launch_pdl(k_scan_cols_lookback<1>, dim3((unsigned)grid), kLbThreads, kTileBytes, s, p, m);
   return cudaGetLastError();
 }
 

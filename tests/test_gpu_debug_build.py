@@ -51,7 +51,7 @@ def test_sum(dbg, n):
 
 
 @pytest.mark.parametrize("shape", [(37, 513, 67), (64, 40_000, 1), (3000, 100, 1), (5, 1000, 12),
-                                   (20_000, 100, 3), (2, 300_000, 64)])
+                                   (20_000, 100, 3), (2, 300_000, 64), (30_000, 101, 5)])
 def test_axis_sum(dbg, shape):
     x = on_device(inputs.make(shape, "uniform_pm1", 32))
     o, r, i = shape
@@ -65,7 +65,8 @@ def test_axis_sum(dbg, shape):
 @pytest.mark.parametrize("shape,flags", [((33, 10_000, 1), 1), ((2, 600_001, 1), 1), ((5001, 100, 1), 0),
                                          ((1, 3_000_000, 1), 3), ((8, 1000, 12), 2), ((2, 8192, 4096), 2),
                                          ((20_000, 100, 3), 1), ((64, 4096, 2), 0), ((1, 400_000, 2), 1),
-                                         ((3, 7000, 4095), 0)])
+                                         ((3, 7000, 4095), 0), ((100_000, 7, 3), 2), ((30_000, 101, 5), 0),
+                                         ((2, 300_000, 3), 0), ((2, 300_000, 3), 3)])
 def test_cumsum(dbg, shape, flags):
     x = on_device(inputs.make(shape, "uniform01", 33))
     y = torch.empty_like(x)
