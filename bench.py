@@ -77,6 +77,8 @@ PROFILE_CASES = {
     "cumsum_4096x4096x2_d1": dict(inputs.WORKLOADS["cumsum_4096x4096x2_d1"]),
     "cumsum_1x40000000x4_d1": dict(inputs.WORKLOADS["cumsum_1x40000000x4_d1"]),
     "sum_1e5": dict(op="sum", shape=(100_000,), dist="uniform01", seed=42),
+    "cumsum_500000x7x3_d1": dict(op="cumsum", shape=(500_000, 7, 3), dim=1, reverse=False,
+                                 exclusive=False, dist="uniform01", seed=13),
     "cumsum_1x50000000x2_d1": dict(op="cumsum", shape=(1, 50_000_000, 2), dim=1, reverse=False,
                                    exclusive=False, dist="uniform01", seed=13),
 }
