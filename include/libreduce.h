@@ -334,8 +334,9 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 short row (the automatic choice for planes of at
  *                                 most 768 floats); 9 planes of 2 to 8 columns
  *                                 read flat as segmented class runs (x 16-byte
- *                                 aligned, planes longer than a thread's run of
- *                                 20 to 36 floats; the
+ *                                 aligned, N >= 2; planes of at most one
+ *                                 thread's run of 20 to 36 floats only when
+ *                                 forced; the
  *                                 automatic choice from one item of planes per SM
  *                                 on)
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
@@ -364,9 +365,9 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 every 2nd or 4th element, by the row kernels
  *                                 (the automatic choice for 2-column planes of at
  *                                 least 4096 floats, after forms 8 and 9); 8 planes
- *                                 of 2 to 8 columns read flat as segmented class
- *                                 runs (x and y 16-byte aligned, planes longer than
- *                                 a thread's run of 20 to 36 floats; the automatic
+ *                                 of 2 to 8, 9, 10, 12 or 14 columns read flat as
+ *                                 segmented class runs (x and y 16-byte aligned,
+ *                                 N >= 2; the automatic
  *                                 choice from one item per SM on, an item being one
  *                                 plane or as many short planes as fit a tile of
  *                                 2560 to 4608 floats); 9 the same tiles with a

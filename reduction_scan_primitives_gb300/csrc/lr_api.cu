@@ -61,7 +61,7 @@ struct DeviceState {
   int occ_rscan_short = 0;
   int occ_rscan_period[3] = {};     // float4 block per row, period 1, 2, 4
   int occ_lookback_period[3] = {};  // L2 look-back, period 1, 2, 4
-  int occ_planes[kPlanesMaxP - 1][2] = {};  // narrow planes read flat: [P - 2][scan]
+  int occ_planes[kPlanesMaxScanP - 1][2] = {};  // narrow planes read flat: [P - 2][scan]
   int occ_planes_lb[kPlanesMaxP - 1] = {};  // the same, look-back form: [P - 2]
 };
 
@@ -136,9 +136,12 @@ int device_state(DeviceState** out, int* dev_out) {
       st.occ_lookback_period[pi] = std::max(1, occupancy_rscan_lookback_period(1 << pi));
     }
     st.occ_rscan_short = std::max(1, occupancy_rscan_short());
-    for (int pi = 0; pi < kPlanesMaxP - 1; ++pi) {
-      for (int sc = 0; sc < 2; ++sc) st.occ_planes[pi][sc] = std::max(1, occupancy_planes(pi + 2, sc != 0));
-      st.occ_planes_lb[pi] = std::max(1, occupancy_planes_lookback(pi + 2));
+    for (int pi = 0; pi < kPlanesMaxScanP - 1; ++pi) {
+      const int P = pi + 2;
+      if (planes_scan_columns(P)) st.occ_planes[pi][1] = std::max(1, occupancy_planes(P, true));
+      if (P > kPlanesMaxP) continue;
+      st.occ_planes[pi][0] = std::max(1, occupancy_planes(P, false));
+      st.occ_planes_lb[pi] = std::max(1, occupancy_planes_lookback(P));
     }
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
@@ -537,9 +540,9 @@ int run_narrow(const Provider& pv, const float* x, int64_t outer, int64_t reduce
   return launched(launch_reduce_narrow(vec, op, p, grid, s));
 }
 
-// Narrow planes of 2-8 columns read flat as segmented class runs
-// (lr_planes.cu): planes per item and items, or false when the shape does not
-// fit (planes of one row).  Short planes go k >= 2 to a tile (the item's
+// Narrow planes read flat as segmented class runs (lr_planes.cuh): 2-8
+// columns, and for scans also 9, 10, 12 and 14.  Planes per item and items,
+// or false when the shape does not fit (planes of one row).  Short planes go k >= 2 to a tile (the item's
 // start is rounded down to planes_align floats), planes no longer than a
 // thread's run with several boundaries in a run; longer ones one to an item.
 struct PlaneRunPlan {
@@ -547,9 +550,11 @@ struct PlaneRunPlan {
   unsigned long long magic = 0;
   bool multi = false;  // planes no longer than a thread's run: several boundaries in a run
 };
-bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl) {
+bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, bool scan) {
   int64_t L = 0;
-  if (inner < 2 || inner > kPlanesMaxP || outer <= 0 || N < 2 || mul_overflows(N, inner, &L)) return false;
+  if (inner < 2 || inner > kPlanesMaxScanP || (!scan && inner > kPlanesMaxP) || !planes_scan_columns((int)inner) ||
+      outer <= 0 || N < 2 || mul_overflows(N, inner, &L))
+    return false;
   const int64_t align = planes_align((int)inner);
   const int64_t k = (planes_tile_len((int)inner) - align + 1) / L;
   pl->k = k >= 2 ? k : 1;
@@ -648,7 +653,7 @@ int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, 
     const bool wide_forced = op == kOpSum && fv >= 0 && fv < kNumColsVariants;
     PlaneRunPlan pl;
     if ((fv < 0 || fv == kColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
-        (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && plane_run_plan(outer, reduce, inner, &pl) &&
+        (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && plane_run_plan(outer, reduce, inner, &pl, false) &&
         (fv == kColsPlaneRuns || plane_runs_fill(st, pl, inner, false)))
       return run_planes(pv, pl, x, outer, reduce, inner, out, epi, false, op, s);
     if (fv == kColsPlaneRuns) fv = -1;  // forced on a shape it does not take: the automatic choice
@@ -1181,12 +1186,12 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
     PlaneRunPlan pl;
     if ((fv < 0 || fv == kScanColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
         ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
-        plane_run_plan(outer, N, inner, &pl) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl, inner, true)))
+        plane_run_plan(outer, N, inner, &pl, true) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl, inner, true)))
       return run_planes(pv, pl, x, outer, N, inner, y, (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0),
                         true, kOpSum, s);
     if ((fv < 0 || fv == kScanColsPlaneLookback) && g_opt_axis_split.load() <= 0 &&
         ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
-        plane_run_plan(outer, N, inner, &pl) && !pl.multi &&
+        plane_run_plan(outer, N, inner, &pl, true) && !pl.multi && inner <= kPlanesMaxP &&
         (fv == kScanColsPlaneLookback || plane_runs_split(st, pl, N, inner))) {
       // Few long planes: each plane's tiles over blocks, carries by look-back.
       const int rc = run_planes_lookback(pv, x, outer, N, inner, y,

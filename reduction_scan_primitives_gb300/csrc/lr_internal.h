@@ -157,12 +157,20 @@ struct ShortRowsParams {
 // for scans) must be 16-byte aligned and N >= 2 (with L <= planes_run_len(P)
 // the kernels take the form for several plane boundaries in one thread's run).
 constexpr int kPlanesThreads = 128;  // threads per block (these kernels only)
-constexpr int kPlanesMaxP = 8;       // columns: 2 .. kPlanesMaxP
-// Consecutive floats per thread (whole rows of P columns), the alignment of
-// runs and tiles (16 bytes and P), and floats per tile.
-__host__ __device__ constexpr int planes_run_len(int P) { return P == 5 ? 20 : P == 7 ? 28 : P == 8 ? 24 : 36; }
+constexpr int kPlanesMaxP = 8;       // columns of every form: 2 .. kPlanesMaxP
+constexpr int kPlanesMaxScanP = 14;  // scans also take 9, 10, 12 and 14 columns
+__host__ __device__ constexpr bool planes_scan_columns(int P) {
+  return (P >= 2 && P <= kPlanesMaxP) || P == 9 || P == 10 || P == 12 || P == 14;
+}
+// Consecutive floats per thread (whole rows of P columns, at most 36), the
+// alignment of runs and tiles (lcm(4, P) floats: 16 bytes and P), and floats
+// per tile.
+__host__ __device__ constexpr int planes_run_len(int P) {
+  return P == 5 || P == 10 ? 20 : P == 7 || P == 14 ? 28 : P == 8 ? 24 : 36;
+}
 __host__ __device__ constexpr int planes_align(int P) {
-  return P == 3 || P == 6 ? 12 : P == 5 ? 20 : P == 7 ? 28 : P == 8 ? 8 : 4;
+  return P == 3 || P == 6 || P == 12 ? 12 : P == 5 ? 20 : P == 7 ? 28 : P == 8 ? 8 : P == 9 ? 36 : P == 10 ? 20
+       : P == 14 ? 28 : 4;
 }
 __host__ __device__ constexpr int planes_tile_len(int P) { return kPlanesThreads * planes_run_len(P); }
 struct PlaneRunParams {

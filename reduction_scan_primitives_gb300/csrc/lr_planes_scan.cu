@@ -41,6 +41,10 @@ cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cud
     case 6: return launch_scan_p<6>(p, g, s);
     case 7: return launch_scan_p<7>(p, g, s);
     case 8: return launch_scan_p<8>(p, g, s);
+    case 9: return launch_scan_p<9>(p, g, s);
+    case 10: return launch_scan_p<10>(p, g, s);
+    case 12: return launch_scan_p<12>(p, g, s);
+    case 14: return launch_scan_p<14>(p, g, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -55,6 +59,10 @@ int occupancy_planes(int P, bool scan) {
     case 6: return occupancy_scan_p<6>();
     case 7: return occupancy_scan_p<7>();
     case 8: return occupancy_scan_p<8>();
+    case 9: return occupancy_scan_p<9>();
+    case 10: return occupancy_scan_p<10>();
+    case 12: return occupancy_scan_p<12>();
+    case 14: return occupancy_scan_p<14>();
     default: return 0;
   }
 }

@@ -35,7 +35,10 @@ SHAPES = [(100_000, 100, 3), (4096, 4096, 2), (20_001, 19, 2), (30_001, 13, 4), 
           (100_000, 100, 8), (9999, 4, 8), (64, 50_001, 5), (3, 200_000, 8),
           # planes no longer than a thread's run: several boundaries in a run
           (500_000, 7, 3), (300_001, 2, 2), (200_000, 5, 4), (100_000, 3, 8), (100_001, 9, 4),
-          (70_000, 18, 2), (7, 4, 5), (40_000, 4, 7), (33_333, 12, 3), (50_000, 6, 6)]
+          (70_000, 18, 2), (7, 4, 5), (40_000, 4, 7), (33_333, 12, 3), (50_000, 6, 6),
+          # scans of 9, 10, 12 and 14 columns (runs of 36, 20, 36, 28 floats)
+          (100_000, 100, 9), (30_001, 37, 10), (20_000, 100, 12), (9999, 101, 14), (200_000, 3, 12),
+          (1000, 4001, 9), (64, 10_000, 14), (50_000, 2, 10)]
 
 
 def scan(x, reverse, exclusive, forced=True, out=None):
