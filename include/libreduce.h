@@ -334,9 +334,7 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 short row (the automatic choice for planes of at
  *                                 most 768 floats); 9 planes of 2 to 8 columns
  *                                 read flat as segmented class runs (x 16-byte
- *                                 aligned, N >= 2; planes of at most one
- *                                 thread's run of 20 to 36 floats only when
- *                                 forced; the
+ *                                 aligned, N >= 2; the
  *                                 automatic choice from one item of planes per SM
  *                                 on)
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,

@@ -576,14 +576,12 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, b
 // (fractions, runs against them: scans [1000, 10000, 8] 0.72 / 0.83, sums
 // [100000, 100, 8] 0.57 / 0.60; short-plane scans [100000, 100, 8] 0.89 /
 // 0.54 take the runs).
-// Reductions of planes no longer than a thread's run write every plane's
-// totals from scattered threads and stay with the short-row planes form
-// ([2e6, 8, 2] 0.41 against 0.62, [1e6, 5, 4] 0.35 against 0.56); their
-// scans take the runs ([500000, 7, 3] 0.87 against 0.53, [2e6, 8, 2] 0.88
-// against 0.64, [1e6, 4, 8] 0.84 against 0.62).
+// Planes no longer than a thread's run take the runs too: scans [500000,
+// 7, 3] 0.87 against 0.53, [2e6, 8, 2] 0.88 against 0.64, [1e6, 4, 8] 0.84
+// against 0.62; sums [500000, 7, 3] 0.74 against 0.39, [2e6, 8, 2] 0.81
+// against 0.63, [1e6, 3, 6] 0.52 against 0.41.
 bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t inner, bool scan) {
   if (inner == 8 && (!scan || pl.k < 2)) return false;
-  if (!scan && pl.multi) return false;
   return pl.items >= st->sm_count;
 }
 // Fewer items than SMs: the look-back form, whose blocks take single tiles,

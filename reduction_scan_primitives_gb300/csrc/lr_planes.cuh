@@ -147,11 +147,9 @@ struct RunState {
   int hp;            // the head: scan position in my run where a plane starts (kRunOf<P>: none)
   bool head_before;  // a lane before mine in the warp holds a head
   // Planes no longer than a run (several boundaries in it): the position of
-  // my first float (in scan order) within its plane, the last head, and for a
-  // reduction the scan positions where a plane ends and the item-relative
-  // plane of my first float.
+  // my first float (in scan order) within its plane, the last head, and the
+  // item-relative plane of my first float.
   int pos0, hlast, qfirst;
-  unsigned long long ends;
 };
 
 // Planes of L <= kRunOf<P> floats (every run holds a boundary): the head
@@ -248,25 +246,19 @@ __device__ __forceinline__ void runs_phase1(RunState<P>& st, const float* buf, i
     // Planes no longer than a run: a float restarts its class when it lies
     // in its plane's first row in scan order (position < P forward, >= L - P
     // reverse); the position walks with the float.  A reduction keeps every
-    // running value and notes where planes end (position L - 1, forward).
+    // running value.
     int pos = st.pos0;
-    unsigned long long ends = 0;
 #pragma unroll
     for (int e = 0; e < kRunOf<P>; ++e) {
       const int c = e % P;
       const bool restart = REV ? pos >= L - P : pos < P;
       const float before = restart ? Op::identity() : acc[c];
       acc[c] = restart ? st.v[e] : Op::combine(acc[c], st.v[e]);
-      if constexpr (SCAN) {
-        st.v[e] = EXCL ? before : acc[c];
-      } else {
-        st.v[e] = acc[c];
-        if (pos == L - 1) ends |= 1ull << e;
-      }
+      if constexpr (SCAN) st.v[e] = EXCL ? before : acc[c];
+      else st.v[e] = acc[c];
       if constexpr (REV) pos = pos == 0 ? L - 1 : pos - 1;
       else pos = pos + 1 == L ? 0 : pos + 1;
     }
-    st.ends = ends;
     // A class with no float after the last head keeps nothing for the new
     // plane (class c first appears hlast + ((c - hlast) mod P) floats in).
     const int hl = st.hlast;
@@ -450,7 +442,12 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
       if constexpr (MULTI) find_heads_short<P, REV>(a - rlo, Li, p.magic, st);
       else find_head<P, REV>(a, rlo, rhi, p.k == 1, Li, p.magic, st.hp, dd, qf);
       runs_phase1<P, SCAN, REV, EXCL, Op, MULTI>(st, buf, a, s_wagg[par], s_wflag[par], Li);
-      if constexpr (!SCAN) fence_proxy_async_smem();  // the buffer is refilled after barrier 1
+      // A scan, and a reduction of planes no longer than a run, use the tile
+      // buffer after barrier 1 (outputs, running values): the previous
+      // tile's buffer is refilled then.  Other reductions are done with it.
+      constexpr bool kReuse = SCAN || MULTI;
+      if constexpr (!kReuse) fence_proxy_async_smem();  // the buffer is refilled after barrier 1
+      if constexpr (!SCAN && MULTI) put_run<P, false>(st.v, buf, a);  // running values, my own slots
       // Barrier 1: warp totals visible; every thread is past its wait for
       // this tile and done with the previous tile's buffer.
       if (__syncthreads_or(!landed)) {
@@ -459,10 +456,10 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
       }
       if (t == 0) {
         --outstanding;
-        if (s_pc.item < p.items && (!SCAN || started)) {
+        if (s_pc.item < p.items && (!kReuse || started)) {
           // Refill: a scan's previous buffer (once its bulk store has read
           // it), a reduction's current one (its runs are in registers).
-          const int rs = SCAN ? (stage + kStages - 1) % kStages : stage;
+          const int rs = kReuse ? (stage + kStages - 1) % kStages : stage;
           if constexpr (SCAN) bulk_store_wait_read();
           Cursor pc = s_pc;
           issue_tile<P>(p, pc, REV, s_buf[rs], &s_bar[rs]);
@@ -482,28 +479,28 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
         store_tile_out(buf, p.y + ts, min(max(rlo, 0), kTileOf<P>), min(max(rhi, 0), kTileOf<P>));
         fence_proxy_async_smem();
       } else if constexpr (MULTI) {
-        // Every plane ending in my run (forward, where class c of a plane
-        // ends on its last row): its class totals are the running values
-        // there, with my carry for the plane that began before my run (a
-        // class that ended in an earlier run: the carry alone).
+        // Every plane ending in my run (forward, at position L - 1: my
+        // floats e1, e1 + L, ...): its class totals are the running values
+        // at its last row, read back from my own slots of the tile, with my
+        // carry for the plane that began before my run (a class whose last
+        // float lies in an earlier run: the carry alone).
+        const int L = Li;
         int q = st.qfirst;
+        for (int e = L - 1 - st.pos0; e < kRunOf<P>; e += L, ++q) {
+          if (q < 0 || q >= it.planes) continue;
+          float* out = p.y + (it.first + q) * P;
 #pragma unroll
-        for (int e = 0; e < kRunOf<P>; ++e) {
-          if ((st.ends >> e) & 1ull) {
-            if (q >= 0 && q < it.planes) {
-              float* out = p.y + (it.first + q) * P;
-#pragma unroll
-              for (int c = 0; c < P; ++c) {
-                const int idx = e - ((e % P - c + P) % P);  // class c's last float of this plane
-                float val;
-                if (idx < 0) val = cl[c];
-                else val = idx < st.hp ? Op::combine(cl[c], st.v[idx < 0 ? 0 : idx]) : st.v[idx < 0 ? 0 : idx];
-                st_plain(out + c, finish(val, p.flags, p.N));
-              }
+          for (int c = 0; c < P; ++c) {
+            const int idx = e - ((e % P - c + P) % P);  // class c's last float of this plane
+            float val = cl[c];
+            if (idx >= 0) {
+              const float r = buf[a + idx];
+              val = idx < st.hp ? Op::combine(cl[c], r) : r;
             }
-            ++q;
+            st_plain(out + c, finish(val, p.flags, p.N));
           }
         }
+        fence_proxy_async_smem();  // the buffer is refilled after the next tile's barrier 1
       } else {
         // A plane ending in my run: its class totals are my carry plus my
         // floats before the boundary.

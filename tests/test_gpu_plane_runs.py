@@ -141,11 +141,11 @@ def test_neighbours_untouched(reverse):
 
 
 @pytest.mark.parametrize("shape,sums", [((100_000, 100, 3), True), ((4096, 4096, 2), True), ((50_000, 40, 4), True),
-                                        ((500_000, 7, 3), False)])
+                                        ((500_000, 7, 3), True), ((100_000, 100, 8), False)])
 def test_automatic_choice_takes_plane_runs(shape, sums):
     """Aligned planes whose items fill the GPU take this form without options:
-    the automatic result is the forced one bit for bit (sums of planes no
-    longer than a thread's run keep the short-row form)."""
+    the automatic result is the forced one bit for bit (sums of 8 columns keep
+    the narrow kernels)."""
     x = inputs.make(shape, "uniform_pm1", 37)
     auto = scan(x, False, False, forced=False).clone()
     forced = scan(x, False, False)
