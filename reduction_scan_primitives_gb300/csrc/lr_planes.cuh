@@ -18,21 +18,23 @@
 //
 // Thread t of the 128 owns run m of R consecutive floats of the tile (m = t;
 // m = 127 - t for a reverse scan, whose scan order runs down memory): R = 36
-// for 2, 3, 4 and 6 columns, 20 for 5, 28 for 7, 24 for 8 (kRunOf).  R holds
-// whole rows and every run starts at a multiple of P, so the column class of
-// each of a thread's floats is known at compile time; as L > R, a run holds
-// at most one plane boundary (its "head": the scan position where a plane
-// starts, in scan order).  The steps:
+// for 2, 3, 4, 6, 9 and 12 columns, 20 for 5 and 10, 28 for 7 and 14, 24 for
+// 8 (kRunOf).  R holds whole rows and every run starts at a multiple of P, so
+// the column class of each of a thread's floats is known at compile time.
+// When L > R a run holds at most one plane boundary (its "head": the scan
+// position where a plane starts, in scan order); planes no longer than a run
+// take the MULTI form, which walks each float's position in its plane and
+// restarts a class on its plane's first row.  The steps:
 //   1. a sequential per-class scan over the run, restarting at the head;
 //   2. a segmented shuffle scan of the run totals across the warp (per class,
 //      the lanes before a lane's last head excluded);
 //   3. the warps' totals through shared memory, folded in warp order with the
 //      carry of the previous tile (same segment rule);
-//   4. each float before its run's head gets its lane's carry; a scan writes
-//      the run back in place and the tile leaves by one bulk store of its
-//      whole 16-byte granules (the item's partial first and last granules by
-//      plain stores); a reduction writes the P totals of each plane that ends
-//      in the run.
+//   4. each float before its run's (first) head gets its lane's carry; a
+//      scan writes the run back in place and the tile leaves by one bulk
+//      store of its whole 16-byte granules (the item's partial first and
+//      last granules by plain stores); a reduction writes the P totals of
+//      each plane that ends in the run.
 // Every output is a sum over its own terms in a fixed order (an exclusive
 // output leaves its own term out of the running value), nothing is
 // subtracted, and reruns are bit-identical.  Floats of the tile outside the
