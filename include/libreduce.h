@@ -365,10 +365,11 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 least 4096 floats, after forms 8 and 9); 8 planes
  *                                 of 2 to 8, 9, 10, 12 or 14 columns read flat as
  *                                 segmented class runs (x and y 16-byte aligned,
- *                                 N >= 2; the automatic
- *                                 choice from one item per SM on, an item being one
- *                                 plane or as many short planes as fit a tile of
- *                                 2560 to 4608 floats); 9 the same tiles with a
+ *                                 N >= 2), and of 16 or 32 columns as float4
+ *                                 columns of 9 rows per thread (N >= 10); the
+ *                                 automatic choice from one item per SM on, an
+ *                                 item being one plane or as many short planes as
+ *                                 fit a tile (2560 to 4608 floats); 9 the same tiles with a
  *                                 plane's tiles spread over blocks and their carries
  *                                 from a look-back (the automatic choice for fewer
  *                                 items than SMs when planes hold two tiles or more)

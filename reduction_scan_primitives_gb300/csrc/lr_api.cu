@@ -541,7 +541,8 @@ int run_narrow(const Provider& pv, const float* x, int64_t outer, int64_t reduce
 }
 
 // Narrow planes read flat as segmented class runs (lr_planes.cuh): 2-8
-// columns, and for scans also 9, 10, 12 and 14.  Planes per item and items,
+// columns, and for scans also 9, 10, 12 and 14 (and 16 and 32 as
+// column-group runs).  Planes per item and items,
 // or false when the shape does not fit (planes of one row).  Short planes go k >= 2 to a tile (the item's
 // start is rounded down to planes_align floats), planes no longer than a
 // thread's run with several boundaries in a run; longer ones one to an item.
@@ -555,6 +556,15 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, b
   if (inner < 2 || inner > kPlanesMaxScanP || (!scan && inner > kPlanesMaxP) || !planes_scan_columns((int)inner) ||
       outer <= 0 || N < 2 || mul_overflows(N, inner, &L))
     return false;
+  if (planes_cg((int)inner)) {  // column-group runs: tiles of whole rows, boundaries in rows
+    if (N <= kPlanesCgRows) return false;
+    const int64_t k = planes_cg_tile_rows((int)inner) / N;
+    pl->k = k >= 2 ? k : 1;
+    pl->items = ceil_div(outer, pl->k);
+    pl->magic = pl->k >= 2 ? ((1ull << 32) + (unsigned long long)N - 1) / (unsigned long long)N : 0;
+    pl->multi = false;
+    return true;
+  }
   const int64_t align = planes_align((int)inner);
   const int64_t k = (planes_tile_len((int)inner) - align + 1) / L;
   pl->k = k >= 2 ? k : 1;
@@ -579,7 +589,9 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, b
 // Planes no longer than a thread's run take the runs too: scans [500000,
 // 7, 3] 0.87 against 0.53, [2e6, 8, 2] 0.88 against 0.64, [1e6, 4, 8] 0.84
 // against 0.62; sums [500000, 7, 3] 0.74 against 0.39, [2e6, 8, 2] 0.81
-// against 0.63, [1e6, 3, 6] 0.52 against 0.41.
+// against 0.63, [1e6, 3, 6] 0.52 against 0.41.  Scans of 16 and 32 columns
+// (column groups): [100000, 100, 16] 0.88 against 0.42, [50000, 100, 32]
+// 0.89 against 0.55, [1000, 10000, 16] 0.92 against 0.87.
 bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t inner, bool scan) {
   if (inner == 8 && (!scan || pl.k < 2)) return false;
   return pl.items >= st->sm_count;

@@ -158,10 +158,16 @@ struct ShortRowsParams {
 // the kernels take the form for several plane boundaries in one thread's run).
 constexpr int kPlanesThreads = 128;  // threads per block (these kernels only)
 constexpr int kPlanesMaxP = 8;       // columns of every form: 2 .. kPlanesMaxP
-constexpr int kPlanesMaxScanP = 14;  // scans also take 9, 10, 12 and 14 columns
+constexpr int kPlanesMaxScanP = 32;  // scans also take 9, 10, 12, 14, 16 and 32 columns
 __host__ __device__ constexpr bool planes_scan_columns(int P) {
-  return (P >= 2 && P <= kPlanesMaxP) || P == 9 || P == 10 || P == 12 || P == 14;
+  return (P >= 2 && P <= kPlanesMaxP) || P == 9 || P == 10 || P == 12 || P == 14 || P == 16 || P == 32;
 }
+// 16 and 32 columns: column-group runs (one float4 column of kPlanesCgRows
+// rows per thread) in tiles of planes_cg_tile_rows(P) whole rows; planes of
+// more than kPlanesCgRows rows.
+constexpr int kPlanesCgRows = 9;
+__host__ __device__ constexpr bool planes_cg(int P) { return P == 16 || P == 32; }
+__host__ __device__ constexpr int planes_cg_tile_rows(int P) { return kPlanesThreads / (P / 4) * kPlanesCgRows; }
 // Consecutive floats per thread (whole rows of P columns, at most 36), the
 // alignment of runs and tiles (lcm(4, P) floats: 16 bytes and P), and floats
 // per tile.
@@ -330,7 +336,7 @@ enum ColsVariant {
 constexpr int kColsNarrow = kNumColsVariants;
 constexpr int kColsNarrowWarp = kNumColsVariants + 1;
 constexpr int kColsShortPlanes = kNumColsVariants + 2;  // chunks of whole narrow planes (short-row kernels)
-constexpr int kColsPlaneRuns = kNumColsVariants + 3;    // planes of 2-4 columns, segmented class runs
+constexpr int kColsPlaneRuns = kNumColsVariants + 3;    // narrow planes, segmented class runs (lr_planes.cuh)
 enum RScanVariant { kRScanV1S4 = 0, kRScanV4S2 = 1, kRScanV4S4 = 2, kNumRScanVariants };
 enum LookbackVariant {
   kLookbackV1 = 0,  // scalar items, one tile per block, tile kept in registers
@@ -355,7 +361,7 @@ constexpr int kScanColsNarrowWarp = kNumScanColsVariants + 1;
 constexpr int kScanColsLookback = kNumScanColsVariants + 2;  // k_scan_cols_lookback
 constexpr int kScanColsShortPlanes = kNumScanColsVariants + 3;  // chunks of whole narrow planes (short-row kernels)
 constexpr int kScanColsPeriodRows = kNumScanColsVariants + 4;   // planes of 2 or 4 columns as flat rows
-constexpr int kScanColsPlaneRuns = kNumScanColsVariants + 5;    // planes of 2-4 columns, segmented class runs
+constexpr int kScanColsPlaneRuns = kNumScanColsVariants + 5;    // narrow planes, segmented class runs (lr_planes.cuh)
 constexpr int kScanColsPlaneLookback = kNumScanColsVariants + 6;  // the same tiles, a plane over blocks (look-back)
 enum TileScanVariant { kTileV1 = 0, kTileV4 = 1, kNumTileVariants };
 

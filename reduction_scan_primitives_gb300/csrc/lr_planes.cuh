@@ -539,6 +539,247 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Scans of planes of 16 or 32 columns: column-group runs.
+//
+// With P = 16 or 32 a run of whole rows would leave a thread one or two rows
+// and the lane scan P classes; here thread t instead owns column group g =
+// t % G (G = P / 4 float4 columns) of a run of kCgRows consecutive rows, row
+// group m = t / G (reversed for a reverse scan).  Its classes are the four
+// components of its float4, the same for every row, so the per-thread scan
+// is one addition per float and a plane boundary restarts all four at once.
+// The lanes of a warp with the same g (G apart) carry the row groups' totals
+// in log2(32 / G) shuffle steps; warps fold through shared memory as in
+// k_planes.  A tile holds kCgRows * 128 / G whole rows (4608 floats) from the
+// item's start (rows are 16-byte multiples, so no rounding), lands by one bulk
+// copy and leaves by one bulk store of the item's rows.  The runs of the 8
+// threads of a shared-memory phase fall in distinct banks: kCgRows is odd.
+// Planes must be longer than a run (N > kCgRows rows).
+// ---------------------------------------------------------------------------
+constexpr int kCgRows = kPlanesCgRows;  // rows per thread run
+template <int P>
+constexpr int kCgGroups = P / 4;  // float4 column groups per row
+template <int P>
+constexpr int kCgTileRows = planes_cg_tile_rows(P);
+template <int P>
+constexpr int kCgTile = kCgTileRows<P> * P;  // floats per tile
+
+template <int P>
+__device__ __forceinline__ PlaneItem cg_item(const PlaneRunParams& p, int64_t i) {
+  const int64_t L = p.N * P;
+  PlaneItem it;
+  it.first = i * p.k;
+  const int64_t planes = min(p.k, p.outer - it.first);
+  it.planes = (int)planes;
+  it.lo = it.first * L;
+  it.hi = it.lo + planes * L;
+  it.vlo = it.lo;
+  it.tiles = (int)((it.hi - it.lo + kCgTile<P> - 1) / kCgTile<P>);
+  return it;
+}
+
+template <int P>
+__device__ __forceinline__ void cg_issue(const PlaneRunParams& p, Cursor& c, bool rev, float* buf,
+                                         unsigned long long* bar) {
+  if (c.item >= p.items) return;
+  const int64_t ts = c.it.lo + (int64_t)(rev ? c.it.tiles - 1 - c.tile : c.tile) * kCgTile<P>;
+  const int64_t te = min(ts + kCgTile<P>, c.it.hi);
+  const unsigned bytes = (unsigned)(te - ts) * 4u;  // whole rows: a multiple of 16
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_load(buf, p.x + ts, bytes, bar);
+  if (++c.tile == c.it.tiles) {
+    c.item += gridDim.x;
+    c.tile = 0;
+    if (c.item < p.items) c.it = cg_item<P>(p, c.item);
+  }
+}
+
+template <int P, bool REV, bool EXCL>
+__global__ void __launch_bounds__(kT, 4) k_planes_cg(PlaneRunParams p) {
+  pdl_begin();
+  constexpr int G = kCgGroups<P>;
+  constexpr int S = kCgRows;
+  constexpr int RG = kT / G;  // row groups per tile
+  __shared__ __align__(128) float s_buf[kStages][kCgTile<P>];
+  __shared__ __align__(8) unsigned long long s_bar[kStages];
+  __shared__ float4 s_wagg[2][kNW][G];  // each warp's last-segment totals, by column group
+  __shared__ int s_wflag[2][kNW];
+  __shared__ float4 s_carry[2][G];
+  __shared__ Cursor s_pc;
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int w = t >> 5;
+  const int g = t % G;
+  const int m = REV ? RG - 1 - t / G : t / G;  // my row group, in memory order
+  const int row0 = m * S;                       // its first row in a tile
+  const unsigned gmask = (G == 4 ? 0x11111111u : 0x01010101u) << g;  // lanes of my column group
+  const int Ni = (int)min(p.N, (int64_t)INT32_MAX);
+
+  int outstanding = 0;
+  if (t == 0) {
+    Cursor pc;
+    pc.item = blockIdx.x;
+    pc.tile = 0;
+    if (pc.item < p.items) pc.it = cg_item<P>(p, pc.item);
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(&s_bar[s], 1);
+    fence_mbar_init();
+#pragma unroll
+    for (int s = 0; s < kStages; ++s)
+      if (pc.item < p.items) {
+        cg_issue<P>(p, pc, REV, s_buf[s], &s_bar[s]);
+        ++outstanding;
+      }
+    s_pc = pc;
+  }
+  __syncthreads();
+
+  int stage = 0;
+  unsigned phase = 0;
+  int par = 0;
+  bool started = false;
+  bool fail = false;
+  for (int64_t item = blockIdx.x; item < p.items && !fail; item += gridDim.x) {
+    const PlaneItem it = cg_item<P>(p, item);
+    const int64_t item_rows = (it.hi - it.lo) / P;
+    for (int j = 0; j < it.tiles; ++j) {
+      const bool landed = mbar_wait_copy(&s_bar[stage], phase);
+      const int jt = REV ? it.tiles - 1 - j : j;        // memory tile index
+      const int64_t tr0 = (int64_t)jt * kCgTileRows<P>;  // its first row (item-relative)
+      const int64_t ts = it.lo + tr0 * P;
+      float* buf = s_buf[stage];
+      // The head: forward, the first plane start at or after my first row
+      // (rows q*N, q = 0 .. planes; the one at the item's end isolates rows
+      // past it); reverse, the last row of a plane (q*N - 1, q >= 1).
+      const int rr = (int)min(tr0 + row0, (int64_t)INT32_MAX / 2);  // my first row, item-relative
+      int hp = S;
+      if (p.k == 1) {
+        if constexpr (!REV) {
+          const int d = rr == 0 ? 0 : Ni - rr;
+          if (d >= 0 && d < S) hp = d;
+        } else {
+          const int e = rr + S - Ni;
+          if (e >= 0 && e < S) hp = e;
+        }
+      } else {
+        if constexpr (!REV) {
+          const int q = rr == 0 ? 0 : (int)(((unsigned long long)(rr - 1) * p.magic) >> 32) + 1;
+          const int d = q * Ni - rr;
+          if (d < S) hp = d;
+        } else {
+          const int gq = rr + S;
+          const int q = (int)(((unsigned long long)gq * p.magic) >> 32);
+          const int e = gq - q * Ni;
+          if (q >= 1 && e < S) hp = e;
+        }
+      }
+      // 1. My rows in scan order, scanned per component; the head row
+      // restarts all four.
+      float4 v[S];
+#pragma unroll
+      for (int e = 0; e < S; ++e) {
+        const int row = row0 + (REV ? S - 1 - e : e);
+        v[e] = *reinterpret_cast<const float4*>(buf + row * P + 4 * g);
+      }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < S; ++e) {
+        const bool restart = e == hp;
+        const float4 before = restart ? make_float4(0.f, 0.f, 0.f, 0.f) : acc;
+        acc = make_float4(before.x + v[e].x, before.y + v[e].y, before.z + v[e].z, before.w + v[e].w);
+        v[e] = EXCL ? before : acc;
+      }
+      // 2. Segmented scan over the row groups of my column group in this
+      // warp (lanes G apart): lane l adds lanes at or after its last lane
+      // with a head.
+      const unsigned hmask = __ballot_sync(kFullMask, hp < S) & gmask;
+      const unsigned upto = hmask & (kFullMask >> (31 - lane));
+      const int hh = upto ? 31 - __clz((int)upto) : g;
+      float4 inc = acc;
+#pragma unroll
+      for (int o = G; o < 32; o <<= 1) {
+        const float ux = __shfl_up_sync(kFullMask, inc.x, o), uy = __shfl_up_sync(kFullMask, inc.y, o);
+        const float uz = __shfl_up_sync(kFullMask, inc.z, o), uw = __shfl_up_sync(kFullMask, inc.w, o);
+        if (lane - o >= hh) inc = make_float4(ux + inc.x, uy + inc.y, uz + inc.z, uw + inc.w);
+      }
+      float4 ex;
+      ex.x = __shfl_up_sync(kFullMask, inc.x, G);
+      ex.y = __shfl_up_sync(kFullMask, inc.y, G);
+      ex.z = __shfl_up_sync(kFullMask, inc.z, G);
+      ex.w = __shfl_up_sync(kFullMask, inc.w, G);
+      const bool head_before = (hmask & ((1u << lane) - 1u)) != 0;
+      if (lane >= 32 - G) {  // the warp's last row group holds its totals
+        s_wagg[par][w][g] = inc;
+        if (g == 0) s_wflag[par][w] = hmask != 0;  // a head in any row group of the warp
+      }
+      if (__syncthreads_or(!landed)) {
+        fail = true;
+        break;
+      }
+      if (t == 0) {
+        --outstanding;
+        if (s_pc.item < p.items && started) {
+          const int rs = (stage + kStages - 1) % kStages;
+          bulk_store_wait_read();
+          Cursor pc = s_pc;
+          cg_issue<P>(p, pc, REV, s_buf[rs], &s_bar[rs]);
+          s_pc = pc;
+          ++outstanding;
+        }
+      }
+      // 3. Carry into my warp for my column group, then into my row group.
+      float4 cw = j == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : s_carry[par][g];
+#pragma unroll
+      for (int q = 0; q < kNW - 1; ++q) {
+        if (q < w) {
+          const float4 a = s_wagg[par][q][g];
+          cw = s_wflag[par][q] ? a : make_float4(cw.x + a.x, cw.y + a.y, cw.z + a.z, cw.w + a.w);
+        }
+      }
+      if (w == kNW - 1 && lane >= 32 - G) {
+        const float4 a = s_wagg[par][kNW - 1][g];
+        s_carry[par ^ 1][g] = s_wflag[par][kNW - 1] ? a : make_float4(cw.x + a.x, cw.y + a.y, cw.z + a.z, cw.w + a.w);
+      }
+      const float4 cl = lane < G ? cw
+                                 : (head_before ? ex : make_float4(cw.x + ex.x, cw.y + ex.y, cw.z + ex.z, cw.w + ex.w));
+      // 4. Rows before the head take the carry; back in place, then the
+      // item's rows of the tile leave by one bulk store.
+#pragma unroll
+      for (int e = 0; e < S; ++e) {
+        if (e < hp) v[e] = make_float4(cl.x + v[e].x, cl.y + v[e].y, cl.z + v[e].z, cl.w + v[e].w);
+        const int row = row0 + (REV ? S - 1 - e : e);
+        *reinterpret_cast<float4*>(buf + row * P + 4 * g) = v[e];
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (t == 0) {
+        const int64_t rows = min((int64_t)kCgTileRows<P>, item_rows - tr0);
+        bulk_store(p.y + ts, buf, (unsigned)(rows * P) * 4u);
+      }
+      fence_proxy_async_smem();
+      started = true;
+      par ^= 1;
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (t == 0) {
+    if (fail) {
+      atomicOr(p.err_word, 1u);
+      for (int k = 0; k < outstanding; ++k) {
+        mbar_wait_copy(&s_bar[stage], phase);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    bulk_store_wait_all();
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Few long planes: one tile per block, the carry by look-back.
 //
 // The block with ticket t (tickets in scan order, plane after plane)

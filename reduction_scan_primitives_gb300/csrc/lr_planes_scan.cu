@@ -29,6 +29,27 @@ int occupancy_scan_p() {
                    occupancy_of(k_planes<P, true, true, true, OpSum, true>)});
 }
 
+// Column-group runs (16 and 32 columns).
+template <int P>
+cudaError_t launch_cg_p(const PlaneRunParams& p, dim3 g, cudaStream_t s) {
+  const bool rev = (p.flags & kScanMirror) == 0;
+  const bool excl = (p.flags & kScanExclusive) != 0;
+  if (rev) {
+    if (excl) launch_pdl(k_planes_cg<P, true, true>, g, kT, 0, s, p);
+    else launch_pdl(k_planes_cg<P, true, false>, g, kT, 0, s, p);
+  } else {
+    if (excl) launch_pdl(k_planes_cg<P, false, true>, g, kT, 0, s, p);
+    else launch_pdl(k_planes_cg<P, false, false>, g, kT, 0, s, p);
+  }
+  return cudaGetLastError();
+}
+
+template <int P>
+int occupancy_cg_p() {
+  return std::min({occupancy_of(k_planes_cg<P, false, false>), occupancy_of(k_planes_cg<P, false, true>),
+                   occupancy_of(k_planes_cg<P, true, false>), occupancy_of(k_planes_cg<P, true, true>)});
+}
+
 }  // namespace
 
 cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cudaStream_t s) {
@@ -45,6 +66,8 @@ cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cud
     case 10: return launch_scan_p<10>(p, g, s);
     case 12: return launch_scan_p<12>(p, g, s);
     case 14: return launch_scan_p<14>(p, g, s);
+    case 16: return launch_cg_p<16>(p, g, s);
+    case 32: return launch_cg_p<32>(p, g, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -63,6 +86,8 @@ int occupancy_planes(int P, bool scan) {
     case 10: return occupancy_scan_p<10>();
     case 12: return occupancy_scan_p<12>();
     case 14: return occupancy_scan_p<14>();
+    case 16: return occupancy_cg_p<16>();
+    case 32: return occupancy_cg_p<32>();
     default: return 0;
   }
 }

@@ -1,7 +1,8 @@
-"""Narrow planes of 2 to 8 columns read flat as segmented class runs (GPU):
+"""Narrow planes of 2 to 32 columns read flat as segmented class runs (GPU):
 [outer, N, P] scanned or reduced along N by k_planes, which reads each tile of
 the flat array into shared memory and scans runs of whole rows per thread, the
-column classes fixed and the segments restarting at plane boundaries.
+column classes fixed and the segments restarting at plane boundaries; scans of
+16 and 32 columns by k_planes_cg, a float4 column of 9 rows per thread.
 Against the oracle element by element: planes no longer than a thread's run
 (several boundaries in a run), short planes many to a tile (plane
 boundaries at and inside runs), planes of about one tile, planes over many
@@ -38,7 +39,14 @@ SHAPES = [(100_000, 100, 3), (4096, 4096, 2), (20_001, 19, 2), (30_001, 13, 4), 
           (70_000, 18, 2), (7, 4, 5), (40_000, 4, 7), (33_333, 12, 3), (50_000, 6, 6),
           # scans of 9, 10, 12 and 14 columns (runs of 36, 20, 36, 28 floats)
           (100_000, 100, 9), (30_001, 37, 10), (20_000, 100, 12), (9999, 101, 14), (200_000, 3, 12),
-          (1000, 4001, 9), (64, 10_000, 14), (50_000, 2, 10)]
+          (1000, 4001, 9), (64, 10_000, 14), (50_000, 2, 10),
+          # scans of 16 and 32 columns (column-group runs of 9 rows, tiles of
+          # 288 / 144 rows): many planes to a tile with a ragged last item,
+          # planes of 10 rows, planes filling a tile exactly, one plane to a
+          # tile, planes over 2 to 70 tiles
+          (20_000, 100, 16), (30_001, 13, 16), (9999, 10, 32), (50_001, 11, 32), (10_000, 144, 16),
+          (40_000, 72, 32), (5000, 145, 16), (2000, 289, 16), (300, 5001, 32), (64, 10_000, 16),
+          (3, 20_000, 16), (7, 12, 16)]
 
 
 def scan(x, reverse, exclusive, forced=True, out=None):
@@ -61,7 +69,8 @@ def test_scan_against_oracle(shape, reverse, exclusive):
 
 
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
-@pytest.mark.parametrize("shape", [(40_000, 25, 3), (3000, 2401, 2), (1000, 2500, 4), (200_000, 7, 3)])
+@pytest.mark.parametrize("shape", [(40_000, 25, 3), (3000, 2401, 2), (1000, 2500, 4), (200_000, 7, 3), (20_000, 50, 16),
+                                   (3000, 1001, 32)])
 def test_scan_integers_exact_and_bitwise(shape, reverse, exclusive):
     """{0..3} inputs: every prefix is an integer below 2^24, so exact."""
     x = inputs.make(shape, "int:0:3", 32)
@@ -128,8 +137,10 @@ def test_reduce_integers_exact_and_bitwise(shape):
 @pytest.mark.parametrize("reverse", [False, True])
 def test_neighbours_untouched(reverse):
     """Output at a 16-byte offset inside a larger buffer of sentinels; planes
-    whose boundaries fall inside float4 granules (L = 6002 and L = 38)."""
-    for shape in [(7, 3001, 2), (5001, 19, 2)]:
+    whose boundaries fall inside float4 granules (L = 6002 and L = 38), and
+    column-group tiles whose last item ends short of a tile (16 and 32
+    columns)."""
+    for shape in [(7, 3001, 2), (5001, 19, 2), (1001, 13, 16), (3, 1001, 32)]:
         x = inputs.make(shape, "uniform01", 36)
         n = x.numel()
         buf = torch.full((n + 12,), 5.0, device="cuda")
@@ -141,11 +152,12 @@ def test_neighbours_untouched(reverse):
 
 
 @pytest.mark.parametrize("shape,sums", [((100_000, 100, 3), True), ((4096, 4096, 2), True), ((50_000, 40, 4), True),
-                                        ((500_000, 7, 3), True), ((100_000, 100, 8), False)])
+                                        ((500_000, 7, 3), True), ((100_000, 100, 8), False),
+                                        ((100_000, 100, 16), False), ((50_000, 100, 32), False)])
 def test_automatic_choice_takes_plane_runs(shape, sums):
     """Aligned planes whose items fill the GPU take this form without options:
     the automatic result is the forced one bit for bit (sums of 8 columns keep
-    the narrow kernels)."""
+    the narrow kernels; sums of 16 and 32 columns have no plane-run form)."""
     x = inputs.make(shape, "uniform_pm1", 37)
     auto = scan(x, False, False, forced=False).clone()
     forced = scan(x, False, False)
