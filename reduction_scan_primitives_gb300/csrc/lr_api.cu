@@ -642,10 +642,12 @@ int run_planes_lookback(const Provider& pv, const float* x, int64_t outer, int64
   auto* ticket_word = reinterpret_cast<unsigned long long*>(sc.header + 2);
   const int64_t spin = g_opt_spin_limit.load();
   const int64_t lag_opt = g_opt_lookback_lag.load();
-  // The lag as for the row look-back, from this kernel's resident blocks.
+  // The lag: 5/4 of this kernel's resident blocks in either direction (a
+  // block publishes its tile before it waits on any node).  With 912
+  // resident, lags of 960 and 1536 tickets were slower than 1152 on [1, 4e7,
+  // 4], [1, 1e8, 2], [1, 5e7, 3] and [64, 1e6, 2], both directions.
   const int64_t resident = (int64_t)st->sm_count * st->occ_planes_lb[inner - 2];
-  const int64_t lag_auto =
-      std::max<int64_t>(64, ceil_div((flags & kScanMirror) ? resident * 5 / 4 : resident * 5 / 3, 64) * 64);
+  const int64_t lag_auto = std::max<int64_t>(64, ceil_div(resident * 5 / 4, 64) * 64);
   const int64_t lag = std::min<int64_t>(total, lag_opt > 0 ? lag_opt : lag_auto);
   PlaneLbParams p{x, y, outer, N, tiles, sc.nodes, ticket_word, sc.header,
                   spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag, flags};

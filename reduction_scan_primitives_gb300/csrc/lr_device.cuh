@@ -196,16 +196,29 @@ __device__ __forceinline__ float wait_node(const unsigned long long* node, unsig
 // The P class words of one look-back node (consecutive words from `node`):
 // all P loads are issued at once, then only the words not yet carrying this
 // launch's epoch are polled (bounded, as wait_node).
+// In two steps, so that other work hides the loads' latency: load_node_classes
+// issues the loads, settle_node_classes polls the words that did not carry
+// the epoch yet.
 template <int P>
-__device__ __forceinline__ void wait_node_classes(const unsigned long long* node, unsigned epoch, int64_t limit,
-                                                  const unsigned* abort_word, bool* fail, float (&out)[P]) {
-  unsigned long long word[P];
+__device__ __forceinline__ void load_node_classes(const unsigned long long* node, unsigned long long (&word)[P]) {
 #pragma unroll
   for (int c = 0; c < P; ++c) word[c] = ld_relaxed_u64(node + c);
+}
+template <int P>
+__device__ __forceinline__ void settle_node_classes(const unsigned long long* node, const unsigned long long (&word)[P],
+                                                    unsigned epoch, int64_t limit, const unsigned* abort_word,
+                                                    bool* fail, float (&out)[P]) {
 #pragma unroll
   for (int c = 0; c < P; ++c)
     out[c] = (unsigned)(word[c] >> 32) == epoch ? __uint_as_float((unsigned)word[c])
                                                 : wait_node(node + c, epoch, limit, abort_word, fail);
+}
+template <int P>
+__device__ __forceinline__ void wait_node_classes(const unsigned long long* node, unsigned epoch, int64_t limit,
+                                                  const unsigned* abort_word, bool* fail, float (&out)[P]) {
+  unsigned long long word[P];
+  load_node_classes<P>(node, word);
+  settle_node_classes<P>(node, word, epoch, limit, abort_word, fail, out);
 }
 
 // a[i] selected by a run-time index (registers cannot be indexed at run time).

@@ -791,8 +791,11 @@ __global__ void __launch_bounds__(kT, 4) k_planes_cg(PlaneRunParams p) {
 //      tile scan of both kernels with that carry, and a bulk store;
 //   3. sums tile t per class (a fixed tree) and publishes the sums, and every
 //      parent node this tile completes, as the row look-back does.
-// A forward scan takes 3 before 2, a reverse scan 2 before 3 (as the row
-// look-back measured best).  Tickets are taken in order by running blocks
+// Steps 2 and 3 interleave: the loads of tile u's look-back nodes go out
+// before the wait for tile t, whose node word goes out as soon as its sums
+// are in (no wait of tile u's delays it), then tile u's scan and bulk store,
+// and last the parents tile t completes.
+// Tickets are taken in order by running blocks
 // and a block waits only on tiles of smaller tickets, so every wait ends;
 // each is bounded all the same.  (A persistent form, each block taking its
 // next ticket and starting its copies while it works on the current one, ran
@@ -889,26 +892,102 @@ __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
   int levels = 1;
   while (levels < kPlanesLbLevels && ((p.tiles - 1) >> (5 * levels)) != 0) ++levels;
 
-  // ---- write out tile u = ticket - lag ----
-  const auto write_out = [&]() {
-    const int64_t u = ticket - p.lag;
-    if (u < 0) return;
-    const LbTile<P> g = lb_tile<P, REV>(p, u);
-    if (!g.real) return;
-    const unsigned long long* vals = p.node_val + g.plane * 2 * p.tiles * P;
-    if (w < levels) {
-      int64_t off = 0, count = p.tiles;
-      for (int q = 0; q < w; ++q) {
-        off += count;
-        count >>= 5;
+  const int64_t u = ticket - p.lag;
+  const bool pub = ticket < total;  // tile `ticket` is summed and published
+  const LbTile<P> gt = lb_tile<P, REV>(p, pub ? ticket : 0);
+  const LbTile<P> gu = lb_tile<P, REV>(p, u >= 0 ? u : 0);
+  const bool wr = u >= 0 && gu.real;  // tile u is written out
+
+  // 1. The loads of tile u's look-back nodes go out first (warp L reads
+  // level L; every node it needs was published about lag tickets ago), so
+  // that their latency passes while tile `ticket` is on its way from HBM.
+  const unsigned long long* node = nullptr;  // my lane's node, if any
+  unsigned long long word[P];
+  if (wr && w < levels) {
+    int64_t off = 0, count = p.tiles;
+    for (int q = 0; q < w; ++q) {
+      off += count;
+      count >>= 5;
+    }
+    const int64_t m = gu.j >> (5 * w);
+    const int d = (int)(m & 31);
+    if (lane < d) {
+      node = p.node_val + gu.plane * 2 * p.tiles * P + (off + (m - d) + lane) * P;
+      load_node_classes<P>(node, word);
+    }
+  }
+
+  // 2. Tile `ticket`'s class sums: my run's, in scan order (the classes as
+  // the tile scan numbers them), only the plane's own floats; warp trees,
+  // then the warp sums in order; warp 0 publishes them at once.
+  float own[P];
+#pragma unroll
+  for (int c = 0; c < P; ++c) own[c] = 0.f;
+  bool landed = true;
+  if (pub && gt.real) {  // an empty last tile publishes zeros
+    landed = mbar_wait_copy(&s_bar[0], 0u);
+    const int tlo = rel_sat(gt.lo, gt.ts);
+    const int thi = rel_sat(gt.hi, gt.ts);
+    const float4* src = reinterpret_cast<const float4*>(s_new + a);
+    const bool edge = tlo > a || thi < a + kRunOf<P>;
+#pragma unroll
+    for (int k = 0; k < kChunksOf<P>; ++k) {
+      const float4 q = src[k];
+      const float e4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = 4 * k + c;  // memory position a + i
+        const int e = REV ? kRunOf<P> - 1 - i : i;
+        const bool in = !edge || (a + i >= tlo && a + i < thi);
+        own[e % P] += in ? e4[c] : 0.f;
       }
-      const int64_t m = g.j >> (5 * w);
-      const int d = (int)(m & 31);
+    }
+#pragma unroll
+    for (int c = 0; c < P; ++c) {
+      own[c] = warp_reduce<OpSum>(own[c]);
+      if (lane == 0) s_red[w][c] = own[c];
+    }
+  }
+  // A copy that never landed: nothing published (the tiles behind wait out
+  // and fail) and no outputs.
+  const auto give_up = [&]() {
+    if (t == 0) {
+      atomicOr(p.err_word, 1u);
+      atomicExch(p.err_word + 1, epoch);
+      if (s_copies & 1) mbar_wait_copy(&s_bar[0], 0u);
+      if (s_copies & 2) mbar_wait_copy(&s_bar[1], 0u);
+    }
+  };
+  if (__syncthreads_or(!landed)) {
+    give_up();
+    return;
+  }
+  unsigned long long* tvals = p.node_val + gt.plane * 2 * p.tiles * P;
+  const bool publishing = pub && ticket != p.stall_tile;
+  if (pub && gt.real) {
+#pragma unroll
+    for (int c = 0; c < P; ++c) {
+      float r = s_red[0][c];
+#pragma unroll
+      for (int q = 1; q < kNW; ++q) r += s_red[q][c];
+      own[c] = r;
+    }
+  }
+  if (publishing && w == 0 && lane < P) st_relaxed_u64(tvals + gt.j * P + lane, pack_node(epoch, pick_class<P>(own, lane)));
+
+  // 3. Tile u up to its block fold: the look-back partials (the words not
+  // yet published are polled, bounded), then the run and lane scans of the
+  // reread (normally an L2 hit).
+  RunState<P> st;
+  int rlo = 0, rhi = 0;
+  landed = true;
+  if (wr) {
+    if (w < levels) {
       bool fail = false;
       float sib[P];
 #pragma unroll
       for (int c = 0; c < P; ++c) sib[c] = 0.f;
-      if (lane < d) wait_node_classes<P>(vals + (off + (m - d) + lane) * P, epoch, p.spin_limit, abort_word, &fail, sib);
+      if (node) settle_node_classes<P>(node, word, epoch, p.spin_limit, abort_word, &fail, sib);
 #pragma unroll
       for (int c = 0; c < P; ++c) {
         const float part = warp_tree_adjacent(sib[c]);
@@ -916,19 +995,22 @@ __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
       }
       if (__any_sync(kFullMask, fail) && lane == 0) s_fail = 1;
     }
-    const bool landed = mbar_wait_copy(&s_bar[1], 0u);
-    const int rlo = rel_sat(g.lo, g.ts);
-    const int rhi = rel_sat(g.hi, g.ts);
-    RunState<P> st;
+    landed = mbar_wait_copy(&s_bar[1], 0u);
+    rlo = rel_sat(gu.lo, gu.ts);
+    rhi = rel_sat(gu.hi, gu.ts);
     int dd, qf;
     find_head<P, REV>(a, rlo, rhi, true, 0, 0ull, st.hp, dd, qf);
     runs_phase1<P, true, REV, EXCL, OpSum>(st, s_old, a, s_wagg, s_wflag);
-    // The barrier also publishes s_part: each class's carry is its
-    // look-back partials from the lowest level up.
-    if (__syncthreads_or(!landed)) {
-      if (t == 0) s_fail = 1;
-      return;  // the copy never landed: no outputs
-    }
+  }
+  // The barrier publishes s_part and the warp folds.
+  if (__syncthreads_or(!landed)) {
+    give_up();
+    return;
+  }
+
+  // 4. The rest of tile u: each class's carry is its look-back partials from
+  // the lowest level up; back in place, then one bulk store.
+  if (wr) {
     float carry[P], cl[P];
 #pragma unroll
     for (int c = 0; c < P; ++c) {
@@ -939,100 +1021,47 @@ __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
     runs_phase2<P, true, OpSum>(st, carry, s_wagg, s_wflag, nullptr, cl);
     put_run<P, REV>(st.v, s_old, a);
     fence_proxy_async_smem();
-    __syncthreads();
-    store_tile_out(s_old, p.y + g.ts, min(max(rlo, 0), kTileOf<P>), min(max(rhi, 0), kTileOf<P>));
-  };
-
-  // ---- sum tile `ticket` per class and publish it ----
-  const auto publish = [&]() {
-    if (ticket >= total) return;
-    const LbTile<P> g = lb_tile<P, REV>(p, ticket);
-    float own[P];
-#pragma unroll
-    for (int c = 0; c < P; ++c) own[c] = 0.f;
-    if (g.real) {  // an empty last tile publishes zeros
-      const bool landed = mbar_wait_copy(&s_bar[0], 0u);
-      // My run's class sums in scan order (the classes as the tile scan
-      // numbers them), only the plane's own floats.
-      const int rlo = rel_sat(g.lo, g.ts);
-      const int rhi = rel_sat(g.hi, g.ts);
-      const float4* src = reinterpret_cast<const float4*>(s_new + a);
-      const bool edge = rlo > a || rhi < a + kRunOf<P>;
-#pragma unroll
-      for (int k = 0; k < kChunksOf<P>; ++k) {
-        const float4 q = src[k];
-        const float e4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int i = 4 * k + c;  // memory position a + i
-          const int e = REV ? kRunOf<P> - 1 - i : i;
-          const bool in = !edge || (a + i >= rlo && a + i < rhi);
-          own[e % P] += in ? e4[c] : 0.f;
-        }
-      }
-      // Block sums per class: warp trees, then the warp totals in order.
-#pragma unroll
-      for (int c = 0; c < P; ++c) {
-        own[c] = warp_reduce<OpSum>(own[c]);
-        if (lane == 0) s_red[w][c] = own[c];
-      }
-      if (__syncthreads_or(!landed)) {
-        if (t == 0) s_fail = 1;
-        return;  // nothing published: the tiles behind it wait out and fail
-      }
-#pragma unroll
-      for (int c = 0; c < P; ++c) {
-        float r = s_red[0][c];
-#pragma unroll
-        for (int q = 1; q < kNW; ++q) r += s_red[q][c];
-        own[c] = r;
-      }
-    }
-    unsigned long long* vals = p.node_val + g.plane * 2 * p.tiles * P;
-    if (w == 0 && ticket != p.stall_tile) {
-      if (lane < P) st_relaxed_u64(vals + g.j * P + lane, pack_node(epoch, pick_class<P>(own, lane)));
-      if ((g.j & 31) == 31) {  // publish every parent this tile completes
-        bool fail = false;
-        int64_t off = 0, count = p.tiles, m = g.j;
-        for (int L = 0; L < levels && (m & 31) == 31; ++L) {
-          float sib[P];
-#pragma unroll
-          for (int c = 0; c < P; ++c) sib[c] = 0.f;
-          if (lane < 31)
-            wait_node_classes<P>(vals + (off + (m - 31) + lane) * P, epoch, p.spin_limit, abort_word, &fail, sib);
-          if (__any_sync(kFullMask, fail)) break;
-#pragma unroll
-          for (int c = 0; c < P; ++c) {
-            const float parent = warp_tree_adjacent(lane < 31 ? sib[c] : own[c]);
-            own[c] = __shfl_sync(kFullMask, parent, 0);
-          }
-          const int64_t next_off = off + count;
-          if (lane < P)
-            st_relaxed_u64(vals + (next_off + (m >> 5)) * P + lane, pack_node(epoch, pick_class<P>(own, lane)));
-          off = next_off;
-          count >>= 5;
-          m >>= 5;
-        }
-        if (fail && lane == 0) s_fail = 1;
-      }
-    }
-  };
-
-  if constexpr (!REV) publish();
-  write_out();
-  if constexpr (REV) publish();
+  }
   __syncthreads();
+  if (wr) store_tile_out(s_old, p.y + gu.ts, min(max(rlo, 0), kTileOf<P>), min(max(rhi, 0), kTileOf<P>));
+
+  // 5. Every parent node tile `ticket` completes (warp 0, after the store is
+  // on its way): the 31 siblings before it and its own sums.
+  if (publishing && w == 0 && (gt.j & 31) == 31) {
+    bool fail = false;
+    int64_t off = 0, count = p.tiles, m = gt.j;
+    for (int L = 0; L < levels && (m & 31) == 31; ++L) {
+      float sib[P];
+#pragma unroll
+      for (int c = 0; c < P; ++c) sib[c] = 0.f;
+      if (lane < 31)
+        wait_node_classes<P>(tvals + (off + (m - 31) + lane) * P, epoch, p.spin_limit, abort_word, &fail, sib);
+      if (__any_sync(kFullMask, fail)) break;
+#pragma unroll
+      for (int c = 0; c < P; ++c) {
+        const float parent = warp_tree_adjacent(lane < 31 ? sib[c] : own[c]);
+        own[c] = __shfl_sync(kFullMask, parent, 0);
+      }
+      const int64_t next_off = off + count;
+      if (lane < P)
+        st_relaxed_u64(tvals + (next_off + (m >> 5)) * P + lane, pack_node(epoch, pick_class<P>(own, lane)));
+      off = next_off;
+      count >>= 5;
+      m >>= 5;
+    }
+    if (fail && lane == 0) s_fail = 1;
+  }
+  // s_fail's other writers came before the barriers above; thread 0 wrote
+  // the last one itself.
   if (t == 0) {
     if (s_fail) {
       atomicOr(p.err_word, 1u);
       atomicExch(p.err_word + 1, epoch);
     }
-    // No copy may still write into this block's shared memory, and the bulk
-    // store must have read it, when the block leaves (bounded waits; a
-    // landed copy returns at once).
-    if (s_copies & 1) mbar_wait_copy(&s_bar[0], 0u);
-    if (s_copies & 2) mbar_wait_copy(&s_bar[1], 0u);
-    bulk_store_wait_all();
+    // Both copies have landed (waited above); the bulk store must have read
+    // this block's shared memory before the block leaves.  Its writes need
+    // no wait: they are complete when the grid is.
+    bulk_store_wait_read();
   }
 }
 
