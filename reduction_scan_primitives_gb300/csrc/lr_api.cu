@@ -1178,9 +1178,11 @@ int run_scan_cols_lookback(const Provider& pv, const float* x, int64_t outer, in
   const int64_t spin = g_opt_spin_limit.load();
   const int64_t lag_opt = g_opt_lookback_lag.load();
   const int64_t resident = (int64_t)pv.st->sm_count * pv.st->occ_scan_cols_lb;
-  // 5/4 of the resident blocks: measured flat from 0.7x to 1.7x on [2, 8192,
-  // 4096], best near 1.25x on [1, 100000, 1024]; 2.2x falls out of L2.
-  const int64_t lag = std::min<int64_t>(total, lag_opt > 0 ? lag_opt : std::max<int64_t>(64, ceil_div(resident * 5 / 4, 64) * 64));
+  // 5/6 of the resident blocks (512 of 608): best or within 0.5% of best
+  // from 320 to 768 on [2, 8192, 4096], [1, 16384, 4096], [4, 4096, 2048],
+  // [8, 2048, 4096], [1, 65536, 512], [2, 32768, 1024] and [1, 100000, 1024]
+  // (768 was 1-5% slower; 448 and below wait on the look-back).
+  const int64_t lag = std::min<int64_t>(total, lag_opt > 0 ? lag_opt : std::max<int64_t>(64, ceil_div(resident * 5 / 6, 64) * 64));
   ScanColsLookbackParams p{x, y, outer, N, inner, col_tiles, tiles, sc.nodes, ticket_word, sc.header,
                            spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag,
                            reverse ? 1 : 0, exclusive ? 1 : 0};
