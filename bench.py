@@ -53,7 +53,7 @@ NEXT_WORKLOADS = ["cumsum_fwd_32768x32768", "cumsum_fwd_excl_1x1e9", "cumsum_128
                   "max_1e9", "norm_128x4096x4095_d1", "mean_4096x65536_d1", "min_65536x4096_d0",
                   "rcumsum_1x1e9_ws", "axis_65536x4096_d0_ws", "rcumsum_2000000x100", "sum_4000000x32_d1",
                   "cumsum_100000x100x3_d1", "sum_100000x100x3_d1", "cumsum_4096x4096x2_d1",
-                  "cumsum_1x40000000x4_d1"]
+                  "cumsum_1x40000000x4_d1", "cumsum_100000x100x16_d1"]
 # Small cases of each kernel for ncu captures: larger than L2, a few GB at most.
 PROFILE_CASES = {
     "sum_2e8": dict(op="sum", shape=(200_000_000,), dist="uniform01", seed=42),
@@ -76,6 +76,8 @@ PROFILE_CASES = {
     "sum_100000x100x3_d1": dict(inputs.WORKLOADS["sum_100000x100x3_d1"]),
     "cumsum_4096x4096x2_d1": dict(inputs.WORKLOADS["cumsum_4096x4096x2_d1"]),
     "cumsum_1x40000000x4_d1": dict(inputs.WORKLOADS["cumsum_1x40000000x4_d1"]),
+    "cumsum_40000x100x16_d1": dict(op="cumsum", shape=(40_000, 100, 16), dim=1, reverse=False,
+                                   exclusive=False, dist="uniform01", seed=13),
     "sum_1e5": dict(op="sum", shape=(100_000,), dist="uniform01", seed=42),
     "cumsum_500000x7x3_d1": dict(op="cumsum", shape=(500_000, 7, 3), dim=1, reverse=False,
                                  exclusive=False, dist="uniform01", seed=13),

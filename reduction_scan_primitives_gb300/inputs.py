@@ -107,7 +107,7 @@ WORKLOADS = {
                                 exclusive=False, dist="uniform01", seed=3),
     "sum_4000000x32_d1": dict(op="reduce", rop="sum", shape=(4_000_000, 32), dim=1,
                               dist="uniform_pm1", seed=11),
-    # Narrow planes (scans and sums along dim 1 with 2-4 columns): many tiny
+    # Narrow planes (scans and sums along dim 1 with 2-16 columns): many tiny
     # planes, planes one block wide, and one long plane.
     "cumsum_100000x100x3_d1": dict(op="cumsum", shape=(100_000, 100, 3), dim=1, reverse=False,
                                    exclusive=False, dist="uniform01", seed=13),
@@ -117,6 +117,9 @@ WORKLOADS = {
                                   exclusive=False, dist="uniform01", seed=13),
     "cumsum_1x40000000x4_d1": dict(op="cumsum", shape=(1, 40_000_000, 4), dim=1, reverse=False,
                                    exclusive=False, dist="uniform01", seed=13),
+    # Planes of 16 columns (float4 column groups).
+    "cumsum_100000x100x16_d1": dict(op="cumsum", shape=(100_000, 100, 16), dim=1, reverse=False,
+                                    exclusive=False, dist="uniform01", seed=13),
     # The same calls with caller-provided scratch.
     "rcumsum_1x1e9_ws": dict(op="cumsum", shape=(1, 1_000_000_000), dim=1, reverse=True,
                              exclusive=False, dist="uniform01", seed=3, ws=True),

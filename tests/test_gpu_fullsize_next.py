@@ -212,7 +212,8 @@ def test_short_rows_full_size():
     assert_close(s.cpu().numpy(), ref[:, 0], scale[:, 0], "short rows sum")
 
 
-@pytest.mark.parametrize("name", ["cumsum_100000x100x3_d1", "cumsum_4096x4096x2_d1", "cumsum_1x40000000x4_d1"])
+@pytest.mark.parametrize("name", ["cumsum_100000x100x3_d1", "cumsum_4096x4096x2_d1", "cumsum_1x40000000x4_d1",
+                                  "cumsum_100000x100x16_d1"])
 def test_narrow_plane_scans_every_output(name):
     """The bench's narrow-plane scans at full size, every output against the
     oracle, and a rerun bit for bit."""
