@@ -1,5 +1,6 @@
 // lr_planes.cuh -- cumulative sums and reductions along the middle axis of
-// [outer, N, P] for narrow planes of P = 2 .. 8 columns (sm_103a).
+// [outer, N, P] for narrow planes (sm_103a): reductions of 2 .. 8 columns,
+// scans of 2 .. 10, 12, 14, 16 and 32 columns.
 //
 // The POPCORNBENCH trace l1_p91 discusses scanning a dimension other than the
 // last; here that dimension has stride P.  Read flat, plane o is the L = N*P
@@ -35,6 +36,8 @@
 //      store of its whole 16-byte granules (the item's partial first and
 //      last granules by plain stores); a reduction writes the P totals of
 //      each plane that ends in the run.
+// Scans of 16 and 32 columns (k_planes_cg) give thread t one float4 column
+// of a run of 9 rows instead, so that its classes are the four components.
 // Every output is a sum over its own terms in a fixed order (an exclusive
 // output leaves its own term out of the running value), nothing is
 // subtracted, and reruns are bit-identical.  Floats of the tile outside the

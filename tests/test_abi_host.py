@@ -202,3 +202,16 @@ def test_plane_run_division_is_exact():
         e = np.arange(0, 4608 + 72 + 64 * d, dtype=np.uint64)
         magic = np.uint64(((1 << 32) + d - 1) // d)
         assert np.array_equal((e * magic) >> np.uint64(32), e // np.uint64(d)), d
+
+
+def test_column_group_row_division_is_exact():
+    """The 16- and 32-column scans find plane boundaries among the rows of a
+    tile holding k >= 2 planes of N rows (10 <= N <= 144: half a tile of 288
+    or 144 rows) by (r * ceil(2^32 / N)) >> 32 for r up to a tile and a run
+    (9 rows) past it; that is r // N there."""
+    import numpy as np
+    for rows in (288, 144):
+        for d in range(10, rows // 2 + 1):
+            r = np.arange(0, rows + 9 + 1, dtype=np.uint64)
+            magic = np.uint64(((1 << 32) + d - 1) // d)
+            assert np.array_equal((r * magic) >> np.uint64(32), r // np.uint64(d)), (rows, d)
