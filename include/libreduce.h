@@ -365,9 +365,13 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 least 4096 floats, after forms 8 and 9); 8 planes
  *                                 of 2 to 8, 9, 10, 12 or 14 columns read flat as
  *                                 segmented class runs (x and y 16-byte aligned,
- *                                 N >= 2), and of 16 or 32 columns as float4
- *                                 columns of 9 rows per thread (N >= 10); the
- *                                 automatic choice from one item per SM on, an
+ *                                 N >= 2), and of every other column count up
+ *                                 to 128 as column groups (a float4, float2 or
+ *                                 float of adjacent columns per thread over
+ *                                 runs of 9, 17 or 33 rows; N above the run);
+ *                                 the automatic choice from one item per SM on
+ *                                 (column groups of 64 columns or more only
+ *                                 below 512 rows), an
  *                                 item being one plane or as many short planes as
  *                                 fit a tile (2560 to 4608 floats); 9 the same tiles with a
  *                                 plane's tiles spread over blocks and their carries

@@ -63,6 +63,7 @@ struct DeviceState {
   int occ_lookback_period[3] = {};  // L2 look-back, period 1, 2, 4
   int occ_planes[kPlanesMaxScanP - 1][2] = {};  // narrow planes read flat: [P - 2][scan]
   int occ_planes_lb[kPlanesMaxP - 1] = {};  // the same, look-back form: [P - 2]
+  int occ_planes_cg[kPlanesCgInstances] = {};  // scans as column groups, by instance
 };
 
 // Index of a period (1, 2, 4) in the per-period tables.
@@ -143,6 +144,7 @@ int device_state(DeviceState** out, int* dev_out) {
       st.occ_planes[pi][0] = std::max(1, occupancy_planes(P, false));
       st.occ_planes_lb[pi] = std::max(1, occupancy_planes_lookback(P));
     }
+    for (int ci = 0; ci < kPlanesCgInstances; ++ci) st.occ_planes_cg[ci] = std::max(1, occupancy_planes_cg(ci));
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
   }
@@ -470,6 +472,7 @@ constexpr int64_t kDefaultSpinLimit = 1 << 20;  // polls (with short sleeps): we
 constexpr int kColLbNoFit = -2;  // distinct from kQueried
 constexpr int kNoPlanes = -3;  // distinct from kQueried and kColLbNoFit
 constexpr int64_t kShortPlaneInnerMax = 256;  // widest plane the short-row kernels take
+constexpr int64_t kShortPlaneAutoInnerMax = 64;  // widest plane the automatic choice gives them
 int try_reduce_short_planes(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner,
                             float* out, int op, int epi, bool forced, cudaStream_t s);
 
@@ -541,8 +544,8 @@ int run_narrow(const Provider& pv, const float* x, int64_t outer, int64_t reduce
 }
 
 // Narrow planes read flat as segmented class runs (lr_planes.cuh): 2-8
-// columns, and for scans also 9, 10, 12 and 14 (and 16 and 32 as
-// column-group runs).  Planes per item and items,
+// columns, and for scans also 9, 10, 12 and 14; scans of every other column
+// count up to 128 as column groups.  Planes per item and items,
 // or false when the shape does not fit (planes of one row).  Short planes go k >= 2 to a tile (the item's
 // start is rounded down to planes_align floats), planes no longer than a
 // thread's run with several boundaries in a run; longer ones one to an item.
@@ -550,21 +553,24 @@ struct PlaneRunPlan {
   int64_t k = 1, items = 0;
   unsigned long long magic = 0;
   bool multi = false;  // planes no longer than a thread's run: several boundaries in a run
+  bool cg = false;     // column groups (k_planes_cg)
 };
 bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, bool scan) {
   int64_t L = 0;
-  if (inner < 2 || inner > kPlanesMaxScanP || (!scan && inner > kPlanesMaxP) || !planes_scan_columns((int)inner) ||
-      outer <= 0 || N < 2 || mul_overflows(N, inner, &L))
-    return false;
-  if (planes_cg((int)inner)) {  // column-group runs: tiles of whole rows, boundaries in rows
-    if (N <= kPlanesCgRows) return false;
+  if (inner < 2 || outer <= 0 || N < 2 || mul_overflows(N, inner, &L)) return false;
+  if (scan && inner <= kPlanesCgMaxP && planes_cg((int)inner)) {
+    // Column groups: tiles of whole rows, boundaries in rows.
+    if (N <= planes_cg_run_rows((int)inner)) return false;
     const int64_t k = planes_cg_tile_rows((int)inner) / N;
     pl->k = k >= 2 ? k : 1;
     pl->items = ceil_div(outer, pl->k);
     pl->magic = pl->k >= 2 ? ((1ull << 32) + (unsigned long long)N - 1) / (unsigned long long)N : 0;
     pl->multi = false;
+    pl->cg = true;
     return true;
   }
+  if (inner > kPlanesMaxScanP || (!scan && inner > kPlanesMaxP) || !planes_scan_columns((int)inner)) return false;
+  pl->cg = false;
   const int64_t align = planes_align((int)inner);
   const int64_t k = (planes_tile_len((int)inner) - align + 1) / L;
   pl->k = k >= 2 ? k : 1;
@@ -589,11 +595,17 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, b
 // Planes no longer than a thread's run take the runs too: scans [500000,
 // 7, 3] 0.87 against 0.53, [2e6, 8, 2] 0.88 against 0.64, [1e6, 4, 8] 0.84
 // against 0.62; sums [500000, 7, 3] 0.74 against 0.39, [2e6, 8, 2] 0.81
-// against 0.63, [1e6, 3, 6] 0.52 against 0.41.  Scans of 16 and 32 columns
-// (column groups): [100000, 100, 16] 0.88 against 0.42, [50000, 100, 32]
-// 0.89 against 0.55, [1000, 10000, 16] 0.92 against 0.87.
-bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t inner, bool scan) {
+// against 0.63, [1e6, 3, 6] 0.52 against 0.41.  Scans as column groups
+// (11 to 128 columns, and 16 and 32) against the best other form: [58181,
+// 100, 11] 0.84 / 0.50, [4923, 1000, 13] 0.84 / 0.41, [40000, 100, 16] 0.87
+// / 0.41, [3555, 1000, 18] 0.89 / 0.43, [26666, 100, 24] 0.94 / 0.52,
+// [2064, 1000, 31] 0.87 / 0.63, [1333, 1000, 48] 0.88 / 0.73, [10000, 100,
+// 64] 0.87 / 0.82, [6400, 100, 100] 0.84 / 0.70, [640, 1000, 100] 0.81 /
+// 0.69; planes of 64 columns and 512 rows or more stay with the short-row
+// planes ([1000, 1000, 64] 0.82 / 0.89).
+bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t N, int64_t inner, bool scan) {
   if (inner == 8 && (!scan || pl.k < 2)) return false;
+  if (pl.cg && inner == 64 && N >= 512) return false;
   return pl.items >= st->sm_count;
 }
 // Fewer items than SMs: the look-back form, whose blocks take single tiles,
@@ -613,9 +625,10 @@ int run_planes(const Provider& pv, const PlaneRunPlan& pl, const float* x, int64
   Scratch sc;
   const int rc = acquire(pv, need, &sc, s);
   if (rc) return rc;
-  const int64_t slots = (int64_t)st->sm_count * st->occ_planes[inner - 2][scan ? 1 : 0];
-  const int64_t grid = std::max<int64_t>(1, std::min(pl.items, slots));
-  PlaneRunParams p{x, y, outer, N, pl.k, pl.items, pl.magic, flags, sc.header, pl.multi ? 1 : 0};
+  const int occ = pl.cg ? st->occ_planes_cg[cg_instance((int)inner)] : st->occ_planes[inner - 2][scan ? 1 : 0];
+  const int64_t grid = std::max<int64_t>(1, std::min(pl.items, (int64_t)st->sm_count * occ));
+  PlaneRunParams p{x, y, outer, N, pl.k, pl.items, pl.magic, flags, sc.header, pl.multi ? 1 : 0, (int)inner};
+  if (pl.cg) return launched(launch_planes_cg(p, grid, s));
   return launched(scan ? launch_planes_scan((int)inner, p, grid, s)
                        : launch_planes_reduce((int)inner, op, p, grid, s));
 }
@@ -666,7 +679,7 @@ int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, 
     PlaneRunPlan pl;
     if ((fv < 0 || fv == kColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
         (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && plane_run_plan(outer, reduce, inner, &pl, false) &&
-        (fv == kColsPlaneRuns || plane_runs_fill(st, pl, inner, false)))
+        (fv == kColsPlaneRuns || plane_runs_fill(st, pl, reduce, inner, false)))
       return run_planes(pv, pl, x, outer, reduce, inner, out, epi, false, op, s);
     if (fv == kColsPlaneRuns) fv = -1;  // forced on a shape it does not take: the automatic choice
     if ((fv < 0 || fv == kColsShortPlanes) && g_opt_axis_split.load() <= 0) {
@@ -1200,7 +1213,7 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
     PlaneRunPlan pl;
     if ((fv < 0 || fv == kScanColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
         ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
-        plane_run_plan(outer, N, inner, &pl, true) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl, inner, true)))
+        plane_run_plan(outer, N, inner, &pl, true) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl, N, inner, true)))
       return run_planes(pv, pl, x, outer, N, inner, y, (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0),
                         true, kOpSum, s);
     if ((fv < 0 || fv == kScanColsPlaneLookback) && g_opt_axis_split.load() <= 0 &&
@@ -1228,21 +1241,31 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
       return run_rscan_rows(pv, x, outer, N * inner, y, s,
                             (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0), (int)inner);
     }
-    if ((fv < 0 || fv == kScanColsShortPlanes) && g_opt_axis_split.load() <= 0 && N <= kShortRowMax &&
-        inner <= kShortPlaneInnerMax) {
+    if ((fv == kScanColsShortPlanes ||
+         (fv < 0 && inner <= kShortPlaneAutoInnerMax && (inner <= 32 || inner % 4 == 0))) &&
+        g_opt_axis_split.load() <= 0 && N <= kShortRowMax && inner <= kShortPlaneInnerMax) {
       // Narrow planes of at most kShortRowMax rows, whole planes to a chunk:
       // ahead of the narrow kernels wherever a plane fits (fraction of copy
       // bandwidth, planes against the better narrow form: [400000, 100, 3]
       // 0.52 / 0.26, [50000, 512, 2] 0.54 / 0.40, [12000, 2048, 2] 0.49 /
-      // 0.46, [30000, 100, 32] 0.53 / 0.45).
+      // 0.46, [30000, 100, 32] 0.53 / 0.45).  Above 64 columns, and above 32
+      // when the rows are not whole float4s, the wide column scan is ahead
+      // ([640, 1000, 100] 0.69 / 0.57, [500, 1000, 128] 0.85 / 0.71,
+      // [15000, 100, 47] 0.69 / 0.44, [20000, 100, 33] 0.53 / 0.46): forced
+      // only.
       const PlaneForm pf = plane_form(N, inner, kShortScanSolo, kShortScanSoloOdd,
                                       ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0);
       if (pf.ok)
         return run_scan_short_planes(pv, pf, x, outer, N, inner, y, s,
                                      (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0));
     }
-    if (narrow_rows(x, y, inner, &nvec) && (fv < 0 || fv == kScanColsNarrow || fv == kScanColsNarrowWarp ||
-                                            fv == kScanColsShortPlanes || fv == kScanColsPeriodRows)) {
+    // Scalar narrow rows of more than 32 columns (odd widths) go to the wide
+    // column scan unless forced ([3000, 300, 33] 0.62 against 0.25, [2000,
+    // 500, 65] 0.63 against 0.25; from 17 columns on it was already ahead:
+    // [3764, 1000, 17] 0.41 / 0.27).
+    if (narrow_rows(x, y, inner, &nvec) && (nvec == 4 || inner <= 32 || fv >= 0) &&
+        (fv < 0 || fv == kScanColsNarrow || fv == kScanColsNarrowWarp || fv == kScanColsShortPlanes ||
+         fv == kScanColsPeriodRows)) {
       // The block form walks tiles of T rows; a plane of fewer than T/2 rows
       // would leave most of its threads idle: a warp per plane instead
       // (measured on [100000, 100, 3]: 25% against 4% of copy bandwidth; on

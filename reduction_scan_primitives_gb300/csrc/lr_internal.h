@@ -158,16 +158,31 @@ struct ShortRowsParams {
 // the kernels take the form for several plane boundaries in one thread's run).
 constexpr int kPlanesThreads = 128;  // threads per block (these kernels only)
 constexpr int kPlanesMaxP = 8;       // columns of every form: 2 .. kPlanesMaxP
-constexpr int kPlanesMaxScanP = 32;  // scans also take 9, 10, 12, 14, 16 and 32 columns
+constexpr int kPlanesMaxScanP = 14;  // the runs also scan 9, 10, 12 and 14 columns
 __host__ __device__ constexpr bool planes_scan_columns(int P) {
-  return (P >= 2 && P <= kPlanesMaxP) || P == 9 || P == 10 || P == 12 || P == 14 || P == 16 || P == 32;
+  return (P >= 2 && P <= kPlanesMaxP) || P == 9 || P == 10 || P == 12 || P == 14;
 }
-// 16 and 32 columns: column-group runs (one float4 column of kPlanesCgRows
-// rows per thread) in tiles of planes_cg_tile_rows(P) whole rows; planes of
-// more than kPlanesCgRows rows.
-constexpr int kPlanesCgRows = 9;
-__host__ __device__ constexpr bool planes_cg(int P) { return P == 16 || P == 32; }
-__host__ __device__ constexpr int planes_cg_tile_rows(int P) { return kPlanesThreads / (P / 4) * kPlanesCgRows; }
+// Scans as column groups (k_planes_cg), 3 .. kPlanesCgMaxP columns: thread t
+// owns column group t % G of a run of planes_cg_run_rows rows, a group being
+// V = planes_cg_vec(P) adjacent columns (a float4, float2 or float) and G =
+// P / V <= 32; 128 / G row groups of a run make a tile of
+// planes_cg_tile_rows(P) whole rows.  Runs of 9, 17 and 33 rows (1 modulo
+// 32 / gcd(P, 32)) put the threads of a shared-memory phase on distinct
+// banks.  Planes of more than one run (N > planes_cg_run_rows).
+constexpr int kPlanesCgMaxP = 128;
+__host__ __device__ constexpr int planes_cg_vec(int P) { return P % 4 == 0 ? 4 : P % 2 == 0 ? 2 : 1; }
+__host__ __device__ constexpr int planes_cg_run_rows_v(int V) { return V == 4 ? 9 : V == 2 ? 17 : 33; }
+__host__ __device__ constexpr int planes_cg_run_rows(int P) { return planes_cg_run_rows_v(planes_cg_vec(P)); }
+__host__ __device__ constexpr int planes_cg_groups(int P) { return P / planes_cg_vec(P); }
+__host__ __device__ constexpr bool planes_cg_fits(int P) {
+  return P >= 3 && P <= kPlanesCgMaxP && planes_cg_groups(P) <= 32;
+}
+__host__ __device__ constexpr int planes_cg_tile_rows(int P) {
+  return kPlanesThreads / planes_cg_groups(P) * planes_cg_run_rows(P);
+}
+// The automatic choice and the plane-run option take the column groups for
+// every column count the runs do not scan.
+__host__ __device__ constexpr bool planes_cg(int P) { return planes_cg_fits(P) && !planes_scan_columns(P); }
 // Consecutive floats per thread (whole rows of P columns, at most 36), the
 // alignment of runs and tiles (lcm(4, P) floats: 16 bytes and P), and floats
 // per tile.
@@ -190,6 +205,7 @@ struct PlaneRunParams {
   int flags;           // scans: kScanMirror | kScanExclusive; reductions: the epilogue
   unsigned* err_word;  // bit 0 set if a tile's copy never lands
   int multi = 0;       // planes of 2P .. planes_run_len(P) floats: several boundaries in a run
+  int P = 0;           // columns (the column-group kernels take them at run time)
 };
 
 // Scans of few long planes of 2-8 columns, a plane's tiles spread over
@@ -415,6 +431,12 @@ cudaError_t launch_scan_cols_lookback(int vec, const ScanColsLookbackParams& p, 
 cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 cudaError_t launch_planes_reduce(int P, int op, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes(int P, bool scan);  // resident kPlanesThreads-thread blocks per SM
+// Column groups (k_planes_cg): the instance a column count takes (0 .. 5, -1
+// when none), its launch (p.P set) and its resident blocks per SM.
+constexpr int kPlanesCgInstances = 6;
+int cg_instance(int P);
+cudaError_t launch_planes_cg(const PlaneRunParams& p, int64_t grid, cudaStream_t s);
+int occupancy_planes_cg(int instance);
 int occupancy_planes_reduce(int P);
 cudaError_t launch_planes_lookback(int P, const PlaneLbParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes_lookback(int P);

@@ -1,6 +1,6 @@
 // lr_planes.cuh -- cumulative sums and reductions along the middle axis of
 // [outer, N, P] for narrow planes (sm_103a): reductions of 2 .. 8 columns,
-// scans of 2 .. 10, 12, 14, 16 and 32 columns.
+// scans of 2 .. 128 columns.
 //
 // The POPCORNBENCH trace l1_p91 discusses scanning a dimension other than the
 // last; here that dimension has stride P.  Read flat, plane o is the L = N*P
@@ -36,8 +36,9 @@
 //      store of its whole 16-byte granules (the item's partial first and
 //      last granules by plain stores); a reduction writes the P totals of
 //      each plane that ends in the run.
-// Scans of 16 and 32 columns (k_planes_cg) give thread t one float4 column
-// of a run of 9 rows instead, so that its classes are the four components.
+// Scans of other column counts, up to 128 (k_planes_cg), give thread t one
+// column group (a float4, float2 or float) of a run of 9, 17 or 33 rows
+// instead, so that its classes are the group's components.
 // Every output is a sum over its own terms in a fixed order (an exclusive
 // output leaves its own term out of the running value), nothing is
 // subtracted, and reruns are bit-identical.  Floats of the tile outside the
@@ -542,79 +543,111 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Scans of planes of 16 or 32 columns: column-group runs.
+// Scans as column groups, any P of 3 .. 128 columns.
 //
-// With P = 16 or 32 a run of whole rows would leave a thread one or two rows
-// and the lane scan P classes; here thread t instead owns column group g =
-// t % G (G = P / 4 float4 columns) of a run of kCgRows consecutive rows, row
-// group m = t / G (reversed for a reverse scan).  Its classes are the four
-// components of its float4, the same for every row, so the per-thread scan
-// is one addition per float and a plane boundary restarts all four at once.
-// The lanes of a warp with the same g (G apart) carry the row groups' totals
-// in log2(32 / G) shuffle steps; warps fold through shared memory as in
-// k_planes.  A tile holds kCgRows * 128 / G whole rows (4608 floats) from the
-// item's start (rows are 16-byte multiples, so no rounding), lands by one bulk
-// copy and leaves by one bulk store of the item's rows.  The runs of the 8
-// threads of a shared-memory phase fall in distinct banks: kCgRows is odd.
-// Planes must be longer than a run (N > kCgRows rows).
+// A run of whole rows per thread (k_planes) leaves wide planes one or two
+// rows a thread and the lane scan P classes.  Here thread t owns column
+// group g = t % G (V = 4, 2 or 1 adjacent columns: G = P / V groups) of a
+// run of S consecutive rows (S = 9, 17, 33 for V = 4, 2, 1), row group
+// t / G (reversed for a reverse scan); the 128 / G row groups of a tile make
+// it whole rows (threads past them idle, holding zeros).  A thread's classes
+// are its V components in every row, so its scan is one addition per float
+// and a plane boundary restarts all V at once.  The lanes of a warp with the
+// same g (G apart) carry the row groups' totals in log2(32 / G) shuffle
+// steps of a segmented scan; warps fold their per-group totals through
+// shared memory, with a head flag per warp and group.  A tile's rows start
+// anywhere in a 16-byte granule: it lands by one bulk copy of its whole
+// granules, delta floats in, and leaves by one bulk store of its whole
+// granules plus plain stores of the partial ones at its two ends.  S is 1
+// modulo 32 / gcd(P, 32), so a warp's threads read consecutive V-float
+// slots of every row of their runs: no bank conflicts.  Planes must be
+// longer than a run (N > S rows: at most one boundary per run).
 // ---------------------------------------------------------------------------
-constexpr int kCgRows = kPlanesCgRows;  // rows per thread run
-template <int P>
-constexpr int kCgGroups = P / 4;  // float4 column groups per row
-template <int P>
-constexpr int kCgTileRows = planes_cg_tile_rows(P);
-template <int P>
-constexpr int kCgTile = kCgTileRows<P> * P;  // floats per tile
+template <int V>
+constexpr int kCgS = planes_cg_run_rows_v(V);
+template <int V>
+constexpr int kCgBuf = kT * kCgS<V> * V + 8;  // floats per stage: the largest tile, its two partial granules
 
-template <int P>
-__device__ __forceinline__ PlaneItem cg_item(const PlaneRunParams& p, int64_t i) {
-  const int64_t L = p.N * P;
+template <int V>
+__device__ __forceinline__ void cg_ld(const float* p, float (&o)[V]) {
+  if constexpr (V == 4) {
+    const float4 q = *reinterpret_cast<const float4*>(p);
+    o[0] = q.x;
+    o[1] = q.y;
+    o[2] = q.z;
+    o[3] = q.w;
+  } else if constexpr (V == 2) {
+    const float2 q = *reinterpret_cast<const float2*>(p);
+    o[0] = q.x;
+    o[1] = q.y;
+  } else {
+    o[0] = *p;
+  }
+}
+template <int V>
+__device__ __forceinline__ void cg_st(float* p, const float (&o)[V]) {
+  if constexpr (V == 4) *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
+  else if constexpr (V == 2) *reinterpret_cast<float2*>(p) = make_float2(o[0], o[1]);
+  else *p = o[0];
+}
+
+// An item of k planes (tiles of TR whole rows from its first row).
+__device__ __forceinline__ PlaneItem cg_item(const PlaneRunParams& p, int TR, int64_t i) {
   PlaneItem it;
   it.first = i * p.k;
   const int64_t planes = min(p.k, p.outer - it.first);
   it.planes = (int)planes;
-  it.lo = it.first * L;
-  it.hi = it.lo + planes * L;
+  it.lo = it.first * p.N * p.P;
+  it.hi = it.lo + planes * p.N * p.P;
   it.vlo = it.lo;
-  it.tiles = (int)((it.hi - it.lo + kCgTile<P> - 1) / kCgTile<P>);
+  it.tiles = (int)((planes * p.N + TR - 1) / TR);
   return it;
 }
 
-template <int P>
-__device__ __forceinline__ void cg_issue(const PlaneRunParams& p, Cursor& c, bool rev, float* buf,
+// Tile `c.tile` of the cursor's item (in scan order): its whole granules.
+__device__ __forceinline__ void cg_issue(const PlaneRunParams& p, int TR, Cursor& c, bool rev, float* buf,
                                          unsigned long long* bar) {
   if (c.item >= p.items) return;
-  const int64_t ts = c.it.lo + (int64_t)(rev ? c.it.tiles - 1 - c.tile : c.tile) * kCgTile<P>;
-  const int64_t te = min(ts + kCgTile<P>, c.it.hi);
-  const unsigned bytes = (unsigned)(te - ts) * 4u;  // whole rows: a multiple of 16
+  const int64_t tr0 = (int64_t)(rev ? c.it.tiles - 1 - c.tile : c.tile) * TR;
+  const int64_t f0 = c.it.lo + tr0 * p.P;
+  const int64_t f1 = min(f0 + (int64_t)TR * p.P, c.it.hi);
+  const int64_t a0 = f0 & ~(int64_t)3, a1 = (f1 + 3) & ~(int64_t)3;
+  const unsigned bytes = (unsigned)(a1 - a0) * 4u;
   mbar_arrive_expect_tx(bar, bytes);
-  bulk_load(buf, p.x + ts, bytes, bar);
+  bulk_load(buf, p.x + a0, bytes, bar);
   if (++c.tile == c.it.tiles) {
     c.item += gridDim.x;
     c.tile = 0;
-    if (c.item < p.items) c.it = cg_item<P>(p, c.item);
+    if (c.item < p.items) c.it = cg_item(p, TR, c.item);
   }
 }
 
-template <int P, bool REV, bool EXCL>
+// GMAX: the most column groups the instance takes (8 or 32; shared memory
+// for the warp totals).  GFIX: the group count when fixed at compile time
+// (16 and 32 columns), else 0 (taken from p.P).
+template <int V, int GMAX, int GFIX, bool REV, bool EXCL>
 __global__ void __launch_bounds__(kT, 4) k_planes_cg(PlaneRunParams p) {
   pdl_begin();
-  constexpr int G = kCgGroups<P>;
-  constexpr int S = kCgRows;
-  constexpr int RG = kT / G;  // row groups per tile
-  __shared__ __align__(128) float s_buf[kStages][kCgTile<P>];
+  constexpr int S = kCgS<V>;
+  __shared__ __align__(128) float s_buf[kStages][kCgBuf<V>];
   __shared__ __align__(8) unsigned long long s_bar[kStages];
-  __shared__ float4 s_wagg[2][kNW][G];  // each warp's last-segment totals, by column group
-  __shared__ int s_wflag[2][kNW];
-  __shared__ float4 s_carry[2][G];
+  __shared__ float s_wagg[2][kNW][GMAX * V];  // each warp's last-segment totals, by column group
+  __shared__ unsigned char s_wflag[2][kNW][GMAX];  // a head in the warp's lanes of the group
+  __shared__ float s_carry[2][GMAX * V];
   __shared__ Cursor s_pc;
   const int t = threadIdx.x;
   const int lane = t & 31;
   const int w = t >> 5;
+  const int P = GFIX ? GFIX * V : p.P;
+  const int G = GFIX ? GFIX : P / V;
+  const int RG = kT / G;  // row groups per tile
+  const int TR = RG * S;  // rows per tile
   const int g = t % G;
-  const int m = REV ? RG - 1 - t / G : t / G;  // my row group, in memory order
+  const bool active = (GFIX && kT % GFIX == 0) || t / G < RG;  // row groups fill the block with 4 or 8 groups
+  const int m = REV ? RG - 1 - t / G : t / G;  // my row group, in memory order (idle: out of range)
   const int row0 = m * S;                       // its first row in a tile
-  const unsigned gmask = (G == 4 ? 0x11111111u : 0x01010101u) << g;  // lanes of my column group
+  const unsigned gmask = __match_any_sync(kFullMask, g);  // lanes of my column group
+  const int glead = __ffs(gmask) - 1;                     // the first of them
   const int Ni = (int)min(p.N, (int64_t)INT32_MAX);
 
   int outstanding = 0;
@@ -622,14 +655,14 @@ __global__ void __launch_bounds__(kT, 4) k_planes_cg(PlaneRunParams p) {
     Cursor pc;
     pc.item = blockIdx.x;
     pc.tile = 0;
-    if (pc.item < p.items) pc.it = cg_item<P>(p, pc.item);
+    if (pc.item < p.items) pc.it = cg_item(p, TR, pc.item);
 #pragma unroll
     for (int s = 0; s < kStages; ++s) mbar_init(&s_bar[s], 1);
     fence_mbar_init();
 #pragma unroll
     for (int s = 0; s < kStages; ++s)
       if (pc.item < p.items) {
-        cg_issue<P>(p, pc, REV, s_buf[s], &s_bar[s]);
+        cg_issue(p, TR, pc, REV, s_buf[s], &s_bar[s]);
         ++outstanding;
       }
     s_pc = pc;
@@ -642,77 +675,95 @@ __global__ void __launch_bounds__(kT, 4) k_planes_cg(PlaneRunParams p) {
   bool started = false;
   bool fail = false;
   for (int64_t item = blockIdx.x; item < p.items && !fail; item += gridDim.x) {
-    const PlaneItem it = cg_item<P>(p, item);
-    const int64_t item_rows = (it.hi - it.lo) / P;
+    const PlaneItem it = cg_item(p, TR, item);
+    const int64_t item_rows = (int64_t)it.planes * p.N;
     for (int j = 0; j < it.tiles; ++j) {
       const bool landed = mbar_wait_copy(&s_bar[stage], phase);
-      const int jt = REV ? it.tiles - 1 - j : j;        // memory tile index
-      const int64_t tr0 = (int64_t)jt * kCgTileRows<P>;  // its first row (item-relative)
-      const int64_t ts = it.lo + tr0 * P;
+      const int jt = REV ? it.tiles - 1 - j : j;  // memory tile index
+      const int64_t tr0 = (int64_t)jt * TR;       // its first row (item-relative)
+      const int64_t f0 = it.lo + tr0 * P;         // its first float
+      const int delta = V == 4 ? 0 : (int)(f0 & 3);  // where it lies in the copied granules
+      const int rows = (int)min((int64_t)TR, item_rows - tr0);
       float* buf = s_buf[stage];
       // The head: forward, the first plane start at or after my first row
       // (rows q*N, q = 0 .. planes; the one at the item's end isolates rows
       // past it); reverse, the last row of a plane (q*N - 1, q >= 1).
       const int rr = (int)min(tr0 + row0, (int64_t)INT32_MAX / 2);  // my first row, item-relative
       int hp = S;
-      if (p.k == 1) {
-        if constexpr (!REV) {
-          const int d = rr == 0 ? 0 : Ni - rr;
-          if (d >= 0 && d < S) hp = d;
+      if (active) {
+        if (p.k == 1) {
+          if constexpr (!REV) {
+            const int d = rr == 0 ? 0 : Ni - rr;
+            if (d >= 0 && d < S) hp = d;
+          } else {
+            const int e = rr + S - Ni;
+            if (e >= 0 && e < S) hp = e;
+          }
         } else {
-          const int e = rr + S - Ni;
-          if (e >= 0 && e < S) hp = e;
-        }
-      } else {
-        if constexpr (!REV) {
-          const int q = rr == 0 ? 0 : (int)(((unsigned long long)(rr - 1) * p.magic) >> 32) + 1;
-          const int d = q * Ni - rr;
-          if (d < S) hp = d;
-        } else {
-          const int gq = rr + S;
-          const int q = (int)(((unsigned long long)gq * p.magic) >> 32);
-          const int e = gq - q * Ni;
-          if (q >= 1 && e < S) hp = e;
+          if constexpr (!REV) {
+            const int q = rr == 0 ? 0 : (int)(((unsigned long long)(rr - 1) * p.magic) >> 32) + 1;
+            const int d = q * Ni - rr;
+            if (d < S) hp = d;
+          } else {
+            const int gq = rr + S;
+            const int q = (int)(((unsigned long long)gq * p.magic) >> 32);
+            const int e = gq - q * Ni;
+            if (q >= 1 && e < S) hp = e;
+          }
         }
       }
       // 1. My rows in scan order, scanned per component; the head row
-      // restarts all four.
-      float4 v[S];
+      // restarts all V.
+      const float* src = buf + delta + row0 * P + V * g;
+      float v[S][V];
 #pragma unroll
       for (int e = 0; e < S; ++e) {
-        const int row = row0 + (REV ? S - 1 - e : e);
-        v[e] = *reinterpret_cast<const float4*>(buf + row * P + 4 * g);
+        if (active) {
+          cg_ld<V>(src + (REV ? S - 1 - e : e) * P, v[e]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < V; ++c) v[e][c] = 0.f;
+        }
       }
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float acc[V];
+#pragma unroll
+      for (int c = 0; c < V; ++c) acc[c] = 0.f;
 #pragma unroll
       for (int e = 0; e < S; ++e) {
         const bool restart = e == hp;
-        const float4 before = restart ? make_float4(0.f, 0.f, 0.f, 0.f) : acc;
-        acc = make_float4(before.x + v[e].x, before.y + v[e].y, before.z + v[e].z, before.w + v[e].w);
-        v[e] = EXCL ? before : acc;
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          const float before = restart ? 0.f : acc[c];
+          acc[c] = before + v[e][c];
+          v[e][c] = EXCL ? before : acc[c];
+        }
       }
       // 2. Segmented scan over the row groups of my column group in this
       // warp (lanes G apart): lane l adds lanes at or after its last lane
       // with a head.
       const unsigned hmask = __ballot_sync(kFullMask, hp < S) & gmask;
       const unsigned upto = hmask & (kFullMask >> (31 - lane));
-      const int hh = upto ? 31 - __clz((int)upto) : g;
-      float4 inc = acc;
+      const int hh = upto ? 31 - __clz((int)upto) : glead;
+      float inc[V];
 #pragma unroll
+      for (int c = 0; c < V; ++c) inc[c] = acc[c];
       for (int o = G; o < 32; o <<= 1) {
-        const float ux = __shfl_up_sync(kFullMask, inc.x, o), uy = __shfl_up_sync(kFullMask, inc.y, o);
-        const float uz = __shfl_up_sync(kFullMask, inc.z, o), uw = __shfl_up_sync(kFullMask, inc.w, o);
-        if (lane - o >= hh) inc = make_float4(ux + inc.x, uy + inc.y, uz + inc.z, uw + inc.w);
+        float u[V];
+#pragma unroll
+        for (int c = 0; c < V; ++c) u[c] = __shfl_up_sync(kFullMask, inc[c], o);
+        if (lane - o >= hh) {
+#pragma unroll
+          for (int c = 0; c < V; ++c) inc[c] = u[c] + inc[c];
+        }
       }
-      float4 ex;
-      ex.x = __shfl_up_sync(kFullMask, inc.x, G);
-      ex.y = __shfl_up_sync(kFullMask, inc.y, G);
-      ex.z = __shfl_up_sync(kFullMask, inc.z, G);
-      ex.w = __shfl_up_sync(kFullMask, inc.w, G);
+      float ex[V];
+#pragma unroll
+      for (int c = 0; c < V; ++c) ex[c] = __shfl_up_sync(kFullMask, inc[c], G);
       const bool head_before = (hmask & ((1u << lane) - 1u)) != 0;
-      if (lane >= 32 - G) {  // the warp's last row group holds its totals
-        s_wagg[par][w][g] = inc;
-        if (g == 0) s_wflag[par][w] = hmask != 0;  // a head in any row group of the warp
+      if (lane >= 32 - G) {  // the last lane of my group in this warp holds its totals
+#pragma unroll
+        for (int c = 0; c < V; ++c) s_wagg[par][w][g * V + c] = inc[c];
+        s_wflag[par][w][g] = hmask != 0;
       }
       if (__syncthreads_or(!landed)) {
         fail = true;
@@ -724,40 +775,54 @@ __global__ void __launch_bounds__(kT, 4) k_planes_cg(PlaneRunParams p) {
           const int rs = (stage + kStages - 1) % kStages;
           bulk_store_wait_read();
           Cursor pc = s_pc;
-          cg_issue<P>(p, pc, REV, s_buf[rs], &s_bar[rs]);
+          cg_issue(p, TR, pc, REV, s_buf[rs], &s_bar[rs]);
           s_pc = pc;
           ++outstanding;
         }
       }
       // 3. Carry into my warp for my column group, then into my row group.
-      float4 cw = j == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : s_carry[par][g];
+      float cw[V];
+#pragma unroll
+      for (int c = 0; c < V; ++c) cw[c] = j == 0 ? 0.f : s_carry[par][g * V + c];
 #pragma unroll
       for (int q = 0; q < kNW - 1; ++q) {
         if (q < w) {
-          const float4 a = s_wagg[par][q][g];
-          cw = s_wflag[par][q] ? a : make_float4(cw.x + a.x, cw.y + a.y, cw.z + a.z, cw.w + a.w);
+          const bool restart = s_wflag[par][q][g] != 0;
+#pragma unroll
+          for (int c = 0; c < V; ++c) {
+            const float a = s_wagg[par][q][g * V + c];
+            cw[c] = restart ? a : cw[c] + a;
+          }
         }
       }
       if (w == kNW - 1 && lane >= 32 - G) {
-        const float4 a = s_wagg[par][kNW - 1][g];
-        s_carry[par ^ 1][g] = s_wflag[par][kNW - 1] ? a : make_float4(cw.x + a.x, cw.y + a.y, cw.z + a.z, cw.w + a.w);
-      }
-      const float4 cl = lane < G ? cw
-                                 : (head_before ? ex : make_float4(cw.x + ex.x, cw.y + ex.y, cw.z + ex.z, cw.w + ex.w));
-      // 4. Rows before the head take the carry; back in place, then the
-      // item's rows of the tile leave by one bulk store.
+        const bool restart = s_wflag[par][kNW - 1][g] != 0;
 #pragma unroll
-      for (int e = 0; e < S; ++e) {
-        if (e < hp) v[e] = make_float4(cl.x + v[e].x, cl.y + v[e].y, cl.z + v[e].z, cl.w + v[e].w);
-        const int row = row0 + (REV ? S - 1 - e : e);
-        *reinterpret_cast<float4*>(buf + row * P + 4 * g) = v[e];
+        for (int c = 0; c < V; ++c) {
+          const float a = s_wagg[par][kNW - 1][g * V + c];
+          s_carry[par ^ 1][g * V + c] = restart ? a : cw[c] + a;
+        }
+      }
+      float cl[V];
+#pragma unroll
+      for (int c = 0; c < V; ++c) cl[c] = lane < G ? cw[c] : (head_before ? ex[c] : cw[c] + ex[c]);
+      // 4. Rows before the head take the carry; back in place, then the
+      // tile's rows leave: whole granules by one bulk store, the partial
+      // ones at its ends by plain stores.
+      if (active) {
+        float* dst = buf + delta + row0 * P + V * g;
+#pragma unroll
+        for (int e = 0; e < S; ++e) {
+          if (e < hp) {
+#pragma unroll
+            for (int c = 0; c < V; ++c) v[e][c] = cl[c] + v[e][c];
+          }
+          cg_st<V>(dst + (REV ? S - 1 - e : e) * P, v[e]);
+        }
       }
       fence_proxy_async_smem();
       __syncthreads();
-      if (t == 0) {
-        const int64_t rows = min((int64_t)kCgTileRows<P>, item_rows - tr0);
-        bulk_store(p.y + ts, buf, (unsigned)(rows * P) * 4u);
-      }
+      store_tile_out(buf, p.y + (f0 - delta), delta, delta + rows * P);
       fence_proxy_async_smem();
       started = true;
       par ^= 1;
@@ -781,6 +846,7 @@ __global__ void __launch_bounds__(kT, 4) k_planes_cg(PlaneRunParams p) {
     bulk_store_wait_all();
   }
 }
+
 
 // ---------------------------------------------------------------------------
 // Few long planes: one tile per block, the carry by look-back.

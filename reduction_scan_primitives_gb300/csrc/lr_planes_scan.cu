@@ -29,25 +29,27 @@ int occupancy_scan_p() {
                    occupancy_of(k_planes<P, true, true, true, OpSum, true>)});
 }
 
-// Column-group runs (16 and 32 columns).
-template <int P>
-cudaError_t launch_cg_p(const PlaneRunParams& p, dim3 g, cudaStream_t s) {
+// Column groups (any other column count up to 128).
+template <int V, int GMAX, int GFIX>
+cudaError_t launch_cg_v(const PlaneRunParams& p, dim3 g, cudaStream_t s) {
   const bool rev = (p.flags & kScanMirror) == 0;
   const bool excl = (p.flags & kScanExclusive) != 0;
   if (rev) {
-    if (excl) launch_pdl(k_planes_cg<P, true, true>, g, kT, 0, s, p);
-    else launch_pdl(k_planes_cg<P, true, false>, g, kT, 0, s, p);
+    if (excl) launch_pdl(k_planes_cg<V, GMAX, GFIX, true, true>, g, kT, 0, s, p);
+    else launch_pdl(k_planes_cg<V, GMAX, GFIX, true, false>, g, kT, 0, s, p);
   } else {
-    if (excl) launch_pdl(k_planes_cg<P, false, true>, g, kT, 0, s, p);
-    else launch_pdl(k_planes_cg<P, false, false>, g, kT, 0, s, p);
+    if (excl) launch_pdl(k_planes_cg<V, GMAX, GFIX, false, true>, g, kT, 0, s, p);
+    else launch_pdl(k_planes_cg<V, GMAX, GFIX, false, false>, g, kT, 0, s, p);
   }
   return cudaGetLastError();
 }
 
-template <int P>
-int occupancy_cg_p() {
-  return std::min({occupancy_of(k_planes_cg<P, false, false>), occupancy_of(k_planes_cg<P, false, true>),
-                   occupancy_of(k_planes_cg<P, true, false>), occupancy_of(k_planes_cg<P, true, true>)});
+template <int V, int GMAX, int GFIX>
+int occupancy_cg_v() {
+  return std::min({occupancy_of(k_planes_cg<V, GMAX, GFIX, false, false>),
+                   occupancy_of(k_planes_cg<V, GMAX, GFIX, false, true>),
+                   occupancy_of(k_planes_cg<V, GMAX, GFIX, true, false>),
+                   occupancy_of(k_planes_cg<V, GMAX, GFIX, true, true>)});
 }
 
 }  // namespace
@@ -66,8 +68,6 @@ cudaError_t launch_planes_scan(int P, const PlaneRunParams& p, int64_t grid, cud
     case 10: return launch_scan_p<10>(p, g, s);
     case 12: return launch_scan_p<12>(p, g, s);
     case 14: return launch_scan_p<14>(p, g, s);
-    case 16: return launch_cg_p<16>(p, g, s);
-    case 32: return launch_cg_p<32>(p, g, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -86,8 +86,42 @@ int occupancy_planes(int P, bool scan) {
     case 10: return occupancy_scan_p<10>();
     case 12: return occupancy_scan_p<12>();
     case 14: return occupancy_scan_p<14>();
-    case 16: return occupancy_cg_p<16>();
-    case 32: return occupancy_cg_p<32>();
+    default: return 0;
+  }
+}
+
+// The column-group instance for P columns: 0 .. 3 for (V, GMAX) = (1, 32),
+// (2, 32), (4, 8), (4, 32) with the group count taken at run time, 4 and 5
+// for 16 and 32 columns (4 and 8 float4 groups fixed at compile time); -1
+// when P does not fit.
+int cg_instance(int P) {
+  if (!planes_cg_fits(P)) return -1;
+  if (P == 16 || P == 32) return P == 16 ? 4 : 5;
+  const int V = planes_cg_vec(P);
+  return V == 1 ? 0 : V == 2 ? 1 : planes_cg_groups(P) <= 8 ? 2 : 3;
+}
+
+cudaError_t launch_planes_cg(const PlaneRunParams& p, int64_t grid, cudaStream_t s) {
+  const dim3 g((unsigned)grid);
+  switch (cg_instance(p.P)) {
+    case 0: return launch_cg_v<1, 32, 0>(p, g, s);
+    case 1: return launch_cg_v<2, 32, 0>(p, g, s);
+    case 2: return launch_cg_v<4, 8, 0>(p, g, s);
+    case 3: return launch_cg_v<4, 32, 0>(p, g, s);
+    case 4: return launch_cg_v<4, 8, 4>(p, g, s);
+    case 5: return launch_cg_v<4, 8, 8>(p, g, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int occupancy_planes_cg(int instance) {
+  switch (instance) {
+    case 0: return occupancy_cg_v<1, 32, 0>();
+    case 1: return occupancy_cg_v<2, 32, 0>();
+    case 2: return occupancy_cg_v<4, 8, 0>();
+    case 3: return occupancy_cg_v<4, 32, 0>();
+    case 4: return occupancy_cg_v<4, 8, 4>();
+    case 5: return occupancy_cg_v<4, 8, 8>();
     default: return 0;
   }
 }

@@ -205,13 +205,25 @@ def test_plane_run_division_is_exact():
 
 
 def test_column_group_row_division_is_exact():
-    """The 16- and 32-column scans find plane boundaries among the rows of a
-    tile holding k >= 2 planes of N rows (10 <= N <= 144: half a tile of 288
-    or 144 rows) by (r * ceil(2^32 / N)) >> 32 for r up to a tile and a run
-    (9 rows) past it; that is r // N there."""
+    """The column-group scans find plane boundaries among the rows of a tile
+    holding k >= 2 planes of N rows (S < N <= half a tile of TR rows; S = 9,
+    17 or 33 rows a run for float4, float2 or single-float column groups, TR
+    = (128 // G) * S for G groups) by (r * ceil(2^32 / N)) >> 32 for r up to
+    a tile and a run past it; that is r // N there, for every column count
+    of 3 to 128 the kernels take."""
     import numpy as np
-    for rows in (288, 144):
-        for d in range(10, rows // 2 + 1):
-            r = np.arange(0, rows + 9 + 1, dtype=np.uint64)
+    seen = set()
+    for P in range(3, 129):
+        V = 4 if P % 4 == 0 else 2 if P % 2 == 0 else 1
+        G = P // V
+        if G > 32:
+            continue
+        S = {4: 9, 2: 17, 1: 33}[V]
+        rows = (128 // G) * S
+        if (rows, S) in seen:
+            continue
+        seen.add((rows, S))
+        r = np.arange(0, rows + S + 1, dtype=np.uint64)
+        for d in range(S + 1, rows // 2 + 1):
             magic = np.uint64(((1 << 32) + d - 1) // d)
-            assert np.array_equal((r * magic) >> np.uint64(32), r // np.uint64(d)), (rows, d)
+            assert np.array_equal((r * magic) >> np.uint64(32), r // np.uint64(d)), (P, d)

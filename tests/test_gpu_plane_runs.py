@@ -2,7 +2,8 @@
 [outer, N, P] scanned or reduced along N by k_planes, which reads each tile of
 the flat array into shared memory and scans runs of whole rows per thread, the
 column classes fixed and the segments restarting at plane boundaries; scans of
-16 and 32 columns by k_planes_cg, a float4 column of 9 rows per thread.
+other column counts up to 128 by k_planes_cg, one column group (a float4,
+float2 or float) of a run of 9, 17 or 33 rows per thread.
 Against the oracle element by element: planes no longer than a thread's run
 (several boundaries in a run), short planes many to a tile (plane
 boundaries at and inside runs), planes of about one tile, planes over many
@@ -46,7 +47,16 @@ SHAPES = [(100_000, 100, 3), (4096, 4096, 2), (20_001, 19, 2), (30_001, 13, 4), 
           # tile, planes over 2 to 70 tiles
           (20_000, 100, 16), (30_001, 13, 16), (9999, 10, 32), (50_001, 11, 32), (10_000, 144, 16),
           (40_000, 72, 32), (5000, 145, 16), (2000, 289, 16), (300, 5001, 32), (64, 10_000, 16),
-          (3, 20_000, 16), (7, 12, 16)]
+          (3, 20_000, 16), (7, 12, 16),
+          # column groups of other widths: single floats (odd P, runs of 33
+          # rows), float2 (P = 2 mod 4, 17 rows) and float4 (9 rows); group
+          # counts that do not divide 32 (idle threads past the row groups),
+          # 32 groups, tiles starting inside a 16-byte granule, planes of one
+          # run and a row, planes over many tiles
+          (20_000, 34, 11), (3000, 101, 13), (700, 1001, 15), (5000, 77, 17), (400, 2000, 31),
+          (20_000, 18, 18), (4000, 100, 22), (1000, 999, 26), (300, 3001, 30), (2000, 50, 34), (500, 600, 62),
+          (20_000, 10, 20), (5000, 100, 24), (1000, 1000, 28), (3000, 99, 36), (1000, 500, 40), (800, 100, 48),
+          (500, 300, 64), (100, 2000, 100), (64, 3000, 128), (7, 12, 44)]
 
 
 def scan(x, reverse, exclusive, forced=True, out=None):
@@ -70,7 +80,7 @@ def test_scan_against_oracle(shape, reverse, exclusive):
 
 @pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("shape", [(40_000, 25, 3), (3000, 2401, 2), (1000, 2500, 4), (200_000, 7, 3), (20_000, 50, 16),
-                                   (3000, 1001, 32)])
+                                   (3000, 1001, 32), (3000, 70, 13), (1000, 300, 22), (500, 200, 40), (50, 700, 128)])
 def test_scan_integers_exact_and_bitwise(shape, reverse, exclusive):
     """{0..3} inputs: every prefix is an integer below 2^24, so exact."""
     x = inputs.make(shape, "int:0:3", 32)
@@ -140,7 +150,7 @@ def test_neighbours_untouched(reverse):
     whose boundaries fall inside float4 granules (L = 6002 and L = 38), and
     column-group tiles whose last item ends short of a tile (16 and 32
     columns)."""
-    for shape in [(7, 3001, 2), (5001, 19, 2), (1001, 13, 16), (3, 1001, 32)]:
+    for shape in [(7, 3001, 2), (5001, 19, 2), (1001, 13, 16), (3, 1001, 32), (1001, 35, 11), (13, 37, 18)]:
         x = inputs.make(shape, "uniform01", 36)
         n = x.numel()
         buf = torch.full((n + 12,), 5.0, device="cuda")
@@ -153,7 +163,9 @@ def test_neighbours_untouched(reverse):
 
 @pytest.mark.parametrize("shape,sums", [((100_000, 100, 3), True), ((4096, 4096, 2), True), ((50_000, 40, 4), True),
                                         ((500_000, 7, 3), True), ((100_000, 100, 8), False),
-                                        ((100_000, 100, 16), False), ((50_000, 100, 32), False)])
+                                        ((100_000, 100, 16), False), ((50_000, 100, 32), False),
+                                        ((20_000, 100, 13), False), ((20_000, 100, 22), False),
+                                        ((10_000, 100, 40), False)])
 def test_automatic_choice_takes_plane_runs(shape, sums):
     """Aligned planes whose items fill the GPU take this form without options:
     the automatic result is the forced one bit for bit (sums of 8 columns keep
