@@ -601,11 +601,13 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, b
 // / 0.41, [3555, 1000, 18] 0.89 / 0.43, [26666, 100, 24] 0.94 / 0.52,
 // [2064, 1000, 31] 0.87 / 0.63, [1333, 1000, 48] 0.88 / 0.73, [10000, 100,
 // 64] 0.87 / 0.82, [6400, 100, 100] 0.84 / 0.70, [640, 1000, 100] 0.81 /
-// 0.69; planes of 64 columns and 512 rows or more stay with the short-row
-// planes ([1000, 1000, 64] 0.82 / 0.89).
+// 0.69, [5000, 100, 128] 0.90 / 0.82.  Planes of 64 or 128 columns (whole
+// 32-column tiles for the other forms) and 256 rows or more stay with
+// those ([3906, 256, 64] 0.88 / 0.91, [1000, 1000, 64] 0.82 / 0.89,
+// [1953, 256, 128] 0.85 / 0.97).
 bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t N, int64_t inner, bool scan) {
   if (inner == 8 && (!scan || pl.k < 2)) return false;
-  if (pl.cg && inner == 64 && N >= 512) return false;
+  if (pl.cg && inner % 32 == 0 && inner >= 64 && N >= 256) return false;
   return pl.items >= st->sm_count;
 }
 // Fewer items than SMs: the look-back form, whose blocks take single tiles,
