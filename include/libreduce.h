@@ -334,9 +334,12 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 short row (the automatic choice for planes of at
  *                                 most 768 floats); 9 planes of 2 to 8 columns
  *                                 read flat as segmented class runs (x 16-byte
- *                                 aligned, N >= 2; the
- *                                 automatic choice from one item of planes per SM
- *                                 on)
+ *                                 aligned, N >= 2), and of 9 to 128 columns as
+ *                                 column groups (N above the run of 9, 17 or 33
+ *                                 rows); the automatic choice from one item of
+ *                                 planes per SM on (column groups below 64
+ *                                 columns, not on short planes of whole float4
+ *                                 rows that a warp per plane takes)
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
  *                                 2 float4 x 4 (float4 needs x and y at the same
  *                                 offset mod 16 bytes; any N)

@@ -64,6 +64,7 @@ struct DeviceState {
   int occ_planes[kPlanesMaxScanP - 1][2] = {};  // narrow planes read flat: [P - 2][scan]
   int occ_planes_lb[kPlanesMaxP - 1] = {};  // the same, look-back form: [P - 2]
   int occ_planes_cg[kPlanesCgInstances] = {};  // scans as column groups, by instance
+  int occ_planes_cg_reduce[kPlanesCgInstances] = {};  // reductions as column groups
 };
 
 // Index of a period (1, 2, 4) in the per-period tables.
@@ -144,7 +145,10 @@ int device_state(DeviceState** out, int* dev_out) {
       st.occ_planes[pi][0] = std::max(1, occupancy_planes(P, false));
       st.occ_planes_lb[pi] = std::max(1, occupancy_planes_lookback(P));
     }
-    for (int ci = 0; ci < kPlanesCgInstances; ++ci) st.occ_planes_cg[ci] = std::max(1, occupancy_planes_cg(ci));
+    for (int ci = 0; ci < kPlanesCgInstances; ++ci) {
+      st.occ_planes_cg[ci] = std::max(1, occupancy_planes_cg(ci));
+      st.occ_planes_cg_reduce[ci] = std::max(1, occupancy_planes_cg_reduce(ci));
+    }
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
   }
@@ -558,10 +562,17 @@ struct PlaneRunPlan {
 bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, bool scan) {
   int64_t L = 0;
   if (inner < 2 || outer <= 0 || N < 2 || mul_overflows(N, inner, &L)) return false;
-  if (scan && inner <= kPlanesCgMaxP && planes_cg((int)inner)) {
-    // Column groups: tiles of whole rows, boundaries in rows.
+  if (inner <= kPlanesCgMaxP && (scan ? planes_cg((int)inner) : inner > kPlanesMaxP && planes_cg_fits((int)inner))) {
+    // Column groups: tiles of whole rows, boundaries in rows.  Items of
+    // several planes may span up to 8 tiles (while that leaves 2048 items
+    // or more), so that only an item's last tile runs part full: short
+    // planes one to a tile would leave up to half of it idle.
     if (N <= planes_cg_run_rows((int)inner)) return false;
-    const int64_t k = planes_cg_tile_rows((int)inner) / N;
+    const int64_t TR = planes_cg_tile_rows((int)inner);
+    int64_t rows = 0;
+    const int64_t per =
+        mul_overflows(outer, N, &rows) ? 1 : std::max<int64_t>(1, std::min<int64_t>(8, ceil_div(rows, TR) / 2048));
+    const int64_t k = TR * per / N;
     pl->k = k >= 2 ? k : 1;
     pl->items = ceil_div(outer, pl->k);
     pl->magic = pl->k >= 2 ? ((1ull << 32) + (unsigned long long)N - 1) / (unsigned long long)N : 0;
@@ -597,17 +608,26 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, b
 // against 0.62; sums [500000, 7, 3] 0.74 against 0.39, [2e6, 8, 2] 0.81
 // against 0.63, [1e6, 3, 6] 0.52 against 0.41.  Scans as column groups
 // (11 to 128 columns, and 16 and 32) against the best other form: [58181,
-// 100, 11] 0.84 / 0.50, [4923, 1000, 13] 0.84 / 0.41, [40000, 100, 16] 0.87
-// / 0.41, [3555, 1000, 18] 0.89 / 0.43, [26666, 100, 24] 0.94 / 0.52,
-// [2064, 1000, 31] 0.87 / 0.63, [1333, 1000, 48] 0.88 / 0.73, [10000, 100,
-// 64] 0.87 / 0.82, [6400, 100, 100] 0.84 / 0.70, [640, 1000, 100] 0.81 /
-// 0.69, [5000, 100, 128] 0.90 / 0.82.  Planes of 64 or 128 columns (whole
+// 100, 11] 0.89 / 0.50, [4923, 1000, 13] 0.84 / 0.41, [40000, 100, 16] 0.92
+// / 0.41, [3555, 1000, 18] 0.89 / 0.43, [26666, 100, 24] 0.92 / 0.52,
+// [2064, 1000, 31] 0.87 / 0.63, [1333, 1000, 48] 0.87 / 0.73, [10000, 100,
+// 64] 0.88 / 0.82, [6400, 100, 100] 0.85 / 0.70, [640, 1000, 100] 0.81 /
+// 0.69, [5000, 100, 128] 0.89 / 0.82.  Planes of 64 or 128 columns (whole
 // 32-column tiles for the other forms) and 256 rows or more stay with
 // those ([3906, 256, 64] 0.88 / 0.91, [1000, 1000, 64] 0.82 / 0.89,
-// [1953, 256, 128] 0.85 / 0.97).
-bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t N, int64_t inner, bool scan) {
+// [1953, 256, 128] 0.85 / 0.97).  Reductions as column groups (9 to 63
+// columns): [7111, 1000, 9] 0.91 / 0.63, [5818, 1000, 11] 0.90 / 0.45,
+// [3764, 1000, 17] 0.91 / 0.74, [71111, 100, 9] 0.85 / 0.81, [37647, 100,
+// 17] 0.87 / 0.62; a warp per plane stays ahead on short planes of whole
+// float4 rows ([26666, 100, 24] 0.98 / 0.85, [20000, 100, 32] 1.01 /
+// 0.90), and the narrow and short-row forms from 64 columns on ([640,
+// 1000, 100] 0.93 / 0.74, [500, 1000, 128] 0.92 / 0.67).
+bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t outer, int64_t N, int64_t inner,
+                     bool scan) {
   if (inner == 8 && (!scan || pl.k < 2)) return false;
-  if (pl.cg && inner % 32 == 0 && inner >= 64 && N >= 256) return false;
+  if (pl.cg && scan && inner % 32 == 0 && inner >= 64 && N >= 256) return false;
+  if (pl.cg && !scan && (inner >= 64 || (inner % 4 == 0 && narrow_warp_reduce(st, outer, N, inner, 4))))
+    return false;
   return pl.items >= st->sm_count;
 }
 // Fewer items than SMs: the look-back form, whose blocks take single tiles,
@@ -627,10 +647,12 @@ int run_planes(const Provider& pv, const PlaneRunPlan& pl, const float* x, int64
   Scratch sc;
   const int rc = acquire(pv, need, &sc, s);
   if (rc) return rc;
-  const int occ = pl.cg ? st->occ_planes_cg[cg_instance((int)inner)] : st->occ_planes[inner - 2][scan ? 1 : 0];
+  const int ci = pl.cg ? cg_instance((int)inner) : 0;
+  const int occ = pl.cg ? (scan ? st->occ_planes_cg[ci] : st->occ_planes_cg_reduce[ci])
+                        : st->occ_planes[inner - 2][scan ? 1 : 0];
   const int64_t grid = std::max<int64_t>(1, std::min(pl.items, (int64_t)st->sm_count * occ));
   PlaneRunParams p{x, y, outer, N, pl.k, pl.items, pl.magic, flags, sc.header, pl.multi ? 1 : 0, (int)inner};
-  if (pl.cg) return launched(launch_planes_cg(p, grid, s));
+  if (pl.cg) return launched(scan ? launch_planes_cg(p, grid, s) : launch_planes_cg_reduce(op, p, grid, s));
   return launched(scan ? launch_planes_scan((int)inner, p, grid, s)
                        : launch_planes_reduce((int)inner, op, p, grid, s));
 }
@@ -681,7 +703,7 @@ int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, 
     PlaneRunPlan pl;
     if ((fv < 0 || fv == kColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
         (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && plane_run_plan(outer, reduce, inner, &pl, false) &&
-        (fv == kColsPlaneRuns || plane_runs_fill(st, pl, reduce, inner, false)))
+        (fv == kColsPlaneRuns || plane_runs_fill(st, pl, outer, reduce, inner, false)))
       return run_planes(pv, pl, x, outer, reduce, inner, out, epi, false, op, s);
     if (fv == kColsPlaneRuns) fv = -1;  // forced on a shape it does not take: the automatic choice
     if ((fv < 0 || fv == kColsShortPlanes) && g_opt_axis_split.load() <= 0) {
@@ -1215,7 +1237,7 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
     PlaneRunPlan pl;
     if ((fv < 0 || fv == kScanColsPlaneRuns) && g_opt_axis_split.load() <= 0 &&
         ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
-        plane_run_plan(outer, N, inner, &pl, true) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl, N, inner, true)))
+        plane_run_plan(outer, N, inner, &pl, true) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl, outer, N, inner, true)))
       return run_planes(pv, pl, x, outer, N, inner, y, (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0),
                         true, kOpSum, s);
     if ((fv < 0 || fv == kScanColsPlaneLookback) && g_opt_axis_split.load() <= 0 &&

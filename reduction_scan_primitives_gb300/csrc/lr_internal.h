@@ -437,6 +437,8 @@ constexpr int kPlanesCgInstances = 6;
 int cg_instance(int P);
 cudaError_t launch_planes_cg(const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes_cg(int instance);
+cudaError_t launch_planes_cg_reduce(int op, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
+int occupancy_planes_cg_reduce(int instance);
 int occupancy_planes_reduce(int P);
 cudaError_t launch_planes_lookback(int P, const PlaneLbParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes_lookback(int P);

@@ -848,6 +848,204 @@ __global__ void __launch_bounds__(kT, 4) k_planes_cg(PlaneRunParams p) {
 }
 
 
+// Reductions as column groups (9 .. 128 columns): the same tiles, groups and
+// runs as the scans, walked forward.  A thread keeps the combination of its
+// rows before its head (pre) and from it on; the segmented lane scan and
+// the warp fold carry the runs' last segments as for a scan.  The plane that
+// ends in a thread's run (at most one: N > S) gets that thread's carry
+// combined with its pre, V columns written by the thread.  A tile's rows go
+// to registers before the tile's one barrier, after which its buffer is
+// refilled at once; the warp totals alternate by tile parity.
+// ---------------------------------------------------------------------------
+template <int V, int GMAX, int GFIX, typename Op>
+__global__ void __launch_bounds__(kT, 4) k_planes_cg_reduce(PlaneRunParams p) {
+  pdl_begin();
+  constexpr int S = kCgS<V>;
+  __shared__ __align__(128) float s_buf[kStages][kCgBuf<V>];
+  __shared__ __align__(8) unsigned long long s_bar[kStages];
+  __shared__ float s_wagg[2][kNW][GMAX * V];
+  __shared__ unsigned char s_wflag[2][kNW][GMAX];
+  __shared__ float s_carry[2][GMAX * V];
+  __shared__ Cursor s_pc;
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int w = t >> 5;
+  const int P = GFIX ? GFIX * V : p.P;
+  const int G = GFIX ? GFIX : P / V;
+  const int RG = kT / G;
+  const int TR = RG * S;
+  const int g = t % G;
+  const bool active = (GFIX && kT % GFIX == 0) || t / G < RG;
+  const int row0 = (t / G) * S;
+  const unsigned gmask = __match_any_sync(kFullMask, g);
+  const int glead = __ffs(gmask) - 1;
+  const int Ni = (int)min(p.N, (int64_t)INT32_MAX);
+
+  int outstanding = 0;
+  if (t == 0) {
+    Cursor pc;
+    pc.item = blockIdx.x;
+    pc.tile = 0;
+    if (pc.item < p.items) pc.it = cg_item(p, TR, pc.item);
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(&s_bar[s], 1);
+    fence_mbar_init();
+#pragma unroll
+    for (int s = 0; s < kStages; ++s)
+      if (pc.item < p.items) {
+        cg_issue(p, TR, pc, false, s_buf[s], &s_bar[s]);
+        ++outstanding;
+      }
+    s_pc = pc;
+  }
+  __syncthreads();
+
+  int stage = 0;
+  unsigned phase = 0;
+  int par = 0;
+  bool fail = false;
+  for (int64_t item = blockIdx.x; item < p.items && !fail; item += gridDim.x) {
+    const PlaneItem it = cg_item(p, TR, item);
+    for (int j = 0; j < it.tiles; ++j) {
+      const bool landed = mbar_wait_copy(&s_bar[stage], phase);
+      const int64_t tr0 = (int64_t)j * TR;
+      const int64_t f0 = it.lo + tr0 * P;
+      const int delta = V == 4 ? 0 : (int)(f0 & 3);
+      const float* buf = s_buf[stage];
+      // The head (the first plane start at or after my first row) and the
+      // plane that ends in my run: its last row is dd - 1 rows in, and it is
+      // plane qf - 1 of the item.
+      const int rr = (int)min(tr0 + row0, (int64_t)INT32_MAX / 2);
+      int hp = S, dd = 0, qf = 0;
+      if (active) {
+        if (p.k == 1) {
+          const int d = rr == 0 ? 0 : Ni - rr;
+          if (d >= 0 && d < S) hp = d;
+          if (rr > 0 && d >= 1 && d <= S) {
+            dd = d;
+            qf = 1;
+          }
+        } else {
+          const int q = rr == 0 ? 0 : (int)(((unsigned long long)(rr - 1) * p.magic) >> 32) + 1;
+          const int d = q * Ni - rr;
+          if (d < S) hp = d;
+          if (q >= 1 && d >= 1 && d <= S) {
+            dd = d;
+            qf = q;
+          }
+        }
+      }
+      // 1. My rows combined per component, before the head and from it on.
+      float pre[V], post[V];
+#pragma unroll
+      for (int c = 0; c < V; ++c) pre[c] = post[c] = Op::identity();
+      if (active) {
+        const float* src = buf + delta + row0 * P + V * g;
+#pragma unroll
+        for (int e = 0; e < S; ++e) {
+          float r[V];
+          cg_ld<V>(src + e * P, r);
+#pragma unroll
+          for (int c = 0; c < V; ++c) {
+            const float x = Op::prep(r[c]);
+            if (e < hp) pre[c] = Op::combine(pre[c], x);
+            else post[c] = Op::combine(post[c], x);
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the buffer is refilled after the barrier
+      // 2. Segmented scan of the runs' last segments over my column group's
+      // lanes in this warp.
+      const unsigned hmask = __ballot_sync(kFullMask, hp < S) & gmask;
+      const unsigned upto = hmask & (kFullMask >> (31 - lane));
+      const int hh = upto ? 31 - __clz((int)upto) : glead;
+      float inc[V];
+#pragma unroll
+      for (int c = 0; c < V; ++c) inc[c] = hp < S ? post[c] : pre[c];
+      for (int o = G; o < 32; o <<= 1) {
+        float u[V];
+#pragma unroll
+        for (int c = 0; c < V; ++c) u[c] = __shfl_up_sync(kFullMask, inc[c], o);
+        if (lane - o >= hh) {
+#pragma unroll
+          for (int c = 0; c < V; ++c) inc[c] = Op::combine(u[c], inc[c]);
+        }
+      }
+      float ex[V];
+#pragma unroll
+      for (int c = 0; c < V; ++c) ex[c] = __shfl_up_sync(kFullMask, inc[c], G);
+      const bool head_before = (hmask & ((1u << lane) - 1u)) != 0;
+      if (lane >= 32 - G) {
+#pragma unroll
+        for (int c = 0; c < V; ++c) s_wagg[par][w][g * V + c] = inc[c];
+        s_wflag[par][w][g] = hmask != 0;
+      }
+      // The one barrier: warp totals visible, every thread done with the
+      // tile's buffer, which is refilled now.
+      if (__syncthreads_or(!landed)) {
+        fail = true;
+        break;
+      }
+      if (t == 0) {
+        --outstanding;
+        if (s_pc.item < p.items) {
+          Cursor pc = s_pc;
+          cg_issue(p, TR, pc, false, s_buf[stage], &s_bar[stage]);
+          s_pc = pc;
+          ++outstanding;
+        }
+      }
+      // 3. Carry into my warp for my column group, then into my run.
+      float cw[V];
+#pragma unroll
+      for (int c = 0; c < V; ++c) cw[c] = j == 0 ? Op::identity() : s_carry[par][g * V + c];
+#pragma unroll
+      for (int q = 0; q < kNW - 1; ++q) {
+        if (q < w) {
+          const bool restart = s_wflag[par][q][g] != 0;
+#pragma unroll
+          for (int c = 0; c < V; ++c) {
+            const float a = s_wagg[par][q][g * V + c];
+            cw[c] = restart ? a : Op::combine(cw[c], a);
+          }
+        }
+      }
+      if (w == kNW - 1 && lane >= 32 - G) {
+        const bool restart = s_wflag[par][kNW - 1][g] != 0;
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          const float a = s_wagg[par][kNW - 1][g * V + c];
+          s_carry[par ^ 1][g * V + c] = restart ? a : Op::combine(cw[c], a);
+        }
+      }
+      // 4. The plane ending in my run: the carry and my rows before its end.
+      if (dd >= 1 && qf <= it.planes) {
+        float* out = p.y + (it.first + qf - 1) * P + V * g;
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          const float cl = lane < G ? cw[c] : (head_before ? ex[c] : Op::combine(cw[c], ex[c]));
+          st_plain(out + c, finish(Op::combine(cl, pre[c]), p.flags, p.N));
+        }
+      }
+      par ^= 1;
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (t == 0 && fail) {
+    atomicOr(p.err_word, 1u);
+    for (int k = 0; k < outstanding; ++k) {
+      mbar_wait_copy(&s_bar[stage], phase);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Few long planes: one tile per block, the carry by look-back.
 //

@@ -205,12 +205,12 @@ def test_plane_run_division_is_exact():
 
 
 def test_column_group_row_division_is_exact():
-    """The column-group scans find plane boundaries among the rows of a tile
-    holding k >= 2 planes of N rows (S < N <= half a tile of TR rows; S = 9,
-    17 or 33 rows a run for float4, float2 or single-float column groups, TR
-    = (128 // G) * S for G groups) by (r * ceil(2^32 / N)) >> 32 for r up to
-    a tile and a run past it; that is r // N there, for every column count
-    of 3 to 128 the kernels take."""
+    """The column-group scans and reductions find plane boundaries among the
+    rows of an item of k >= 2 planes of N rows spanning up to 8 tiles of TR
+    rows (S < N <= 4 TR; S = 9, 17 or 33 rows a run for float4, float2 or
+    single-float column groups, TR = (128 // G) * S for G groups) by
+    (r * ceil(2^32 / N)) >> 32 for r up to 8 tiles and a run past them; that
+    is r // N there, for every column count of 3 to 128 the kernels take."""
     import numpy as np
     seen = set()
     for P in range(3, 129):
@@ -223,7 +223,7 @@ def test_column_group_row_division_is_exact():
         if (rows, S) in seen:
             continue
         seen.add((rows, S))
-        r = np.arange(0, rows + S + 1, dtype=np.uint64)
-        for d in range(S + 1, rows // 2 + 1):
+        r = np.arange(0, 8 * rows + S + 1, dtype=np.uint64)
+        for d in range(S + 1, 4 * rows + 1):
             magic = np.uint64(((1 << 32) + d - 1) // d)
             assert np.array_equal((r * magic) >> np.uint64(32), r // np.uint64(d)), (P, d)

@@ -56,7 +56,9 @@ SHAPES = [(100_000, 100, 3), (4096, 4096, 2), (20_001, 19, 2), (30_001, 13, 4), 
           (20_000, 34, 11), (3000, 101, 13), (700, 1001, 15), (5000, 77, 17), (400, 2000, 31),
           (20_000, 18, 18), (4000, 100, 22), (1000, 999, 26), (300, 3001, 30), (2000, 50, 34), (500, 600, 62),
           (20_000, 10, 20), (5000, 100, 24), (1000, 1000, 28), (3000, 99, 36), (1000, 500, 40), (800, 100, 48),
-          (500, 300, 64), (100, 2000, 100), (64, 3000, 128), (7, 12, 44)]
+          (500, 300, 64), (100, 2000, 100), (64, 3000, 128), (7, 12, 44),
+          # enough planes for items of many planes over several tiles
+          (60_000, 40, 20), (80_000, 35, 11), (50_000, 20, 18)]
 
 
 def scan(x, reverse, exclusive, forced=True, out=None):
@@ -96,7 +98,15 @@ def test_scan_integers_exact_and_bitwise(shape, reverse, exclusive):
                                    (7, 13, 3), (4096, 2305, 2), (40_000, 9, 4), (30_000, 101, 5),
                                    (10_000, 7, 6), (500, 3001, 7), (100_000, 100, 8),
                                    (500_000, 7, 3), (300_001, 2, 2), (100_000, 3, 8), (40_000, 4, 7),
-                                   (33_333, 12, 3)])
+                                   (33_333, 12, 3),
+                                   # column groups, 9-128 columns: every group width,
+                                   # group counts that do not divide 32, planes of a
+                                   # run and a row, one plane over many tiles
+                                   (20_000, 34, 9), (5000, 101, 10), (3000, 999, 11), (10_000, 10, 12),
+                                   (2000, 77, 13), (700, 2001, 16), (4000, 35, 17), (3000, 100, 20),
+                                   (1000, 300, 26), (400, 2000, 31), (2000, 50, 32), (1000, 99, 40),
+                                   (300, 1000, 64), (100, 2000, 100), (64, 3000, 128), (7, 12, 44),
+                                   (60_000, 40, 20), (80_000, 35, 11), (50_000, 20, 18)])
 def test_reduce_against_oracle(shape, op):
     L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
     x = inputs.make(shape, "uniform_pm1", 33)
@@ -112,16 +122,18 @@ def test_reduce_against_oracle(shape, op):
 
 
 @pytest.mark.parametrize("op", ["max", "min", "sum"])
-def test_reduce_nan_stays_in_its_plane(op):
-    shape = (5000, 37, 3)  # L = 111: plane ends inside runs
+@pytest.mark.parametrize("shape", [(5000, 37, 3), (3000, 37, 13)])
+def test_reduce_nan_stays_in_its_plane(op, shape):
+    """L = 111 (3 columns): plane ends inside runs; 13 columns: column groups."""
     x = inputs.make(shape, "uniform_pm1", 34)
+    o, n, i = shape
     x[17, 5, 1] = float("nan")
-    x[4999, 36, 2] = float("nan")
+    x[o - 1, n - 1, 2] = float("nan")
     L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
     out = L.reduce_axis_op_f32(on_device(x), 1, op).cpu().numpy()
     L.check()
-    nan = np.isnan(out.reshape(shape[0], 3))
-    assert nan[17, 1] and nan[4999, 2] and nan.sum() == 2
+    nan = np.isnan(out.reshape(o, i))
+    assert nan[17, 1] and nan[o - 1, 2] and nan.sum() == 2
     if op == "sum":
         ref, scale = oracle.axis_sum(x.numpy(), *shape)
         keep = ~np.isnan(ref)
@@ -131,7 +143,8 @@ def test_reduce_nan_stays_in_its_plane(op):
         assert_op_close(out, ref, scale, op, shape[1], f"plane runs {op} with NaN")
 
 
-@pytest.mark.parametrize("shape", [(6000, 100, 3), (300, 3001, 4), (100_000, 5, 3)])
+@pytest.mark.parametrize("shape", [(6000, 100, 3), (300, 3001, 4), (100_000, 5, 3), (3000, 99, 11), (500, 1000, 20),
+                                   (2000, 40, 34)])
 def test_reduce_integers_exact_and_bitwise(shape):
     x = inputs.make(shape, "int:-8:8", 35)
     L.set_option(L.OPT_COLS_VARIANT, REDUCE_RUNS)
