@@ -334,12 +334,13 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 short row (the automatic choice for planes of at
  *                                 most 768 floats); 9 planes of 2 to 8 columns
  *                                 read flat as segmented class runs (x 16-byte
- *                                 aligned, N >= 2), and of 9 to 128 columns as
- *                                 column groups (N above the run of 9, 17 or 33
- *                                 rows); the automatic choice from one item of
- *                                 planes per SM on (column groups below 64
+ *                                 aligned, N >= 2), and of 3 or 5 to 128 columns
+ *                                 as column groups (N above the run of 9, 17 or
+ *                                 33 rows); the automatic choice from one item
+ *                                 of planes per SM on (column groups below 64
  *                                 columns, not on short planes of whole float4
- *                                 rows that a warp per plane takes)
+ *                                 rows of 16 columns and more, which a warp per
+ *                                 plane takes)
  *   LIBREDUCE_OPT_RSCAN_VARIANT   scan tile: 0 scalar x 4 sub-tiles, 1 float4 x 2,
  *                                 2 float4 x 4 (float4 needs x and y at the same
  *                                 offset mod 16 bytes; any N)
@@ -368,15 +369,15 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 least 4096 floats, after forms 8 and 9); 8 planes
  *                                 of 2 to 8, 9, 10, 12 or 14 columns read flat as
  *                                 segmented class runs (x and y 16-byte aligned,
- *                                 N >= 2), and of every other column count up
- *                                 to 128 as column groups (a float4, float2 or
- *                                 float of adjacent columns per thread over
- *                                 runs of 9, 17 or 33 rows; N above the run);
- *                                 the automatic choice from one item per SM on
- *                                 (column groups of 64 columns or more only
- *                                 below 512 rows), an
- *                                 item being one plane or as many short planes as
- *                                 fit a tile (2560 to 4608 floats); 9 the same tiles with a
+ *                                 N >= 2), and of 6 to 128 columns as column
+ *                                 groups where the planes are longer than their
+ *                                 runs (a float4, float2 or float of adjacent
+ *                                 columns per thread over runs of 9, 17 or 33
+ *                                 rows); the automatic choice from one item per
+ *                                 SM on (column groups of 64 or 128 columns only
+ *                                 below 256 rows), an item being one plane or
+ *                                 several short planes (up to 8 tiles of them
+ *                                 for column groups); 9 the same tiles with a
  *                                 plane's tiles spread over blocks and their carries
  *                                 from a look-back (the automatic choice for fewer
  *                                 items than SMs when planes hold two tiles or more)

@@ -559,15 +559,15 @@ struct PlaneRunPlan {
   bool multi = false;  // planes no longer than a thread's run: several boundaries in a run
   bool cg = false;     // column groups (k_planes_cg)
 };
-bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, bool scan) {
+bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, bool scan, bool allow_cg = true) {
   int64_t L = 0;
   if (inner < 2 || outer <= 0 || N < 2 || mul_overflows(N, inner, &L)) return false;
-  if (inner <= kPlanesCgMaxP && (scan ? planes_cg((int)inner) : inner > kPlanesMaxP && planes_cg_fits((int)inner))) {
+  if (allow_cg && inner <= kPlanesCgMaxP && (scan ? planes_cg_scan((int)inner) : planes_cg_reduce((int)inner)) &&
+      N > planes_cg_run_rows((int)inner)) {
     // Column groups: tiles of whole rows, boundaries in rows.  Items of
     // several planes may span up to 8 tiles (while that leaves 2048 items
     // or more), so that only an item's last tile runs part full: short
     // planes one to a tile would leave up to half of it idle.
-    if (N <= planes_cg_run_rows((int)inner)) return false;
     const int64_t TR = planes_cg_tile_rows((int)inner);
     int64_t rows = 0;
     const int64_t per =
@@ -624,9 +624,10 @@ bool plane_run_plan(int64_t outer, int64_t N, int64_t inner, PlaneRunPlan* pl, b
 // 1000, 100] 0.93 / 0.74, [500, 1000, 128] 0.92 / 0.67).
 bool plane_runs_fill(const DeviceState* st, const PlaneRunPlan& pl, int64_t outer, int64_t N, int64_t inner,
                      bool scan) {
-  if (inner == 8 && (!scan || pl.k < 2)) return false;
+  if (!pl.cg && inner == 8 && (!scan || pl.k < 2)) return false;
   if (pl.cg && scan && inner % 32 == 0 && inner >= 64 && N >= 256) return false;
-  if (pl.cg && !scan && (inner >= 64 || (inner % 4 == 0 && narrow_warp_reduce(st, outer, N, inner, 4))))
+  if (pl.cg && !scan &&
+      (inner >= 64 || (inner >= 16 && inner % 4 == 0 && narrow_warp_reduce(st, outer, N, inner, 4))))
     return false;
   return pl.items >= st->sm_count;
 }
@@ -1242,7 +1243,7 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
                         true, kOpSum, s);
     if ((fv < 0 || fv == kScanColsPlaneLookback) && g_opt_axis_split.load() <= 0 &&
         ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
-        plane_run_plan(outer, N, inner, &pl, true) && !pl.multi && inner <= kPlanesMaxP &&
+        plane_run_plan(outer, N, inner, &pl, true, false) && !pl.multi && inner <= kPlanesMaxP &&
         (fv == kScanColsPlaneLookback || plane_runs_split(st, pl, N, inner))) {
       // Few long planes: each plane's tiles over blocks, carries by look-back.
       const int rc = run_planes_lookback(pv, x, outer, N, inner, y,

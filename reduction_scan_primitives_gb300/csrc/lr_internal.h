@@ -181,8 +181,11 @@ __host__ __device__ constexpr int planes_cg_tile_rows(int P) {
   return kPlanesThreads / planes_cg_groups(P) * planes_cg_run_rows(P);
 }
 // The automatic choice and the plane-run option take the column groups for
-// every column count the runs do not scan.
-__host__ __device__ constexpr bool planes_cg(int P) { return planes_cg_fits(P) && !planes_scan_columns(P); }
+// scans of 6 columns and more and reductions of 3 and of 5 columns and more
+// (ahead of the runs there: measured), the runs for the rest and for planes
+// no longer than a column-group run.
+__host__ __device__ constexpr bool planes_cg_scan(int P) { return planes_cg_fits(P) && P >= 6; }
+__host__ __device__ constexpr bool planes_cg_reduce(int P) { return planes_cg_fits(P) && (P == 3 || P >= 5); }
 // Consecutive floats per thread (whole rows of P columns, at most 36), the
 // alignment of runs and tiles (lcm(4, P) floats: 16 bytes and P), and floats
 // per tile.

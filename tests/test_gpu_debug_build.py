@@ -51,7 +51,8 @@ def test_sum(dbg, n):
 
 
 @pytest.mark.parametrize("shape", [(37, 513, 67), (64, 40_000, 1), (3000, 100, 1), (5, 1000, 12),
-                                   (20_000, 100, 3), (2, 300_000, 64), (30_000, 101, 5)])
+                                   (20_000, 100, 3), (2, 300_000, 64), (30_000, 101, 5),
+                                   (3000, 99, 11), (4000, 35, 17), (1000, 300, 40), (60_000, 40, 20)])
 def test_axis_sum(dbg, shape):
     x = on_device(inputs.make(shape, "uniform_pm1", 32))
     o, r, i = shape
@@ -66,7 +67,9 @@ def test_axis_sum(dbg, shape):
                                          ((1, 3_000_000, 1), 3), ((8, 1000, 12), 2), ((2, 8192, 4096), 2),
                                          ((20_000, 100, 3), 1), ((64, 4096, 2), 0), ((1, 400_000, 2), 1),
                                          ((3, 7000, 4095), 0), ((100_000, 7, 3), 2), ((30_000, 101, 5), 0),
-                                         ((2, 300_000, 3), 0), ((2, 300_000, 3), 3)])
+                                         ((2, 300_000, 3), 0), ((2, 300_000, 3), 3),
+                                         ((3000, 101, 13), 1), ((700, 1001, 15), 2), ((2000, 50, 34), 0),
+                                         ((100, 2000, 100), 3), ((20_000, 100, 16), 0), ((60_000, 40, 20), 1)])
 def test_cumsum(dbg, shape, flags):
     x = on_device(inputs.make(shape, "uniform01", 33))
     y = torch.empty_like(x)
