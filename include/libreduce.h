@@ -380,7 +380,8 @@ LIBREDUCE_API uint64_t libreduce_debug_bad_address(void);
  *                                 for column groups); 9 the same tiles with a
  *                                 plane's tiles spread over blocks and their carries
  *                                 from a look-back (the automatic choice for fewer
- *                                 items than SMs when planes hold two tiles or more)
+ *                                 items than SMs when planes hold two tiles or more;
+ *                                 column groups for 7 to 128 columns, but 64 and 128)
  *                                 (float4 columns need inner % 4 == 0 and aligned x, y) */
 #define LIBREDUCE_OPT_CONTIG_VARIANT 5
 #define LIBREDUCE_OPT_COLS_VARIANT 6

@@ -65,6 +65,7 @@ struct DeviceState {
   int occ_planes_lb[kPlanesMaxP - 1] = {};  // the same, look-back form: [P - 2]
   int occ_planes_cg[kPlanesCgInstances] = {};  // scans as column groups, by instance
   int occ_planes_cg_reduce[kPlanesCgInstances] = {};  // reductions as column groups
+  int occ_planes_cg_lb[kPlanesCgInstances] = {};      // few long planes as column groups
 };
 
 // Index of a period (1, 2, 4) in the per-period tables.
@@ -148,6 +149,7 @@ int device_state(DeviceState** out, int* dev_out) {
     for (int ci = 0; ci < kPlanesCgInstances; ++ci) {
       st.occ_planes_cg[ci] = std::max(1, occupancy_planes_cg(ci));
       st.occ_planes_cg_reduce[ci] = std::max(1, occupancy_planes_cg_reduce(ci));
+      st.occ_planes_cg_lb[ci] = std::max(1, occupancy_planes_cg_lookback(ci));
     }
     cudaGetLastError();  // occupancy queries leave no error behind
     st.ready = true;
@@ -690,6 +692,35 @@ int run_planes_lookback(const Provider& pv, const float* x, int64_t outer, int64
   PlaneLbParams p{x, y, outer, N, tiles, sc.nodes, ticket_word, sc.header,
                   spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag, flags};
   return launched(launch_planes_lookback((int)inner, p, total + lag, s));  // one block per ticket
+}
+
+// Scans of few long planes as column groups (k_planes_cg_lb): one block per
+// tile of TR whole rows, each column's carry from the plane's look-back
+// tree (P node words per tile).  kColLbNoFit when the tiles exceed the node
+// words.  The lag as for the plane look-back: 5/4 of the resident blocks.
+int run_planes_cg_lookback(const Provider& pv, const float* x, int64_t outer, int64_t N, int64_t inner, float* y,
+                           int flags, cudaStream_t s) {
+  DeviceState* st = pv.st;
+  const int64_t tiles = ceil_div(N, (int64_t)planes_cg_tile_rows((int)inner));
+  int64_t total = 0;
+  if (mul_overflows(outer, tiles, &total) || total > kMaxLookbackTiles / inner ||
+      tiles > (int64_t(1) << (5 * kPlanesLbLevels)))
+    return kColLbNoFit;
+  Need need;
+  need.header = true;
+  need.nodes = 2 * total * inner;
+  Scratch sc;
+  const int rc = acquire(pv, need, &sc, s);
+  if (rc) return rc;
+  auto* ticket_word = reinterpret_cast<unsigned long long*>(sc.header + 2);
+  const int64_t spin = g_opt_spin_limit.load();
+  const int64_t lag_opt = g_opt_lookback_lag.load();
+  const int64_t resident = (int64_t)st->sm_count * st->occ_planes_cg_lb[cg_instance((int)inner)];
+  const int64_t lag_auto = std::max<int64_t>(64, ceil_div(resident * 5 / 4, 64) * 64);
+  const int64_t lag = std::min<int64_t>(total, lag_opt > 0 ? lag_opt : lag_auto);
+  PlaneLbParams p{x, y, outer, N, tiles, sc.nodes, ticket_word, sc.header,
+                  spin > 0 ? spin : kDefaultSpinLimit, g_opt_stall_tile.load(), lag, flags, (int)inner};
+  return launched(launch_planes_cg_lookback(p, total + lag, s));
 }
 
 int run_cols(const Provider& pv, const float* x, int64_t outer, int64_t reduce, int64_t inner,
@@ -1241,6 +1272,24 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
         plane_run_plan(outer, N, inner, &pl, true) && (fv == kScanColsPlaneRuns || plane_runs_fill(st, pl, outer, N, inner, true)))
       return run_planes(pv, pl, x, outer, N, inner, y, (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0),
                         true, kOpSum, s);
+    if ((fv < 0 || fv == kScanColsPlaneLookback) && g_opt_axis_split.load() <= 0 &&
+        ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+        plane_run_plan(outer, N, inner, &pl, true) && pl.cg &&
+        (fv == kScanColsPlaneLookback ||
+         (pl.items < st->sm_count && N >= 2 * planes_cg_tile_rows((int)inner) && !(inner % 32 == 0 && inner >= 64) &&
+          !(inner <= kPlanesMaxP && planes_run_len((int)inner) == 36)))) {
+      // Few long planes of 7-128 columns: column-group tiles over blocks,
+      // carries by look-back (fraction of copy bandwidth against the
+      // automatic choice before: [32, 5e5, 9] 0.53 / 0.23, [100, 1e5, 10]
+      // 0.67 / 0.24, [64, 2e5, 13] 0.55 / 0.29, [1, 1e7, 16] 0.73 / 0.60,
+      // [4, 2e6, 20] 0.62 / 0.46, [1, 4e6, 31] 0.51 / 0.32, [100, 50000, 32]
+      // 0.86 / 0.76).  6 columns keep the plane look-back's runs ([16, 1e6,
+      // 6] 0.67 / 0.60), 64 and 128 the column look-back's whole 32-column
+      // tiles.
+      const int rc = run_planes_cg_lookback(pv, x, outer, N, inner, y,
+                                            (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0), s);
+      if (rc != kColLbNoFit) return rc;
+    }
     if ((fv < 0 || fv == kScanColsPlaneLookback) && g_opt_axis_split.load() <= 0 &&
         ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
         plane_run_plan(outer, N, inner, &pl, true, false) && !pl.multi && inner <= kPlanesMaxP &&

@@ -230,6 +230,7 @@ struct PlaneLbParams {
   int64_t stall_tile;               // test fault: this ticket never publishes (-1: none)
   int64_t lag;                      // tickets between a tile's two touches
   int flags;                        // kScanMirror | kScanExclusive
+  int P = 0;                        // columns (the column-group form takes them at run time)
 };
 
 // --- Reduce-then-scan along rows (three passes) ------------------------------
@@ -442,6 +443,9 @@ cudaError_t launch_planes_cg(const PlaneRunParams& p, int64_t grid, cudaStream_t
 int occupancy_planes_cg(int instance);
 cudaError_t launch_planes_cg_reduce(int op, const PlaneRunParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes_cg_reduce(int instance);
+// Few long planes as column groups: tiles over blocks, carries by look-back.
+cudaError_t launch_planes_cg_lookback(const PlaneLbParams& p, int64_t grid, cudaStream_t s);
+int occupancy_planes_cg_lookback(int instance);
 int occupancy_planes_reduce(int P);
 cudaError_t launch_planes_lookback(int P, const PlaneLbParams& p, int64_t grid, cudaStream_t s);
 int occupancy_planes_lookback(int P);

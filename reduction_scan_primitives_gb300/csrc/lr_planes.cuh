@@ -566,7 +566,8 @@ __global__ void __launch_bounds__(kT, 4) k_planes(PlaneRunParams p) {
 template <int V>
 constexpr int kCgS = planes_cg_run_rows_v(V);
 template <int V>
-constexpr int kCgBuf = kT * kCgS<V> * V + 8;  // floats per stage: the largest tile, its two partial granules
+constexpr int kCgBuf = kT * kCgS<V> * V + (V == 4 ? 0 : 8);  // floats per stage: the largest tile (and, for
+                                                            // float2 / float groups, its two partial granules)
 
 template <int V>
 __device__ __forceinline__ void cg_ld(const float* p, float (&o)[V]) {
@@ -1328,6 +1329,368 @@ __global__ void __launch_bounds__(kT, kLbBlocks) k_planes_lb(PlaneLbParams p) {
     // Both copies have landed (waited above); the bulk store must have read
     // this block's shared memory before the block leaves.  Its writes need
     // no wait: they are complete when the grid is.
+    bulk_store_wait_read();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Few long planes as column groups (6 .. 128 columns): one tile per block,
+// each column's carry by look-back.
+//
+// The tiles, groups and runs of k_planes_cg over one plane each (tiles of TR
+// whole rows from the plane's start, in scan order), with the tickets and
+// the per-plane 32-ary look-back tree of k_planes_lb: P node words per tile,
+// one per column.  The block with ticket t
+//   1. copies tile t and rereads tile u = t - lag (normally an L2 hit);
+//   2. sums tile t per column -- each thread its run, a tree over the lanes
+//      of its column group, then the warps in order -- and publishes the P
+//      words at once;
+//   3. reads tile u's look-back, level by level: warp w takes siblings w,
+//      w + 4, ... with lane = column (lanes cover columns 32 apart), the
+//      warps' partials added in warp order, the levels lowest first;
+//   4. scans tile u as k_planes_cg does, that carry entering its first
+//      warp, and bulk-stores it;
+//   5. publishes every parent tile t completes (its 31 siblings as the
+//      look-back reads them, then its own sums).
+// Every wait is on a smaller ticket and bounded; every sum has a fixed order.
+// ---------------------------------------------------------------------------
+// One warp's share of a level's siblings for one column: siblings w, w + 4,
+// ... below d of the node row at `first` (sibling s at first + s * P), all
+// loads issued before any is waited on (bounded), summed in sibling order.
+__device__ __forceinline__ float cg_lb_siblings(const unsigned long long* first, int P, int d, int w, unsigned epoch,
+                                                int64_t limit, const unsigned* abort_word, bool* fail) {
+  constexpr int kPer = (31 + kNW - 1) / kNW;
+  unsigned long long word[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int sb = w + kNW * i;
+    word[i] = sb < d ? ld_relaxed_u64(first + (int64_t)sb * P) : 0ull;
+  }
+  float part = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int sb = w + kNW * i;
+    if (sb < d)
+      part += (unsigned)(word[i] >> 32) == epoch ? __uint_as_float((unsigned)word[i])
+                                                 : wait_node(first + (int64_t)sb * P, epoch, limit, abort_word, fail);
+  }
+  return part;
+}
+
+template <int V, int GMAX, int GFIX, bool REV, bool EXCL>
+__global__ void __launch_bounds__(kT, 6) k_planes_cg_lb(PlaneLbParams p) {
+  pdl_begin();
+  constexpr int S = kCgS<V>;
+  constexpr int PMAX = GMAX * V;  // the most columns the instance takes
+  __shared__ __align__(128) float s_new[kCgBuf<V>];  // tile `ticket`
+  __shared__ __align__(128) float s_old[kCgBuf<V>];  // tile `ticket - lag`
+  __shared__ __align__(8) unsigned long long s_bar[2];
+  // Per-warp partials: tile sums, then look-back sums, then (step 4, after
+  // the look-back's last barrier) the warps' scan totals.
+  __shared__ float s_part[kNW][PMAX];
+  float(&s_wagg)[kNW][PMAX] = s_part;
+  __shared__ unsigned char s_wflag[kNW][GMAX];
+  __shared__ float s_carry[PMAX];  // carry into tile u, per column
+  __shared__ float s_own[PMAX];    // tile `ticket`'s sums, per column
+  __shared__ unsigned s_ticket, s_epoch;
+  __shared__ int s_fail, s_copies;
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int w = t >> 5;
+  const unsigned* abort_word = p.err_word + 1;
+  const int P = GFIX ? GFIX * V : p.P;
+  const int G = GFIX ? GFIX : P / V;
+  const int RG = kT / G;
+  const int TR = RG * S;
+  const int g = t % G;
+  const bool active = (GFIX && kT % GFIX == 0) || t / G < RG;
+  const int m = REV ? RG - 1 - t / G : t / G;
+  const int row0 = m * S;
+  const unsigned gmask = __match_any_sync(kFullMask, g);
+  const int glead = __ffs(gmask) - 1;
+  const int64_t total = p.outer * p.tiles;
+  const int64_t L = p.N * P;  // floats per plane
+  const int Ni = (int)min(p.N, (int64_t)INT32_MAX);
+
+  // A ticket's plane and its tile in memory order (scan-order tile j).
+  const auto locate = [&](int64_t q, int64_t& plane, int64_t& j, int64_t& tr0, int& rows) {
+    plane = (unsigned)q / (unsigned)p.tiles;
+    j = q - plane * p.tiles;
+    const int64_t jt = REV ? p.tiles - 1 - j : j;
+    tr0 = jt * TR;
+    rows = (int)min((int64_t)TR, p.N - tr0);
+  };
+  const auto copy = [&](int64_t q, float* buf, unsigned long long* bar) {
+    int64_t plane, j, tr0;
+    int rows;
+    locate(q, plane, j, tr0, rows);
+    const int64_t f0 = plane * L + tr0 * P;
+    const int64_t a0 = f0 & ~(int64_t)3, a1 = (f0 + (int64_t)rows * P + 3) & ~(int64_t)3;
+    const unsigned bytes = (unsigned)(a1 - a0) * 4u;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(buf, p.x + a0, bytes, bar);
+  };
+
+  if (t == 0) {
+    const Ticket tk = take_ticket(p.ticket_word);
+    s_ticket = tk.ticket;
+    s_epoch = tk.epoch;
+    s_fail = 0;
+    if ((int64_t)tk.ticket == total + p.lag - 1) next_launch(p.ticket_word, tk.epoch);
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    fence_mbar_init();
+    int copies = 0;
+    if ((int64_t)tk.ticket < total) {
+      copy(tk.ticket, s_new, &s_bar[0]);
+      copies |= 1;
+    }
+    const int64_t u = (int64_t)tk.ticket - p.lag;
+    if (u >= 0 && u < total) {
+      copy(u, s_old, &s_bar[1]);
+      copies |= 2;
+    }
+    s_copies = copies;
+  }
+  __syncthreads();
+  const int64_t ticket = s_ticket;
+  const unsigned epoch = s_epoch;
+  if (ticket >= total + p.lag) {  // a stale counter: no copy was started, touch nothing
+    if (t == 0) atomicOr(p.err_word, 2u);
+    return;
+  }
+  int levels = 1;
+  while (levels < kPlanesLbLevels && ((p.tiles - 1) >> (5 * levels)) != 0) ++levels;
+  const int64_t u = ticket - p.lag;
+  const bool pub = ticket < total;
+  const bool wr = u >= 0;
+  const auto give_up = [&]() {
+    if (t == 0) {
+      atomicOr(p.err_word, 1u);
+      atomicExch(p.err_word + 1, epoch);
+      if (s_copies & 1) mbar_wait_copy(&s_bar[0], 0u);
+      if (s_copies & 2) mbar_wait_copy(&s_bar[1], 0u);
+    }
+  };
+
+  // 2. Tile `ticket`'s column sums (only the plane's rows), published at once.
+  int64_t tplane = 0, tj = 0, ttr0 = 0;
+  int trows = 0;
+  bool landed = true;
+  if (pub) {
+    locate(ticket, tplane, tj, ttr0, trows);
+    landed = mbar_wait_copy(&s_bar[0], 0u);
+    const int delta = V == 4 ? 0 : (int)((tplane * L + ttr0 * P) & 3);
+    float a[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) a[c] = 0.f;
+    if (active) {
+      const float* src = s_new + delta + row0 * P + V * g;
+#pragma unroll
+      for (int e = 0; e < S; ++e) {
+        if (row0 + e < trows) {
+          float r[V];
+          cg_ld<V>(src + e * P, r);
+#pragma unroll
+          for (int c = 0; c < V; ++c) a[c] += r[c];
+        }
+      }
+    }
+    // A tree over the lanes of my column group in this warp (lane + o in
+    // range only), its first lane holding the warp's sums.
+    for (int o = G; o < 32; o <<= 1) {
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        const float q = __shfl_down_sync(kFullMask, a[c], o);
+        if (lane + o < 32) a[c] += q;
+      }
+    }
+    if (lane < G) {
+#pragma unroll
+      for (int c = 0; c < V; ++c) s_part[w][g * V + c] = a[c];
+    }
+  }
+  if (__syncthreads_or(!landed)) {
+    give_up();
+    return;
+  }
+  const bool publishing = pub && ticket != p.stall_tile;
+  unsigned long long* tvals = p.node_val + tplane * 2 * p.tiles * P;
+  if (pub) {
+    for (int c = t; c < P; c += kT) {
+      float r = s_part[0][c];
+#pragma unroll
+      for (int q = 1; q < kNW; ++q) r += s_part[q][c];
+      s_own[c] = r;
+      if (publishing) st_relaxed_u64(tvals + tj * P + c, pack_node(epoch, r));
+    }
+  }
+  __syncthreads();  // s_part free again; s_own complete
+
+  // 3. Tile u's carry, per column: the look-back, level by level.
+  int64_t uplane = 0, uj = 0, utr0 = 0;
+  int urows = 0;
+  if (wr) {
+    locate(u, uplane, uj, utr0, urows);
+    const unsigned long long* uvals = p.node_val + uplane * 2 * p.tiles * P;
+    for (int c = t; c < P; c += kT) s_carry[c] = 0.f;
+    int64_t off = 0, count = p.tiles;
+    for (int Lv = 0; Lv < levels; ++Lv) {
+      const int64_t mm = uj >> (5 * Lv);
+      const int d = (int)(mm & 31);
+      bool fail = false;
+      for (int c = lane; c < P; c += 32) s_part[w][c] = cg_lb_siblings(uvals + (off + (mm - d)) * P + c, P, d, w, epoch, p.spin_limit, abort_word, &fail);
+      if (__any_sync(kFullMask, fail) && lane == 0) s_fail = 1;
+      __syncthreads();
+      for (int c = t; c < P; c += kT) {
+        float r = s_part[0][c];
+#pragma unroll
+        for (int q = 1; q < kNW; ++q) r += s_part[q][c];
+        s_carry[c] += r;
+      }
+      __syncthreads();
+      off += count;
+      count >>= 5;
+    }
+  }
+
+  // 4. Tile u: the scan of k_planes_cg with that carry.
+  landed = true;
+  float v[S][V];
+  int hp = S;
+  int delta_u = 0;
+  if (wr) {
+    landed = mbar_wait_copy(&s_bar[1], 0u);
+    delta_u = V == 4 ? 0 : (int)((uplane * L + utr0 * P) & 3);
+    const int rr = (int)min(utr0 + row0, (int64_t)INT32_MAX / 2);
+    if (active) {
+      if constexpr (!REV) {
+        const int dh = rr == 0 ? 0 : Ni - rr;
+        if (dh >= 0 && dh < S) hp = dh;
+      } else {
+        const int e = rr + S - Ni;
+        if (e >= 0 && e < S) hp = e;
+      }
+    }
+    const float* src = s_old + delta_u + row0 * P + V * g;
+#pragma unroll
+    for (int e = 0; e < S; ++e) {
+      if (active) {
+        cg_ld<V>(src + (REV ? S - 1 - e : e) * P, v[e]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < V; ++c) v[e][c] = 0.f;
+      }
+    }
+  }
+  float acc[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) acc[c] = 0.f;
+  if (wr) {
+#pragma unroll
+    for (int e = 0; e < S; ++e) {
+      const bool restart = e == hp;
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        const float before = restart ? 0.f : acc[c];
+        acc[c] = before + v[e][c];
+        v[e][c] = EXCL ? before : acc[c];
+      }
+    }
+  }
+  const unsigned hmask = __ballot_sync(kFullMask, hp < S) & gmask;
+  const unsigned upto = hmask & (kFullMask >> (31 - lane));
+  const int hh = upto ? 31 - __clz((int)upto) : glead;
+  float inc[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) inc[c] = acc[c];
+  for (int o = G; o < 32; o <<= 1) {
+    float q[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) q[c] = __shfl_up_sync(kFullMask, inc[c], o);
+    if (lane - o >= hh) {
+#pragma unroll
+      for (int c = 0; c < V; ++c) inc[c] = q[c] + inc[c];
+    }
+  }
+  float ex[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) ex[c] = __shfl_up_sync(kFullMask, inc[c], G);
+  const bool head_before = (hmask & ((1u << lane) - 1u)) != 0;
+  if (lane >= 32 - G) {
+#pragma unroll
+    for (int c = 0; c < V; ++c) s_wagg[w][g * V + c] = inc[c];
+    s_wflag[w][g] = hmask != 0;
+  }
+  if (__syncthreads_or(!landed)) {
+    give_up();
+    return;
+  }
+  if (wr) {
+    float cw[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) cw[c] = s_carry[g * V + c];
+#pragma unroll
+    for (int q = 0; q < kNW - 1; ++q) {
+      if (q < w) {
+        const bool restart = s_wflag[q][g] != 0;
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          const float a = s_wagg[q][g * V + c];
+          cw[c] = restart ? a : cw[c] + a;
+        }
+      }
+    }
+    float cl[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) cl[c] = lane < G ? cw[c] : (head_before ? ex[c] : cw[c] + ex[c]);
+    if (active) {
+      float* dst = s_old + delta_u + row0 * P + V * g;
+#pragma unroll
+      for (int e = 0; e < S; ++e) {
+        if (e < hp) {
+#pragma unroll
+          for (int c = 0; c < V; ++c) v[e][c] = cl[c] + v[e][c];
+        }
+        cg_st<V>(dst + (REV ? S - 1 - e : e) * P, v[e]);
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  if (wr) store_tile_out(s_old, p.y + (uplane * L + utr0 * P - delta_u), delta_u, delta_u + urows * P);
+
+  // 5. Every parent tile `ticket` completes: its 31 siblings (warp
+  // partials in warp order, as the look-back), then its own sums.
+  if (publishing && (tj & 31) == 31) {
+    bool fail = false;
+    int64_t off = 0, count = p.tiles, mm = tj;
+    for (int Lv = 0; Lv + 1 < levels && (mm & 31) == 31; ++Lv) {
+      const int64_t next_off = off + count;
+      for (int c = lane; c < P; c += 32)
+        s_part[w][c] = cg_lb_siblings(tvals + (off + (mm - 31)) * P + c, P, 31, w, epoch, p.spin_limit, abort_word, &fail);
+      __syncthreads();
+      for (int c = t; c < P; c += kT) {
+        float r = s_part[0][c];
+#pragma unroll
+        for (int q = 1; q < kNW; ++q) r += s_part[q][c];
+        r += s_own[c];
+        s_own[c] = r;
+        st_relaxed_u64(tvals + (next_off + (mm >> 5)) * P + c, pack_node(epoch, r));
+      }
+      __syncthreads();
+      off = next_off;
+      count >>= 5;
+      mm >>= 5;
+    }
+    if (fail) s_fail = 1;
+  }
+  __syncthreads();
+  if (t == 0) {
+    if (s_fail) {
+      atomicOr(p.err_word, 1u);
+      atomicExch(p.err_word + 1, epoch);
+    }
     bulk_store_wait_read();
   }
 }

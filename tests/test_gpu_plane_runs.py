@@ -284,3 +284,69 @@ def test_lookback_bounded_wait_reports_timeout():
     L.check()
     ref, scale = oracle.cumsum(x.numpy(), *shape, False, False)
     assert_close(L.cumsum_f32(xd, 1).cpu().numpy(), ref, scale, "after timeout")
+
+
+# ---- few long planes as column groups (6-128 columns): k_planes_cg_lb ----------
+# Every group width (float for odd widths, float2, float4), group counts that do
+# not divide 32, 32 groups, tiles starting inside a 16-byte granule, planes of
+# two tiles, of 33 tiles (a level-1 parent completed by its 32nd tile) and of
+# ~1700 tiles (two levels and a third); the existing shapes of 6-8 columns
+# above take it too.
+CG_LB_SHAPES = [(1, 500_003, 11), (3, 200_000, 16), (5, 100_001, 13), (2, 60_000, 31), (4, 30_000, 40),
+                (7, 1300, 20), (1, 300_000, 6), (2, 100_000, 18), (1, 2_000_000, 10), (3, 9801, 22),
+                (2, 20_000, 128), (1, 5000, 64)]
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape", CG_LB_SHAPES)
+def test_column_group_lookback_against_oracle(shape, reverse, exclusive):
+    x = inputs.make(shape, "uniform_pm1", 46)
+    y = scan_lb(x, reverse, exclusive)
+    ref, scale = oracle.cumsum(x.numpy(), *shape, reverse, exclusive)
+    assert_close(y.cpu().numpy(), ref, scale, f"column-group look-back {shape} rev={reverse} excl={exclusive}")
+
+
+@pytest.mark.parametrize("reverse,exclusive", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("shape", [(2, 400_001, 13), (1, 300_000, 20)])
+def test_column_group_lookback_integers_exact_and_bitwise(shape, reverse, exclusive):
+    """{0..3}: every prefix below 2^24, so exact."""
+    x = inputs.make(shape, "int:0:3", 47)
+    a = scan_lb(x, reverse, exclusive).clone()
+    b = scan_lb(x, reverse, exclusive)
+    assert bitwise_equal(a, b), "reruns differ"
+    ref, _ = oracle.cumsum(x.numpy(), *shape, reverse, exclusive)
+    assert_exact(a.cpu().numpy(), ref, f"column-group look-back integers {shape}")
+
+
+@pytest.mark.parametrize("lag", [64, 640, 4096])
+def test_column_group_lookback_lags(lag):
+    shape = (1, 1_000_001, 16)
+    x = inputs.make(shape, "uniform_pm1", 48)
+    base = scan_lb(x, True, False).clone()
+    L.set_option(L.OPT_LOOKBACK_LAG, lag)
+    assert bitwise_equal(base, scan_lb(x, True, False))
+
+
+@pytest.mark.parametrize("shape", [(1, 2_000_000, 16), (8, 200_000, 13), (3, 300_000, 24)])
+def test_column_group_lookback_is_the_automatic_choice(shape):
+    x = inputs.make(shape, "uniform_pm1", 49)
+    auto = scan_lb(x, False, False, forced=False).clone()
+    assert bitwise_equal(auto, scan_lb(x, False, False))
+
+
+def test_column_group_lookback_bounded_wait_reports_timeout():
+    shape = (1, 500_000, 16)
+    x = inputs.make(shape, "uniform01", 50)
+    xd = on_device(x)
+    L.set_option(L.OPT_SCAN_COLS_VARIANT, SCAN_LOOKBACK)
+    L.set_option(L.OPT_SPIN_LIMIT, 2000)
+    L.set_option(L.OPT_STALL_TILE, 5)
+    L.cumsum_f32(xd, 1)
+    with pytest.raises(L.LibreduceError) as ei:
+        L.check()
+    assert ei.value.status == L.ERR_TIMEOUT
+    L.set_option(L.OPT_STALL_TILE, -1)
+    L.set_option(L.OPT_SPIN_LIMIT, 0)
+    L.check()
+    ref, scale = oracle.cumsum(x.numpy(), *shape, False, False)
+    assert_close(L.cumsum_f32(xd, 1).cpu().numpy(), ref, scale, "after timeout")
