@@ -79,6 +79,8 @@ PROFILE_CASES = {
     "cumsum_40000x100x16_d1": dict(op="cumsum", shape=(40_000, 100, 16), dim=1, reverse=False,
                                    exclusive=False, dist="uniform01", seed=13),
     "sum_5000x1000x13_d1": dict(op="reduce", rop="sum", shape=(5000, 1000, 13), dim=1, dist="uniform_pm1", seed=13),
+    "cumsum_1x10000000x16_d1": dict(op="cumsum", shape=(1, 10_000_000, 16), dim=1, reverse=False,
+                                    exclusive=False, dist="uniform01", seed=13),
     "sum_1e5": dict(op="sum", shape=(100_000,), dist="uniform01", seed=42),
     "cumsum_500000x7x3_d1": dict(op="cumsum", shape=(500_000, 7, 3), dim=1, reverse=False,
                                  exclusive=False, dist="uniform01", seed=13),
