@@ -1333,11 +1333,13 @@ int run_scan_cols(const Provider& pv, const float* x, int64_t outer, int64_t N, 
         return run_scan_short_planes(pv, pf, x, outer, N, inner, y, s,
                                      (reverse ? 0 : kScanMirror) | (exclusive ? kScanExclusive : 0));
     }
-    // Scalar narrow rows of more than 32 columns (odd widths) go to the wide
-    // column scan unless forced ([3000, 300, 33] 0.62 against 0.25, [2000,
-    // 500, 65] 0.63 against 0.25; from 17 columns on it was already ahead:
-    // [3764, 1000, 17] 0.41 / 0.27).
-    if (narrow_rows(x, y, inner, &nvec) && (nvec == 4 || inner <= 32 || fv >= 0) &&
+    // Scalar narrow rows of more than 32 columns (odd widths) and float4 ones
+    // of more than 64 go to the wide column scan unless forced ([3000, 300,
+    // 33] 0.62 against 0.25, [2000, 500, 65] 0.63 against 0.25; from 17
+    // columns on it was already ahead: [3764, 1000, 17] 0.41 / 0.27; float4
+    // rows [2604, 256, 96] 0.96 / 0.66, [500, 1000, 128] 0.85 / 0.71 for the
+    // best wide variant).
+    if (narrow_rows(x, y, inner, &nvec) && (fv >= 0 || (nvec == 4 ? inner <= 64 : inner <= 32)) &&
         (fv < 0 || fv == kScanColsNarrow || fv == kScanColsNarrowWarp || fv == kScanColsShortPlanes ||
          fv == kScanColsPeriodRows)) {
       // The block form walks tiles of T rows; a plane of fewer than T/2 rows
